@@ -1,0 +1,138 @@
+"""Seeded synthetic inputs for the fused pre-norm linear layer.
+
+This module draws random tensors and nothing else: it holds none of the
+layer's arithmetic, so both the CUDA path and the fp64 oracle can be fed from
+it without sharing any of the method.  Every tensor is drawn on the CPU from
+one ``torch.Generator`` per case, in fp32, then cast to the case's 16-bit
+type.
+
+The workload shapes and value distributions are the ones the pages quote for
+this path ("LayerNorm 融合算子如何让大模型推理再快 15%？深度拆解 ATB 的实现",
+§2.1: x [8, 128, 8192] into an 8192x8192 linear; "昇腾CANN的MatMul融合玩法，
+让大模型推理快3倍", §二 strategies 1-3: [512, 14336] against [49152, 14336]
+weights, and the FFN 14336 -> 49152 -> 14336), at the sizes of the five
+workloads below.  No dataset or trained weight is involved.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import torch
+
+F16, BF16 = torch.float16, torch.bfloat16
+
+# Rows of W drawn per randn call: bounds the fp32 temporary and fixes the
+# draw order (changing it changes the tensors).
+_CHUNK_ROWS = 2048
+
+
+@dataclass(frozen=True)
+class Workload:
+    """One named workload: the op, its sizes and its input distribution."""
+    name: str
+    op: str                   # layernorm_linear | rmsnorm_linear | linear_silu | ffn
+    M: int
+    K: int
+    N: int                    # output features (F, the hidden width, for ffn)
+    dtype: torch.dtype
+    bias: bool
+    eps: float
+    seed: int
+    x_mean: float = 0.0       # mean offset added to x
+    outlier_frac: float = 0.0  # fraction of rows scaled by outlier_scale
+    outlier_scale: float = 1.0
+    m_choices: tuple = field(default_factory=tuple)  # decode: allowed M
+
+    @property
+    def flops(self) -> float:
+        """2*M*N*K per GEMM (the FFN has two)."""
+        g = 2.0 * self.M * self.N * self.K
+        return 2.0 * g if self.op == "ffn" else g
+
+    def with_m(self, M: int) -> "Workload":
+        d = dict(self.__dict__)
+        d["M"] = M
+        return Workload(**d)
+
+
+WORKLOADS = [
+    Workload("ln_linear_bias_f16_m64_k256_n512", "layernorm_linear",
+             64, 256, 512, F16, True, 1e-5, 1234),
+    Workload("ln_linear_bias_f16_m1024_k8192_n8192", "layernorm_linear",
+             1024, 8192, 8192, F16, True, 1e-5, 1235),
+    Workload("rms_linear_f16_m512_k14336_n49152_outliers", "rmsnorm_linear",
+             512, 14336, 49152, F16, False, 1e-6, 1236,
+             outlier_frac=0.01, outlier_scale=50.0),
+    Workload("ffn_linear_silu_linear_f16_m512_k14336_f49152", "ffn",
+             512, 14336, 49152, F16, False, 0.0, 1237),
+    Workload("decode_ln_linear_bias_bf16_k8192_n28672", "layernorm_linear",
+             16, 8192, 28672, BF16, True, 1e-5, 1238, x_mean=3.0,
+             m_choices=(1, 4, 16)),
+]
+BY_NAME = {w.name: w for w in WORKLOADS}
+
+
+def _normal(gen, shape, std=1.0, mean=0.0):
+    return torch.randn(shape, generator=gen, dtype=torch.float32) * std + mean
+
+
+def _weight(gen, rows: int, cols: int, std: float, dtype) -> torch.Tensor:
+    out = torch.empty((rows, cols), dtype=dtype)
+    for r0 in range(0, rows, _CHUNK_ROWS):
+        r1 = min(rows, r0 + _CHUNK_ROWS)
+        out[r0:r1] = (torch.randn((r1 - r0, cols), generator=gen,
+                                  dtype=torch.float32) * std).to(dtype)
+    return out
+
+
+def make(w: Workload, seed: int | None = None) -> dict:
+    """Draw the inputs of workload ``w`` (CPU tensors).
+
+    Keys: x [M, K]; gamma, beta [K] (norm ops); W [N, K]; bias [N] or None;
+    for ffn: W1 [F, K], W2 [K, F].  Also 'outlier_rows' (long tensor).
+    Distributions: x ~ N(x_mean, 1) with a seeded ``outlier_frac`` of rows
+    scaled by ``outlier_scale``; gamma ~ 1 + 0.1 N(0,1); beta, bias ~
+    0.1 N(0,1); W ~ N(0, 1/K) (W2 ~ N(0, 1/F)).
+    """
+    g = torch.Generator("cpu")
+    g.manual_seed(w.seed if seed is None else seed)
+    M, K, N, dt = w.M, w.K, w.N, w.dtype
+    x = _normal(g, (M, K), 1.0, w.x_mean)
+    n_out = int(round(w.outlier_frac * M))
+    outliers = torch.randperm(M, generator=g)[:n_out].sort().values
+    if n_out:
+        x[outliers] *= w.outlier_scale
+    d = {"x": x.to(dt), "outlier_rows": outliers, "gamma": None,
+         "beta": None, "bias": None}
+    if w.op == "ffn":
+        d["W1"] = _weight(g, N, K, K ** -0.5, dt)
+        d["W2"] = _weight(g, K, N, N ** -0.5, dt)
+        return d
+    if w.op in ("layernorm_linear", "rmsnorm_linear"):
+        d["gamma"] = (1.0 + 0.1 * _normal(g, (K,))).to(dt)
+    if w.op == "layernorm_linear":
+        d["beta"] = (0.1 * _normal(g, (K,))).to(dt)
+    d["W"] = _weight(g, N, K, K ** -0.5, dt)
+    if w.bias:
+        d["bias"] = (0.1 * _normal(g, (N,))).to(dt)
+    return d
+
+
+def case(op: str, M: int, K: int, N: int, dtype=F16, bias: bool = True,
+         eps: float = 1e-5, seed: int = 7, x_mean: float = 0.0,
+         outlier_frac: float = 0.0, outlier_scale: float = 1.0) -> dict:
+    """Inputs for an ad-hoc shape (edge-case sweeps) with the same recipe."""
+    w = Workload(f"{op}_{M}x{K}x{N}", op, M, K, N, dtype, bias, eps, seed,
+                 x_mean=x_mean, outlier_frac=outlier_frac,
+                 outlier_scale=outlier_scale)
+    return make(w)
+
+
+def sample_rows(M: int, count: int, seed: int, always=()) -> torch.Tensor:
+    """A seeded sorted sample of ``count`` distinct rows of M, plus the rows
+    in ``always`` (e.g. the outlier rows)."""
+    g = torch.Generator("cpu")
+    g.manual_seed(seed)
+    pick = torch.randperm(M, generator=g)[:min(count, M)]
+    rows = torch.cat([pick, torch.as_tensor(list(always), dtype=torch.long)])
+    return torch.unique(rows).sort().values
