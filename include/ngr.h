@@ -1,0 +1,156 @@
+/*
+ * ngr.h -- C ABI of the fused pre-norm linear layer library for NVIDIA GB300
+ * (sm_103a).
+ *
+ * The library computes a LayerNorm or RMSNorm row reduction whose normalized
+ * rows feed a dense matrix product directly, with a bias and/or SiLU
+ * epilogue; the normalized activations exist only in on-chip memory and are
+ * never written to device memory.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor arguments are DEVICE pointers to dense row-major arrays owned
+ *    by the caller.  The library allocates no device memory and frees none;
+ *    temporaries live in the caller's `workspace` (see ngr_workspace_bytes).
+ *  - x is [M, K]; W is [N, K] (the nn.Linear layout: y = a . W^T); gamma and
+ *    beta are [K]; bias is [N]; y is [M, N].  Every tensor has the element
+ *    type `dtype` (NGR_F16 or NGR_BF16).  Statistics, the normalization and
+ *    the accumulation are FP32; y is rounded to nearest-even once.
+ *  - Alignment: K % 8 == 0 and N % 8 == 0 (16-byte row pitch), every pointer
+ *    16-byte aligned, the workspace 256-byte aligned.  M is arbitrary
+ *    (M == 0 is a no-op that returns NGR_OK).
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and is asynchronous: the call returns once the kernels are
+ *    launched.  Argument errors are detected before anything is launched and
+ *    returned as a negative ngr_status; launch failures return
+ *    NGR_ERR_CUDA.  Errors raised inside a kernel (a bounded wait that ran
+ *    out) are recorded in the workspace's error word: read them with
+ *    ngr_workspace_error.  With the environment variable NGR_DEBUG=1 every
+ *    call synchronizes its stream and returns that word's status itself.
+ *  - The kernels need an sm_103 device (GB300); any other device gives
+ *    NGR_ERR_ARCH.  There is no fallback path.
+ *  - Calls are thread-safe.  Two calls that share one workspace must be
+ *    ordered (the same stream, or synchronized).
+ *
+ * Sources, cited by page title and section:
+ *  [LNF] "LayerNorm 融合算子如何让大模型推理再快 15%？深度拆解 ATB 的实现"
+ *  [MMF] "昇腾CANN的MatMul融合玩法，让大模型推理快3倍"
+ *  [ATB] "CANN推理加速库ascend-transformer-boost ATB算子融合实战：昇腾NPU上
+ *        LayerNorm+MatMul融合与Llama2大模型推理优化深度指南"
+ */
+#ifndef NGR_H
+#define NGR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so that this header needs no
+ * CUDA header. */
+typedef struct CUstream_st *ngr_stream_t;
+
+typedef enum { NGR_F16 = 0, NGR_BF16 = 1 } ngr_dtype;
+
+typedef enum {
+    NGR_OK = 0,
+    NGR_ERR_NULL = -1,      /* a required pointer is NULL */
+    NGR_ERR_SHAPE = -2,     /* M < 0, K <= 0, N <= 0, or too large */
+    NGR_ERR_ALIGN = -3,     /* K or N not a multiple of 8, or a pointer misaligned */
+    NGR_ERR_DTYPE = -4,     /* dtype is not NGR_F16 / NGR_BF16 */
+    NGR_ERR_WORKSPACE = -5, /* workspace NULL or smaller than ngr_workspace_bytes */
+    NGR_ERR_ARCH = -6,      /* no sm_103 device current */
+    NGR_ERR_CUDA = -7,      /* a CUDA runtime/driver call failed */
+    NGR_ERR_TIMEOUT = -8,   /* a kernel's bounded wait ran out (see ngr_workspace_error) */
+    NGR_ERR_ARG = -9        /* any other invalid argument */
+} ngr_status;
+
+/* Operation codes for ngr_workspace_bytes. */
+typedef enum {
+    NGR_OP_LAYERNORM_LINEAR = 0,
+    NGR_OP_RMSNORM_LINEAR = 1,
+    NGR_OP_LINEAR_SILU = 2,
+    NGR_OP_FFN = 3
+} ngr_op;
+
+/* Bytes of device workspace that `op` needs for these sizes (for NGR_OP_FFN
+ * pass the hidden width F as N; the FFN's intermediate H is included only if
+ * `ffn_h_in_workspace` is nonzero).  Pure host arithmetic: needs no GPU and
+ * never fails (returns 0 for invalid sizes). */
+size_t ngr_workspace_bytes(int op, int64_t M, int64_t K, int64_t N,
+                           int ffn_h_in_workspace);
+
+/* y = LayerNorm(x) . W^T (+ bias).
+ * Per row i: mu = mean_k x[i,k]; var = mean_k (x[i,k] - mu)^2 (biased);
+ * a[i,k] = (x[i,k] - mu) / sqrt(var + eps) * gamma[k] + beta[k];
+ * y[i,n] = sum_k a[i,k] W[n,k] + bias[n].
+ * [LNF] §1.1 (statistics, normalize, affine), §2.1 (LayerNormLinearFusion:
+ * layer_norm then matmul with the weight transposed, the normalized rows kept
+ * on chip), §2.3 (FP32 statistics); [ATB] LayerNormMatMul fusion
+ * (fused_layernorm_matmul(x, w, bias)).
+ * bias may be NULL.  gamma, beta, W, x, y, workspace may not. */
+int ngr_fused_layernorm_linear(const void *x, const void *gamma,
+                               const void *beta, const void *W,
+                               const void *bias, float eps, int64_t M,
+                               int64_t K, int64_t N, int dtype, void *y,
+                               void *workspace, size_t workspace_bytes,
+                               ngr_stream_t stream);
+
+/* y = RMSNorm(x) . W^T (+ bias).
+ * a[i,k] = x[i,k] / sqrt(mean_k x[i,k]^2 + eps) * gamma[k]; no beta.
+ * [MMF] §二 strategy 3 (fused_rms_norm_matmul(x, w.T)); [ATB] Llama2 section
+ * (RMSNorm feeding the projections).  bias may be NULL. */
+int ngr_fused_rmsnorm_linear(const void *x, const void *gamma, const void *W,
+                             const void *bias, float eps, int64_t M, int64_t K,
+                             int64_t N, int dtype, void *y, void *workspace,
+                             size_t workspace_bytes, ngr_stream_t stream);
+
+/* y = SiLU(x . W^T + bias), SiLU(z) = z / (1 + exp(-z)); bias (may be NULL)
+ * is added before the activation.
+ * [MMF] §二 strategy 1 (fused_matmul_silu(x, w.T)). */
+int ngr_fused_linear_silu(const void *x, const void *W, const void *bias,
+                          int64_t M, int64_t K, int64_t N, int dtype, void *y,
+                          void *workspace, size_t workspace_bytes,
+                          ngr_stream_t stream);
+
+/* FFN chain: H = SiLU(x . W1^T) [M, F], y = H . W2^T [M, K].
+ * W1 is [F, K], W2 is [K, F].  H is written to device memory exactly once
+ * and read once: into `h` ([M, F], dtype) when non-NULL, else into the
+ * workspace (size it with ffn_h_in_workspace = 1).  F % 8 == 0.
+ * [MMF] §二 strategy 2 (fused_matmul_silu_matmul(x, w1.T, w2.T)). */
+int ngr_ffn_linear_silu_linear(const void *x, const void *W1, const void *W2,
+                               int64_t M, int64_t K, int64_t F, int dtype,
+                               void *h, void *y, void *workspace,
+                               size_t workspace_bytes, ngr_stream_t stream);
+
+/* Step a1 alone: per-row FP32 statistics into stats[2*M] as (mu, rstd)
+ * pairs.  norm: 1 = LayerNorm, 2 = RMSNorm (mu = 0).  [LNF] §1.1, §2.3.
+ * Exposed so the statistics stage can be checked by itself. */
+int ngr_row_stats(int norm, const void *x, float eps, int64_t M, int64_t K,
+                  int dtype, float *stats, ngr_stream_t stream);
+
+/* Synchronize `stream`, then return and clear the error word kept in
+ * `workspace` (NGR_OK, or NGR_ERR_TIMEOUT when a kernel's bounded wait ran
+ * out).  NGR_ERR_CUDA if the synchronization itself fails. */
+int ngr_workspace_error(void *workspace, ngr_stream_t stream);
+
+/* Launch one tiny kernel whose mbarrier wait can never complete, bounded by
+ * `timeout_us`; it must give up, record NGR_ERR_TIMEOUT in the workspace's
+ * error word and exit.  Exercises the bounded-wait path without faulting or
+ * hanging the device.  Needs ngr_workspace_bytes(any op, 0, 8, 8, 0) bytes. */
+int ngr_debug_bounded_wait(void *workspace, uint32_t timeout_us,
+                           ngr_stream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+const char *ngr_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int ngr_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NGR_H */

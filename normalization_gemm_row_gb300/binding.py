@@ -1,0 +1,265 @@
+"""ctypes binding of the CUDA library (the C ABI declared in include/ngr.h).
+
+Two layers, both argument marshalling only -- every step of the layer runs in
+the library's kernels:
+
+- ``ngr_*`` functions with the C names and C arguments (device pointers as
+  integers, sizes, dtype code, stream handle), returning the status code;
+- tensor-level helpers with the op names (``fused_layernorm_linear`` ...)
+  that take CUDA torch tensors, allocate the output and workspace with torch
+  when not given, pass pointers and the current stream, and raise
+  ``NgrError`` on a non-zero status.
+
+There is no fallback: if the shared library is missing or fails to load,
+every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from ._build import LIB_PATH
+
+NGR_F16, NGR_BF16 = 0, 1
+OP_LAYERNORM_LINEAR, OP_RMSNORM_LINEAR, OP_LINEAR_SILU, OP_FFN = 0, 1, 2, 3
+STATUS = {0: "NGR_OK", -1: "NGR_ERR_NULL", -2: "NGR_ERR_SHAPE",
+          -3: "NGR_ERR_ALIGN", -4: "NGR_ERR_DTYPE", -5: "NGR_ERR_WORKSPACE",
+          -6: "NGR_ERR_ARCH", -7: "NGR_ERR_CUDA", -8: "NGR_ERR_TIMEOUT",
+          -9: "NGR_ERR_ARG"}
+
+# Every symbol include/ngr.h declares, with (restype, argtypes).
+_P, _I64, _I, _F, _SZ, _U32 = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
+                               ctypes.c_float, ctypes.c_size_t, ctypes.c_uint32)
+SIGNATURES = {
+    "ngr_workspace_bytes": (_SZ, [_I, _I64, _I64, _I64, _I]),
+    "ngr_fused_layernorm_linear": (_I, [_P, _P, _P, _P, _P, _F, _I64, _I64, _I64, _I, _P, _P, _SZ, _P]),
+    "ngr_fused_rmsnorm_linear": (_I, [_P, _P, _P, _P, _F, _I64, _I64, _I64, _I, _P, _P, _SZ, _P]),
+    "ngr_fused_linear_silu": (_I, [_P, _P, _P, _I64, _I64, _I64, _I, _P, _P, _SZ, _P]),
+    "ngr_ffn_linear_silu_linear": (_I, [_P, _P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _SZ, _P]),
+    "ngr_row_stats": (_I, [_I, _P, _F, _I64, _I64, _I, _P, _P]),
+    "ngr_workspace_error": (_I, [_P, _P]),
+    "ngr_debug_bounded_wait": (_I, [_P, _U32, _P]),
+    "ngr_status_string": (ctypes.c_char_p, [_I]),
+    "ngr_version": (_I, []),
+}
+
+
+class NgrError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what} failed: {status_string(status)}")
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        with _lock:
+            if _lib is None:
+                if not os.path.exists(LIB_PATH):
+                    raise RuntimeError(
+                        f"CUDA library not found at {LIB_PATH}; build it with "
+                        "normalization_gemm_row_gb300.build()")
+                handle = ctypes.CDLL(LIB_PATH)
+                for name, (res, args) in SIGNATURES.items():
+                    f = getattr(handle, name)
+                    f.restype, f.argtypes = res, args
+                _lib = handle
+    return _lib
+
+
+# ---- C-named entry points ------------------------------------------------------
+def ngr_workspace_bytes(op, M, K, N, ffn_h_in_workspace=0) -> int:
+    return int(lib().ngr_workspace_bytes(op, M, K, N, ffn_h_in_workspace))
+
+
+def ngr_fused_layernorm_linear(x, gamma, beta, W, bias, eps, M, K, N, dtype, y,
+                               ws, ws_bytes, stream) -> int:
+    return lib().ngr_fused_layernorm_linear(x, gamma, beta, W, bias, eps, M, K,
+                                            N, dtype, y, ws, ws_bytes, stream)
+
+
+def ngr_fused_rmsnorm_linear(x, gamma, W, bias, eps, M, K, N, dtype, y, ws,
+                             ws_bytes, stream) -> int:
+    return lib().ngr_fused_rmsnorm_linear(x, gamma, W, bias, eps, M, K, N,
+                                          dtype, y, ws, ws_bytes, stream)
+
+
+def ngr_fused_linear_silu(x, W, bias, M, K, N, dtype, y, ws, ws_bytes,
+                          stream) -> int:
+    return lib().ngr_fused_linear_silu(x, W, bias, M, K, N, dtype, y, ws,
+                                       ws_bytes, stream)
+
+
+def ngr_ffn_linear_silu_linear(x, W1, W2, M, K, F, dtype, h, y, ws, ws_bytes,
+                               stream) -> int:
+    return lib().ngr_ffn_linear_silu_linear(x, W1, W2, M, K, F, dtype, h, y,
+                                            ws, ws_bytes, stream)
+
+
+def ngr_row_stats(norm, x, eps, M, K, dtype, stats, stream) -> int:
+    return lib().ngr_row_stats(norm, x, eps, M, K, dtype, stats, stream)
+
+
+def ngr_workspace_error(ws, stream) -> int:
+    return lib().ngr_workspace_error(ws, stream)
+
+
+def ngr_debug_bounded_wait(ws, timeout_us, stream) -> int:
+    return lib().ngr_debug_bounded_wait(ws, timeout_us, stream)
+
+
+def ngr_status_string(status: int) -> str:
+    return lib().ngr_status_string(status).decode()
+
+
+def ngr_version() -> int:
+    return int(lib().ngr_version())
+
+
+def status_string(status: int) -> str:
+    try:
+        return ngr_status_string(status)
+    except Exception:
+        return STATUS.get(status, f"status {status}")
+
+
+# ---- tensor-level helpers ----------------------------------------------------------
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return NGR_F16
+    if t.dtype == torch.bfloat16:
+        return NGR_BF16
+    raise TypeError(f"tensors must be float16 or bfloat16, got {t.dtype}")
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _check(*ts, dtype):
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError("all tensors must be CUDA tensors")
+        if t.dtype != dtype:
+            raise TypeError("all tensors must share one dtype")
+        if not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _workspace(nbytes, device, workspace):
+    if workspace is None:
+        return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+    if workspace.numel() * workspace.element_size() < nbytes:
+        raise ValueError(f"workspace smaller than the {nbytes} bytes needed")
+    return workspace
+
+
+def _raise(rc, what):
+    if rc != 0:
+        raise NgrError(rc, what)
+
+
+def fused_layernorm_linear(x, gamma, beta, W, bias=None, eps=1e-5, out=None,
+                           workspace=None, stream=None):
+    """y = LayerNorm(x) . W^T (+ bias); x [..., K], W [N, K]."""
+    K = x.shape[-1]
+    N = W.shape[0]
+    x2 = x.reshape(-1, K)
+    M = x2.shape[0]
+    _check(x2, gamma, beta, W, bias, out, dtype=x.dtype)
+    y = out if out is not None else torch.empty((M, N), dtype=x.dtype, device=x.device)
+    nb = ngr_workspace_bytes(OP_LAYERNORM_LINEAR, M, K, N)
+    ws = _workspace(nb, x.device, workspace)
+    rc = ngr_fused_layernorm_linear(_ptr(x2), _ptr(gamma), _ptr(beta), _ptr(W),
+                                    _ptr(bias), float(eps), M, K, N,
+                                    _dtype_code(x), _ptr(y), _ptr(ws),
+                                    ws.numel() * ws.element_size(),
+                                    _stream(stream))
+    _raise(rc, "fused_layernorm_linear")
+    return y.reshape(*x.shape[:-1], N)
+
+
+def fused_rmsnorm_linear(x, gamma, W, bias=None, eps=1e-6, out=None,
+                         workspace=None, stream=None):
+    """y = RMSNorm(x) . W^T (+ bias)."""
+    K = x.shape[-1]
+    N = W.shape[0]
+    x2 = x.reshape(-1, K)
+    M = x2.shape[0]
+    _check(x2, gamma, W, bias, out, dtype=x.dtype)
+    y = out if out is not None else torch.empty((M, N), dtype=x.dtype, device=x.device)
+    nb = ngr_workspace_bytes(OP_RMSNORM_LINEAR, M, K, N)
+    ws = _workspace(nb, x.device, workspace)
+    rc = ngr_fused_rmsnorm_linear(_ptr(x2), _ptr(gamma), _ptr(W), _ptr(bias),
+                                  float(eps), M, K, N, _dtype_code(x), _ptr(y),
+                                  _ptr(ws), ws.numel() * ws.element_size(),
+                                  _stream(stream))
+    _raise(rc, "fused_rmsnorm_linear")
+    return y.reshape(*x.shape[:-1], N)
+
+
+def fused_linear_silu(x, W, bias=None, out=None, workspace=None, stream=None):
+    """y = SiLU(x . W^T + bias)."""
+    K = x.shape[-1]
+    N = W.shape[0]
+    x2 = x.reshape(-1, K)
+    M = x2.shape[0]
+    _check(x2, W, bias, out, dtype=x.dtype)
+    y = out if out is not None else torch.empty((M, N), dtype=x.dtype, device=x.device)
+    nb = ngr_workspace_bytes(OP_LINEAR_SILU, M, K, N)
+    ws = _workspace(nb, x.device, workspace)
+    rc = ngr_fused_linear_silu(_ptr(x2), _ptr(W), _ptr(bias), M, K, N,
+                               _dtype_code(x), _ptr(y), _ptr(ws),
+                               ws.numel() * ws.element_size(), _stream(stream))
+    _raise(rc, "fused_linear_silu")
+    return y.reshape(*x.shape[:-1], N)
+
+
+def ffn_linear_silu_linear(x, W1, W2, out=None, h=None, workspace=None,
+                           stream=None):
+    """y = SiLU(x . W1^T) . W2^T; W1 [F, K], W2 [K, F].  H goes to ``h``
+    when given, else into the workspace."""
+    K = x.shape[-1]
+    F = W1.shape[0]
+    x2 = x.reshape(-1, K)
+    M = x2.shape[0]
+    _check(x2, W1, W2, out, h, dtype=x.dtype)
+    y = out if out is not None else torch.empty((M, K), dtype=x.dtype, device=x.device)
+    nb = ngr_workspace_bytes(OP_FFN, M, K, F, 1 if h is None else 0)
+    ws = _workspace(nb, x.device, workspace)
+    rc = ngr_ffn_linear_silu_linear(_ptr(x2), _ptr(W1), _ptr(W2), M, K, F,
+                                    _dtype_code(x), _ptr(h), _ptr(y), _ptr(ws),
+                                    ws.numel() * ws.element_size(),
+                                    _stream(stream))
+    _raise(rc, "ffn_linear_silu_linear")
+    return y.reshape(*x.shape[:-1], K)
+
+
+def row_stats(x, norm: int, eps: float, stream=None) -> torch.Tensor:
+    """(mu, rstd) per row as a float32 [M, 2] tensor (norm 1 = LayerNorm,
+    2 = RMSNorm)."""
+    K = x.shape[-1]
+    x2 = x.reshape(-1, K)
+    M = x2.shape[0]
+    _check(x2, dtype=x.dtype)
+    st = torch.empty((M, 2), dtype=torch.float32, device=x.device)
+    rc = ngr_row_stats(norm, _ptr(x2), float(eps), M, K, _dtype_code(x),
+                       _ptr(st), _stream(stream))
+    _raise(rc, "row_stats")
+    return st

@@ -1,0 +1,462 @@
+// ngr_api.cu -- the C ABI declared in include/ngr.h: argument checks,
+// workspace layout, TMA descriptor encoding, choice of kernel and launch on
+// the caller's stream.  No device memory is allocated here.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "ngr.h"
+#include "ngr_internal.h"
+#include "ngr_ptx.cuh"
+
+namespace ngr {
+namespace {
+
+constexpr size_t kHeaderBytes = 256;  // error word + padding
+constexpr int kMaxDevices = 64;
+
+size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+struct WsLayout {
+    size_t stats = 0, gamma_f = 0, beta_f = 0;
+    size_t partials = 0, counters = 0, counters2 = 0, h = 0;
+    size_t total = 0;
+};
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Workspace regions, in order: header | stats | gamma_f | beta_f |
+// decode partials | counters | counters of the FFN's second GEMM | H.
+WsLayout ws_layout(int op, int64_t M, int64_t K, int64_t N, bool h_in_ws)
+{
+    WsLayout L;
+    size_t off = kHeaderBytes;
+    const bool norm = op == NGR_OP_LAYERNORM_LINEAR || op == NGR_OP_RMSNORM_LINEAR;
+    if (norm) {
+        L.stats = off;
+        off += align256(static_cast<size_t>(M) * 8);
+        L.gamma_f = off;
+        off += align256(static_cast<size_t>(K) * 4);
+        L.beta_f = off;
+        off += align256(static_cast<size_t>(K) * 4);
+    }
+    if (M > 0 && M <= kDecodeMaxM) {
+        const int64_t mn = M <= 16 ? 16 : 32;
+        const int64_t tiles1 = ceil_div(N, 128);
+        const int64_t tiles2 = op == NGR_OP_FFN ? ceil_div(K, 128) : 0;
+        const int64_t tmax = tiles1 > tiles2 ? tiles1 : tiles2;
+        L.partials = off;
+        off += align256(static_cast<size_t>(tmax) * kDecodeMaxContrib * mn * 128 * 4);
+        L.counters = off;
+        off += align256(static_cast<size_t>(tiles1) * 4 * 4);
+        if (op == NGR_OP_FFN) {
+            L.counters2 = off;
+            off += align256(static_cast<size_t>(tiles2) * 4 * 4);
+        }
+    }
+    if (op == NGR_OP_FFN && h_in_ws) {
+        L.h = off;
+        off += align256(static_cast<size_t>(M) * static_cast<size_t>(N) * 2);
+    }
+    L.total = off;
+    return L;
+}
+
+// ------------------------------------------------------------- device info
+struct DevInfo {
+    bool ready = false;
+    bool arch_ok = false;
+    int sms = 0;
+};
+std::mutex g_dev_mu;
+DevInfo g_dev[kMaxDevices];
+
+int current_device_info(DevInfo *out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return NGR_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return NGR_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    DevInfo &d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return NGR_ERR_CUDA;
+        d.arch_ok = (major == 10 && minor == 3);
+        d.sms = sms;
+        d.ready = true;
+    }
+    *out = d;
+    return d.arch_ok ? NGR_OK : NGR_ERR_ARCH;
+}
+
+// ------------------------------------------------------------ environment
+bool debug_mode()
+{
+    static const bool on = [] {
+        const char *v = std::getenv("NGR_DEBUG");
+        return v && v[0] && std::strcmp(v, "0") != 0;
+    }();
+    return on;
+}
+
+unsigned long long wait_timeout_ns()
+{
+    static const unsigned long long ns = [] {
+        const char *v = std::getenv("NGR_WAIT_TIMEOUT_MS");
+        long long ms = v ? std::atoll(v) : 0;
+        if (ms <= 0) ms = 2000;
+        return static_cast<unsigned long long>(ms) * 1000000ull;
+    }();
+    return ns;
+}
+
+// ---------------------------------------------------------- tensor maps
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// Row-major [rows, cols] 16-bit matrix, box {64 columns, box_rows rows},
+// 128-byte swizzle (the layout the tensor core reads K-major operands in).
+bool map_2d(CUtensorMap *m, const void *ptr, bool bf16, int64_t rows, int64_t cols,
+            uint32_t box_rows)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+               const_cast<void *>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// FP32 vector [n], box {64}.
+bool map_1d_f32(CUtensorMap *m, const float *ptr, int64_t n)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[1] = {static_cast<cuuint64_t>(n)};
+    cuuint32_t box[1] = {static_cast<cuuint32_t>(kBK)};
+    cuuint32_t estr[1] = {1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1, const_cast<float *>(ptr), dims, nullptr,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------- validation
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int64_t kMaxDim = int64_t(1) << 31;
+
+int check_sizes(int64_t M, int64_t K, int64_t N, int dtype)
+{
+    if (dtype != NGR_F16 && dtype != NGR_BF16) return NGR_ERR_DTYPE;
+    if (M < 0 || K <= 0 || N <= 0) return NGR_ERR_SHAPE;
+    if (M >= kMaxDim || K >= kMaxDim || N >= kMaxDim) return NGR_ERR_SHAPE;
+    if (K % 8 != 0 || N % 8 != 0) return NGR_ERR_ALIGN;
+    return NGR_OK;
+}
+
+int finish(int rc, void *ws, cudaStream_t stream)
+{
+    if (rc != NGR_OK) return rc;
+    if (cudaGetLastError() != cudaSuccess) return NGR_ERR_CUDA;
+    if (debug_mode()) return ngr_workspace_error(ws, reinterpret_cast<ngr_stream_t>(stream));
+    return NGR_OK;
+}
+
+// One linear layer y = act(norm(x) W^T + bias) on its own, given the
+// workspace regions.  `stats_ready` says whether a preceding grid on the
+// stream produced what this one reads (then it is launched as a
+// programmatic dependent).
+int launch_layer(int norm, bool silu, bool bf16, const void *x, const void *W,
+                 const void *bias, int64_t M, int64_t K, int64_t N, void *y,
+                 char *ws, const WsLayout &L, size_t counters_off, bool pdl,
+                 const DevInfo &di, cudaStream_t stream)
+{
+    int *err = reinterpret_cast<int *>(ws);
+    const bool has_norm = norm != kNormNone;
+    float2 *stats = has_norm ? reinterpret_cast<float2 *>(ws + L.stats) : nullptr;
+    float *gf = has_norm ? reinterpret_cast<float *>(ws + L.gamma_f) : nullptr;
+    float *bf = has_norm ? reinterpret_cast<float *>(ws + L.beta_f) : nullptr;
+    if (M <= kDecodeMaxM) {
+        DecodeArgs d;
+        std::memset(&d, 0, sizeof(d));
+        const int mn = M <= 16 ? 16 : 32;
+        if (!map_2d(&d.map_w, W, bf16, N, K, 128) || !map_2d(&d.map_x, x, bf16, M, K, mn))
+            return NGR_ERR_CUDA;
+        if (has_norm && (!map_1d_f32(&d.map_gamma, gf, K) || !map_1d_f32(&d.map_beta, bf, K)))
+            return NGR_ERR_CUDA;
+        d.stats = stats;
+        d.bias = bias;
+        d.y = y;
+        d.partials = reinterpret_cast<float *>(ws + L.partials);
+        d.counters = reinterpret_cast<int *>(ws + counters_off);
+        d.err = err;
+        d.M = static_cast<int>(M);
+        d.N = static_cast<int>(N);
+        d.K = static_cast<int>(K);
+        d.n_tiles = static_cast<int>(ceil_div(N, 128));
+        d.k_blocks = static_cast<int>(ceil_div(K, kBK));
+        d.units = static_cast<long long>(d.n_tiles) * d.k_blocks;
+        d.grid = plan_decode_grid(d.n_tiles, d.k_blocks, di.sms);
+        d.timeout_ns = wait_timeout_ns();
+        return launch_decode(norm, silu, bf16, mn, d, pdl, stream);
+    }
+    GemmArgs a;
+    std::memset(&a, 0, sizeof(a));
+    const GemmPlan plan = plan_gemm(M, N, K, di.sms);
+    if (!map_2d(&a.map_a, x, bf16, M, K, kBM) ||
+        !map_2d(&a.map_b, W, bf16, N, K, static_cast<uint32_t>(plan.bn)))
+        return NGR_ERR_CUDA;
+    if (has_norm && (!map_1d_f32(&a.map_gamma, gf, K) || !map_1d_f32(&a.map_beta, bf, K)))
+        return NGR_ERR_CUDA;
+    a.stats = stats;
+    a.bias = bias;
+    a.y = y;
+    a.err = err;
+    a.M = static_cast<int>(M);
+    a.N = static_cast<int>(N);
+    a.K = static_cast<int>(K);
+    a.m_tiles = static_cast<int>(ceil_div(M, kBM));
+    a.n_tiles = static_cast<int>(ceil_div(N, plan.bn));
+    a.k_blocks = static_cast<int>(ceil_div(K, kBK));
+    a.num_tiles = a.m_tiles * a.n_tiles;
+    a.timeout_ns = wait_timeout_ns();
+    return launch_gemm(norm, silu, bf16, plan, a, pdl, stream);
+}
+
+int norm_linear(int op, int norm, bool silu, const void *x, const void *gamma, const void *beta,
+                const void *W, const void *bias, float eps, int64_t M, int64_t K, int64_t N,
+                int dtype, void *y, void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    int rc = check_sizes(M, K, N, dtype);
+    if (rc != NGR_OK) return rc;
+    if (M == 0) return NGR_OK;
+    if (!x || !W || !y || !ws) return ws ? NGR_ERR_NULL : (x && W && y ? NGR_ERR_WORKSPACE : NGR_ERR_NULL);
+    if (norm != kNormNone && !gamma) return NGR_ERR_NULL;
+    if (norm == kNormLayer && !beta) return NGR_ERR_NULL;
+    if (!aligned16(x) || !aligned16(W) || !aligned16(y) || (gamma && !aligned16(gamma)) ||
+        (beta && !aligned16(beta)) || (bias && !aligned16(bias)))
+        return NGR_ERR_ALIGN;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return NGR_ERR_ALIGN;
+    const WsLayout L = ws_layout(op, M, K, N, false);
+    if (ws_bytes < L.total) return NGR_ERR_WORKSPACE;
+    DevInfo di;
+    rc = current_device_info(&di);
+    if (rc != NGR_OK) return rc;
+    const bool bf16 = dtype == NGR_BF16;
+    char *w = static_cast<char *>(ws);
+    if (debug_mode() && cudaMemsetAsync(w, 0, 4, stream) != cudaSuccess) return NGR_ERR_CUDA;
+    const bool decode = M <= kDecodeMaxM;
+    const bool need_stats = norm != kNormNone || decode;
+    if (need_stats) {
+        rc = launch_rowstats(norm == kNormNone ? kNormRms : norm, bf16, x,
+                             norm == kNormNone ? 0 : M, K, eps,
+                             reinterpret_cast<float2 *>(w + L.stats), gamma, beta,
+                             norm == kNormNone ? nullptr : reinterpret_cast<float *>(w + L.gamma_f),
+                             norm == kNormLayer ? reinterpret_cast<float *>(w + L.beta_f)
+                                                : (norm == kNormRms ? reinterpret_cast<float *>(w + L.beta_f) : nullptr),
+                             decode ? reinterpret_cast<int *>(w + L.counters) : nullptr,
+                             decode ? static_cast<int>(ceil_div(N, 128) * 4) : 0, di.sms, stream);
+        if (rc != NGR_OK) return rc;
+    }
+    rc = launch_layer(norm, silu, bf16, x, W, bias, M, K, N, y, w, L, L.counters, need_stats, di,
+                      stream);
+    return finish(rc, ws, stream);
+}
+
+__global__ void bounded_wait_probe_kernel(int *err, unsigned long long timeout_ns)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbarrier_init();
+    }
+    __syncthreads();
+    // Nothing ever arrives on `bar`: the wait must run out and record it.
+    if (threadIdx.x == 0) (void)mbar_wait(&bar, 0, err, timeout_ns);
+    __syncthreads();
+}
+
+}  // namespace
+
+int launch_bounded_wait_probe(int *err, unsigned long long timeout_ns, cudaStream_t stream)
+{
+    bounded_wait_probe_kernel<<<1, 32, 0, stream>>>(err, timeout_ns);
+    return cudaGetLastError() == cudaSuccess ? 0 : -7;
+}
+
+}  // namespace ngr
+
+using namespace ngr;
+
+extern "C" {
+
+size_t ngr_workspace_bytes(int op, int64_t M, int64_t K, int64_t N, int ffn_h_in_workspace)
+{
+    if (op < NGR_OP_LAYERNORM_LINEAR || op > NGR_OP_FFN) return 0;
+    if (M < 0 || K <= 0 || N <= 0 || M >= kMaxDim || K >= kMaxDim || N >= kMaxDim) return 0;
+    return ws_layout(op, M, K, N, ffn_h_in_workspace != 0).total;
+}
+
+int ngr_fused_layernorm_linear(const void *x, const void *gamma, const void *beta, const void *W,
+                               const void *bias, float eps, int64_t M, int64_t K, int64_t N,
+                               int dtype, void *y, void *workspace, size_t workspace_bytes,
+                               ngr_stream_t stream)
+{
+    return norm_linear(NGR_OP_LAYERNORM_LINEAR, kNormLayer, false, x, gamma, beta, W, bias, eps,
+                       M, K, N, dtype, y, workspace, workspace_bytes,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ngr_fused_rmsnorm_linear(const void *x, const void *gamma, const void *W, const void *bias,
+                             float eps, int64_t M, int64_t K, int64_t N, int dtype, void *y,
+                             void *workspace, size_t workspace_bytes, ngr_stream_t stream)
+{
+    return norm_linear(NGR_OP_RMSNORM_LINEAR, kNormRms, false, x, gamma, nullptr, W, bias, eps, M,
+                       K, N, dtype, y, workspace, workspace_bytes,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ngr_fused_linear_silu(const void *x, const void *W, const void *bias, int64_t M, int64_t K,
+                          int64_t N, int dtype, void *y, void *workspace, size_t workspace_bytes,
+                          ngr_stream_t stream)
+{
+    return norm_linear(NGR_OP_LINEAR_SILU, kNormNone, true, x, nullptr, nullptr, W, bias, 0.f, M,
+                       K, N, dtype, y, workspace, workspace_bytes,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ngr_ffn_linear_silu_linear(const void *x, const void *W1, const void *W2, int64_t M,
+                               int64_t K, int64_t F, int dtype, void *h, void *y, void *workspace,
+                               size_t workspace_bytes, ngr_stream_t stream_)
+{
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    int rc = check_sizes(M, K, F, dtype);
+    if (rc != NGR_OK) return rc;
+    if (M == 0) return NGR_OK;
+    if (!x || !W1 || !W2 || !y) return NGR_ERR_NULL;
+    if (!workspace) return NGR_ERR_WORKSPACE;
+    if (!aligned16(x) || !aligned16(W1) || !aligned16(W2) || !aligned16(y) ||
+        (h && !aligned16(h)))
+        return NGR_ERR_ALIGN;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return NGR_ERR_ALIGN;
+    const WsLayout L = ws_layout(NGR_OP_FFN, M, K, F, h == nullptr);
+    if (workspace_bytes < L.total) return NGR_ERR_WORKSPACE;
+    DevInfo di;
+    rc = current_device_info(&di);
+    if (rc != NGR_OK) return rc;
+    const bool bf16 = dtype == NGR_BF16;
+    char *w = static_cast<char *>(workspace);
+    void *H = h ? h : static_cast<void *>(w + L.h);
+    if (debug_mode() && cudaMemsetAsync(w, 0, 4, stream) != cudaSuccess) return NGR_ERR_CUDA;
+    const bool decode = M <= kDecodeMaxM;
+    if (decode) {
+        // Zero both GEMMs' split-K counters (they are adjacent).
+        const int n1 = static_cast<int>(ceil_div(F, 128) * 4);
+        const int n2 = static_cast<int>(ceil_div(K, 128) * 4);
+        const int n = static_cast<int>((L.counters2 - L.counters) / 4) + n2;
+        (void)n1;
+        rc = launch_rowstats(kNormRms, bf16, x, 0, K, 0.f, nullptr, nullptr, nullptr, nullptr,
+                             nullptr, reinterpret_cast<int *>(w + L.counters), n, di.sms, stream);
+        if (rc != NGR_OK) return rc;
+    }
+    rc = launch_layer(kNormNone, true, bf16, x, W1, nullptr, M, K, F, H, w, L, L.counters, decode,
+                      di, stream);
+    if (rc != NGR_OK) return rc;
+    rc = launch_layer(kNormNone, false, bf16, H, W2, nullptr, M, F, K, y, w, L, L.counters2, true,
+                      di, stream);
+    return finish(rc, workspace, stream);
+}
+
+int ngr_row_stats(int norm, const void *x, float eps, int64_t M, int64_t K, int dtype,
+                  float *stats, ngr_stream_t stream)
+{
+    if (norm != kNormLayer && norm != kNormRms) return NGR_ERR_ARG;
+    int rc = check_sizes(M, K, 8, dtype);
+    if (rc != NGR_OK) return rc;
+    if (M == 0) return NGR_OK;
+    if (!x || !stats) return NGR_ERR_NULL;
+    if (!aligned16(x) || (reinterpret_cast<uintptr_t>(stats) & 7u) != 0) return NGR_ERR_ALIGN;
+    DevInfo di;
+    rc = current_device_info(&di);
+    if (rc != NGR_OK) return rc;
+    rc = launch_rowstats(norm, dtype == NGR_BF16, x, M, K, eps, reinterpret_cast<float2 *>(stats),
+                         nullptr, nullptr, nullptr, nullptr, nullptr, 0, di.sms,
+                         reinterpret_cast<cudaStream_t>(stream));
+    if (rc != NGR_OK) return rc;
+    return cudaGetLastError() == cudaSuccess ? NGR_OK : NGR_ERR_CUDA;
+}
+
+int ngr_workspace_error(void *workspace, ngr_stream_t stream)
+{
+    if (!workspace) return NGR_ERR_WORKSPACE;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return NGR_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return NGR_ERR_CUDA;
+    if (v != 0 && cudaMemset(workspace, 0, sizeof(int)) != cudaSuccess) return NGR_ERR_CUDA;
+    return v == 0 ? NGR_OK : NGR_ERR_TIMEOUT;
+}
+
+int ngr_debug_bounded_wait(void *workspace, uint32_t timeout_us, ngr_stream_t stream_)
+{
+    if (!workspace) return NGR_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return NGR_ERR_ALIGN;
+    DevInfo di;
+    int rc = current_device_info(&di);
+    if (rc != NGR_OK) return rc;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (cudaMemsetAsync(workspace, 0, sizeof(int), stream) != cudaSuccess) return NGR_ERR_CUDA;
+    rc = launch_bounded_wait_probe(static_cast<int *>(workspace),
+                                   static_cast<unsigned long long>(timeout_us) * 1000ull, stream);
+    return rc == 0 ? NGR_OK : NGR_ERR_CUDA;
+}
+
+const char *ngr_status_string(int status)
+{
+    switch (status) {
+    case NGR_OK: return "NGR_OK";
+    case NGR_ERR_NULL: return "NGR_ERR_NULL: a required pointer is NULL";
+    case NGR_ERR_SHAPE: return "NGR_ERR_SHAPE: invalid M, K or N";
+    case NGR_ERR_ALIGN: return "NGR_ERR_ALIGN: K or N not a multiple of 8, or a misaligned pointer";
+    case NGR_ERR_DTYPE: return "NGR_ERR_DTYPE: dtype must be NGR_F16 or NGR_BF16";
+    case NGR_ERR_WORKSPACE: return "NGR_ERR_WORKSPACE: workspace missing or too small";
+    case NGR_ERR_ARCH: return "NGR_ERR_ARCH: the current device is not sm_103 (GB300)";
+    case NGR_ERR_CUDA: return "NGR_ERR_CUDA: a CUDA call failed";
+    case NGR_ERR_TIMEOUT: return "NGR_ERR_TIMEOUT: a kernel's bounded wait ran out";
+    case NGR_ERR_ARG: return "NGR_ERR_ARG: invalid argument";
+    default: return "unknown ngr status";
+    }
+}
+
+int ngr_version(void) { return 100; }
+
+}  // extern "C"

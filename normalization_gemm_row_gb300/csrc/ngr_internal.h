@@ -1,0 +1,88 @@
+// ngr_internal.h -- declarations shared by the library's translation units
+// (kernel launchers, argument blocks, workspace layout).  Not installed.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace ngr {
+
+enum { kNormNone = 0, kNormLayer = 1, kNormRms = 2 };
+
+// Tile geometry shared by host and device.
+constexpr int kBM = 128;        // rows of x per tile (UMMA M)
+constexpr int kBK = 64;         // K per pipeline stage: 64 x 2 B = one 128-byte swizzle row
+constexpr int kUmmaK = 16;      // K per tcgen05.mma (kind::f16)
+constexpr int kGemmThreads = 384;  // 12 warps: producer, MMA, TMEM, spare, 4 transform, 4 epilogue
+
+// Decode (swap-AB) path: weight rows on the UMMA M side, tokens on N.
+constexpr int kDecodeMaxM = 32;      // M up to this uses the decode path
+constexpr int kDecodeMaxContrib = 4; // CTAs sharing one 128-row weight tile (split-K)
+constexpr int kDecodeThreads = 384;
+
+// Arguments of the persistent GEMM kernel (normal orientation: x rows on M).
+struct alignas(128) GemmArgs {
+    CUtensorMap map_a;      // activations [M, K], box {64, 128}, 128-byte swizzle
+    CUtensorMap map_b;      // weights [N, K], box {64, BN}, 128-byte swizzle
+    CUtensorMap map_gamma;  // [K], box {64}
+    CUtensorMap map_beta;   // [K], box {64}
+    const float2 *stats;    // [M] (mu, rstd); unused without a norm
+    const void *bias;       // [N] or nullptr
+    void *y;                // [M, N]
+    int *err;               // device error word
+    int M, N, K;
+    int m_tiles, n_tiles, k_blocks, num_tiles;
+    unsigned long long timeout_ns;
+};
+
+// Arguments of the decode kernel (swap-AB, split-K over a stream of
+// (weight tile, k block) units).
+struct alignas(128) DecodeArgs {
+    CUtensorMap map_w;      // weights [N, K], box {64, 128}, 128-byte swizzle
+    CUtensorMap map_x;      // activations [M, K], box {64, MN}, 128-byte swizzle
+    CUtensorMap map_gamma;
+    CUtensorMap map_beta;
+    const float2 *stats;
+    const void *bias;
+    void *y;
+    float *partials;        // [n_tiles][kDecodeMaxContrib][MN][128] fp32
+    int *counters;          // [n_tiles], zero at kernel start
+    int *err;
+    int M, N, K;
+    int n_tiles, k_blocks;
+    long long units;        // n_tiles * k_blocks
+    int grid;               // CTAs the units are divided among
+    unsigned long long timeout_ns;
+};
+
+// GEMM tile variant selected by the host planner.
+struct GemmPlan {
+    int bn;          // N tile (UMMA N)
+    int stages;      // pipeline depth
+    int grid;        // persistent CTAs
+    size_t smem;     // dynamic shared memory bytes
+};
+
+// Launchers (return 0 or a negative ngr_status).
+int launch_rowstats(int norm, bool bf16, const void *x, int64_t M, int64_t K,
+                    float eps, float2 *stats, const void *gamma,
+                    const void *beta, float *gamma_f, float *beta_f,
+                    int *counters, int n_counters, int num_sms,
+                    cudaStream_t stream);
+
+int launch_gemm(int norm, bool silu, bool bf16, const GemmPlan &plan,
+                const GemmArgs &args, bool pdl, cudaStream_t stream);
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms);
+size_t gemm_smem_bytes(int bn, int stages, bool norm);
+
+int launch_decode(int norm, bool silu, bool bf16, int mn, const DecodeArgs &args,
+                  bool pdl, cudaStream_t stream);
+int plan_decode_grid(int64_t n_tiles, int64_t k_blocks, int num_sms);
+size_t decode_smem_bytes(int mn);
+
+int launch_bounded_wait_probe(int *err, unsigned long long timeout_ns,
+                              cudaStream_t stream);
+
+}  // namespace ngr

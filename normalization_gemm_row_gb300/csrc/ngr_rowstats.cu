@@ -1,0 +1,210 @@
+// ngr_rowstats.cu -- step a1: per-row FP32 statistics of x [M, K].
+//
+// "LayerNorm 融合算子如何让大模型推理再快 15%？深度拆解 ATB 的实现", §1.1: the
+// statistics are a reduction over each row (a sum and a sum of squares);
+// §2.3: they are computed in FP32.  One warp reduces one row with 16-byte
+// loads.  LayerNorm uses a shifted, mergeable form so that a large row mean
+// (inputs centred far from zero) does not cancel the variance: each lane
+// keeps (n, mean, M2) of its own elements, built from sums of (x - s) with s
+// the lane's first element, and the lanes are merged pairwise with the
+// parallel-variance update of Chan, Golub and LeVeque (1979):
+//   n = na + nb,  d = mb - ma,  mean = ma + d nb / n,
+//   M2 = M2a + M2b + d^2 na nb / n.
+// var = M2 / K (biased), rstd = 1 / sqrt(var + eps).  RMSNorm: rstd =
+// 1 / sqrt(sum x^2 / K + eps) and mu = 0.
+//
+// The same launch converts gamma and beta to FP32 once per call (the GEMM's
+// producer streams them with the tiles) and zeroes the split-K tile counters
+// of the decode path when asked to, so that they start from zero every call.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "ngr_internal.h"
+#include "ngr_ptx.cuh"
+
+namespace ngr {
+
+template <bool BF16>
+__device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8])
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if constexpr (BF16) {
+            __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162 *>(&w[i]);
+            float2 p = __bfloat1622float2(h);
+            f[2 * i] = p.x;
+            f[2 * i + 1] = p.y;
+        } else {
+            __half2 h = *reinterpret_cast<const __half2 *>(&w[i]);
+            float2 p = __half22float2(h);
+            f[2 * i] = p.x;
+            f[2 * i + 1] = p.y;
+        }
+    }
+}
+
+template <int NORM, bool BF16>
+__global__ void __launch_bounds__(256) rowstats_kernel(
+    const uint4 *__restrict__ x, int64_t M, int64_t K, float eps,
+    float2 *__restrict__ stats, const void *__restrict__ gamma,
+    const void *__restrict__ beta, float *__restrict__ gamma_f,
+    float *__restrict__ beta_f, int *__restrict__ counters, int n_counters)
+{
+    // The dependent GEMM may start its prologue while this grid runs; it
+    // waits for this grid's completion before reading the statistics.
+    pdl_launch_dependents();
+
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+
+    const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t gstride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    if (counters) {
+        for (int64_t i = gtid; i < n_counters; i += gstride) counters[i] = 0;
+    }
+    if (gamma_f) {
+        for (int64_t k = gtid; k < K; k += gstride) {
+            if constexpr (BF16) {
+                gamma_f[k] = __bfloat162float(static_cast<const __nv_bfloat16 *>(gamma)[k]);
+                if (beta_f)
+                    beta_f[k] = beta ? __bfloat162float(static_cast<const __nv_bfloat16 *>(beta)[k]) : 0.f;
+            } else {
+                gamma_f[k] = __half2float(static_cast<const __half *>(gamma)[k]);
+                if (beta_f)
+                    beta_f[k] = beta ? __half2float(static_cast<const __half *>(beta)[k]) : 0.f;
+            }
+        }
+    }
+
+    const int64_t vec_per_row = K >> 3;  // 8 elements per 16-byte vector
+    for (int64_t row = warp; row < M; row += nwarps) {
+        const uint4 *xr = x + row * vec_per_row;
+        if constexpr (NORM == kNormLayer) {
+            float s = 0.f, s1 = 0.f, s2 = 0.f;
+            float n = 0.f;
+            bool have_shift = false;
+            int64_t v = lane;
+            // Four loads in flight per lane.
+            for (; v + 96 < vec_per_row; v += 128) {
+                uint4 q[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) q[u] = __ldg(xr + v + 32 * u);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    float f[8];
+                    unpack8<BF16>(q[u], f);
+                    if (!have_shift) {
+                        s = f[0];
+                        have_shift = true;
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float d = f[i] - s;
+                        s1 += d;
+                        s2 = fmaf(d, d, s2);
+                    }
+                    n += 8.f;
+                }
+            }
+            for (; v < vec_per_row; v += 32) {
+                float f[8];
+                unpack8<BF16>(__ldg(xr + v), f);
+                if (!have_shift) {
+                    s = f[0];
+                    have_shift = true;
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float d = f[i] - s;
+                    s1 += d;
+                    s2 = fmaf(d, d, s2);
+                }
+                n += 8.f;
+            }
+            // This lane's (n, mean, M2).
+            float mean = n > 0.f ? s + s1 / n : 0.f;
+            float m2 = n > 0.f ? fmaxf(s2 - s1 * (s1 / n), 0.f) : 0.f;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                const float nb = __shfl_xor_sync(0xffffffffu, n, off);
+                const float mb = __shfl_xor_sync(0xffffffffu, mean, off);
+                const float m2b = __shfl_xor_sync(0xffffffffu, m2, off);
+                const float nt = n + nb;
+                if (nt > 0.f) {
+                    const float d = mb - mean;
+                    const float wb = nb / nt;
+                    // Symmetric in (a, b) up to rounding, so both lanes of
+                    // a pair keep the same merged value.
+                    mean = fmaf(d, wb, mean);
+                    m2 = m2 + m2b + d * d * (n * wb);
+                    n = nt;
+                }
+            }
+            if (lane == 0) {
+                const float var = m2 / static_cast<float>(K);
+                stats[row] = make_float2(mean, 1.0f / sqrtf(var + eps));
+            }
+        } else {
+            float ss = 0.f;
+            int64_t v = lane;
+            for (; v + 96 < vec_per_row; v += 128) {
+                uint4 q[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) q[u] = __ldg(xr + v + 32 * u);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    float f[8];
+                    unpack8<BF16>(q[u], f);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
+                }
+            }
+            for (; v < vec_per_row; v += 32) {
+                float f[8];
+                unpack8<BF16>(__ldg(xr + v), f);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+                ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            if (lane == 0)
+                stats[row] = make_float2(0.f, 1.0f / sqrtf(ss / static_cast<float>(K) + eps));
+        }
+    }
+}
+
+int launch_rowstats(int norm, bool bf16, const void *x, int64_t M, int64_t K,
+                    float eps, float2 *stats, const void *gamma,
+                    const void *beta, float *gamma_f, float *beta_f,
+                    int *counters, int n_counters, int num_sms,
+                    cudaStream_t stream)
+{
+    const int threads = 256;
+    const int64_t rows_per_block = threads / 32;
+    int64_t blocks = (M + rows_per_block - 1) / rows_per_block;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    if (blocks > cap) blocks = cap;
+    const int64_t kblocks = (K + threads - 1) / threads;
+    if (gamma_f && blocks < kblocks) blocks = kblocks < cap ? kblocks : cap;
+    if (blocks < 1) blocks = 1;
+    const uint4 *xv = static_cast<const uint4 *>(x);
+    dim3 grid(static_cast<unsigned>(blocks)), block(threads);
+    if (norm == kNormLayer) {
+        if (bf16)
+            rowstats_kernel<kNormLayer, true><<<grid, block, 0, stream>>>(xv, M, K, eps, stats, gamma, beta, gamma_f, beta_f, counters, n_counters);
+        else
+            rowstats_kernel<kNormLayer, false><<<grid, block, 0, stream>>>(xv, M, K, eps, stats, gamma, beta, gamma_f, beta_f, counters, n_counters);
+    } else {
+        if (bf16)
+            rowstats_kernel<kNormRms, true><<<grid, block, 0, stream>>>(xv, M, K, eps, stats, gamma, beta, gamma_f, beta_f, counters, n_counters);
+        else
+            rowstats_kernel<kNormRms, false><<<grid, block, 0, stream>>>(xv, M, K, eps, stats, gamma, beta, gamma_f, beta_f, counters, n_counters);
+    }
+    return cudaGetLastError() == cudaSuccess ? 0 : -7;
+}
+
+}  // namespace ngr

@@ -1,0 +1,119 @@
+"""The C-ABI library on the host: it loads, exports every symbol the header
+declares, and rejects bad arguments before touching a GPU (no compute call
+is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import normalization_gemm_row_gb300 as pkg
+from normalization_gemm_row_gb300 import binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ngr.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pkg.build()
+    return B.lib()
+
+
+def header_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ngr_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_symbols_exported(lib):
+    syms = header_symbols()
+    assert len(syms) >= 10
+    for s in syms:
+        assert hasattr(lib, s), f"{s} declared in ngr.h but not exported"
+    # The binding marshals every declared entry point, and nothing else.
+    assert sorted(B.SIGNATURES) == syms
+
+
+def test_version_and_status_strings(lib):
+    assert B.ngr_version() >= 100
+    for code, name in B.STATUS.items():
+        assert B.ngr_status_string(code).startswith(name)
+    assert "unknown" in B.ngr_status_string(12345)
+
+
+def test_workspace_bytes_layout(lib):
+    wb = B.ngr_workspace_bytes
+    assert wb(B.OP_LAYERNORM_LINEAR, 0, 8, 8) == 256 + 2 * 256  # header, fp32 gamma, beta
+    assert wb(B.OP_LINEAR_SILU, 0, 8, 8) == 256
+    big = wb(B.OP_LAYERNORM_LINEAR, 1024, 8192, 8192)
+    # header + stats (8 B/row) + fp32 gamma and beta
+    assert big == 256 + 1024 * 8 + 2 * 8192 * 4
+    assert wb(B.OP_RMSNORM_LINEAR, 1024, 8192, 8192) == big
+    assert wb(B.OP_LINEAR_SILU, 1024, 8192, 8192) == 256
+    # decode sizes carry split-K partials and counters
+    dec = wb(B.OP_LAYERNORM_LINEAR, 16, 8192, 28672)
+    tiles = 28672 // 128
+    assert dec >= 256 + 256 + 2 * 8192 * 4 + tiles * 4 * 16 * 128 * 4 + tiles * 16
+    assert wb(B.OP_LAYERNORM_LINEAR, 17, 64, 64) > wb(B.OP_LAYERNORM_LINEAR, 16, 64, 64)
+    # the FFN's H only when it lives in the workspace
+    h0 = wb(B.OP_FFN, 512, 14336, 49152, 0)
+    h1 = wb(B.OP_FFN, 512, 14336, 49152, 1)
+    assert h1 - h0 == 512 * 49152 * 2
+    # invalid sizes give 0
+    assert wb(B.OP_FFN, -1, 8, 8) == 0 and wb(7, 1, 8, 8) == 0 and wb(0, 1, 0, 8) == 0
+
+
+A16 = 0x10000  # a fake, 16-byte aligned address: never dereferenced here
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(x=0), -1),                                # NULL x
+    (dict(gamma=0), -1),                            # NULL gamma
+    (dict(beta=0), -1),                             # NULL beta (LayerNorm)
+    (dict(K=12), -3),                               # K not a multiple of 8
+    (dict(N=20), -3),                               # N not a multiple of 8
+    (dict(x=A16 + 2), -3),                          # misaligned x
+    (dict(bias=A16 + 8), -3),                       # misaligned bias
+    (dict(ws=A16 + 16), -3),                        # workspace not 256-B aligned
+    (dict(dtype=3), -4),                            # bad dtype
+    (dict(M=-1), -2),                               # negative M
+    (dict(K=0), -2),
+    (dict(ws_bytes=100), -5),                       # workspace too small
+    (dict(ws=0), -5),                               # no workspace
+    (dict(M=0), 0),                                 # empty batch is a no-op
+])
+def test_layernorm_linear_rejects_before_launch(lib, kw, expect):
+    a = dict(x=A16, gamma=A16, beta=A16, W=A16, bias=None, eps=1e-5, M=4,
+             K=64, N=64, dtype=0, y=A16, ws=A16 * 16, ws_bytes=1 << 20,
+             stream=None)
+    a.update(kw)
+    rc = B.ngr_fused_layernorm_linear(a["x"], a["gamma"], a["beta"], a["W"],
+                                      a["bias"], a["eps"], a["M"], a["K"],
+                                      a["N"], a["dtype"], a["y"], a["ws"],
+                                      a["ws_bytes"], a["stream"])
+    assert rc == expect, B.ngr_status_string(rc)
+
+
+def test_other_entry_points_reject(lib):
+    assert B.ngr_fused_rmsnorm_linear(A16, 0, A16, None, 1e-6, 4, 64, 64, 0,
+                                      A16, A16 * 16, 1 << 20, None) == -1
+    assert B.ngr_fused_linear_silu(A16, A16, None, 4, 60, 64, 1, A16, A16 * 16,
+                                   1 << 20, None) == -3
+    assert B.ngr_ffn_linear_silu_linear(A16, A16, 0, 4, 64, 64, 0, None, A16,
+                                        A16 * 16, 1 << 20, None) == -1
+    # H in the workspace needs room for it
+    need = B.ngr_workspace_bytes(B.OP_FFN, 64, 64, 64, 1)
+    assert B.ngr_ffn_linear_silu_linear(A16, A16, A16, 64, 64, 64, 0, None,
+                                        A16, A16 * 16, need - 256, None) == -5
+    assert B.ngr_row_stats(3, A16, 1e-5, 4, 64, 0, A16, None) == -9
+    assert B.ngr_row_stats(1, A16, 1e-5, 4, 64, 0, 0, None) == -1
+    assert B.ngr_workspace_error(None, None) == -5
+    assert B.ngr_debug_bounded_wait(None, 10, None) == -5
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(B, "_lib", None)
+    monkeypatch.setattr(B, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not found"):
+        B.lib()
