@@ -146,6 +146,10 @@ int ngr_debug_bounded_wait(void *workspace, uint32_t timeout_us,
 /* Human-readable name of a status code (static storage). */
 const char *ngr_status_string(int status);
 
+/* Text describing the last CUDA failure seen by this thread (the call that
+ * failed and the CUDA error); empty if none.  Static thread-local storage. */
+const char *ngr_last_error(void);
+
 /* Library version, major * 10000 + minor * 100 + patch. */
 int ngr_version(void);
 

@@ -44,13 +44,20 @@ SIGNATURES = {
     "ngr_debug_bounded_wait": (_I, [_P, _U32, _P]),
     "ngr_status_string": (ctypes.c_char_p, [_I]),
     "ngr_version": (_I, []),
+    "ngr_last_error": (ctypes.c_char_p, []),
 }
 
 
 class NgrError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
-        super().__init__(f"{what} failed: {status_string(status)}")
+        msg = f"{what} failed: {status_string(status)}"
+        if status == -7:
+            try:
+                msg += f" [{ngr_last_error()}]"
+            except Exception:
+                pass
+        super().__init__(msg)
 
 
 _lib = None
@@ -122,6 +129,10 @@ def ngr_status_string(status: int) -> str:
 
 def ngr_version() -> int:
     return int(lib().ngr_version())
+
+
+def ngr_last_error() -> str:
+    return lib().ngr_last_error().decode()
 
 
 def status_string(status: int) -> str:

@@ -6,6 +6,7 @@
 
 #include <cstdint>
 #include <cstdlib>
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 
@@ -14,6 +15,18 @@
 #include "ngr_ptx.cuh"
 
 namespace ngr {
+
+namespace {
+thread_local char g_last_error[512] = "";
+}
+
+int record_cuda_error(const char *what, int code, const char *detail)
+{
+    std::snprintf(g_last_error, sizeof(g_last_error), "%s failed: code %d (%s)", what, code,
+                  detail ? detail : "");
+    return -7;
+}
+
 namespace {
 
 constexpr size_t kHeaderBytes = 256;  // error word + padding
@@ -78,7 +91,8 @@ DevInfo g_dev[kMaxDevices];
 int current_device_info(DevInfo *out)
 {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return NGR_ERR_CUDA;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return record_cuda_error("cudaGetDevice", e, cudaGetErrorString(e));
     if (dev < 0 || dev >= kMaxDevices) return NGR_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_dev_mu);
     DevInfo &d = g_dev[dev];
@@ -143,29 +157,47 @@ bool map_2d(CUtensorMap *m, const void *ptr, bool bf16, int64_t rows, int64_t co
             uint32_t box_rows)
 {
     EncodeTiledFn enc = encode_fn();
-    if (!enc) return false;
+    if (!enc) {
+        record_cuda_error("cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)", 0, "");
+        return false;
+    }
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
     cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
     cuuint32_t estr[2] = {1, 1};
-    return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-               const_cast<void *>(ptr), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    const CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                           const_cast<void *>(ptr), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        record_cuda_error("cuTensorMapEncodeTiled (2-D)", static_cast<int>(r), "");
+        return false;
+    }
+    return true;
 }
 
-// FP32 vector [n], box {64}.
-bool map_1d_f32(CUtensorMap *m, const float *ptr, int64_t n)
+// FP32 gamma and beta as the two rows of a [2, K] matrix whose rows are
+// `row_stride` bytes apart; box {64 columns, 2 rows}, no swizzle.
+bool map_gb(CUtensorMap *m, const float *gamma_f, int64_t K, size_t row_stride)
 {
     EncodeTiledFn enc = encode_fn();
-    if (!enc) return false;
-    cuuint64_t dims[1] = {static_cast<cuuint64_t>(n)};
-    cuuint32_t box[1] = {static_cast<cuuint32_t>(kBK)};
-    cuuint32_t estr[1] = {1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1, const_cast<float *>(ptr), dims, nullptr,
-               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    if (!enc) {
+        record_cuda_error("cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)", 0, "");
+        return false;
+    }
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), 2};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_stride)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), 2};
+    cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(gamma_f),
+                           dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        record_cuda_error("cuTensorMapEncodeTiled (gamma/beta)", static_cast<int>(r), "");
+        return false;
+    }
+    return true;
 }
 
 // ------------------------------------------------------------- validation
@@ -185,7 +217,8 @@ int check_sizes(int64_t M, int64_t K, int64_t N, int dtype)
 int finish(int rc, void *ws, cudaStream_t stream)
 {
     if (rc != NGR_OK) return rc;
-    if (cudaGetLastError() != cudaSuccess) return NGR_ERR_CUDA;
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return record_cuda_error("kernel launch", e, cudaGetErrorString(e));
     if (debug_mode()) return ngr_workspace_error(ws, reinterpret_cast<ngr_stream_t>(stream));
     return NGR_OK;
 }
@@ -199,25 +232,26 @@ int launch_layer(int norm, bool silu, bool bf16, const void *x, const void *W,
                  char *ws, const WsLayout &L, size_t counters_off, bool pdl,
                  const DevInfo &di, cudaStream_t stream)
 {
+    // A kernel launched as a programmatic dependent is never a call's first.
+    const int zero_err = pdl ? 0 : 1;
     int *err = reinterpret_cast<int *>(ws);
     const bool has_norm = norm != kNormNone;
     float2 *stats = has_norm ? reinterpret_cast<float2 *>(ws + L.stats) : nullptr;
     float *gf = has_norm ? reinterpret_cast<float *>(ws + L.gamma_f) : nullptr;
-    float *bf = has_norm ? reinterpret_cast<float *>(ws + L.beta_f) : nullptr;
     if (M <= kDecodeMaxM) {
         DecodeArgs d;
         std::memset(&d, 0, sizeof(d));
         const int mn = M <= 16 ? 16 : 32;
         if (!map_2d(&d.map_w, W, bf16, N, K, 128) || !map_2d(&d.map_x, x, bf16, M, K, mn))
             return NGR_ERR_CUDA;
-        if (has_norm && (!map_1d_f32(&d.map_gamma, gf, K) || !map_1d_f32(&d.map_beta, bf, K)))
-            return NGR_ERR_CUDA;
+        if (has_norm && !map_gb(&d.map_gb, gf, K, L.beta_f - L.gamma_f)) return NGR_ERR_CUDA;
         d.stats = stats;
         d.bias = bias;
         d.y = y;
         d.partials = reinterpret_cast<float *>(ws + L.partials);
         d.counters = reinterpret_cast<int *>(ws + counters_off);
         d.err = err;
+        d.zero_err = zero_err;
         d.M = static_cast<int>(M);
         d.N = static_cast<int>(N);
         d.K = static_cast<int>(K);
@@ -234,12 +268,12 @@ int launch_layer(int norm, bool silu, bool bf16, const void *x, const void *W,
     if (!map_2d(&a.map_a, x, bf16, M, K, kBM) ||
         !map_2d(&a.map_b, W, bf16, N, K, static_cast<uint32_t>(plan.bn)))
         return NGR_ERR_CUDA;
-    if (has_norm && (!map_1d_f32(&a.map_gamma, gf, K) || !map_1d_f32(&a.map_beta, bf, K)))
-        return NGR_ERR_CUDA;
+    if (has_norm && !map_gb(&a.map_gb, gf, K, L.beta_f - L.gamma_f)) return NGR_ERR_CUDA;
     a.stats = stats;
     a.bias = bias;
     a.y = y;
     a.err = err;
+    a.zero_err = zero_err;
     a.M = static_cast<int>(M);
     a.N = static_cast<int>(N);
     a.K = static_cast<int>(K);
@@ -283,7 +317,8 @@ int norm_linear(int op, int norm, bool silu, const void *x, const void *gamma, c
                              norm == kNormLayer ? reinterpret_cast<float *>(w + L.beta_f)
                                                 : (norm == kNormRms ? reinterpret_cast<float *>(w + L.beta_f) : nullptr),
                              decode ? reinterpret_cast<int *>(w + L.counters) : nullptr,
-                             decode ? static_cast<int>(ceil_div(N, 128) * 4) : 0, di.sms, stream);
+                             decode ? static_cast<int>(ceil_div(N, 128) * 4) : 0,
+                             reinterpret_cast<int *>(w), di.sms, stream);
         if (rc != NGR_OK) return rc;
     }
     rc = launch_layer(norm, silu, bf16, x, W, bias, M, K, N, y, w, L, L.counters, need_stats, di,
@@ -294,13 +329,16 @@ int norm_linear(int op, int norm, bool silu, const void *x, const void *gamma, c
 __global__ void bounded_wait_probe_kernel(int *err, unsigned long long timeout_ns)
 {
     __shared__ uint64_t bar;
+    __shared__ int abort_flag;
     if (threadIdx.x == 0) {
+        abort_flag = 0;
         mbar_init(&bar, 1);
         fence_mbarrier_init();
     }
     __syncthreads();
     // Nothing ever arrives on `bar`: the wait must run out and record it.
-    if (threadIdx.x == 0) (void)mbar_wait(&bar, 0, err, timeout_ns);
+    const WaitCtx wc{&abort_flag, err, timeout_ns};
+    if (threadIdx.x == 0) (void)mbar_wait(&bar, 0, wc);
     __syncthreads();
 }
 
@@ -384,7 +422,8 @@ int ngr_ffn_linear_silu_linear(const void *x, const void *W1, const void *W2, in
         const int n = static_cast<int>((L.counters2 - L.counters) / 4) + n2;
         (void)n1;
         rc = launch_rowstats(kNormRms, bf16, x, 0, K, 0.f, nullptr, nullptr, nullptr, nullptr,
-                             nullptr, reinterpret_cast<int *>(w + L.counters), n, di.sms, stream);
+                             nullptr, reinterpret_cast<int *>(w + L.counters), n,
+                             reinterpret_cast<int *>(w), di.sms, stream);
         if (rc != NGR_OK) return rc;
     }
     rc = launch_layer(kNormNone, true, bf16, x, W1, nullptr, M, K, F, H, w, L, L.counters, decode,
@@ -408,7 +447,7 @@ int ngr_row_stats(int norm, const void *x, float eps, int64_t M, int64_t K, int 
     rc = current_device_info(&di);
     if (rc != NGR_OK) return rc;
     rc = launch_rowstats(norm, dtype == NGR_BF16, x, M, K, eps, reinterpret_cast<float2 *>(stats),
-                         nullptr, nullptr, nullptr, nullptr, nullptr, 0, di.sms,
+                         nullptr, nullptr, nullptr, nullptr, nullptr, 0, nullptr, di.sms,
                          reinterpret_cast<cudaStream_t>(stream));
     if (rc != NGR_OK) return rc;
     return cudaGetLastError() == cudaSuccess ? NGR_OK : NGR_ERR_CUDA;
@@ -458,5 +497,7 @@ const char *ngr_status_string(int status)
 }
 
 int ngr_version(void) { return 100; }
+
+const char *ngr_last_error(void) { return g_last_error; }
 
 }  // extern "C"

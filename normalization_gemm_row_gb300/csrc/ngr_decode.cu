@@ -31,12 +31,11 @@ template <int MN, int STAGES>
 struct DecodeSmem {
     static constexpr int kW = 128 * kBK * 2;   // 16 KB weight tile
     static constexpr int kX = MN * kBK * 2;    // MN x 128 B token tile
-    static constexpr int kGB = kBK * 4;
+    static constexpr int kGB = 2 * kBK * 4;    // FP32 gamma[64] then beta[64]
     static constexpr int off_w = 0;
     static constexpr int off_x = off_w + STAGES * kW;
     static constexpr int off_g = off_x + STAGES * kX;
-    static constexpr int off_be = off_g + STAGES * kGB;
-    static constexpr int off_bar = off_be + STAGES * kGB;
+    static constexpr int off_bar = off_g + STAGES * kGB;
     static constexpr int n_bars = 3 * STAGES + 5;
     static constexpr int off_tmem = off_bar + n_bars * 8;
     static constexpr int bytes = off_tmem + 16;
@@ -57,8 +56,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 {
     using L = DecodeSmem<MN, STAGES>;
     constexpr bool kNorm = NORM != kNormNone;
-    constexpr bool kBeta = NORM == kNormLayer;
-    constexpr uint32_t kTx = L::kW + L::kX + (kNorm ? L::kGB : 0) + (kBeta ? L::kGB : 0);
+    constexpr uint32_t kTx = L::kW + L::kX + (kNorm ? L::kGB : 0);
     constexpr uint32_t kTmemCols = 2 * MN <= 32 ? 32 : 64;
     constexpr uint32_t kIdesc = idesc_f16(BF16, 128, MN);
     static_assert(MN == 16 || MN == 32, "token tile");
@@ -69,7 +67,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     uint8_t *sW = smem + L::off_w;
     uint8_t *sX = smem + L::off_x;
     float *sG = reinterpret_cast<float *>(smem + L::off_g);
-    float *sBe = reinterpret_cast<float *>(smem + L::off_be);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::off_bar);
     uint64_t *full = bars;
     uint64_t *empty = bars + STAGES;
@@ -81,14 +78,16 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    int *err = args.err;
-    const uint64_t tmo = args.timeout_ns;
+    __shared__ int abort_flag;
+    const WaitCtx wc{&abort_flag, args.err, args.timeout_ns};
 
     if (threadIdx.x == 0) {
+        abort_flag = 0;
+        // The first kernel of a call clears the call's error word.
+        if (args.zero_err && blockIdx.x == 0) *args.err = 0;
         prefetch_tmap(&args.map_w);
         prefetch_tmap(&args.map_x);
-        if constexpr (kNorm) prefetch_tmap(&args.map_gamma);
-        if constexpr (kBeta) prefetch_tmap(&args.map_beta);
+        if constexpr (kNorm) prefetch_tmap(&args.map_gb);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
@@ -129,14 +128,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             for (long long u = u_begin; u < u_end; ++u) {
                 const int tile = static_cast<int>(u / KB);
                 const int kc = static_cast<int>(u % KB) * kBK;
-                if (!mbar_wait(&empty[stage], phase ^ 1u, err, tmo)) break;
+                if (!mbar_wait(&empty[stage], phase ^ 1u, wc)) break;
                 mbar_arrive_expect_tx(&full[stage], kTx);
                 tma_load_2d(sW + stage * L::kW, &args.map_w, &full[stage], kc, tile * 128, pol_w);
                 tma_load_2d(sX + stage * L::kX, &args.map_x, &full[stage], kc, 0, pol_x);
                 if constexpr (kNorm)
-                    tma_load_1d(sG + stage * kBK, &args.map_gamma, &full[stage], kc, pol_x);
-                if constexpr (kBeta)
-                    tma_load_1d(sBe + stage * kBK, &args.map_beta, &full[stage], kc, pol_x);
+                    tma_load_2d(sG + stage * 2 * kBK, &args.map_gb, &full[stage], kc, 0, pol_x);
                 ++fills;
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
@@ -145,7 +142,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                 int s = stage - j;
                 uint32_t p = phase;
                 if (s < 0) { s += STAGES; p ^= 1u; }
-                mbar_wait(&full[s], p, err, tmo);
+                mbar_wait(&full[s], p, wc);
             }
         }
     } else if (warp == 1) {
@@ -160,14 +157,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             while (ok && u < u_end) {
                 const long long tile = u / KB;
                 const long long seg_end = (tile + 1) * KB < u_end ? (tile + 1) * KB : u_end;
-                if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, err, tmo)) break;
+                if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, wc)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * MN);
                 bool first = true;
                 for (; u < seg_end; ++u) {
-                    if (!mbar_wait(&full[stage], phase, err, tmo)) { ok = false; break; }
+                    if (!mbar_wait(&full[stage], phase, wc)) { ok = false; break; }
                     if constexpr (kNorm) {
-                        if (!mbar_wait(&ready[stage], phase, err, tmo)) { ok = false; break; }
+                        if (!mbar_wait(&ready[stage], phase, wc)) { ok = false; break; }
                     }
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(sW + stage * L::kW);
@@ -187,7 +184,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                 if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
             }
             umma_commit(drain);
-            mbar_wait(drain, 0, err, tmo);
+            mbar_wait(drain, 0, wc);
         }
     } else if (warp >= 4 && warp < 8) {
         if constexpr (kNorm) {
@@ -209,9 +206,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             for (long long u = u_begin; u < u_end; ++u) {
-                if (!mbar_wait_warp(&full[stage], phase, err, tmo)) break;
-                const float *g = sG + stage * kBK + 8 * c;
-                const float *b = sBe + stage * kBK + 8 * c;
+                if (!mbar_wait_warp(&full[stage], phase, wc)) break;
+                const float *g = sG + stage * 2 * kBK + 8 * c;
+                const float *b = g + kBK;
 #pragma unroll
                 for (int h = 0; h < MN / 16; ++h) {
                     const int r = (t >> 3) + 16 * h;
@@ -236,7 +233,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             const long long tile = u / KB;
             const long long seg_end = (tile + 1) * KB < u_end ? (tile + 1) * KB : u_end;
             u = seg_end;
-            if (!mbar_wait_warp(&acc_full[acc], acc_phase, err, tmo)) break;
+            if (!mbar_wait_warp(&acc_full[acc], acc_phase, wc)) break;
             tc_fence_after();
             float v[MN];
             {
@@ -340,8 +337,9 @@ static int launch_decode_variant(const DecodeArgs &args, bool pdl, cudaStream_t 
 {
     auto kern = decode_kernel<NORM, SILU, BF16, MN, 10>;
     constexpr int smem = DecodeSmem<MN, 10>::alloc;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-        return -7;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess)
+        return record_cuda_error("cudaFuncSetAttribute(max dynamic smem)", e, cudaGetErrorString(e));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(args.grid));
     cfg.blockDim = dim3(kDecodeThreads);
@@ -352,7 +350,8 @@ static int launch_decode_variant(const DecodeArgs &args, bool pdl, cudaStream_t 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kern, args) == cudaSuccess ? 0 : -7;
+    e = cudaLaunchKernelEx(&cfg, kern, args);
+    return e == cudaSuccess ? 0 : record_cuda_error("cudaLaunchKernelEx", e, cudaGetErrorString(e));
 }
 
 int launch_decode(int norm, bool silu, bool bf16, int mn, const DecodeArgs &args, bool pdl,

@@ -119,12 +119,11 @@ template <int BN, int STAGES>
 struct GemmSmem {
     static constexpr int kA = kBM * kBK * 2;        // 16 KB
     static constexpr int kB = BN * kBK * 2;         // BN x 128 B
-    static constexpr int kGB = kBK * 4;             // 64 FP32 gamma (or beta) values
+    static constexpr int kGB = 2 * kBK * 4;         // FP32 gamma[64] then beta[64]
     static constexpr int off_a = 0;
     static constexpr int off_b = off_a + STAGES * kA;
     static constexpr int off_g = off_b + STAGES * kB;
-    static constexpr int off_be = off_g + STAGES * kGB;
-    static constexpr int off_bar = off_be + STAGES * kGB;
+    static constexpr int off_bar = off_g + STAGES * kGB;
     static constexpr int n_bars = 3 * STAGES + 5;
     static constexpr int off_tmem = off_bar + n_bars * 8;
     static constexpr int bytes = off_tmem + 16;
@@ -137,8 +136,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 {
     using L = GemmSmem<BN, STAGES>;
     constexpr bool kNorm = NORM != kNormNone;
-    constexpr bool kBeta = NORM == kNormLayer;
-    constexpr uint32_t kTx = L::kA + L::kB + (kNorm ? L::kGB : 0) + (kBeta ? L::kGB : 0);
+    constexpr uint32_t kTx = L::kA + L::kB + (kNorm ? L::kGB : 0);
     constexpr uint32_t kTmemCols = TmemCols<BN>::value;
     constexpr uint32_t kIdesc = idesc_f16(BF16, kBM, BN);
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "UMMA N for M = 128");
@@ -148,8 +146,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *sA = smem + L::off_a;
     uint8_t *sB = smem + L::off_b;
-    float *sG = reinterpret_cast<float *>(smem + L::off_g);    // FP32 gamma per stage
-    float *sBe = reinterpret_cast<float *>(smem + L::off_be);  // FP32 beta per stage
+    float *sG = reinterpret_cast<float *>(smem + L::off_g);    // FP32 gamma, beta per stage
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::off_bar);
     uint64_t *full = bars;                 // TMA landed          (1 arrival + tx)
     uint64_t *empty = bars + STAGES;       // MMA done with stage (1 commit)
@@ -161,14 +158,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    int *err = args.err;
-    const uint64_t tmo = args.timeout_ns;
+    __shared__ int abort_flag;
+    const WaitCtx wc{&abort_flag, args.err, args.timeout_ns};
 
     if (threadIdx.x == 0) {
+        abort_flag = 0;
+        // The first kernel of a call clears the call's error word.
+        if (args.zero_err && blockIdx.x == 0) *args.err = 0;
         prefetch_tmap(&args.map_a);
         prefetch_tmap(&args.map_b);
-        if constexpr (kNorm) prefetch_tmap(&args.map_gamma);
-        if constexpr (kBeta) prefetch_tmap(&args.map_beta);
+        if constexpr (kNorm) prefetch_tmap(&args.map_gb);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
@@ -213,15 +212,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const int m0 = (tile % m_tiles) * kBM;
                 const int n0 = (tile / m_tiles) * BN;
                 for (int kb = 0; kb < k_blocks; ++kb) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, err, tmo)) { ok = false; break; }
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, wc)) { ok = false; break; }
                     mbar_arrive_expect_tx(&full[stage], kTx);
                     const int kc = kb * kBK;
                     tma_load_2d(sA + stage * L::kA, &args.map_a, &full[stage], kc, m0, pol_x);
                     tma_load_2d(sB + stage * L::kB, &args.map_b, &full[stage], kc, n0, pol_w);
                     if constexpr (kNorm)
-                        tma_load_1d(sG + stage * kBK, &args.map_gamma, &full[stage], kc, pol_x);
-                    if constexpr (kBeta)
-                        tma_load_1d(sBe + stage * kBK, &args.map_beta, &full[stage], kc, pol_x);
+                        tma_load_2d(sG + stage * 2 * kBK, &args.map_gb, &full[stage], kc, 0, pol_x);
                     ++fills;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -233,7 +230,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 int s = stage - j;
                 uint32_t p = phase;
                 if (s < 0) { s += STAGES; p ^= 1u; }
-                mbar_wait(&full[s], p, err, tmo);
+                mbar_wait(&full[s], p, wc);
             }
         }
     } else if (warp == 1) {
@@ -245,13 +242,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint32_t acc_phase = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, err, tmo)) break;
+                if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, wc)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
                 for (int kb = 0; kb < k_blocks; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, err, tmo)) { ok = false; break; }
+                    if (!mbar_wait(&full[stage], phase, wc)) { ok = false; break; }
                     if constexpr (kNorm) {
-                        if (!mbar_wait(&ready[stage], phase, err, tmo)) { ok = false; break; }
+                        if (!mbar_wait(&ready[stage], phase, wc)) { ok = false; break; }
                     }
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(sA + stage * L::kA);
@@ -271,7 +268,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             // All MMAs issued by this thread complete before TMEM is freed.
             umma_commit(drain);
-            mbar_wait(drain, 0, err, tmo);
+            mbar_wait(drain, 0, wc);
         }
     } else if (warp >= 4 && warp < 8) {
         if constexpr (kNorm) {
@@ -288,9 +285,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const float sc = st.y;
                 const float of = -st.x * st.y;
                 for (int kb = 0; kb < k_blocks; ++kb) {
-                    if (!mbar_wait_warp(&full[stage], phase, err, tmo)) { ok = false; break; }
-                    const float *g = sG + stage * kBK;
-                    const float *b = sBe + stage * kBK;
+                    if (!mbar_wait_warp(&full[stage], phase, wc)) { ok = false; break; }
+                    const float *g = sG + stage * 2 * kBK;
+                    const float *b = g + kBK;
                     uint8_t *arow = sA + stage * L::kA + t * 128;
                     const int sw = t & 7;
 #pragma unroll
@@ -315,7 +312,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         uint32_t acc_phase = 0;
         const int M = args.M, N = args.N;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-            if (!mbar_wait_warp(&acc_full[acc], acc_phase, err, tmo)) break;
+            if (!mbar_wait_warp(&acc_full[acc], acc_phase, wc)) break;
             tc_fence_after();
             const int row = (tile % m_tiles) * kBM + q * 32 + lane;
             const int nt0 = (tile / m_tiles) * BN;
@@ -385,8 +382,9 @@ int launch_gemm_variant(const GemmArgs &args, int grid, bool pdl, cudaStream_t s
 {
     auto kern = gemm_kernel<NORM, SILU, BF16, BN, STAGES>;
     constexpr int smem = GemmSmem<BN, STAGES>::alloc;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-        return -7;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess)
+        return record_cuda_error("cudaFuncSetAttribute(max dynamic smem)", e, cudaGetErrorString(e));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(kGemmThreads);
@@ -397,7 +395,8 @@ int launch_gemm_variant(const GemmArgs &args, int grid, bool pdl, cudaStream_t s
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kern, args) == cudaSuccess ? 0 : -7;
+    e = cudaLaunchKernelEx(&cfg, kern, args);
+    return e == cudaSuccess ? 0 : record_cuda_error("cudaLaunchKernelEx", e, cudaGetErrorString(e));
 }
 
 // Dispatch one BN over the (norm, activation, dtype) combinations the

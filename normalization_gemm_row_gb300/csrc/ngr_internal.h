@@ -26,12 +26,12 @@ constexpr int kDecodeThreads = 384;
 struct alignas(128) GemmArgs {
     CUtensorMap map_a;      // activations [M, K], box {64, 128}, 128-byte swizzle
     CUtensorMap map_b;      // weights [N, K], box {64, BN}, 128-byte swizzle
-    CUtensorMap map_gamma;  // [K], box {64}
-    CUtensorMap map_beta;   // [K], box {64}
+    CUtensorMap map_gb;     // FP32 [2, K] = rows gamma, beta; box {64, 2}
     const float2 *stats;    // [M] (mu, rstd); unused without a norm
     const void *bias;       // [N] or nullptr
     void *y;                // [M, N]
     int *err;               // device error word
+    int zero_err;           // nonzero: this kernel is the call's first and clears *err
     int M, N, K;
     int m_tiles, n_tiles, k_blocks, num_tiles;
     unsigned long long timeout_ns;
@@ -42,14 +42,14 @@ struct alignas(128) GemmArgs {
 struct alignas(128) DecodeArgs {
     CUtensorMap map_w;      // weights [N, K], box {64, 128}, 128-byte swizzle
     CUtensorMap map_x;      // activations [M, K], box {64, MN}, 128-byte swizzle
-    CUtensorMap map_gamma;
-    CUtensorMap map_beta;
+    CUtensorMap map_gb;
     const float2 *stats;
     const void *bias;
     void *y;
     float *partials;        // [n_tiles][kDecodeMaxContrib][MN][128] fp32
     int *counters;          // [n_tiles], zero at kernel start
     int *err;
+    int zero_err;
     int M, N, K;
     int n_tiles, k_blocks;
     long long units;        // n_tiles * k_blocks
@@ -65,12 +65,16 @@ struct GemmPlan {
     size_t smem;     // dynamic shared memory bytes
 };
 
+// Record why a CUDA call failed (thread-local; read back through
+// ngr_last_error).  Returns -7 (NGR_ERR_CUDA) for use in return statements.
+int record_cuda_error(const char *what, int code, const char *detail);
+
 // Launchers (return 0 or a negative ngr_status).
 int launch_rowstats(int norm, bool bf16, const void *x, int64_t M, int64_t K,
                     float eps, float2 *stats, const void *gamma,
                     const void *beta, float *gamma_f, float *beta_f,
-                    int *counters, int n_counters, int num_sms,
-                    cudaStream_t stream);
+                    int *counters, int n_counters, int *err_to_clear,
+                    int num_sms, cudaStream_t stream);
 
 int launch_gemm(int norm, bool silu, bool bf16, const GemmPlan &plan,
                 const GemmArgs &args, bool pdl, cudaStream_t stream);

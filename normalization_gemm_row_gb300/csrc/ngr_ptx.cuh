@@ -67,21 +67,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// Where a bounded wait reports to: `abort` is a per-CTA flag in shared
+// memory (zeroed at kernel start) that tells the CTA's other roles to stop;
+// `err` is the device error word of the call, which kernels only ever set.
+struct WaitCtx {
+    int *abort;                 // shared memory
+    int *err;                   // global memory
+    unsigned long long timeout_ns;
+};
+
 // Wait for the phase of `bar` with parity `parity` to complete.  Gives up
-// after `timeout_ns` of global time, or as soon as another thread of the grid
-// has recorded an error in *err; on giving up it records kDevErrTimeout
-// (first error wins) and returns false.
-static __device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err,
-                                       uint64_t timeout_ns)
+// after `timeout_ns` of global time, or as soon as another role of this CTA
+// has given up; on giving up it raises the CTA's abort flag, records
+// kDevErrTimeout in the error word and returns false.
+static __device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const WaitCtx &w)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63u) == 0) {
-            if (*reinterpret_cast<volatile int *>(err) != 0) return false;
-            if (global_timer_ns() - t0 > timeout_ns) {
-                atomicCAS(err, 0, kDevErrTimeout);
+            if (*reinterpret_cast<volatile int *>(w.abort) != 0) return false;
+            if (global_timer_ns() - t0 > w.timeout_ns) {
+                *reinterpret_cast<volatile int *>(w.abort) = 1;
+                atomicExch(w.err, kDevErrTimeout);
                 return false;
             }
         }
@@ -91,11 +100,10 @@ static __device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, in
 // Warp-uniform form for roles whose next step is warp-collective: lane 0
 // waits, the verdict is broadcast, and every lane then acquires the
 // completed phase itself.  All 32 lanes must call it.
-__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity,
-                                               int *err, uint64_t timeout_ns)
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, const WaitCtx &w)
 {
     int ok = 0;
-    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, err, timeout_ns) ? 1 : 0;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, w) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (ok) (void)mbar_try_wait(bar, parity);
     return ok != 0;

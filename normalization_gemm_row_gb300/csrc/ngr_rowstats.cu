@@ -15,7 +15,8 @@
 //
 // The same launch converts gamma and beta to FP32 once per call (the GEMM's
 // producer streams them with the tiles) and zeroes the split-K tile counters
-// of the decode path when asked to, so that they start from zero every call.
+// of the decode path when asked to, so that they start from zero every call;
+// as the first kernel of a call it also clears the call's error word.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -50,7 +51,8 @@ __global__ void __launch_bounds__(256) rowstats_kernel(
     const uint4 *__restrict__ x, int64_t M, int64_t K, float eps,
     float2 *__restrict__ stats, const void *__restrict__ gamma,
     const void *__restrict__ beta, float *__restrict__ gamma_f,
-    float *__restrict__ beta_f, int *__restrict__ counters, int n_counters)
+    float *__restrict__ beta_f, int *__restrict__ counters, int n_counters,
+    int *__restrict__ err_to_clear)
 {
     // The dependent GEMM may start its prologue while this grid runs; it
     // waits for this grid's completion before reading the statistics.
@@ -62,6 +64,7 @@ __global__ void __launch_bounds__(256) rowstats_kernel(
 
     const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t gstride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    if (err_to_clear && gtid == 0) *err_to_clear = 0;
     if (counters) {
         for (int64_t i = gtid; i < n_counters; i += gstride) counters[i] = 0;
     }
@@ -180,8 +183,8 @@ __global__ void __launch_bounds__(256) rowstats_kernel(
 int launch_rowstats(int norm, bool bf16, const void *x, int64_t M, int64_t K,
                     float eps, float2 *stats, const void *gamma,
                     const void *beta, float *gamma_f, float *beta_f,
-                    int *counters, int n_counters, int num_sms,
-                    cudaStream_t stream)
+                    int *counters, int n_counters, int *err_to_clear,
+                    int num_sms, cudaStream_t stream)
 {
     const int threads = 256;
     const int64_t rows_per_block = threads / 32;
@@ -195,16 +198,17 @@ int launch_rowstats(int norm, bool bf16, const void *x, int64_t M, int64_t K,
     dim3 grid(static_cast<unsigned>(blocks)), block(threads);
     if (norm == kNormLayer) {
         if (bf16)
-            rowstats_kernel<kNormLayer, true><<<grid, block, 0, stream>>>(xv, M, K, eps, stats, gamma, beta, gamma_f, beta_f, counters, n_counters);
+            rowstats_kernel<kNormLayer, true><<<grid, block, 0, stream>>>(xv, M, K, eps, stats, gamma, beta, gamma_f, beta_f, counters, n_counters, err_to_clear);
         else
-            rowstats_kernel<kNormLayer, false><<<grid, block, 0, stream>>>(xv, M, K, eps, stats, gamma, beta, gamma_f, beta_f, counters, n_counters);
+            rowstats_kernel<kNormLayer, false><<<grid, block, 0, stream>>>(xv, M, K, eps, stats, gamma, beta, gamma_f, beta_f, counters, n_counters, err_to_clear);
     } else {
         if (bf16)
-            rowstats_kernel<kNormRms, true><<<grid, block, 0, stream>>>(xv, M, K, eps, stats, gamma, beta, gamma_f, beta_f, counters, n_counters);
+            rowstats_kernel<kNormRms, true><<<grid, block, 0, stream>>>(xv, M, K, eps, stats, gamma, beta, gamma_f, beta_f, counters, n_counters, err_to_clear);
         else
-            rowstats_kernel<kNormRms, false><<<grid, block, 0, stream>>>(xv, M, K, eps, stats, gamma, beta, gamma_f, beta_f, counters, n_counters);
+            rowstats_kernel<kNormRms, false><<<grid, block, 0, stream>>>(xv, M, K, eps, stats, gamma, beta, gamma_f, beta_f, counters, n_counters, err_to_clear);
     }
-    return cudaGetLastError() == cudaSuccess ? 0 : -7;
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? 0 : record_cuda_error("row statistics launch", e, cudaGetErrorString(e));
 }
 
 }  // namespace ngr

@@ -141,6 +141,21 @@ def test_deterministic_repeat():
     assert torch.equal(y1, y2)
 
 
+@pytest.mark.parametrize("M", [16, 300])
+def test_garbage_workspace(M):
+    """A workspace full of garbage (here 0xFF bytes) must not matter: every
+    call initialises what it reads from it."""
+    d = inputs.case("layernorm_linear", M, 8192, 1024, torch.float16, True, seed=5)
+    g = to_dev(d)
+    nb = B.ngr_workspace_bytes(B.OP_LAYERNORM_LINEAR, M, 8192, 1024)
+    ws = torch.full((nb,), 255, dtype=torch.uint8, device="cuda")
+    y = ngr.fused_layernorm_linear(g["x"], g["gamma"], g["beta"], g["W"], g["bias"], 1e-5,
+                                   workspace=ws)
+    s = torch.cuda.current_stream().cuda_stream
+    assert B.ngr_workspace_error(ws.data_ptr(), s) == 0
+    assert_parity(y.double().cpu().numpy(), ref_op("layernorm_linear", d, 1e-5), f"garbage ws M={M}")
+
+
 def test_row_stats_against_oracle():
     for norm in (oracle.NORM_LAYER, oracle.NORM_RMS):
         for dt in (torch.float16, torch.bfloat16):
