@@ -1,0 +1,512 @@
+"""Benchmark of the fused pre-norm linear layer on GB300.
+
+One step = one fused LayerNorm + linear + bias call over one batch:
+x [1024, 8192] fp16 (the [8, 128, 8192] activations) against W [8192, 8192]
+with FP32 statistics and accumulation.  Prints ONE JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--no-cpu-baseline]
+
+--impl reference times the fp64 CPU oracle (the reference arm of this
+build) on the host cores, each step a bounded sample of rows of the same
+workload.  Under torchrun with N > 1 every rank runs an independent replica
+on its own GPU (the layer's rows are independent; no collective on the data
+path) and the job value is N x work / max-over-ranks time.
+
+Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier
+and torch.cuda.synchronize(), timed with CUDA events on the launching
+stream.  Inputs rotate over enough independent sets (x, W, bias, y) that the
+bytes touched between two uses of one set exceed twice the L2 size, so no
+step finds its weights in L2.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+import torch.distributed as dist  # noqa: E402
+
+L2_BYTES = 129 * 2 ** 20
+DEFAULT_WORKLOAD = "ln_linear_bias_f16_m1024_k8192_n8192"
+PROFILES = os.path.join(ROOT, "profiles")
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (replicas)
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not dist.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier():
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(value: float) -> float:
+    """Largest `value` over all ranks (the job's time is its slowest rank)."""
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(units_per_rank: float, world: int, max_seconds: float) -> float:
+    """Whole-job throughput: the units every rank processed over the slowest
+    rank's time."""
+    return units_per_rank * world / max_seconds
+
+
+# ----------------------------------------------------------------------------
+# clocks sampled during the timed region
+class ClockSampler:
+    FIELDS = ("index,timestamp,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "100", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self) -> dict:
+        time.sleep(0.25)
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    p = [c.strip() for c in line.split(",")]
+                    if len(p) < 10:
+                        continue
+                    try:
+                        ts = time.mktime(time.strptime(p[1].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                        ts += float("0." + p[1].split(".")[1]) if "." in p[1] else 0.0
+                        rows.append(dict(ts=ts, sm=float(p[2]), sm_max=float(p[3]),
+                                         power=float(p[4]) if p[4] not in ("[N/A]", "N/A") else None,
+                                         hw=p[6], hw_thermal=p[7], sw_thermal=p[8], sw_power=p[9]))
+                    except (ValueError, IndexError):
+                        continue
+        finally:
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        inside = [r for r in rows if self.t0 - 0.05 <= r["ts"] <= self.t1 + 0.05]
+        extended = False
+        if len(inside) < 3:
+            # The timed region was shorter than a few sampling periods: use
+            # the samples nearest to it (the same load ran around it).
+            mid = 0.5 * (self.t0 + self.t1)
+            inside = sorted(rows, key=lambda r: abs(r["ts"] - mid))[:3]
+            extended = True
+        reasons = set()
+        for r in inside:
+            for k, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                            ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+                if r[k].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in inside),
+                "sm_max_mhz": max(r["sm_max"] for r in inside),
+                "reasons": sorted(reasons), "samples": len(inside),
+                "window_extended": extended}
+
+
+# ----------------------------------------------------------------------------
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
+                "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def kernel_source_hash() -> str:
+    """Hash of the sources of the tile kernel, to tell whether a stored ncu
+    traffic figure still describes the kernel that runs."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "normalization_gemm_row_gb300", "csrc")
+    for name in ("ngr_gemm_kernel.cuh", "ngr_ptx.cuh", "ngr_internal.h", "ngr_decode.cu"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(workload: str):
+    """Per-launch DRAM bytes of the dominant kernel from the committed ncu
+    summary, if it was taken on the current kernel sources; else None."""
+    path = os.path.join(PROFILES, f"traffic_{workload}.txt")
+    try:
+        kv = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("kernel_source_hash") != kernel_source_hash():
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# ----------------------------------------------------------------------------
+def our_arm(args, rank, world, local):
+    import normalization_gemm_row_gb300 as ngr
+    from normalization_gemm_row_gb300 import binding as B
+    from normalization_gemm_row_gb300 import inputs
+
+    ngr.build()
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+    w = inputs.BY_NAME[args.workload]
+    if args.m is not None:
+        w = w.with_m(args.m)
+    M, K, N = w.M, w.K, w.N
+    decode = M <= 32
+    ffn = w.op == "ffn"
+
+    # Input sets: one seeded draw on the host, copied to every set (identical
+    # values, distinct buffers), enough sets that the bytes between two uses
+    # of a set exceed 2 x L2.
+    host = inputs.make(w)
+    keys = ["x", "W1", "W2"] if ffn else ["x", "gamma", "beta", "W", "bias"]
+    keys = [k for k in keys if host.get(k) is not None]
+    out_cols = K if ffn else N
+    set_bytes = sum(host[k].numel() * host[k].element_size() for k in keys) + M * out_cols * 2
+    n_sets = max(2, min(16, math.ceil(2 * L2_BYTES / set_bytes) + 1))
+    sets = []
+    for _ in range(n_sets):
+        s = {k: host[k].to(dev) for k in keys}
+        s["y"] = torch.empty((M, out_cols), dtype=w.dtype, device=dev)
+        if ffn:
+            s["h"] = torch.empty((M, N), dtype=w.dtype, device=dev)
+        op_code = {"layernorm_linear": B.OP_LAYERNORM_LINEAR, "rmsnorm_linear": B.OP_RMSNORM_LINEAR,
+                   "linear_silu": B.OP_LINEAR_SILU, "ffn": B.OP_FFN}[w.op]
+        nb = B.ngr_workspace_bytes(op_code, M, K, N, 0)
+        s["ws"] = torch.empty(max(nb, 256), dtype=torch.uint8, device=dev)
+        sets.append(s)
+
+    def step(s, stream=None):
+        if w.op == "layernorm_linear":
+            ngr.fused_layernorm_linear(s["x"], s["gamma"], s["beta"], s["W"], s.get("bias"), w.eps,
+                                       out=s["y"], workspace=s["ws"], stream=stream)
+        elif w.op == "rmsnorm_linear":
+            ngr.fused_rmsnorm_linear(s["x"], s["gamma"], s["W"], s.get("bias"), w.eps,
+                                     out=s["y"], workspace=s["ws"], stream=stream)
+        elif w.op == "linear_silu":
+            ngr.fused_linear_silu(s["x"], s["W"], s.get("bias"), out=s["y"], workspace=s["ws"],
+                                  stream=stream)
+        else:
+            ngr.ffn_linear_silu_linear(s["x"], s["W1"], s["W2"], out=s["y"], h=s["h"],
+                                       workspace=s["ws"], stream=stream)
+
+    # kernels one call launches: statistics (norm ops, and every decode call,
+    # which also clears its split-K counters) + one GEMM per linear layer
+    if ffn:
+        kernels_per_step = 3 if decode else 2
+    elif w.op == "linear_silu":
+        kernels_per_step = 2 if decode else 1
+    else:
+        kernels_per_step = 2
+    stream = torch.cuda.current_stream(dev)
+    for i in range(args.warmup):
+        step(sets[i % n_sets])
+    torch.cuda.synchronize(dev)
+
+    # -------------------------------------------------- timed region (value)
+    clocks = ClockSampler(local if world > 1 else dev.index)
+    clocks.start()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    clocks.mark_start()
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(sets[i % n_sets])
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks.mark_end()
+    barrier()
+    clock_info = clocks.stop()
+    ms_total = ev0.elapsed_time(ev1)
+    ms_total_max = max_over_ranks(ms_total)
+    flops = w.flops
+    algo_bytes = sum(host[k].numel() * host[k].element_size() for k in keys) + M * out_cols * 2
+    if ffn:
+        algo_bytes += 2 * M * N * 2  # H written once and read once
+    ms_step = ms_total_max / args.steps
+    if decode:
+        metric, unit = "fused LN+GEMM HBM GB/s at M<=16 (decode)", "GB/s"
+        value = job_value(algo_bytes * args.steps / 1e9, world, ms_total_max / 1e3)
+    else:
+        metric, unit = "fused LN/RMSNorm+GEMM TFLOP/s (% dense FP16 peak)", "TFLOP/s"
+        value = job_value(flops * args.steps / 1e12, world, ms_total_max / 1e3)
+
+    # ------------------------- dominant-kernel time (CUDA events per kernel)
+    torch.cuda.synchronize(dev)
+    B.kernel_timing_start(args.steps)
+    for i in range(args.steps):
+        step(sets[i % n_sets])
+    times = B.kernel_timing_stop()
+    assert len(times) == args.steps and all(len(t) == kernels_per_step for t in times), times[:2]
+    per_kernel = [statistics.mean(t[j] for t in times) for j in range(kernels_per_step)]
+    dom = max(range(kernels_per_step), key=lambda j: per_kernel[j])
+    peaks = measured_peaks()
+    if decode:
+        achieved = algo_bytes / (per_kernel[dom] / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        dom_flops = flops if not ffn else flops / 2.0
+        achieved = dom_flops / (per_kernel[dom] / 1e3) / 1e12
+        # fp16 and bf16 run at the same dense tensor rate (ratio 1).
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = stored_traffic(w.name if args.m is None else f"{w.name}_m{M}")
+    roof["peak_source"] = peaks["source"] + " (burst)"
+    roof["kernel_ms"] = per_kernel[dom]
+    roof["kernel_ms_all"] = per_kernel
+
+    # ----------------------------------------- end to end from host buffers
+    x_host = host["x"].pin_memory()
+    y_host = torch.empty((M, out_cols), dtype=w.dtype).pin_memory()
+    for i in range(min(3, args.warmup + 1)):
+        s = sets[i % n_sets]
+        s["x"].copy_(x_host, non_blocking=True)
+        step(s)
+        y_host.copy_(s["y"], non_blocking=True)
+    torch.cuda.synchronize(dev)
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        s = sets[i % n_sets]
+        s["x"].copy_(x_host, non_blocking=True)
+        step(s)
+        y_host.copy_(s["y"], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1))
+    if decode:
+        e2e_value = job_value(algo_bytes * args.steps / 1e9, world, e2e_ms / 1e3)
+    else:
+        e2e_value = job_value(flops * args.steps / 1e12, world, e2e_ms / 1e3)
+    e2e = {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": M * K * 2,
+           "d2h_bytes_per_step": M * out_cols * 2}
+
+    out = {
+        "metric": metric, "value": value, "unit": unit, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16" if w.dtype == torch.float16 else "bf16",
+        "data": "synthetic (seeded; shapes and distributions of the pages' workload)",
+        "config": {"workload": w.name, "op": w.op, "M": M, "K": K, "N": N,
+                   "bias": w.bias, "eps": w.eps, "global_batch": M * world,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": f"{n_sets} rotating input sets of {set_bytes / 2**20:.0f} MiB "
+                         f"(> 2 x L2 between reuses)",
+                   "accumulate": "fp32", "statistics": "fp32"},
+        "roofline": roof,
+        "e2e": e2e,
+        "gpu_launches": kernels_per_step * args.steps,
+        "clocks": clock_info,
+        "pct_of_dense_fp16_peak": None if decode else 100.0 * value / world / peaks["bf16_tflops"],
+    }
+    return out, w, host
+
+
+def cpu_baseline(w, host, target_s: float):
+    """The fp64 oracle as it stands on the host cores, on a bounded sample
+    of rows of the same workload.  Returns the cpu_baseline object."""
+    import oracle
+    oracle.build()
+    lib = oracle.load()
+    M = w.M
+
+    def run(rows):
+        if w.op == "layernorm_linear":
+            oracle.layernorm_linear(host["x"], host["gamma"], host["beta"], host["W"],
+                                    host["bias"], w.eps, rows, lib)
+        elif w.op == "rmsnorm_linear":
+            oracle.rmsnorm_linear(host["x"], host["gamma"], host["W"], host["bias"], w.eps,
+                                  rows, lib)
+        elif w.op == "linear_silu":
+            oracle.linear_silu(host["x"], host["W"], host["bias"], rows, lib)
+        else:
+            oracle.ffn(host["x"], host["W1"], host["W2"], rows, lib)
+
+    threads = oracle.num_threads(lib)
+    if w.M <= 32:
+        # decode: the whole batch (its cost is streaming W once in fp64)
+        t = time.perf_counter()
+        run(list(range(M)))
+        dt = time.perf_counter() - t
+        nbytes = (w.N * w.K + M * w.K + M * w.N) * 2
+        return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                "sample": f"all {M} rows of {w.name} (fp64), {dt:.1f} s"}
+    probe_rows = list(range(min(M, max(4, threads))))
+    t = time.perf_counter()
+    run(probe_rows)
+    per_row = (time.perf_counter() - t) / len(probe_rows)
+    n = int(max(len(probe_rows), min(M, target_s / max(per_row, 1e-9))))
+    n = max(threads, (n // threads) * threads) if n >= threads else n
+    n = min(n, M)
+    rows = list(range(n))
+    t = time.perf_counter()
+    run(rows)
+    dt = time.perf_counter() - t
+    flops_per_row = w.flops / w.M
+    value = flops_per_row * n / dt / 1e12
+    return {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} of {M} rows of {w.name} (fp64, all columns), {dt:.1f} s"}
+
+
+def reference_arm(args, rank):
+    """The fp64 CPU oracle timed as the reference arm, on rank 0 only."""
+    if rank != 0:
+        return None
+    import oracle
+    from normalization_gemm_row_gb300 import inputs
+    oracle.build()
+    lib = oracle.load()
+    w = inputs.BY_NAME[args.workload]
+    if args.m is not None:
+        w = w.with_m(args.m)
+    host = inputs.make(w)
+    threads = oracle.num_threads(lib)
+    rows_per_step = max(1, min(w.M, args.ref_rows or threads))
+
+    def step(i):
+        r0 = (i * rows_per_step) % w.M
+        rows = [(r0 + j) % w.M for j in range(rows_per_step)]
+        if w.op == "layernorm_linear":
+            oracle.layernorm_linear(host["x"], host["gamma"], host["beta"], host["W"],
+                                    host["bias"], w.eps, rows, lib)
+        elif w.op == "rmsnorm_linear":
+            oracle.rmsnorm_linear(host["x"], host["gamma"], host["W"], host["bias"], w.eps,
+                                  rows, lib)
+        elif w.op == "linear_silu":
+            oracle.linear_silu(host["x"], host["W"], host["bias"], rows, lib)
+        else:
+            oracle.ffn(host["x"], host["W1"], host["W2"], rows, lib)
+
+    for i in range(args.warmup):
+        step(i)
+    t = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    dt = time.perf_counter() - t
+    flops = w.flops / w.M * rows_per_step * args.steps
+    value = flops / dt / 1e12
+    unit = "TFLOP/s"
+    return {
+        "impl": "reference",
+        "metric": "fused LN/RMSNorm+GEMM TFLOP/s (% dense FP16 peak)", "value": value,
+        "unit": unit, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": w.name, "op": w.op, "M": w.M, "K": w.K, "N": w.N,
+                   "rows_per_step": rows_per_step},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": threads, "kind": "oracle",
+                         "sample": f"{rows_per_step} of {w.M} rows per step, fp64"},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--m", type=int, default=None, help="override M (decode workload: 1, 4 or 16)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-rows", type=int, default=0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank, world, local = dist_setup(args.gpus)
+
+    if args.impl == "reference":
+        out = reference_arm(args, rank)
+        if rank == 0:
+            print(json.dumps(out), flush=True)
+        return 0
+
+    out, w, host = our_arm(args, rank, world, local)
+    if rank == 0:
+        if args.no_cpu_baseline:
+            out["cpu_baseline"] = None
+        else:
+            out["cpu_baseline"] = cpu_baseline(w, host, args.cpu_seconds)
+        print(json.dumps(out), flush=True)
+    if dist.is_available() and dist.is_initialized():
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

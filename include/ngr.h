@@ -143,6 +143,23 @@ int ngr_workspace_error(void *workspace, ngr_stream_t stream);
 int ngr_debug_bounded_wait(void *workspace, uint32_t timeout_us,
                            ngr_stream_t stream);
 
+/* Profiling aid: time every kernel of this thread's next `n_calls` calls.
+ * Each such call records CUDA events (the library's own, created here; no
+ * device memory) on its stream just before and just after each kernel it
+ * launches, at most NGR_MAX_KERNELS_PER_CALL per call.  Recording between a
+ * call's kernels keeps them from overlapping, so time whole calls with this
+ * off.  Returns NGR_OK, NGR_ERR_ARG for n_calls <= 0, NGR_ERR_CUDA if
+ * events cannot be created. */
+#define NGR_MAX_KERNELS_PER_CALL 4
+int ngr_kernel_timing_start(int n_calls);
+
+/* End the timing started by ngr_kernel_timing_start: wait for its events and
+ * write the time in milliseconds of kernel k of timed call c to
+ * ms[c * NGR_MAX_KERNELS_PER_CALL + k] (-1 where the call launched fewer
+ * kernels), for as many calls as `capacity` floats hold.  Returns the number
+ * of calls timed (>= 0) or a negative ngr_status. */
+int ngr_kernel_timing_stop(float *ms, int capacity);
+
 /* Human-readable name of a status code (static storage). */
 const char *ngr_status_string(int status);
 

@@ -45,6 +45,8 @@ SIGNATURES = {
     "ngr_status_string": (ctypes.c_char_p, [_I]),
     "ngr_version": (_I, []),
     "ngr_last_error": (ctypes.c_char_p, []),
+    "ngr_kernel_timing_start": (_I, [_I]),
+    "ngr_kernel_timing_stop": (_I, [_P, _I]),
 }
 
 
@@ -133,6 +135,34 @@ def ngr_version() -> int:
 
 def ngr_last_error() -> str:
     return lib().ngr_last_error().decode()
+
+
+MAX_KERNELS_PER_CALL = 4
+
+
+def ngr_kernel_timing_start(n_calls) -> int:
+    return lib().ngr_kernel_timing_start(n_calls)
+
+
+def ngr_kernel_timing_stop(ms, capacity) -> int:
+    return lib().ngr_kernel_timing_stop(ms, capacity)
+
+
+def kernel_timing_start(n_calls: int):
+    """Time each kernel of this thread's next ``n_calls`` library calls."""
+    _raise(ngr_kernel_timing_start(n_calls), "ngr_kernel_timing_start")
+
+
+def kernel_timing_stop():
+    """Per-call lists of kernel times (ms) of the calls timed since
+    ``kernel_timing_start``."""
+    k = MAX_KERNELS_PER_CALL
+    cap = 65536 * k
+    buf = (ctypes.c_float * cap)()
+    n = ngr_kernel_timing_stop(buf, cap)
+    if n < 0:
+        raise NgrError(n, "ngr_kernel_timing_stop")
+    return [[buf[c * k + j] for j in range(k) if buf[c * k + j] >= 0] for c in range(n)]
 
 
 def status_string(status: int) -> str:

@@ -9,6 +9,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "ngr.h"
 #include "ngr_internal.h"
@@ -18,7 +19,36 @@ namespace ngr {
 
 namespace {
 thread_local char g_last_error[512] = "";
+
+// Per-thread kernel timing (see ngr_kernel_timing_start): the library's own
+// events, two per kernel slot, reused across timing sessions.
+constexpr int kSlots = NGR_MAX_KERNELS_PER_CALL;
+thread_local std::vector<cudaEvent_t> t_events;
+thread_local std::vector<int> t_count;  // kernels recorded per timed call
+thread_local bool t_armed = false;
+thread_local int t_calls = 0;           // calls to time in this session
+thread_local int t_call = 0;            // index of the current call
+thread_local int t_kernel = 0;          // index of the next kernel in the call
+
+void events_reset() { t_kernel = 0; }
+void events_call_done()
+{
+    if (t_armed && t_call < t_calls) ++t_call;
 }
+void event_before(cudaStream_t s)
+{
+    if (t_armed && t_call < t_calls && t_kernel < kSlots)
+        cudaEventRecord(t_events[2 * (t_call * kSlots + t_kernel)], s);
+}
+void event_after(cudaStream_t s)
+{
+    if (t_armed && t_call < t_calls && t_kernel < kSlots) {
+        cudaEventRecord(t_events[2 * (t_call * kSlots + t_kernel) + 1], s);
+        ++t_kernel;
+        t_count[t_call] = t_kernel;
+    }
+}
+}  // namespace
 
 int record_cuda_error(const char *what, int code, const char *detail)
 {
@@ -309,7 +339,9 @@ int norm_linear(int op, int norm, bool silu, const void *x, const void *gamma, c
     if (debug_mode() && cudaMemsetAsync(w, 0, 4, stream) != cudaSuccess) return NGR_ERR_CUDA;
     const bool decode = M <= kDecodeMaxM;
     const bool need_stats = norm != kNormNone || decode;
+    events_reset();
     if (need_stats) {
+        event_before(stream);
         rc = launch_rowstats(norm == kNormNone ? kNormRms : norm, bf16, x,
                              norm == kNormNone ? 0 : M, K, eps,
                              reinterpret_cast<float2 *>(w + L.stats), gamma, beta,
@@ -319,10 +351,14 @@ int norm_linear(int op, int norm, bool silu, const void *x, const void *gamma, c
                              decode ? reinterpret_cast<int *>(w + L.counters) : nullptr,
                              decode ? static_cast<int>(ceil_div(N, 128) * 4) : 0,
                              reinterpret_cast<int *>(w), di.sms, stream);
+        event_after(stream);
         if (rc != NGR_OK) return rc;
     }
+    event_before(stream);
     rc = launch_layer(norm, silu, bf16, x, W, bias, M, K, N, y, w, L, L.counters, need_stats, di,
                       stream);
+    event_after(stream);
+    events_call_done();
     return finish(rc, ws, stream);
 }
 
@@ -415,7 +451,9 @@ int ngr_ffn_linear_silu_linear(const void *x, const void *W1, const void *W2, in
     void *H = h ? h : static_cast<void *>(w + L.h);
     if (debug_mode() && cudaMemsetAsync(w, 0, 4, stream) != cudaSuccess) return NGR_ERR_CUDA;
     const bool decode = M <= kDecodeMaxM;
+    events_reset();
     if (decode) {
+        event_before(stream);
         // Zero both GEMMs' split-K counters (they are adjacent).
         const int n1 = static_cast<int>(ceil_div(F, 128) * 4);
         const int n2 = static_cast<int>(ceil_div(K, 128) * 4);
@@ -424,13 +462,19 @@ int ngr_ffn_linear_silu_linear(const void *x, const void *W1, const void *W2, in
         rc = launch_rowstats(kNormRms, bf16, x, 0, K, 0.f, nullptr, nullptr, nullptr, nullptr,
                              nullptr, reinterpret_cast<int *>(w + L.counters), n,
                              reinterpret_cast<int *>(w), di.sms, stream);
+        event_after(stream);
         if (rc != NGR_OK) return rc;
     }
+    event_before(stream);
     rc = launch_layer(kNormNone, true, bf16, x, W1, nullptr, M, K, F, H, w, L, L.counters, decode,
                       di, stream);
+    event_after(stream);
     if (rc != NGR_OK) return rc;
+    event_before(stream);
     rc = launch_layer(kNormNone, false, bf16, H, W2, nullptr, M, F, K, y, w, L, L.counters2, true,
                       di, stream);
+    event_after(stream);
+    events_call_done();
     return finish(rc, workspace, stream);
 }
 
@@ -477,6 +521,48 @@ int ngr_debug_bounded_wait(void *workspace, uint32_t timeout_us, ngr_stream_t st
     rc = launch_bounded_wait_probe(static_cast<int *>(workspace),
                                    static_cast<unsigned long long>(timeout_us) * 1000ull, stream);
     return rc == 0 ? NGR_OK : NGR_ERR_CUDA;
+}
+
+int ngr_kernel_timing_start(int n_calls)
+{
+    if (n_calls <= 0) return NGR_ERR_ARG;
+    const size_t need = static_cast<size_t>(n_calls) * kSlots * 2;
+    while (t_events.size() < need) {
+        cudaEvent_t e;
+        const cudaError_t err = cudaEventCreate(&e);
+        if (err != cudaSuccess) return record_cuda_error("cudaEventCreate", err, cudaGetErrorString(err));
+        t_events.push_back(e);
+    }
+    t_count.assign(static_cast<size_t>(n_calls), 0);
+    t_calls = n_calls;
+    t_call = 0;
+    t_kernel = 0;
+    t_armed = true;
+    return NGR_OK;
+}
+
+int ngr_kernel_timing_stop(float *ms, int capacity)
+{
+    if (!t_armed) return 0;
+    t_armed = false;
+    int written = 0;
+    for (int c = 0; c < t_call; ++c) {
+        if (ms && (c + 1) * kSlots > capacity) break;
+        for (int k = 0; k < kSlots; ++k) {
+            float v = -1.f;
+            if (k < t_count[c]) {
+                cudaEvent_t b = t_events[2 * (c * kSlots + k)];
+                cudaEvent_t e = t_events[2 * (c * kSlots + k) + 1];
+                cudaError_t err = cudaEventSynchronize(e);
+                if (err == cudaSuccess) err = cudaEventElapsedTime(&v, b, e);
+                if (err != cudaSuccess)
+                    return record_cuda_error("kernel timing", err, cudaGetErrorString(err));
+            }
+            if (ms) ms[c * kSlots + k] = v;
+        }
+        ++written;
+    }
+    return written;
 }
 
 const char *ngr_status_string(int status)

@@ -156,6 +156,23 @@ def test_garbage_workspace(M):
     assert_parity(y.double().cpu().numpy(), ref_op("layernorm_linear", d, 1e-5), f"garbage ws M={M}")
 
 
+def test_side_stream_and_kernel_timing():
+    """Calls on a non-default torch stream, with per-kernel timing on."""
+    d = inputs.case("layernorm_linear", 300, 1024, 520, torch.float16, True, seed=9)
+    g = to_dev(d)
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        B.kernel_timing_start(3)
+        for _ in range(2):
+            y = ngr.fused_layernorm_linear(g["x"], g["gamma"], g["beta"], g["W"], g["bias"], 1e-5)
+        times = B.kernel_timing_stop()
+    side.synchronize()
+    assert len(times) == 2 and all(len(t) == 2 for t in times)   # statistics + GEMM
+    assert all(0 < t < 100 for row in times for t in row)
+    assert B.kernel_timing_stop() == []                          # nothing armed any more
+    assert_parity(y.double().cpu().numpy(), ref_op("layernorm_linear", d, 1e-5), "side stream")
+
+
 def test_row_stats_against_oracle():
     for norm in (oracle.NORM_LAYER, oracle.NORM_RMS):
         for dt in (torch.float16, torch.bfloat16):
