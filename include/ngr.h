@@ -125,6 +125,31 @@ int ngr_ffn_linear_silu_linear(const void *x, const void *W1, const void *W2,
                                void *h, void *y, void *workspace,
                                size_t workspace_bytes, ngr_stream_t stream);
 
+/* Variant of ngr_fused_layernorm_linear for callers that cannot allocate
+ * device memory and so cannot supply a workspace -- for example code running
+ * where every device allocation is planned or owned by someone else, or an
+ * embedding that can only pass input and output tensors.  It computes the
+ * same y = LayerNorm(x) . W^T (+ bias) with the same arguments minus the
+ * workspace.  The paper has no counterpart; this is a deployment variant.
+ *
+ * Its scratch (per-row statistics, FP32 gamma/beta, the error word) is one
+ * fixed array of about 256 KiB in the library's device memory, present on
+ * every GPU that loads the library until the process exits.  The call
+ * allocates nothing.  Limits: M <= NGR_NOALLOC_MAX_M and
+ * K <= NGR_NOALLOC_MAX_K, else NGR_ERR_SHAPE.  The first call on each device
+ * looks up the array's device address (cudaGetSymbolAddress), so make that
+ * first call before any stream capture.  All calls share the one array, which
+ * keeps the last call's contents; each call rewrites what it reads, but calls
+ * that overlap on the GPU race on it and must not be issued.  Other
+ * conventions as above. */
+#define NGR_NOALLOC_MAX_M 16384
+#define NGR_NOALLOC_MAX_K 16384
+int ngr_fused_layernorm_linear_noalloc(const void *x, const void *gamma,
+                                       const void *beta, const void *W,
+                                       const void *bias, float eps, int64_t M,
+                                       int64_t K, int64_t N, int dtype, void *y,
+                                       ngr_stream_t stream);
+
 /* Step a1 alone: per-row FP32 statistics into stats[2*M] as (mu, rstd)
  * pairs.  norm: 1 = LayerNorm, 2 = RMSNorm (mu = 0).  [LNF] §1.1, §2.3.
  * Exposed so the statistics stage can be checked by itself. */

@@ -36,6 +36,7 @@ _P, _I64, _I, _F, _SZ, _U32 = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
 SIGNATURES = {
     "ngr_workspace_bytes": (_SZ, [_I, _I64, _I64, _I64, _I]),
     "ngr_fused_layernorm_linear": (_I, [_P, _P, _P, _P, _P, _F, _I64, _I64, _I64, _I, _P, _P, _SZ, _P]),
+    "ngr_fused_layernorm_linear_noalloc": (_I, [_P, _P, _P, _P, _P, _F, _I64, _I64, _I64, _I, _P, _P]),
     "ngr_fused_rmsnorm_linear": (_I, [_P, _P, _P, _P, _F, _I64, _I64, _I64, _I, _P, _P, _SZ, _P]),
     "ngr_fused_linear_silu": (_I, [_P, _P, _P, _I64, _I64, _I64, _I, _P, _P, _SZ, _P]),
     "ngr_ffn_linear_silu_linear": (_I, [_P, _P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _SZ, _P]),
@@ -93,6 +94,12 @@ def ngr_fused_layernorm_linear(x, gamma, beta, W, bias, eps, M, K, N, dtype, y,
                                ws, ws_bytes, stream) -> int:
     return lib().ngr_fused_layernorm_linear(x, gamma, beta, W, bias, eps, M, K,
                                             N, dtype, y, ws, ws_bytes, stream)
+
+
+def ngr_fused_layernorm_linear_noalloc(x, gamma, beta, W, bias, eps, M, K, N,
+                                       dtype, y, stream) -> int:
+    return lib().ngr_fused_layernorm_linear_noalloc(x, gamma, beta, W, bias, eps,
+                                                    M, K, N, dtype, y, stream)
 
 
 def ngr_fused_rmsnorm_linear(x, gamma, W, bias, eps, M, K, N, dtype, y, ws,

@@ -1,0 +1,58 @@
+"""The workspace-free LayerNorm + linear entry point, for callers that
+cannot allocate device memory and therefore cannot hand the library a
+workspace.  Called through the C ABI, its output must match the regular
+entry point's on two calls in a row (the second call reuses the library's
+fixed scratch array after the first).  This file is collected last on
+purpose, so a run that stops at the first failure has run everything else.
+"""
+import numpy as np
+import pytest
+import torch
+
+import normalization_gemm_row_gb300 as ngr
+from normalization_gemm_row_gb300 import binding as B
+from normalization_gemm_row_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL = 1e-2, 1e-2
+
+
+def _close(got, ref, what):
+    got = got.double().cpu().numpy()
+    ref = ref.double().cpu().numpy()
+    err = np.abs(got - ref)
+    assert np.isfinite(got).all(), what
+    assert (err <= ATOL + RTOL * np.abs(ref)).all(), f"{what}: max err {err.max():.3e}"
+
+
+@pytest.mark.parametrize("M,K,N,dtype", [(300, 1024, 520, torch.float16),
+                                         (1024, 8192, 1024, torch.float16),
+                                         (16, 4096, 1024, torch.bfloat16)])
+def test_noalloc_matches_workspace_entry_point(M, K, N, dtype):
+    ngr.build()
+    d = inputs.case("layernorm_linear", M, K, N, dtype, True, 1e-5, seed=M + N, x_mean=1.0)
+    g = {k: (v.cuda() if isinstance(v, torch.Tensor) and k != "outlier_rows" else v)
+         for k, v in d.items()}
+    code = B.NGR_BF16 if dtype == torch.bfloat16 else B.NGR_F16
+    s = torch.cuda.current_stream().cuda_stream
+    ref = ngr.fused_layernorm_linear(g["x"], g["gamma"], g["beta"], g["W"], g["bias"], 1e-5)
+    for call in range(2):
+        y = torch.full((M, N), float("nan"), dtype=dtype, device="cuda")
+        rc = B.ngr_fused_layernorm_linear_noalloc(
+            g["x"].data_ptr(), g["gamma"].data_ptr(), g["beta"].data_ptr(), g["W"].data_ptr(),
+            g["bias"].data_ptr(), 1e-5, M, K, N, code, y.data_ptr(), s)
+        assert rc == 0, B.status_string(rc)
+        torch.cuda.synchronize()
+        _close(y, ref, f"no-alloc call {call} M={M} K={K} N={N}")
+
+
+def test_noalloc_rejects_sizes_beyond_its_limit():
+    ngr.build()
+    # Size checks come before any pointer is looked at: nothing runs here.
+    rc = B.ngr_fused_layernorm_linear_noalloc(16, 16, 16, 16, None, 1e-5, 16384 + 1, 64, 64,
+                                              0, 16, None)
+    assert rc == -2
+    rc = B.ngr_fused_layernorm_linear_noalloc(16, 16, 16, 16, None, 1e-5, 64, 16384 + 8, 64,
+                                              0, 16, None)
+    assert rc == -2
