@@ -27,6 +27,8 @@
  *    out) are recorded in the workspace's error word: read them with
  *    ngr_workspace_error.  With the environment variable NGR_DEBUG=1 every
  *    call synchronizes its stream and returns that word's status itself.
+ *    With NGR_TRACE=1 every call prints the kernel variant it chose (tile
+ *    width, stages, grid) to stderr.
  *  - The kernels need an sm_103 device (GB300); any other device gives
  *    NGR_ERR_ARCH.  There is no fallback path.
  *  - Calls are thread-safe.  Two calls that share one workspace must be

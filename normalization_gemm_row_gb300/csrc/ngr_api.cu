@@ -150,6 +150,15 @@ bool debug_mode()
     return on;
 }
 
+bool trace_mode()
+{
+    static const bool on = [] {
+        const char *v = std::getenv("NGR_TRACE");
+        return v && v[0] && std::strcmp(v, "0") != 0;
+    }();
+    return on;
+}
+
 unsigned long long wait_timeout_ns()
 {
     static const unsigned long long ns = [] {
@@ -289,14 +298,22 @@ int launch_layer(int norm, bool silu, bool bf16, const void *x, const void *W,
         d.k_blocks = static_cast<int>(ceil_div(K, kBK));
         d.units = static_cast<long long>(d.n_tiles) * d.k_blocks;
         d.grid = plan_decode_grid(d.n_tiles, d.k_blocks, di.sms);
+        if (trace_mode())
+            std::fprintf(stderr, "ngr: decode kernel M=%lld N=%lld K=%lld MN=%d grid=%d units=%lld\n",
+                         static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(K),
+                         mn, d.grid, d.units);
         d.timeout_ns = wait_timeout_ns();
         return launch_decode(norm, silu, bf16, mn, d, pdl, stream);
     }
     GemmArgs a;
     std::memset(&a, 0, sizeof(a));
-    const GemmPlan plan = plan_gemm(M, N, K, di.sms);
+    const GemmPlan plan = plan_gemm(M, N, K, di.sms, norm != kNormNone);
+    if (trace_mode())
+        std::fprintf(stderr, "ngr: tile kernel M=%lld N=%lld K=%lld norm=%d %s BN=%d stages=%d grid=%d smem=%zu\n",
+                     static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(K), norm,
+                     plan.pair ? "cta-pair" : "single-cta", plan.bn, plan.stages, plan.grid, plan.smem);
     if (!map_2d(&a.map_a, x, bf16, M, K, kBM) ||
-        !map_2d(&a.map_b, W, bf16, N, K, static_cast<uint32_t>(plan.bn)))
+        !map_2d(&a.map_b, W, bf16, N, K, static_cast<uint32_t>(plan.b_rows)))
         return NGR_ERR_CUDA;
     if (has_norm && !map_gb(&a.map_gb, gf, K, L.beta_f - L.gamma_f)) return NGR_ERR_CUDA;
     a.stats = stats;
@@ -307,7 +324,7 @@ int launch_layer(int norm, bool silu, bool bf16, const void *x, const void *W,
     a.M = static_cast<int>(M);
     a.N = static_cast<int>(N);
     a.K = static_cast<int>(K);
-    a.m_tiles = static_cast<int>(ceil_div(M, kBM));
+    a.m_tiles = static_cast<int>(ceil_div(M, plan.bm));
     a.n_tiles = static_cast<int>(ceil_div(N, plan.bn));
     a.k_blocks = static_cast<int>(ceil_div(K, kBK));
     a.num_tiles = a.m_tiles * a.n_tiles;

@@ -1,0 +1,17 @@
+// ngr_gemm2_bn256.cu -- CTA-pair tile kernel instantiations for a 256-column
+// N tile (6 pipeline stages).  One translation unit per tile width so they
+// compile in parallel.
+#include "ngr_gemm2_kernel.cuh"
+
+namespace ngr {
+
+int launch_gemm2_bn256(int norm, bool silu, bool bf16, const GemmArgs &args, int grid,
+                      bool pdl, cudaStream_t stream)
+{
+    return launch_gemm2_bn<256, 6>(norm, silu, bf16, args, grid, pdl, stream);
+}
+
+size_t gemm2_smem_bn256() { return Gemm2Smem<256, 6>::alloc; }
+int gemm2_max_clusters_bn256() { return gemm2_max_clusters<256, 6>(); }
+
+}  // namespace ngr

@@ -1,0 +1,475 @@
+// ngr_gemm2_kernel.cuh -- the fused pre-norm linear layer on a CTA pair
+// (tcgen05 cta_group::2): same computation as gemm_kernel, on 256 x BN
+// output tiles.
+//
+// The two CTAs of a cluster share each tile: CTA r loads rows
+// [m0 + 128 r, +128) of x and rows [n0 + r BN/2, +BN/2) of W into its own
+// shared memory (no multicast), normalizes its own x rows in place, and the
+// even CTA issues one tcgen05.mma.cta_group::2 per K step that reads A from
+// both CTAs by rows and B from both CTAs by columns, accumulating its 128
+// rows of D in each CTA's tensor memory.  Per CTA this halves the W bytes
+// loaded and read from shared memory per FLOP compared with a single-CTA
+// 128 x BN tile, which is what keeps enough bytes in flight to feed the
+// tensor core.
+//
+// Synchronization (barriers are per CTA unless marked "leader"):
+//   full[s]        TMA landed in this CTA (its producer's expect_tx);
+//   ready[s]       leader: each transform warp of both CTAs (or one relay
+//                  thread per CTA without a norm) arrives once its CTA's
+//                  stage is ready for the tensor core;
+//   empty[s]       the leader's tcgen05.commit, multicast to both CTAs;
+//   acc_full[a]    the leader's commit at the end of a tile, multicast;
+//   acc_empty[a]   leader: each epilogue warp of both CTAs arrives after
+//                  draining its rows of accumulator a.
+#pragma once
+
+#include "ngr_gemm_kernel.cuh"
+
+namespace ngr {
+
+// Tensor-memory columns of one slot of the normalized A operand (K = 64 as
+// 32 packed pairs).  With a norm the kernel keeps one accumulator and gives
+// the rest of the 512 columns to up to 8 A slots, so that the transform can
+// run several k blocks ahead of the MMA; the epilogue (about 3 % of a tile)
+// then does not overlap the next tile's main loop.
+constexpr int kASlotCols = kBK / 2;
+constexpr int kMaxASlots = 8;
+
+// Where the normalized A operand lives in the CTA-pair kernel: 1 = tensor
+// memory (written with tcgen05.st by row-owning threads), 0 = shared memory
+// (normalized in place, like the single-CTA kernel).
+#ifndef NGR_PAIR_A_TMEM
+#define NGR_PAIR_A_TMEM 0
+#endif
+
+template <int BN, int STAGES>
+struct Gemm2Smem {
+    static constexpr int kA = kBM * kBK * 2;          // 16 KB: this CTA's 128 x rows
+    static constexpr int kB = (BN / 2) * kBK * 2;     // this CTA's BN/2 W rows
+    static constexpr int kGB = 2 * kBK * 4;           // FP32 gamma[64], beta[64]
+    static constexpr int off_a = 0;
+    static constexpr int off_b = off_a + STAGES * kA;
+    static constexpr int off_g = off_b + STAGES * kB;
+    static constexpr int off_bar = off_g + STAGES * kGB;
+    static constexpr int n_bars = 3 * STAGES + 5 + kMaxASlots;
+    static constexpr int off_tmem = off_bar + n_bars * 8;
+    static constexpr int bytes = off_tmem + 16;
+    static constexpr int alloc = bytes + 1024;
+};
+
+
+// The transform role of the CTA-pair kernel with A in tensor memory.
+// Transform thread t belongs to group g = t / kGroupThreads, which handles
+// the k blocks with running index it % groups == g; k block `it` uses A slot
+// it % SLOTS, free once the MMAs of k block it - SLOTS have completed.  Each warp of a group covers the
+// tensor-memory lane quarter warp % 4, and each lane one row: it reads its
+// row's 64 raw x values from the swizzled shared-memory stage, normalizes
+// them in FP32, packs them to 16-bit pairs and stores the 32 columns with
+// tcgen05.st.  The shared-memory stage is only read.
+template <int NORM, bool BF16, int STAGES, int KA, int SLOTS, typename M0Fn, typename ArriveFn>
+__device__ __forceinline__ void transform_role_tmem(
+    int t, int tile0, int tile_step, int num_tiles, int k_blocks, int M, const float2 *stats,
+    const uint8_t *sA, const float *sG, uint64_t *full, uint64_t *a_free, uint32_t tmem_base,
+    uint32_t a_col0, const WaitCtx &wc, M0Fn m0_of, ArriveFn arrive)
+{
+    const int g = t / kGroupThreads;
+    const int lane = threadIdx.x & 31;
+    const int q = (threadIdx.x >> 5) & 3;   // lane quarter this warp may access
+    const int r = q * 32 + lane;            // row of the 128-row tile
+    const int sw = r & 7;
+    const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + a_col0;
+    pdl_wait();
+    int stage = 0;
+    uint32_t phase = 0;
+    int it = 0;
+    for (int tile = tile0; tile < num_tiles; tile += tile_step) {
+        const int row = m0_of(tile) + r;
+        float2 st = make_float2(0.f, 0.f);
+        if (row < M) st = stats[row];
+        const float2 so = make_float2(st.y, -st.x * st.y);
+        for (int kb = 0; kb < k_blocks; ++kb, ++it) {
+            if (it % kTransformGroups == g) {
+                if (!mbar_wait_warp(&full[stage], phase, wc)) return;
+                const int slot = it % SLOTS;
+                const int use = it / SLOTS;
+                if (use > 0 && !mbar_wait_warp(&a_free[slot], (use - 1) & 1, wc)) return;
+                tc_fence_after();
+                const uint8_t *xrow = sA + stage * KA + r * 128;
+                const float *gs = sG + stage * 2 * kBK;
+                uint32_t packed[32];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(xrow + ((c ^ sw) << 4));
+                    const float4 g0 = *reinterpret_cast<const float4 *>(gs + 8 * c);
+                    const float4 g1 = *reinterpret_cast<const float4 *>(gs + 8 * c + 4);
+                    const float2 gg[4] = {make_float2(g0.x, g0.y), make_float2(g0.z, g0.w),
+                                          make_float2(g1.x, g1.y), make_float2(g1.z, g1.w)};
+                    float2 bb[4];
+                    if constexpr (NORM == kNormLayer) {
+                        const float4 b0 = *reinterpret_cast<const float4 *>(gs + kBK + 8 * c);
+                        const float4 b1 = *reinterpret_cast<const float4 *>(gs + kBK + 8 * c + 4);
+                        bb[0] = make_float2(b0.x, b0.y);
+                        bb[1] = make_float2(b0.z, b0.w);
+                        bb[2] = make_float2(b1.x, b1.y);
+                        bb[3] = make_float2(b1.z, b1.w);
+                    }
+                    const uint4 o = transform8_pk<NORM, BF16>(v, so, gg, bb);
+                    packed[4 * c + 0] = o.x;
+                    packed[4 * c + 1] = o.y;
+                    packed[4 * c + 2] = o.z;
+                    packed[4 * c + 3] = o.w;
+                }
+                tmem_st32(tbase + static_cast<uint32_t>(slot * kASlotCols), packed);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) arrive(stage);
+            }
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+    }
+}
+
+template <int NORM, bool SILU, bool BF16, int BN, int STAGES>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm2_kernel(const __grid_constant__ GemmArgs args)
+{
+    using L = Gemm2Smem<BN, STAGES>;
+    constexpr bool kNorm = NORM != kNormNone;
+    constexpr uint32_t kTx = L::kA + L::kB + (kNorm ? L::kGB : 0);
+    // Accumulators (two of BN columns, or one with a norm), then the A slots.
+    constexpr bool kATmem = kNorm && NGR_PAIR_A_TMEM;
+    constexpr int kAccBufs = kATmem ? 1 : 2;
+    constexpr uint32_t kACol0 = kAccBufs * BN;
+    constexpr uint32_t kTmemCols = 512;
+    constexpr int kSlotsFit = static_cast<int>((kTmemCols - kACol0) / kASlotCols);
+    constexpr int kASlots = kSlotsFit < kMaxASlots ? kSlotsFit : kMaxASlots;
+    static_assert(!kATmem || (kASlots >= 2 && kASlots % kTransformGroups == 0),
+                  "tensor memory: accumulator + A slots");
+    constexpr uint32_t kIdesc = idesc_f16(BF16, 2 * kBM, BN);
+    // ready[s] arrivals: one per warp of the transform group that owns the
+    // stage, in each CTA, or one relay thread per CTA without a norm.
+    constexpr uint32_t kReadyCount = kNorm ? 2 * kGroupWarps : 2;
+    static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "UMMA N for M = 256");
+    static_assert((BN / 2) % 8 == 0, "B half tile rows");
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *sA = smem + L::off_a;
+    uint8_t *sB = smem + L::off_b;
+    float *sG = reinterpret_cast<float *>(smem + L::off_g);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::off_bar);
+    uint64_t *full = bars;
+    uint64_t *empty = bars + STAGES;
+    uint64_t *ready = bars + 2 * STAGES;
+    uint64_t *acc_full = bars + 3 * STAGES;
+    uint64_t *acc_empty = bars + 3 * STAGES + 2;
+    uint64_t *drain = bars + 3 * STAGES + 4;
+    uint64_t *a_free = bars + 3 * STAGES + 5;   // [kMaxASlots] A slot read by the MMAs (commit, multicast)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::off_tmem);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    __shared__ int abort_flag;
+    const WaitCtx wc{&abort_flag, args.err, args.timeout_ns};
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        if (args.zero_err && blockIdx.x == 0) *args.err = 0;
+        prefetch_tmap(&args.map_a);
+        prefetch_tmap(&args.map_b);
+        if constexpr (kNorm) prefetch_tmap(&args.map_gb);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+            mbar_init(&ready[s], kReadyCount);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&acc_full[a], 1);
+            mbar_init(&acc_empty[a], 2 * 4);
+        }
+        mbar_init(drain, 1);
+        for (int j = 0; j < kMaxASlots; ++j) mbar_init(&a_free[j], 1);
+        fence_mbarrier_init();
+    }
+    if (warp == 2) {
+        tmem_alloc_pair(tmem_slot, kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    // Both CTAs' barriers are initialized before any remote arrive.
+    cluster_sync_all();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    pdl_launch_dependents();
+
+    const int m_tiles = args.m_tiles;   // 256-row pair tiles
+    const int k_blocks = args.k_blocks;
+    const int num_tiles = args.num_tiles;
+    const int cluster = blockIdx.x >> 1;
+    const int n_clusters = gridDim.x >> 1;
+    // Leader-side addresses of ready[] and acc_empty[] (shared::cluster).
+    const uint32_t ready_leader = mapa_shared(smem_u32(ready), 0);
+    const uint32_t acc_empty_leader = mapa_shared(smem_u32(acc_empty), 0);
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            pdl_wait();
+            const uint64_t pol_x = policy_evict_last();
+            const uint64_t pol_w = policy_evict_first();
+            int stage = 0;
+            uint32_t phase = 0;
+            long long fills = 0;
+            bool ok = true;
+            for (int tile = cluster; ok && tile < num_tiles; tile += n_clusters) {
+                const int m0 = (tile % m_tiles) * 2 * kBM + static_cast<int>(rank) * kBM;
+                const int n0 = (tile / m_tiles) * BN + static_cast<int>(rank) * (BN / 2);
+                for (int kb = 0; kb < k_blocks; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, wc)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&full[stage], kTx);
+                    const int kc = kb * kBK;
+                    tma_load_2d(sA + stage * L::kA, &args.map_a, &full[stage], kc, m0, pol_x);
+                    tma_load_2d(sB + stage * L::kB, &args.map_b, &full[stage], kc, n0, pol_w);
+                    if constexpr (kNorm)
+                        tma_load_2d(sG + stage * 2 * kBK, &args.map_gb, &full[stage], kc, 0, pol_x);
+                    ++fills;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            const int outstanding = fills < STAGES ? static_cast<int>(fills) : STAGES;
+            for (int j = 1; j <= outstanding; ++j) {
+                int s = stage - j;
+                uint32_t p = phase;
+                if (s < 0) { s += STAGES; p ^= 1u; }
+                mbar_wait(&full[s], p, wc);
+            }
+        }
+    } else if (warp == 1) {
+        if (leader && lane == 0) {
+            // ------------------------------------- MMA issuer (even CTA)
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            int it = 0;
+            bool ok = true;
+            for (int tile = cluster; ok && tile < num_tiles; tile += n_clusters) {
+                if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, wc)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kb = 0; kb < k_blocks; ++kb) {
+                    if (!mbar_wait(&ready[stage], phase, wc)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t b_addr = smem_u32(sB + stage * L::kB);
+                    if constexpr (kATmem) {
+                        const int slot = it % kASlots;
+                        const uint32_t a_tmem = tmem_base + kACol0 +
+                                                static_cast<uint32_t>(slot * kASlotCols);
+#pragma unroll
+                        for (int k = 0; k < kBK / kUmmaK; ++k) {
+                            umma_f16_ts_pair(d_tmem, a_tmem + static_cast<uint32_t>(k * (kUmmaK / 2)),
+                                             sdesc_kmajor_sw128(b_addr + k * 32), kIdesc,
+                                             (kb | k) != 0 ? 1u : 0u);
+                        }
+                        umma_commit_pair(&a_free[slot], 0x3);
+                    } else {
+                        const uint32_t a_addr = smem_u32(sA + stage * L::kA);
+#pragma unroll
+                        for (int k = 0; k < kBK / kUmmaK; ++k) {
+                            umma_f16_ss_pair(d_tmem, sdesc_kmajor_sw128(a_addr + k * 32),
+                                             sdesc_kmajor_sw128(b_addr + k * 32), kIdesc,
+                                             (kb | k) != 0 ? 1u : 0u);
+                        }
+                    }
+                    umma_commit_pair(&empty[stage], 0x3);
+                    ++it;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                umma_commit_pair(&acc_full[acc], 0x3);
+                if (++acc == kAccBufs) { acc = 0; acc_phase ^= 1u; }
+            }
+            umma_commit_pair(drain, 0x1);
+            mbar_wait(drain, 0, wc);
+        }
+    } else if (warp >= kTransformWarp0 && warp < kEpilogueWarp0) {
+        const int t = threadIdx.x - kTransformWarp0 * 32;
+        if constexpr (kATmem) {
+            // ------------------------------------------ transform (A -> TMEM)
+            transform_role_tmem<NORM, BF16, STAGES, L::kA, kASlots>(
+                t, cluster, n_clusters, num_tiles, k_blocks, args.M, args.stats, sA, sG, full,
+                a_free, tmem_base, kACol0, wc,
+                [&](int tile) { return (tile % m_tiles) * 2 * kBM + static_cast<int>(rank) * kBM; },
+                [&](int st) { mbar_arrive_cluster(ready_leader + 8u * static_cast<uint32_t>(st)); });
+        } else if constexpr (kNorm) {
+            // ----------------------------------------- transform (A in place)
+            transform_role<NORM, BF16, STAGES, L::kA>(
+                t, cluster, n_clusters, num_tiles, k_blocks, args.M, args.stats, sA, sG, full, wc,
+                [&](int tile) { return (tile % m_tiles) * 2 * kBM + static_cast<int>(rank) * kBM; },
+                [&](int st) { mbar_arrive_cluster(ready_leader + 8u * static_cast<uint32_t>(st)); });
+        } else if (t == 0) {
+            // ------------------------------------------------------- relay
+            // Without a norm the stage needs no work: one thread tells the
+            // leader that this CTA's copies have landed.
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int tile = cluster; ok && tile < num_tiles; tile += n_clusters) {
+                for (int kb = 0; kb < k_blocks; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, wc)) { ok = false; break; }
+                    mbar_arrive_cluster(ready_leader + 8u * static_cast<uint32_t>(stage));
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+        }
+    } else if (warp >= kEpilogueWarp0) {
+        // --------------------------------------------------------- epilogue
+        const int q = warp & 3;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        const int M = args.M, N = args.N;
+        for (int tile = cluster; tile < num_tiles; tile += n_clusters) {
+            if (!mbar_wait_warp(&acc_full[acc], acc_phase, wc)) break;
+            tc_fence_after();
+            const int row = (tile % m_tiles) * 2 * kBM + static_cast<int>(rank) * kBM + q * 32 + lane;
+            const int nt0 = (tile / m_tiles) * BN;
+            const uint32_t t_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                    static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 32) {
+                const int n0 = nt0 + c;
+                if (n0 >= N) break;  // uniform across the warp
+                uint32_t r[32];
+                tmem_ld32(t_base + static_cast<uint32_t>(c), r);
+                tmem_ld_wait();
+                float v[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                if (args.bias != nullptr) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        if (n0 + 8 * j < N) {
+                            const uint4 bv = __ldg(reinterpret_cast<const uint4 *>(
+                                static_cast<const uint16_t *>(args.bias) + n0 + 8 * j));
+                            const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const float2 f = to_float2<BF16>(bw[i]);
+                                v[8 * j + 2 * i] += f.x;
+                                v[8 * j + 2 * i + 1] += f.y;
+                            }
+                        }
+                    }
+                }
+                if constexpr (SILU) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = silu_f(v[j]);
+                }
+                if (row < M) {
+                    uint16_t *yrow = static_cast<uint16_t *>(args.y) + static_cast<int64_t>(row) * N;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        if (n0 + 8 * j < N) {
+                            uint4 o;
+                            o.x = from_float2<BF16>(v[8 * j + 0], v[8 * j + 1]);
+                            o.y = from_float2<BF16>(v[8 * j + 2], v[8 * j + 3]);
+                            o.z = from_float2<BF16>(v[8 * j + 4], v[8 * j + 5]);
+                            o.w = from_float2<BF16>(v[8 * j + 6], v[8 * j + 7]);
+                            *reinterpret_cast<uint4 *>(yrow + n0 + 8 * j) = o;
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(acc_empty_leader + 8u * static_cast<uint32_t>(acc));
+            if (++acc == kAccBufs) { acc = 0; acc_phase ^= 1u; }
+        }
+    }
+
+    // Neither CTA frees its tensor memory or leaves while the pair may
+    // still touch it (the leader's MMAs write both CTAs' tensor memory; the
+    // peer arrives on the leader's barriers).
+    tc_fence_before();
+    cluster_sync_all();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, kTmemCols);
+    }
+}
+
+template <int NORM, bool SILU, bool BF16, int BN, int STAGES>
+int launch_gemm2_variant(const GemmArgs &args, int grid, bool pdl, cudaStream_t stream)
+{
+    auto kern = gemm2_kernel<NORM, SILU, BF16, BN, STAGES>;
+    constexpr int smem = Gemm2Smem<BN, STAGES>::alloc;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess)
+        return record_cuda_error("cudaFuncSetAttribute(max dynamic smem)", e, cudaGetErrorString(e));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 2 : 1;
+    e = cudaLaunchKernelEx(&cfg, kern, args);
+    return e == cudaSuccess ? 0 : record_cuda_error("cudaLaunchKernelEx (CTA pair)", e, cudaGetErrorString(e));
+}
+
+// How many CTA pairs of this kernel can be resident at once on the current
+// device (pairs must share a GPC, so this can be below SMs / 2).
+template <int BN, int STAGES>
+int gemm2_max_clusters()
+{
+    auto kern = gemm2_kernel<kNormNone, false, false, BN, STAGES>;
+    constexpr int smem = Gemm2Smem<BN, STAGES>::alloc;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) return 0;
+    return n;
+}
+
+template <int BN, int STAGES>
+int launch_gemm2_bn(int norm, bool silu, bool bf16, const GemmArgs &args, int grid, bool pdl,
+                    cudaStream_t stream)
+{
+#define NGR_CASE2(N_, S_, B_)                                                     \
+    if (norm == N_ && silu == S_ && bf16 == B_)                                   \
+        return launch_gemm2_variant<N_, S_, B_, BN, STAGES>(args, grid, pdl, stream);
+    NGR_CASE2(kNormLayer, false, false)
+    NGR_CASE2(kNormLayer, false, true)
+    NGR_CASE2(kNormRms, false, false)
+    NGR_CASE2(kNormRms, false, true)
+    NGR_CASE2(kNormNone, true, false)
+    NGR_CASE2(kNormNone, true, true)
+    NGR_CASE2(kNormNone, false, false)
+    NGR_CASE2(kNormNone, false, true)
+#undef NGR_CASE2
+    return -9;
+}
+
+}  // namespace ngr

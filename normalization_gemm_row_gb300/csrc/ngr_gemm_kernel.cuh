@@ -23,11 +23,12 @@
 //   warp 2      allocates and frees tensor memory (2 x BN columns: the
 //               epilogue drains one accumulator while the next tile's
 //               mainloop fills the other);
-//   warps 4-7   transform: normalize + affine the x tile IN PLACE in shared
-//               memory (thread t owns row t; FP32 math, one rounding to the
-//               16-bit operand type), then fence the generic-proxy writes for
-//               the tensor core and signal the MMA warp;
-//   warps 8-11  epilogue: tcgen05.ld of its 32 accumulator rows, + bias,
+//   warps 4-11  transform: normalize + affine the x tile IN PLACE in shared
+//               memory (each thread one 16-byte chunk column of 4 rows;
+//               packed FP32x2 math, one rounding to the 16-bit operand
+//               type), then fence the generic-proxy writes for the tensor
+//               core and signal the MMA warp;
+//   warps 12-15 epilogue: tcgen05.ld of its 32 accumulator rows, + bias,
 //               SiLU, round to fp16/bf16, 16-byte stores to y.
 // The normalized activations exist only in shared memory.
 #pragma once
@@ -108,6 +109,120 @@ __device__ __forceinline__ uint4 transform8(uint4 v, float sc, float of,
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// Two consecutive 16-bit values as FP32 (exact).
+template <bool BF16>
+__device__ __forceinline__ float2 unpack2(uint32_t w)
+{
+    if constexpr (BF16)
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    else
+        return __half22float2(*reinterpret_cast<const __half2 *>(&w));
+}
+
+// Normalize + affine 8 elements with packed FP32x2 arithmetic:
+// LayerNorm a = (x * rstd + (-mu * rstd)) * gamma + beta, RMSNorm
+// a = (x * rstd) * gamma; one rounding to the 16-bit type at the end.
+// so = (rstd, -mu * rstd) of the row; g[4], b[4] = gamma/beta pairs of the
+// 8 columns.
+template <int NORM, bool BF16>
+__device__ __forceinline__ uint4 transform8_pk(uint4 v, float2 so, const float2 (&g)[4],
+                                               const float2 (&b)[4])
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+    const float2 sc = make_float2(so.x, so.x);
+    const float2 of = make_float2(so.y, so.y);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = unpack2<BF16>(w[i]);
+        float2 a;
+        if constexpr (NORM == kNormLayer)
+            a = __ffma2_rn(__ffma2_rn(f, sc, of), g[i], b[i]);
+        else
+            a = __fmul2_rn(__fmul2_rn(f, sc), g[i]);
+        o[i] = from_float2<BF16>(a.x, a.y);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// The transform role, shared by the tile kernels.  Transform thread t
+// (0 <= t < kTransformThreads) belongs to group t / kGroupThreads; group g
+// normalizes the stages of the k blocks with running index % groups == g.
+// Within a group, thread u owns 16-byte chunk u % 8 (8 columns) of rows
+// u / 8 + (kGroupThreads / 8) i: a quarter-warp covers one 128-byte row
+// (conflict free under the swizzle) and gamma/beta of the chunk are read
+// once per stage.  After its stores each thread fences them for the async
+// proxy, and one lane per warp calls arrive(stage).
+// m0_of(tile) gives the tile's first x row in this CTA.
+template <int NORM, bool BF16, int STAGES, int KA, typename M0Fn, typename ArriveFn>
+__device__ __forceinline__ void transform_role(int t, int tile0, int tile_step, int num_tiles,
+                                               int k_blocks, int M, const float2 *stats,
+                                               uint8_t *sA, const float *sG, uint64_t *full,
+                                               const WaitCtx &wc, M0Fn m0_of, ArriveFn arrive)
+{
+    constexpr int kRows = kBM * 8 / kGroupThreads;   // rows per thread
+    constexpr int kRowStep = kGroupThreads / 8;
+    const int g = t / kGroupThreads;
+    const int u = t % kGroupThreads;
+    const int c = u & 7;
+    const int r0 = u >> 3;
+    const int pc = (c ^ (r0 & 7)) << 4;  // swizzled chunk offset (row % 8 == r0 % 8)
+    const int lane = threadIdx.x & 31;
+    pdl_wait();                          // statistics come from the previous grid
+    int stage = 0;
+    uint32_t phase = 0;
+    int it = 0;                          // running k-block index over this CTA's tiles
+    for (int tile = tile0; tile < num_tiles; tile += tile_step) {
+        const int m0 = m0_of(tile);
+        float2 so[kRows];
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) {
+            const int row = m0 + r0 + kRowStep * i;
+            float2 st = make_float2(0.f, 0.f);
+            if (row < M) st = stats[row];
+            so[i] = make_float2(st.y, -st.x * st.y);
+        }
+        for (int kb = 0; kb < k_blocks; ++kb, ++it) {
+            if (it % kTransformGroups == g) {
+                if (!mbar_wait_warp(&full[stage], phase, wc)) return;
+                // gamma/beta of columns 8c..8c+7; the two halves are read
+                // in separate instructions so that a quarter-warp touches
+                // 8 distinct 16-byte slots of one 128-byte line each time.
+                const float *gp = sG + stage * 2 * kBK + 8 * c;
+                float4 q[4];
+                q[0] = *reinterpret_cast<const float4 *>(gp);
+                q[1] = *reinterpret_cast<const float4 *>(gp + 4);
+                if constexpr (NORM == kNormLayer) {
+                    q[2] = *reinterpret_cast<const float4 *>(gp + kBK);
+                    q[3] = *reinterpret_cast<const float4 *>(gp + kBK + 4);
+                }
+                const float2 gg[4] = {make_float2(q[0].x, q[0].y), make_float2(q[0].z, q[0].w),
+                                      make_float2(q[1].x, q[1].y), make_float2(q[1].z, q[1].w)};
+                float2 bb[4];
+                if constexpr (NORM == kNormLayer) {
+                    bb[0] = make_float2(q[2].x, q[2].y);
+                    bb[1] = make_float2(q[2].z, q[2].w);
+                    bb[2] = make_float2(q[3].x, q[3].y);
+                    bb[3] = make_float2(q[3].z, q[3].w);
+                }
+                uint8_t *base = sA + stage * KA + r0 * 128 + pc;
+                uint4 v[kRows];
+#pragma unroll
+                for (int i = 0; i < kRows; ++i)
+                    v[i] = *reinterpret_cast<const uint4 *>(base + i * kRowStep * 128);
+#pragma unroll
+                for (int i = 0; i < kRows; ++i)
+                    *reinterpret_cast<uint4 *>(base + i * kRowStep * 128) =
+                        transform8_pk<NORM, BF16>(v[i], so[i], gg, bb);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) arrive(stage);
+            }
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+    }
+}
+
 template <int BN>
 struct TmemCols {
     static constexpr uint32_t need = 2 * BN;
@@ -171,7 +286,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
-            mbar_init(&ready[s], 128);
+            mbar_init(&ready[s], kGroupWarps);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&acc_full[a], 1);
@@ -270,42 +385,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             umma_commit(drain);
             mbar_wait(drain, 0, wc);
         }
-    } else if (warp >= 4 && warp < 8) {
+    } else if (warp >= kTransformWarp0 && warp < kEpilogueWarp0) {
         if constexpr (kNorm) {
             // ---------------------------------------------------- transform
-            const int t = threadIdx.x - 128;  // row of the tile this thread owns
-            pdl_wait();                       // statistics come from the previous grid
-            int stage = 0;
-            uint32_t phase = 0;
-            bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                const int row = (tile % m_tiles) * kBM + t;
-                float2 st = make_float2(0.f, 0.f);
-                if (row < args.M) st = args.stats[row];
-                const float sc = st.y;
-                const float of = -st.x * st.y;
-                for (int kb = 0; kb < k_blocks; ++kb) {
-                    if (!mbar_wait_warp(&full[stage], phase, wc)) { ok = false; break; }
-                    const float *g = sG + stage * 2 * kBK;
-                    const float *b = g + kBK;
-                    uint8_t *arow = sA + stage * L::kA + t * 128;
-                    const int sw = t & 7;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        // Logical 16-byte chunk c of this row sits at chunk
-                        // c ^ (row % 8) under the 128-byte swizzle; visiting
-                        // chunks in logical order keeps the 8 rows of a
-                        // quarter-warp on 8 distinct bank groups.
-                        uint4 *p = reinterpret_cast<uint4 *>(arow + ((c ^ sw) << 4));
-                        *p = transform8<NORM, BF16>(*p, sc, of, g + 8 * c, b + 8 * c);
-                    }
-                    fence_proxy_async_smem();
-                    mbar_arrive(&ready[stage]);
-                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-                }
-            }
+            transform_role<NORM, BF16, STAGES, L::kA>(
+                threadIdx.x - kTransformWarp0 * 32, blockIdx.x, gridDim.x, num_tiles, k_blocks,
+                args.M, args.stats, sA, sG, full, wc,
+                [&](int tile) { return (tile % m_tiles) * kBM; },
+                [&](int st) { mbar_arrive(&ready[st]); });
         }
-    } else if (warp >= 8) {
+    } else if (warp >= kEpilogueWarp0) {
         // --------------------------------------------------------- epilogue
         const int q = warp & 3;  // tensor-memory lane quarter this warp may read
         int acc = 0;

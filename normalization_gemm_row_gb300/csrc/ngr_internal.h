@@ -15,7 +15,16 @@ enum { kNormNone = 0, kNormLayer = 1, kNormRms = 2 };
 constexpr int kBM = 128;        // rows of x per tile (UMMA M)
 constexpr int kBK = 64;         // K per pipeline stage: 64 x 2 B = one 128-byte swizzle row
 constexpr int kUmmaK = 16;      // K per tcgen05.mma (kind::f16)
-constexpr int kGemmThreads = 384;  // 12 warps: producer, MMA, TMEM, spare, 4 transform, 4 epilogue
+// Tile kernel: 16 warps -- producer, MMA, TMEM, spare, 8 transform, 4 epilogue.
+constexpr int kGemmThreads = 512;
+constexpr int kTransformWarp0 = 4;
+constexpr int kTransformThreads = 256;
+constexpr int kEpilogueWarp0 = 12;
+// The transform warps form groups that take turns on consecutive stages,
+// so that several stages are normalized at once.
+constexpr int kTransformGroups = 2;
+constexpr int kGroupThreads = kTransformThreads / kTransformGroups;
+constexpr int kGroupWarps = kGroupThreads / 32;
 
 // Decode (swap-AB) path: weight rows on the UMMA M side, tokens on N.
 constexpr int kDecodeMaxM = 32;      // M up to this uses the decode path
@@ -61,8 +70,11 @@ struct alignas(128) DecodeArgs {
 struct GemmPlan {
     int bn;          // N tile (UMMA N)
     int stages;      // pipeline depth
-    int grid;        // persistent CTAs
+    int grid;        // persistent CTAs (a multiple of 2 for CTA pairs)
     size_t smem;     // dynamic shared memory bytes
+    bool pair;       // CTA-pair kernel (tcgen05 cta_group::2, 256-row tiles)
+    int bm;          // rows per output tile: 128, or 256 for a CTA pair
+    int b_rows;      // rows of W each CTA loads per tile (BN, or BN / 2)
 };
 
 // Record why a CUDA call failed (thread-local; read back through
@@ -78,7 +90,7 @@ int launch_rowstats(int norm, bool bf16, const void *x, int64_t M, int64_t K,
 
 int launch_gemm(int norm, bool silu, bool bf16, const GemmPlan &plan,
                 const GemmArgs &args, bool pdl, cudaStream_t stream);
-GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms);
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, bool norm);
 size_t gemm_smem_bytes(int bn, int stages, bool norm);
 
 int launch_decode(int norm, bool silu, bool bf16, int mn, const DecodeArgs &args,

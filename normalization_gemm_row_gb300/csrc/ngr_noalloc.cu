@@ -146,13 +146,13 @@ extern "C" int ngr_fused_layernorm_linear_noalloc(const void *x, const void *gam
     // Steps a2-a4: the tile kernel, as a programmatic dependent of a1.
     GemmArgs a;
     std::memset(&a, 0, sizeof(a));
-    const GemmPlan plan = plan_gemm(M, N, K, sms);
+    const GemmPlan plan = plan_gemm(M, N, K, sms, true);
     const CUtensorMapDataType t16 =
         bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     if (!na_map(&a.map_a, t16, const_cast<void *>(x), K, M, K * 2, kBK, kBM,
                 CU_TENSOR_MAP_SWIZZLE_128B) ||
         !na_map(&a.map_b, t16, const_cast<void *>(W), K, N, K * 2, kBK,
-                static_cast<uint32_t>(plan.bn), CU_TENSOR_MAP_SWIZZLE_128B) ||
+                static_cast<uint32_t>(plan.b_rows), CU_TENSOR_MAP_SWIZZLE_128B) ||
         !na_map(&a.map_gb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, gamma_f, K, 2, kNaGB, kBK, 2,
                 CU_TENSOR_MAP_SWIZZLE_NONE))
         return NGR_ERR_CUDA;
@@ -164,7 +164,7 @@ extern "C" int ngr_fused_layernorm_linear_noalloc(const void *x, const void *gam
     a.M = static_cast<int>(M);
     a.N = static_cast<int>(N);
     a.K = static_cast<int>(K);
-    a.m_tiles = static_cast<int>((M + kBM - 1) / kBM);
+    a.m_tiles = static_cast<int>((M + plan.bm - 1) / plan.bm);
     a.n_tiles = static_cast<int>((N + plan.bn - 1) / plan.bn);
     a.k_blocks = static_cast<int>((K + kBK - 1) / kBK);
     a.num_tiles = a.m_tiles * a.n_tiles;

@@ -2,11 +2,11 @@
 //
 // "LayerNorm 融合算子如何让大模型推理再快 15%？深度拆解 ATB 的实现", §1.1: the
 // statistics are a reduction over each row (a sum and a sum of squares);
-// §2.3: they are computed in FP32.  One warp reduces one row with 16-byte
+// §2.3: they are computed in FP32.  One CTA reduces one row with 16-byte
 // loads.  LayerNorm uses a shifted, mergeable form so that a large row mean
-// (inputs centred far from zero) does not cancel the variance: each lane
+// (inputs centred far from zero) does not cancel the variance: each thread
 // keeps (n, mean, M2) of its own elements, built from sums of (x - s) with s
-// the lane's first element, and the lanes are merged pairwise with the
+// the thread's first element, and threads are merged pairwise with the
 // parallel-variance update of Chan, Golub and LeVeque (1979):
 //   n = na + nb,  d = mb - ma,  mean = ma + d nb / n,
 //   M2 = M2a + M2b + d^2 na nb / n.
@@ -46,8 +46,26 @@ __device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8])
     }
 }
 
+// Merge (nb, mb, m2b) into (n, mean, m2): the parallel-variance update.
+__device__ __forceinline__ void chan_merge(float &n, float &mean, float &m2, float nb, float mb,
+                                           float m2b)
+{
+    const float nt = n + nb;
+    if (nt > 0.f) {
+        const float d = mb - mean;
+        const float wb = nb / nt;
+        mean = fmaf(d, wb, mean);
+        m2 = m2 + m2b + d * d * (n * wb);
+        n = nt;
+    }
+}
+
+constexpr int kStatsThreads = 256;
+
+// One CTA per row (grid-stride over rows): every thread issues all of its
+// 16-byte loads of the row at once, so a row costs one memory round trip.
 template <int NORM, bool BF16>
-__global__ void __launch_bounds__(256) rowstats_kernel(
+__global__ void __launch_bounds__(kStatsThreads) rowstats_kernel(
     const uint4 *__restrict__ x, int64_t M, int64_t K, float eps,
     float2 *__restrict__ stats, const void *__restrict__ gamma,
     const void *__restrict__ beta, float *__restrict__ gamma_f,
@@ -58,11 +76,10 @@ __global__ void __launch_bounds__(256) rowstats_kernel(
     // waits for this grid's completion before reading the statistics.
     pdl_launch_dependents();
 
-    const int lane = threadIdx.x & 31;
-    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-
-    const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int wid = tid >> 5;
+    const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + tid;
     const int64_t gstride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     if (err_to_clear && gtid == 0) *err_to_clear = 0;
     if (counters) {
@@ -82,21 +99,25 @@ __global__ void __launch_bounds__(256) rowstats_kernel(
         }
     }
 
+    __shared__ float red[3][kStatsThreads / 32];
     const int64_t vec_per_row = K >> 3;  // 8 elements per 16-byte vector
-    for (int64_t row = warp; row < M; row += nwarps) {
+    for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
         const uint4 *xr = x + row * vec_per_row;
         if constexpr (NORM == kNormLayer) {
-            float s = 0.f, s1 = 0.f, s2 = 0.f;
-            float n = 0.f;
+            // This thread's elements as shifted sums, shift = its first element.
+            float s = 0.f, s1 = 0.f, s2 = 0.f, n = 0.f;
             bool have_shift = false;
-            int64_t v = lane;
-            // Four loads in flight per lane.
-            for (; v + 96 < vec_per_row; v += 128) {
+            for (int64_t v0 = tid; v0 < vec_per_row; v0 += 4 * kStatsThreads) {
                 uint4 q[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) q[u] = __ldg(xr + v + 32 * u);
+                for (int u = 0; u < 4; ++u) {
+                    const int64_t v = v0 + static_cast<int64_t>(u) * kStatsThreads;
+                    if (v < vec_per_row) q[u] = __ldg(xr + v);
+                }
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
+                    const int64_t v = v0 + static_cast<int64_t>(u) * kStatsThreads;
+                    if (v >= vec_per_row) break;
                     float f[8];
                     unpack8<BF16>(q[u], f);
                     if (!have_shift) {
@@ -112,22 +133,6 @@ __global__ void __launch_bounds__(256) rowstats_kernel(
                     n += 8.f;
                 }
             }
-            for (; v < vec_per_row; v += 32) {
-                float f[8];
-                unpack8<BF16>(__ldg(xr + v), f);
-                if (!have_shift) {
-                    s = f[0];
-                    have_shift = true;
-                }
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float d = f[i] - s;
-                    s1 += d;
-                    s2 = fmaf(d, d, s2);
-                }
-                n += 8.f;
-            }
-            // This lane's (n, mean, M2).
             float mean = n > 0.f ? s + s1 / n : 0.f;
             float m2 = n > 0.f ? fmaxf(s2 - s1 * (s1 / n), 0.f) : 0.f;
 #pragma unroll
@@ -135,47 +140,50 @@ __global__ void __launch_bounds__(256) rowstats_kernel(
                 const float nb = __shfl_xor_sync(0xffffffffu, n, off);
                 const float mb = __shfl_xor_sync(0xffffffffu, mean, off);
                 const float m2b = __shfl_xor_sync(0xffffffffu, m2, off);
-                const float nt = n + nb;
-                if (nt > 0.f) {
-                    const float d = mb - mean;
-                    const float wb = nb / nt;
-                    // Symmetric in (a, b) up to rounding, so both lanes of
-                    // a pair keep the same merged value.
-                    mean = fmaf(d, wb, mean);
-                    m2 = m2 + m2b + d * d * (n * wb);
-                    n = nt;
-                }
+                chan_merge(n, mean, m2, nb, mb, m2b);
             }
             if (lane == 0) {
-                const float var = m2 / static_cast<float>(K);
-                stats[row] = make_float2(mean, 1.0f / sqrtf(var + eps));
+                red[0][wid] = n;
+                red[1][wid] = mean;
+                red[2][wid] = m2;
             }
+            __syncthreads();
+            if (tid == 0) {
+                float tn = red[0][0], tm = red[1][0], t2 = red[2][0];
+                for (int w = 1; w < kStatsThreads / 32; ++w) chan_merge(tn, tm, t2, red[0][w], red[1][w], red[2][w]);
+                const float var = t2 / static_cast<float>(K);
+                stats[row] = make_float2(tm, 1.0f / sqrtf(var + eps));
+            }
+            __syncthreads();
         } else {
             float ss = 0.f;
-            int64_t v = lane;
-            for (; v + 96 < vec_per_row; v += 128) {
+            for (int64_t v0 = tid; v0 < vec_per_row; v0 += 4 * kStatsThreads) {
                 uint4 q[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) q[u] = __ldg(xr + v + 32 * u);
+                for (int u = 0; u < 4; ++u) {
+                    const int64_t v = v0 + static_cast<int64_t>(u) * kStatsThreads;
+                    if (v < vec_per_row) q[u] = __ldg(xr + v);
+                }
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
+                    const int64_t v = v0 + static_cast<int64_t>(u) * kStatsThreads;
+                    if (v >= vec_per_row) break;
                     float f[8];
                     unpack8<BF16>(q[u], f);
 #pragma unroll
                     for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
                 }
             }
-            for (; v < vec_per_row; v += 32) {
-                float f[8];
-                unpack8<BF16>(__ldg(xr + v), f);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
+            for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            if (lane == 0) red[0][wid] = ss;
+            __syncthreads();
+            if (tid == 0) {
+                float t = 0.f;
+                for (int w = 0; w < kStatsThreads / 32; ++w) t += red[0][w];
+                stats[row] = make_float2(0.f, 1.0f / sqrtf(t / static_cast<float>(K) + eps));
             }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
-                ss += __shfl_xor_sync(0xffffffffu, ss, off);
-            if (lane == 0)
-                stats[row] = make_float2(0.f, 1.0f / sqrtf(ss / static_cast<float>(K) + eps));
+            __syncthreads();
         }
     }
 }
@@ -186,10 +194,9 @@ int launch_rowstats(int norm, bool bf16, const void *x, int64_t M, int64_t K,
                     int *counters, int n_counters, int *err_to_clear,
                     int num_sms, cudaStream_t stream)
 {
-    const int threads = 256;
-    const int64_t rows_per_block = threads / 32;
-    int64_t blocks = (M + rows_per_block - 1) / rows_per_block;
-    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    const int threads = kStatsThreads;
+    int64_t blocks = M;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 16;
     if (blocks > cap) blocks = cap;
     const int64_t kblocks = (K + threads - 1) / threads;
     if (gamma_f && blocks < kblocks) blocks = kblocks < cap ? kblocks : cap;
