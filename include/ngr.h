@@ -127,6 +127,32 @@ int ngr_ffn_linear_silu_linear(const void *x, const void *W1, const void *W2,
                                void *h, void *y, void *workspace,
                                size_t workspace_bytes, ngr_stream_t stream);
 
+/* Inference-mode weight fold, step 1 of 2 ([LNF] §6.2: with gamma and beta
+ * fixed, gamma is folded into the matmul weight once, ahead of the calls).
+ * norm: 1 = LayerNorm, 2 = RMSNorm (beta ignored, may be NULL).  Writes
+ *   Wf[n,k] = gamma[k] W[n,k] rounded to `dtype`           ([N, K], dtype),
+ *   cb[n]     = c[n]  = sum_k Wf[n,k] (from the rounded Wf)   (FP32),
+ *   cb[N + n] = b'[n] = sum_k beta[k] W[n,k] + bias[n]      (FP32),
+ * so cb is FP32 [2, N].  bias may be NULL.  All pointers are device memory,
+ * 16-byte aligned; K % 8 == 0, N % 8 == 0.  Reads W once, writes Wf once. */
+int ngr_fold_prepare(int norm, const void *gamma, const void *beta,
+                     const void *W, const void *bias, int64_t K, int64_t N,
+                     int dtype, void *Wf, float *cb, ngr_stream_t stream);
+
+/* Inference-mode weight fold, step 2 of 2: the same layer as
+ * ngr_fused_layernorm_linear (norm = 1) or ngr_fused_rmsnorm_linear
+ * (norm = 2), from the folded weight:
+ *   y[i,n] = rstd_i (x[i,:] . Wf[n,:]) - rstd_i mu_i c[n] + b'[n]
+ * (RMSNorm: mu = 0), mu and rstd the FP32 row statistics of x.  The matrix
+ * product runs on raw x; no normalized operand exists at all.  Workspace as
+ * for the unfolded op (ngr_workspace_bytes of NGR_OP_LAYERNORM_LINEAR or
+ * NGR_OP_RMSNORM_LINEAR).  [LNF] §6.2. */
+int ngr_fused_norm_linear_folded(int norm, const void *x, const void *Wf,
+                                 const float *cb, float eps, int64_t M,
+                                 int64_t K, int64_t N, int dtype, void *y,
+                                 void *workspace, size_t workspace_bytes,
+                                 ngr_stream_t stream);
+
 /* Variant of ngr_fused_layernorm_linear for callers that cannot allocate
  * device memory and so cannot supply a workspace -- for example code running
  * where every device allocation is planned or owned by someone else, or an

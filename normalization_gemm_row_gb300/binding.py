@@ -41,6 +41,8 @@ SIGNATURES = {
     "ngr_fused_linear_silu": (_I, [_P, _P, _P, _I64, _I64, _I64, _I, _P, _P, _SZ, _P]),
     "ngr_ffn_linear_silu_linear": (_I, [_P, _P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _SZ, _P]),
     "ngr_row_stats": (_I, [_I, _P, _F, _I64, _I64, _I, _P, _P]),
+    "ngr_fold_prepare": (_I, [_I, _P, _P, _P, _P, _I64, _I64, _I, _P, _P, _P]),
+    "ngr_fused_norm_linear_folded": (_I, [_I, _P, _P, _P, _F, _I64, _I64, _I64, _I, _P, _P, _SZ, _P]),
     "ngr_workspace_error": (_I, [_P, _P]),
     "ngr_debug_bounded_wait": (_I, [_P, _U32, _P]),
     "ngr_status_string": (ctypes.c_char_p, [_I]),
@@ -118,6 +120,16 @@ def ngr_ffn_linear_silu_linear(x, W1, W2, M, K, F, dtype, h, y, ws, ws_bytes,
                                stream) -> int:
     return lib().ngr_ffn_linear_silu_linear(x, W1, W2, M, K, F, dtype, h, y,
                                             ws, ws_bytes, stream)
+
+
+def ngr_fold_prepare(norm, gamma, beta, W, bias, K, N, dtype, Wf, cb, stream) -> int:
+    return lib().ngr_fold_prepare(norm, gamma, beta, W, bias, K, N, dtype, Wf, cb, stream)
+
+
+def ngr_fused_norm_linear_folded(norm, x, Wf, cb, eps, M, K, N, dtype, y, ws,
+                                 ws_bytes, stream) -> int:
+    return lib().ngr_fused_norm_linear_folded(norm, x, Wf, cb, eps, M, K, N, dtype,
+                                              y, ws, ws_bytes, stream)
 
 
 def ngr_row_stats(norm, x, eps, M, K, dtype, stats, stream) -> int:
@@ -297,6 +309,39 @@ def ffn_linear_silu_linear(x, W1, W2, out=None, h=None, workspace=None,
                                     _stream(stream))
     _raise(rc, "ffn_linear_silu_linear")
     return y.reshape(*x.shape[:-1], K)
+
+
+def fold_prepare(norm: int, gamma, beta, W, bias=None, stream=None):
+    """Inference-mode fold of gamma (and beta, bias) into the weight:
+    returns (Wf [N, K] in W's dtype, cb float32 [2, N] = (c, b'))."""
+    N, K = W.shape
+    _check(gamma, beta, W, bias, dtype=W.dtype)
+    Wf = torch.empty_like(W)
+    cb = torch.empty((2, N), dtype=torch.float32, device=W.device)
+    rc = ngr_fold_prepare(norm, _ptr(gamma), _ptr(beta), _ptr(W), _ptr(bias), K, N,
+                          _dtype_code(W), _ptr(Wf), _ptr(cb), _stream(stream))
+    _raise(rc, "fold_prepare")
+    return Wf, cb
+
+
+def fused_norm_linear_folded(norm: int, x, Wf, cb, eps, out=None, workspace=None,
+                             stream=None):
+    """y = norm(x) . W^T (+ bias) computed from the folded weight."""
+    K = x.shape[-1]
+    N = Wf.shape[0]
+    x2 = x.reshape(-1, K)
+    M = x2.shape[0]
+    _check(x2, Wf, out, dtype=x.dtype)
+    if cb.dtype != torch.float32 or not cb.is_cuda or not cb.is_contiguous():
+        raise TypeError("cb must be a contiguous float32 CUDA tensor [2, N]")
+    y = out if out is not None else torch.empty((M, N), dtype=x.dtype, device=x.device)
+    op = OP_LAYERNORM_LINEAR if norm == 1 else OP_RMSNORM_LINEAR
+    ws = _workspace(ngr_workspace_bytes(op, M, K, N), x.device, workspace)
+    rc = ngr_fused_norm_linear_folded(norm, _ptr(x2), _ptr(Wf), _ptr(cb), float(eps), M, K, N,
+                                      _dtype_code(x), _ptr(y), _ptr(ws),
+                                      ws.numel() * ws.element_size(), _stream(stream))
+    _raise(rc, "fused_norm_linear_folded")
+    return y.reshape(*x.shape[:-1], N)
 
 
 def row_stats(x, norm: int, eps: float, stream=None) -> torch.Tensor:

@@ -269,13 +269,15 @@ int finish(int rc, void *ws, cudaStream_t stream)
 int launch_layer(int norm, bool silu, bool bf16, const void *x, const void *W,
                  const void *bias, int64_t M, int64_t K, int64_t N, void *y,
                  char *ws, const WsLayout &L, size_t counters_off, bool pdl,
-                 const DevInfo &di, cudaStream_t stream)
+                 const DevInfo &di, cudaStream_t stream, const float *fold_c = nullptr,
+                 const float *fold_b = nullptr)
 {
     // A kernel launched as a programmatic dependent is never a call's first.
     const int zero_err = pdl ? 0 : 1;
     int *err = reinterpret_cast<int *>(ws);
-    const bool has_norm = norm != kNormNone;
-    float2 *stats = has_norm ? reinterpret_cast<float2 *>(ws + L.stats) : nullptr;
+    const bool has_norm = norm == kNormLayer || norm == kNormRms;   // transform stage
+    const bool has_stats = norm != kNormNone;
+    float2 *stats = has_stats ? reinterpret_cast<float2 *>(ws + L.stats) : nullptr;
     float *gf = has_norm ? reinterpret_cast<float *>(ws + L.gamma_f) : nullptr;
     if (M <= kDecodeMaxM) {
         DecodeArgs d;
@@ -286,6 +288,8 @@ int launch_layer(int norm, bool silu, bool bf16, const void *x, const void *W,
         if (has_norm && !map_gb(&d.map_gb, gf, K, L.beta_f - L.gamma_f)) return NGR_ERR_CUDA;
         d.stats = stats;
         d.bias = bias;
+        d.fold_c = fold_c;
+        d.fold_b = fold_b;
         d.y = y;
         d.partials = reinterpret_cast<float *>(ws + L.partials);
         d.counters = reinterpret_cast<int *>(ws + counters_off);
@@ -307,7 +311,7 @@ int launch_layer(int norm, bool silu, bool bf16, const void *x, const void *W,
     }
     GemmArgs a;
     std::memset(&a, 0, sizeof(a));
-    const GemmPlan plan = plan_gemm(M, N, K, di.sms, norm != kNormNone);
+    const GemmPlan plan = plan_gemm(M, N, K, di.sms, has_norm);
     if (trace_mode())
         std::fprintf(stderr, "ngr: tile kernel M=%lld N=%lld K=%lld norm=%d %s BN=%d stages=%d grid=%d smem=%zu\n",
                      static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(K), norm,
@@ -318,6 +322,8 @@ int launch_layer(int norm, bool silu, bool bf16, const void *x, const void *W,
     if (has_norm && !map_gb(&a.map_gb, gf, K, L.beta_f - L.gamma_f)) return NGR_ERR_CUDA;
     a.stats = stats;
     a.bias = bias;
+    a.fold_c = fold_c;
+    a.fold_b = fold_b;
     a.y = y;
     a.err = err;
     a.zero_err = zero_err;
@@ -374,6 +380,47 @@ int norm_linear(int op, int norm, bool silu, const void *x, const void *gamma, c
     event_before(stream);
     rc = launch_layer(norm, silu, bf16, x, W, bias, M, K, N, y, w, L, L.counters, need_stats, di,
                       stream);
+    event_after(stream);
+    events_call_done();
+    return finish(rc, ws, stream);
+}
+
+// The folded layer: statistics of x (a1), then one GEMM on raw x against the
+// folded weight with the statistics applied in the epilogue (a7).
+int folded_linear(int norm, const void *x, const void *Wf, const float *cb, float eps,
+                  int64_t M, int64_t K, int64_t N, int dtype, void *y, void *ws,
+                  size_t ws_bytes, cudaStream_t stream)
+{
+    if (norm != kNormLayer && norm != kNormRms) return NGR_ERR_ARG;
+    int rc = check_sizes(M, K, N, dtype);
+    if (rc != NGR_OK) return rc;
+    if (M == 0) return NGR_OK;
+    if (!x || !Wf || !cb || !y) return NGR_ERR_NULL;
+    if (!ws) return NGR_ERR_WORKSPACE;
+    if (!aligned16(x) || !aligned16(Wf) || !aligned16(cb) || !aligned16(y)) return NGR_ERR_ALIGN;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return NGR_ERR_ALIGN;
+    const WsLayout L = ws_layout(norm == kNormLayer ? NGR_OP_LAYERNORM_LINEAR : NGR_OP_RMSNORM_LINEAR,
+                                 M, K, N, false);
+    if (ws_bytes < L.total) return NGR_ERR_WORKSPACE;
+    DevInfo di;
+    rc = current_device_info(&di);
+    if (rc != NGR_OK) return rc;
+    const bool bf16 = dtype == NGR_BF16;
+    char *w = static_cast<char *>(ws);
+    if (debug_mode() && cudaMemsetAsync(w, 0, 4, stream) != cudaSuccess) return NGR_ERR_CUDA;
+    const bool decode = M <= kDecodeMaxM;
+    events_reset();
+    event_before(stream);
+    rc = launch_rowstats(norm, bf16, x, M, K, eps, reinterpret_cast<float2 *>(w + L.stats), nullptr,
+                         nullptr, nullptr, nullptr,
+                         decode ? reinterpret_cast<int *>(w + L.counters) : nullptr,
+                         decode ? static_cast<int>(ceil_div(N, 128) * 4) : 0,
+                         reinterpret_cast<int *>(w), di.sms, stream);
+    event_after(stream);
+    if (rc != NGR_OK) return rc;
+    event_before(stream);
+    rc = launch_layer(norm == kNormLayer ? kNormFoldLayer : kNormFoldRms, false, bf16, x, Wf,
+                      nullptr, M, K, N, y, w, L, L.counters, true, di, stream, cb, cb + N);
     event_after(stream);
     events_call_done();
     return finish(rc, ws, stream);
@@ -493,6 +540,33 @@ int ngr_ffn_linear_silu_linear(const void *x, const void *W1, const void *W2, in
     event_after(stream);
     events_call_done();
     return finish(rc, workspace, stream);
+}
+
+int ngr_fold_prepare(int norm, const void *gamma, const void *beta, const void *W,
+                     const void *bias, int64_t K, int64_t N, int dtype, void *Wf, float *cb,
+                     ngr_stream_t stream)
+{
+    if (norm != kNormLayer && norm != kNormRms) return NGR_ERR_ARG;
+    int rc = check_sizes(0, K, N, dtype);
+    if (rc != NGR_OK) return rc;
+    if (!gamma || !W || !Wf || !cb || (norm == kNormLayer && !beta)) return NGR_ERR_NULL;
+    if (!aligned16(gamma) || !aligned16(W) || !aligned16(Wf) || !aligned16(cb) ||
+        (beta && !aligned16(beta)) || (bias && !aligned16(bias)))
+        return NGR_ERR_ALIGN;
+    DevInfo di;
+    rc = current_device_info(&di);
+    if (rc != NGR_OK) return rc;
+    rc = launch_fold_prepare(norm, dtype == NGR_BF16, gamma, norm == kNormLayer ? beta : nullptr, W,
+                             bias, K, N, Wf, cb, di.sms, reinterpret_cast<cudaStream_t>(stream));
+    return rc == 0 ? NGR_OK : rc;
+}
+
+int ngr_fused_norm_linear_folded(int norm, const void *x, const void *Wf, const float *cb,
+                                 float eps, int64_t M, int64_t K, int64_t N, int dtype, void *y,
+                                 void *workspace, size_t workspace_bytes, ngr_stream_t stream)
+{
+    return folded_linear(norm, x, Wf, cb, eps, M, K, N, dtype, y, workspace, workspace_bytes,
+                         reinterpret_cast<cudaStream_t>(stream));
 }
 
 int ngr_row_stats(int norm, const void *x, float eps, int64_t M, int64_t K, int dtype,

@@ -55,7 +55,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     decode_kernel(const __grid_constant__ DecodeArgs args)
 {
     using L = DecodeSmem<MN, STAGES>;
-    constexpr bool kNorm = NORM != kNormNone;
+    constexpr bool kNorm = NORM == kNormLayer || NORM == kNormRms;  // transform stage
     constexpr uint32_t kTx = L::kW + L::kX + (kNorm ? L::kGB : 0);
     constexpr uint32_t kTmemCols = 2 * MN <= 32 ? 32 : 64;
     constexpr uint32_t kIdesc = idesc_f16(BF16, 128, MN);
@@ -281,11 +281,23 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                 }
             }
             if (finish && n < N) {
-                float bn = 0.f;
-                if (args.bias != nullptr) bn = to_float1<BF16>(args.bias, n);
+                float bn = 0.f, cn = 0.f;
+                if constexpr (is_fold(NORM)) {
+                    bn = args.fold_b[n];
+                    if constexpr (NORM == kNormFoldLayer) cn = args.fold_c[n];
+                } else if (args.bias != nullptr) {
+                    bn = to_float1<BF16>(args.bias, n);
+                }
                 uint16_t *y = static_cast<uint16_t *>(args.y);
                 for (int m = 0; m < M && m < MN; ++m) {
-                    float z = v[m] + bn;
+                    float z;
+                    if constexpr (is_fold(NORM)) {
+                        // y = rstd acc - rstd mu c + b'
+                        const float2 st = args.stats[m];
+                        z = fmaf(v[m], st.y, fmaf(-st.x * st.y, cn, bn));
+                    } else {
+                        z = v[m] + bn;
+                    }
                     if constexpr (SILU) z = silu_f(z);
                     uint16_t o;
                     if constexpr (BF16) {
@@ -369,6 +381,10 @@ int launch_decode(int norm, bool silu, bool bf16, int mn, const DecodeArgs &args
     NGR_DCASE(kNormNone, true, true)
     NGR_DCASE(kNormNone, false, false)
     NGR_DCASE(kNormNone, false, true)
+    NGR_DCASE(kNormFoldLayer, false, false)
+    NGR_DCASE(kNormFoldLayer, false, true)
+    NGR_DCASE(kNormFoldRms, false, false)
+    NGR_DCASE(kNormFoldRms, false, true)
 #undef NGR_DCASE
     return -9;
 }

@@ -72,6 +72,7 @@ __device__ __forceinline__ void transform_role_tmem(
     const uint8_t *sA, const float *sG, uint64_t *full, uint64_t *a_free, uint32_t tmem_base,
     uint32_t a_col0, const WaitCtx &wc, M0Fn m0_of, ArriveFn arrive)
 {
+    static_assert(KA > 0 && kGroupThreads == 128, "a group must cover the four lane quarters");
     const int g = t / kGroupThreads;
     const int lane = threadIdx.x & 31;
     const int q = (threadIdx.x >> 5) & 3;   // lane quarter this warp may access
@@ -135,7 +136,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm2_kernel(const __grid_constant__ GemmArgs args)
 {
     using L = Gemm2Smem<BN, STAGES>;
-    constexpr bool kNorm = NORM != kNormNone;
+    constexpr bool kNorm = NORM == kNormLayer || NORM == kNormRms;  // transform stage
     constexpr uint32_t kTx = L::kA + L::kB + (kNorm ? L::kGB : 0);
     // Accumulators (two of BN columns, or one with a norm), then the A slots.
     constexpr bool kATmem = kNorm && NGR_PAIR_A_TMEM;
@@ -331,11 +332,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int q = warp & 3;
         int acc = 0;
         uint32_t acc_phase = 0;
-        const int M = args.M, N = args.N;
+        const int N = args.N;
+        if constexpr (is_fold(NORM)) pdl_wait();  // row statistics from the previous grid
         for (int tile = cluster; tile < num_tiles; tile += n_clusters) {
             if (!mbar_wait_warp(&acc_full[acc], acc_phase, wc)) break;
             tc_fence_after();
             const int row = (tile % m_tiles) * 2 * kBM + static_cast<int>(rank) * kBM + q * 32 + lane;
+            const float2 so = fold_row_scale<NORM>(args, row);
             const int nt0 = (tile / m_tiles) * BN;
             const uint32_t t_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                     static_cast<uint32_t>(acc * BN);
@@ -349,40 +352,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 float v[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                if (args.bias != nullptr) {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        if (n0 + 8 * j < N) {
-                            const uint4 bv = __ldg(reinterpret_cast<const uint4 *>(
-                                static_cast<const uint16_t *>(args.bias) + n0 + 8 * j));
-                            const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const float2 f = to_float2<BF16>(bw[i]);
-                                v[8 * j + 2 * i] += f.x;
-                                v[8 * j + 2 * i + 1] += f.y;
-                            }
-                        }
-                    }
-                }
-                if constexpr (SILU) {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = silu_f(v[j]);
-                }
-                if (row < M) {
-                    uint16_t *yrow = static_cast<uint16_t *>(args.y) + static_cast<int64_t>(row) * N;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        if (n0 + 8 * j < N) {
-                            uint4 o;
-                            o.x = from_float2<BF16>(v[8 * j + 0], v[8 * j + 1]);
-                            o.y = from_float2<BF16>(v[8 * j + 2], v[8 * j + 3]);
-                            o.z = from_float2<BF16>(v[8 * j + 4], v[8 * j + 5]);
-                            o.w = from_float2<BF16>(v[8 * j + 6], v[8 * j + 7]);
-                            *reinterpret_cast<uint4 *>(yrow + n0 + 8 * j) = o;
-                        }
-                    }
-                }
+                epilogue_store32<NORM, SILU, BF16>(v, row, n0, args, so);
             }
             tc_fence_before();
             __syncwarp();
@@ -468,6 +438,10 @@ int launch_gemm2_bn(int norm, bool silu, bool bf16, const GemmArgs &args, int gr
     NGR_CASE2(kNormNone, true, true)
     NGR_CASE2(kNormNone, false, false)
     NGR_CASE2(kNormNone, false, true)
+    NGR_CASE2(kNormFoldLayer, false, false)
+    NGR_CASE2(kNormFoldLayer, false, true)
+    NGR_CASE2(kNormFoldRms, false, false)
+    NGR_CASE2(kNormFoldRms, false, true)
 #undef NGR_CASE2
     return -9;
 }

@@ -145,6 +145,81 @@ __device__ __forceinline__ uint4 transform8_pk(uint4 v, float2 so, const float2 
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// The epilogue of 32 accumulator columns [n0, n0 + 32) of one row: + bias,
+// or with a folded norm y = rstd acc + (-mu rstd) c[n] + b'[n] (so =
+// (rstd, -mu rstd) of the row), then SiLU, rounding, 16-byte stores.
+template <int NORM, bool SILU, bool BF16>
+__device__ __forceinline__ void epilogue_store32(float (&v)[32], int row, int n0,
+                                                 const GemmArgs &args, float2 so)
+{
+    const int M = args.M, N = args.N;
+    if constexpr (is_fold(NORM)) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (n0 + 8 * j < N) {
+                const float4 b0 = __ldg(reinterpret_cast<const float4 *>(args.fold_b + n0 + 8 * j));
+                const float4 b1 = __ldg(reinterpret_cast<const float4 *>(args.fold_b + n0 + 8 * j + 4));
+                float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+                if constexpr (NORM == kNormFoldLayer) {
+                    const float4 c0 = __ldg(reinterpret_cast<const float4 *>(args.fold_c + n0 + 8 * j));
+                    const float4 c1 = __ldg(reinterpret_cast<const float4 *>(args.fold_c + n0 + 8 * j + 4));
+                    const float cc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) bb[i] = fmaf(so.y, cc[i], bb[i]);
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[8 * j + i] = fmaf(v[8 * j + i], so.x, bb[i]);
+            }
+        }
+    } else if (args.bias != nullptr) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (n0 + 8 * j < N) {
+                const uint4 bv = __ldg(reinterpret_cast<const uint4 *>(
+                    static_cast<const uint16_t *>(args.bias) + n0 + 8 * j));
+                const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 f = to_float2<BF16>(bw[i]);
+                    v[8 * j + 2 * i] += f.x;
+                    v[8 * j + 2 * i + 1] += f.y;
+                }
+            }
+        }
+    }
+    if constexpr (SILU) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = silu_f(v[j]);
+    }
+    if (row < M) {
+        uint16_t *yrow = static_cast<uint16_t *>(args.y) + static_cast<int64_t>(row) * N;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (n0 + 8 * j < N) {
+                uint4 o;
+                o.x = from_float2<BF16>(v[8 * j + 0], v[8 * j + 1]);
+                o.y = from_float2<BF16>(v[8 * j + 2], v[8 * j + 3]);
+                o.z = from_float2<BF16>(v[8 * j + 4], v[8 * j + 5]);
+                o.w = from_float2<BF16>(v[8 * j + 6], v[8 * j + 7]);
+                *reinterpret_cast<uint4 *>(yrow + n0 + 8 * j) = o;
+            }
+        }
+    }
+}
+
+// (rstd, -mu rstd) of `row` for the folded epilogue.
+template <int NORM>
+__device__ __forceinline__ float2 fold_row_scale(const GemmArgs &args, int row)
+{
+    if constexpr (is_fold(NORM)) {
+        float2 st = make_float2(0.f, 0.f);
+        if (row < args.M) st = args.stats[row];
+        return make_float2(st.y, NORM == kNormFoldLayer ? -st.x * st.y : 0.f);
+    } else {
+        return make_float2(1.f, 0.f);
+    }
+}
+
 // The transform role, shared by the tile kernels.  Transform thread t
 // (0 <= t < kTransformThreads) belongs to group t / kGroupThreads; group g
 // normalizes the stages of the k blocks with running index % groups == g.
@@ -162,6 +237,11 @@ __device__ __forceinline__ void transform_role(int t, int tile0, int tile_step, 
 {
     constexpr int kRows = kBM * 8 / kGroupThreads;   // rows per thread
     constexpr int kRowStep = kGroupThreads / 8;
+    constexpr int kBatch = kRows < 8 ? kRows : 8;
+    // A group waits on a stage barrier kTransformGroups fills after its
+    // previous one; with more groups than stages it could be two phases
+    // ahead, which a parity wait cannot tell from a completed phase.
+    static_assert(kTransformGroups <= STAGES, "more transform groups than pipeline stages");
     const int g = t / kGroupThreads;
     const int u = t % kGroupThreads;
     const int c = u & 7;
@@ -206,14 +286,19 @@ __device__ __forceinline__ void transform_role(int t, int tile0, int tile_step, 
                     bb[3] = make_float2(q[3].z, q[3].w);
                 }
                 uint8_t *base = sA + stage * KA + r0 * 128 + pc;
-                uint4 v[kRows];
+                // Rows in batches of up to 8: all loads of a batch are in
+                // flight before its first store.
 #pragma unroll
-                for (int i = 0; i < kRows; ++i)
-                    v[i] = *reinterpret_cast<const uint4 *>(base + i * kRowStep * 128);
+                for (int b0 = 0; b0 < kRows; b0 += kBatch) {
+                    uint4 v[kBatch];
 #pragma unroll
-                for (int i = 0; i < kRows; ++i)
-                    *reinterpret_cast<uint4 *>(base + i * kRowStep * 128) =
-                        transform8_pk<NORM, BF16>(v[i], so[i], gg, bb);
+                    for (int i = 0; i < kBatch; ++i)
+                        v[i] = *reinterpret_cast<const uint4 *>(base + (b0 + i) * kRowStep * 128);
+#pragma unroll
+                    for (int i = 0; i < kBatch; ++i)
+                        *reinterpret_cast<uint4 *>(base + (b0 + i) * kRowStep * 128) =
+                            transform8_pk<NORM, BF16>(v[i], so[b0 + i], gg, bb);
+                }
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) arrive(stage);
@@ -250,7 +335,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ GemmArgs args)
 {
     using L = GemmSmem<BN, STAGES>;
-    constexpr bool kNorm = NORM != kNormNone;
+    constexpr bool kNorm = NORM == kNormLayer || NORM == kNormRms;  // transform stage
     constexpr uint32_t kTx = L::kA + L::kB + (kNorm ? L::kGB : 0);
     constexpr uint32_t kTmemCols = TmemCols<BN>::value;
     constexpr uint32_t kIdesc = idesc_f16(BF16, kBM, BN);
@@ -399,11 +484,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int q = warp & 3;  // tensor-memory lane quarter this warp may read
         int acc = 0;
         uint32_t acc_phase = 0;
-        const int M = args.M, N = args.N;
+        const int N = args.N;
+        if constexpr (is_fold(NORM)) pdl_wait();  // row statistics from the previous grid
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             if (!mbar_wait_warp(&acc_full[acc], acc_phase, wc)) break;
             tc_fence_after();
             const int row = (tile % m_tiles) * kBM + q * 32 + lane;
+            const float2 so = fold_row_scale<NORM>(args, row);
             const int nt0 = (tile / m_tiles) * BN;
             const uint32_t t_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                     static_cast<uint32_t>(acc * BN);
@@ -417,40 +504,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 float v[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                if (args.bias != nullptr) {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        if (n0 + 8 * j < N) {
-                            const uint4 bv = __ldg(reinterpret_cast<const uint4 *>(
-                                static_cast<const uint16_t *>(args.bias) + n0 + 8 * j));
-                            const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const float2 f = to_float2<BF16>(bw[i]);
-                                v[8 * j + 2 * i] += f.x;
-                                v[8 * j + 2 * i + 1] += f.y;
-                            }
-                        }
-                    }
-                }
-                if constexpr (SILU) {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = silu_f(v[j]);
-                }
-                if (row < M) {
-                    uint16_t *yrow = static_cast<uint16_t *>(args.y) + static_cast<int64_t>(row) * N;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        if (n0 + 8 * j < N) {
-                            uint4 o;
-                            o.x = from_float2<BF16>(v[8 * j + 0], v[8 * j + 1]);
-                            o.y = from_float2<BF16>(v[8 * j + 2], v[8 * j + 3]);
-                            o.z = from_float2<BF16>(v[8 * j + 4], v[8 * j + 5]);
-                            o.w = from_float2<BF16>(v[8 * j + 6], v[8 * j + 7]);
-                            *reinterpret_cast<uint4 *>(yrow + n0 + 8 * j) = o;
-                        }
-                    }
-                }
+                epilogue_store32<NORM, SILU, BF16>(v, row, n0, args, so);
             }
             tc_fence_before();
             mbar_arrive(&acc_empty[acc]);
@@ -505,6 +559,10 @@ int launch_gemm_bn(int norm, bool silu, bool bf16, const GemmArgs &args, int gri
     NGR_CASE(kNormNone, true, true)
     NGR_CASE(kNormNone, false, false)
     NGR_CASE(kNormNone, false, true)
+    NGR_CASE(kNormFoldLayer, false, false)
+    NGR_CASE(kNormFoldLayer, false, true)
+    NGR_CASE(kNormFoldRms, false, false)
+    NGR_CASE(kNormFoldRms, false, true)
 #undef NGR_CASE
     return -9;
 }

@@ -9,7 +9,14 @@
 
 namespace ngr {
 
-enum { kNormNone = 0, kNormLayer = 1, kNormRms = 2 };
+enum { kNormNone = 0, kNormLayer = 1, kNormRms = 2, kNormFoldLayer = 3, kNormFoldRms = 4 };
+
+// Folded (inference-mode) forms: the GEMM runs on raw x against
+// W' = gamma o W and the row statistics are applied in the epilogue.
+__host__ __device__ constexpr bool is_fold(int norm)
+{
+    return norm == kNormFoldLayer || norm == kNormFoldRms;
+}
 
 // Tile geometry shared by host and device.
 constexpr int kBM = 128;        // rows of x per tile (UMMA M)
@@ -22,7 +29,10 @@ constexpr int kTransformThreads = 256;
 constexpr int kEpilogueWarp0 = 12;
 // The transform warps form groups that take turns on consecutive stages,
 // so that several stages are normalized at once.
-constexpr int kTransformGroups = 2;
+#ifndef NGR_TRANSFORM_GROUPS
+#define NGR_TRANSFORM_GROUPS 2
+#endif
+constexpr int kTransformGroups = NGR_TRANSFORM_GROUPS;
 constexpr int kGroupThreads = kTransformThreads / kTransformGroups;
 constexpr int kGroupWarps = kGroupThreads / 32;
 
@@ -38,6 +48,8 @@ struct alignas(128) GemmArgs {
     CUtensorMap map_gb;     // FP32 [2, K] = rows gamma, beta; box {64, 2}
     const float2 *stats;    // [M] (mu, rstd); unused without a norm
     const void *bias;       // [N] or nullptr
+    const float *fold_c;    // folded forms: c[n] = sum_k W'[n,k] (FP32)
+    const float *fold_b;    // folded forms: b'[n] = beta . W[n,:] + bias[n] (FP32)
     void *y;                // [M, N]
     int *err;               // device error word
     int zero_err;           // nonzero: this kernel is the call's first and clears *err
@@ -54,6 +66,8 @@ struct alignas(128) DecodeArgs {
     CUtensorMap map_gb;
     const float2 *stats;
     const void *bias;
+    const float *fold_c;
+    const float *fold_b;
     void *y;
     float *partials;        // [n_tiles][kDecodeMaxContrib][MN][128] fp32
     int *counters;          // [n_tiles], zero at kernel start
@@ -97,6 +111,10 @@ int launch_decode(int norm, bool silu, bool bf16, int mn, const DecodeArgs &args
                   bool pdl, cudaStream_t stream);
 int plan_decode_grid(int64_t n_tiles, int64_t k_blocks, int num_sms);
 size_t decode_smem_bytes(int mn);
+
+int launch_fold_prepare(int norm, bool bf16, const void *gamma, const void *beta,
+                        const void *W, const void *bias, int64_t K, int64_t N, void *Wf,
+                        float *cb, int num_sms, cudaStream_t stream);
 
 int launch_bounded_wait_probe(int *err, unsigned long long timeout_ns,
                               cudaStream_t stream);

@@ -238,3 +238,60 @@ def test_full_size_decode_all_rows(M):
     y = run_op(w.op, to_dev(d), w.eps)
     torch.cuda.synchronize()
     assert_parity(y.double().cpu().numpy(), ref_op(w.op, d, w.eps), f"{w.name} M={M}")
+
+
+# ------------------------------------------------------- inference-mode fold (a7)
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
+@pytest.mark.parametrize("norm", [oracle.NORM_LAYER, oracle.NORM_RMS], ids=["ln", "rms"])
+def test_fold_prepare_against_oracle(norm, dtype):
+    d = inputs.case("layernorm_linear", 4, 1000, 136, dtype, True, 1e-5, seed=21)
+    g = to_dev(d)
+    beta = g["beta"] if norm == oracle.NORM_LAYER else None
+    Wf, cb = B.fold_prepare(norm, g["gamma"], beta, g["W"], g["bias"])
+    torch.cuda.synchronize()
+    Wf_ref, c_ref, b_ref = oracle.fold_prepare(norm, d["gamma"], d["beta"] if beta is not None else None,
+                                               d["W"], d["bias"])
+    # W' is gamma * W rounded once to the 16-bit type: within half a unit in
+    # the last place of the exact product (relative 2^-11 / 2^-8), or half the
+    # subnormal spacing (2^-25 for fp16) where the product underflows.
+    u = 2.0 ** -11 if dtype == torch.float16 else 2.0 ** -8
+    tiny = 2.0 ** -25 if dtype == torch.float16 else 2.0 ** -134
+    got = Wf.double().cpu().numpy()
+    err = np.abs(got - Wf_ref)
+    assert (err <= u * np.abs(Wf_ref) + tiny).all(), float((err - u * np.abs(Wf_ref)).max())
+    cbh = cb.double().cpu().numpy()
+    # c comes from the rounded W' (so it differs from the exact sum by the
+    # accumulated roundings); b' from the unrounded product.
+    assert np.allclose(cbh[0], c_ref, rtol=1e-2, atol=1e-2)
+    assert np.allclose(cbh[1], b_ref, rtol=1e-4, atol=1e-4)
+
+
+FOLD_SHAPES = [(1, 1000, 136), (16, 4096, 520), (32, 512, 264), (33, 1000, 136),
+               (300, 1000, 520), (129, 256, 8)]
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
+@pytest.mark.parametrize("norm", [oracle.NORM_LAYER, oracle.NORM_RMS], ids=["ln", "rms"])
+@pytest.mark.parametrize("M,K,N", FOLD_SHAPES)
+def test_folded_layer_against_direct_oracle(norm, dtype, M, K, N):
+    op = "layernorm_linear" if norm == oracle.NORM_LAYER else "rmsnorm_linear"
+    d = inputs.case(op, M, K, N, dtype, True, 1e-5, seed=M * 7 + N,
+                    x_mean=3.0 if norm == oracle.NORM_LAYER else 0.0)
+    g = to_dev(d)
+    Wf, cb = B.fold_prepare(norm, g["gamma"], g["beta"], g["W"], g["bias"])
+    y = B.fused_norm_linear_folded(norm, g["x"], Wf, cb, 1e-5)
+    torch.cuda.synchronize()
+    assert_parity(y.double().cpu().numpy(), ref_op(op, d, 1e-5), f"folded {op} {M}x{K}x{N}")
+
+
+@pytest.mark.parametrize("idx,M", [(1, None), (4, 16), (4, 1)])
+def test_folded_full_size(idx, M):
+    w, d, rows = full_case(inputs.WORKLOADS[idx], M)
+    g = to_dev(d)
+    norm = oracle.NORM_LAYER
+    Wf, cb = B.fold_prepare(norm, g["gamma"], g["beta"], g["W"], g["bias"])
+    y = B.fused_norm_linear_folded(norm, g["x"], Wf, cb, w.eps)
+    torch.cuda.synchronize()
+    got = y[torch.as_tensor(rows, device="cuda")].double().cpu().numpy()
+    del g, y, Wf
+    assert_parity(got, ref_op(w.op, d, w.eps, rows), f"folded {w.name} M={w.M}")
