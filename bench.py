@@ -355,6 +355,78 @@ def our_arm(args, rank, world, local):
     e2e = {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": M * K * 2,
            "d2h_bytes_per_step": M * out_cols * 2}
 
+    # ---------------- same workload through the inference-mode fold (a7)
+    alternatives = {}
+    if w.op in ("layernorm_linear", "rmsnorm_linear") and not args.no_alternatives:
+        nrm = 1 if w.op == "layernorm_linear" else 2
+        p0 = torch.cuda.Event(enable_timing=True)
+        p1 = torch.cuda.Event(enable_timing=True)
+        p0.record(stream)
+        folded = [B.fold_prepare(nrm, s["gamma"], s.get("beta"), s["W"], s.get("bias")) for s in sets]
+        p1.record(stream)
+        torch.cuda.synchronize(dev)
+        prep_ms = p0.elapsed_time(p1) / n_sets
+
+        def fstep(i):
+            s = sets[i % n_sets]
+            Wf, cb = folded[i % n_sets]
+            B.fused_norm_linear_folded(nrm, s["x"], Wf, cb, w.eps, out=s["y"], workspace=s["ws"])
+
+        for i in range(args.warmup):
+            fstep(i)
+        torch.cuda.synchronize(dev)
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for i in range(args.steps):
+            fstep(i)
+        f1.record(stream)
+        torch.cuda.synchronize(dev)
+        fms = f0.elapsed_time(f1) / args.steps
+        B.kernel_timing_start(args.steps)
+        for i in range(args.steps):
+            fstep(i)
+        ftimes = B.kernel_timing_stop()
+        fk = [statistics.mean(t[j] for t in ftimes) for j in range(len(ftimes[0]))]
+        fval = (algo_bytes / (fms / 1e3) / 1e9) if decode else (flops / (fms / 1e3) / 1e12)
+        alternatives["inference_fold"] = {
+            "what": "gamma folded into W once (W' = gamma o W, c = colsum W', b' = beta.W + bias); "
+                    "per step: row statistics + one GEMM on raw x, y = rstd acc - rstd mu c + b'",
+            "value": fval, "unit": unit, "ms_per_step": fms, "kernel_ms": fk,
+            "prepare_ms_once_per_weight": prep_ms,
+            "frac": (fval / (peaks["hbm_gbs"] if decode else peaks["bf16_tflops"])),
+        }
+        del folded
+    # ---------------- unfused torch pipeline on the same GPU (cuBLAS GEMM)
+    if not args.no_alternatives:
+        import torch.nn.functional as F
+
+        def tstep(i):
+            s = sets[i % n_sets]
+            if w.op == "layernorm_linear":
+                return F.linear(F.layer_norm(s["x"], (K,), s["gamma"], s["beta"], w.eps), s["W"], s.get("bias"))
+            if w.op == "rmsnorm_linear":
+                return F.linear(F.rms_norm(s["x"], (K,), s["gamma"], w.eps), s["W"], s.get("bias"))
+            if w.op == "linear_silu":
+                return F.silu(F.linear(s["x"], s["W"], s.get("bias")))
+            return F.linear(F.silu(F.linear(s["x"], s["W1"])), s["W2"])
+
+        for i in range(args.warmup):
+            tstep(i)
+        torch.cuda.synchronize(dev)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.steps):
+            tstep(i)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        tms = t0.elapsed_time(t1) / args.steps
+        alternatives["torch_unfused_same_gpu"] = {
+            "what": "torch layer_norm/rms_norm -> linear (cuBLAS) [-> silu], normalized rows written to HBM",
+            "value": (algo_bytes / (tms / 1e3) / 1e9) if decode else (flops / (tms / 1e3) / 1e12),
+            "unit": unit, "ms_per_step": tms}
+
     out = {
         "metric": metric, "value": value, "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -372,6 +444,7 @@ def our_arm(args, rank, world, local):
         "gpu_launches": kernels_per_step * args.steps,
         "clocks": clock_info,
         "pct_of_dense_fp16_peak": None if decode else 100.0 * value / world / peaks["bf16_tflops"],
+        "alternatives": alternatives,
     }
     return out, w, host
 
@@ -483,6 +556,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--m", type=int, default=None, help="override M (decode workload: 1, 4 or 16)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-alternatives", action="store_true",
+                    help="skip the inference-fold and unfused-torch comparison runs")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-rows", type=int, default=0)
     args = ap.parse_args(argv)
