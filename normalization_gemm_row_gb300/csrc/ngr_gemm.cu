@@ -105,6 +105,16 @@ static int pair_override()
     return v;
 }
 
+// NGR_BN=128|192|224|256 restricts the planner to that N tile width.
+static int bn_override()
+{
+    static const int v = [] {
+        const char *e = std::getenv("NGR_BN");
+        return e ? std::atoi(e) : 0;
+    }();
+    return v;
+}
+
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, bool norm)
 {
     (void)K;
@@ -112,6 +122,7 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, bool norm)
     GemmPlan best{256, 4, 1, 0, false, kBM, 256};
     double best_cost = -1.0;
     for (int bn : kTileWidths) {
+        if (bn_override() && bn != bn_override()) continue;
         const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + bn - 1) / bn);
         const int64_t grid = tiles < num_sms ? tiles : num_sms;
         const int64_t per_cta = (tiles + grid - 1) / grid;
@@ -125,6 +136,7 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, bool norm)
         if (pair_override() == 1) best_cost = 1e300;
         const int pairs = max_pairs(num_sms);
         for (int bn : kTileWidths) {
+            if (bn_override() && bn != bn_override()) continue;
             const int64_t tiles = ((M + 2 * kBM - 1) / (2 * kBM)) * ((N + bn - 1) / bn);
             const int64_t clusters = tiles < pairs ? tiles : pairs;
             if (clusters < 1) continue;

@@ -13,10 +13,11 @@
 // tensor core.
 //
 // Synchronization (barriers are per CTA unless marked "leader"):
-//   full[s]        TMA landed in this CTA (its producer's expect_tx);
-//   ready[s]       leader: each transform warp of both CTAs (or one relay
-//                  thread per CTA without a norm) arrives once its CTA's
-//                  stage is ready for the tensor core;
+//   full[s]        with a norm: this CTA's copies landed (its producer's
+//                  expect_tx); without: the leader's, on which both CTAs'
+//                  copies complete (cta_group::2 TMA) -- the MMA waits on it;
+//   ready[s]       leader, with a norm: each transform warp of both CTAs
+//                  arrives once its CTA's stage is normalized;
 //   empty[s]       the leader's tcgen05.commit, multicast to both CTAs;
 //   acc_full[a]    the leader's commit at the end of a tile, multicast;
 //   acc_empty[a]   leader: each epilogue warp of both CTAs arrives after
@@ -149,8 +150,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                   "tensor memory: accumulator + A slots");
     constexpr uint32_t kIdesc = idesc_f16(BF16, 2 * kBM, BN);
     // ready[s] arrivals: one per warp of the transform group that owns the
-    // stage, in each CTA, or one relay thread per CTA without a norm.
-    constexpr uint32_t kReadyCount = kNorm ? 2 * kGroupWarps : 2;
+    // stage, in each CTA (used with a norm only).
+    constexpr uint32_t kReadyCount = 2 * kGroupWarps;
     static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "UMMA N for M = 256");
     static_assert((BN / 2) % 8 == 0, "B half tile rows");
 
@@ -214,6 +215,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int n_clusters = gridDim.x >> 1;
     // Leader-side addresses of ready[] and acc_empty[] (shared::cluster).
     const uint32_t ready_leader = mapa_shared(smem_u32(ready), 0);
+    const uint32_t full_leader = mapa_shared(smem_u32(full), 0);
     const uint32_t acc_empty_leader = mapa_shared(smem_u32(acc_empty), 0);
 
     if (warp == 0) {
@@ -231,22 +233,37 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const int n0 = (tile / m_tiles) * BN + static_cast<int>(rank) * (BN / 2);
                 for (int kb = 0; kb < k_blocks; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, wc)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&full[stage], kTx);
                     const int kc = kb * kBK;
-                    tma_load_2d(sA + stage * L::kA, &args.map_a, &full[stage], kc, m0, pol_x);
-                    tma_load_2d(sB + stage * L::kB, &args.map_b, &full[stage], kc, n0, pol_w);
-                    if constexpr (kNorm)
+                    if constexpr (kNorm) {
+                        // Each CTA normalizes its own stage: local barrier.
+                        mbar_arrive_expect_tx(&full[stage], kTx);
+                        tma_load_2d(sA + stage * L::kA, &args.map_a, &full[stage], kc, m0, pol_x);
+                        tma_load_2d(sB + stage * L::kB, &args.map_b, &full[stage], kc, n0, pol_w);
                         tma_load_2d(sG + stage * 2 * kBK, &args.map_gb, &full[stage], kc, 0, pol_x);
+                    } else {
+                        // Both CTAs' copies complete on the leader's barrier,
+                        // which expects the bytes of both.
+                        const uint32_t fb = full_leader + 8u * static_cast<uint32_t>(stage);
+                        if (leader) mbar_arrive_expect_tx(&full[stage], 2 * kTx);
+                        tma_load_2d_pair(sA + stage * L::kA, &args.map_a, fb, kc, m0, pol_x);
+                        tma_load_2d_pair(sB + stage * L::kB, &args.map_b, fb, kc, n0, pol_w);
+                    }
                     ++fills;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
             }
-            const int outstanding = fills < STAGES ? static_cast<int>(fills) : STAGES;
-            for (int j = 1; j <= outstanding; ++j) {
-                int s = stage - j;
-                uint32_t p = phase;
-                if (s < 0) { s += STAGES; p ^= 1u; }
-                mbar_wait(&full[s], p, wc);
+            // Copies signalled on this CTA's own barriers: wait for the last
+            // fills.  (Without a norm the peer's copies complete on the
+            // leader's barriers; the leader's MMAs, and so the final cluster
+            // barrier, come after them.)
+            if (kNorm || leader) {
+                const int outstanding = fills < STAGES ? static_cast<int>(fills) : STAGES;
+                for (int j = 1; j <= outstanding; ++j) {
+                    int s = stage - j;
+                    uint32_t p = phase;
+                    if (s < 0) { s += STAGES; p ^= 1u; }
+                    mbar_wait(&full[s], p, wc);
+                }
             }
         }
     } else if (warp == 1) {
@@ -263,7 +280,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
                 for (int kb = 0; kb < k_blocks; ++kb) {
-                    if (!mbar_wait(&ready[stage], phase, wc)) { ok = false; break; }
+                    if (!mbar_wait(kNorm ? &ready[stage] : &full[stage], phase, wc)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t b_addr = smem_u32(sB + stage * L::kB);
                     if constexpr (kATmem) {
@@ -312,20 +329,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 t, cluster, n_clusters, num_tiles, k_blocks, args.M, args.stats, sA, sG, full, wc,
                 [&](int tile) { return (tile % m_tiles) * 2 * kBM + static_cast<int>(rank) * kBM; },
                 [&](int st) { mbar_arrive_cluster(ready_leader + 8u * static_cast<uint32_t>(st)); });
-        } else if (t == 0) {
-            // ------------------------------------------------------- relay
-            // Without a norm the stage needs no work: one thread tells the
-            // leader that this CTA's copies have landed.
-            int stage = 0;
-            uint32_t phase = 0;
-            bool ok = true;
-            for (int tile = cluster; ok && tile < num_tiles; tile += n_clusters) {
-                for (int kb = 0; kb < k_blocks; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, wc)) { ok = false; break; }
-                    mbar_arrive_cluster(ready_leader + 8u * static_cast<uint32_t>(stage));
-                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-                }
-            }
         }
     } else if (warp >= kEpilogueWarp0) {
         // --------------------------------------------------------- epilogue

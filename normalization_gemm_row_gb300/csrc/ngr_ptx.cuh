@@ -428,4 +428,19 @@ __device__ __forceinline__ void umma_f16_ts_pair(uint32_t d_tmem, uint32_t a_tme
         : "memory");
 }
 
+// 2-D tiled load into this CTA's shared memory whose completion (transaction
+// bytes) is signalled on an mbarrier of either CTA of the pair, given by its
+// shared::cluster address.
+__device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *m,
+                                                 uint32_t bar_cluster_addr, int c0, int c1,
+                                                 uint64_t cache_hint)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster_addr), "r"(c0), "r"(c1),
+        "l"(cache_hint)
+        : "memory");
+}
+
 }  // namespace ngr
