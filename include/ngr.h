@@ -196,6 +196,18 @@ int ngr_workspace_error(void *workspace, ngr_stream_t stream);
 int ngr_debug_bounded_wait(void *workspace, uint32_t timeout_us,
                            ngr_stream_t stream);
 
+/* Tuning aid: restrict the choice of the tile kernel (M > 32) for every
+ * later call in this process, on every thread.  `pair`: -1 let the planner
+ * decide, 0 the single-CTA kernel (128-row tiles), 1 the CTA-pair kernel
+ * (256-row tiles; only taken when M > 128).  `bn`: 0 any, else the N tile
+ * (or sub-tile) width, one of 128, 192, 224, 256.  `nsub`: 0 any, else the
+ * N sub-tiles per CTA-pair tile, 1 or 2 (2 only with bn 224 or 256).  The
+ * planner picks the cheapest variant that satisfies all three; if none does
+ * it ignores the restriction.  ngr_set_tile_config(-1, 0, 0) restores the
+ * default.  The environment variables NGR_PAIR, NGR_BN and NGR_NSUB give
+ * the initial setting.  Returns NGR_OK or NGR_ERR_ARG. */
+int ngr_set_tile_config(int pair, int bn, int nsub);
+
 /* Profiling aid: time every kernel of this thread's next `n_calls` calls.
  * Each such call records CUDA events (the library's own, created here; no
  * device memory) on its stream just before and just after each kernel it

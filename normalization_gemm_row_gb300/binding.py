@@ -48,6 +48,7 @@ SIGNATURES = {
     "ngr_status_string": (ctypes.c_char_p, [_I]),
     "ngr_version": (_I, []),
     "ngr_last_error": (ctypes.c_char_p, []),
+    "ngr_set_tile_config": (_I, [_I, _I, _I]),
     "ngr_kernel_timing_start": (_I, [_I]),
     "ngr_kernel_timing_stop": (_I, [_P, _I]),
 }
@@ -154,6 +155,15 @@ def ngr_version() -> int:
 
 def ngr_last_error() -> str:
     return lib().ngr_last_error().decode()
+
+
+def ngr_set_tile_config(pair, bn, nsub) -> int:
+    return lib().ngr_set_tile_config(pair, bn, nsub)
+
+
+def set_tile_config(pair: int = -1, bn: int = 0, nsub: int = 0):
+    """Restrict the tile-kernel choice (-1/0/0 restores the planner's)."""
+    _raise(ngr_set_tile_config(pair, bn, nsub), "ngr_set_tile_config")
 
 
 MAX_KERNELS_PER_CALL = 4

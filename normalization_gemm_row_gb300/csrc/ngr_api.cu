@@ -313,9 +313,10 @@ int launch_layer(int norm, bool silu, bool bf16, const void *x, const void *W,
     std::memset(&a, 0, sizeof(a));
     const GemmPlan plan = plan_gemm(M, N, K, di.sms, has_norm);
     if (trace_mode())
-        std::fprintf(stderr, "ngr: tile kernel M=%lld N=%lld K=%lld norm=%d %s BN=%d stages=%d grid=%d smem=%zu\n",
+        std::fprintf(stderr, "ngr: tile kernel M=%lld N=%lld K=%lld norm=%d %s BN=%d x %d stages=%d grid=%d smem=%zu\n",
                      static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(K), norm,
-                     plan.pair ? "cta-pair" : "single-cta", plan.bn, plan.stages, plan.grid, plan.smem);
+                     plan.pair ? "cta-pair" : "single-cta", plan.bn, plan.nsub, plan.stages, plan.grid,
+                     plan.smem);
     if (!map_2d(&a.map_a, x, bf16, M, K, kBM) ||
         !map_2d(&a.map_b, W, bf16, N, K, static_cast<uint32_t>(plan.b_rows)))
         return NGR_ERR_CUDA;
@@ -331,7 +332,7 @@ int launch_layer(int norm, bool silu, bool bf16, const void *x, const void *W,
     a.N = static_cast<int>(N);
     a.K = static_cast<int>(K);
     a.m_tiles = static_cast<int>(ceil_div(M, plan.bm));
-    a.n_tiles = static_cast<int>(ceil_div(N, plan.bn));
+    a.n_tiles = static_cast<int>(ceil_div(N, plan.tw));
     a.k_blocks = static_cast<int>(ceil_div(K, kBK));
     a.num_tiles = a.m_tiles * a.n_tiles;
     a.timeout_ns = wait_timeout_ns();
@@ -612,6 +613,11 @@ int ngr_debug_bounded_wait(void *workspace, uint32_t timeout_us, ngr_stream_t st
     rc = launch_bounded_wait_probe(static_cast<int *>(workspace),
                                    static_cast<unsigned long long>(timeout_us) * 1000ull, stream);
     return rc == 0 ? NGR_OK : NGR_ERR_CUDA;
+}
+
+int ngr_set_tile_config(int pair, int bn, int nsub)
+{
+    return set_tile_config(pair, bn, nsub) == 0 ? NGR_OK : NGR_ERR_ARG;
 }
 
 int ngr_kernel_timing_start(int n_calls)

@@ -6,6 +6,7 @@
 // per-tile overhead term (each tile re-normalizes its x tile and drains its
 // accumulator), so that wave quantization on the SM count at hand is
 // avoided without shrinking tiles needlessly.
+#include <atomic>
 #include <cstdlib>
 #include <mutex>
 
@@ -30,6 +31,10 @@ size_t gemm2_smem_bn192();
 size_t gemm2_smem_bn224();
 size_t gemm2_smem_bn256();
 int gemm2_max_clusters_bn224();
+int launch_gemm2w_bn224(int, bool, bool, const GemmArgs &, int, bool, cudaStream_t);
+int launch_gemm2w_bn256(int, bool, bool, const GemmArgs &, int, bool, cudaStream_t);
+size_t gemm2w_smem_bn224();
+size_t gemm2w_smem_bn256();
 
 static const int kTileWidths[] = {256, 224, 192, 128};
 
@@ -63,8 +68,9 @@ static int stages2_for(int bn)
     }
 }
 
-static size_t gemm2_smem_bytes(int bn)
+static size_t gemm2_smem_bytes(int bn, int nsub)
 {
+    if (nsub == 2) return bn == 224 ? gemm2w_smem_bn224() : gemm2w_smem_bn256();
     switch (bn) {
     case 128: return gemm2_smem_bn128();
     case 192: return gemm2_smem_bn192();
@@ -90,72 +96,107 @@ static int max_pairs(int num_sms)
 
 // Relative cost of one N column of a 128-row slice on one SM: the CTA-pair
 // kernel streams half the W bytes per FLOP and runs closer to the tensor
-// peak (measured), so it is preferred unless its tiles quantize worse.
+// peak (measured), so it is preferred unless its tiles quantize worse; its
+// two-sub-tile form streams fewer bytes still but does not overlap the
+// epilogue, which the larger per-tile term stands for.
 constexpr double kPairCostFactor = 0.8;
+constexpr double kWideCostFactor = 0.7;
+constexpr int kWideTileOverhead = 32;
 
-// NGR_PAIR=0 never picks the CTA-pair kernel, NGR_PAIR=1 always does when
-// M > 128; unset, the cost model decides.
-static int pair_override()
+// Stages of the two-sub-tile CTA-pair kernel for a sub-tile width.
+static int stages2w_for(int bn) { return bn == 224 ? 5 : 4; }
+static const int kWideWidths[] = {256, 224};
+
+// Tile-kernel restrictions (ngr_set_tile_config): pair -1/0/1, bn 0 or a
+// width, nsub 0/1/2.  Initialized from NGR_PAIR, NGR_BN and NGR_NSUB.
+static int env_int(const char *name, int dflt)
 {
-    static const int v = [] {
-        const char *e = std::getenv("NGR_PAIR");
-        if (!e || !e[0]) return -1;
-        return e[0] == '0' ? 0 : 1;
-    }();
-    return v;
+    const char *e = std::getenv(name);
+    return (e && e[0]) ? std::atoi(e) : dflt;
+}
+static std::atomic<int> g_pair{env_int("NGR_PAIR", -1) < 0 ? -1 : (env_int("NGR_PAIR", -1) ? 1 : 0)};
+static std::atomic<int> g_bn{env_int("NGR_BN", 0)};
+static std::atomic<int> g_nsub{env_int("NGR_NSUB", 0)};
+
+int set_tile_config(int pair, int bn, int nsub)
+{
+    if (pair < -1 || pair > 1) return -9;
+    if (bn != 0 && bn != 128 && bn != 192 && bn != 224 && bn != 256) return -9;
+    if (nsub < 0 || nsub > 2) return -9;
+    if (nsub == 2 && (pair == 0 || (bn != 0 && bn != 224 && bn != 256))) return -9;
+    g_pair.store(pair);
+    g_bn.store(bn);
+    g_nsub.store(nsub);
+    return 0;
 }
 
-// NGR_BN=128|192|224|256 restricts the planner to that N tile width.
-static int bn_override()
+// The cheapest variant allowed by the restrictions (pair, bn, nsub as in
+// set_tile_config); none allowed gives a negative cost.
+static GemmPlan plan_with(int64_t M, int64_t N, int num_sms, int want_pair, int want_bn,
+                          int want_nsub, double *cost_out)
 {
-    static const int v = [] {
-        const char *e = std::getenv("NGR_BN");
-        return e ? std::atoi(e) : 0;
-    }();
-    return v;
+    GemmPlan best{256, 4, 1, 0, false, kBM, 256, 1, 256};
+    double best_cost = -1.0;
+    auto take = [&](double cost, const GemmPlan &p) {
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = p;
+        }
+    };
+    if (want_pair != 1 && want_nsub != 2) {
+        for (int bn : kTileWidths) {
+            if (want_bn && bn != want_bn) continue;
+            const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + bn - 1) / bn);
+            const int64_t grid = tiles < num_sms ? tiles : num_sms;
+            const int64_t per_cta = (tiles + grid - 1) / grid;
+            take(static_cast<double>(per_cta) * (bn + 16),
+                 GemmPlan{bn, stages_for(bn), static_cast<int>(grid), 0, false, kBM, bn, 1, bn});
+        }
+    }
+    if (M > kBM && want_pair != 0) {
+        const int pairs = max_pairs(num_sms);
+        auto consider = [&](int bn, int nsub, int stages, double factor, int overhead) {
+            if (want_bn && bn != want_bn) return;
+            if (want_nsub && nsub != want_nsub) return;
+            const int tw = bn * nsub;
+            const int64_t tiles = ((M + 2 * kBM - 1) / (2 * kBM)) * ((N + tw - 1) / tw);
+            const int64_t clusters = tiles < pairs ? tiles : pairs;
+            if (clusters < 1) return;
+            const int64_t per = (tiles + clusters - 1) / clusters;
+            take(factor * static_cast<double>(per) * (tw + overhead),
+                 GemmPlan{bn, stages, static_cast<int>(2 * clusters), 0, true, 2 * kBM, bn / 2,
+                          nsub, tw});
+        };
+        for (int bn : kTileWidths) consider(bn, 1, stages2_for(bn), kPairCostFactor, 16);
+        for (int bn : kWideWidths)
+            consider(bn, 2, stages2w_for(bn), kWideCostFactor, kWideTileOverhead);
+    }
+    *cost_out = best_cost;
+    return best;
 }
 
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, bool norm)
 {
     (void)K;
     (void)norm;
-    GemmPlan best{256, 4, 1, 0, false, kBM, 256};
-    double best_cost = -1.0;
-    for (int bn : kTileWidths) {
-        if (bn_override() && bn != bn_override()) continue;
-        const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + bn - 1) / bn);
-        const int64_t grid = tiles < num_sms ? tiles : num_sms;
-        const int64_t per_cta = (tiles + grid - 1) / grid;
-        const double cost = static_cast<double>(per_cta) * (bn + 16);
-        if (best_cost < 0 || cost < best_cost) {
-            best_cost = cost;
-            best = GemmPlan{bn, stages_for(bn), static_cast<int>(grid), 0, false, kBM, bn};
-        }
-    }
-    if (M > kBM && pair_override() != 0) {
-        if (pair_override() == 1) best_cost = 1e300;
-        const int pairs = max_pairs(num_sms);
-        for (int bn : kTileWidths) {
-            if (bn_override() && bn != bn_override()) continue;
-            const int64_t tiles = ((M + 2 * kBM - 1) / (2 * kBM)) * ((N + bn - 1) / bn);
-            const int64_t clusters = tiles < pairs ? tiles : pairs;
-            if (clusters < 1) continue;
-            const int64_t per = (tiles + clusters - 1) / clusters;
-            const double cost = kPairCostFactor * static_cast<double>(per) * (bn + 16);
-            if (cost < best_cost) {
-                best_cost = cost;
-                best = GemmPlan{bn, stages2_for(bn), static_cast<int>(2 * clusters), 0, true,
-                                2 * kBM, bn / 2};
-            }
-        }
-    }
-    best.smem = best.pair ? gemm2_smem_bytes(best.bn) : gemm_smem_bytes(best.bn, best.stages, true);
+    double cost = -1.0;
+    GemmPlan best = plan_with(M, N, num_sms, g_pair.load(), g_bn.load(), g_nsub.load(), &cost);
+    if (cost < 0) best = plan_with(M, N, num_sms, -1, 0, 0, &cost);
+    best.smem = best.pair ? gemm2_smem_bytes(best.bn, best.nsub)
+                          : gemm_smem_bytes(best.bn, best.stages, true);
     return best;
 }
 
 int launch_gemm(int norm, bool silu, bool bf16, const GemmPlan &plan, const GemmArgs &args,
                 bool pdl, cudaStream_t stream)
 {
+    if (plan.pair && plan.nsub == 2) {
+        switch (plan.bn) {
+        case 224: return launch_gemm2w_bn224(norm, silu, bf16, args, plan.grid, pdl, stream);
+        case 256: return launch_gemm2w_bn256(norm, silu, bf16, args, plan.grid, pdl, stream);
+        default: return -9;
+        }
+    }
     if (plan.pair) {
         switch (plan.bn) {
         case 128: return launch_gemm2_bn128(norm, silu, bf16, args, plan.grid, pdl, stream);

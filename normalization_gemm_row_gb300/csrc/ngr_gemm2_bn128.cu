@@ -8,10 +8,10 @@ namespace ngr {
 int launch_gemm2_bn128(int norm, bool silu, bool bf16, const GemmArgs &args, int grid,
                       bool pdl, cudaStream_t stream)
 {
-    return launch_gemm2_bn<128, 8>(norm, silu, bf16, args, grid, pdl, stream);
+    return launch_gemm2_bn<128, 8, 1>(norm, silu, bf16, args, grid, pdl, stream);
 }
 
-size_t gemm2_smem_bn128() { return Gemm2Smem<128, 8>::alloc; }
-int gemm2_max_clusters_bn128() { return gemm2_max_clusters<128, 8>(); }
+size_t gemm2_smem_bn128() { return Gemm2Smem<128, 8, 1>::alloc; }
+int gemm2_max_clusters_bn128() { return gemm2_max_clusters<128, 8, 1>(); }
 
 }  // namespace ngr

@@ -8,10 +8,10 @@ namespace ngr {
 int launch_gemm2_bn192(int norm, bool silu, bool bf16, const GemmArgs &args, int grid,
                       bool pdl, cudaStream_t stream)
 {
-    return launch_gemm2_bn<192, 7>(norm, silu, bf16, args, grid, pdl, stream);
+    return launch_gemm2_bn<192, 7, 1>(norm, silu, bf16, args, grid, pdl, stream);
 }
 
-size_t gemm2_smem_bn192() { return Gemm2Smem<192, 7>::alloc; }
-int gemm2_max_clusters_bn192() { return gemm2_max_clusters<192, 7>(); }
+size_t gemm2_smem_bn192() { return Gemm2Smem<192, 7, 1>::alloc; }
+int gemm2_max_clusters_bn192() { return gemm2_max_clusters<192, 7, 1>(); }
 
 }  // namespace ngr

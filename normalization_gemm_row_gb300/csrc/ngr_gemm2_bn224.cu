@@ -8,10 +8,10 @@ namespace ngr {
 int launch_gemm2_bn224(int norm, bool silu, bool bf16, const GemmArgs &args, int grid,
                       bool pdl, cudaStream_t stream)
 {
-    return launch_gemm2_bn<224, 7>(norm, silu, bf16, args, grid, pdl, stream);
+    return launch_gemm2_bn<224, 7, 1>(norm, silu, bf16, args, grid, pdl, stream);
 }
 
-size_t gemm2_smem_bn224() { return Gemm2Smem<224, 7>::alloc; }
-int gemm2_max_clusters_bn224() { return gemm2_max_clusters<224, 7>(); }
+size_t gemm2_smem_bn224() { return Gemm2Smem<224, 7, 1>::alloc; }
+int gemm2_max_clusters_bn224() { return gemm2_max_clusters<224, 7, 1>(); }
 
 }  // namespace ngr

@@ -1,16 +1,20 @@
 // ngr_gemm2_kernel.cuh -- the fused pre-norm linear layer on a CTA pair
-// (tcgen05 cta_group::2): same computation as gemm_kernel, on 256 x BN
+// (tcgen05 cta_group::2): same computation as gemm_kernel, on 256 x (NSUB BN)
 // output tiles.
 //
 // The two CTAs of a cluster share each tile: CTA r loads rows
-// [m0 + 128 r, +128) of x and rows [n0 + r BN/2, +BN/2) of W into its own
-// shared memory (no multicast), normalizes its own x rows in place, and the
-// even CTA issues one tcgen05.mma.cta_group::2 per K step that reads A from
-// both CTAs by rows and B from both CTAs by columns, accumulating its 128
+// [m0 + 128 r, +128) of x and, for each of the NSUB sub-tiles j, rows
+// [n0 + j BN + r BN/2, +BN/2) of W into its own shared memory (no
+// multicast), normalizes its own x rows in place, and the even CTA issues
+// per K step one tcgen05.mma.cta_group::2 per sub-tile, each reading A from
+// both CTAs by rows and its B from both CTAs by columns, accumulating its 128
 // rows of D in each CTA's tensor memory.  Per CTA this halves the W bytes
 // loaded and read from shared memory per FLOP compared with a single-CTA
-// 128 x BN tile, which is what keeps enough bytes in flight to feed the
-// tensor core.
+// 128 x BN tile; with NSUB = 2 the normalized A stage also serves twice the
+// columns, which cuts the shared-memory fill bytes per FLOP by another
+// quarter and halves the normalization work per FLOP.  The price is one
+// accumulator instead of two: the epilogue of a tile does not overlap the
+// next tile's MMAs.
 //
 // Synchronization (barriers are per CTA unless marked "leader"):
 //   full[s]        with a norm: this CTA's copies landed (its producer's
@@ -43,10 +47,11 @@ constexpr int kMaxASlots = 8;
 #define NGR_PAIR_A_TMEM 0
 #endif
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int NSUB>
 struct Gemm2Smem {
     static constexpr int kA = kBM * kBK * 2;          // 16 KB: this CTA's 128 x rows
-    static constexpr int kB = (BN / 2) * kBK * 2;     // this CTA's BN/2 W rows
+    static constexpr int kBSub = (BN / 2) * kBK * 2;  // this CTA's BN/2 W rows of one sub-tile
+    static constexpr int kB = NSUB * kBSub;
     static constexpr int kGB = 2 * kBK * 4;           // FP32 gamma[64], beta[64]
     static constexpr int off_a = 0;
     static constexpr int off_b = off_a + STAGES * kA;
@@ -132,17 +137,22 @@ __device__ __forceinline__ void transform_role_tmem(
     }
 }
 
-template <int NORM, bool SILU, bool BF16, int BN, int STAGES>
+template <int NORM, bool SILU, bool BF16, int BN, int STAGES, int NSUB>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm2_kernel(const __grid_constant__ GemmArgs args)
 {
-    using L = Gemm2Smem<BN, STAGES>;
+    using L = Gemm2Smem<BN, STAGES, NSUB>;
     constexpr bool kNorm = NORM == kNormLayer || NORM == kNormRms;  // transform stage
-    constexpr uint32_t kTx = L::kA + L::kB + (kNorm ? L::kGB : 0);
-    // Accumulators (two of BN columns, or one with a norm), then the A slots.
-    constexpr bool kATmem = kNorm && NGR_PAIR_A_TMEM;
-    constexpr int kAccBufs = kATmem ? 1 : 2;
-    constexpr uint32_t kACol0 = kAccBufs * BN;
+    constexpr int kTW = NSUB * BN;   // output tile width
+    // Bytes one stage of this CTA receives when n_sub sub-tiles are in range.
+    auto stage_tx = [](int n_sub) -> uint32_t {
+        return static_cast<uint32_t>(L::kA + n_sub * L::kBSub + (kNorm ? L::kGB : 0));
+    };
+    // Accumulators (two of kTW columns when they fit and A is not in tensor
+    // memory, else one), then the A slots.
+    constexpr bool kATmem = kNorm && NGR_PAIR_A_TMEM && NSUB == 1;
+    constexpr int kAccBufs = (kATmem || NSUB > 1) ? 1 : 2;
+    constexpr uint32_t kACol0 = kAccBufs * kTW;
     constexpr uint32_t kTmemCols = 512;
     constexpr int kSlotsFit = static_cast<int>((kTmemCols - kACol0) / kASlotCols);
     constexpr int kASlots = kSlotsFit < kMaxASlots ? kSlotsFit : kMaxASlots;
@@ -153,7 +163,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // stage, in each CTA (used with a norm only).
     constexpr uint32_t kReadyCount = 2 * kGroupWarps;
     static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "UMMA N for M = 256");
-    static_assert((BN / 2) % 8 == 0, "B half tile rows");
+    static_assert((BN / 2) % 8 == 0, "B half tile rows (1024-byte swizzle atoms)");
+    static_assert(NSUB >= 1 && kAccBufs * kTW <= 512, "accumulators fit in tensor memory");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -230,23 +241,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             bool ok = true;
             for (int tile = cluster; ok && tile < num_tiles; tile += n_clusters) {
                 const int m0 = (tile % m_tiles) * 2 * kBM + static_cast<int>(rank) * kBM;
-                const int n0 = (tile / m_tiles) * BN + static_cast<int>(rank) * (BN / 2);
+                const int nt0 = (tile / m_tiles) * kTW;
+                const int n0 = nt0 + static_cast<int>(rank) * (BN / 2);
+                // Sub-tiles wholly past N are neither loaded nor multiplied.
+                const int n_sub = min(NSUB, (args.N - nt0 + BN - 1) / BN);
+                const uint32_t tx = stage_tx(n_sub);
                 for (int kb = 0; kb < k_blocks; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, wc)) { ok = false; break; }
                     const int kc = kb * kBK;
+                    uint8_t *sb = sB + stage * L::kB;
                     if constexpr (kNorm) {
                         // Each CTA normalizes its own stage: local barrier.
-                        mbar_arrive_expect_tx(&full[stage], kTx);
+                        mbar_arrive_expect_tx(&full[stage], tx);
                         tma_load_2d(sA + stage * L::kA, &args.map_a, &full[stage], kc, m0, pol_x);
-                        tma_load_2d(sB + stage * L::kB, &args.map_b, &full[stage], kc, n0, pol_w);
+                        for (int j = 0; j < n_sub; ++j)
+                            tma_load_2d(sb + j * L::kBSub, &args.map_b, &full[stage], kc, n0 + j * BN, pol_w);
                         tma_load_2d(sG + stage * 2 * kBK, &args.map_gb, &full[stage], kc, 0, pol_x);
                     } else {
                         // Both CTAs' copies complete on the leader's barrier,
                         // which expects the bytes of both.
                         const uint32_t fb = full_leader + 8u * static_cast<uint32_t>(stage);
-                        if (leader) mbar_arrive_expect_tx(&full[stage], 2 * kTx);
+                        if (leader) mbar_arrive_expect_tx(&full[stage], 2 * tx);
                         tma_load_2d_pair(sA + stage * L::kA, &args.map_a, fb, kc, m0, pol_x);
-                        tma_load_2d_pair(sB + stage * L::kB, &args.map_b, fb, kc, n0, pol_w);
+                        for (int j = 0; j < n_sub; ++j)
+                            tma_load_2d_pair(sb + j * L::kBSub, &args.map_b, fb, kc, n0 + j * BN, pol_w);
                     }
                     ++fills;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -278,7 +296,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (int tile = cluster; ok && tile < num_tiles; tile += n_clusters) {
                 if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, wc)) break;
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kTW);
+                const int n_sub = min(NSUB, (args.N - (tile / m_tiles) * kTW + BN - 1) / BN);
                 for (int kb = 0; kb < k_blocks; ++kb) {
                     if (!mbar_wait(kNorm ? &ready[stage] : &full[stage], phase, wc)) { ok = false; break; }
                     tc_fence_after();
@@ -298,9 +317,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         const uint32_t a_addr = smem_u32(sA + stage * L::kA);
 #pragma unroll
                         for (int k = 0; k < kBK / kUmmaK; ++k) {
-                            umma_f16_ss_pair(d_tmem, sdesc_kmajor_sw128(a_addr + k * 32),
-                                             sdesc_kmajor_sw128(b_addr + k * 32), kIdesc,
-                                             (kb | k) != 0 ? 1u : 0u);
+                            const uint64_t a_desc = sdesc_kmajor_sw128(a_addr + k * 32);
+#pragma unroll
+                            for (int j = 0; j < NSUB; ++j) {
+                                if (j < n_sub)
+                                    umma_f16_ss_pair(d_tmem + static_cast<uint32_t>(j * BN), a_desc,
+                                                     sdesc_kmajor_sw128(b_addr + j * L::kBSub + k * 32),
+                                                     kIdesc, (kb | k) != 0 ? 1u : 0u);
+                            }
                         }
                     }
                     umma_commit_pair(&empty[stage], 0x3);
@@ -342,11 +366,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             tc_fence_after();
             const int row = (tile % m_tiles) * 2 * kBM + static_cast<int>(rank) * kBM + q * 32 + lane;
             const float2 so = fold_row_scale<NORM>(args, row);
-            const int nt0 = (tile / m_tiles) * BN;
+            const int nt0 = (tile / m_tiles) * kTW;
             const uint32_t t_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                    static_cast<uint32_t>(acc * BN);
+                                    static_cast<uint32_t>(acc * kTW);
 #pragma unroll 1
-            for (int c = 0; c < BN; c += 32) {
+            for (int c = 0; c < kTW; c += 32) {
                 const int n0 = nt0 + c;
                 if (n0 >= N) break;  // uniform across the warp
                 uint32_t r[32];
@@ -375,11 +399,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
 }
 
-template <int NORM, bool SILU, bool BF16, int BN, int STAGES>
+template <int NORM, bool SILU, bool BF16, int BN, int STAGES, int NSUB>
 int launch_gemm2_variant(const GemmArgs &args, int grid, bool pdl, cudaStream_t stream)
 {
-    auto kern = gemm2_kernel<NORM, SILU, BF16, BN, STAGES>;
-    constexpr int smem = Gemm2Smem<BN, STAGES>::alloc;
+    auto kern = gemm2_kernel<NORM, SILU, BF16, BN, STAGES, NSUB>;
+    constexpr int smem = Gemm2Smem<BN, STAGES, NSUB>::alloc;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess)
         return record_cuda_error("cudaFuncSetAttribute(max dynamic smem)", e, cudaGetErrorString(e));
@@ -403,11 +427,11 @@ int launch_gemm2_variant(const GemmArgs &args, int grid, bool pdl, cudaStream_t 
 
 // How many CTA pairs of this kernel can be resident at once on the current
 // device (pairs must share a GPC, so this can be below SMs / 2).
-template <int BN, int STAGES>
+template <int BN, int STAGES, int NSUB>
 int gemm2_max_clusters()
 {
-    auto kern = gemm2_kernel<kNormNone, false, false, BN, STAGES>;
-    constexpr int smem = Gemm2Smem<BN, STAGES>::alloc;
+    auto kern = gemm2_kernel<kNormNone, false, false, BN, STAGES, NSUB>;
+    constexpr int smem = Gemm2Smem<BN, STAGES, NSUB>::alloc;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg = {};
@@ -426,13 +450,13 @@ int gemm2_max_clusters()
     return n;
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int NSUB>
 int launch_gemm2_bn(int norm, bool silu, bool bf16, const GemmArgs &args, int grid, bool pdl,
                     cudaStream_t stream)
 {
 #define NGR_CASE2(N_, S_, B_)                                                     \
     if (norm == N_ && silu == S_ && bf16 == B_)                                   \
-        return launch_gemm2_variant<N_, S_, B_, BN, STAGES>(args, grid, pdl, stream);
+        return launch_gemm2_variant<N_, S_, B_, BN, STAGES, NSUB>(args, grid, pdl, stream);
     NGR_CASE2(kNormLayer, false, false)
     NGR_CASE2(kNormLayer, false, true)
     NGR_CASE2(kNormRms, false, false)

@@ -88,7 +88,9 @@ struct GemmPlan {
     size_t smem;     // dynamic shared memory bytes
     bool pair;       // CTA-pair kernel (tcgen05 cta_group::2, 256-row tiles)
     int bm;          // rows per output tile: 128, or 256 for a CTA pair
-    int b_rows;      // rows of W each CTA loads per tile (BN, or BN / 2)
+    int b_rows;      // rows of W in one TMA box (BN, or BN / 2 for a CTA pair)
+    int nsub;        // N sub-tiles of BN columns per output tile (CTA pair: 1 or 2)
+    int tw;          // output tile width in N: bn * nsub
 };
 
 // Record why a CUDA call failed (thread-local; read back through
@@ -105,6 +107,7 @@ int launch_rowstats(int norm, bool bf16, const void *x, int64_t M, int64_t K,
 int launch_gemm(int norm, bool silu, bool bf16, const GemmPlan &plan,
                 const GemmArgs &args, bool pdl, cudaStream_t stream);
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, bool norm);
+int set_tile_config(int pair, int bn, int nsub);
 size_t gemm_smem_bytes(int bn, int stages, bool norm);
 
 int launch_decode(int norm, bool silu, bool bf16, int mn, const DecodeArgs &args,

@@ -165,7 +165,7 @@ extern "C" int ngr_fused_layernorm_linear_noalloc(const void *x, const void *gam
     a.N = static_cast<int>(N);
     a.K = static_cast<int>(K);
     a.m_tiles = static_cast<int>((M + plan.bm - 1) / plan.bm);
-    a.n_tiles = static_cast<int>((N + plan.bn - 1) / plan.bn);
+    a.n_tiles = static_cast<int>((N + plan.tw - 1) / plan.tw);
     a.k_blocks = static_cast<int>((K + kBK - 1) / kBK);
     a.num_tiles = a.m_tiles * a.n_tiles;
     a.timeout_ns = 2000ull * 1000000ull;

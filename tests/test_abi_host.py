@@ -117,3 +117,16 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(B, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not found"):
         B.lib()
+
+
+def test_set_tile_config_arguments(lib):
+    ok = [(-1, 0, 0), (0, 128, 0), (1, 224, 2), (1, 0, 2), (-1, 256, 1)]
+    bad = [(2, 0, 0), (-2, 0, 0), (1, 100, 0), (1, 192, 2), (0, 0, 2), (-1, 0, 3),
+           (-1, 0, -1)]
+    try:
+        for a in ok:
+            assert B.ngr_set_tile_config(*a) == 0, a
+        for a in bad:
+            assert B.ngr_set_tile_config(*a) == -9, a
+    finally:
+        assert B.ngr_set_tile_config(-1, 0, 0) == 0

@@ -1,0 +1,110 @@
+"""GPU parity of every tile-kernel variant the planner can choose, each
+forced through ngr_set_tile_config, against the fp64 oracle on the same
+seeded inputs: the single-CTA kernel (128-row tiles), the CTA-pair kernel
+(256-row tiles, one N sub-tile, two accumulators) and its two-sub-tile form
+(256 x 2 BN tiles sharing each x stage, one accumulator).
+
+The shapes span several tiles in M, N and K with ragged tails everywhere:
+M = 600 is two full 256-row pair tiles plus 88 rows; K = 1000 ends in a
+40-column k block; N = 1000 leaves a last two-sub-tile tile whose second
+sub-tile lies wholly past N (skipped) and whose first holds 104 columns, so
+that the second CTA's half of it is wholly past N as well.
+
+Bar: |y - y_ref| <= 1e-2 + 1e-2 |y_ref| (fp16/bf16 output, FP32 statistics
+and accumulation), every element.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import normalization_gemm_row_gb300 as ngr
+from normalization_gemm_row_gb300 import binding as B
+from normalization_gemm_row_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL = 1e-2, 1e-2
+
+# (pair, bn, nsub) as ngr_set_tile_config takes them.
+CONFIGS = [(0, 128, 1), (0, 192, 1), (0, 224, 1), (0, 256, 1),
+           (1, 128, 1), (1, 192, 1), (1, 224, 1), (1, 256, 1),
+           (1, 224, 2), (1, 256, 2)]
+IDS = [f"{'pair' if p else 'single'}-bn{bn}x{ns}" for p, bn, ns in CONFIGS]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ngr.build()
+    oracle.build()
+    torch.cuda.init()
+    yield
+    B.set_tile_config(-1, 0, 0)
+
+
+@pytest.fixture(params=CONFIGS, ids=IDS)
+def tile_config(request):
+    pair, bn, nsub = request.param
+    B.set_tile_config(pair, bn, nsub)
+    yield request.param
+    B.set_tile_config(-1, 0, 0)
+
+
+def to_dev(d):
+    return {k: (v.cuda() if isinstance(v, torch.Tensor) and k != "outlier_rows" else v)
+            for k, v in d.items()}
+
+
+def check(got, ref, what):
+    got = got.double().cpu().numpy()
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    err = np.abs(got - ref)
+    bad = err > ATOL + RTOL * np.abs(ref)
+    assert not bad.any(), (f"{what}: {bad.sum()} / {bad.size} out of tolerance, max err "
+                           f"{err.max():.4e} at {np.unravel_index(err.argmax(), err.shape)}")
+
+
+M, K, N = 600, 1000, 1000
+
+
+def test_layernorm_f16_bias(tile_config):
+    d = inputs.case("layernorm_linear", M, K, N, torch.float16, True, 1e-5, seed=11, x_mean=2.0)
+    g = to_dev(d)
+    y = ngr.fused_layernorm_linear(g["x"], g["gamma"], g["beta"], g["W"], g["bias"], 1e-5)
+    torch.cuda.synchronize()
+    check(y, oracle.layernorm_linear(d["x"], d["gamma"], d["beta"], d["W"], d["bias"], 1e-5),
+          f"LN {tile_config}")
+
+
+def test_rmsnorm_bf16(tile_config):
+    d = inputs.case("rmsnorm_linear", M, K, N + 480, torch.bfloat16, False, 1e-6, seed=12)
+    g = to_dev(d)
+    y = ngr.fused_rmsnorm_linear(g["x"], g["gamma"], g["W"], None, 1e-6)
+    torch.cuda.synchronize()
+    check(y, oracle.rmsnorm_linear(d["x"], d["gamma"], d["W"], None, 1e-6), f"RMS {tile_config}")
+
+
+def test_linear_silu_f16(tile_config):
+    d = inputs.case("linear_silu", M, K, N, torch.float16, True, 0.0, seed=13)
+    g = to_dev(d)
+    y = ngr.fused_linear_silu(g["x"], g["W"], g["bias"])
+    torch.cuda.synchronize()
+    check(y, oracle.linear_silu(d["x"], d["W"], d["bias"]), f"SiLU {tile_config}")
+
+
+def test_folded_layernorm_bf16(tile_config):
+    d = inputs.case("layernorm_linear", M, K, N, torch.bfloat16, True, 1e-5, seed=14, x_mean=3.0)
+    g = to_dev(d)
+    Wf, cb = B.fold_prepare(oracle.NORM_LAYER, g["gamma"], g["beta"], g["W"], g["bias"])
+    y = B.fused_norm_linear_folded(oracle.NORM_LAYER, g["x"], Wf, cb, 1e-5)
+    torch.cuda.synchronize()
+    check(y, oracle.layernorm_linear(d["x"], d["gamma"], d["beta"], d["W"], d["bias"], 1e-5),
+          f"folded LN {tile_config}")
+
+
+def test_ffn_f16(tile_config):
+    d = inputs.case("ffn", 300, 512, 1000, torch.float16, False, 0.0, seed=15)
+    g = to_dev(d)
+    y = ngr.ffn_linear_silu_linear(g["x"], g["W1"], g["W2"])
+    torch.cuda.synchronize()
+    check(y, oracle.ffn(d["x"], d["W1"], d["W2"]), f"FFN {tile_config}")
