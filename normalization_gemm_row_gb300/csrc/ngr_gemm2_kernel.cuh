@@ -24,28 +24,32 @@
 //                  arrives once its CTA's stage is normalized;
 //   empty[s]       the leader's tcgen05.commit, multicast to both CTAs;
 //   acc_full[a]    the leader's commit at the end of a tile, multicast;
-//   acc_empty[a]   leader: each epilogue warp of both CTAs arrives after
-//                  draining its rows of accumulator a.
+//   acc_empty[a]   leader: each draining warp of both CTAs arrives after
+//                  reading its share of accumulator a.
+//
+// Draining an accumulator: epilogue warps 12-15 drain every tile.  Without
+// a norm the transform warps 4-11 have no other work and drain with them
+// (three warps per tensor-memory lane quarter, each taking every third
+// 32-column chunk); with a norm they join only on the cluster's last tile,
+// when no stage is left to normalize, so that the tail is short.
 #pragma once
 
 #include "ngr_gemm_kernel.cuh"
 
 namespace ngr {
 
-// Tensor-memory columns of one slot of the normalized A operand (K = 64 as
-// 32 packed pairs).  With a norm the kernel keeps one accumulator and gives
-// the rest of the 512 columns to up to 8 A slots, so that the transform can
-// run several k blocks ahead of the MMA; the epilogue (about 3 % of a tile)
-// then does not overlap the next tile's main loop.
-constexpr int kASlotCols = kBK / 2;
-constexpr int kMaxASlots = 8;
-
-// Where the normalized A operand lives in the CTA-pair kernel: 1 = tensor
-// memory (written with tcgen05.st by row-owning threads), 0 = shared memory
-// (normalized in place, like the single-CTA kernel).
+// Where the normalized A operand lives in the CTA-pair kernel with a norm:
+// 1 = tensor memory (written with tcgen05.st by row-owning threads; the
+// MMAs read it from there), 0 = shared memory (normalized in place, like
+// the single-CTA kernel).  One switch for one-sub-tile tiles, one for
+// two-sub-tile tiles.
 #ifndef NGR_PAIR_A_TMEM
 #define NGR_PAIR_A_TMEM 0
 #endif
+#ifndef NGR_PAIR_A_TMEM_WIDE
+#define NGR_PAIR_A_TMEM_WIDE 0
+#endif
+constexpr int kMaxASlots = 8;
 
 template <int BN, int STAGES, int NSUB>
 struct Gemm2Smem {
@@ -65,25 +69,34 @@ struct Gemm2Smem {
 
 
 // The transform role of the CTA-pair kernel with A in tensor memory.
-// Transform thread t belongs to group g = t / kGroupThreads, which handles
-// the k blocks with running index it % groups == g; k block `it` uses A slot
-// it % SLOTS, free once the MMAs of k block it - SLOTS have completed.  Each warp of a group covers the
-// tensor-memory lane quarter warp % 4, and each lane one row: it reads its
-// row's 64 raw x values from the swizzled shared-memory stage, normalizes
-// them in FP32, packs them to 16-bit pairs and stores the 32 columns with
-// tcgen05.st.  The shared-memory stage is only read.
-template <int NORM, bool BF16, int STAGES, int KA, int SLOTS, typename M0Fn, typename ArriveFn>
+// A slot holds SLOT_K of a k block's 64 columns (SLOT_K / 2 tensor-memory
+// columns of packed 16-bit pairs); a k block fills HALVES = 64 / SLOT_K
+// slots, the j-th of the running sequence going to slot j % SLOTS, which is
+// free once the MMAs that read its previous contents have completed
+// (a_free, committed by the MMA issuer to both CTAs).  With one slot per k
+// block, transform group g takes the k blocks with running index
+// it % groups == g; with two, group h fills slot half h of every k block.
+// Each warp covers the tensor-memory lane quarter warp % 4, and each lane
+// one row: it reads its row's raw x chunks from the swizzled shared-memory
+// stage (only read), normalizes them in FP32, packs them to 16-bit pairs
+// and stores them with tcgen05.st.
+template <int NORM, bool BF16, int STAGES, int KA, int SLOTS, int HALVES, typename M0Fn,
+          typename ArriveFn>
 __device__ __forceinline__ void transform_role_tmem(
     int t, int tile0, int tile_step, int num_tiles, int k_blocks, int M, const float2 *stats,
     const uint8_t *sA, const float *sG, uint64_t *full, uint64_t *a_free, uint32_t tmem_base,
     uint32_t a_col0, const WaitCtx &wc, M0Fn m0_of, ArriveFn arrive)
 {
+    constexpr int kChunks = 8 / HALVES;   // 16-byte chunks of a row per slot
+    constexpr int kCols = kChunks * 4;    // tensor-memory columns per slot
     static_assert(KA > 0 && kGroupThreads == 128, "a group must cover the four lane quarters");
+    static_assert(HALVES == 1 || (HALVES == 2 && kTransformGroups == 2), "one group per slot half");
     const int g = t / kGroupThreads;
     const int lane = threadIdx.x & 31;
     const int q = (threadIdx.x >> 5) & 3;   // lane quarter this warp may access
     const int r = q * 32 + lane;            // row of the 128-row tile
     const int sw = r & 7;
+    const int h = HALVES > 1 ? g : 0;       // slot half this thread fills
     const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + a_col0;
     pdl_wait();
     int stage = 0;
@@ -95,17 +108,19 @@ __device__ __forceinline__ void transform_role_tmem(
         if (row < M) st = stats[row];
         const float2 so = make_float2(st.y, -st.x * st.y);
         for (int kb = 0; kb < k_blocks; ++kb, ++it) {
-            if (it % kTransformGroups == g) {
+            if (HALVES > 1 || it % kTransformGroups == g) {
                 if (!mbar_wait_warp(&full[stage], phase, wc)) return;
-                const int slot = it % SLOTS;
-                const int use = it / SLOTS;
+                const int sidx = it * HALVES + h;
+                const int slot = sidx % SLOTS;
+                const int use = sidx / SLOTS;
                 if (use > 0 && !mbar_wait_warp(&a_free[slot], (use - 1) & 1, wc)) return;
                 tc_fence_after();
                 const uint8_t *xrow = sA + stage * KA + r * 128;
                 const float *gs = sG + stage * 2 * kBK;
-                uint32_t packed[32];
+                uint32_t packed[kCols];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
+                for (int c0 = 0; c0 < kChunks; ++c0) {
+                    const int c = h * kChunks + c0;
                     const uint4 v = *reinterpret_cast<const uint4 *>(xrow + ((c ^ sw) << 4));
                     const float4 g0 = *reinterpret_cast<const float4 *>(gs + 8 * c);
                     const float4 g1 = *reinterpret_cast<const float4 *>(gs + 8 * c + 4);
@@ -121,12 +136,14 @@ __device__ __forceinline__ void transform_role_tmem(
                         bb[3] = make_float2(b1.z, b1.w);
                     }
                     const uint4 o = transform8_pk<NORM, BF16>(v, so, gg, bb);
-                    packed[4 * c + 0] = o.x;
-                    packed[4 * c + 1] = o.y;
-                    packed[4 * c + 2] = o.z;
-                    packed[4 * c + 3] = o.w;
+                    packed[4 * c0 + 0] = o.x;
+                    packed[4 * c0 + 1] = o.y;
+                    packed[4 * c0 + 2] = o.z;
+                    packed[4 * c0 + 3] = o.w;
                 }
-                tmem_st32(tbase + static_cast<uint32_t>(slot * kASlotCols), packed);
+                const uint32_t taddr = tbase + static_cast<uint32_t>(slot * kCols);
+                if constexpr (kCols == 32) tmem_st32(taddr, packed);
+                else tmem_st16(taddr, packed);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
@@ -149,22 +166,34 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         return static_cast<uint32_t>(L::kA + n_sub * L::kBSub + (kNorm ? L::kGB : 0));
     };
     // Accumulators (two of kTW columns when they fit and A is not in tensor
-    // memory, else one), then the A slots.
-    constexpr bool kATmem = kNorm && NGR_PAIR_A_TMEM && NSUB == 1;
+    // memory, else one), then the A slots: a whole k block per slot with one
+    // sub-tile, half a k block with two (only 64 columns are left beside a
+    // 448-column accumulator).
+    constexpr uint32_t kTmemCols = 512;
+    constexpr int kSlotK = NSUB > 1 ? 32 : kBK;        // K columns of x per A slot
+    constexpr int kHalvesA = kBK / kSlotK;             // A slots per k block
+    constexpr int kSlotCols = kSlotK / 2;              // tensor-memory columns per slot
+    // (A in tensor memory needs at least two k blocks' slots beside one
+    // accumulator: not with a 512-column tile.)
+    constexpr bool kATmem = kNorm && (NSUB > 1 ? NGR_PAIR_A_TMEM_WIDE : NGR_PAIR_A_TMEM) &&
+                            static_cast<int>(kTmemCols) - kTW >= 2 * kHalvesA * kSlotCols;
     constexpr int kAccBufs = (kATmem || NSUB > 1) ? 1 : 2;
     constexpr uint32_t kACol0 = kAccBufs * kTW;
-    constexpr uint32_t kTmemCols = 512;
-    constexpr int kSlotsFit = static_cast<int>((kTmemCols - kACol0) / kASlotCols);
+    constexpr int kSlotsFit = static_cast<int>((kTmemCols - kACol0) / kSlotCols);
     constexpr int kASlots = kSlotsFit < kMaxASlots ? kSlotsFit : kMaxASlots;
-    static_assert(!kATmem || (kASlots >= 2 && kASlots % kTransformGroups == 0),
+    static_assert(!kATmem || (kASlots >= 2 * kHalvesA && kASlots % (kHalvesA * kTransformGroups) == 0),
                   "tensor memory: accumulator + A slots");
     constexpr uint32_t kIdesc = idesc_f16(BF16, 2 * kBM, BN);
-    // ready[s] arrivals: one per warp of the transform group that owns the
-    // stage, in each CTA (used with a norm only).
-    constexpr uint32_t kReadyCount = 2 * kGroupWarps;
+    // ready[s] arrivals: one per warp of each transform group that works on
+    // the stage, in each CTA (used with a norm only).
+    constexpr uint32_t kReadyCount = 2 * kGroupWarps * (kATmem ? kHalvesA : 1);
     static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "UMMA N for M = 256");
     static_assert((BN / 2) % 8 == 0, "B half tile rows (1024-byte swizzle atoms)");
     static_assert(NSUB >= 1 && kAccBufs * kTW <= 512, "accumulators fit in tensor memory");
+    // Warps per CTA that drain every accumulator (and arrive on acc_empty).
+    constexpr bool kHelpAlways = !kNorm;
+    constexpr bool kHelpLast = kNorm;
+    constexpr int kDrainWarps = kHelpAlways ? 12 : 4;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -202,7 +231,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&acc_full[a], 1);
-            mbar_init(&acc_empty[a], 2 * 4);
+            mbar_init(&acc_empty[a], 2 * kDrainWarps);
         }
         mbar_init(drain, 1);
         for (int j = 0; j < kMaxASlots; ++j) mbar_init(&a_free[j], 1);
@@ -303,16 +332,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     tc_fence_after();
                     const uint32_t b_addr = smem_u32(sB + stage * L::kB);
                     if constexpr (kATmem) {
-                        const int slot = it % kASlots;
-                        const uint32_t a_tmem = tmem_base + kACol0 +
-                                                static_cast<uint32_t>(slot * kASlotCols);
 #pragma unroll
-                        for (int k = 0; k < kBK / kUmmaK; ++k) {
-                            umma_f16_ts_pair(d_tmem, a_tmem + static_cast<uint32_t>(k * (kUmmaK / 2)),
-                                             sdesc_kmajor_sw128(b_addr + k * 32), kIdesc,
-                                             (kb | k) != 0 ? 1u : 0u);
+                        for (int hh = 0; hh < kHalvesA; ++hh) {
+                            const int slot = (it * kHalvesA + hh) % kASlots;
+                            const uint32_t a_tmem = tmem_base + kACol0 +
+                                                    static_cast<uint32_t>(slot * kSlotCols);
+#pragma unroll
+                            for (int k = 0; k < kSlotK / kUmmaK; ++k) {
+                                const int kk = hh * (kSlotK / kUmmaK) + k;   // K step in the block
+#pragma unroll
+                                for (int j = 0; j < NSUB; ++j) {
+                                    if (j < n_sub)
+                                        umma_f16_ts_pair(d_tmem + static_cast<uint32_t>(j * BN),
+                                                         a_tmem + static_cast<uint32_t>(k * (kUmmaK / 2)),
+                                                         sdesc_kmajor_sw128(b_addr + j * L::kBSub + kk * 32),
+                                                         kIdesc, (kb | kk) != 0 ? 1u : 0u);
+                                }
+                            }
+                            umma_commit_pair(&a_free[slot], 0x3);
                         }
-                        umma_commit_pair(&a_free[slot], 0x3);
                     } else {
                         const uint32_t a_addr = smem_u32(sA + stage * L::kA);
 #pragma unroll
@@ -338,53 +376,79 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             umma_commit_pair(drain, 0x1);
             mbar_wait(drain, 0, wc);
         }
-    } else if (warp >= kTransformWarp0 && warp < kEpilogueWarp0) {
-        const int t = threadIdx.x - kTransformWarp0 * 32;
-        if constexpr (kATmem) {
-            // ------------------------------------------ transform (A -> TMEM)
-            transform_role_tmem<NORM, BF16, STAGES, L::kA, kASlots>(
-                t, cluster, n_clusters, num_tiles, k_blocks, args.M, args.stats, sA, sG, full,
-                a_free, tmem_base, kACol0, wc,
-                [&](int tile) { return (tile % m_tiles) * 2 * kBM + static_cast<int>(rank) * kBM; },
-                [&](int st) { mbar_arrive_cluster(ready_leader + 8u * static_cast<uint32_t>(st)); });
-        } else if constexpr (kNorm) {
-            // ----------------------------------------- transform (A in place)
-            transform_role<NORM, BF16, STAGES, L::kA>(
-                t, cluster, n_clusters, num_tiles, k_blocks, args.M, args.stats, sA, sG, full, wc,
-                [&](int tile) { return (tile % m_tiles) * 2 * kBM + static_cast<int>(rank) * kBM; },
-                [&](int st) { mbar_arrive_cluster(ready_leader + 8u * static_cast<uint32_t>(st)); });
-        }
-    } else if (warp >= kEpilogueWarp0) {
-        // --------------------------------------------------------- epilogue
-        const int q = warp & 3;
-        int acc = 0;
-        uint32_t acc_phase = 0;
-        const int N = args.N;
-        if constexpr (is_fold(NORM)) pdl_wait();  // row statistics from the previous grid
-        for (int tile = cluster; tile < num_tiles; tile += n_clusters) {
-            if (!mbar_wait_warp(&acc_full[acc], acc_phase, wc)) break;
-            tc_fence_after();
-            const int row = (tile % m_tiles) * 2 * kBM + static_cast<int>(rank) * kBM + q * 32 + lane;
-            const float2 so = fold_row_scale<NORM>(args, row);
-            const int nt0 = (tile / m_tiles) * kTW;
-            const uint32_t t_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                    static_cast<uint32_t>(acc * kTW);
-#pragma unroll 1
-            for (int c = 0; c < kTW; c += 32) {
-                const int n0 = nt0 + c;
-                if (n0 >= N) break;  // uniform across the warp
-                uint32_t r[32];
-                tmem_ld32(t_base + static_cast<uint32_t>(c), r);
-                tmem_ld_wait();
-                float v[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                epilogue_store32<NORM, SILU, BF16>(v, row, n0, args, so);
+    } else if (warp >= kTransformWarp0) {
+        const bool epi_warp = warp >= kEpilogueWarp0;
+        if (!epi_warp) {
+            const int t = threadIdx.x - kTransformWarp0 * 32;
+            if constexpr (kATmem) {
+                // ------------------------------------------ transform (A -> TMEM)
+                transform_role_tmem<NORM, BF16, STAGES, L::kA, kASlots, kHalvesA>(
+                    t, cluster, n_clusters, num_tiles, k_blocks, args.M, args.stats, sA, sG, full,
+                    a_free, tmem_base, kACol0, wc,
+                    [&](int tile) { return (tile % m_tiles) * 2 * kBM + static_cast<int>(rank) * kBM; },
+                    [&](int st) { mbar_arrive_cluster(ready_leader + 8u * static_cast<uint32_t>(st)); });
+            } else if constexpr (kNorm) {
+                // ----------------------------------------- transform (A in place)
+                transform_role<NORM, BF16, STAGES, L::kA>(
+                    t, cluster, n_clusters, num_tiles, k_blocks, args.M, args.stats, sA, sG, full, wc,
+                    [&](int tile) { return (tile % m_tiles) * 2 * kBM + static_cast<int>(rank) * kBM; },
+                    [&](int st) { mbar_arrive_cluster(ready_leader + 8u * static_cast<uint32_t>(st)); });
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(acc_empty_leader + 8u * static_cast<uint32_t>(acc));
-            if (++acc == kAccBufs) { acc = 0; acc_phase ^= 1u; }
+        }
+        if (epi_warp || kHelpAlways || kHelpLast) {
+            // ----------------------------------------------------- epilogue
+            const int q = warp & 3;                 // tensor-memory lane quarter
+            const int e = epi_warp ? 0 : 1 + (warp - kTransformWarp0) / 4;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            const int N = args.N;
+            if constexpr (is_fold(NORM)) pdl_wait();  // row statistics from the previous grid
+            for (int tile = cluster; tile < num_tiles; tile += n_clusters) {
+                const int cur = acc;
+                const uint32_t cur_phase = acc_phase;
+                if (++acc == kAccBufs) { acc = 0; acc_phase ^= 1u; }
+                const bool helped = kHelpAlways || (kHelpLast && tile + n_clusters >= num_tiles);
+                if (!epi_warp && !helped) continue;
+                const int step = (helped ? 3 : 1) * 32;
+                const int nt0 = (tile / m_tiles) * kTW;
+                const int ncols = min(kTW, N - nt0);
+                // Warm L1 with this warp's epilogue vectors while the MMAs run.
+                for (int c = e * 32; c < ncols; c += step) {
+                    if constexpr (is_fold(NORM)) {
+                        if (lane == 0) prefetch_l1(args.fold_b + nt0 + c);
+                        if (NORM == kNormFoldLayer && lane == 1) prefetch_l1(args.fold_c + nt0 + c);
+                    } else {
+                        if (lane == 0 && args.bias)
+                            prefetch_l1(static_cast<const uint16_t *>(args.bias) + nt0 + c);
+                    }
+                }
+                if (!mbar_wait_warp(&acc_full[cur], cur_phase, wc)) break;
+                tc_fence_after();
+                const int row = (tile % m_tiles) * 2 * kBM + static_cast<int>(rank) * kBM + q * 32 + lane;
+                const float2 so = fold_row_scale<NORM>(args, row);
+                const uint32_t t_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                        static_cast<uint32_t>(cur * kTW);
+                // The load of the next chunk is in flight while this one is
+                // finished and stored.
+                uint32_t r[32];
+                int c = e * 32;
+                if (c < ncols) tmem_ld32(t_base + static_cast<uint32_t>(c), r);
+#pragma unroll 1
+                while (c < ncols) {
+                    tmem_ld_wait();
+                    float v[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                    const int cn = c + step;
+                    if (cn < ncols) tmem_ld32(t_base + static_cast<uint32_t>(cn), r);
+                    epilogue_store32<NORM, SILU, BF16>(v, row, nt0 + c, args, so);
+                    c = cn;
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (epi_warp || kHelpAlways)
+                    if (lane == 0) mbar_arrive_cluster(acc_empty_leader + 8u * static_cast<uint32_t>(cur));
+            }
         }
     }
 

@@ -64,8 +64,12 @@ constexpr int kStatsThreads = 256;
 
 // One CTA per row (grid-stride over rows): every thread issues all of its
 // 16-byte loads of the row at once, so a row costs one memory round trip.
+// At most 32 registers, so that 8 CTAs (2048 threads) fit on an SM and the
+// rows of a batch of up to 8 x SMs run in a single wave.
+constexpr int kStatsCtasPerSm = 8;
+
 template <int NORM, bool BF16>
-__global__ void __launch_bounds__(kStatsThreads) rowstats_kernel(
+__global__ void __launch_bounds__(kStatsThreads, kStatsCtasPerSm) rowstats_kernel(
     const uint4 *__restrict__ x, int64_t M, int64_t K, float eps,
     float2 *__restrict__ stats, const void *__restrict__ gamma,
     const void *__restrict__ beta, float *__restrict__ gamma_f,
@@ -196,7 +200,7 @@ int launch_rowstats(int norm, bool bf16, const void *x, int64_t M, int64_t K,
 {
     const int threads = kStatsThreads;
     int64_t blocks = M;
-    const int64_t cap = static_cast<int64_t>(num_sms) * 16;
+    const int64_t cap = static_cast<int64_t>(num_sms) * kStatsCtasPerSm;   // one wave
     if (blocks > cap) blocks = cap;
     const int64_t kblocks = (K + threads - 1) / threads;
     if (gamma_f && blocks < kblocks) blocks = kblocks < cap ? kblocks : cap;
