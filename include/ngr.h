@@ -4,8 +4,12 @@
  *
  * The library computes a LayerNorm or RMSNorm row reduction whose normalized
  * rows feed a dense matrix product directly, with a bias and/or SiLU
- * epilogue; the normalized activations exist only in on-chip memory and are
- * never written to device memory.
+ * epilogue.  For M > 32 the normalized activations exist only in on-chip
+ * memory and are never written to device memory.  For decode-sized batches
+ * (M <= 32) the statistics kernel writes them once into the workspace (at
+ * most 32 x K values, which stay in L2) and the weight-streaming kernel
+ * reads them there, instead of re-normalizing the same rows for every
+ * weight tile.
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -201,7 +205,7 @@ int ngr_debug_bounded_wait(void *workspace, uint32_t timeout_us,
  * decide, 0 the single-CTA kernel (128-row tiles), 1 the CTA-pair kernel
  * (256-row tiles; only taken when M > 128).  `bn`: 0 any, else the N tile
  * (or sub-tile) width, one of 128, 192, 224, 256.  `nsub`: 0 any, else the
- * N sub-tiles per CTA-pair tile, 1 or 2 (2 only with bn 224 or 256).  The
+ * N sub-tiles per CTA-pair tile, 1 or 2 (2 only with bn 192, 224 or 256).  The
  * planner picks the cheapest variant that satisfies all three; if none does
  * it ignores the restriction.  ngr_set_tile_config(-1, 0, 0) restores the
  * default.  The environment variables NGR_PAIR, NGR_BN and NGR_NSUB give

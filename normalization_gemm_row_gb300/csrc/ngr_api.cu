@@ -65,7 +65,7 @@ constexpr int kMaxDevices = 64;
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
 struct WsLayout {
-    size_t stats = 0, gamma_f = 0, beta_f = 0;
+    size_t stats = 0, gamma_f = 0, beta_f = 0, xhat = 0;
     size_t partials = 0, counters = 0, counters2 = 0, h = 0;
     size_t total = 0;
 };
@@ -73,7 +73,8 @@ struct WsLayout {
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // Workspace regions, in order: header | stats | gamma_f | beta_f |
-// decode partials | counters | counters of the FFN's second GEMM | H.
+// normalized rows (decode sizes) | decode partials | counters | counters of
+// the FFN's second GEMM | H.
 WsLayout ws_layout(int op, int64_t M, int64_t K, int64_t N, bool h_in_ws)
 {
     WsLayout L;
@@ -86,6 +87,10 @@ WsLayout ws_layout(int op, int64_t M, int64_t K, int64_t N, bool h_in_ws)
         off += align256(static_cast<size_t>(K) * 4);
         L.beta_f = off;
         off += align256(static_cast<size_t>(K) * 4);
+        if (M > 0 && M <= kDecodeMaxM) {
+            L.xhat = off;
+            off += align256(static_cast<size_t>(M) * static_cast<size_t>(K) * 2);
+        }
     }
     if (M > 0 && M <= kDecodeMaxM) {
         const int64_t mn = M <= 16 ? 16 : 32;
@@ -374,13 +379,19 @@ int norm_linear(int op, int norm, bool silu, const void *x, const void *gamma, c
                                                 : (norm == kNormRms ? reinterpret_cast<float *>(w + L.beta_f) : nullptr),
                              decode ? reinterpret_cast<int *>(w + L.counters) : nullptr,
                              decode ? static_cast<int>(ceil_div(N, 128) * 4) : 0,
-                             reinterpret_cast<int *>(w), di.sms, stream);
+                             reinterpret_cast<int *>(w), di.sms, stream,
+                             decode && norm != kNormNone ? w + L.xhat : nullptr);
         event_after(stream);
         if (rc != NGR_OK) return rc;
     }
     event_before(stream);
-    rc = launch_layer(norm, silu, bf16, x, W, bias, M, K, N, y, w, L, L.counters, need_stats, di,
-                      stream);
+    // Decode sizes multiply the normalized rows the statistics kernel wrote.
+    if (decode && norm != kNormNone)
+        rc = launch_layer(kNormNone, silu, bf16, w + L.xhat, W, bias, M, K, N, y, w, L, L.counters,
+                          true, di, stream);
+    else
+        rc = launch_layer(norm, silu, bf16, x, W, bias, M, K, N, y, w, L, L.counters, need_stats,
+                          di, stream);
     event_after(stream);
     events_call_done();
     return finish(rc, ws, stream);

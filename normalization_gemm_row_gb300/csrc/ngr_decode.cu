@@ -12,8 +12,12 @@
 //    per SM as one contiguous run each, so every SM streams the same number
 //    of weight bytes without a tail wave; a run that covers part of a weight
 //    tile leaves an FP32 partial of that tile (split-K);
-//  - the tokens' k slice is normalized in place in shared memory by the
-//    transform warps exactly as in the tile kernel (never written to HBM);
+//  - the tokens arrive already normalized: at these sizes the statistics
+//    kernel writes the normalized rows once (at most 32 x K 16-bit values,
+//    which stay in L2), computed exactly as the tile kernel's transform
+//    does, instead of every weight tile re-normalizing the same k slice on
+//    the weight stream's critical path; with a folded weight the raw rows
+//    are used and the statistics are applied in the epilogue;
 //  - each epilogue warp owns 32 weight rows: it writes its partial, and the
 //    last of the CTAs sharing a tile (an atomic counter per 32-row slice)
 //    sums the partials in a fixed order (deterministic), adds the bias,
@@ -31,11 +35,9 @@ template <int MN, int STAGES>
 struct DecodeSmem {
     static constexpr int kW = 128 * kBK * 2;   // 16 KB weight tile
     static constexpr int kX = MN * kBK * 2;    // MN x 128 B token tile
-    static constexpr int kGB = 2 * kBK * 4;    // FP32 gamma[64] then beta[64]
     static constexpr int off_w = 0;
     static constexpr int off_x = off_w + STAGES * kW;
-    static constexpr int off_g = off_x + STAGES * kX;
-    static constexpr int off_bar = off_g + STAGES * kGB;
+    static constexpr int off_bar = off_x + STAGES * kX;
     static constexpr int n_bars = 3 * STAGES + 5;
     static constexpr int off_tmem = off_bar + n_bars * 8;
     static constexpr int bytes = off_tmem + 16;
@@ -55,8 +57,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     decode_kernel(const __grid_constant__ DecodeArgs args)
 {
     using L = DecodeSmem<MN, STAGES>;
-    constexpr bool kNorm = NORM == kNormLayer || NORM == kNormRms;  // transform stage
-    constexpr uint32_t kTx = L::kW + L::kX + (kNorm ? L::kGB : 0);
+    static_assert(NORM == kNormNone || is_fold(NORM), "tokens arrive normalized or the weight is folded");
+    constexpr uint32_t kTx = L::kW + L::kX;
     constexpr uint32_t kTmemCols = 2 * MN <= 32 ? 32 : 64;
     constexpr uint32_t kIdesc = idesc_f16(BF16, 128, MN);
     static_assert(MN == 16 || MN == 32, "token tile");
@@ -66,11 +68,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *sW = smem + L::off_w;
     uint8_t *sX = smem + L::off_x;
-    float *sG = reinterpret_cast<float *>(smem + L::off_g);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::off_bar);
     uint64_t *full = bars;
     uint64_t *empty = bars + STAGES;
-    uint64_t *ready = bars + 2 * STAGES;
     uint64_t *acc_full = bars + 3 * STAGES;
     uint64_t *acc_empty = bars + 3 * STAGES + 2;
     uint64_t *drain = bars + 3 * STAGES + 4;
@@ -87,11 +87,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         if (args.zero_err && blockIdx.x == 0) *args.err = 0;
         prefetch_tmap(&args.map_w);
         prefetch_tmap(&args.map_x);
-        if constexpr (kNorm) prefetch_tmap(&args.map_gb);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
-            mbar_init(&ready[s], 128);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&acc_full[a], 1);
@@ -132,8 +130,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                 mbar_arrive_expect_tx(&full[stage], kTx);
                 tma_load_2d(sW + stage * L::kW, &args.map_w, &full[stage], kc, tile * 128, pol_w);
                 tma_load_2d(sX + stage * L::kX, &args.map_x, &full[stage], kc, 0, pol_x);
-                if constexpr (kNorm)
-                    tma_load_2d(sG + stage * 2 * kBK, &args.map_gb, &full[stage], kc, 0, pol_x);
                 ++fills;
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
@@ -163,9 +159,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                 bool first = true;
                 for (; u < seg_end; ++u) {
                     if (!mbar_wait(&full[stage], phase, wc)) { ok = false; break; }
-                    if constexpr (kNorm) {
-                        if (!mbar_wait(&ready[stage], phase, wc)) { ok = false; break; }
-                    }
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(sW + stage * L::kW);
                     const uint32_t b_addr = smem_u32(sX + stage * L::kX);
@@ -185,41 +178,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             }
             umma_commit(drain);
             mbar_wait(drain, 0, wc);
-        }
-    } else if (warp >= 4 && warp < 8) {
-        if constexpr (kNorm) {
-            // ---------------------------------------------------- transform
-            // Thread t normalizes 16-byte chunk (t & 7) of token row t >> 3
-            // (and row 16 + (t >> 3) when MN = 32).
-            const int t = threadIdx.x - 128;
-            const int c = t & 7;
-            pdl_wait();
-            float sc[MN / 16], of[MN / 16];
-#pragma unroll
-            for (int h = 0; h < MN / 16; ++h) {
-                const int r = (t >> 3) + 16 * h;
-                float2 st = make_float2(0.f, 0.f);
-                if (r < args.M) st = args.stats[r];
-                sc[h] = st.y;
-                of[h] = -st.x * st.y;
-            }
-            int stage = 0;
-            uint32_t phase = 0;
-            for (long long u = u_begin; u < u_end; ++u) {
-                if (!mbar_wait_warp(&full[stage], phase, wc)) break;
-                const float *g = sG + stage * 2 * kBK + 8 * c;
-                const float *b = g + kBK;
-#pragma unroll
-                for (int h = 0; h < MN / 16; ++h) {
-                    const int r = (t >> 3) + 16 * h;
-                    uint4 *p = reinterpret_cast<uint4 *>(sX + stage * L::kX + r * 128 +
-                                                         ((c ^ (r & 7)) << 4));
-                    *p = transform8<NORM, BF16>(*p, sc[h], of[h], g, b);
-                }
-                fence_proxy_async_smem();
-                mbar_arrive(&ready[stage]);
-                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-            }
         }
     } else if (warp >= 8) {
         // --------------------------------------------------------- epilogue
@@ -373,10 +331,6 @@ int launch_decode(int norm, bool silu, bool bf16, int mn, const DecodeArgs &args
     if (norm == N_ && silu == S_ && bf16 == B_)                                   \
         return mn <= 16 ? launch_decode_variant<N_, S_, B_, 16>(args, pdl, stream) \
                         : launch_decode_variant<N_, S_, B_, 32>(args, pdl, stream);
-    NGR_DCASE(kNormLayer, false, false)
-    NGR_DCASE(kNormLayer, false, true)
-    NGR_DCASE(kNormRms, false, false)
-    NGR_DCASE(kNormRms, false, true)
     NGR_DCASE(kNormNone, true, false)
     NGR_DCASE(kNormNone, true, true)
     NGR_DCASE(kNormNone, false, false)

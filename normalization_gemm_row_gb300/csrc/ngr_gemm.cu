@@ -31,8 +31,10 @@ size_t gemm2_smem_bn192();
 size_t gemm2_smem_bn224();
 size_t gemm2_smem_bn256();
 int gemm2_max_clusters_bn224();
+int launch_gemm2w_bn192(int, bool, bool, const GemmArgs &, int, bool, cudaStream_t);
 int launch_gemm2w_bn224(int, bool, bool, const GemmArgs &, int, bool, cudaStream_t);
 int launch_gemm2w_bn256(int, bool, bool, const GemmArgs &, int, bool, cudaStream_t);
+size_t gemm2w_smem_bn192();
 size_t gemm2w_smem_bn224();
 size_t gemm2w_smem_bn256();
 
@@ -70,7 +72,7 @@ static int stages2_for(int bn)
 
 static size_t gemm2_smem_bytes(int bn, int nsub)
 {
-    if (nsub == 2) return bn == 224 ? gemm2w_smem_bn224() : gemm2w_smem_bn256();
+    if (nsub == 2) return bn == 192 ? gemm2w_smem_bn192() : bn == 224 ? gemm2w_smem_bn224() : gemm2w_smem_bn256();
     switch (bn) {
     case 128: return gemm2_smem_bn128();
     case 192: return gemm2_smem_bn192();
@@ -104,8 +106,8 @@ constexpr double kWideCostFactor = 0.7;
 constexpr int kWideTileOverhead = 32;
 
 // Stages of the two-sub-tile CTA-pair kernel for a sub-tile width.
-static int stages2w_for(int bn) { return bn == 224 ? 5 : 4; }
-static const int kWideWidths[] = {256, 224};
+static int stages2w_for(int bn) { return bn == 256 ? 4 : 5; }
+static const int kWideWidths[] = {256, 224, 192};
 
 // Tile-kernel restrictions (ngr_set_tile_config): pair -1/0/1, bn 0 or a
 // width, nsub 0/1/2.  Initialized from NGR_PAIR, NGR_BN and NGR_NSUB.
@@ -123,7 +125,7 @@ int set_tile_config(int pair, int bn, int nsub)
     if (pair < -1 || pair > 1) return -9;
     if (bn != 0 && bn != 128 && bn != 192 && bn != 224 && bn != 256) return -9;
     if (nsub < 0 || nsub > 2) return -9;
-    if (nsub == 2 && (pair == 0 || (bn != 0 && bn != 224 && bn != 256))) return -9;
+    if (nsub == 2 && (pair == 0 || (bn != 0 && bn != 192 && bn != 224 && bn != 256))) return -9;
     g_pair.store(pair);
     g_bn.store(bn);
     g_nsub.store(nsub);
@@ -192,6 +194,7 @@ int launch_gemm(int norm, bool silu, bool bf16, const GemmPlan &plan, const Gemm
 {
     if (plan.pair && plan.nsub == 2) {
         switch (plan.bn) {
+        case 192: return launch_gemm2w_bn192(norm, silu, bf16, args, plan.grid, pdl, stream);
         case 224: return launch_gemm2w_bn224(norm, silu, bf16, args, plan.grid, pdl, stream);
         case 256: return launch_gemm2w_bn256(norm, silu, bf16, args, plan.grid, pdl, stream);
         default: return -9;

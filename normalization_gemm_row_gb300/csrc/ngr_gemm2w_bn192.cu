@@ -1,0 +1,17 @@
+// ngr_gemm2w_bn192.cu -- CTA-pair tile kernel instantiations for a 256 x 384
+// output tile made of two 192-column sub-tiles that share each x stage
+// (5 pipeline stages, one accumulator).
+#include "ngr_gemm2_kernel.cuh"
+
+namespace ngr {
+
+int launch_gemm2w_bn192(int norm, bool silu, bool bf16, const GemmArgs &args, int grid,
+                       bool pdl, cudaStream_t stream)
+{
+    return launch_gemm2_bn<192, 5, 2>(norm, silu, bf16, args, grid, pdl, stream);
+}
+
+size_t gemm2w_smem_bn192() { return Gemm2Smem<192, 5, 2>::alloc; }
+int gemm2w_max_clusters_bn192() { return gemm2_max_clusters<192, 5, 2>(); }
+
+}  // namespace ngr

@@ -102,7 +102,7 @@ int launch_rowstats(int norm, bool bf16, const void *x, int64_t M, int64_t K,
                     float eps, float2 *stats, const void *gamma,
                     const void *beta, float *gamma_f, float *beta_f,
                     int *counters, int n_counters, int *err_to_clear,
-                    int num_sms, cudaStream_t stream);
+                    int num_sms, cudaStream_t stream, void *xhat = nullptr);
 
 int launch_gemm(int norm, bool silu, bool bf16, const GemmPlan &plan,
                 const GemmArgs &args, bool pdl, cudaStream_t stream);

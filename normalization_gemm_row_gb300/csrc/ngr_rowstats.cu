@@ -13,6 +13,11 @@
 // var = M2 / K (biased), rstd = 1 / sqrt(var + eps).  RMSNorm: rstd =
 // 1 / sqrt(sum x^2 / K + eps) and mu = 0.
 //
+// For decode-sized batches the kernel also writes the normalized rows
+// xhat = (x - mu) rstd gamma + beta (RMSNorm: x rstd gamma), with the FP32
+// arithmetic and the single rounding of the tile kernel's transform, so that
+// the weight-streaming kernel multiplies them without re-normalizing.
+//
 // The same launch converts gamma and beta to FP32 once per call (the GEMM's
 // producer streams them with the tiles) and zeroes the split-K tile counters
 // of the decode path when asked to, so that they start from zero every call;
@@ -46,6 +51,49 @@ __device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8])
     }
 }
 
+// Normalize 8 elements: a = (x rstd + (-mu rstd)) gamma + beta in FP32
+// (RMSNorm: (x rstd) gamma), one rounding to the 16-bit type.
+template <bool BF16>
+__device__ __forceinline__ float2 unpack_pair(uint32_t w)
+{
+    if constexpr (BF16)
+        return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w));
+    else
+        return __half22float2(*reinterpret_cast<const __half2 *>(&w));
+}
+
+template <int NORM, bool BF16>
+__device__ __forceinline__ uint4 normalize8(const uint4 &v, const uint4 &g, const uint4 &b,
+                                            float sc, float of)
+{
+    const uint32_t wx[4] = {v.x, v.y, v.z, v.w};
+    const uint32_t wg[4] = {g.x, g.y, g.z, g.w};
+    const uint32_t wb[4] = {b.x, b.y, b.z, b.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 fx = unpack_pair<BF16>(wx[i]);
+        const float2 fg = unpack_pair<BF16>(wg[i]);
+        float a0, a1;
+        if constexpr (NORM == kNormLayer) {
+            const float2 fb = unpack_pair<BF16>(wb[i]);
+            a0 = fmaf(fmaf(fx.x, sc, of), fg.x, fb.x);
+            a1 = fmaf(fmaf(fx.y, sc, of), fg.y, fb.y);
+        } else {
+            a0 = (fx.x * sc) * fg.x;
+            a1 = (fx.y * sc) * fg.y;
+        }
+        if constexpr (BF16) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(a0, a1);
+            o[i] = *reinterpret_cast<const uint32_t *>(&h);
+        } else {
+            const __half2 h = __floats2half2_rn(a0, a1);
+            o[i] = *reinterpret_cast<const uint32_t *>(&h);
+        }
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // Merge (nb, mb, m2b) into (n, mean, m2): the parallel-variance update.
 __device__ __forceinline__ void chan_merge(float &n, float &mean, float &m2, float nb, float mb,
                                            float m2b)
@@ -65,16 +113,17 @@ constexpr int kStatsThreads = 256;
 // One CTA per row (grid-stride over rows): every thread issues all of its
 // 16-byte loads of the row at once, so a row costs one memory round trip.
 // At most 32 registers, so that 8 CTAs (2048 threads) fit on an SM and the
-// rows of a batch of up to 8 x SMs run in a single wave.
+// rows of a batch of up to 8 x SMs run in a single wave.  The variant that
+// also writes the normalized rows serves at most 32 rows and is not capped.
 constexpr int kStatsCtasPerSm = 8;
 
-template <int NORM, bool BF16>
-__global__ void __launch_bounds__(kStatsThreads, kStatsCtasPerSm) rowstats_kernel(
+template <int NORM, bool BF16, bool XHAT>
+__global__ void __launch_bounds__(kStatsThreads, XHAT ? 1 : kStatsCtasPerSm) rowstats_kernel(
     const uint4 *__restrict__ x, int64_t M, int64_t K, float eps,
     float2 *__restrict__ stats, const void *__restrict__ gamma,
     const void *__restrict__ beta, float *__restrict__ gamma_f,
     float *__restrict__ beta_f, int *__restrict__ counters, int n_counters,
-    int *__restrict__ err_to_clear)
+    int *__restrict__ err_to_clear, uint4 *__restrict__ xhat)
 {
     // The dependent GEMM may start its prologue while this grid runs; it
     // waits for this grid's completion before reading the statistics.
@@ -104,6 +153,7 @@ __global__ void __launch_bounds__(kStatsThreads, kStatsCtasPerSm) rowstats_kerne
     }
 
     __shared__ float red[3][kStatsThreads / 32];
+    __shared__ float2 row_stats;
     const int64_t vec_per_row = K >> 3;  // 8 elements per 16-byte vector
     for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
         const uint4 *xr = x + row * vec_per_row;
@@ -156,7 +206,8 @@ __global__ void __launch_bounds__(kStatsThreads, kStatsCtasPerSm) rowstats_kerne
                 float tn = red[0][0], tm = red[1][0], t2 = red[2][0];
                 for (int w = 1; w < kStatsThreads / 32; ++w) chan_merge(tn, tm, t2, red[0][w], red[1][w], red[2][w]);
                 const float var = t2 / static_cast<float>(K);
-                stats[row] = make_float2(tm, 1.0f / sqrtf(var + eps));
+                row_stats = make_float2(tm, 1.0f / sqrtf(var + eps));
+                stats[row] = row_stats;
             }
             __syncthreads();
         } else {
@@ -185,9 +236,24 @@ __global__ void __launch_bounds__(kStatsThreads, kStatsCtasPerSm) rowstats_kerne
             if (tid == 0) {
                 float t = 0.f;
                 for (int w = 0; w < kStatsThreads / 32; ++w) t += red[0][w];
-                stats[row] = make_float2(0.f, 1.0f / sqrtf(t / static_cast<float>(K) + eps));
+                row_stats = make_float2(0.f, 1.0f / sqrtf(t / static_cast<float>(K) + eps));
+                stats[row] = row_stats;
             }
             __syncthreads();
+        }
+        if constexpr (XHAT) {
+            // The row is still in L1: normalize it and write it out.
+            const float sc = row_stats.y;
+            const float of = NORM == kNormLayer ? -row_stats.x * row_stats.y : 0.f;
+            const uint4 *gv = static_cast<const uint4 *>(gamma);
+            const uint4 *bv = static_cast<const uint4 *>(beta);
+            uint4 *out = xhat + row * vec_per_row;
+#pragma unroll 1
+            for (int64_t v = tid; v < vec_per_row; v += kStatsThreads)
+                out[v] = normalize8<NORM, BF16>(__ldg(xr + v), __ldg(gv + v),
+                                                NORM == kNormLayer ? __ldg(bv + v) : make_uint4(0, 0, 0, 0),
+                                                sc, of);
+            __syncthreads();   // row_stats is rewritten by the next row
         }
     }
 }
@@ -196,7 +262,7 @@ int launch_rowstats(int norm, bool bf16, const void *x, int64_t M, int64_t K,
                     float eps, float2 *stats, const void *gamma,
                     const void *beta, float *gamma_f, float *beta_f,
                     int *counters, int n_counters, int *err_to_clear,
-                    int num_sms, cudaStream_t stream)
+                    int num_sms, cudaStream_t stream, void *xhat)
 {
     const int threads = kStatsThreads;
     int64_t blocks = M;
@@ -207,17 +273,22 @@ int launch_rowstats(int norm, bool bf16, const void *x, int64_t M, int64_t K,
     if (blocks < 1) blocks = 1;
     const uint4 *xv = static_cast<const uint4 *>(x);
     dim3 grid(static_cast<unsigned>(blocks)), block(threads);
+    uint4 *xh = static_cast<uint4 *>(xhat);
+#define NGR_STATS(N_, B_)                                                                     \
+    if (xh)                                                                                   \
+        rowstats_kernel<N_, B_, true><<<grid, block, 0, stream>>>(                            \
+            xv, M, K, eps, stats, gamma, beta, gamma_f, beta_f, counters, n_counters,          \
+            err_to_clear, xh);                                                                \
+    else                                                                                      \
+        rowstats_kernel<N_, B_, false><<<grid, block, 0, stream>>>(                           \
+            xv, M, K, eps, stats, gamma, beta, gamma_f, beta_f, counters, n_counters,          \
+            err_to_clear, nullptr);
     if (norm == kNormLayer) {
-        if (bf16)
-            rowstats_kernel<kNormLayer, true><<<grid, block, 0, stream>>>(xv, M, K, eps, stats, gamma, beta, gamma_f, beta_f, counters, n_counters, err_to_clear);
-        else
-            rowstats_kernel<kNormLayer, false><<<grid, block, 0, stream>>>(xv, M, K, eps, stats, gamma, beta, gamma_f, beta_f, counters, n_counters, err_to_clear);
+        if (bf16) { NGR_STATS(kNormLayer, true) } else { NGR_STATS(kNormLayer, false) }
     } else {
-        if (bf16)
-            rowstats_kernel<kNormRms, true><<<grid, block, 0, stream>>>(xv, M, K, eps, stats, gamma, beta, gamma_f, beta_f, counters, n_counters, err_to_clear);
-        else
-            rowstats_kernel<kNormRms, false><<<grid, block, 0, stream>>>(xv, M, K, eps, stats, gamma, beta, gamma_f, beta_f, counters, n_counters, err_to_clear);
+        if (bf16) { NGR_STATS(kNormRms, true) } else { NGR_STATS(kNormRms, false) }
     }
+#undef NGR_STATS
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? 0 : record_cuda_error("row statistics launch", e, cudaGetErrorString(e));
 }

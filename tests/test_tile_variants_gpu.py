@@ -29,7 +29,7 @@ ATOL, RTOL = 1e-2, 1e-2
 # (pair, bn, nsub) as ngr_set_tile_config takes them.
 CONFIGS = [(0, 128, 1), (0, 192, 1), (0, 224, 1), (0, 256, 1),
            (1, 128, 1), (1, 192, 1), (1, 224, 1), (1, 256, 1),
-           (1, 224, 2), (1, 256, 2)]
+           (1, 192, 2), (1, 224, 2), (1, 256, 2)]
 IDS = [f"{'pair' if p else 'single'}-bn{bn}x{ns}" for p, bn, ns in CONFIGS]
 
 
