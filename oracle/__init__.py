@@ -26,7 +26,7 @@ _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "libngr_oracle.so")
 
 NORM_NONE, NORM_LAYER, NORM_RMS = 0, 1, 2
-ACT_NONE, ACT_SILU = 0, 1
+ACT_NONE, ACT_SILU, ACT_RELU, ACT_GELU = 0, 1, 2, 3
 _DT = {torch.float16: 0, torch.bfloat16: 1}
 
 _lock = threading.Lock()
@@ -64,10 +64,14 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.ngo_ffn.argtypes = [P, P, P, I64, I64, I64, I, P, I64, P]
     lib.ngo_fold_prepare.argtypes = [I, P, P, P, P, I64, I64, I, P, P, P]
     lib.ngo_folded_linear.argtypes = [I, I, P, P, P, P, D, I64, I64, I64, I, P, I64, P]
+    lib.ngo_mlp.argtypes = [I, I, P, P, P, P, P, P, P, D, I64, I64, I64, I64, I, P, I64, P]
+    lib.ngo_swiglu.argtypes = [I, P, P, P, P, P, D, I64, I64, I64, I, P, I64, P]
+    lib.ngo_mlp_swiglu.argtypes = [I, P, P, P, P, P, P, D, I64, I64, I64, I64, I, P, I64, P]
     lib.ngo_num_threads.argtypes = []
     for f in (lib.ngo_decode, lib.ngo_row_stats, lib.ngo_normalize,
               lib.ngo_norm_linear, lib.ngo_ffn, lib.ngo_fold_prepare,
-              lib.ngo_folded_linear, lib.ngo_num_threads):
+              lib.ngo_folded_linear, lib.ngo_mlp, lib.ngo_swiglu,
+              lib.ngo_mlp_swiglu, lib.ngo_num_threads):
         f.restype = ctypes.c_int
     return lib
 
@@ -190,6 +194,57 @@ def ffn(x, W1, W2, rows=None, lib=None) -> np.ndarray:
     xb, w1, w2 = _bits(x), _bits(W1), _bits(W2)
     _check(lib.ngo_ffn(_ptr(xb), _ptr(w1), _ptr(w2), M, K, F, _DT[x.dtype],
                        _ptr(r), nr, _ptr(y)), "ffn")
+    return y
+
+
+def mlp(norm: int, act: int, x, gamma, beta, W1, b1, W2, b2, eps: float,
+        rows=None, lib=None) -> np.ndarray:
+    """y [nrows, N] = act(norm(x[rows]) . W1^T + b1) . W2^T + b2 in float64
+    (the hidden activations unrounded).  W1 is [F, K], W2 [N, F]."""
+    lib = lib or load()
+    M, K = x.shape
+    F = W1.shape[0]
+    N = W2.shape[0]
+    if W1.shape[1] != K or W2.shape[1] != F:
+        raise ValueError("W1 must be [F, K] and W2 [N, F]")
+    r, nr = _rows(rows, M)
+    y = np.empty((nr, N), dtype=np.float64)
+    bits = [_bits(t) for t in (x, gamma, beta, W1, b1, W2, b2)]
+    _check(lib.ngo_mlp(norm, act, *[_ptr(b) for b in bits], eps, M, K, F, N,
+                       _DT[x.dtype], _ptr(r), nr, _ptr(y)), "mlp")
+    return y
+
+
+def swiglu(norm: int, x, gamma, beta, Wg, Wu, eps: float, rows=None,
+           lib=None) -> np.ndarray:
+    """h [nrows, F] = SiLU(a . Wg^T) * (a . Wu^T), a = norm(x[rows]), float64."""
+    lib = lib or load()
+    M, K = x.shape
+    F = Wg.shape[0]
+    if tuple(Wg.shape) != (F, K) or tuple(Wu.shape) != (F, K):
+        raise ValueError("Wg and Wu must be [F, K]")
+    r, nr = _rows(rows, M)
+    h = np.empty((nr, F), dtype=np.float64)
+    bits = [_bits(t) for t in (x, gamma, beta, Wg, Wu)]
+    _check(lib.ngo_swiglu(norm, *[_ptr(b) for b in bits], eps, M, K, F,
+                          _DT[x.dtype], _ptr(r), nr, _ptr(h)), "swiglu")
+    return h
+
+
+def mlp_swiglu(norm: int, x, gamma, beta, Wg, Wu, Wd, eps: float, rows=None,
+               lib=None) -> np.ndarray:
+    """y [nrows, N] = swiglu(...) . Wd^T in float64 (h unrounded); Wd [N, F]."""
+    lib = lib or load()
+    M, K = x.shape
+    F = Wg.shape[0]
+    N = Wd.shape[0]
+    if tuple(Wg.shape) != (F, K) or tuple(Wu.shape) != (F, K) or Wd.shape[1] != F:
+        raise ValueError("Wg, Wu must be [F, K] and Wd [N, F]")
+    r, nr = _rows(rows, M)
+    y = np.empty((nr, N), dtype=np.float64)
+    bits = [_bits(t) for t in (x, gamma, beta, Wg, Wu, Wd)]
+    _check(lib.ngo_mlp_swiglu(norm, *[_ptr(b) for b in bits], eps, M, K, F, N,
+                              _DT[x.dtype], _ptr(r), nr, _ptr(y)), "mlp_swiglu")
     return y
 
 

@@ -21,7 +21,14 @@
  *    (MatMul + SiLU), strategy 2 (MatMul -> SiLU -> MatMul, the FFN),
  *    strategy 3 (RMSNorm + MatMul).
  *  - "CANN推理加速库ascend-transformer-boost ATB算子融合实战...", the
- *    LayerNormMatMul fusion section (fused_layernorm_matmul(x, w, bias)).
+ *    LayerNormMatMul fusion section (fused_layernorm_matmul(x, w, bias));
+ *    Llama2 inference, model structure and fusion opportunities (one
+ *    RMSNorm feeding the Q/K/V projections; the FFN's SwiGLU, a SiLU-gated
+ *    linear transform, fused with its matmuls).
+ *  - "LayerNorm 融合算子如何让大模型推理再快 15%？", §3.3 (a fusion chain
+ *    LayerNorm -> MatMul -> BiasAdd -> ReLU -> MatMul -> BiasAdd).
+ *  - "昇腾CANN的MatMul融合玩法", the table of fused GEMM instructions
+ *    (MatMul + ReLU / GELU / SiLU).
  *
  * Readings taken where the pages are silent or at odds:
  *  - variance is the biased one (divide by K), as torch's layer_norm that
@@ -30,6 +37,10 @@
  *  - RMSNorm applies gamma, and no beta;
  *  - bias is optional; with SiLU the order is matmul, + bias, then SiLU;
  *  - SiLU(z) = z * sigmoid(z) = z / (1 + exp(-z));
+ *  - GELU(z) = z * Phi(z) = z (1 + erf(z / sqrt 2)) / 2, the exact form (the
+ *    pages name GELU without defining it); ReLU(z) = max(z, 0);
+ *  - SwiGLU is the Llama form h_j = SiLU(a . Wg[j]) * (a . Wu[j]) with the
+ *    gate and up projections both [F, K] and no biases;
  *  - W is [N, K] row-major (the nn.Linear layout), y = a . W^T;
  *  - the FFN keeps its intermediate H in fp64, unrounded.
  *
@@ -44,7 +55,7 @@
 
 enum { NGO_F16 = 0, NGO_BF16 = 1 };
 enum { NGO_NORM_NONE = 0, NGO_NORM_LAYER = 1, NGO_NORM_RMS = 2 };
-enum { NGO_ACT_NONE = 0, NGO_ACT_SILU = 1 };
+enum { NGO_ACT_NONE = 0, NGO_ACT_SILU = 1, NGO_ACT_RELU = 2, NGO_ACT_GELU = 3 };
 
 /* ---- exact decoding of the 16-bit inputs ---------------------------------
  * IEEE-754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.
@@ -149,8 +160,19 @@ static void normalize_row(int norm, const double *x, int64_t K, double mu,
 /* SiLU(z) = z * sigmoid(z) */
 static double silu(double z) { return z / (1.0 + exp(-z)); }
 
+/* The activation applied after the bias. */
+static double activation(int act, double z)
+{
+    switch (act) {
+    case NGO_ACT_SILU: return silu(z);
+    case NGO_ACT_RELU: return z > 0.0 ? z : 0.0;
+    case NGO_ACT_GELU: return 0.5 * z * (1.0 + erf(z / sqrt(2.0)));
+    default: return z;
+    }
+}
+
 /* ---- a3 + a4: one output row of the linear layer -----------------------------
- * z_n = sum_k a_k * W[n, k] (+ bias_n) ; y_n = z_n or SiLU(z_n).
+ * z_n = sum_k a_k * W[n, k] (+ bias_n) ; y_n = act(z_n).
  * W rows are decoded on the fly through the table. */
 static void linear_row(const double *a, const uint16_t *W, const double *T,
                        const double *bias, int act, int64_t K, int64_t N,
@@ -161,7 +183,7 @@ static void linear_row(const double *a, const uint16_t *W, const double *T,
         double z = 0.0;
         for (int64_t k = 0; k < K; ++k) z += a[k] * T[w[k]];
         if (bias) z += bias[n];
-        y[n] = act == NGO_ACT_SILU ? silu(z) : z;
+        y[n] = activation(act, z);
     }
 }
 
@@ -303,6 +325,151 @@ int ngo_ffn(const uint16_t *x, const uint16_t *W1, const uint16_t *W2,
     return failed ? -9 : 0;
 }
 
+/* Decode a [n] 16-bit vector (NULL stays NULL); the caller frees. */
+static double *decode_vec(const uint16_t *v, int64_t n, const double *T, int *failed)
+{
+    if (!v) return NULL;
+    double *d = malloc((size_t)n * sizeof(double));
+    if (!d) { *failed = 1; return NULL; }
+    for (int64_t i = 0; i < n; ++i) d[i] = T[v[i]];
+    return d;
+}
+
+/* ---- the general two-layer chain (LayerNorm fusion chain, FFN) ---------------
+ * a = norm(x) ; h_j = act(a . W1[j] + b1_j) kept in fp64 ;
+ * y_n = h . W2[n] + b2_n.  W1 is [F, K], W2 is [N, F]; b1, b2 may be NULL. */
+int ngo_mlp(int norm, int act, const uint16_t *x, const uint16_t *gamma,
+            const uint16_t *beta, const uint16_t *W1, const uint16_t *b1,
+            const uint16_t *W2, const uint16_t *b2, double eps, int64_t M,
+            int64_t K, int64_t F, int64_t N, int dt, const int64_t *rows,
+            int64_t nrows, double *y)
+{
+    int rc = check_common(dt, M, K, F, rows, nrows);
+    if (rc) return rc;
+    if (N <= 0) return -2;
+    if (!x || !W1 || !W2 || !y) return -1;
+    if (norm != NGO_NORM_NONE && !gamma) return -1;
+    if (norm == NGO_NORM_LAYER && !beta) return -1;
+    const double *T = table_for(dt);
+    int failed = 0;
+    double *g = decode_vec(gamma, K, T, &failed);
+    double *b = decode_vec(beta, K, T, &failed);
+    double *c1 = decode_vec(b1, F, T, &failed);
+    double *c2 = decode_vec(b2, N, T, &failed);
+#pragma omp parallel for schedule(dynamic)
+    for (int64_t i = 0; i < nrows; ++i) {
+        if (failed) continue;
+        int64_t r = rows ? rows[i] : i;
+        double *xr = malloc((size_t)K * sizeof(double));
+        double *a = malloc((size_t)K * sizeof(double));
+        double *h = malloc((size_t)F * sizeof(double));
+        if (!xr || !a || !h) { free(xr); free(a); free(h); failed = 1; continue; }
+        for (int64_t k = 0; k < K; ++k) xr[k] = T[x[r * K + k]];
+        double mu, rstd;
+        row_stats(norm, xr, K, eps, &mu, &rstd);
+        normalize_row(norm, xr, K, mu, rstd, g, b, a);
+        linear_row(a, W1, T, c1, act, K, F, h);
+        linear_row(h, W2, T, c2, NGO_ACT_NONE, F, N, y + i * N);
+        free(xr);
+        free(a);
+        free(h);
+    }
+    free(g);
+    free(b);
+    free(c1);
+    free(c2);
+    return failed ? -9 : 0;
+}
+
+/* ---- SwiGLU: one norm feeding the gate and up projections ---------------------
+ * a = norm(x) ; h_j = SiLU(a . Wg[j]) * (a . Wu[j]) ; Wg, Wu are [F, K]. */
+static void swiglu_row(const double *a, const uint16_t *Wg, const uint16_t *Wu,
+                       const double *T, int64_t K, int64_t F, double *h)
+{
+    for (int64_t j = 0; j < F; ++j) {
+        double zg = 0.0, zu = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            zg += a[k] * T[Wg[j * K + k]];
+            zu += a[k] * T[Wu[j * K + k]];
+        }
+        h[j] = silu(zg) * zu;
+    }
+}
+
+int ngo_swiglu(int norm, const uint16_t *x, const uint16_t *gamma, const uint16_t *beta,
+               const uint16_t *Wg, const uint16_t *Wu, double eps, int64_t M,
+               int64_t K, int64_t F, int dt, const int64_t *rows, int64_t nrows,
+               double *h)
+{
+    int rc = check_common(dt, M, K, F, rows, nrows);
+    if (rc) return rc;
+    if (!x || !Wg || !Wu || !h) return -1;
+    if (norm != NGO_NORM_NONE && !gamma) return -1;
+    if (norm == NGO_NORM_LAYER && !beta) return -1;
+    const double *T = table_for(dt);
+    int failed = 0;
+    double *g = decode_vec(gamma, K, T, &failed);
+    double *b = decode_vec(beta, K, T, &failed);
+#pragma omp parallel for schedule(dynamic)
+    for (int64_t i = 0; i < nrows; ++i) {
+        if (failed) continue;
+        int64_t r = rows ? rows[i] : i;
+        double *xr = malloc((size_t)K * sizeof(double));
+        double *a = malloc((size_t)K * sizeof(double));
+        if (!xr || !a) { free(xr); free(a); failed = 1; continue; }
+        for (int64_t k = 0; k < K; ++k) xr[k] = T[x[r * K + k]];
+        double mu, rstd;
+        row_stats(norm, xr, K, eps, &mu, &rstd);
+        normalize_row(norm, xr, K, mu, rstd, g, b, a);
+        swiglu_row(a, Wg, Wu, T, K, F, h + i * F);
+        free(xr);
+        free(a);
+    }
+    free(g);
+    free(b);
+    return failed ? -9 : 0;
+}
+
+/* The Llama MLP: h as ngo_swiglu (fp64, unrounded), y_n = h . Wd[n]; Wd is
+ * [N, F]. */
+int ngo_mlp_swiglu(int norm, const uint16_t *x, const uint16_t *gamma,
+                   const uint16_t *beta, const uint16_t *Wg, const uint16_t *Wu,
+                   const uint16_t *Wd, double eps, int64_t M, int64_t K, int64_t F,
+                   int64_t N, int dt, const int64_t *rows, int64_t nrows, double *y)
+{
+    int rc = check_common(dt, M, K, F, rows, nrows);
+    if (rc) return rc;
+    if (N <= 0) return -2;
+    if (!x || !Wg || !Wu || !Wd || !y) return -1;
+    if (norm != NGO_NORM_NONE && !gamma) return -1;
+    if (norm == NGO_NORM_LAYER && !beta) return -1;
+    const double *T = table_for(dt);
+    int failed = 0;
+    double *g = decode_vec(gamma, K, T, &failed);
+    double *b = decode_vec(beta, K, T, &failed);
+#pragma omp parallel for schedule(dynamic)
+    for (int64_t i = 0; i < nrows; ++i) {
+        if (failed) continue;
+        int64_t r = rows ? rows[i] : i;
+        double *xr = malloc((size_t)K * sizeof(double));
+        double *a = malloc((size_t)K * sizeof(double));
+        double *h = malloc((size_t)F * sizeof(double));
+        if (!xr || !a || !h) { free(xr); free(a); free(h); failed = 1; continue; }
+        for (int64_t k = 0; k < K; ++k) xr[k] = T[x[r * K + k]];
+        double mu, rstd;
+        row_stats(norm, xr, K, eps, &mu, &rstd);
+        normalize_row(norm, xr, K, mu, rstd, g, b, a);
+        swiglu_row(a, Wg, Wu, T, K, F, h);
+        linear_row(h, Wd, T, NULL, NGO_ACT_NONE, F, N, y + i * N);
+        free(xr);
+        free(a);
+        free(h);
+    }
+    free(g);
+    free(b);
+    return failed ? -9 : 0;
+}
+
 /* ---- a7: the inference-mode weight fold -----------------------------------------
  * "LayerNorm 融合算子如何让大模型推理再快 15%？", §6.2: in inference gamma and
  * beta are fixed, so gamma is folded into the matmul weight beforehand.
@@ -358,7 +525,7 @@ int ngo_folded_linear(int norm, int act, const uint16_t *x, const double *Wf,
             double s = 0.0;
             for (int64_t k = 0; k < K; ++k) s += xr[k] * Wf[n * K + k];
             double z = rstd * s - rstd * mu * c[n] + bprime[n];
-            y[i * N + n] = act == NGO_ACT_SILU ? silu(z) : z;
+            y[i * N + n] = activation(act, z);
         }
         free(xr);
     }

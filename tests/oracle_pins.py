@@ -14,7 +14,10 @@ mathematics fix:
 - brute force on tiny inputs (unfused Python loops, a different evaluation
   order: normalized matrix materialized, then the product);
 - row selection: a sampled row equals the same row of a full evaluation;
-- the inference-mode fold agrees with the direct form in fp64.
+- the inference-mode fold agrees with the direct form in fp64;
+- the activations, the two-layer chain and SwiGLU against torch's float64
+  ``relu``, ``gelu`` (exact erf form), ``silu``, ``layer_norm``, ``rms_norm``
+  and ``linear``, SwiGLU also against brute force on tiny inputs.
 
 The same functions run against oracle builds with planted mistakes
 (``test_oracle_pins.py``) to show that each plausible mistake fails a pin.
@@ -285,7 +288,123 @@ def pin_stats_vs_numpy(lib):
            what="rms rstd")
 
 
+def pin_activations_vs_library(lib):
+    """Identity layer (no norm, W = I, no bias): y = act(x) exactly as
+    torch's float64 relu / gelu (erf form) / silu, on values that include 0,
+    +-1, +-2 and the tails."""
+    vals = [0.0, 1.0, -1.0, 2.0, -2.0, 0.5, -0.5, 3.0, -3.0, 8.0, -8.0, 0.125, -6.0, 4.0, -4.0, 1.5]
+    K = len(vals)
+    x = torch.tensor([vals], dtype=torch.float64).to(torch.float16)
+    eye = torch.eye(K, dtype=torch.float16)
+    X = _exact(x)
+    for act, ref in ((oracle.ACT_RELU, F.relu(X)),
+                     (oracle.ACT_GELU, F.gelu(X, approximate="none")),
+                     (oracle.ACT_SILU, F.silu(X)),
+                     (oracle.ACT_NONE, X)):
+        y = oracle.norm_linear(oracle.NORM_NONE, act, x, None, None, eye, None,
+                               0.0, lib=lib)
+        _close(y, ref.numpy(), rtol=1e-14, atol=1e-15, what=f"act {act}")
+    # GELU(1) = Phi(1) and GELU(-1) = -(1 - Phi(1)), Phi from scipy's ndtr
+    from scipy.special import ndtr
+    y = oracle.norm_linear(oracle.NORM_NONE, oracle.ACT_GELU, x, None, None,
+                           eye, None, 0.0, lib=lib)
+    _close([y[0][1], y[0][2]], [ndtr(1.0), -ndtr(-1.0)], rtol=1e-14,
+           what="GELU(+-1) vs normal CDF")
+
+
+def pin_mlp_vs_torch(lib):
+    """The two-layer chain norm -> linear(+b1) -> act -> linear(+b2) against
+    torch float64, for every norm and activation, biases present and not."""
+    M, K, Fh, N = 5, 32, 24, 20
+    for dt in (torch.float16, torch.bfloat16):
+        x = _rand((M, K), 50, dt, 1.0, 2.0)
+        g = _rand((K,), 51, dt, 0.1, 1.0)
+        b = _rand((K,), 52, dt, 0.1)
+        W1 = _rand((Fh, K), 53, dt, K ** -0.5)
+        b1 = _rand((Fh,), 54, dt, 0.2)
+        W2 = _rand((N, Fh), 55, dt, Fh ** -0.5)
+        b2 = _rand((N,), 56, dt, 0.2)
+        X, G, B, A1, C1, A2, C2 = map(_exact, (x, g, b, W1, b1, W2, b2))
+        acts = {oracle.ACT_NONE: lambda t: t, oracle.ACT_SILU: F.silu,
+                oracle.ACT_RELU: F.relu,
+                oracle.ACT_GELU: lambda t: F.gelu(t, approximate="none")}
+        norms = {oracle.NORM_NONE: lambda t: t,
+                 oracle.NORM_LAYER: lambda t: F.layer_norm(t, (K,), G, B, 1e-5),
+                 oracle.NORM_RMS: lambda t: F.rms_norm(t, (K,), G, 1e-5)}
+        for nid, nf in norms.items():
+            for aid, af in acts.items():
+                for with_bias in (True, False):
+                    bb1, bb2 = (b1, b2) if with_bias else (None, None)
+                    y = oracle.mlp(nid, aid, x, g if nid else None,
+                                   b if nid == oracle.NORM_LAYER else None,
+                                   W1, bb1, W2, bb2, 1e-5, lib=lib)
+                    h = af(F.linear(nf(X), A1, C1 if with_bias else None))
+                    ref = F.linear(h, A2, C2 if with_bias else None)
+                    _close(y, ref.numpy(), rtol=1e-11, atol=1e-12,
+                           what=f"mlp norm={nid} act={aid} bias={with_bias}")
+
+
+def pin_swiglu_vs_torch(lib):
+    """SwiGLU h = SiLU(a . Wg^T) * (a . Wu^T) and the Llama MLP h . Wd^T
+    against torch float64 for every norm."""
+    M, K, Fh, N = 4, 40, 24, 16
+    x = _rand((M, K), 60, torch.bfloat16, 1.0, 1.0)
+    g = _rand((K,), 61, torch.bfloat16, 0.1, 1.0)
+    b = _rand((K,), 62, torch.bfloat16, 0.1)
+    Wg = _rand((Fh, K), 63, torch.bfloat16, K ** -0.5)
+    Wu = _rand((Fh, K), 64, torch.bfloat16, K ** -0.5)
+    Wd = _rand((N, Fh), 65, torch.bfloat16, Fh ** -0.5)
+    X, G, B, AG, AU, AD = map(_exact, (x, g, b, Wg, Wu, Wd))
+    norms = {oracle.NORM_NONE: lambda t: t,
+             oracle.NORM_LAYER: lambda t: F.layer_norm(t, (K,), G, B, 1e-5),
+             oracle.NORM_RMS: lambda t: F.rms_norm(t, (K,), G, 1e-5)}
+    for nid, nf in norms.items():
+        gg = g if nid else None
+        bb = b if nid == oracle.NORM_LAYER else None
+        a = nf(X)
+        href = F.silu(F.linear(a, AG)) * F.linear(a, AU)
+        h = oracle.swiglu(nid, x, gg, bb, Wg, Wu, 1e-5, lib=lib)
+        _close(h, href.numpy(), rtol=1e-11, atol=1e-12, what=f"swiglu norm={nid}")
+        y = oracle.mlp_swiglu(nid, x, gg, bb, Wg, Wu, Wd, 1e-5, lib=lib)
+        _close(y, F.linear(href, AD).numpy(), rtol=1e-11, atol=1e-12,
+               what=f"mlp_swiglu norm={nid}")
+
+
+def pin_swiglu_brute_force(lib):
+    """SwiGLU in pure Python loops on tiny inputs, RMSNorm first; with the
+    gate and up weights equal the result is SiLU(z) * z; with the up weight
+    zero it is exactly zero; rows can be sampled."""
+    M, K, Fh = 3, 8, 5
+    x = _rand((M, K), 66, torch.float16, 1.0, 0.5)
+    g = _rand((K,), 67, torch.float16, 0.1, 1.0)
+    Wg = _rand((Fh, K), 68, torch.float16, 0.4)
+    Wu = _rand((Fh, K), 69, torch.float16, 0.4)
+    X, G, AG, AU = (_exact(t).tolist() for t in (x, g, Wg, Wu))
+    eps = 1e-3
+    H = []
+    for i in range(M):
+        r = 1.0 / math.sqrt(math.fsum(v * v for v in X[i]) / K + eps)
+        a = [X[i][k] * r * G[k] for k in range(K)]
+        row = []
+        for j in range(Fh):
+            zg = math.fsum(a[k] * AG[j][k] for k in range(K))
+            zu = math.fsum(a[k] * AU[j][k] for k in range(K))
+            row.append(zg / (1.0 + math.exp(-zg)) * zu)
+        H.append(row)
+    h = oracle.swiglu(oracle.NORM_RMS, x, g, None, Wg, Wu, eps, lib=lib)
+    _close(h, H, rtol=1e-12, atol=1e-12, what="swiglu brute force")
+    hs = oracle.swiglu(oracle.NORM_RMS, x, g, None, Wg, Wu, eps, rows=[2, 0], lib=lib)
+    assert np.array_equal(hs, h[[2, 0]]), "swiglu row selection"
+    hz = oracle.swiglu(oracle.NORM_RMS, x, g, None, Wg, torch.zeros_like(Wu), eps, lib=lib)
+    assert np.all(hz == 0.0), "swiglu with a zero up projection"
+    hgg = oracle.swiglu(oracle.NORM_RMS, x, g, None, Wg, Wg, eps, lib=lib)
+    z = oracle.norm_linear(oracle.NORM_RMS, oracle.ACT_NONE, x, g, None, Wg, None, eps, lib=lib)
+    _close(hgg, z * z / (1.0 + np.exp(-z)), rtol=1e-12, atol=1e-14, what="swiglu Wu = Wg")
+
+
 ALL_PINS = [pin_decode, pin_closed_forms, pin_layernorm_invariants,
             pin_rms_invariants, pin_identity_reduces_to_norm,
             pin_full_path_vs_torch, pin_ffn_vs_torch, pin_brute_force,
-            pin_row_selection, pin_fold_identity, pin_stats_vs_numpy]
+            pin_row_selection, pin_fold_identity, pin_stats_vs_numpy,
+            pin_activations_vs_library, pin_mlp_vs_torch, pin_swiglu_vs_torch,
+            pin_swiglu_brute_force]

@@ -40,14 +40,29 @@ MUTANTS = [
     ("bias subtracted", "if (bias) z += bias[n];", "if (bias) z -= bias[n];"),
     ("bias dropped", "if (bias) z += bias[n];", "if (bias) z += 0.0;"),
     ("SiLU sign", "return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
-    ("SiLU before bias", "if (bias) z += bias[n];\n        y[n] = act == NGO_ACT_SILU ? silu(z) : z;",
-     "y[n] = act == NGO_ACT_SILU ? silu(z) : z;\n        if (bias) y[n] += bias[n];"),
+    ("activation before bias", "if (bias) z += bias[n];\n        y[n] = activation(act, z);",
+     "y[n] = activation(act, z);\n        if (bias) y[n] += bias[n];"),
+    ("GELU without the 1/sqrt(2)", "return 0.5 * z * (1.0 + erf(z / sqrt(2.0)));",
+     "return 0.5 * z * (1.0 + erf(z));"),
+    ("GELU as z * sigmoid(1.702 z)", "return 0.5 * z * (1.0 + erf(z / sqrt(2.0)));",
+     "return z / (1.0 + exp(-1.702 * z));"),
+    ("ReLU leaks", "case NGO_ACT_RELU: return z > 0.0 ? z : 0.0;",
+     "case NGO_ACT_RELU: return z > 0.0 ? z : 0.01 * z;"),
+    ("SwiGLU gate and up swapped", "h[j] = silu(zg) * zu;", "h[j] = zg * silu(zu);"),
+    ("SwiGLU gate not activated", "h[j] = silu(zg) * zu;", "h[j] = zg * zu;"),
+    ("chain drops the second bias", "linear_row(h, W2, T, c2, NGO_ACT_NONE, F, N, y + i * N);",
+     "linear_row(h, W2, T, NULL, NGO_ACT_NONE, F, N, y + i * N);"),
+    ("chain activation after the second layer",
+     "linear_row(a, W1, T, c1, act, K, F, h);\n        linear_row(h, W2, T, c2, NGO_ACT_NONE, F, N, y + i * N);",
+     "linear_row(a, W1, T, c1, NGO_ACT_NONE, K, F, h);\n        linear_row(h, W2, T, c2, act, F, N, y + i * N);"),
+    ("chain skips the norm", "normalize_row(norm, xr, K, mu, rstd, g, b, a);\n        linear_row(a, W1, T, c1, act, K, F, h);",
+     "normalize_row(NGO_NORM_NONE, xr, K, mu, rstd, g, b, a);\n        linear_row(a, W1, T, c1, act, K, F, h);"),
     ("binary16 exponent off by one", "v = ldexp((double)(f | 0x400), e - 25);",
      "v = ldexp((double)(f | 0x400), e - 24);"),
     ("FFN without SiLU", "linear_row(xr, W1, T, NULL, NGO_ACT_SILU, K, F, h);",
      "linear_row(xr, W1, T, NULL, NGO_ACT_NONE, K, F, h);"),
-    ("sample index used as row", "        row_stats(norm, xr, K, eps, &mu, &rstd);\n        normalize_row(norm, xr, K, mu, rstd, g, b, a);\n        linear_row(",
-     "        for (int64_t k = 0; k < K; ++k) xr[k] = T[x[i * K + k]];\n        row_stats(norm, xr, K, eps, &mu, &rstd);\n        normalize_row(norm, xr, K, mu, rstd, g, b, a);\n        linear_row("),
+    ("sample index used as row", "        row_stats(norm, xr, K, eps, &mu, &rstd);\n        normalize_row(norm, xr, K, mu, rstd, g, b, a);\n        linear_row(a, W, T, bi, act, K, N, y + i * N);",
+     "        for (int64_t k = 0; k < K; ++k) xr[k] = T[x[i * K + k]];\n        row_stats(norm, xr, K, eps, &mu, &rstd);\n        normalize_row(norm, xr, K, mu, rstd, g, b, a);\n        linear_row(a, W, T, bi, act, K, N, y + i * N);"),
     ("fold drops the mean term", "double z = rstd * s - rstd * mu * c[n] + bprime[n];",
      "double z = rstd * s + bprime[n];"),
 ]
