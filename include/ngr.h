@@ -78,13 +78,33 @@ typedef enum {
     NGR_OP_LAYERNORM_LINEAR = 0,
     NGR_OP_RMSNORM_LINEAR = 1,
     NGR_OP_LINEAR_SILU = 2,
-    NGR_OP_FFN = 3
+    NGR_OP_FFN = 3,
+    NGR_OP_NORM_LINEAR = 4,   /* ngr_fused_norm_linear_act */
+    NGR_OP_MLP = 5,           /* ngr_fused_mlp */
+    NGR_OP_SWIGLU = 6,        /* ngr_fused_norm_swiglu */
+    NGR_OP_MLP_SWIGLU = 7     /* ngr_fused_mlp_swiglu */
 } ngr_op;
 
-/* Bytes of device workspace that `op` needs for these sizes (for NGR_OP_FFN
- * pass the hidden width F as N; the FFN's intermediate H is included only if
- * `ffn_h_in_workspace` is nonzero).  Pure host arithmetic: needs no GPU and
- * never fails (returns 0 for invalid sizes). */
+/* Row normalization applied to x before the first product. */
+typedef enum {
+    NGR_NORM_NONE = 0,
+    NGR_NORM_LAYER = 1,       /* (x - mu) rstd gamma + beta */
+    NGR_NORM_RMS = 2          /* x rstd gamma */
+} ngr_norm;
+
+/* Activation applied after the bias. */
+typedef enum {
+    NGR_ACT_NONE = 0,
+    NGR_ACT_SILU = 1,         /* z / (1 + exp(-z)) */
+    NGR_ACT_RELU = 2,         /* max(z, 0) */
+    NGR_ACT_GELU = 3          /* z (1 + erf(z / sqrt 2)) / 2, the exact form */
+} ngr_act;
+
+/* Bytes of device workspace that `op` needs for these sizes.  For the
+ * two-GEMM ops (FFN, MLP, MLP_SWIGLU) and SWIGLU pass the hidden width F as
+ * N; their intermediate H is included only if `ffn_h_in_workspace` is
+ * nonzero.  Pure host arithmetic: needs no GPU and never fails (returns 0
+ * for invalid sizes). */
 size_t ngr_workspace_bytes(int op, int64_t M, int64_t K, int64_t N,
                            int ffn_h_in_workspace);
 
@@ -130,6 +150,56 @@ int ngr_ffn_linear_silu_linear(const void *x, const void *W1, const void *W2,
                                int64_t M, int64_t K, int64_t F, int dtype,
                                void *h, void *y, void *workspace,
                                size_t workspace_bytes, ngr_stream_t stream);
+
+/* The general fused layer: y = act(norm(x) . W^T + bias), norm one of
+ * ngr_norm, act one of ngr_act (others give NGR_ERR_ARG).  gamma is needed
+ * unless norm is NGR_NORM_NONE, beta only with NGR_NORM_LAYER (ignored
+ * otherwise); bias may be NULL.  Workspace: NGR_OP_NORM_LINEAR.
+ * [LNF] §1.1, §2.1; [MMF] §二 strategies 1 and 3 and the table of fused GEMM
+ * instructions (MatMul + ReLU / GELU / SiLU). */
+int ngr_fused_norm_linear_act(int norm, int act, const void *x,
+                              const void *gamma, const void *beta,
+                              const void *W, const void *bias, float eps,
+                              int64_t M, int64_t K, int64_t N, int dtype,
+                              void *y, void *workspace, size_t workspace_bytes,
+                              ngr_stream_t stream);
+
+/* The two-layer fusion chain:
+ *   H = act(norm(x) . W1^T + b1) [M, F],  y = H . W2^T + b2 [M, K].
+ * W1 is [F, K], W2 is [K, F]; b1 [F] and b2 [K] may be NULL.  H is written
+ * once and read once, into `h` ([M, F]) when non-NULL, else into the
+ * workspace (NGR_OP_MLP with ffn_h_in_workspace = 1).  norm / act / gamma /
+ * beta as in ngr_fused_norm_linear_act.
+ * [LNF] §3.3 (LayerNorm -> MatMul -> BiasAdd -> ReLU -> MatMul -> BiasAdd
+ * fused as one chain). */
+int ngr_fused_mlp(int norm, int act, const void *x, const void *gamma,
+                  const void *beta, const void *W1, const void *b1,
+                  const void *W2, const void *b2, float eps, int64_t M,
+                  int64_t K, int64_t F, int dtype, void *h, void *y,
+                  void *workspace, size_t workspace_bytes, ngr_stream_t stream);
+
+/* SwiGLU with its norm: a = norm(x);
+ *   h[i, j] = SiLU(a[i, :] . Wg[j, :]) * (a[i, :] . Wu[j, :])  [M, F].
+ * Wg (gate) and Wu (up) are [F, K].  The two products share every
+ * normalized x tile on chip and h is written once.  Workspace:
+ * NGR_OP_SWIGLU.  [ATB] Llama2 inference, model structure and fusion
+ * opportunities (the FFN's SwiGLU, a SiLU-gated linear transform, fused
+ * with its matmuls; one RMSNorm feeding several projections). */
+int ngr_fused_norm_swiglu(int norm, const void *x, const void *gamma,
+                          const void *beta, const void *Wg, const void *Wu,
+                          float eps, int64_t M, int64_t K, int64_t F, int dtype,
+                          void *h, void *workspace, size_t workspace_bytes,
+                          ngr_stream_t stream);
+
+/* The Llama MLP: h as ngr_fused_norm_swiglu, then y = h . Wd^T [M, K] with
+ * Wd [K, F].  h goes to `h` ([M, F]) when non-NULL, else to the workspace
+ * (NGR_OP_MLP_SWIGLU with ffn_h_in_workspace = 1).  [ATB] as above (the
+ * RMSNorm -> MatMul -> SiLU -> MatMul path of the decoder layer). */
+int ngr_fused_mlp_swiglu(int norm, const void *x, const void *gamma,
+                         const void *beta, const void *Wg, const void *Wu,
+                         const void *Wd, float eps, int64_t M, int64_t K,
+                         int64_t F, int dtype, void *h, void *y, void *workspace,
+                         size_t workspace_bytes, ngr_stream_t stream);
 
 /* Inference-mode weight fold, step 1 of 2 ([LNF] §6.2: with gamma and beta
  * fixed, gamma is folded into the matmul weight once, ahead of the calls).

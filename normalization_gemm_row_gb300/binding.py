@@ -25,6 +25,9 @@ from ._build import LIB_PATH
 
 NGR_F16, NGR_BF16 = 0, 1
 OP_LAYERNORM_LINEAR, OP_RMSNORM_LINEAR, OP_LINEAR_SILU, OP_FFN = 0, 1, 2, 3
+OP_NORM_LINEAR, OP_MLP, OP_SWIGLU, OP_MLP_SWIGLU = 4, 5, 6, 7
+NORM_NONE, NORM_LAYER, NORM_RMS = 0, 1, 2
+ACT_NONE, ACT_SILU, ACT_RELU, ACT_GELU = 0, 1, 2, 3
 STATUS = {0: "NGR_OK", -1: "NGR_ERR_NULL", -2: "NGR_ERR_SHAPE",
           -3: "NGR_ERR_ALIGN", -4: "NGR_ERR_DTYPE", -5: "NGR_ERR_WORKSPACE",
           -6: "NGR_ERR_ARCH", -7: "NGR_ERR_CUDA", -8: "NGR_ERR_TIMEOUT",
@@ -40,6 +43,10 @@ SIGNATURES = {
     "ngr_fused_rmsnorm_linear": (_I, [_P, _P, _P, _P, _F, _I64, _I64, _I64, _I, _P, _P, _SZ, _P]),
     "ngr_fused_linear_silu": (_I, [_P, _P, _P, _I64, _I64, _I64, _I, _P, _P, _SZ, _P]),
     "ngr_ffn_linear_silu_linear": (_I, [_P, _P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _SZ, _P]),
+    "ngr_fused_norm_linear_act": (_I, [_I, _I, _P, _P, _P, _P, _P, _F, _I64, _I64, _I64, _I, _P, _P, _SZ, _P]),
+    "ngr_fused_mlp": (_I, [_I, _I, _P, _P, _P, _P, _P, _P, _P, _F, _I64, _I64, _I64, _I, _P, _P, _P, _SZ, _P]),
+    "ngr_fused_norm_swiglu": (_I, [_I, _P, _P, _P, _P, _P, _F, _I64, _I64, _I64, _I, _P, _P, _SZ, _P]),
+    "ngr_fused_mlp_swiglu": (_I, [_I, _P, _P, _P, _P, _P, _P, _F, _I64, _I64, _I64, _I, _P, _P, _P, _SZ, _P]),
     "ngr_row_stats": (_I, [_I, _P, _F, _I64, _I64, _I, _P, _P]),
     "ngr_fold_prepare": (_I, [_I, _P, _P, _P, _P, _I64, _I64, _I, _P, _P, _P]),
     "ngr_fused_norm_linear_folded": (_I, [_I, _P, _P, _P, _F, _I64, _I64, _I64, _I, _P, _P, _SZ, _P]),
@@ -121,6 +128,30 @@ def ngr_ffn_linear_silu_linear(x, W1, W2, M, K, F, dtype, h, y, ws, ws_bytes,
                                stream) -> int:
     return lib().ngr_ffn_linear_silu_linear(x, W1, W2, M, K, F, dtype, h, y,
                                             ws, ws_bytes, stream)
+
+
+def ngr_fused_norm_linear_act(norm, act, x, gamma, beta, W, bias, eps, M, K, N, dtype, y,
+                              ws, ws_bytes, stream) -> int:
+    return lib().ngr_fused_norm_linear_act(norm, act, x, gamma, beta, W, bias, eps, M, K, N,
+                                           dtype, y, ws, ws_bytes, stream)
+
+
+def ngr_fused_mlp(norm, act, x, gamma, beta, W1, b1, W2, b2, eps, M, K, F, dtype, h, y,
+                  ws, ws_bytes, stream) -> int:
+    return lib().ngr_fused_mlp(norm, act, x, gamma, beta, W1, b1, W2, b2, eps, M, K, F,
+                               dtype, h, y, ws, ws_bytes, stream)
+
+
+def ngr_fused_norm_swiglu(norm, x, gamma, beta, Wg, Wu, eps, M, K, F, dtype, h, ws,
+                          ws_bytes, stream) -> int:
+    return lib().ngr_fused_norm_swiglu(norm, x, gamma, beta, Wg, Wu, eps, M, K, F, dtype, h,
+                                       ws, ws_bytes, stream)
+
+
+def ngr_fused_mlp_swiglu(norm, x, gamma, beta, Wg, Wu, Wd, eps, M, K, F, dtype, h, y, ws,
+                         ws_bytes, stream) -> int:
+    return lib().ngr_fused_mlp_swiglu(norm, x, gamma, beta, Wg, Wu, Wd, eps, M, K, F, dtype,
+                                      h, y, ws, ws_bytes, stream)
 
 
 def ngr_fold_prepare(norm, gamma, beta, W, bias, K, N, dtype, Wf, cb, stream) -> int:
@@ -318,6 +349,80 @@ def ffn_linear_silu_linear(x, W1, W2, out=None, h=None, workspace=None,
                                     ws.numel() * ws.element_size(),
                                     _stream(stream))
     _raise(rc, "ffn_linear_silu_linear")
+    return y.reshape(*x.shape[:-1], K)
+
+
+def fused_norm_linear_act(x, W, norm: int = NORM_NONE, act: int = ACT_NONE, gamma=None,
+                          beta=None, bias=None, eps=1e-5, out=None, workspace=None,
+                          stream=None):
+    """y = act(norm(x) . W^T + bias) for any norm (NORM_*) and activation
+    (ACT_*)."""
+    K = x.shape[-1]
+    N = W.shape[0]
+    x2 = x.reshape(-1, K)
+    M = x2.shape[0]
+    _check(x2, W, gamma, beta, bias, out, dtype=x.dtype)
+    y = out if out is not None else torch.empty((M, N), dtype=x.dtype, device=x.device)
+    nb = ngr_workspace_bytes(OP_NORM_LINEAR, M, K, N)
+    ws = _workspace(nb, x.device, workspace)
+    rc = ngr_fused_norm_linear_act(norm, act, _ptr(x2), _ptr(gamma), _ptr(beta), _ptr(W),
+                                   _ptr(bias), eps, M, K, N, _dtype_code(x), _ptr(y),
+                                   _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    _raise(rc, "fused_norm_linear_act")
+    return y.reshape(*x.shape[:-1], N)
+
+
+def fused_mlp(x, W1, W2, norm: int = NORM_NONE, act: int = ACT_SILU, gamma=None, beta=None,
+              b1=None, b2=None, eps=1e-5, out=None, h=None, workspace=None, stream=None):
+    """y = act(norm(x) . W1^T + b1) . W2^T + b2; W1 [F, K], W2 [K, F]."""
+    K = x.shape[-1]
+    F = W1.shape[0]
+    x2 = x.reshape(-1, K)
+    M = x2.shape[0]
+    _check(x2, W1, W2, gamma, beta, b1, b2, out, h, dtype=x.dtype)
+    y = out if out is not None else torch.empty((M, K), dtype=x.dtype, device=x.device)
+    nb = ngr_workspace_bytes(OP_MLP, M, K, F, 1 if h is None else 0)
+    ws = _workspace(nb, x.device, workspace)
+    rc = ngr_fused_mlp(norm, act, _ptr(x2), _ptr(gamma), _ptr(beta), _ptr(W1), _ptr(b1),
+                       _ptr(W2), _ptr(b2), eps, M, K, F, _dtype_code(x), _ptr(h), _ptr(y),
+                       _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    _raise(rc, "fused_mlp")
+    return y.reshape(*x.shape[:-1], K)
+
+
+def fused_norm_swiglu(x, Wg, Wu, norm: int = NORM_NONE, gamma=None, beta=None, eps=1e-5,
+                      out=None, workspace=None, stream=None):
+    """h = SiLU(norm(x) . Wg^T) * (norm(x) . Wu^T); Wg, Wu [F, K]."""
+    K = x.shape[-1]
+    F = Wg.shape[0]
+    x2 = x.reshape(-1, K)
+    M = x2.shape[0]
+    _check(x2, Wg, Wu, gamma, beta, out, dtype=x.dtype)
+    h = out if out is not None else torch.empty((M, F), dtype=x.dtype, device=x.device)
+    nb = ngr_workspace_bytes(OP_SWIGLU, M, K, F)
+    ws = _workspace(nb, x.device, workspace)
+    rc = ngr_fused_norm_swiglu(norm, _ptr(x2), _ptr(gamma), _ptr(beta), _ptr(Wg), _ptr(Wu),
+                               eps, M, K, F, _dtype_code(x), _ptr(h), _ptr(ws),
+                               ws.numel() * ws.element_size(), _stream(stream))
+    _raise(rc, "fused_norm_swiglu")
+    return h.reshape(*x.shape[:-1], F)
+
+
+def fused_mlp_swiglu(x, Wg, Wu, Wd, norm: int = NORM_NONE, gamma=None, beta=None, eps=1e-5,
+                     out=None, h=None, workspace=None, stream=None):
+    """y = (SiLU(norm(x) . Wg^T) * (norm(x) . Wu^T)) . Wd^T; Wd [K, F]."""
+    K = x.shape[-1]
+    F = Wg.shape[0]
+    x2 = x.reshape(-1, K)
+    M = x2.shape[0]
+    _check(x2, Wg, Wu, Wd, gamma, beta, out, h, dtype=x.dtype)
+    y = out if out is not None else torch.empty((M, K), dtype=x.dtype, device=x.device)
+    nb = ngr_workspace_bytes(OP_MLP_SWIGLU, M, K, F, 1 if h is None else 0)
+    ws = _workspace(nb, x.device, workspace)
+    rc = ngr_fused_mlp_swiglu(norm, _ptr(x2), _ptr(gamma), _ptr(beta), _ptr(Wg), _ptr(Wu),
+                              _ptr(Wd), eps, M, K, F, _dtype_code(x), _ptr(h), _ptr(y),
+                              _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    _raise(rc, "fused_mlp_swiglu")
     return y.reshape(*x.shape[:-1], K)
 
 

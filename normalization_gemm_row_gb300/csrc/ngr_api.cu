@@ -73,13 +73,25 @@ struct WsLayout {
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // Workspace regions, in order: header | stats | gamma_f | beta_f |
-// normalized rows (decode sizes) | decode partials | counters | counters of
-// the FFN's second GEMM | H.
+// normalized rows (decode sizes) | decode partials | counters of the first
+// GEMM | counters of the second GEMM (FFN / MLP chains) | H.
+//
+// Ops with a norm: LayerNorm/RMSNorm linear, the general norm + activation
+// layer, the MLP chain and both SwiGLU forms (sized for the worst case: a
+// call without a norm uses less).  At decode sizes (M <= 32) the first GEMM
+// runs on the decode kernel except for SwiGLU, whose gated tiles run on the
+// CTA-pair kernel at every M; the second GEMM of a chain (K output
+// columns) always takes the decode kernel there.
 WsLayout ws_layout(int op, int64_t M, int64_t K, int64_t N, bool h_in_ws)
 {
     WsLayout L;
     size_t off = kHeaderBytes;
-    const bool norm = op == NGR_OP_LAYERNORM_LINEAR || op == NGR_OP_RMSNORM_LINEAR;
+    const bool norm = op == NGR_OP_LAYERNORM_LINEAR || op == NGR_OP_RMSNORM_LINEAR ||
+                      op == NGR_OP_NORM_LINEAR || op == NGR_OP_MLP || op == NGR_OP_SWIGLU ||
+                      op == NGR_OP_MLP_SWIGLU;
+    const bool gated = op == NGR_OP_SWIGLU || op == NGR_OP_MLP_SWIGLU;
+    const bool chain = op == NGR_OP_FFN || op == NGR_OP_MLP || op == NGR_OP_MLP_SWIGLU;
+    const bool decode = M > 0 && M <= kDecodeMaxM;
     if (norm) {
         L.stats = off;
         off += align256(static_cast<size_t>(M) * 8);
@@ -87,26 +99,24 @@ WsLayout ws_layout(int op, int64_t M, int64_t K, int64_t N, bool h_in_ws)
         off += align256(static_cast<size_t>(K) * 4);
         L.beta_f = off;
         off += align256(static_cast<size_t>(K) * 4);
-        if (M > 0 && M <= kDecodeMaxM) {
+        if (decode && !gated) {
             L.xhat = off;
             off += align256(static_cast<size_t>(M) * static_cast<size_t>(K) * 2);
         }
     }
-    if (M > 0 && M <= kDecodeMaxM) {
+    if (decode) {
         const int64_t mn = M <= 16 ? 16 : 32;
-        const int64_t tiles1 = ceil_div(N, 128);
-        const int64_t tiles2 = op == NGR_OP_FFN ? ceil_div(K, 128) : 0;
+        const int64_t tiles1 = gated ? 0 : ceil_div(N, 128);
+        const int64_t tiles2 = chain ? ceil_div(K, 128) : 0;
         const int64_t tmax = tiles1 > tiles2 ? tiles1 : tiles2;
         L.partials = off;
         off += align256(static_cast<size_t>(tmax) * kDecodeMaxContrib * mn * 128 * 4);
         L.counters = off;
         off += align256(static_cast<size_t>(tiles1) * 4 * 4);
-        if (op == NGR_OP_FFN) {
-            L.counters2 = off;
-            off += align256(static_cast<size_t>(tiles2) * 4 * 4);
-        }
+        L.counters2 = off;
+        off += align256(static_cast<size_t>(tiles2) * 4 * 4);
     }
-    if (op == NGR_OP_FFN && h_in_ws) {
+    if (chain && h_in_ws) {
         L.h = off;
         off += align256(static_cast<size_t>(M) * static_cast<size_t>(N) * 2);
     }
@@ -271,7 +281,7 @@ int finish(int rc, void *ws, cudaStream_t stream)
 // workspace regions.  `stats_ready` says whether a preceding grid on the
 // stream produced what this one reads (then it is launched as a
 // programmatic dependent).
-int launch_layer(int norm, bool silu, bool bf16, const void *x, const void *W,
+int launch_layer(int norm, int act, bool bf16, const void *x, const void *W,
                  const void *bias, int64_t M, int64_t K, int64_t N, void *y,
                  char *ws, const WsLayout &L, size_t counters_off, bool pdl,
                  const DevInfo &di, cudaStream_t stream, const float *fold_c = nullptr,
@@ -312,7 +322,8 @@ int launch_layer(int norm, bool silu, bool bf16, const void *x, const void *W,
                          static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(K),
                          mn, d.grid, d.units);
         d.timeout_ns = wait_timeout_ns();
-        return launch_decode(norm, silu, bf16, mn, d, pdl, stream);
+        d.act = act;
+        return launch_decode(norm, bf16, mn, d, pdl, stream);
     }
     GemmArgs a;
     std::memset(&a, 0, sizeof(a));
@@ -341,10 +352,48 @@ int launch_layer(int norm, bool silu, bool bf16, const void *x, const void *W,
     a.k_blocks = static_cast<int>(ceil_div(K, kBK));
     a.num_tiles = a.m_tiles * a.n_tiles;
     a.timeout_ns = wait_timeout_ns();
-    return launch_gemm(norm, silu, bf16, plan, a, pdl, stream);
+    a.act = act;
+    return launch_gemm(norm, bf16, plan, a, pdl, stream);
 }
 
-int norm_linear(int op, int norm, bool silu, const void *x, const void *gamma, const void *beta,
+// The gated (SwiGLU) layer h = SiLU(norm(x) Wg^T) * (norm(x) Wu^T) on the
+// CTA-pair kernel, at any M.
+int launch_gated(int norm, bool bf16, const void *x, const void *Wg, const void *Wu, int64_t M,
+                 int64_t K, int64_t F, void *h, char *ws, const WsLayout &L, bool pdl,
+                 const DevInfo &di, cudaStream_t stream)
+{
+    GemmArgs a;
+    std::memset(&a, 0, sizeof(a));
+    const bool has_norm = norm == kNormLayer || norm == kNormRms;
+    const GemmPlan plan = plan_gemm_gated(M, F, di.sms);
+    if (trace_mode())
+        std::fprintf(stderr, "ngr: gated tile kernel M=%lld F=%lld K=%lld norm=%d BN=%d stages=%d grid=%d smem=%zu\n",
+                     static_cast<long long>(M), static_cast<long long>(F), static_cast<long long>(K), norm,
+                     plan.bn, plan.stages, plan.grid, plan.smem);
+    if (!map_2d(&a.map_a, x, bf16, M, K, kBM) ||
+        !map_2d(&a.map_b, Wg, bf16, F, K, static_cast<uint32_t>(plan.b_rows)) ||
+        !map_2d(&a.map_b2, Wu, bf16, F, K, static_cast<uint32_t>(plan.b_rows)))
+        return NGR_ERR_CUDA;
+    if (has_norm && !map_gb(&a.map_gb, reinterpret_cast<float *>(ws + L.gamma_f), K,
+                            L.beta_f - L.gamma_f))
+        return NGR_ERR_CUDA;
+    a.stats = has_norm ? reinterpret_cast<float2 *>(ws + L.stats) : nullptr;
+    a.y = h;
+    a.err = reinterpret_cast<int *>(ws);
+    a.zero_err = pdl ? 0 : 1;
+    a.act = kActNone;
+    a.M = static_cast<int>(M);
+    a.N = static_cast<int>(F);
+    a.K = static_cast<int>(K);
+    a.m_tiles = static_cast<int>(ceil_div(M, plan.bm));
+    a.n_tiles = static_cast<int>(ceil_div(F, plan.tw));
+    a.k_blocks = static_cast<int>(ceil_div(K, kBK));
+    a.num_tiles = a.m_tiles * a.n_tiles;
+    a.timeout_ns = wait_timeout_ns();
+    return launch_gemm(norm, bf16, plan, a, pdl, stream);
+}
+
+int norm_linear(int op, int norm, int act, const void *x, const void *gamma, const void *beta,
                 const void *W, const void *bias, float eps, int64_t M, int64_t K, int64_t N,
                 int dtype, void *y, void *ws, size_t ws_bytes, cudaStream_t stream)
 {
@@ -387,10 +436,10 @@ int norm_linear(int op, int norm, bool silu, const void *x, const void *gamma, c
     event_before(stream);
     // Decode sizes multiply the normalized rows the statistics kernel wrote.
     if (decode && norm != kNormNone)
-        rc = launch_layer(kNormNone, silu, bf16, w + L.xhat, W, bias, M, K, N, y, w, L, L.counters,
+        rc = launch_layer(kNormNone, act, bf16, w + L.xhat, W, bias, M, K, N, y, w, L, L.counters,
                           true, di, stream);
     else
-        rc = launch_layer(norm, silu, bf16, x, W, bias, M, K, N, y, w, L, L.counters, need_stats,
+        rc = launch_layer(norm, act, bf16, x, W, bias, M, K, N, y, w, L, L.counters, need_stats,
                           di, stream);
     event_after(stream);
     events_call_done();
@@ -431,9 +480,136 @@ int folded_linear(int norm, const void *x, const void *Wf, const float *cb, floa
     event_after(stream);
     if (rc != NGR_OK) return rc;
     event_before(stream);
-    rc = launch_layer(norm == kNormLayer ? kNormFoldLayer : kNormFoldRms, false, bf16, x, Wf,
+    rc = launch_layer(norm == kNormLayer ? kNormFoldLayer : kNormFoldRms, kActNone, bf16, x, Wf,
                       nullptr, M, K, N, y, w, L, L.counters, true, di, stream, cb, cb + N);
     event_after(stream);
+    events_call_done();
+    return finish(rc, ws, stream);
+}
+
+// y = act(norm(x) W1^T + b1) W2^T + b2 (the FFN is norm none, SiLU, no
+// biases): statistics (and, at decode sizes, the normalized rows and zeroed
+// split-K counters), then two GEMMs, the second a programmatic dependent of
+// the first; H [M, F] is written once and read once.
+int mlp_chain(int op, int norm, int act, const void *x, const void *gamma, const void *beta,
+              const void *W1, const void *b1, const void *W2, const void *b2, float eps,
+              int64_t M, int64_t K, int64_t F, int dtype, void *h, void *y, void *ws,
+              size_t ws_bytes, cudaStream_t stream)
+{
+    int rc = check_sizes(M, K, F, dtype);
+    if (rc != NGR_OK) return rc;
+    if (M == 0) return NGR_OK;
+    if (!x || !W1 || !W2 || !y) return NGR_ERR_NULL;
+    if (norm != kNormNone && !gamma) return NGR_ERR_NULL;
+    if (norm == kNormLayer && !beta) return NGR_ERR_NULL;
+    if (!ws) return NGR_ERR_WORKSPACE;
+    if (!aligned16(x) || !aligned16(W1) || !aligned16(W2) || !aligned16(y) ||
+        (h && !aligned16(h)) || (gamma && !aligned16(gamma)) || (beta && !aligned16(beta)) ||
+        (b1 && !aligned16(b1)) || (b2 && !aligned16(b2)))
+        return NGR_ERR_ALIGN;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return NGR_ERR_ALIGN;
+    const WsLayout L = ws_layout(op, M, K, F, h == nullptr);
+    if (ws_bytes < L.total) return NGR_ERR_WORKSPACE;
+    DevInfo di;
+    rc = current_device_info(&di);
+    if (rc != NGR_OK) return rc;
+    const bool bf16 = dtype == NGR_BF16;
+    char *w = static_cast<char *>(ws);
+    void *H = h ? h : static_cast<void *>(w + L.h);
+    if (debug_mode() && cudaMemsetAsync(w, 0, 4, stream) != cudaSuccess) return NGR_ERR_CUDA;
+    const bool decode = M <= kDecodeMaxM;
+    const bool need_stats = norm != kNormNone || decode;
+    events_reset();
+    if (need_stats) {
+        event_before(stream);
+        // Both GEMMs' split-K counters (adjacent) are zeroed here.
+        const int n_counters =
+            decode ? static_cast<int>((L.counters2 - L.counters) / 4 + ceil_div(K, 128) * 4) : 0;
+        rc = launch_rowstats(norm == kNormNone ? kNormRms : norm, bf16, x,
+                             norm == kNormNone ? 0 : M, K, eps,
+                             norm == kNormNone ? nullptr : reinterpret_cast<float2 *>(w + L.stats),
+                             gamma, beta,
+                             norm == kNormNone ? nullptr : reinterpret_cast<float *>(w + L.gamma_f),
+                             norm == kNormNone ? nullptr : reinterpret_cast<float *>(w + L.beta_f),
+                             decode ? reinterpret_cast<int *>(w + L.counters) : nullptr, n_counters,
+                             reinterpret_cast<int *>(w), di.sms, stream,
+                             decode && norm != kNormNone ? w + L.xhat : nullptr);
+        event_after(stream);
+        if (rc != NGR_OK) return rc;
+    }
+    event_before(stream);
+    if (decode && norm != kNormNone)
+        rc = launch_layer(kNormNone, act, bf16, w + L.xhat, W1, b1, M, K, F, H, w, L, L.counters,
+                          true, di, stream);
+    else
+        rc = launch_layer(norm, act, bf16, x, W1, b1, M, K, F, H, w, L, L.counters, need_stats, di,
+                          stream);
+    event_after(stream);
+    if (rc != NGR_OK) return rc;
+    event_before(stream);
+    rc = launch_layer(kNormNone, kActNone, bf16, H, W2, b2, M, F, K, y, w, L, L.counters2, true, di,
+                      stream);
+    event_after(stream);
+    events_call_done();
+    return finish(rc, ws, stream);
+}
+
+// SwiGLU h = SiLU(norm(x) Wg^T) * (norm(x) Wu^T) (gated CTA-pair kernel),
+// and with Wd the Llama MLP y = h Wd^T (a second, plain GEMM).
+int swiglu_chain(int op, int norm, const void *x, const void *gamma, const void *beta,
+                 const void *Wg, const void *Wu, const void *Wd, float eps, int64_t M, int64_t K,
+                 int64_t F, int dtype, void *h, void *y, void *ws, size_t ws_bytes,
+                 cudaStream_t stream)
+{
+    const bool down = op == NGR_OP_MLP_SWIGLU;
+    int rc = check_sizes(M, K, F, dtype);
+    if (rc != NGR_OK) return rc;
+    if (M == 0) return NGR_OK;
+    if (!x || !Wg || !Wu || (down ? (!Wd || !y) : !h)) return NGR_ERR_NULL;
+    if (norm != kNormNone && !gamma) return NGR_ERR_NULL;
+    if (norm == kNormLayer && !beta) return NGR_ERR_NULL;
+    if (!ws) return NGR_ERR_WORKSPACE;
+    if (!aligned16(x) || !aligned16(Wg) || !aligned16(Wu) || (Wd && !aligned16(Wd)) ||
+        (y && !aligned16(y)) || (h && !aligned16(h)) || (gamma && !aligned16(gamma)) ||
+        (beta && !aligned16(beta)))
+        return NGR_ERR_ALIGN;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return NGR_ERR_ALIGN;
+    const WsLayout L = ws_layout(op, M, K, F, down && h == nullptr);
+    if (ws_bytes < L.total) return NGR_ERR_WORKSPACE;
+    DevInfo di;
+    rc = current_device_info(&di);
+    if (rc != NGR_OK) return rc;
+    const bool bf16 = dtype == NGR_BF16;
+    char *w = static_cast<char *>(ws);
+    void *H = h ? h : static_cast<void *>(w + L.h);
+    if (debug_mode() && cudaMemsetAsync(w, 0, 4, stream) != cudaSuccess) return NGR_ERR_CUDA;
+    const bool decode = M <= kDecodeMaxM;
+    const bool need_stats = norm != kNormNone || (down && decode);
+    events_reset();
+    if (need_stats) {
+        event_before(stream);
+        rc = launch_rowstats(norm == kNormNone ? kNormRms : norm, bf16, x,
+                             norm == kNormNone ? 0 : M, K, eps,
+                             norm == kNormNone ? nullptr : reinterpret_cast<float2 *>(w + L.stats),
+                             gamma, beta,
+                             norm == kNormNone ? nullptr : reinterpret_cast<float *>(w + L.gamma_f),
+                             norm == kNormNone ? nullptr : reinterpret_cast<float *>(w + L.beta_f),
+                             down && decode ? reinterpret_cast<int *>(w + L.counters2) : nullptr,
+                             down && decode ? static_cast<int>(ceil_div(K, 128) * 4) : 0,
+                             reinterpret_cast<int *>(w), di.sms, stream);
+        event_after(stream);
+        if (rc != NGR_OK) return rc;
+    }
+    event_before(stream);
+    rc = launch_gated(norm, bf16, x, Wg, Wu, M, K, F, H, w, L, need_stats, di, stream);
+    event_after(stream);
+    if (rc != NGR_OK) return rc;
+    if (down) {
+        event_before(stream);
+        rc = launch_layer(kNormNone, kActNone, bf16, H, Wd, nullptr, M, F, K, y, w, L, L.counters2,
+                          true, di, stream);
+        event_after(stream);
+    }
     events_call_done();
     return finish(rc, ws, stream);
 }
@@ -470,7 +646,7 @@ extern "C" {
 
 size_t ngr_workspace_bytes(int op, int64_t M, int64_t K, int64_t N, int ffn_h_in_workspace)
 {
-    if (op < NGR_OP_LAYERNORM_LINEAR || op > NGR_OP_FFN) return 0;
+    if (op < NGR_OP_LAYERNORM_LINEAR || op > NGR_OP_MLP_SWIGLU) return 0;
     if (M < 0 || K <= 0 || N <= 0 || M >= kMaxDim || K >= kMaxDim || N >= kMaxDim) return 0;
     return ws_layout(op, M, K, N, ffn_h_in_workspace != 0).total;
 }
@@ -480,7 +656,7 @@ int ngr_fused_layernorm_linear(const void *x, const void *gamma, const void *bet
                                int dtype, void *y, void *workspace, size_t workspace_bytes,
                                ngr_stream_t stream)
 {
-    return norm_linear(NGR_OP_LAYERNORM_LINEAR, kNormLayer, false, x, gamma, beta, W, bias, eps,
+    return norm_linear(NGR_OP_LAYERNORM_LINEAR, kNormLayer, kActNone, x, gamma, beta, W, bias, eps,
                        M, K, N, dtype, y, workspace, workspace_bytes,
                        reinterpret_cast<cudaStream_t>(stream));
 }
@@ -489,7 +665,7 @@ int ngr_fused_rmsnorm_linear(const void *x, const void *gamma, const void *W, co
                              float eps, int64_t M, int64_t K, int64_t N, int dtype, void *y,
                              void *workspace, size_t workspace_bytes, ngr_stream_t stream)
 {
-    return norm_linear(NGR_OP_RMSNORM_LINEAR, kNormRms, false, x, gamma, nullptr, W, bias, eps, M,
+    return norm_linear(NGR_OP_RMSNORM_LINEAR, kNormRms, kActNone, x, gamma, nullptr, W, bias, eps, M,
                        K, N, dtype, y, workspace, workspace_bytes,
                        reinterpret_cast<cudaStream_t>(stream));
 }
@@ -498,60 +674,64 @@ int ngr_fused_linear_silu(const void *x, const void *W, const void *bias, int64_
                           int64_t N, int dtype, void *y, void *workspace, size_t workspace_bytes,
                           ngr_stream_t stream)
 {
-    return norm_linear(NGR_OP_LINEAR_SILU, kNormNone, true, x, nullptr, nullptr, W, bias, 0.f, M,
+    return norm_linear(NGR_OP_LINEAR_SILU, kNormNone, kActSilu, x, nullptr, nullptr, W, bias, 0.f, M,
                        K, N, dtype, y, workspace, workspace_bytes,
                        reinterpret_cast<cudaStream_t>(stream));
 }
 
 int ngr_ffn_linear_silu_linear(const void *x, const void *W1, const void *W2, int64_t M,
                                int64_t K, int64_t F, int dtype, void *h, void *y, void *workspace,
-                               size_t workspace_bytes, ngr_stream_t stream_)
+                               size_t workspace_bytes, ngr_stream_t stream)
 {
-    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-    int rc = check_sizes(M, K, F, dtype);
-    if (rc != NGR_OK) return rc;
-    if (M == 0) return NGR_OK;
-    if (!x || !W1 || !W2 || !y) return NGR_ERR_NULL;
-    if (!workspace) return NGR_ERR_WORKSPACE;
-    if (!aligned16(x) || !aligned16(W1) || !aligned16(W2) || !aligned16(y) ||
-        (h && !aligned16(h)))
-        return NGR_ERR_ALIGN;
-    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return NGR_ERR_ALIGN;
-    const WsLayout L = ws_layout(NGR_OP_FFN, M, K, F, h == nullptr);
-    if (workspace_bytes < L.total) return NGR_ERR_WORKSPACE;
-    DevInfo di;
-    rc = current_device_info(&di);
-    if (rc != NGR_OK) return rc;
-    const bool bf16 = dtype == NGR_BF16;
-    char *w = static_cast<char *>(workspace);
-    void *H = h ? h : static_cast<void *>(w + L.h);
-    if (debug_mode() && cudaMemsetAsync(w, 0, 4, stream) != cudaSuccess) return NGR_ERR_CUDA;
-    const bool decode = M <= kDecodeMaxM;
-    events_reset();
-    if (decode) {
-        event_before(stream);
-        // Zero both GEMMs' split-K counters (they are adjacent).
-        const int n1 = static_cast<int>(ceil_div(F, 128) * 4);
-        const int n2 = static_cast<int>(ceil_div(K, 128) * 4);
-        const int n = static_cast<int>((L.counters2 - L.counters) / 4) + n2;
-        (void)n1;
-        rc = launch_rowstats(kNormRms, bf16, x, 0, K, 0.f, nullptr, nullptr, nullptr, nullptr,
-                             nullptr, reinterpret_cast<int *>(w + L.counters), n,
-                             reinterpret_cast<int *>(w), di.sms, stream);
-        event_after(stream);
-        if (rc != NGR_OK) return rc;
-    }
-    event_before(stream);
-    rc = launch_layer(kNormNone, true, bf16, x, W1, nullptr, M, K, F, H, w, L, L.counters, decode,
-                      di, stream);
-    event_after(stream);
-    if (rc != NGR_OK) return rc;
-    event_before(stream);
-    rc = launch_layer(kNormNone, false, bf16, H, W2, nullptr, M, F, K, y, w, L, L.counters2, true,
-                      di, stream);
-    event_after(stream);
-    events_call_done();
-    return finish(rc, workspace, stream);
+    return mlp_chain(NGR_OP_FFN, kNormNone, kActSilu, x, nullptr, nullptr, W1, nullptr, W2, nullptr,
+                     0.f, M, K, F, dtype, h, y, workspace, workspace_bytes,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ngr_fused_norm_linear_act(int norm, int act, const void *x, const void *gamma,
+                              const void *beta, const void *W, const void *bias, float eps,
+                              int64_t M, int64_t K, int64_t N, int dtype, void *y,
+                              void *workspace, size_t workspace_bytes, ngr_stream_t stream)
+{
+    if (norm < kNormNone || norm > kNormRms || act < kActNone || act > kActGelu)
+        return NGR_ERR_ARG;
+    return norm_linear(NGR_OP_NORM_LINEAR, norm, act, x, gamma, norm == kNormLayer ? beta : nullptr,
+                       W, bias, eps, M, K, N, dtype, y, workspace, workspace_bytes,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ngr_fused_mlp(int norm, int act, const void *x, const void *gamma, const void *beta,
+                  const void *W1, const void *b1, const void *W2, const void *b2, float eps,
+                  int64_t M, int64_t K, int64_t F, int dtype, void *h, void *y, void *workspace,
+                  size_t workspace_bytes, ngr_stream_t stream)
+{
+    if (norm < kNormNone || norm > kNormRms || act < kActNone || act > kActGelu)
+        return NGR_ERR_ARG;
+    return mlp_chain(NGR_OP_MLP, norm, act, x, gamma, norm == kNormLayer ? beta : nullptr, W1, b1,
+                     W2, b2, eps, M, K, F, dtype, h, y, workspace, workspace_bytes,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ngr_fused_norm_swiglu(int norm, const void *x, const void *gamma, const void *beta,
+                          const void *Wg, const void *Wu, float eps, int64_t M, int64_t K,
+                          int64_t F, int dtype, void *h, void *workspace, size_t workspace_bytes,
+                          ngr_stream_t stream)
+{
+    if (norm < kNormNone || norm > kNormRms) return NGR_ERR_ARG;
+    return swiglu_chain(NGR_OP_SWIGLU, norm, x, gamma, norm == kNormLayer ? beta : nullptr, Wg, Wu,
+                        nullptr, eps, M, K, F, dtype, h, nullptr, workspace, workspace_bytes,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ngr_fused_mlp_swiglu(int norm, const void *x, const void *gamma, const void *beta,
+                         const void *Wg, const void *Wu, const void *Wd, float eps, int64_t M,
+                         int64_t K, int64_t F, int dtype, void *h, void *y, void *workspace,
+                         size_t workspace_bytes, ngr_stream_t stream)
+{
+    if (norm < kNormNone || norm > kNormRms) return NGR_ERR_ARG;
+    return swiglu_chain(NGR_OP_MLP_SWIGLU, norm, x, gamma, norm == kNormLayer ? beta : nullptr, Wg,
+                        Wu, Wd, eps, M, K, F, dtype, h, y, workspace, workspace_bytes,
+                        reinterpret_cast<cudaStream_t>(stream));
 }
 
 int ngr_fold_prepare(int norm, const void *gamma, const void *beta, const void *W,

@@ -52,7 +52,7 @@ __host__ __device__ __forceinline__ long long decode_owner(long long u, long lon
     return ((u + 1) * grid - 1) / units;
 }
 
-template <int NORM, bool SILU, bool BF16, int MN, int STAGES>
+template <int NORM, bool BF16, int MN, int STAGES>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
     decode_kernel(const __grid_constant__ DecodeArgs args)
 {
@@ -256,7 +256,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                     } else {
                         z = v[m] + bn;
                     }
-                    if constexpr (SILU) z = silu_f(z);
+                    if (args.act == kActSilu) z = silu_f(z);
+                    else if (args.act == kActRelu) z = fmaxf(z, 0.0f);
+                    else if (args.act == kActGelu) z = gelu_f(z);
                     uint16_t o;
                     if constexpr (BF16) {
                         __nv_bfloat16 h = __float2bfloat16_rn(z);
@@ -302,10 +304,10 @@ int plan_decode_grid(int64_t n_tiles, int64_t k_blocks, int num_sms)
     return static_cast<int>(g < 1 ? 1 : g);
 }
 
-template <int NORM, bool SILU, bool BF16, int MN>
+template <int NORM, bool BF16, int MN>
 static int launch_decode_variant(const DecodeArgs &args, bool pdl, cudaStream_t stream)
 {
-    auto kern = decode_kernel<NORM, SILU, BF16, MN, 10>;
+    auto kern = decode_kernel<NORM, BF16, MN, 10>;
     constexpr int smem = DecodeSmem<MN, 10>::alloc;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess)
@@ -324,21 +326,19 @@ static int launch_decode_variant(const DecodeArgs &args, bool pdl, cudaStream_t 
     return e == cudaSuccess ? 0 : record_cuda_error("cudaLaunchKernelEx", e, cudaGetErrorString(e));
 }
 
-int launch_decode(int norm, bool silu, bool bf16, int mn, const DecodeArgs &args, bool pdl,
+int launch_decode(int norm, bool bf16, int mn, const DecodeArgs &args, bool pdl,
                   cudaStream_t stream)
 {
-#define NGR_DCASE(N_, S_, B_)                                                     \
-    if (norm == N_ && silu == S_ && bf16 == B_)                                   \
-        return mn <= 16 ? launch_decode_variant<N_, S_, B_, 16>(args, pdl, stream) \
-                        : launch_decode_variant<N_, S_, B_, 32>(args, pdl, stream);
-    NGR_DCASE(kNormNone, true, false)
-    NGR_DCASE(kNormNone, true, true)
-    NGR_DCASE(kNormNone, false, false)
-    NGR_DCASE(kNormNone, false, true)
-    NGR_DCASE(kNormFoldLayer, false, false)
-    NGR_DCASE(kNormFoldLayer, false, true)
-    NGR_DCASE(kNormFoldRms, false, false)
-    NGR_DCASE(kNormFoldRms, false, true)
+#define NGR_DCASE(N_, B_)                                                         \
+    if (norm == N_ && bf16 == B_)                                                 \
+        return mn <= 16 ? launch_decode_variant<N_, B_, 16>(args, pdl, stream)    \
+                        : launch_decode_variant<N_, B_, 32>(args, pdl, stream);
+    NGR_DCASE(kNormNone, false)
+    NGR_DCASE(kNormNone, true)
+    NGR_DCASE(kNormFoldLayer, false)
+    NGR_DCASE(kNormFoldLayer, true)
+    NGR_DCASE(kNormFoldRms, false)
+    NGR_DCASE(kNormFoldRms, true)
 #undef NGR_DCASE
     return -9;
 }

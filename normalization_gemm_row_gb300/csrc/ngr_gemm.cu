@@ -14,26 +14,29 @@
 
 namespace ngr {
 
-int launch_gemm_bn128(int, bool, bool, const GemmArgs &, int, bool, cudaStream_t);
-int launch_gemm_bn192(int, bool, bool, const GemmArgs &, int, bool, cudaStream_t);
-int launch_gemm_bn224(int, bool, bool, const GemmArgs &, int, bool, cudaStream_t);
-int launch_gemm_bn256(int, bool, bool, const GemmArgs &, int, bool, cudaStream_t);
+int launch_gemm_bn128(int, bool, const GemmArgs &, int, bool, cudaStream_t);
+int launch_gemm_bn192(int, bool, const GemmArgs &, int, bool, cudaStream_t);
+int launch_gemm_bn224(int, bool, const GemmArgs &, int, bool, cudaStream_t);
+int launch_gemm_bn256(int, bool, const GemmArgs &, int, bool, cudaStream_t);
 size_t gemm_smem_bn128();
 size_t gemm_smem_bn192();
 size_t gemm_smem_bn224();
 size_t gemm_smem_bn256();
-int launch_gemm2_bn128(int, bool, bool, const GemmArgs &, int, bool, cudaStream_t);
-int launch_gemm2_bn192(int, bool, bool, const GemmArgs &, int, bool, cudaStream_t);
-int launch_gemm2_bn224(int, bool, bool, const GemmArgs &, int, bool, cudaStream_t);
-int launch_gemm2_bn256(int, bool, bool, const GemmArgs &, int, bool, cudaStream_t);
+int launch_gemm2_bn128(int, bool, const GemmArgs &, int, bool, cudaStream_t);
+int launch_gemm2_bn192(int, bool, const GemmArgs &, int, bool, cudaStream_t);
+int launch_gemm2_bn224(int, bool, const GemmArgs &, int, bool, cudaStream_t);
+int launch_gemm2_bn256(int, bool, const GemmArgs &, int, bool, cudaStream_t);
 size_t gemm2_smem_bn128();
 size_t gemm2_smem_bn192();
 size_t gemm2_smem_bn224();
 size_t gemm2_smem_bn256();
 int gemm2_max_clusters_bn224();
-int launch_gemm2w_bn192(int, bool, bool, const GemmArgs &, int, bool, cudaStream_t);
-int launch_gemm2w_bn224(int, bool, bool, const GemmArgs &, int, bool, cudaStream_t);
-int launch_gemm2w_bn256(int, bool, bool, const GemmArgs &, int, bool, cudaStream_t);
+int launch_gemm2w_bn192(int, bool, const GemmArgs &, int, bool, cudaStream_t);
+int launch_gemm2w_bn224(int, bool, const GemmArgs &, int, bool, cudaStream_t);
+int launch_gemm2w_bn256(int, bool, const GemmArgs &, int, bool, cudaStream_t);
+int launch_gemm2g_bn192(int, bool, const GemmArgs &, int, bool, cudaStream_t);
+int launch_gemm2g_bn224(int, bool, const GemmArgs &, int, bool, cudaStream_t);
+int launch_gemm2g_bn256(int, bool, const GemmArgs &, int, bool, cudaStream_t);
 size_t gemm2w_smem_bn192();
 size_t gemm2w_smem_bn224();
 size_t gemm2w_smem_bn256();
@@ -152,7 +155,7 @@ static GemmPlan plan_with(int64_t M, int64_t N, int num_sms, int want_pair, int 
             const int64_t grid = tiles < num_sms ? tiles : num_sms;
             const int64_t per_cta = (tiles + grid - 1) / grid;
             take(static_cast<double>(per_cta) * (bn + 16),
-                 GemmPlan{bn, stages_for(bn), static_cast<int>(grid), 0, false, kBM, bn, 1, bn});
+                 GemmPlan{bn, stages_for(bn), static_cast<int>(grid), 0, false, kBM, bn, 1, bn, false});
         }
     }
     if (M > kBM && want_pair != 0) {
@@ -167,7 +170,7 @@ static GemmPlan plan_with(int64_t M, int64_t N, int num_sms, int want_pair, int 
             const int64_t per = (tiles + clusters - 1) / clusters;
             take(factor * static_cast<double>(per) * (tw + overhead),
                  GemmPlan{bn, stages, static_cast<int>(2 * clusters), 0, true, 2 * kBM, bn / 2,
-                          nsub, tw});
+                          nsub, tw, false});
         };
         for (int bn : kTileWidths) consider(bn, 1, stages2_for(bn), kPairCostFactor, 16);
         for (int bn : kWideWidths)
@@ -189,31 +192,63 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, bool norm)
     return best;
 }
 
-int launch_gemm(int norm, bool silu, bool bf16, const GemmPlan &plan, const GemmArgs &args,
-                bool pdl, cudaStream_t stream)
+GemmPlan plan_gemm_gated(int64_t M, int64_t N, int num_sms)
 {
+    // Gate and up sub-tiles of BN columns each: 256 x BN outputs per tile,
+    // 2 BN accumulator columns.  The widest tile that does not add a wave.
+    const int pairs = max_pairs(num_sms);
+    GemmPlan best{224, stages2w_for(224), 2, 0, true, 2 * kBM, 112, 2, 224, true};
+    double best_cost = -1.0;
+    for (int bn : kWideWidths) {
+        if (g_bn.load() && bn != g_bn.load()) continue;
+        const int64_t tiles = ((M + 2 * kBM - 1) / (2 * kBM)) * ((N + bn - 1) / bn);
+        const int64_t clusters = tiles < pairs ? tiles : pairs;
+        if (clusters < 1) continue;
+        const int64_t per = (tiles + clusters - 1) / clusters;
+        const double cost = static_cast<double>(per) * (bn + kWideTileOverhead / 2);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = GemmPlan{bn, stages2w_for(bn), static_cast<int>(2 * clusters), 0, true,
+                            2 * kBM, bn / 2, 2, bn, true};
+        }
+    }
+    best.smem = gemm2_smem_bytes(best.bn, 2);
+    return best;
+}
+
+int launch_gemm(int norm, bool bf16, const GemmPlan &plan, const GemmArgs &args, bool pdl,
+                cudaStream_t stream)
+{
+    if (plan.gated) {
+        switch (plan.bn) {
+        case 192: return launch_gemm2g_bn192(norm, bf16, args, plan.grid, pdl, stream);
+        case 224: return launch_gemm2g_bn224(norm, bf16, args, plan.grid, pdl, stream);
+        case 256: return launch_gemm2g_bn256(norm, bf16, args, plan.grid, pdl, stream);
+        default: return -9;
+        }
+    }
     if (plan.pair && plan.nsub == 2) {
         switch (plan.bn) {
-        case 192: return launch_gemm2w_bn192(norm, silu, bf16, args, plan.grid, pdl, stream);
-        case 224: return launch_gemm2w_bn224(norm, silu, bf16, args, plan.grid, pdl, stream);
-        case 256: return launch_gemm2w_bn256(norm, silu, bf16, args, plan.grid, pdl, stream);
+        case 192: return launch_gemm2w_bn192(norm, bf16, args, plan.grid, pdl, stream);
+        case 224: return launch_gemm2w_bn224(norm, bf16, args, plan.grid, pdl, stream);
+        case 256: return launch_gemm2w_bn256(norm, bf16, args, plan.grid, pdl, stream);
         default: return -9;
         }
     }
     if (plan.pair) {
         switch (plan.bn) {
-        case 128: return launch_gemm2_bn128(norm, silu, bf16, args, plan.grid, pdl, stream);
-        case 192: return launch_gemm2_bn192(norm, silu, bf16, args, plan.grid, pdl, stream);
-        case 224: return launch_gemm2_bn224(norm, silu, bf16, args, plan.grid, pdl, stream);
-        case 256: return launch_gemm2_bn256(norm, silu, bf16, args, plan.grid, pdl, stream);
+        case 128: return launch_gemm2_bn128(norm, bf16, args, plan.grid, pdl, stream);
+        case 192: return launch_gemm2_bn192(norm, bf16, args, plan.grid, pdl, stream);
+        case 224: return launch_gemm2_bn224(norm, bf16, args, plan.grid, pdl, stream);
+        case 256: return launch_gemm2_bn256(norm, bf16, args, plan.grid, pdl, stream);
         default: return -9;
         }
     }
     switch (plan.bn) {
-    case 128: return launch_gemm_bn128(norm, silu, bf16, args, plan.grid, pdl, stream);
-    case 192: return launch_gemm_bn192(norm, silu, bf16, args, plan.grid, pdl, stream);
-    case 224: return launch_gemm_bn224(norm, silu, bf16, args, plan.grid, pdl, stream);
-    case 256: return launch_gemm_bn256(norm, silu, bf16, args, plan.grid, pdl, stream);
+    case 128: return launch_gemm_bn128(norm, bf16, args, plan.grid, pdl, stream);
+    case 192: return launch_gemm_bn192(norm, bf16, args, plan.grid, pdl, stream);
+    case 224: return launch_gemm_bn224(norm, bf16, args, plan.grid, pdl, stream);
+    case 256: return launch_gemm_bn256(norm, bf16, args, plan.grid, pdl, stream);
     default: return -9;
     }
 }

@@ -16,6 +16,13 @@
 // accumulator instead of two: the epilogue of a tile does not overlap the
 // next tile's MMAs.
 //
+// GATED (SwiGLU, NSUB = 2): sub-tile 0 multiplies the gate weight and
+// sub-tile 1 the up weight over the same BN output columns, so each output
+// tile is 256 x BN and the epilogue writes SiLU(gate) * up from the two
+// accumulators ("CANN推理加速库ascend-transformer-boost ATB算子融合实战...",
+// Llama2 inference, model structure and fusion opportunities: the FFN's
+// SiLU-gated linear transform fused with its matmuls).
+//
 // Synchronization (barriers are per CTA unless marked "leader"):
 //   full[s]        with a norm: this CTA's copies landed (its producer's
 //                  expect_tx); without: the leader's, on which both CTAs'
@@ -154,13 +161,15 @@ __device__ __forceinline__ void transform_role_tmem(
     }
 }
 
-template <int NORM, bool SILU, bool BF16, int BN, int STAGES, int NSUB>
+template <int NORM, bool BF16, int BN, int STAGES, int NSUB, bool GATED>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm2_kernel(const __grid_constant__ GemmArgs args)
 {
     using L = Gemm2Smem<BN, STAGES, NSUB>;
     constexpr bool kNorm = NORM == kNormLayer || NORM == kNormRms;  // transform stage
-    constexpr int kTW = NSUB * BN;   // output tile width
+    constexpr int kTW = NSUB * BN;                 // accumulator columns of a tile
+    constexpr int kOutW = GATED ? BN : kTW;        // output columns of a tile
+    static_assert(!GATED || (NSUB == 2 && !is_fold(NORM)), "gated tiles: gate and up sub-tiles");
     // Bytes one stage of this CTA receives when n_sub sub-tiles are in range.
     auto stage_tx = [](int n_sub) -> uint32_t {
         return static_cast<uint32_t>(L::kA + n_sub * L::kBSub + (kNorm ? L::kGB : 0));
@@ -175,7 +184,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     constexpr int kSlotCols = kSlotK / 2;              // tensor-memory columns per slot
     // (A in tensor memory needs at least two k blocks' slots beside one
     // accumulator: not with a 512-column tile.)
-    constexpr bool kATmem = kNorm && (NSUB > 1 ? NGR_PAIR_A_TMEM_WIDE : NGR_PAIR_A_TMEM) &&
+    constexpr bool kATmem = kNorm && !GATED && (NSUB > 1 ? NGR_PAIR_A_TMEM_WIDE : NGR_PAIR_A_TMEM) &&
                             static_cast<int>(kTmemCols) - kTW >= 2 * kHalvesA * kSlotCols;
     constexpr int kAccBufs = (kATmem || NSUB > 1) ? 1 : 2;
     constexpr uint32_t kACol0 = kAccBufs * kTW;
@@ -223,6 +232,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (args.zero_err && blockIdx.x == 0) *args.err = 0;
         prefetch_tmap(&args.map_a);
         prefetch_tmap(&args.map_b);
+        if constexpr (GATED) prefetch_tmap(&args.map_b2);
         if constexpr (kNorm) prefetch_tmap(&args.map_gb);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
@@ -270,10 +280,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             bool ok = true;
             for (int tile = cluster; ok && tile < num_tiles; tile += n_clusters) {
                 const int m0 = (tile % m_tiles) * 2 * kBM + static_cast<int>(rank) * kBM;
-                const int nt0 = (tile / m_tiles) * kTW;
+                const int nt0 = (tile / m_tiles) * kOutW;
                 const int n0 = nt0 + static_cast<int>(rank) * (BN / 2);
-                // Sub-tiles wholly past N are neither loaded nor multiplied.
-                const int n_sub = min(NSUB, (args.N - nt0 + BN - 1) / BN);
+                // Sub-tiles wholly past N are neither loaded nor multiplied
+                // (gated: both sub-tiles cover the same columns).
+                const int n_sub = GATED ? 2 : min(NSUB, (args.N - nt0 + BN - 1) / BN);
+                // W box of sub-tile j: its tensor and its first row.
+                auto wmap = [&](int j) { return (GATED && j == 1) ? &args.map_b2 : &args.map_b; };
+                auto wrow = [&](int j) { return GATED ? n0 : n0 + j * BN; };
                 const uint32_t tx = stage_tx(n_sub);
                 for (int kb = 0; kb < k_blocks; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, wc)) { ok = false; break; }
@@ -284,7 +298,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         mbar_arrive_expect_tx(&full[stage], tx);
                         tma_load_2d(sA + stage * L::kA, &args.map_a, &full[stage], kc, m0, pol_x);
                         for (int j = 0; j < n_sub; ++j)
-                            tma_load_2d(sb + j * L::kBSub, &args.map_b, &full[stage], kc, n0 + j * BN, pol_w);
+                            tma_load_2d(sb + j * L::kBSub, wmap(j), &full[stage], kc, wrow(j), pol_w);
                         tma_load_2d(sG + stage * 2 * kBK, &args.map_gb, &full[stage], kc, 0, pol_x);
                     } else {
                         // Both CTAs' copies complete on the leader's barrier,
@@ -293,7 +307,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         if (leader) mbar_arrive_expect_tx(&full[stage], 2 * tx);
                         tma_load_2d_pair(sA + stage * L::kA, &args.map_a, fb, kc, m0, pol_x);
                         for (int j = 0; j < n_sub; ++j)
-                            tma_load_2d_pair(sb + j * L::kBSub, &args.map_b, fb, kc, n0 + j * BN, pol_w);
+                            tma_load_2d_pair(sb + j * L::kBSub, wmap(j), fb, kc, wrow(j), pol_w);
                     }
                     ++fills;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -326,7 +340,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, wc)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kTW);
-                const int n_sub = min(NSUB, (args.N - (tile / m_tiles) * kTW + BN - 1) / BN);
+                const int n_sub = GATED ? 2 : min(NSUB, (args.N - (tile / m_tiles) * kTW + BN - 1) / BN);
                 for (int kb = 0; kb < k_blocks; ++kb) {
                     if (!mbar_wait(kNorm ? &ready[stage] : &full[stage], phase, wc)) { ok = false; break; }
                     tc_fence_after();
@@ -410,8 +424,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const bool helped = kHelpAlways || (kHelpLast && tile + n_clusters >= num_tiles);
                 if (!epi_warp && !helped) continue;
                 const int step = (helped ? 3 : 1) * 32;
-                const int nt0 = (tile / m_tiles) * kTW;
-                const int ncols = min(kTW, N - nt0);
+                const int nt0 = (tile / m_tiles) * kOutW;
+                const int ncols = min(kOutW, N - nt0);
                 // Warm L1 with this warp's epilogue vectors while the MMAs run.
                 for (int c = e * 32; c < ncols; c += step) {
                     if constexpr (is_fold(NORM)) {
@@ -428,21 +442,38 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const float2 so = fold_row_scale<NORM>(args, row);
                 const uint32_t t_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                         static_cast<uint32_t>(cur * kTW);
-                // The load of the next chunk is in flight while this one is
-                // finished and stored.
-                uint32_t r[32];
-                int c = e * 32;
-                if (c < ncols) tmem_ld32(t_base + static_cast<uint32_t>(c), r);
+                if constexpr (GATED) {
+                    // h = SiLU(gate) * up, the gate in columns [0, BN), the
+                    // up projection in [BN, 2 BN) of the accumulator.
 #pragma unroll 1
-                while (c < ncols) {
-                    tmem_ld_wait();
-                    float v[32];
+                    for (int c = e * 32; c < ncols; c += step) {
+                        uint32_t rg[32], ru[32];
+                        tmem_ld32(t_base + static_cast<uint32_t>(c), rg);
+                        tmem_ld32(t_base + static_cast<uint32_t>(BN + c), ru);
+                        tmem_ld_wait();
+                        float v[32];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                    const int cn = c + step;
-                    if (cn < ncols) tmem_ld32(t_base + static_cast<uint32_t>(cn), r);
-                    epilogue_store32<NORM, SILU, BF16>(v, row, nt0 + c, args, so);
-                    c = cn;
+                        for (int j = 0; j < 32; ++j)
+                            v[j] = silu_f(__uint_as_float(rg[j])) * __uint_as_float(ru[j]);
+                        store_row32<BF16>(v, row, nt0 + c, args.y, args.M, N);
+                    }
+                } else {
+                    // The load of the next chunk is in flight while this one
+                    // is finished and stored.
+                    uint32_t r[32];
+                    int c = e * 32;
+                    if (c < ncols) tmem_ld32(t_base + static_cast<uint32_t>(c), r);
+#pragma unroll 1
+                    while (c < ncols) {
+                        tmem_ld_wait();
+                        float v[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                        const int cn = c + step;
+                        if (cn < ncols) tmem_ld32(t_base + static_cast<uint32_t>(cn), r);
+                        epilogue_store32<NORM, BF16>(v, row, nt0 + c, args, so);
+                        c = cn;
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -463,10 +494,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
 }
 
-template <int NORM, bool SILU, bool BF16, int BN, int STAGES, int NSUB>
+template <int NORM, bool BF16, int BN, int STAGES, int NSUB, bool GATED>
 int launch_gemm2_variant(const GemmArgs &args, int grid, bool pdl, cudaStream_t stream)
 {
-    auto kern = gemm2_kernel<NORM, SILU, BF16, BN, STAGES, NSUB>;
+    auto kern = gemm2_kernel<NORM, BF16, BN, STAGES, NSUB, GATED>;
     constexpr int smem = Gemm2Smem<BN, STAGES, NSUB>::alloc;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess)
@@ -494,7 +525,7 @@ int launch_gemm2_variant(const GemmArgs &args, int grid, bool pdl, cudaStream_t 
 template <int BN, int STAGES, int NSUB>
 int gemm2_max_clusters()
 {
-    auto kern = gemm2_kernel<kNormNone, false, false, BN, STAGES, NSUB>;
+    auto kern = gemm2_kernel<kNormNone, false, BN, STAGES, NSUB, false>;
     constexpr int smem = Gemm2Smem<BN, STAGES, NSUB>::alloc;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return 0;
@@ -515,25 +546,41 @@ int gemm2_max_clusters()
 }
 
 template <int BN, int STAGES, int NSUB>
-int launch_gemm2_bn(int norm, bool silu, bool bf16, const GemmArgs &args, int grid, bool pdl,
+int launch_gemm2_bn(int norm, bool bf16, const GemmArgs &args, int grid, bool pdl,
                     cudaStream_t stream)
 {
-#define NGR_CASE2(N_, S_, B_)                                                     \
-    if (norm == N_ && silu == S_ && bf16 == B_)                                   \
-        return launch_gemm2_variant<N_, S_, B_, BN, STAGES, NSUB>(args, grid, pdl, stream);
-    NGR_CASE2(kNormLayer, false, false)
-    NGR_CASE2(kNormLayer, false, true)
-    NGR_CASE2(kNormRms, false, false)
-    NGR_CASE2(kNormRms, false, true)
-    NGR_CASE2(kNormNone, true, false)
-    NGR_CASE2(kNormNone, true, true)
-    NGR_CASE2(kNormNone, false, false)
-    NGR_CASE2(kNormNone, false, true)
-    NGR_CASE2(kNormFoldLayer, false, false)
-    NGR_CASE2(kNormFoldLayer, false, true)
-    NGR_CASE2(kNormFoldRms, false, false)
-    NGR_CASE2(kNormFoldRms, false, true)
+#define NGR_CASE2(N_, B_)                                                         \
+    if (norm == N_ && bf16 == B_)                                                 \
+        return launch_gemm2_variant<N_, B_, BN, STAGES, NSUB, false>(args, grid, pdl, stream);
+    NGR_CASE2(kNormLayer, false)
+    NGR_CASE2(kNormLayer, true)
+    NGR_CASE2(kNormRms, false)
+    NGR_CASE2(kNormRms, true)
+    NGR_CASE2(kNormNone, false)
+    NGR_CASE2(kNormNone, true)
+    NGR_CASE2(kNormFoldLayer, false)
+    NGR_CASE2(kNormFoldLayer, true)
+    NGR_CASE2(kNormFoldRms, false)
+    NGR_CASE2(kNormFoldRms, true)
 #undef NGR_CASE2
+    return -9;
+}
+
+// The gated (SwiGLU) tiles: norm none / LayerNorm / RMSNorm.
+template <int BN, int STAGES>
+int launch_gemm2_gated_bn(int norm, bool bf16, const GemmArgs &args, int grid, bool pdl,
+                          cudaStream_t stream)
+{
+#define NGR_CASEG(N_, B_)                                                         \
+    if (norm == N_ && bf16 == B_)                                                 \
+        return launch_gemm2_variant<N_, B_, BN, STAGES, 2, true>(args, grid, pdl, stream);
+    NGR_CASEG(kNormLayer, false)
+    NGR_CASEG(kNormLayer, true)
+    NGR_CASEG(kNormRms, false)
+    NGR_CASEG(kNormRms, true)
+    NGR_CASEG(kNormNone, false)
+    NGR_CASEG(kNormNone, true)
+#undef NGR_CASEG
     return -9;
 }
 

@@ -1,0 +1,14 @@
+// ngr_gemm2g_bn256.cu -- gated (SwiGLU) CTA-pair tile kernel instantiations:
+// 256 x 256 output tiles, the gate and up projections as two 256-column
+// sub-tiles sharing each x stage (4 pipeline stages).
+#include "ngr_gemm2_kernel.cuh"
+
+namespace ngr {
+
+int launch_gemm2g_bn256(int norm, bool bf16, const GemmArgs &args, int grid, bool pdl,
+                       cudaStream_t stream)
+{
+    return launch_gemm2_gated_bn<256, 4>(norm, bf16, args, grid, pdl, stream);
+}
+
+}  // namespace ngr

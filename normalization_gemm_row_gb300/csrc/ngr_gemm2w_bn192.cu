@@ -5,10 +5,10 @@
 
 namespace ngr {
 
-int launch_gemm2w_bn192(int norm, bool silu, bool bf16, const GemmArgs &args, int grid,
+int launch_gemm2w_bn192(int norm, bool bf16, const GemmArgs &args, int grid,
                        bool pdl, cudaStream_t stream)
 {
-    return launch_gemm2_bn<192, 5, 2>(norm, silu, bf16, args, grid, pdl, stream);
+    return launch_gemm2_bn<192, 5, 2>(norm, bf16, args, grid, pdl, stream);
 }
 
 size_t gemm2w_smem_bn192() { return Gemm2Smem<192, 5, 2>::alloc; }

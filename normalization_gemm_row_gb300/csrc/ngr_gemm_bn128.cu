@@ -5,10 +5,10 @@
 
 namespace ngr {
 
-int launch_gemm_bn128(int norm, bool silu, bool bf16, const GemmArgs &args, int grid,
+int launch_gemm_bn128(int norm, bool bf16, const GemmArgs &args, int grid,
                      bool pdl, cudaStream_t stream)
 {
-    return launch_gemm_bn<128, 6>(norm, silu, bf16, args, grid, pdl, stream);
+    return launch_gemm_bn<128, 6>(norm, bf16, args, grid, pdl, stream);
 }
 
 size_t gemm_smem_bn128() { return GemmSmem<128, 6>::alloc; }

@@ -76,6 +76,49 @@ __device__ __forceinline__ float silu_f(float z)
     return __fdividef(z, 1.0f + __expf(-z));
 }
 
+// GELU, exact form: z Phi(z) = z (1 + erf(z / sqrt 2)) / 2.
+__device__ __forceinline__ float gelu_f(float z)
+{
+    return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f));
+}
+
+// The epilogue activation of 32 values (`act` is uniform across the warp).
+__device__ __forceinline__ void apply_act32(int act, float (&v)[32])
+{
+    if (act == kActSilu) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = silu_f(v[j]);
+    } else if (act == kActRelu) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = fmaxf(v[j], 0.0f);
+    } else if (act == kActGelu) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = gelu_f(v[j]);
+    }
+}
+
+// Round 32 values of one output row to the 16-bit type and store the
+// columns [n0, n0 + 32) that lie inside [0, N) (N % 8 == 0) with 16-byte
+// stores; rows at or past M are skipped.
+template <bool BF16>
+__device__ __forceinline__ void store_row32(const float (&v)[32], int row, int n0, void *y, int M,
+                                            int N)
+{
+    if (row >= M) return;
+    uint16_t *yrow = static_cast<uint16_t *>(y) + static_cast<int64_t>(row) * N;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        if (n0 + 8 * j < N) {
+            uint4 o;
+            o.x = from_float2<BF16>(v[8 * j + 0], v[8 * j + 1]);
+            o.y = from_float2<BF16>(v[8 * j + 2], v[8 * j + 3]);
+            o.z = from_float2<BF16>(v[8 * j + 4], v[8 * j + 5]);
+            o.w = from_float2<BF16>(v[8 * j + 6], v[8 * j + 7]);
+            *reinterpret_cast<uint4 *>(yrow + n0 + 8 * j) = o;
+        }
+    }
+}
+
 // Normalize + affine 8 consecutive elements held as 4 packed 16-bit pairs.
 // g and b point at the FP32 gamma/beta of those 8 columns.
 template <int NORM, bool BF16>
@@ -147,8 +190,8 @@ __device__ __forceinline__ uint4 transform8_pk(uint4 v, float2 so, const float2 
 
 // The epilogue of 32 accumulator columns [n0, n0 + 32) of one row: + bias,
 // or with a folded norm y = rstd acc + (-mu rstd) c[n] + b'[n] (so =
-// (rstd, -mu rstd) of the row), then SiLU, rounding, 16-byte stores.
-template <int NORM, bool SILU, bool BF16>
+// (rstd, -mu rstd) of the row), then the activation, rounding, 16-byte stores.
+template <int NORM, bool BF16>
 __device__ __forceinline__ void epilogue_store32(float (&v)[32], int row, int n0,
                                                  const GemmArgs &args, float2 so)
 {
@@ -187,24 +230,8 @@ __device__ __forceinline__ void epilogue_store32(float (&v)[32], int row, int n0
             }
         }
     }
-    if constexpr (SILU) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = silu_f(v[j]);
-    }
-    if (row < M) {
-        uint16_t *yrow = static_cast<uint16_t *>(args.y) + static_cast<int64_t>(row) * N;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            if (n0 + 8 * j < N) {
-                uint4 o;
-                o.x = from_float2<BF16>(v[8 * j + 0], v[8 * j + 1]);
-                o.y = from_float2<BF16>(v[8 * j + 2], v[8 * j + 3]);
-                o.z = from_float2<BF16>(v[8 * j + 4], v[8 * j + 5]);
-                o.w = from_float2<BF16>(v[8 * j + 6], v[8 * j + 7]);
-                *reinterpret_cast<uint4 *>(yrow + n0 + 8 * j) = o;
-            }
-        }
-    }
+    apply_act32(args.act, v);
+    store_row32<BF16>(v, row, n0, args.y, M, N);
 }
 
 // (rstd, -mu rstd) of `row` for the folded epilogue.
@@ -330,7 +357,7 @@ struct GemmSmem {
     static constexpr int alloc = bytes + 1024;              // slack to align the base to 1 KB
 };
 
-template <int NORM, bool SILU, bool BF16, int BN, int STAGES>
+template <int NORM, bool BF16, int BN, int STAGES>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ GemmArgs args)
 {
@@ -504,7 +531,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 float v[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                epilogue_store32<NORM, SILU, BF16>(v, row, n0, args, so);
+                epilogue_store32<NORM, BF16>(v, row, n0, args, so);
             }
             tc_fence_before();
             mbar_arrive(&acc_empty[acc]);
@@ -520,10 +547,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
 }
 
-template <int NORM, bool SILU, bool BF16, int BN, int STAGES>
+template <int NORM, bool BF16, int BN, int STAGES>
 int launch_gemm_variant(const GemmArgs &args, int grid, bool pdl, cudaStream_t stream)
 {
-    auto kern = gemm_kernel<NORM, SILU, BF16, BN, STAGES>;
+    auto kern = gemm_kernel<NORM, BF16, BN, STAGES>;
     constexpr int smem = GemmSmem<BN, STAGES>::alloc;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess)
@@ -542,27 +569,25 @@ int launch_gemm_variant(const GemmArgs &args, int grid, bool pdl, cudaStream_t s
     return e == cudaSuccess ? 0 : record_cuda_error("cudaLaunchKernelEx", e, cudaGetErrorString(e));
 }
 
-// Dispatch one BN over the (norm, activation, dtype) combinations the
-// library uses.
+// Dispatch one BN over the (norm, dtype) combinations the library uses
+// (the activation is a runtime argument).
 template <int BN, int STAGES>
-int launch_gemm_bn(int norm, bool silu, bool bf16, const GemmArgs &args, int grid,
-                   bool pdl, cudaStream_t stream)
+int launch_gemm_bn(int norm, bool bf16, const GemmArgs &args, int grid, bool pdl,
+                   cudaStream_t stream)
 {
-#define NGR_CASE(N_, S_, B_)                                                      \
-    if (norm == N_ && silu == S_ && bf16 == B_)                                   \
-        return launch_gemm_variant<N_, S_, B_, BN, STAGES>(args, grid, pdl, stream);
-    NGR_CASE(kNormLayer, false, false)
-    NGR_CASE(kNormLayer, false, true)
-    NGR_CASE(kNormRms, false, false)
-    NGR_CASE(kNormRms, false, true)
-    NGR_CASE(kNormNone, true, false)
-    NGR_CASE(kNormNone, true, true)
-    NGR_CASE(kNormNone, false, false)
-    NGR_CASE(kNormNone, false, true)
-    NGR_CASE(kNormFoldLayer, false, false)
-    NGR_CASE(kNormFoldLayer, false, true)
-    NGR_CASE(kNormFoldRms, false, false)
-    NGR_CASE(kNormFoldRms, false, true)
+#define NGR_CASE(N_, B_)                                                          \
+    if (norm == N_ && bf16 == B_)                                                 \
+        return launch_gemm_variant<N_, B_, BN, STAGES>(args, grid, pdl, stream);
+    NGR_CASE(kNormLayer, false)
+    NGR_CASE(kNormLayer, true)
+    NGR_CASE(kNormRms, false)
+    NGR_CASE(kNormRms, true)
+    NGR_CASE(kNormNone, false)
+    NGR_CASE(kNormNone, true)
+    NGR_CASE(kNormFoldLayer, false)
+    NGR_CASE(kNormFoldLayer, true)
+    NGR_CASE(kNormFoldRms, false)
+    NGR_CASE(kNormFoldRms, true)
 #undef NGR_CASE
     return -9;
 }

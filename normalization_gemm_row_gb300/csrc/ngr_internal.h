@@ -11,6 +11,9 @@ namespace ngr {
 
 enum { kNormNone = 0, kNormLayer = 1, kNormRms = 2, kNormFoldLayer = 3, kNormFoldRms = 4 };
 
+// Epilogue activation, applied after the bias (a runtime argument).
+enum { kActNone = 0, kActSilu = 1, kActRelu = 2, kActGelu = 3 };
+
 // Folded (inference-mode) forms: the GEMM runs on raw x against
 // W' = gamma o W and the row statistics are applied in the epilogue.
 __host__ __device__ constexpr bool is_fold(int norm)
@@ -46,6 +49,7 @@ struct alignas(128) GemmArgs {
     CUtensorMap map_a;      // activations [M, K], box {64, 128}, 128-byte swizzle
     CUtensorMap map_b;      // weights [N, K], box {64, BN}, 128-byte swizzle
     CUtensorMap map_gb;     // FP32 [2, K] = rows gamma, beta; box {64, 2}
+    CUtensorMap map_b2;     // gated (SwiGLU) kernel: the up projection [N, K], like map_b
     const float2 *stats;    // [M] (mu, rstd); unused without a norm
     const void *bias;       // [N] or nullptr
     const float *fold_c;    // folded forms: c[n] = sum_k W'[n,k] (FP32)
@@ -53,6 +57,7 @@ struct alignas(128) GemmArgs {
     void *y;                // [M, N]
     int *err;               // device error word
     int zero_err;           // nonzero: this kernel is the call's first and clears *err
+    int act;                // kAct*: activation after the bias (not used when gated)
     int M, N, K;
     int m_tiles, n_tiles, k_blocks, num_tiles;
     unsigned long long timeout_ns;
@@ -73,6 +78,7 @@ struct alignas(128) DecodeArgs {
     int *counters;          // [n_tiles], zero at kernel start
     int *err;
     int zero_err;
+    int act;                // kAct*
     int M, N, K;
     int n_tiles, k_blocks;
     long long units;        // n_tiles * k_blocks
@@ -90,7 +96,8 @@ struct GemmPlan {
     int bm;          // rows per output tile: 128, or 256 for a CTA pair
     int b_rows;      // rows of W in one TMA box (BN, or BN / 2 for a CTA pair)
     int nsub;        // N sub-tiles of BN columns per output tile (CTA pair: 1 or 2)
-    int tw;          // output tile width in N: bn * nsub
+    int tw;          // output tile width in N: bn * nsub, or bn when gated
+    bool gated;      // SwiGLU: sub-tile 0 multiplies the gate weight, 1 the up weight
 };
 
 // Record why a CUDA call failed (thread-local; read back through
@@ -104,14 +111,17 @@ int launch_rowstats(int norm, bool bf16, const void *x, int64_t M, int64_t K,
                     int *counters, int n_counters, int *err_to_clear,
                     int num_sms, cudaStream_t stream, void *xhat = nullptr);
 
-int launch_gemm(int norm, bool silu, bool bf16, const GemmPlan &plan,
-                const GemmArgs &args, bool pdl, cudaStream_t stream);
+int launch_gemm(int norm, bool bf16, const GemmPlan &plan, const GemmArgs &args, bool pdl,
+                cudaStream_t stream);
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, bool norm);
+// The SwiGLU variant: CTA-pair tiles of 256 x BN outputs, two BN-column
+// accumulators (gate, up) per tile.
+GemmPlan plan_gemm_gated(int64_t M, int64_t N, int num_sms);
 int set_tile_config(int pair, int bn, int nsub);
 size_t gemm_smem_bytes(int bn, int stages, bool norm);
 
-int launch_decode(int norm, bool silu, bool bf16, int mn, const DecodeArgs &args,
-                  bool pdl, cudaStream_t stream);
+int launch_decode(int norm, bool bf16, int mn, const DecodeArgs &args, bool pdl,
+                  cudaStream_t stream);
 int plan_decode_grid(int64_t n_tiles, int64_t k_blocks, int num_sms);
 size_t decode_smem_bytes(int mn);
 

@@ -169,7 +169,8 @@ extern "C" int ngr_fused_layernorm_linear_noalloc(const void *x, const void *gam
     a.k_blocks = static_cast<int>((K + kBK - 1) / kBK);
     a.num_tiles = a.m_tiles * a.n_tiles;
     a.timeout_ns = 2000ull * 1000000ull;
-    rc = launch_gemm(kNormLayer, false, bf16, plan, a, true, stream);
+    a.act = kActNone;
+    rc = launch_gemm(kNormLayer, bf16, plan, a, true, stream);
     if (rc != NGR_OK) return rc;
     return cudaGetLastError() == cudaSuccess ? NGR_OK : NGR_ERR_CUDA;
 }

@@ -30,7 +30,8 @@ _CHUNK_ROWS = 2048
 class Workload:
     """One named workload: the op, its sizes and its input distribution."""
     name: str
-    op: str                   # layernorm_linear | rmsnorm_linear | linear_silu | ffn
+    op: str                   # layernorm_linear | rmsnorm_linear | linear_silu | ffn |
+                              # norm_linear | mlp | swiglu | mlp_swiglu
     M: int
     K: int
     N: int                    # output features (F, the hidden width, for ffn)
@@ -42,12 +43,15 @@ class Workload:
     outlier_frac: float = 0.0  # fraction of rows scaled by outlier_scale
     outlier_scale: float = 1.0
     m_choices: tuple = field(default_factory=tuple)  # decode: allowed M
+    norm: str = "none"        # norm_linear / mlp / swiglu / mlp_swiglu: none | layer | rms
+    act: str = "none"         # norm_linear / mlp: none | silu | relu | gelu
 
     @property
     def flops(self) -> float:
-        """2*M*N*K per GEMM (the FFN has two)."""
+        """2*M*N*K per product: the FFN and the MLP chain have two, SwiGLU
+        two (gate, up) and its MLP form three."""
         g = 2.0 * self.M * self.N * self.K
-        return 2.0 * g if self.op == "ffn" else g
+        return g * {"ffn": 2, "mlp": 2, "swiglu": 2, "mlp_swiglu": 3}.get(self.op, 1)
 
     def with_m(self, M: int) -> "Workload":
         d = dict(self.__dict__)
@@ -68,6 +72,14 @@ WORKLOADS = [
     Workload("decode_ln_linear_bias_bf16_k8192_n28672", "layernorm_linear",
              16, 8192, 28672, BF16, True, 1e-5, 1238, x_mean=3.0,
              m_choices=(1, 4, 16)),
+    # LayerNorm -> MatMul -> BiasAdd -> ReLU -> MatMul -> BiasAdd at width 8192
+    # (the LayerNorm page's fusion chain), batch as the 8 x 128 token case.
+    Workload("chain_ln_linear_bias_relu_linear_bias_f16_m1024_k8192_f8192", "mlp",
+             1024, 8192, 8192, F16, True, 1e-5, 1239, norm="layer", act="relu"),
+    # RMSNorm -> gate/up -> SiLU-gated product -> down at the Llama2-70B MLP
+    # widths (hidden 8192, intermediate 28672).
+    Workload("mlp_swiglu_rms_bf16_m512_k8192_f28672", "mlp_swiglu",
+             512, 8192, 28672, BF16, False, 1e-5, 1240, norm="rms"),
 ]
 BY_NAME = {w.name: w for w in WORKLOADS}
 
@@ -108,6 +120,29 @@ def make(w: Workload, seed: int | None = None) -> dict:
         d["W1"] = _weight(g, N, K, K ** -0.5, dt)
         d["W2"] = _weight(g, K, N, N ** -0.5, dt)
         return d
+    if w.op in ("norm_linear", "mlp", "swiglu", "mlp_swiglu"):
+        # x; gamma (and beta for layer) by the norm; then the weights:
+        # norm_linear W [N, K] (+ bias [N]); mlp W1 [F, K], b1 [F], W2 [K, F],
+        # b2 [K]; swiglu Wg, Wu [F, K]; mlp_swiglu also Wd [K, F].
+        if w.norm in ("layer", "rms"):
+            d["gamma"] = (1.0 + 0.1 * _normal(g, (K,))).to(dt)
+        if w.norm == "layer":
+            d["beta"] = (0.1 * _normal(g, (K,))).to(dt)
+        if w.op == "norm_linear":
+            d["W"] = _weight(g, N, K, K ** -0.5, dt)
+            if w.bias:
+                d["bias"] = (0.1 * _normal(g, (N,))).to(dt)
+        elif w.op == "mlp":
+            d["W1"] = _weight(g, N, K, K ** -0.5, dt)
+            d["W2"] = _weight(g, K, N, N ** -0.5, dt)
+            d["b1"] = (0.1 * _normal(g, (N,))).to(dt) if w.bias else None
+            d["b2"] = (0.1 * _normal(g, (K,))).to(dt) if w.bias else None
+        else:
+            d["Wg"] = _weight(g, N, K, K ** -0.5, dt)
+            d["Wu"] = _weight(g, N, K, K ** -0.5, dt)
+            if w.op == "mlp_swiglu":
+                d["Wd"] = _weight(g, K, N, N ** -0.5, dt)
+        return d
     if w.op in ("layernorm_linear", "rmsnorm_linear"):
         d["gamma"] = (1.0 + 0.1 * _normal(g, (K,))).to(dt)
     if w.op == "layernorm_linear":
@@ -120,11 +155,12 @@ def make(w: Workload, seed: int | None = None) -> dict:
 
 def case(op: str, M: int, K: int, N: int, dtype=F16, bias: bool = True,
          eps: float = 1e-5, seed: int = 7, x_mean: float = 0.0,
-         outlier_frac: float = 0.0, outlier_scale: float = 1.0) -> dict:
+         outlier_frac: float = 0.0, outlier_scale: float = 1.0,
+         norm: str = "none", act: str = "none") -> dict:
     """Inputs for an ad-hoc shape (edge-case sweeps) with the same recipe."""
     w = Workload(f"{op}_{M}x{K}x{N}", op, M, K, N, dtype, bias, eps, seed,
                  x_mean=x_mean, outlier_frac=outlier_frac,
-                 outlier_scale=outlier_scale)
+                 outlier_scale=outlier_scale, norm=norm, act=act)
     return make(w)
 
 

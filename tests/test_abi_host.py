@@ -60,8 +60,57 @@ def test_workspace_bytes_layout(lib):
     h0 = wb(B.OP_FFN, 512, 14336, 49152, 0)
     h1 = wb(B.OP_FFN, 512, 14336, 49152, 1)
     assert h1 - h0 == 512 * 49152 * 2
-    # invalid sizes give 0
-    assert wb(B.OP_FFN, -1, 8, 8) == 0 and wb(7, 1, 8, 8) == 0 and wb(0, 1, 0, 8) == 0
+    # invalid sizes or ops give 0
+    assert wb(B.OP_FFN, -1, 8, 8) == 0 and wb(8, 1, 8, 8) == 0 and wb(0, 1, 0, 8) == 0
+    assert wb(-1, 1, 8, 8) == 0
+
+
+def test_workspace_bytes_new_ops(lib):
+    wb = B.ngr_workspace_bytes
+    # the general layer is sized like the LayerNorm layer
+    assert wb(B.OP_NORM_LINEAR, 1024, 8192, 8192) == wb(B.OP_LAYERNORM_LINEAR, 1024, 8192, 8192)
+    assert wb(B.OP_NORM_LINEAR, 16, 8192, 28672) == wb(B.OP_LAYERNORM_LINEAR, 16, 8192, 28672)
+    # the chain adds norm regions to the FFN's, and H only when asked
+    m0 = wb(B.OP_MLP, 512, 4096, 11008, 0)
+    assert m0 == wb(B.OP_FFN, 512, 4096, 11008, 0) + 2 * 4096 * 4 + 512 * 8
+    assert wb(B.OP_MLP, 512, 4096, 11008, 1) - m0 == 512 * 11008 * 2
+    # SwiGLU runs on the tile kernel at every M: no split-K regions, no H
+    assert wb(B.OP_SWIGLU, 4, 4096, 11008) == 256 + 256 + 2 * 4096 * 4
+    assert wb(B.OP_SWIGLU, 4, 4096, 11008, 1) == wb(B.OP_SWIGLU, 4, 4096, 11008)
+    # ... but its MLP form keeps the down projection's split-K regions at decode sizes
+    assert wb(B.OP_MLP_SWIGLU, 4, 4096, 11008) > wb(B.OP_SWIGLU, 4, 4096, 11008)
+    assert wb(B.OP_MLP_SWIGLU, 512, 4096, 11008) == wb(B.OP_SWIGLU, 512, 4096, 11008)
+    assert (wb(B.OP_MLP_SWIGLU, 512, 4096, 11008, 1) - wb(B.OP_MLP_SWIGLU, 512, 4096, 11008)
+            == 512 * 11008 * 2)
+
+
+def test_new_entry_points_reject(lib):
+    big = 1 << 24
+    ws = A16 * 16
+    # norm / act out of range
+    assert B.ngr_fused_norm_linear_act(3, 0, A16, A16, A16, A16, None, 1e-5, 4, 64, 64, 0,
+                                       A16, ws, big, None) == -9
+    assert B.ngr_fused_norm_linear_act(0, 4, A16, None, None, A16, None, 0.0, 4, 64, 64, 0,
+                                       A16, ws, big, None) == -9
+    # gamma required with a norm, beta with LayerNorm
+    assert B.ngr_fused_norm_linear_act(2, 0, A16, 0, None, A16, None, 1e-5, 4, 64, 64, 0,
+                                       A16, ws, big, None) == -1
+    assert B.ngr_fused_mlp(1, 2, A16, A16, 0, A16, None, A16, None, 1e-5, 4, 64, 64, 0,
+                           None, A16, ws, big, None) == -1
+    assert B.ngr_fused_mlp(0, 5, A16, None, None, A16, None, A16, None, 0.0, 4, 64, 64, 0,
+                           None, A16, ws, big, None) == -9
+    assert B.ngr_fused_mlp(0, 1, A16, None, None, A16, A16 + 4, A16, None, 0.0, 4, 64, 64, 0,
+                           None, A16, ws, big, None) == -3           # misaligned b1
+    assert B.ngr_fused_norm_swiglu(2, A16, A16, None, A16, 0, 1e-5, 4, 64, 64, 0, A16, ws,
+                                   big, None) == -1                  # no up weight
+    assert B.ngr_fused_norm_swiglu(0, A16, None, None, A16, A16, 0.0, 4, 64, 60, 0, A16, ws,
+                                   big, None) == -3                  # F % 8
+    assert B.ngr_fused_norm_swiglu(0, A16, None, None, A16, A16, 0.0, 4, 64, 64, 0, A16, ws,
+                                   100, None) == -5                  # workspace too small
+    assert B.ngr_fused_mlp_swiglu(2, A16, A16, None, A16, A16, 0, 1e-5, 4, 64, 64, 0, None,
+                                  A16, ws, big, None) == -1          # no down weight
+    assert B.ngr_fused_mlp_swiglu(2, A16, A16, None, A16, A16, A16, 1e-5, 0, 64, 64, 0, None,
+                                  A16, ws, big, None) == 0           # empty batch
 
 
 A16 = 0x10000  # a fake, 16-byte aligned address: never dereferenced here
