@@ -209,6 +209,68 @@ def stored_traffic(workload: str):
 
 
 # ----------------------------------------------------------------------------
+# ----------------------------------------------------------- per-op details
+_NORM_IDS = {"none": 0, "layer": 1, "rms": 2}
+_ACT_IDS = {"none": 0, "silu": 1, "relu": 2, "gelu": 3}
+_TWO_GEMM = ("ffn", "mlp", "mlp_swiglu")
+
+
+def op_keys(w):
+    """Input tensors of workload ``w``'s op, in the generator's key names."""
+    return {"ffn": ["x", "W1", "W2"],
+            "mlp": ["x", "gamma", "beta", "W1", "b1", "W2", "b2"],
+            "swiglu": ["x", "gamma", "beta", "Wg", "Wu"],
+            "mlp_swiglu": ["x", "gamma", "beta", "Wg", "Wu", "Wd"]}.get(
+        w.op, ["x", "gamma", "beta", "W", "bias"])
+
+
+def op_out_cols(w):
+    return w.K if w.op in _TWO_GEMM else w.N
+
+
+def op_kernel_flops(w, decode):
+    """FLOPs of each kernel one call launches, in launch order (the
+    statistics kernel counts 0): statistics for norm ops and for decode
+    calls (which also clear split-K counters), then one GEMM per product
+    (SwiGLU's gate and up share one)."""
+    g = 2.0 * w.M * w.N * w.K
+    has_norm = w.op in ("layernorm_linear", "rmsnorm_linear") or w.norm != "none"
+    if w.op == "swiglu":
+        return ([0.0] if has_norm else []) + [2 * g]
+    if w.op == "mlp_swiglu":
+        return ([0.0] if has_norm or decode else []) + [2 * g, g]
+    if w.op in ("ffn", "mlp"):
+        return ([0.0] if has_norm or decode else []) + [g, g]
+    return ([0.0] if has_norm or decode else []) + [g]
+
+
+def oracle_run(w, host, rows, lib):
+    """The oracle for the listed rows of workload ``w`` (fp64)."""
+    import oracle
+    if w.op == "layernorm_linear":
+        return oracle.layernorm_linear(host["x"], host["gamma"], host["beta"], host["W"],
+                                       host["bias"], w.eps, rows, lib)
+    if w.op == "rmsnorm_linear":
+        return oracle.rmsnorm_linear(host["x"], host["gamma"], host["W"], host["bias"], w.eps,
+                                     rows, lib)
+    if w.op == "linear_silu":
+        return oracle.linear_silu(host["x"], host["W"], host["bias"], rows, lib)
+    if w.op == "ffn":
+        return oracle.ffn(host["x"], host["W1"], host["W2"], rows, lib)
+    nid = _NORM_IDS[w.norm]
+    if w.op == "norm_linear":
+        return oracle.norm_linear(nid, _ACT_IDS[w.act], host["x"], host["gamma"], host["beta"],
+                                  host["W"], host["bias"], w.eps, rows, lib)
+    if w.op == "mlp":
+        return oracle.mlp(nid, _ACT_IDS[w.act], host["x"], host["gamma"], host["beta"],
+                          host["W1"], host["b1"], host["W2"], host["b2"], w.eps, rows, lib)
+    if w.op == "swiglu":
+        return oracle.swiglu(nid, host["x"], host["gamma"], host["beta"], host["Wg"],
+                             host["Wu"], w.eps, rows, lib)
+    return oracle.mlp_swiglu(nid, host["x"], host["gamma"], host["beta"], host["Wg"],
+                             host["Wu"], host["Wd"], w.eps, rows, lib)
+
+
 def our_arm(args, rank, world, local):
     import normalization_gemm_row_gb300 as ngr
     from normalization_gemm_row_gb300 import binding as B
@@ -222,51 +284,63 @@ def our_arm(args, rank, world, local):
         w = w.with_m(args.m)
     M, K, N = w.M, w.K, w.N
     decode = M <= 32
-    ffn = w.op == "ffn"
+    two_gemm = w.op in _TWO_GEMM
 
     # Input sets: one seeded draw on the host, copied to every set (identical
     # values, distinct buffers), enough sets that the bytes between two uses
     # of a set exceed 2 x L2.
     host = inputs.make(w)
-    keys = ["x", "W1", "W2"] if ffn else ["x", "gamma", "beta", "W", "bias"]
-    keys = [k for k in keys if host.get(k) is not None]
-    out_cols = K if ffn else N
+    keys = [k for k in op_keys(w) if host.get(k) is not None]
+    out_cols = op_out_cols(w)
     set_bytes = sum(host[k].numel() * host[k].element_size() for k in keys) + M * out_cols * 2
     n_sets = max(2, min(16, math.ceil(2 * L2_BYTES / set_bytes) + 1))
+    op_code = {"layernorm_linear": B.OP_LAYERNORM_LINEAR, "rmsnorm_linear": B.OP_RMSNORM_LINEAR,
+               "linear_silu": B.OP_LINEAR_SILU, "ffn": B.OP_FFN, "norm_linear": B.OP_NORM_LINEAR,
+               "mlp": B.OP_MLP, "swiglu": B.OP_SWIGLU, "mlp_swiglu": B.OP_MLP_SWIGLU}[w.op]
     sets = []
     for _ in range(n_sets):
         s = {k: host[k].to(dev) for k in keys}
         s["y"] = torch.empty((M, out_cols), dtype=w.dtype, device=dev)
-        if ffn:
+        if two_gemm:
             s["h"] = torch.empty((M, N), dtype=w.dtype, device=dev)
-        op_code = {"layernorm_linear": B.OP_LAYERNORM_LINEAR, "rmsnorm_linear": B.OP_RMSNORM_LINEAR,
-                   "linear_silu": B.OP_LINEAR_SILU, "ffn": B.OP_FFN}[w.op]
         nb = B.ngr_workspace_bytes(op_code, M, K, N, 0)
         s["ws"] = torch.empty(max(nb, 256), dtype=torch.uint8, device=dev)
         sets.append(s)
+    nid, aid = _NORM_IDS[w.norm], _ACT_IDS[w.act]
 
     def step(s, stream=None):
+        g = s.get
         if w.op == "layernorm_linear":
-            ngr.fused_layernorm_linear(s["x"], s["gamma"], s["beta"], s["W"], s.get("bias"), w.eps,
+            ngr.fused_layernorm_linear(s["x"], s["gamma"], s["beta"], s["W"], g("bias"), w.eps,
                                        out=s["y"], workspace=s["ws"], stream=stream)
         elif w.op == "rmsnorm_linear":
-            ngr.fused_rmsnorm_linear(s["x"], s["gamma"], s["W"], s.get("bias"), w.eps,
+            ngr.fused_rmsnorm_linear(s["x"], s["gamma"], s["W"], g("bias"), w.eps,
                                      out=s["y"], workspace=s["ws"], stream=stream)
         elif w.op == "linear_silu":
-            ngr.fused_linear_silu(s["x"], s["W"], s.get("bias"), out=s["y"], workspace=s["ws"],
+            ngr.fused_linear_silu(s["x"], s["W"], g("bias"), out=s["y"], workspace=s["ws"],
                                   stream=stream)
-        else:
+        elif w.op == "ffn":
             ngr.ffn_linear_silu_linear(s["x"], s["W1"], s["W2"], out=s["y"], h=s["h"],
                                        workspace=s["ws"], stream=stream)
+        elif w.op == "norm_linear":
+            ngr.fused_norm_linear_act(s["x"], s["W"], norm=nid, act=aid, gamma=g("gamma"),
+                                      beta=g("beta"), bias=g("bias"), eps=w.eps, out=s["y"],
+                                      workspace=s["ws"], stream=stream)
+        elif w.op == "mlp":
+            ngr.fused_mlp(s["x"], s["W1"], s["W2"], norm=nid, act=aid, gamma=g("gamma"),
+                          beta=g("beta"), b1=g("b1"), b2=g("b2"), eps=w.eps, out=s["y"],
+                          h=s["h"], workspace=s["ws"], stream=stream)
+        elif w.op == "swiglu":
+            ngr.fused_norm_swiglu(s["x"], s["Wg"], s["Wu"], norm=nid, gamma=g("gamma"),
+                                  beta=g("beta"), eps=w.eps, out=s["y"], workspace=s["ws"],
+                                  stream=stream)
+        else:
+            ngr.fused_mlp_swiglu(s["x"], s["Wg"], s["Wu"], s["Wd"], norm=nid, gamma=g("gamma"),
+                                 beta=g("beta"), eps=w.eps, out=s["y"], h=s["h"],
+                                 workspace=s["ws"], stream=stream)
 
-    # kernels one call launches: statistics (norm ops, and every decode call,
-    # which also clears its split-K counters) + one GEMM per linear layer
-    if ffn:
-        kernels_per_step = 3 if decode else 2
-    elif w.op == "linear_silu":
-        kernels_per_step = 2 if decode else 1
-    else:
-        kernels_per_step = 2
+    kernel_flops = op_kernel_flops(w, decode)
+    kernels_per_step = len(kernel_flops)
     stream = torch.cuda.current_stream(dev)
     for i in range(args.warmup):
         step(sets[i % n_sets])
@@ -292,7 +366,7 @@ def our_arm(args, rank, world, local):
     ms_total_max = max_over_ranks(ms_total)
     flops = w.flops
     algo_bytes = sum(host[k].numel() * host[k].element_size() for k in keys) + M * out_cols * 2
-    if ffn:
+    if two_gemm:
         algo_bytes += 2 * M * N * 2  # H written once and read once
     ms_step = ms_total_max / args.steps
     if decode:
@@ -316,8 +390,7 @@ def our_arm(args, rank, world, local):
         achieved = algo_bytes / (per_kernel[dom] / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     else:
-        dom_flops = flops if not ffn else flops / 2.0
-        achieved = dom_flops / (per_kernel[dom] / 1e3) / 1e12
+        achieved = kernel_flops[dom] / (per_kernel[dom] / 1e3) / 1e12
         # fp16 and bf16 run at the same dense tensor rate (ratio 1).
         roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s"}
@@ -402,6 +475,16 @@ def our_arm(args, rank, world, local):
     if not args.no_alternatives:
         import torch.nn.functional as F
 
+        tacts = {"none": lambda t: t, "silu": F.silu, "relu": F.relu,
+                 "gelu": lambda t: F.gelu(t, approximate="none")}
+
+        def tnorm(s):
+            if w.norm == "layer":
+                return F.layer_norm(s["x"], (K,), s["gamma"], s["beta"], w.eps)
+            if w.norm == "rms":
+                return F.rms_norm(s["x"], (K,), s["gamma"], w.eps)
+            return s["x"]
+
         def tstep(i):
             s = sets[i % n_sets]
             if w.op == "layernorm_linear":
@@ -410,7 +493,16 @@ def our_arm(args, rank, world, local):
                 return F.linear(F.rms_norm(s["x"], (K,), s["gamma"], w.eps), s["W"], s.get("bias"))
             if w.op == "linear_silu":
                 return F.silu(F.linear(s["x"], s["W"], s.get("bias")))
-            return F.linear(F.silu(F.linear(s["x"], s["W1"])), s["W2"])
+            if w.op == "ffn":
+                return F.linear(F.silu(F.linear(s["x"], s["W1"])), s["W2"])
+            if w.op == "norm_linear":
+                return tacts[w.act](F.linear(tnorm(s), s["W"], s.get("bias")))
+            if w.op == "mlp":
+                return F.linear(tacts[w.act](F.linear(tnorm(s), s["W1"], s.get("b1"))), s["W2"],
+                                s.get("b2"))
+            a = tnorm(s)
+            h = F.silu(F.linear(a, s["Wg"])) * F.linear(a, s["Wu"])
+            return h if w.op == "swiglu" else F.linear(h, s["Wd"])
 
         for i in range(args.warmup):
             tstep(i)
@@ -424,7 +516,8 @@ def our_arm(args, rank, world, local):
         torch.cuda.synchronize(dev)
         tms = t0.elapsed_time(t1) / args.steps
         alternatives["torch_unfused_same_gpu"] = {
-            "what": "torch layer_norm/rms_norm -> linear (cuBLAS) [-> silu], normalized rows written to HBM",
+            "what": "the same computation as separate torch ops (layer_norm/rms_norm, linear on "
+                    "cuBLAS, activations, the SwiGLU product), intermediates written to HBM",
             "value": (algo_bytes / (tms / 1e3) / 1e9) if decode else (flops / (tms / 1e3) / 1e12),
             "unit": unit, "ms_per_step": tms}
 
@@ -459,16 +552,7 @@ def cpu_baseline(w, host, target_s: float):
     M = w.M
 
     def run(rows):
-        if w.op == "layernorm_linear":
-            oracle.layernorm_linear(host["x"], host["gamma"], host["beta"], host["W"],
-                                    host["bias"], w.eps, rows, lib)
-        elif w.op == "rmsnorm_linear":
-            oracle.rmsnorm_linear(host["x"], host["gamma"], host["W"], host["bias"], w.eps,
-                                  rows, lib)
-        elif w.op == "linear_silu":
-            oracle.linear_silu(host["x"], host["W"], host["bias"], rows, lib)
-        else:
-            oracle.ffn(host["x"], host["W1"], host["W2"], rows, lib)
+        oracle_run(w, host, rows, lib)
 
     threads = oracle.num_threads(lib)
     if w.M <= 32:
@@ -518,16 +602,7 @@ def reference_arm(args, rank):
     def step(i):
         r0 = (i * rows_per_step) % w.M
         rows = [(r0 + j) % w.M for j in range(rows_per_step)]
-        if w.op == "layernorm_linear":
-            oracle.layernorm_linear(host["x"], host["gamma"], host["beta"], host["W"],
-                                    host["bias"], w.eps, rows, lib)
-        elif w.op == "rmsnorm_linear":
-            oracle.rmsnorm_linear(host["x"], host["gamma"], host["W"], host["bias"], w.eps,
-                                  rows, lib)
-        elif w.op == "linear_silu":
-            oracle.linear_silu(host["x"], host["W"], host["bias"], rows, lib)
-        else:
-            oracle.ffn(host["x"], host["W1"], host["W2"], rows, lib)
+        oracle_run(w, host, rows, lib)
 
     for i in range(args.warmup):
         step(i)
