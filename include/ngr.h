@@ -22,7 +22,15 @@
  *    the accumulation are FP32; y is rounded to nearest-even once.
  *  - Alignment: K % 8 == 0 and N % 8 == 0 (16-byte row pitch), every pointer
  *    16-byte aligned, the workspace 256-byte aligned.  M is arbitrary
- *    (M == 0 is a no-op that returns NGR_OK).
+ *    (M == 0 is a no-op that returns NGR_OK).  The single-layer entry
+ *    points (ngr_fused_layernorm_linear, ngr_fused_rmsnorm_linear,
+ *    ngr_fused_linear_silu, ngr_fused_norm_linear_act) also take any K and
+ *    N: when either is not a multiple of 8 they copy x, W, gamma, beta and
+ *    bias into the workspace with rows padded by zeros to a multiple of 8,
+ *    run the aligned kernels and copy the real columns of y out
+ *    ([MMF] §五 optimization 1: a 513 x 14337 activation).  ngr_workspace_bytes
+ *    includes those copies; W is copied on every such call.  Pointers then
+ *    need only 2-byte alignment (y 16-byte when N % 8 == 0).
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *    stream) and is asynchronous: the call returns once the kernels are
  *    launched.  Argument errors are detected before anything is launched and
@@ -64,7 +72,7 @@ typedef enum {
     NGR_OK = 0,
     NGR_ERR_NULL = -1,      /* a required pointer is NULL */
     NGR_ERR_SHAPE = -2,     /* M < 0, K <= 0, N <= 0, or too large */
-    NGR_ERR_ALIGN = -3,     /* K or N not a multiple of 8, or a pointer misaligned */
+    NGR_ERR_ALIGN = -3,     /* K or N not a multiple of 8 (where required), or a pointer misaligned */
     NGR_ERR_DTYPE = -4,     /* dtype is not NGR_F16 / NGR_BF16 */
     NGR_ERR_WORKSPACE = -5, /* workspace NULL or smaller than ngr_workspace_bytes */
     NGR_ERR_ARCH = -6,      /* no sm_103 device current */

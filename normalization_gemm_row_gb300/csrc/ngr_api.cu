@@ -66,11 +66,22 @@ size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
 struct WsLayout {
     size_t stats = 0, gamma_f = 0, beta_f = 0, xhat = 0;
+    // padded copies (single-layer ops with K or N not a multiple of 8)
+    size_t xp = 0, wp = 0, gp = 0, bp = 0, biasp = 0, yp = 0;
+    bool padded = false;
     size_t partials = 0, counters = 0, counters2 = 0, h = 0;
     size_t total = 0;
 };
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int64_t round8(int64_t v) { return (v + 7) & ~static_cast<int64_t>(7); }
+
+// Ops that take any K and N (through padded copies).
+bool single_layer_op(int op)
+{
+    return op == NGR_OP_LAYERNORM_LINEAR || op == NGR_OP_RMSNORM_LINEAR ||
+           op == NGR_OP_LINEAR_SILU || op == NGR_OP_NORM_LINEAR;
+}
 
 // Workspace regions, in order: header | stats | gamma_f | beta_f |
 // normalized rows (decode sizes) | decode partials | counters of the first
@@ -82,10 +93,15 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // runs on the decode kernel except for SwiGLU, whose gated tiles run on the
 // CTA-pair kernel at every M; the second GEMM of a chain (K output
 // columns) always takes the decode kernel there.
-WsLayout ws_layout(int op, int64_t M, int64_t K, int64_t N, bool h_in_ws)
+WsLayout ws_layout(int op, int64_t M, int64_t K_, int64_t N_, bool h_in_ws)
 {
     WsLayout L;
     size_t off = kHeaderBytes;
+    // A single layer with K or N not a multiple of 8 runs on rows padded to
+    // K8 / N8; the padded copies follow the regular regions.
+    const bool pad = single_layer_op(op) && (K_ % 8 != 0 || N_ % 8 != 0);
+    const int64_t K = pad ? round8(K_) : K_;
+    const int64_t N = pad ? round8(N_) : N_;
     const bool norm = op == NGR_OP_LAYERNORM_LINEAR || op == NGR_OP_RMSNORM_LINEAR ||
                       op == NGR_OP_NORM_LINEAR || op == NGR_OP_MLP || op == NGR_OP_SWIGLU ||
                       op == NGR_OP_MLP_SWIGLU;
@@ -118,6 +134,21 @@ WsLayout ws_layout(int op, int64_t M, int64_t K, int64_t N, bool h_in_ws)
     }
     if (chain && h_in_ws) {
         L.h = off;
+        off += align256(static_cast<size_t>(M) * static_cast<size_t>(N) * 2);
+    }
+    if (pad) {
+        L.padded = true;
+        L.xp = off;
+        off += align256(static_cast<size_t>(M) * static_cast<size_t>(K) * 2);
+        L.wp = off;
+        off += align256(static_cast<size_t>(N_) * static_cast<size_t>(K) * 2);
+        L.gp = off;
+        off += align256(static_cast<size_t>(K) * 2);
+        L.bp = off;
+        off += align256(static_cast<size_t>(K) * 2);
+        L.biasp = off;
+        off += align256(static_cast<size_t>(N) * 2);
+        L.yp = off;
         off += align256(static_cast<size_t>(M) * static_cast<size_t>(N) * 2);
     }
     L.total = off;
@@ -207,6 +238,8 @@ EncodeTiledFn encode_fn()
 
 // Row-major [rows, cols] 16-bit matrix, box {64 columns, box_rows rows},
 // 128-byte swizzle (the layout the tensor core reads K-major operands in).
+bool aligned2(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 1u) == 0; }
+
 bool map_2d(CUtensorMap *m, const void *ptr, bool bf16, int64_t rows, int64_t cols,
             uint32_t box_rows)
 {
@@ -285,8 +318,11 @@ int launch_layer(int norm, int act, bool bf16, const void *x, const void *W,
                  const void *bias, int64_t M, int64_t K, int64_t N, void *y,
                  char *ws, const WsLayout &L, size_t counters_off, bool pdl,
                  const DevInfo &di, cudaStream_t stream, const float *fold_c = nullptr,
-                 const float *fold_b = nullptr)
+                 const float *fold_b = nullptr, int64_t w_rows = -1)
 {
+    // W has w_rows rows (N unless the output is padded past W's rows; the
+    // tensor maps zero-fill the rest).
+    if (w_rows < 0) w_rows = N;
     // A kernel launched as a programmatic dependent is never a call's first.
     const int zero_err = pdl ? 0 : 1;
     int *err = reinterpret_cast<int *>(ws);
@@ -298,7 +334,7 @@ int launch_layer(int norm, int act, bool bf16, const void *x, const void *W,
         DecodeArgs d;
         std::memset(&d, 0, sizeof(d));
         const int mn = M <= 16 ? 16 : 32;
-        if (!map_2d(&d.map_w, W, bf16, N, K, 128) || !map_2d(&d.map_x, x, bf16, M, K, mn))
+        if (!map_2d(&d.map_w, W, bf16, w_rows, K, 128) || !map_2d(&d.map_x, x, bf16, M, K, mn))
             return NGR_ERR_CUDA;
         if (has_norm && !map_gb(&d.map_gb, gf, K, L.beta_f - L.gamma_f)) return NGR_ERR_CUDA;
         d.stats = stats;
@@ -334,7 +370,7 @@ int launch_layer(int norm, int act, bool bf16, const void *x, const void *W,
                      plan.pair ? "cta-pair" : "single-cta", plan.bn, plan.nsub, plan.stages, plan.grid,
                      plan.smem);
     if (!map_2d(&a.map_a, x, bf16, M, K, kBM) ||
-        !map_2d(&a.map_b, W, bf16, N, K, static_cast<uint32_t>(plan.b_rows)))
+        !map_2d(&a.map_b, W, bf16, w_rows, K, static_cast<uint32_t>(plan.b_rows)))
         return NGR_ERR_CUDA;
     if (has_norm && !map_gb(&a.map_gb, gf, K, L.beta_f - L.gamma_f)) return NGR_ERR_CUDA;
     a.stats = stats;
@@ -397,51 +433,84 @@ int norm_linear(int op, int norm, int act, const void *x, const void *gamma, con
                 const void *W, const void *bias, float eps, int64_t M, int64_t K, int64_t N,
                 int dtype, void *y, void *ws, size_t ws_bytes, cudaStream_t stream)
 {
-    int rc = check_sizes(M, K, N, dtype);
-    if (rc != NGR_OK) return rc;
+    if (dtype != NGR_F16 && dtype != NGR_BF16) return NGR_ERR_DTYPE;
+    if (M < 0 || K <= 0 || N <= 0 || M >= kMaxDim || K >= kMaxDim || N >= kMaxDim)
+        return NGR_ERR_SHAPE;
     if (M == 0) return NGR_OK;
     if (!x || !W || !y || !ws) return ws ? NGR_ERR_NULL : (x && W && y ? NGR_ERR_WORKSPACE : NGR_ERR_NULL);
     if (norm != kNormNone && !gamma) return NGR_ERR_NULL;
     if (norm == kNormLayer && !beta) return NGR_ERR_NULL;
-    if (!aligned16(x) || !aligned16(W) || !aligned16(y) || (gamma && !aligned16(gamma)) ||
-        (beta && !aligned16(beta)) || (bias && !aligned16(bias)))
+    const bool pad = K % 8 != 0 || N % 8 != 0;
+    // Aligned shapes need 16-byte pointers; padded ones are copied with
+    // 2-byte accesses, except y when N needs no padding (stored directly).
+    auto ok_ptr = [&](const void *p) {
+        return !p || (pad ? aligned2(p) : aligned16(p));
+    };
+    if (!ok_ptr(x) || !ok_ptr(W) || !ok_ptr(gamma) || !ok_ptr(beta) || !ok_ptr(bias) ||
+        !(N % 8 != 0 ? aligned2(y) : aligned16(y)))
         return NGR_ERR_ALIGN;
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return NGR_ERR_ALIGN;
     const WsLayout L = ws_layout(op, M, K, N, false);
     if (ws_bytes < L.total) return NGR_ERR_WORKSPACE;
     DevInfo di;
-    rc = current_device_info(&di);
+    int rc = current_device_info(&di);
     if (rc != NGR_OK) return rc;
     const bool bf16 = dtype == NGR_BF16;
     char *w = static_cast<char *>(ws);
     if (debug_mode() && cudaMemsetAsync(w, 0, 4, stream) != cudaSuccess) return NGR_ERR_CUDA;
+    // Padded operands: rows of K8 (N8) elements with zero tails.
+    const int64_t K8 = round8(K), N8 = round8(N);
+    const void *xa = x, *Wa = W, *ga = gamma, *ba = beta, *biasa = bias;
+    void *ya = y;
+    if (pad) {
+        // An operand is copied when its rows need padding or its pointer
+        // is not 16-byte aligned (the kernels read it with TMA or 16-byte
+        // loads).
+        auto copy = [&](const void *src, int64_t rows, size_t off, const void **dst) {
+            if (!src || (K8 == K && aligned16(src))) return 0;
+            *dst = w + off;
+            return launch_pad_rows(src, rows, K, K, w + off, K8, di.sms, stream);
+        };
+        rc = copy(x, M, L.xp, &xa);
+        if (rc == 0) rc = copy(W, N, L.wp, &Wa);
+        if (rc == 0) rc = copy(gamma, 1, L.gp, &ga);
+        if (rc == 0) rc = copy(beta, 1, L.bp, &ba);
+        if (rc != 0) return rc;
+        if (bias) {
+            rc = launch_pad_rows(bias, 1, N, N, w + L.biasp, N8, di.sms, stream);
+            if (rc != 0) return rc;
+            biasa = w + L.biasp;
+        }
+        if (N8 != N) ya = w + L.yp;
+    }
     const bool decode = M <= kDecodeMaxM;
     const bool need_stats = norm != kNormNone || decode;
     events_reset();
     if (need_stats) {
         event_before(stream);
-        rc = launch_rowstats(norm == kNormNone ? kNormRms : norm, bf16, x,
-                             norm == kNormNone ? 0 : M, K, eps,
-                             reinterpret_cast<float2 *>(w + L.stats), gamma, beta,
+        rc = launch_rowstats(norm == kNormNone ? kNormRms : norm, bf16, xa,
+                             norm == kNormNone ? 0 : M, K8, eps,
+                             reinterpret_cast<float2 *>(w + L.stats), ga, ba,
                              norm == kNormNone ? nullptr : reinterpret_cast<float *>(w + L.gamma_f),
                              norm == kNormLayer ? reinterpret_cast<float *>(w + L.beta_f)
                                                 : (norm == kNormRms ? reinterpret_cast<float *>(w + L.beta_f) : nullptr),
                              decode ? reinterpret_cast<int *>(w + L.counters) : nullptr,
-                             decode ? static_cast<int>(ceil_div(N, 128) * 4) : 0,
+                             decode ? static_cast<int>(ceil_div(N8, 128) * 4) : 0,
                              reinterpret_cast<int *>(w), di.sms, stream,
-                             decode && norm != kNormNone ? w + L.xhat : nullptr);
+                             decode && norm != kNormNone ? w + L.xhat : nullptr, K);
         event_after(stream);
         if (rc != NGR_OK) return rc;
     }
     event_before(stream);
     // Decode sizes multiply the normalized rows the statistics kernel wrote.
     if (decode && norm != kNormNone)
-        rc = launch_layer(kNormNone, act, bf16, w + L.xhat, W, bias, M, K, N, y, w, L, L.counters,
-                          true, di, stream);
+        rc = launch_layer(kNormNone, act, bf16, w + L.xhat, Wa, biasa, M, K8, N8, ya, w, L,
+                          L.counters, true, di, stream, nullptr, nullptr, N);
     else
-        rc = launch_layer(norm, act, bf16, x, W, bias, M, K, N, y, w, L, L.counters, need_stats,
-                          di, stream);
+        rc = launch_layer(norm, act, bf16, xa, Wa, biasa, M, K8, N8, ya, w, L, L.counters,
+                          need_stats, di, stream, nullptr, nullptr, N);
     event_after(stream);
+    if (rc == NGR_OK && ya != y) rc = launch_unpad_rows(ya, M, N, N8, y, di.sms, stream);
     events_call_done();
     return finish(rc, ws, stream);
 }

@@ -109,7 +109,16 @@ int launch_rowstats(int norm, bool bf16, const void *x, int64_t M, int64_t K,
                     float eps, float2 *stats, const void *gamma,
                     const void *beta, float *gamma_f, float *beta_f,
                     int *counters, int n_counters, int *err_to_clear,
-                    int num_sms, cudaStream_t stream, void *xhat = nullptr);
+                    int num_sms, cudaStream_t stream, void *xhat = nullptr,
+                    int64_t k_valid = -1);
+
+// Copies for shapes whose K or N is not a multiple of 8 (ngr_pad.cu):
+// rows of `cols` 16-bit values (pitch `src_pitch`) into rows of `dst_cols`
+// (a multiple of 8) with a zero tail, and back.
+int launch_pad_rows(const void *src, int64_t rows, int64_t cols, int64_t src_pitch, void *dst,
+                    int64_t dst_cols, int num_sms, cudaStream_t stream);
+int launch_unpad_rows(const void *src, int64_t rows, int64_t cols, int64_t src_pitch, void *dst,
+                      int num_sms, cudaStream_t stream);
 
 int launch_gemm(int norm, bool bf16, const GemmPlan &plan, const GemmArgs &args, bool pdl,
                 cudaStream_t stream);

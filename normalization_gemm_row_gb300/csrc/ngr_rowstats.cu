@@ -18,6 +18,10 @@
 // arithmetic and the single rounding of the tile kernel's transform, so that
 // the weight-streaming kernel multiplies them without re-normalizing.
 //
+// When the rows are padded (K is the padded pitch, a multiple of 8), only the
+// first k_valid columns count: the padding is excluded from the LayerNorm
+// sums and every mean divides by k_valid.
+//
 // The same launch converts gamma and beta to FP32 once per call (the GEMM's
 // producer streams them with the tiles) and zeroes the split-K tile counters
 // of the decode path when asked to, so that they start from zero every call;
@@ -123,7 +127,7 @@ __global__ void __launch_bounds__(kStatsThreads, XHAT ? 1 : kStatsCtasPerSm) row
     float2 *__restrict__ stats, const void *__restrict__ gamma,
     const void *__restrict__ beta, float *__restrict__ gamma_f,
     float *__restrict__ beta_f, int *__restrict__ counters, int n_counters,
-    int *__restrict__ err_to_clear, uint4 *__restrict__ xhat)
+    int *__restrict__ err_to_clear, uint4 *__restrict__ xhat, int64_t k_valid)
 {
     // The dependent GEMM may start its prologue while this grid runs; it
     // waits for this grid's completion before reading the statistics.
@@ -174,17 +178,22 @@ __global__ void __launch_bounds__(kStatsThreads, XHAT ? 1 : kStatsCtasPerSm) row
                     if (v >= vec_per_row) break;
                     float f[8];
                     unpack8<BF16>(q[u], f);
-                    if (!have_shift) {
+                    // real columns of this vector (all 8 except in a padded tail)
+                    const int64_t rem = k_valid - 8 * v;
+                    const int nv = rem >= 8 ? 8 : (rem > 0 ? static_cast<int>(rem) : 0);
+                    if (!have_shift && nv > 0) {
                         s = f[0];
                         have_shift = true;
                     }
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        const float d = f[i] - s;
-                        s1 += d;
-                        s2 = fmaf(d, d, s2);
+                        if (i < nv) {
+                            const float d = f[i] - s;
+                            s1 += d;
+                            s2 = fmaf(d, d, s2);
+                        }
                     }
-                    n += 8.f;
+                    n += static_cast<float>(nv);
                 }
             }
             float mean = n > 0.f ? s + s1 / n : 0.f;
@@ -205,7 +214,7 @@ __global__ void __launch_bounds__(kStatsThreads, XHAT ? 1 : kStatsCtasPerSm) row
             if (tid == 0) {
                 float tn = red[0][0], tm = red[1][0], t2 = red[2][0];
                 for (int w = 1; w < kStatsThreads / 32; ++w) chan_merge(tn, tm, t2, red[0][w], red[1][w], red[2][w]);
-                const float var = t2 / static_cast<float>(K);
+                const float var = t2 / static_cast<float>(k_valid);
                 row_stats = make_float2(tm, 1.0f / sqrtf(var + eps));
                 stats[row] = row_stats;
             }
@@ -236,7 +245,7 @@ __global__ void __launch_bounds__(kStatsThreads, XHAT ? 1 : kStatsCtasPerSm) row
             if (tid == 0) {
                 float t = 0.f;
                 for (int w = 0; w < kStatsThreads / 32; ++w) t += red[0][w];
-                row_stats = make_float2(0.f, 1.0f / sqrtf(t / static_cast<float>(K) + eps));
+                row_stats = make_float2(0.f, 1.0f / sqrtf(t / static_cast<float>(k_valid) + eps));
                 stats[row] = row_stats;
             }
             __syncthreads();
@@ -262,8 +271,9 @@ int launch_rowstats(int norm, bool bf16, const void *x, int64_t M, int64_t K,
                     float eps, float2 *stats, const void *gamma,
                     const void *beta, float *gamma_f, float *beta_f,
                     int *counters, int n_counters, int *err_to_clear,
-                    int num_sms, cudaStream_t stream, void *xhat)
+                    int num_sms, cudaStream_t stream, void *xhat, int64_t k_valid)
 {
+    if (k_valid < 0) k_valid = K;
     const int threads = kStatsThreads;
     int64_t blocks = M;
     const int64_t cap = static_cast<int64_t>(num_sms) * kStatsCtasPerSm;   // one wave
@@ -278,11 +288,11 @@ int launch_rowstats(int norm, bool bf16, const void *x, int64_t M, int64_t K,
     if (xh)                                                                                   \
         rowstats_kernel<N_, B_, true><<<grid, block, 0, stream>>>(                            \
             xv, M, K, eps, stats, gamma, beta, gamma_f, beta_f, counters, n_counters,          \
-            err_to_clear, xh);                                                                \
+            err_to_clear, xh, k_valid);                                                                \
     else                                                                                      \
         rowstats_kernel<N_, B_, false><<<grid, block, 0, stream>>>(                           \
             xv, M, K, eps, stats, gamma, beta, gamma_f, beta_f, counters, n_counters,          \
-            err_to_clear, nullptr);
+            err_to_clear, nullptr, k_valid);
     if (norm == kNormLayer) {
         if (bf16) { NGR_STATS(kNormLayer, true) } else { NGR_STATS(kNormLayer, false) }
     } else {

@@ -65,6 +65,31 @@ def test_workspace_bytes_layout(lib):
     assert wb(-1, 1, 8, 8) == 0
 
 
+def test_workspace_bytes_padded_shapes(lib):
+    wb = B.ngr_workspace_bytes
+    a256 = lambda v: (v + 255) // 256 * 256
+    M, K, N = 513, 14337, 520
+    K8 = 14344
+    base = wb(B.OP_LINEAR_SILU, M, K8, N)
+    pads = (a256(M * K8 * 2) + a256(N * K8 * 2) + 2 * a256(K8 * 2) + a256(N * 2)
+            + a256(M * N * 2))
+    assert wb(B.OP_LINEAR_SILU, M, K, N) == base + pads
+    # N not a multiple of 8: the output is padded too
+    assert wb(B.OP_LAYERNORM_LINEAR, 64, 256, 517) > wb(B.OP_LAYERNORM_LINEAR, 64, 256, 520)
+    # ops without the padded path do not grow
+    assert wb(B.OP_FFN, 64, 256, 517) == wb(B.OP_FFN, 64, 256, 517)
+
+
+def test_other_entry_points_still_need_alignment(lib):
+    big = 1 << 24
+    assert B.ngr_fused_norm_swiglu(0, A16, None, None, A16, A16, 0.0, 4, 60, 64, 0, A16,
+                                   A16 * 16, big, None) == -3
+    assert B.ngr_fused_mlp(0, 1, A16, None, None, A16, None, A16, None, 0.0, 4, 60, 64, 0,
+                           None, A16, A16 * 16, big, None) == -3
+    assert B.ngr_fused_norm_linear_folded(1, A16, A16, A16, 1e-5, 4, 60, 64, 0, A16,
+                                          A16 * 16, big, None) == -3
+
+
 def test_workspace_bytes_new_ops(lib):
     wb = B.ngr_workspace_bytes
     # the general layer is sized like the LayerNorm layer
@@ -120,9 +145,12 @@ A16 = 0x10000  # a fake, 16-byte aligned address: never dereferenced here
     (dict(x=0), -1),                                # NULL x
     (dict(gamma=0), -1),                            # NULL gamma
     (dict(beta=0), -1),                             # NULL beta (LayerNorm)
-    (dict(K=12), -3),                               # K not a multiple of 8
-    (dict(N=20), -3),                               # N not a multiple of 8
-    (dict(x=A16 + 2), -3),                          # misaligned x
+    (dict(K=12, ws_bytes=600), -5),                 # K % 8: padded copies need workspace
+    (dict(N=20, ws_bytes=600), -5),                 # N % 8: likewise
+    (dict(K=12, x=A16 + 1), -3),                    # padded path: x not even 2-byte aligned
+    (dict(N=20, y=A16 + 1), -3),                    # padded path: y not 2-byte aligned
+    (dict(K=12, N=24, y=A16 + 2), -3),              # N % 8 == 0: y stored directly, 16-byte
+    (dict(x=A16 + 2), -3),                          # aligned shapes: misaligned x
     (dict(bias=A16 + 8), -3),                       # misaligned bias
     (dict(ws=A16 + 16), -3),                        # workspace not 256-B aligned
     (dict(dtype=3), -4),                            # bad dtype
@@ -147,7 +175,7 @@ def test_layernorm_linear_rejects_before_launch(lib, kw, expect):
 def test_other_entry_points_reject(lib):
     assert B.ngr_fused_rmsnorm_linear(A16, 0, A16, None, 1e-6, 4, 64, 64, 0,
                                       A16, A16 * 16, 1 << 20, None) == -1
-    assert B.ngr_fused_linear_silu(A16, A16, None, 4, 60, 64, 1, A16, A16 * 16,
+    assert B.ngr_fused_linear_silu(A16 + 1, A16, None, 4, 60, 64, 1, A16, A16 * 16,
                                    1 << 20, None) == -3
     assert B.ngr_ffn_linear_silu_linear(A16, A16, 0, 4, 64, 64, 0, None, A16,
                                         A16 * 16, 1 << 20, None) == -1
