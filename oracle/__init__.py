@@ -67,8 +67,9 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.ngo_mlp.argtypes = [I, I, P, P, P, P, P, P, P, D, I64, I64, I64, I64, I, P, I64, P]
     lib.ngo_swiglu.argtypes = [I, P, P, P, P, P, D, I64, I64, I64, I, P, I64, P]
     lib.ngo_mlp_swiglu.argtypes = [I, P, P, P, P, P, P, D, I64, I64, I64, I64, I, P, I64, P]
+    lib.ngo_linear_residual_norm.argtypes = [I, P, P, P, P, P, P, D, I64, I64, I64, I, P, I64, P, P]
     lib.ngo_num_threads.argtypes = []
-    for f in (lib.ngo_decode, lib.ngo_row_stats, lib.ngo_normalize,
+    for f in (lib.ngo_linear_residual_norm, lib.ngo_decode, lib.ngo_row_stats, lib.ngo_normalize,
               lib.ngo_norm_linear, lib.ngo_ffn, lib.ngo_fold_prepare,
               lib.ngo_folded_linear, lib.ngo_mlp, lib.ngo_swiglu,
               lib.ngo_mlp_swiglu, lib.ngo_num_threads):
@@ -246,6 +247,25 @@ def mlp_swiglu(norm: int, x, gamma, beta, Wg, Wu, Wd, eps: float, rows=None,
     _check(lib.ngo_mlp_swiglu(norm, *[_ptr(b) for b in bits], eps, M, K, F, N,
                               _DT[x.dtype], _ptr(r), nr, _ptr(y)), "mlp_swiglu")
     return y
+
+
+def linear_residual_norm(norm: int, x, W, bias, residual, gamma, beta, eps: float,
+                         rows=None, lib=None):
+    """(h, y) [nrows, N] in float64: h = x . W^T + bias + residual, y = norm(h)
+    over its N columns (gamma, beta of length N)."""
+    lib = lib or load()
+    M, K = x.shape
+    N = W.shape[0]
+    if W.shape[1] != K:
+        raise ValueError("W must be [N, K]")
+    r, nr = _rows(rows, M)
+    h = np.empty((nr, N), dtype=np.float64)
+    y = np.empty((nr, N), dtype=np.float64)
+    bits = [_bits(t) for t in (x, W, bias, residual, gamma, beta)]
+    _check(lib.ngo_linear_residual_norm(norm, *[_ptr(b) for b in bits], eps, M, K, N,
+                                        _DT[x.dtype], _ptr(r), nr, _ptr(h), _ptr(y)),
+           "linear_residual_norm")
+    return h, y
 
 
 def fold_prepare(norm: int, gamma, beta, W, bias, lib=None):

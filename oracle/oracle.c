@@ -28,7 +28,8 @@
  *  - "LayerNorm 融合算子如何让大模型推理再快 15%？", §3.3 (a fusion chain
  *    LayerNorm -> MatMul -> BiasAdd -> ReLU -> MatMul -> BiasAdd).
  *  - "昇腾CANN的MatMul融合玩法", the table of fused GEMM instructions
- *    (MatMul + ReLU / GELU / SiLU).
+ *    (MatMul + ReLU / GELU / SiLU); §五 optimization 3 (the output
+ *    projection fused with the RMSNorm that follows it).
  *
  * Readings taken where the pages are silent or at odds:
  *  - variance is the biased one (divide by K), as torch's layer_norm that
@@ -42,7 +43,10 @@
  *  - SwiGLU is the Llama form h_j = SiLU(a . Wg[j]) * (a . Wu[j]) with the
  *    gate and up projections both [F, K] and no biases;
  *  - W is [N, K] row-major (the nn.Linear layout), y = a . W^T;
- *  - the FFN keeps its intermediate H in fp64, unrounded.
+ *  - the FFN keeps its intermediate H in fp64, unrounded;
+ *  - the post-product norm normalizes h = x . W^T + bias (+ residual) over
+ *    its N columns, with gamma and beta of length N; the residual is
+ *    optional (the page draws none; a transformer adds one there).
  *
  * Parity is pinned by tests from definitions, closed forms, invariants,
  * library routines in float64 and brute force on tiny inputs; the pages
@@ -467,6 +471,49 @@ int ngo_mlp_swiglu(int norm, const uint16_t *x, const uint16_t *gamma,
     }
     free(g);
     free(b);
+    return failed ? -9 : 0;
+}
+
+/* ---- a norm after the product ---------------------------------------------------
+ * h_n = sum_k x_k W[n, k] + bias_n + residual_n ; y = norm(h) over n, i.e.
+ * LayerNorm: (h_n - mu_h) rstd_h gamma_n + beta_n, RMSNorm: h_n rstd_h
+ * gamma_n, with the statistics of the row h (two passes, fp64).  h is
+ * returned too (unrounded).  bias and residual may be NULL. */
+int ngo_linear_residual_norm(int norm, const uint16_t *x, const uint16_t *W,
+                             const uint16_t *bias, const uint16_t *residual,
+                             const uint16_t *gamma, const uint16_t *beta, double eps,
+                             int64_t M, int64_t K, int64_t N, int dt,
+                             const int64_t *rows, int64_t nrows, double *h, double *y)
+{
+    int rc = check_common(dt, M, K, N, rows, nrows);
+    if (rc) return rc;
+    if (norm != NGO_NORM_LAYER && norm != NGO_NORM_RMS) return -2;
+    if (!x || !W || !gamma || !h || !y) return -1;
+    if (norm == NGO_NORM_LAYER && !beta) return -1;
+    const double *T = table_for(dt);
+    int failed = 0;
+    double *g = decode_vec(gamma, N, T, &failed);
+    double *b = decode_vec(beta, N, T, &failed);
+    double *bi = decode_vec(bias, N, T, &failed);
+#pragma omp parallel for schedule(dynamic)
+    for (int64_t i = 0; i < nrows; ++i) {
+        if (failed) continue;
+        int64_t r = rows ? rows[i] : i;
+        double *xr = malloc((size_t)K * sizeof(double));
+        if (!xr) { failed = 1; continue; }
+        for (int64_t k = 0; k < K; ++k) xr[k] = T[x[r * K + k]];
+        double *hr = h + i * N;
+        linear_row(xr, W, T, bi, NGO_ACT_NONE, K, N, hr);
+        if (residual)
+            for (int64_t n = 0; n < N; ++n) hr[n] += T[residual[r * N + n]];
+        double mu, rstd;
+        row_stats(norm, hr, N, eps, &mu, &rstd);
+        normalize_row(norm, hr, N, mu, rstd, g, b, y + i * N);
+        free(xr);
+    }
+    free(g);
+    free(b);
+    free(bi);
     return failed ? -9 : 0;
 }
 

@@ -402,9 +402,50 @@ def pin_swiglu_brute_force(lib):
     _close(hgg, z * z / (1.0 + np.exp(-z)), rtol=1e-12, atol=1e-14, what="swiglu Wu = Wg")
 
 
+def pin_post_norm_vs_torch(lib):
+    """h = x . W^T + bias + residual and y = LayerNorm / RMSNorm of h over N
+    against torch float64; without a residual too; and brute force in pure
+    Python on a tiny case (statistics by explicit sums over the N outputs)."""
+    M, K, N = 6, 40, 24
+    for dt in (torch.float16, torch.bfloat16):
+        x = _rand((M, K), 70, dt)
+        W = _rand((N, K), 71, dt, K ** -0.5)
+        bias = _rand((N,), 72, dt, 0.1)
+        res = _rand((M, N), 73, dt, 1.0, 2.0)
+        g = _rand((N,), 74, dt, 0.1, 1.0)
+        b = _rand((N,), 75, dt, 0.1)
+        X, A, C, R, G, Bt = map(_exact, (x, W, bias, res, g, b))
+        for with_res in (True, False):
+            rr = res if with_res else None
+            href = F.linear(X, A, C) + (R if with_res else 0.0)
+            h, y = oracle.linear_residual_norm(oracle.NORM_RMS, x, W, bias, rr, g, None, 1e-6,
+                                               lib=lib)
+            _close(h, href.numpy(), rtol=1e-12, atol=1e-12, what="post-norm h")
+            _close(y, F.rms_norm(href, (N,), G, 1e-6).numpy(), rtol=1e-11, atol=1e-12,
+                   what=f"post RMSNorm res={with_res}")
+            h, y = oracle.linear_residual_norm(oracle.NORM_LAYER, x, W, bias, rr, g, b, 1e-5,
+                                               lib=lib)
+            _close(y, F.layer_norm(href, (N,), G, Bt, 1e-5).numpy(), rtol=1e-11, atol=1e-12,
+                   what=f"post LayerNorm res={with_res}")
+    # brute force
+    M, K, N = 2, 5, 4
+    x = _rand((M, K), 76, torch.float16)
+    W = _rand((N, K), 77, torch.float16, 0.5)
+    res = _rand((M, N), 78, torch.float16)
+    g = _rand((N,), 79, torch.float16, 0.1, 1.0)
+    Xl, Wl, Rl, Gl = (_exact(t).tolist() for t in (x, W, res, g))
+    Y = []
+    for i in range(M):
+        hrow = [math.fsum(Xl[i][k] * Wl[n][k] for k in range(K)) + Rl[i][n] for n in range(N)]
+        r = 1.0 / math.sqrt(math.fsum(v * v for v in hrow) / N + 1e-3)
+        Y.append([hrow[n] * r * Gl[n] for n in range(N)])
+    _, y = oracle.linear_residual_norm(oracle.NORM_RMS, x, W, None, res, g, None, 1e-3, lib=lib)
+    _close(y, Y, rtol=1e-12, atol=1e-12, what="post-norm brute force")
+
+
 ALL_PINS = [pin_decode, pin_closed_forms, pin_layernorm_invariants,
             pin_rms_invariants, pin_identity_reduces_to_norm,
             pin_full_path_vs_torch, pin_ffn_vs_torch, pin_brute_force,
             pin_row_selection, pin_fold_identity, pin_stats_vs_numpy,
             pin_activations_vs_library, pin_mlp_vs_torch, pin_swiglu_vs_torch,
-            pin_swiglu_brute_force]
+            pin_swiglu_brute_force, pin_post_norm_vs_torch]

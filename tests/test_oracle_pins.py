@@ -63,6 +63,13 @@ MUTANTS = [
      "linear_row(xr, W1, T, NULL, NGO_ACT_NONE, K, F, h);"),
     ("sample index used as row", "        row_stats(norm, xr, K, eps, &mu, &rstd);\n        normalize_row(norm, xr, K, mu, rstd, g, b, a);\n        linear_row(a, W, T, bi, act, K, N, y + i * N);",
      "        for (int64_t k = 0; k < K; ++k) xr[k] = T[x[i * K + k]];\n        row_stats(norm, xr, K, eps, &mu, &rstd);\n        normalize_row(norm, xr, K, mu, rstd, g, b, a);\n        linear_row(a, W, T, bi, act, K, N, y + i * N);"),
+    ("post-norm drops the residual", "for (int64_t n = 0; n < N; ++n) hr[n] += T[residual[r * N + n]];",
+     "for (int64_t n = 0; n < N; ++n) hr[n] += 0.0 * T[residual[r * N + n]];"),
+    ("post-norm statistics over N - 1 columns", "row_stats(norm, hr, N, eps, &mu, &rstd);",
+     "row_stats(norm, hr, N - 1, eps, &mu, &rstd);"),
+    ("post-norm residual after the norm",
+     "        if (residual)\n            for (int64_t n = 0; n < N; ++n) hr[n] += T[residual[r * N + n]];\n        double mu, rstd;\n        row_stats(norm, hr, N, eps, &mu, &rstd);",
+     "        double mu, rstd;\n        row_stats(norm, hr, N, eps, &mu, &rstd);"),
     ("fold drops the mean term", "double z = rstd * s - rstd * mu * c[n] + bprime[n];",
      "double z = rstd * s + bprime[n];"),
 ]
