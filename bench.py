@@ -220,7 +220,8 @@ def op_keys(w):
     return {"ffn": ["x", "W1", "W2"],
             "mlp": ["x", "gamma", "beta", "W1", "b1", "W2", "b2"],
             "swiglu": ["x", "gamma", "beta", "Wg", "Wu"],
-            "mlp_swiglu": ["x", "gamma", "beta", "Wg", "Wu", "Wd"]}.get(
+            "mlp_swiglu": ["x", "gamma", "beta", "Wg", "Wu", "Wd"],
+            "linear_residual_norm": ["x", "W", "bias", "residual", "gamma", "beta"]}.get(
         w.op, ["x", "gamma", "beta", "W", "bias"])
 
 
@@ -237,6 +238,8 @@ def op_kernel_flops(w, decode):
     has_norm = w.op in ("layernorm_linear", "rmsnorm_linear") or w.norm != "none"
     if w.op == "swiglu":
         return ([0.0] if has_norm else []) + [2 * g]
+    if w.op == "linear_residual_norm":
+        return ([0.0] if decode else []) + [g, 0.0]
     if w.op == "mlp_swiglu":
         return ([0.0] if has_norm or decode else []) + [2 * g, g]
     if w.op in ("ffn", "mlp"):
@@ -267,6 +270,10 @@ def oracle_run(w, host, rows, lib):
     if w.op == "swiglu":
         return oracle.swiglu(nid, host["x"], host["gamma"], host["beta"], host["Wg"],
                              host["Wu"], w.eps, rows, lib)
+    if w.op == "linear_residual_norm":
+        return oracle.linear_residual_norm(nid, host["x"], host["W"], host["bias"],
+                                           host["residual"], host["gamma"], host["beta"], w.eps,
+                                           rows, lib)[1]
     return oracle.mlp_swiglu(nid, host["x"], host["gamma"], host["beta"], host["Wg"],
                              host["Wu"], host["Wd"], w.eps, rows, lib)
 
@@ -296,12 +303,13 @@ def our_arm(args, rank, world, local):
     n_sets = max(2, min(16, math.ceil(2 * L2_BYTES / set_bytes) + 1))
     op_code = {"layernorm_linear": B.OP_LAYERNORM_LINEAR, "rmsnorm_linear": B.OP_RMSNORM_LINEAR,
                "linear_silu": B.OP_LINEAR_SILU, "ffn": B.OP_FFN, "norm_linear": B.OP_NORM_LINEAR,
-               "mlp": B.OP_MLP, "swiglu": B.OP_SWIGLU, "mlp_swiglu": B.OP_MLP_SWIGLU}[w.op]
+               "mlp": B.OP_MLP, "swiglu": B.OP_SWIGLU, "mlp_swiglu": B.OP_MLP_SWIGLU,
+               "linear_residual_norm": B.OP_LINEAR_RESIDUAL_NORM}[w.op]
     sets = []
     for _ in range(n_sets):
         s = {k: host[k].to(dev) for k in keys}
         s["y"] = torch.empty((M, out_cols), dtype=w.dtype, device=dev)
-        if two_gemm:
+        if two_gemm or w.op == "linear_residual_norm":
             s["h"] = torch.empty((M, N), dtype=w.dtype, device=dev)
         nb = B.ngr_workspace_bytes(op_code, M, K, N, 0)
         s["ws"] = torch.empty(max(nb, 256), dtype=torch.uint8, device=dev)
@@ -330,6 +338,11 @@ def our_arm(args, rank, world, local):
             ngr.fused_mlp(s["x"], s["W1"], s["W2"], norm=nid, act=aid, gamma=g("gamma"),
                           beta=g("beta"), b1=g("b1"), b2=g("b2"), eps=w.eps, out=s["y"],
                           h=s["h"], workspace=s["ws"], stream=stream)
+        elif w.op == "linear_residual_norm":
+            ngr.fused_linear_residual_norm(s["x"], s["W"], s["gamma"], norm=nid, beta=g("beta"),
+                                           bias=g("bias"), residual=s["residual"], eps=w.eps,
+                                           out=s["y"], h=s["h"], workspace=s["ws"],
+                                           stream=stream)
         elif w.op == "swiglu":
             ngr.fused_norm_swiglu(s["x"], s["Wg"], s["Wu"], norm=nid, gamma=g("gamma"),
                                   beta=g("beta"), eps=w.eps, out=s["y"], workspace=s["ws"],
@@ -368,6 +381,8 @@ def our_arm(args, rank, world, local):
     algo_bytes = sum(host[k].numel() * host[k].element_size() for k in keys) + M * out_cols * 2
     if two_gemm:
         algo_bytes += 2 * M * N * 2  # H written once and read once
+    if w.op == "linear_residual_norm":
+        algo_bytes += 2 * M * N * 2  # h written once and read once
     ms_step = ms_total_max / args.steps
     if decode:
         metric, unit = "fused LN+GEMM HBM GB/s at M<=16 (decode)", "GB/s"
@@ -401,11 +416,14 @@ def our_arm(args, rank, world, local):
     roof["kernel_ms_all"] = per_kernel
 
     # ----------------------------------------- end to end from host buffers
-    x_host = host["x"].pin_memory()
+    # per-step activations copied in: x, and the residual stream when the op has one
+    in_keys = [k for k in ("x", "residual") if k in keys]
+    in_host = {k: host[k].pin_memory() for k in in_keys}
     y_host = torch.empty((M, out_cols), dtype=w.dtype).pin_memory()
     for i in range(min(3, args.warmup + 1)):
         s = sets[i % n_sets]
-        s["x"].copy_(x_host, non_blocking=True)
+        for k in in_keys:
+            s[k].copy_(in_host[k], non_blocking=True)
         step(s)
         y_host.copy_(s["y"], non_blocking=True)
     torch.cuda.synchronize(dev)
@@ -415,7 +433,8 @@ def our_arm(args, rank, world, local):
     e0.record(stream)
     for i in range(args.steps):
         s = sets[i % n_sets]
-        s["x"].copy_(x_host, non_blocking=True)
+        for k in in_keys:
+            s[k].copy_(in_host[k], non_blocking=True)
         step(s)
         y_host.copy_(s["y"], non_blocking=True)
     e1.record(stream)
@@ -426,7 +445,8 @@ def our_arm(args, rank, world, local):
         e2e_value = job_value(algo_bytes * args.steps / 1e9, world, e2e_ms / 1e3)
     else:
         e2e_value = job_value(flops * args.steps / 1e12, world, e2e_ms / 1e3)
-    e2e = {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": M * K * 2,
+    e2e = {"value": e2e_value, "unit": unit,
+           "h2d_bytes_per_step": sum(host[k].numel() * host[k].element_size() for k in in_keys),
            "d2h_bytes_per_step": M * out_cols * 2}
 
     # ---------------- same workload through the inference-mode fold (a7)
@@ -500,6 +520,10 @@ def our_arm(args, rank, world, local):
             if w.op == "mlp":
                 return F.linear(tacts[w.act](F.linear(tnorm(s), s["W1"], s.get("b1"))), s["W2"],
                                 s.get("b2"))
+            if w.op == "linear_residual_norm":
+                hh = F.linear(s["x"], s["W"], s.get("bias")) + s["residual"]
+                return (F.rms_norm(hh, (N,), s["gamma"], w.eps) if w.norm == "rms"
+                        else F.layer_norm(hh, (N,), s["gamma"], s["beta"], w.eps))
             a = tnorm(s)
             h = F.silu(F.linear(a, s["Wg"])) * F.linear(a, s["Wu"])
             return h if w.op == "swiglu" else F.linear(h, s["Wd"])

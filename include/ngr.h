@@ -90,7 +90,8 @@ typedef enum {
     NGR_OP_NORM_LINEAR = 4,   /* ngr_fused_norm_linear_act */
     NGR_OP_MLP = 5,           /* ngr_fused_mlp */
     NGR_OP_SWIGLU = 6,        /* ngr_fused_norm_swiglu */
-    NGR_OP_MLP_SWIGLU = 7     /* ngr_fused_mlp_swiglu */
+    NGR_OP_MLP_SWIGLU = 7,    /* ngr_fused_mlp_swiglu */
+    NGR_OP_LINEAR_RESIDUAL_NORM = 8  /* ngr_fused_linear_residual_norm */
 } ngr_op;
 
 /* Row normalization applied to x before the first product. */
@@ -208,6 +209,24 @@ int ngr_fused_mlp_swiglu(int norm, const void *x, const void *gamma,
                          const void *Wd, float eps, int64_t M, int64_t K,
                          int64_t F, int dtype, void *h, void *y, void *workspace,
                          size_t workspace_bytes, ngr_stream_t stream);
+
+/* A norm after the product (the output projection fused with the RMSNorm
+ * that follows it):
+ *   h = x . W^T + bias + residual  [M, N]   (bias, residual may be NULL),
+ *   y = norm(h) over each row's N columns: LayerNorm (h - mu) rstd gamma +
+ *       beta or RMSNorm h rstd gamma, with gamma, beta of length N.
+ * norm: 1 = LayerNorm, 2 = RMSNorm.  h goes to `h` when non-NULL (the
+ * residual stream a transformer keeps), else to the workspace
+ * (NGR_OP_LINEAR_RESIDUAL_NORM with ffn_h_in_workspace = 1).  The product's
+ * epilogue adds bias and residual and writes h once; one statistics pass
+ * per h row then writes y.  [MMF] §五 optimization 3 (MatMul(Output) fused
+ * with the following RMSNorm). */
+int ngr_fused_linear_residual_norm(int norm, const void *x, const void *W,
+                                   const void *bias, const void *residual,
+                                   const void *gamma, const void *beta,
+                                   float eps, int64_t M, int64_t K, int64_t N,
+                                   int dtype, void *h, void *y, void *workspace,
+                                   size_t workspace_bytes, ngr_stream_t stream);
 
 /* Inference-mode weight fold, step 1 of 2 ([LNF] §6.2: with gamma and beta
  * fixed, gamma is folded into the matmul weight once, ahead of the calls).

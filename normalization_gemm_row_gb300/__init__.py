@@ -11,6 +11,7 @@ from ._build import build, LIB_PATH  # noqa: F401
 from .binding import (  # noqa: F401
     ACT_GELU, ACT_NONE, ACT_RELU, ACT_SILU, NORM_LAYER, NORM_NONE, NORM_RMS,
     NgrError, ffn_linear_silu_linear, fold_prepare, fused_layernorm_linear,
-    fused_linear_silu, fused_mlp, fused_mlp_swiglu, fused_norm_linear_act,
+    fused_linear_residual_norm, fused_linear_silu, fused_mlp, fused_mlp_swiglu,
+    fused_norm_linear_act,
     fused_norm_linear_folded, fused_norm_swiglu, fused_rmsnorm_linear,
     row_stats)

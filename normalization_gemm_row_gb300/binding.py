@@ -25,7 +25,7 @@ from ._build import LIB_PATH
 
 NGR_F16, NGR_BF16 = 0, 1
 OP_LAYERNORM_LINEAR, OP_RMSNORM_LINEAR, OP_LINEAR_SILU, OP_FFN = 0, 1, 2, 3
-OP_NORM_LINEAR, OP_MLP, OP_SWIGLU, OP_MLP_SWIGLU = 4, 5, 6, 7
+OP_NORM_LINEAR, OP_MLP, OP_SWIGLU, OP_MLP_SWIGLU, OP_LINEAR_RESIDUAL_NORM = 4, 5, 6, 7, 8
 NORM_NONE, NORM_LAYER, NORM_RMS = 0, 1, 2
 ACT_NONE, ACT_SILU, ACT_RELU, ACT_GELU = 0, 1, 2, 3
 STATUS = {0: "NGR_OK", -1: "NGR_ERR_NULL", -2: "NGR_ERR_SHAPE",
@@ -47,6 +47,7 @@ SIGNATURES = {
     "ngr_fused_mlp": (_I, [_I, _I, _P, _P, _P, _P, _P, _P, _P, _F, _I64, _I64, _I64, _I, _P, _P, _P, _SZ, _P]),
     "ngr_fused_norm_swiglu": (_I, [_I, _P, _P, _P, _P, _P, _F, _I64, _I64, _I64, _I, _P, _P, _SZ, _P]),
     "ngr_fused_mlp_swiglu": (_I, [_I, _P, _P, _P, _P, _P, _P, _F, _I64, _I64, _I64, _I, _P, _P, _P, _SZ, _P]),
+    "ngr_fused_linear_residual_norm": (_I, [_I, _P, _P, _P, _P, _P, _P, _F, _I64, _I64, _I64, _I, _P, _P, _P, _SZ, _P]),
     "ngr_row_stats": (_I, [_I, _P, _F, _I64, _I64, _I, _P, _P]),
     "ngr_fold_prepare": (_I, [_I, _P, _P, _P, _P, _I64, _I64, _I, _P, _P, _P]),
     "ngr_fused_norm_linear_folded": (_I, [_I, _P, _P, _P, _F, _I64, _I64, _I64, _I, _P, _P, _SZ, _P]),
@@ -152,6 +153,12 @@ def ngr_fused_mlp_swiglu(norm, x, gamma, beta, Wg, Wu, Wd, eps, M, K, F, dtype, 
                          ws_bytes, stream) -> int:
     return lib().ngr_fused_mlp_swiglu(norm, x, gamma, beta, Wg, Wu, Wd, eps, M, K, F, dtype,
                                       h, y, ws, ws_bytes, stream)
+
+
+def ngr_fused_linear_residual_norm(norm, x, W, bias, residual, gamma, beta, eps, M, K, N,
+                                   dtype, h, y, ws, ws_bytes, stream) -> int:
+    return lib().ngr_fused_linear_residual_norm(norm, x, W, bias, residual, gamma, beta, eps,
+                                                M, K, N, dtype, h, y, ws, ws_bytes, stream)
 
 
 def ngr_fold_prepare(norm, gamma, beta, W, bias, K, N, dtype, Wf, cb, stream) -> int:
@@ -424,6 +431,29 @@ def fused_mlp_swiglu(x, Wg, Wu, Wd, norm: int = NORM_NONE, gamma=None, beta=None
                               _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
     _raise(rc, "fused_mlp_swiglu")
     return y.reshape(*x.shape[:-1], K)
+
+
+def fused_linear_residual_norm(x, W, gamma, norm: int = NORM_RMS, beta=None, bias=None,
+                               residual=None, eps=1e-5, out=None, h=None, workspace=None,
+                               stream=None):
+    """(h, y): h = x . W^T + bias + residual, y = norm(h) over its N columns
+    (gamma, beta of length N).  h goes to ``h`` when given."""
+    K = x.shape[-1]
+    N = W.shape[0]
+    x2 = x.reshape(-1, K)
+    M = x2.shape[0]
+    r2 = residual.reshape(-1, N) if residual is not None else None
+    _check(x2, W, gamma, beta, bias, r2, out, h, dtype=x.dtype)
+    y = out if out is not None else torch.empty((M, N), dtype=x.dtype, device=x.device)
+    hh = h if h is not None else torch.empty((M, N), dtype=x.dtype, device=x.device)
+    nb = ngr_workspace_bytes(OP_LINEAR_RESIDUAL_NORM, M, K, N, 0)
+    ws = _workspace(nb, x.device, workspace)
+    rc = ngr_fused_linear_residual_norm(norm, _ptr(x2), _ptr(W), _ptr(bias), _ptr(r2),
+                                        _ptr(gamma), _ptr(beta), eps, M, K, N, _dtype_code(x),
+                                        _ptr(hh), _ptr(y), _ptr(ws),
+                                        ws.numel() * ws.element_size(), _stream(stream))
+    _raise(rc, "fused_linear_residual_norm")
+    return hh.reshape(*x.shape[:-1], N), y.reshape(*x.shape[:-1], N)
 
 
 def fold_prepare(norm: int, gamma, beta, W, bias=None, stream=None):

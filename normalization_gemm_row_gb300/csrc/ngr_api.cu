@@ -107,6 +107,7 @@ WsLayout ws_layout(int op, int64_t M, int64_t K_, int64_t N_, bool h_in_ws)
                       op == NGR_OP_MLP_SWIGLU;
     const bool gated = op == NGR_OP_SWIGLU || op == NGR_OP_MLP_SWIGLU;
     const bool chain = op == NGR_OP_FFN || op == NGR_OP_MLP || op == NGR_OP_MLP_SWIGLU;
+    const bool post_norm = op == NGR_OP_LINEAR_RESIDUAL_NORM;
     const bool decode = M > 0 && M <= kDecodeMaxM;
     if (norm) {
         L.stats = off;
@@ -135,6 +136,15 @@ WsLayout ws_layout(int op, int64_t M, int64_t K_, int64_t N_, bool h_in_ws)
     if (chain && h_in_ws) {
         L.h = off;
         off += align256(static_cast<size_t>(M) * static_cast<size_t>(N) * 2);
+    }
+    if (post_norm) {
+        // statistics of the output rows; h [M, N] when the caller keeps none
+        L.stats = off;
+        off += align256(static_cast<size_t>(M) * 8);
+        if (h_in_ws) {
+            L.h = off;
+            off += align256(static_cast<size_t>(M) * static_cast<size_t>(N) * 2);
+        }
     }
     if (pad) {
         L.padded = true;
@@ -318,7 +328,8 @@ int launch_layer(int norm, int act, bool bf16, const void *x, const void *W,
                  const void *bias, int64_t M, int64_t K, int64_t N, void *y,
                  char *ws, const WsLayout &L, size_t counters_off, bool pdl,
                  const DevInfo &di, cudaStream_t stream, const float *fold_c = nullptr,
-                 const float *fold_b = nullptr, int64_t w_rows = -1)
+                 const float *fold_b = nullptr, int64_t w_rows = -1,
+                 const void *residual = nullptr)
 {
     // W has w_rows rows (N unless the output is padded past W's rows; the
     // tensor maps zero-fill the rest).
@@ -341,6 +352,7 @@ int launch_layer(int norm, int act, bool bf16, const void *x, const void *W,
         d.bias = bias;
         d.fold_c = fold_c;
         d.fold_b = fold_b;
+        d.residual = residual;
         d.y = y;
         d.partials = reinterpret_cast<float *>(ws + L.partials);
         d.counters = reinterpret_cast<int *>(ws + counters_off);
@@ -377,6 +389,7 @@ int launch_layer(int norm, int act, bool bf16, const void *x, const void *W,
     a.bias = bias;
     a.fold_c = fold_c;
     a.fold_b = fold_b;
+    a.residual = residual;
     a.y = y;
     a.err = err;
     a.zero_err = zero_err;
@@ -683,6 +696,61 @@ int swiglu_chain(int op, int norm, const void *x, const void *gamma, const void 
     return finish(rc, ws, stream);
 }
 
+// h = x W^T + bias (+ residual), written once; y = norm(h) over its N
+// columns: the product's epilogue adds the bias and the residual, then the
+// statistics kernel reads each h row once, computes its statistics and
+// writes the normalized row (gamma, beta of length N).
+int linear_residual_norm(int norm, const void *x, const void *W, const void *bias,
+                         const void *residual, const void *gamma, const void *beta, float eps,
+                         int64_t M, int64_t K, int64_t N, int dtype, void *h, void *y, void *ws,
+                         size_t ws_bytes, cudaStream_t stream)
+{
+    if (norm != kNormLayer && norm != kNormRms) return NGR_ERR_ARG;
+    int rc = check_sizes(M, K, N, dtype);
+    if (rc != NGR_OK) return rc;
+    if (M == 0) return NGR_OK;
+    if (!x || !W || !gamma || !y || (norm == kNormLayer && !beta)) return NGR_ERR_NULL;
+    if (!ws) return NGR_ERR_WORKSPACE;
+    if (!aligned16(x) || !aligned16(W) || !aligned16(gamma) || !aligned16(y) ||
+        (beta && !aligned16(beta)) || (bias && !aligned16(bias)) ||
+        (residual && !aligned16(residual)) || (h && !aligned16(h)))
+        return NGR_ERR_ALIGN;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return NGR_ERR_ALIGN;
+    const WsLayout L = ws_layout(NGR_OP_LINEAR_RESIDUAL_NORM, M, K, N, h == nullptr);
+    if (ws_bytes < L.total) return NGR_ERR_WORKSPACE;
+    DevInfo di;
+    rc = current_device_info(&di);
+    if (rc != NGR_OK) return rc;
+    const bool bf16 = dtype == NGR_BF16;
+    char *w = static_cast<char *>(ws);
+    void *H = h ? h : static_cast<void *>(w + L.h);
+    if (debug_mode() && cudaMemsetAsync(w, 0, 4, stream) != cudaSuccess) return NGR_ERR_CUDA;
+    const bool decode = M <= kDecodeMaxM;
+    events_reset();
+    if (decode) {
+        // the decode product's split-K counters start from zero
+        event_before(stream);
+        rc = launch_rowstats(kNormRms, bf16, x, 0, K, 0.f, nullptr, nullptr, nullptr, nullptr,
+                             nullptr, reinterpret_cast<int *>(w + L.counters),
+                             static_cast<int>(ceil_div(N, 128) * 4), reinterpret_cast<int *>(w),
+                             di.sms, stream);
+        event_after(stream);
+        if (rc != NGR_OK) return rc;
+    }
+    event_before(stream);
+    rc = launch_layer(kNormNone, kActNone, bf16, x, W, bias, M, K, N, H, w, L, L.counters, decode,
+                      di, stream, nullptr, nullptr, -1, residual);
+    event_after(stream);
+    if (rc != NGR_OK) return rc;
+    // The norm over each h row (a plain launch: it reads the product's output).
+    event_before(stream);
+    rc = launch_rowstats(norm, bf16, H, M, N, eps, reinterpret_cast<float2 *>(w + L.stats), gamma,
+                         beta, nullptr, nullptr, nullptr, 0, nullptr, di.sms, stream, y);
+    event_after(stream);
+    events_call_done();
+    return finish(rc, ws, stream);
+}
+
 __global__ void bounded_wait_probe_kernel(int *err, unsigned long long timeout_ns)
 {
     __shared__ uint64_t bar;
@@ -715,7 +783,7 @@ extern "C" {
 
 size_t ngr_workspace_bytes(int op, int64_t M, int64_t K, int64_t N, int ffn_h_in_workspace)
 {
-    if (op < NGR_OP_LAYERNORM_LINEAR || op > NGR_OP_MLP_SWIGLU) return 0;
+    if (op < NGR_OP_LAYERNORM_LINEAR || op > NGR_OP_LINEAR_RESIDUAL_NORM) return 0;
     if (M < 0 || K <= 0 || N <= 0 || M >= kMaxDim || K >= kMaxDim || N >= kMaxDim) return 0;
     return ws_layout(op, M, K, N, ffn_h_in_workspace != 0).total;
 }
@@ -801,6 +869,17 @@ int ngr_fused_mlp_swiglu(int norm, const void *x, const void *gamma, const void 
     return swiglu_chain(NGR_OP_MLP_SWIGLU, norm, x, gamma, norm == kNormLayer ? beta : nullptr, Wg,
                         Wu, Wd, eps, M, K, F, dtype, h, y, workspace, workspace_bytes,
                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ngr_fused_linear_residual_norm(int norm, const void *x, const void *W, const void *bias,
+                                   const void *residual, const void *gamma, const void *beta,
+                                   float eps, int64_t M, int64_t K, int64_t N, int dtype,
+                                   void *h, void *y, void *workspace, size_t workspace_bytes,
+                                   ngr_stream_t stream)
+{
+    return linear_residual_norm(norm, x, W, bias, residual, gamma, norm == kNormLayer ? beta : nullptr,
+                                eps, M, K, N, dtype, h, y, workspace, workspace_bytes,
+                                reinterpret_cast<cudaStream_t>(stream));
 }
 
 int ngr_fold_prepare(int norm, const void *gamma, const void *beta, const void *W,

@@ -259,6 +259,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                     if (args.act == kActSilu) z = silu_f(z);
                     else if (args.act == kActRelu) z = fmaxf(z, 0.0f);
                     else if (args.act == kActGelu) z = gelu_f(z);
+                    if (args.residual != nullptr)
+                        z += to_float1<BF16>(static_cast<const uint16_t *>(args.residual) +
+                                                 static_cast<long long>(m) * N, n);
                     uint16_t o;
                     if constexpr (BF16) {
                         __nv_bfloat16 h = __float2bfloat16_rn(z);

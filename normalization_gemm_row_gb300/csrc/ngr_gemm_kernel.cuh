@@ -190,7 +190,8 @@ __device__ __forceinline__ uint4 transform8_pk(uint4 v, float2 so, const float2 
 
 // The epilogue of 32 accumulator columns [n0, n0 + 32) of one row: + bias,
 // or with a folded norm y = rstd acc + (-mu rstd) c[n] + b'[n] (so =
-// (rstd, -mu rstd) of the row), then the activation, rounding, 16-byte stores.
+// (rstd, -mu rstd) of the row), then the activation, + residual, rounding,
+// 16-byte stores.
 template <int NORM, bool BF16>
 __device__ __forceinline__ void epilogue_store32(float (&v)[32], int row, int n0,
                                                  const GemmArgs &args, float2 so)
@@ -231,6 +232,22 @@ __device__ __forceinline__ void epilogue_store32(float (&v)[32], int row, int n0
         }
     }
     apply_act32(args.act, v);
+    if (args.residual != nullptr && row < M) {
+        const uint16_t *rrow = static_cast<const uint16_t *>(args.residual) + static_cast<int64_t>(row) * N;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (n0 + 8 * j < N) {
+                const uint4 rv = __ldg(reinterpret_cast<const uint4 *>(rrow + n0 + 8 * j));
+                const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 f = to_float2<BF16>(rw[i]);
+                    v[8 * j + 2 * i] += f.x;
+                    v[8 * j + 2 * i + 1] += f.y;
+                }
+            }
+        }
+    }
     store_row32<BF16>(v, row, n0, args.y, M, N);
 }
 

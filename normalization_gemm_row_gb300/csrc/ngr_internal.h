@@ -54,6 +54,7 @@ struct alignas(128) GemmArgs {
     const void *bias;       // [N] or nullptr
     const float *fold_c;    // folded forms: c[n] = sum_k W'[n,k] (FP32)
     const float *fold_b;    // folded forms: b'[n] = beta . W[n,:] + bias[n] (FP32)
+    const void *residual;   // [M, N] added last, or nullptr
     void *y;                // [M, N]
     int *err;               // device error word
     int zero_err;           // nonzero: this kernel is the call's first and clears *err
@@ -73,6 +74,7 @@ struct alignas(128) DecodeArgs {
     const void *bias;
     const float *fold_c;
     const float *fold_b;
+    const void *residual;   // [M, N] added last, or nullptr
     void *y;
     float *partials;        // [n_tiles][kDecodeMaxContrib][MN][128] fp32
     int *counters;          // [n_tiles], zero at kernel start

@@ -31,7 +31,8 @@ class Workload:
     """One named workload: the op, its sizes and its input distribution."""
     name: str
     op: str                   # layernorm_linear | rmsnorm_linear | linear_silu | ffn |
-                              # norm_linear | mlp | swiglu | mlp_swiglu
+                              # norm_linear | mlp | swiglu | mlp_swiglu |
+                              # linear_residual_norm
     M: int
     K: int
     N: int                    # output features (F, the hidden width, for ffn)
@@ -80,6 +81,10 @@ WORKLOADS = [
     # widths (hidden 8192, intermediate 28672).
     Workload("mlp_swiglu_rms_bf16_m512_k8192_f28672", "mlp_swiglu",
              512, 8192, 28672, BF16, False, 1e-5, 1240, norm="rms"),
+    # The attention output projection with its residual and the RMSNorm that
+    # follows it (Llama2-70B widths).
+    Workload("linear_residual_rmsnorm_bf16_m512_k8192_n8192", "linear_residual_norm",
+             512, 8192, 8192, BF16, False, 1e-5, 1241, norm="rms"),
 ]
 BY_NAME = {w.name: w for w in WORKLOADS}
 
@@ -119,6 +124,17 @@ def make(w: Workload, seed: int | None = None) -> dict:
     if w.op == "ffn":
         d["W1"] = _weight(g, N, K, K ** -0.5, dt)
         d["W2"] = _weight(g, K, N, N ** -0.5, dt)
+        return d
+    if w.op == "linear_residual_norm":
+        # x; W [N, K]; bias [N]; residual [M, N] ~ N(0, 1); the norm's gamma
+        # (and beta) of length N.
+        d["W"] = _weight(g, N, K, K ** -0.5, dt)
+        if w.bias:
+            d["bias"] = (0.1 * _normal(g, (N,))).to(dt)
+        d["residual"] = _normal(g, (M, N)).to(dt)
+        d["gamma"] = (1.0 + 0.1 * _normal(g, (N,))).to(dt)
+        if w.norm == "layer":
+            d["beta"] = (0.1 * _normal(g, (N,))).to(dt)
         return d
     if w.op in ("norm_linear", "mlp", "swiglu", "mlp_swiglu"):
         # x; gamma (and beta for layer) by the norm; then the weights:

@@ -61,7 +61,7 @@ def test_workspace_bytes_layout(lib):
     h1 = wb(B.OP_FFN, 512, 14336, 49152, 1)
     assert h1 - h0 == 512 * 49152 * 2
     # invalid sizes or ops give 0
-    assert wb(B.OP_FFN, -1, 8, 8) == 0 and wb(8, 1, 8, 8) == 0 and wb(0, 1, 0, 8) == 0
+    assert wb(B.OP_FFN, -1, 8, 8) == 0 and wb(9, 1, 8, 8) == 0 and wb(0, 1, 0, 8) == 0
     assert wb(-1, 1, 8, 8) == 0
 
 
@@ -88,6 +88,27 @@ def test_other_entry_points_still_need_alignment(lib):
                            None, A16, A16 * 16, big, None) == -3
     assert B.ngr_fused_norm_linear_folded(1, A16, A16, A16, 1e-5, 4, 60, 64, 0, A16,
                                           A16 * 16, big, None) == -3
+
+
+def test_post_norm_workspace_and_rejections(lib):
+    wb = B.ngr_workspace_bytes
+    w0 = wb(B.OP_LINEAR_RESIDUAL_NORM, 1024, 8192, 8192, 0)
+    assert w0 == 256 + 1024 * 8
+    assert wb(B.OP_LINEAR_RESIDUAL_NORM, 1024, 8192, 8192, 1) - w0 == 1024 * 8192 * 2
+    assert wb(B.OP_LINEAR_RESIDUAL_NORM, 8, 8192, 8192) > 256 + 8 * 8 + 256   # split-K regions
+    f = B.ngr_fused_linear_residual_norm
+    big, ws = 1 << 24, A16 * 16
+    assert f(0, A16, A16, None, None, A16, None, 1e-5, 4, 64, 64, 0, None, A16, ws, big, None) == -9
+    assert f(2, A16, A16, None, None, 0, None, 1e-5, 4, 64, 64, 0, None, A16, ws, big, None) == -1
+    assert f(1, A16, A16, None, None, A16, 0, 1e-5, 4, 64, 64, 0, None, A16, ws, big, None) == -1
+    assert f(2, A16, A16, None, A16 + 8, A16, None, 1e-5, 4, 64, 64, 0, None, A16, ws, big,
+             None) == -3                                               # misaligned residual
+    assert f(2, A16, A16, None, None, A16, None, 1e-5, 4, 64, 60, 0, None, A16, ws, big,
+             None) == -3                                               # N % 8
+    assert f(2, A16, A16, None, None, A16, None, 1e-5, 4, 64, 64, 0, None, A16, ws, 300,
+             None) == -5
+    assert f(2, A16, A16, None, None, A16, None, 1e-5, 0, 64, 64, 0, None, A16, ws, big,
+             None) == 0
 
 
 def test_workspace_bytes_new_ops(lib):

@@ -220,3 +220,45 @@ def test_mlp_swiglu_full_size_sampled_rows():
     ref = oracle.mlp_swiglu(oracle.NORM_RMS, d["x"], d["gamma"], None, d["Wg"], d["Wu"],
                             d["Wd"], w.eps, rows)
     check(got, ref, w.name)
+
+
+# ------------------------------------------------- norm after the product
+@pytest.mark.parametrize("M", [3, 300], ids=["decode", "tile"])
+@pytest.mark.parametrize("norm", ["rms", "layer"])
+@pytest.mark.parametrize("with_res,with_bias", [(True, False), (False, True), (True, True)])
+def test_linear_residual_norm(norm, with_res, with_bias, M):
+    K, N = 512, 520
+    for dtype in (torch.float16, torch.bfloat16):
+        d = inputs.case("norm_linear", M, K, N, dtype, with_bias, 1e-5, seed=M + N + with_res,
+                        norm="none")
+        g = torch.Generator().manual_seed(M + 1)
+        res = (torch.randn((M, N), generator=g) + 1.0).to(dtype) if with_res else None
+        gamma = (1.0 + 0.1 * torch.randn((N,), generator=g)).to(dtype)
+        beta = (0.1 * torch.randn((N,), generator=g)).to(dtype) if norm == "layer" else None
+        h, y = ngr.fused_linear_residual_norm(dev(d["x"]), dev(d["W"]), dev(gamma),
+                                              norm=NORMS[norm][1], beta=dev(beta),
+                                              bias=dev(d["bias"]), residual=dev(res), eps=1e-5)
+        torch.cuda.synchronize()
+        href, yref = oracle.linear_residual_norm(NORMS[norm][0], d["x"], d["W"], d["bias"], res,
+                                                 gamma, beta, 1e-5)
+        check(h, href, f"post-norm h {norm} res={with_res} bias={with_bias} M={M} {dtype}")
+        check(y, yref, f"post-norm y {norm} res={with_res} bias={with_bias} M={M} {dtype}")
+
+
+def test_linear_residual_norm_llama_output_projection():
+    """The Llama-70B attention output projection (8192 x 8192) with the
+    residual and the following RMSNorm, 512 tokens, sampled rows."""
+    M, K, N = 512, 8192, 8192
+    d = inputs.case("norm_linear", M, K, N, torch.bfloat16, False, 1e-5, seed=4242)
+    g = torch.Generator().manual_seed(4243)
+    res = torch.randn((M, N), generator=g).to(torch.bfloat16)
+    gamma = (1.0 + 0.1 * torch.randn((N,), generator=g)).to(torch.bfloat16)
+    h, y = ngr.fused_linear_residual_norm(dev(d["x"]), dev(d["W"]), dev(gamma), norm=B.NORM_RMS,
+                                          residual=dev(res), eps=1e-5)
+    torch.cuda.synchronize()
+    rows = inputs.sample_rows(M, 16, seed=2).tolist()
+    idx = torch.as_tensor(rows, device="cuda")
+    href, yref = oracle.linear_residual_norm(oracle.NORM_RMS, d["x"], d["W"], None, res, gamma,
+                                             None, 1e-5, rows)
+    check(h[idx], href, "llama o-proj h")
+    check(y[idx], yref, "llama o-proj y")
