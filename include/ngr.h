@@ -309,6 +309,15 @@ int ngr_debug_bounded_wait(void *workspace, uint32_t timeout_us,
  * the initial setting.  Returns NGR_OK or NGR_ERR_ARG. */
 int ngr_set_tile_config(int pair, int bn, int nsub);
 
+/* Inspection aid: the tile-kernel variant a call of `op` with these sizes
+ * would launch on the current device, with a workspace of
+ * ngr_workspace_bytes(op, M, K, N, 0) bytes, for its main product (the
+ * chains' second product).  Writes plan[0..5] = pair (0/1), N (sub-)tile
+ * width, sub-tiles per tile, K splits, CTAs, pipeline stages.  Returns
+ * NGR_OK, NGR_ERR_ARG (bad op, or a shape that takes the decode or gated
+ * kernel), NGR_ERR_NULL, or NGR_ERR_ARCH / NGR_ERR_CUDA. */
+int ngr_tile_plan(int op, int64_t M, int64_t K, int64_t N, int *plan);
+
 /* Profiling aid: time every kernel of this thread's next `n_calls` calls.
  * Each such call records CUDA events (the library's own, created here; no
  * device memory) on its stream just before and just after each kernel it

@@ -57,6 +57,7 @@ SIGNATURES = {
     "ngr_version": (_I, []),
     "ngr_last_error": (ctypes.c_char_p, []),
     "ngr_set_tile_config": (_I, [_I, _I, _I]),
+    "ngr_tile_plan": (_I, [_I, _I64, _I64, _I64, _P]),
     "ngr_kernel_timing_start": (_I, [_I]),
     "ngr_kernel_timing_stop": (_I, [_P, _I]),
 }
@@ -197,6 +198,17 @@ def ngr_last_error() -> str:
 
 def ngr_set_tile_config(pair, bn, nsub) -> int:
     return lib().ngr_set_tile_config(pair, bn, nsub)
+
+
+def ngr_tile_plan(op, M, K, N, plan) -> int:
+    return lib().ngr_tile_plan(op, M, K, N, plan)
+
+
+def tile_plan(op: int, M: int, K: int, N: int) -> dict:
+    """The tile-kernel variant a call would launch on the current device."""
+    arr = (ctypes.c_int * 6)()
+    _raise(ngr_tile_plan(op, M, K, N, ctypes.cast(arr, ctypes.c_void_p)), "ngr_tile_plan")
+    return dict(zip(("pair", "bn", "nsub", "splits", "grid", "stages"), list(arr)))
 
 
 def set_tile_config(pair: int = -1, bn: int = 0, nsub: int = 0):

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <cstdlib>
 #include <cstdio>
@@ -69,12 +70,31 @@ struct WsLayout {
     // padded copies (single-layer ops with K or N not a multiple of 8)
     size_t xp = 0, wp = 0, gp = 0, bp = 0, biasp = 0, yp = 0;
     bool padded = false;
+    // K-split counters and partials of the split-eligible product
+    size_t split_cnt = 0, split_cnt_bytes = 0, split_part = 0, split_part_bytes = 0;
     size_t partials = 0, counters = 0, counters2 = 0, h = 0;
     size_t total = 0;
 };
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int64_t round8(int64_t v) { return (v + 7) & ~static_cast<int64_t>(7); }
+
+// Room for a two-way K split of an M x Nout product on the CTA-pair kernel,
+// reserved only when the output has few 256 x 448 tiles (a GPU's pairs
+// would otherwise idle): the largest counters and partials over the pair
+// tile widths, so any two-way plan fits.  Independent of the device.
+void split_reserve(int64_t M, int64_t Nout, size_t *cnt_bytes, size_t *part_bytes)
+{
+    *cnt_bytes = *part_bytes = 0;
+    if (M <= kBM) return;
+    const int64_t mt = (M + 2 * kBM - 1) / (2 * kBM);
+    if (mt * ((Nout + 447) / 448) > 48) return;
+    for (int tw : {128, 192, 224, 256, 384, 448, 512}) {
+        const int64_t tiles = mt * ((Nout + tw - 1) / tw);
+        *cnt_bytes = std::max(*cnt_bytes, split_counter_bytes(tiles, tw));
+        *part_bytes = std::max(*part_bytes, split_partial_bytes(tiles, tw, 2));
+    }
+}
 
 // Ops that take any K and N (through padded copies).
 bool single_layer_op(int op)
@@ -144,6 +164,19 @@ WsLayout ws_layout(int op, int64_t M, int64_t K_, int64_t N_, bool h_in_ws)
         if (h_in_ws) {
             L.h = off;
             off += align256(static_cast<size_t>(M) * static_cast<size_t>(N) * 2);
+        }
+    }
+    {
+        // the product that may split K: the single layer's, or the chain's
+        // second (K output columns)
+        const bool single = single_layer_op(op) || post_norm;
+        const int64_t nout = single ? N : K;
+        if ((single || chain) && !decode) {
+            split_reserve(M, nout, &L.split_cnt_bytes, &L.split_part_bytes);
+            L.split_cnt = off;
+            off += align256(L.split_cnt_bytes);
+            L.split_part = off;
+            off += align256(L.split_part_bytes);
         }
     }
     if (pad) {
@@ -311,6 +344,16 @@ int check_sizes(int64_t M, int64_t K, int64_t N, int dtype)
     return NGR_OK;
 }
 
+// The K-split counters start every call at zero (the kernels also reset
+// each counter after its last use); first on the stream, before any kernel.
+int zero_split_counters(const WsLayout &L, char *ws, cudaStream_t stream)
+{
+    if (L.split_cnt_bytes == 0) return NGR_OK;
+    const cudaError_t e = cudaMemsetAsync(ws + L.split_cnt, 0, L.split_cnt_bytes, stream);
+    return e == cudaSuccess ? NGR_OK : record_cuda_error("cudaMemsetAsync (split counters)", e,
+                                                         cudaGetErrorString(e));
+}
+
 int finish(int rc, void *ws, cudaStream_t stream)
 {
     if (rc != NGR_OK) return rc;
@@ -329,7 +372,7 @@ int launch_layer(int norm, int act, bool bf16, const void *x, const void *W,
                  char *ws, const WsLayout &L, size_t counters_off, bool pdl,
                  const DevInfo &di, cudaStream_t stream, const float *fold_c = nullptr,
                  const float *fold_b = nullptr, int64_t w_rows = -1,
-                 const void *residual = nullptr)
+                 const void *residual = nullptr, bool may_split = false)
 {
     // W has w_rows rows (N unless the output is padded past W's rows; the
     // tensor maps zero-fill the rest).
@@ -375,12 +418,13 @@ int launch_layer(int norm, int act, bool bf16, const void *x, const void *W,
     }
     GemmArgs a;
     std::memset(&a, 0, sizeof(a));
-    const GemmPlan plan = plan_gemm(M, N, K, di.sms, has_norm);
+    const GemmPlan plan = plan_gemm(M, N, K, di.sms, has_norm,
+                                    may_split ? L.split_cnt_bytes + L.split_part_bytes : 0);
     if (trace_mode())
-        std::fprintf(stderr, "ngr: tile kernel M=%lld N=%lld K=%lld norm=%d %s BN=%d x %d stages=%d grid=%d smem=%zu\n",
+        std::fprintf(stderr, "ngr: tile kernel M=%lld N=%lld K=%lld norm=%d %s BN=%d x %d splits=%d stages=%d grid=%d smem=%zu\n",
                      static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(K), norm,
-                     plan.pair ? "cta-pair" : "single-cta", plan.bn, plan.nsub, plan.stages, plan.grid,
-                     plan.smem);
+                     plan.pair ? "cta-pair" : "single-cta", plan.bn, plan.nsub, plan.splits, plan.stages,
+                     plan.grid, plan.smem);
     if (!map_2d(&a.map_a, x, bf16, M, K, kBM) ||
         !map_2d(&a.map_b, W, bf16, w_rows, K, static_cast<uint32_t>(plan.b_rows)))
         return NGR_ERR_CUDA;
@@ -402,6 +446,12 @@ int launch_layer(int norm, int act, bool bf16, const void *x, const void *W,
     a.num_tiles = a.m_tiles * a.n_tiles;
     a.timeout_ns = wait_timeout_ns();
     a.act = act;
+    a.k_splits = plan.splits > 1 ? plan.splits : 1;
+    a.kb_per_split = static_cast<int>(ceil_div(a.k_blocks, a.k_splits));
+    if (a.k_splits > 1) {
+        a.split_counters = reinterpret_cast<int *>(ws + L.split_cnt);
+        a.partials = reinterpret_cast<float *>(ws + L.split_part);
+    }
     return launch_gemm(norm, bf16, plan, a, pdl, stream);
 }
 
@@ -471,6 +521,8 @@ int norm_linear(int op, int norm, int act, const void *x, const void *gamma, con
     const bool bf16 = dtype == NGR_BF16;
     char *w = static_cast<char *>(ws);
     if (debug_mode() && cudaMemsetAsync(w, 0, 4, stream) != cudaSuccess) return NGR_ERR_CUDA;
+    rc = zero_split_counters(L, w, stream);
+    if (rc != NGR_OK) return rc;
     // Padded operands: rows of K8 (N8) elements with zero tails.
     const int64_t K8 = round8(K), N8 = round8(N);
     const void *xa = x, *Wa = W, *ga = gamma, *ba = beta, *biasa = bias;
@@ -518,10 +570,10 @@ int norm_linear(int op, int norm, int act, const void *x, const void *gamma, con
     // Decode sizes multiply the normalized rows the statistics kernel wrote.
     if (decode && norm != kNormNone)
         rc = launch_layer(kNormNone, act, bf16, w + L.xhat, Wa, biasa, M, K8, N8, ya, w, L,
-                          L.counters, true, di, stream, nullptr, nullptr, N);
+                          L.counters, true, di, stream, nullptr, nullptr, N, nullptr, true);
     else
         rc = launch_layer(norm, act, bf16, xa, Wa, biasa, M, K8, N8, ya, w, L, L.counters,
-                          need_stats, di, stream, nullptr, nullptr, N);
+                          need_stats, di, stream, nullptr, nullptr, N, nullptr, true);
     event_after(stream);
     if (rc == NGR_OK && ya != y) rc = launch_unpad_rows(ya, M, N, N8, y, di.sms, stream);
     events_call_done();
@@ -552,6 +604,8 @@ int folded_linear(int norm, const void *x, const void *Wf, const float *cb, floa
     char *w = static_cast<char *>(ws);
     if (debug_mode() && cudaMemsetAsync(w, 0, 4, stream) != cudaSuccess) return NGR_ERR_CUDA;
     const bool decode = M <= kDecodeMaxM;
+    rc = zero_split_counters(L, w, stream);
+    if (rc != NGR_OK) return rc;
     events_reset();
     event_before(stream);
     rc = launch_rowstats(norm, bf16, x, M, K, eps, reinterpret_cast<float2 *>(w + L.stats), nullptr,
@@ -563,7 +617,8 @@ int folded_linear(int norm, const void *x, const void *Wf, const float *cb, floa
     if (rc != NGR_OK) return rc;
     event_before(stream);
     rc = launch_layer(norm == kNormLayer ? kNormFoldLayer : kNormFoldRms, kActNone, bf16, x, Wf,
-                      nullptr, M, K, N, y, w, L, L.counters, true, di, stream, cb, cb + N);
+                      nullptr, M, K, N, y, w, L, L.counters, true, di, stream, cb, cb + N, -1,
+                      nullptr, true);
     event_after(stream);
     events_call_done();
     return finish(rc, ws, stream);
@@ -601,6 +656,8 @@ int mlp_chain(int op, int norm, int act, const void *x, const void *gamma, const
     if (debug_mode() && cudaMemsetAsync(w, 0, 4, stream) != cudaSuccess) return NGR_ERR_CUDA;
     const bool decode = M <= kDecodeMaxM;
     const bool need_stats = norm != kNormNone || decode;
+    rc = zero_split_counters(L, w, stream);
+    if (rc != NGR_OK) return rc;
     events_reset();
     if (need_stats) {
         event_before(stream);
@@ -630,7 +687,7 @@ int mlp_chain(int op, int norm, int act, const void *x, const void *gamma, const
     if (rc != NGR_OK) return rc;
     event_before(stream);
     rc = launch_layer(kNormNone, kActNone, bf16, H, W2, b2, M, F, K, y, w, L, L.counters2, true, di,
-                      stream);
+                      stream, nullptr, nullptr, -1, nullptr, true);
     event_after(stream);
     events_call_done();
     return finish(rc, ws, stream);
@@ -667,6 +724,8 @@ int swiglu_chain(int op, int norm, const void *x, const void *gamma, const void 
     if (debug_mode() && cudaMemsetAsync(w, 0, 4, stream) != cudaSuccess) return NGR_ERR_CUDA;
     const bool decode = M <= kDecodeMaxM;
     const bool need_stats = norm != kNormNone || (down && decode);
+    rc = zero_split_counters(L, w, stream);
+    if (rc != NGR_OK) return rc;
     events_reset();
     if (need_stats) {
         event_before(stream);
@@ -689,7 +748,7 @@ int swiglu_chain(int op, int norm, const void *x, const void *gamma, const void 
     if (down) {
         event_before(stream);
         rc = launch_layer(kNormNone, kActNone, bf16, H, Wd, nullptr, M, F, K, y, w, L, L.counters2,
-                          true, di, stream);
+                          true, di, stream, nullptr, nullptr, -1, nullptr, true);
         event_after(stream);
     }
     events_call_done();
@@ -726,6 +785,8 @@ int linear_residual_norm(int norm, const void *x, const void *W, const void *bia
     void *H = h ? h : static_cast<void *>(w + L.h);
     if (debug_mode() && cudaMemsetAsync(w, 0, 4, stream) != cudaSuccess) return NGR_ERR_CUDA;
     const bool decode = M <= kDecodeMaxM;
+    rc = zero_split_counters(L, w, stream);
+    if (rc != NGR_OK) return rc;
     events_reset();
     if (decode) {
         // the decode product's split-K counters start from zero
@@ -739,7 +800,7 @@ int linear_residual_norm(int norm, const void *x, const void *W, const void *bia
     }
     event_before(stream);
     rc = launch_layer(kNormNone, kActNone, bf16, x, W, bias, M, K, N, H, w, L, L.counters, decode,
-                      di, stream, nullptr, nullptr, -1, residual);
+                      di, stream, nullptr, nullptr, -1, residual, true);
     event_after(stream);
     if (rc != NGR_OK) return rc;
     // The norm over each h row (a plain launch: it reads the product's output).
@@ -952,6 +1013,29 @@ int ngr_debug_bounded_wait(void *workspace, uint32_t timeout_us, ngr_stream_t st
     rc = launch_bounded_wait_probe(static_cast<int *>(workspace),
                                    static_cast<unsigned long long>(timeout_us) * 1000ull, stream);
     return rc == 0 ? NGR_OK : NGR_ERR_CUDA;
+}
+
+int ngr_tile_plan(int op, int64_t M, int64_t K, int64_t N, int *plan)
+{
+    if (!plan) return NGR_ERR_NULL;
+    if (op < NGR_OP_LAYERNORM_LINEAR || op > NGR_OP_LINEAR_RESIDUAL_NORM ||
+        op == NGR_OP_SWIGLU || M <= kDecodeMaxM || K <= 0 || N <= 0)
+        return NGR_ERR_ARG;
+    DevInfo di;
+    const int rc = current_device_info(&di);
+    if (rc != NGR_OK) return rc;
+    const bool chain = op == NGR_OP_FFN || op == NGR_OP_MLP || op == NGR_OP_MLP_SWIGLU;
+    const WsLayout L = ws_layout(op, M, K, N, false);
+    const int64_t n_out = chain ? K : (L.padded ? round8(N) : N);
+    const int64_t k_in = chain ? N : (L.padded ? round8(K) : K);
+    const GemmPlan p = plan_gemm(M, n_out, k_in, di.sms, true, L.split_cnt_bytes + L.split_part_bytes);
+    plan[0] = p.pair ? 1 : 0;
+    plan[1] = p.bn;
+    plan[2] = p.nsub;
+    plan[3] = p.splits > 1 ? p.splits : 1;
+    plan[4] = p.grid;
+    plan[5] = p.stages;
+    return NGR_OK;
 }
 
 int ngr_set_tile_config(int pair, int bn, int nsub)

@@ -99,14 +99,29 @@ static int max_pairs(int num_sms)
     return cache[dev];
 }
 
-// Relative cost of one N column of a 128-row slice on one SM: the CTA-pair
-// kernel streams half the W bytes per FLOP and runs closer to the tensor
-// peak (measured), so it is preferred unless its tiles quantize worse; its
-// two-sub-tile form streams fewer bytes still but does not overlap the
-// epilogue, which the larger per-tile term stands for.
-constexpr double kPairCostFactor = 0.8;
-constexpr double kWideCostFactor = 0.7;
+// Relative time of one N column of a k block per 128 rows on one SM, from
+// measured stage times on GB300: the CTA-pair kernel (256-row tiles) is the
+// unit; the single-CTA kernel streams twice the W bytes per FLOP; the
+// two-sub-tile pair form reuses each x stage for twice the columns but does
+// not overlap its epilogue (the larger per-tile term).  A K split adds the
+// partial write and the reduction of each chunk.
+constexpr double kSingleCostFactor = 1.25;
+constexpr double kPairCostFactor = 1.0;
+constexpr double kWideCostFactor = 0.8;
 constexpr int kWideTileOverhead = 32;
+constexpr int kSplitOverhead = 24;
+constexpr int kMinKbPerSplit = 16;
+
+size_t split_partial_bytes(int64_t num_tiles, int tw, int splits)
+{
+    return static_cast<size_t>(num_tiles) * 2 * 128 * static_cast<size_t>(tw) *
+           static_cast<size_t>(splits) * 4;
+}
+
+size_t split_counter_bytes(int64_t num_tiles, int tw)
+{
+    return static_cast<size_t>(num_tiles) * 2 * 4 * static_cast<size_t>((tw + 31) / 32) * 4;
+}
 
 // Stages of the two-sub-tile CTA-pair kernel for a sub-tile width.
 static int stages2w_for(int bn) { return bn == 256 ? 4 : 5; }
@@ -122,6 +137,8 @@ static int env_int(const char *name, int dflt)
 static std::atomic<int> g_pair{env_int("NGR_PAIR", -1) < 0 ? -1 : (env_int("NGR_PAIR", -1) ? 1 : 0)};
 static std::atomic<int> g_bn{env_int("NGR_BN", 0)};
 static std::atomic<int> g_nsub{env_int("NGR_NSUB", 0)};
+// NGR_MAX_SPLITS caps the K split (1 = never split).
+static const int g_max_splits = env_int("NGR_MAX_SPLITS", 2);
 
 int set_tile_config(int pair, int bn, int nsub)
 {
@@ -136,11 +153,13 @@ int set_tile_config(int pair, int bn, int nsub)
 }
 
 // The cheapest variant allowed by the restrictions (pair, bn, nsub as in
-// set_tile_config); none allowed gives a negative cost.
-static GemmPlan plan_with(int64_t M, int64_t N, int num_sms, int want_pair, int want_bn,
-                          int want_nsub, double *cost_out)
+// set_tile_config); none allowed gives a negative cost.  K splits (CTA pair
+// only) are weighed when the partials fit in max_split_bytes.
+static GemmPlan plan_with(int64_t M, int64_t N, int64_t K, int num_sms, int want_pair,
+                          int want_bn, int want_nsub, size_t max_split_bytes, double *cost_out)
 {
-    GemmPlan best{256, 4, 1, 0, false, kBM, 256, 1, 256};
+    GemmPlan best{256, 4, 1, 0, false, kBM, 256, 1, 256, false, 1};
+    const int64_t k_blocks = (K + kBK - 1) / kBK;
     double best_cost = -1.0;
     auto take = [&](double cost, const GemmPlan &p) {
         if (best_cost < 0 || cost < best_cost) {
@@ -154,8 +173,8 @@ static GemmPlan plan_with(int64_t M, int64_t N, int num_sms, int want_pair, int 
             const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + bn - 1) / bn);
             const int64_t grid = tiles < num_sms ? tiles : num_sms;
             const int64_t per_cta = (tiles + grid - 1) / grid;
-            take(static_cast<double>(per_cta) * (bn + 16),
-                 GemmPlan{bn, stages_for(bn), static_cast<int>(grid), 0, false, kBM, bn, 1, bn, false});
+            take(kSingleCostFactor * static_cast<double>(per_cta) * (bn + 16),
+                 GemmPlan{bn, stages_for(bn), static_cast<int>(grid), 0, false, kBM, bn, 1, bn, false, 1});
         }
     }
     if (M > kBM && want_pair != 0) {
@@ -165,12 +184,22 @@ static GemmPlan plan_with(int64_t M, int64_t N, int num_sms, int want_pair, int 
             if (want_nsub && nsub != want_nsub) return;
             const int tw = bn * nsub;
             const int64_t tiles = ((M + 2 * kBM - 1) / (2 * kBM)) * ((N + tw - 1) / tw);
-            const int64_t clusters = tiles < pairs ? tiles : pairs;
-            if (clusters < 1) return;
-            const int64_t per = (tiles + clusters - 1) / clusters;
-            take(factor * static_cast<double>(per) * (tw + overhead),
-                 GemmPlan{bn, stages, static_cast<int>(2 * clusters), 0, true, 2 * kBM, bn / 2,
-                          nsub, tw, false});
+            for (int splits = 1; splits <= 2 && splits <= g_max_splits; ++splits) {
+                if (splits > 1 && (tiles >= pairs || (k_blocks + 1) / 2 < kMinKbPerSplit ||
+                                   split_partial_bytes(tiles, tw, splits) +
+                                           split_counter_bytes(tiles, tw) >
+                                       max_split_bytes))
+                    continue;
+                const int64_t units = tiles * splits;
+                const int64_t clusters = units < pairs ? units : pairs;
+                if (clusters < 1) return;
+                const int64_t per = (units + clusters - 1) / clusters;
+                const double cols = static_cast<double>(tw) / splits + overhead +
+                                    (splits > 1 ? kSplitOverhead : 0);
+                take(factor * static_cast<double>(per) * cols,
+                     GemmPlan{bn, stages, static_cast<int>(2 * clusters), 0, true, 2 * kBM,
+                              bn / 2, nsub, tw, false, splits});
+            }
         };
         for (int bn : kTileWidths) consider(bn, 1, stages2_for(bn), kPairCostFactor, 16);
         for (int bn : kWideWidths)
@@ -180,13 +209,14 @@ static GemmPlan plan_with(int64_t M, int64_t N, int num_sms, int want_pair, int 
     return best;
 }
 
-GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, bool norm)
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, bool norm,
+                   size_t max_split_bytes)
 {
-    (void)K;
     (void)norm;
     double cost = -1.0;
-    GemmPlan best = plan_with(M, N, num_sms, g_pair.load(), g_bn.load(), g_nsub.load(), &cost);
-    if (cost < 0) best = plan_with(M, N, num_sms, -1, 0, 0, &cost);
+    GemmPlan best = plan_with(M, N, K, num_sms, g_pair.load(), g_bn.load(), g_nsub.load(),
+                              max_split_bytes, &cost);
+    if (cost < 0) best = plan_with(M, N, K, num_sms, -1, 0, 0, max_split_bytes, &cost);
     best.smem = best.pair ? gemm2_smem_bytes(best.bn, best.nsub)
                           : gemm_smem_bytes(best.bn, best.stages, true);
     return best;
@@ -197,7 +227,7 @@ GemmPlan plan_gemm_gated(int64_t M, int64_t N, int num_sms)
     // Gate and up sub-tiles of BN columns each: 256 x BN outputs per tile,
     // 2 BN accumulator columns.  The widest tile that does not add a wave.
     const int pairs = max_pairs(num_sms);
-    GemmPlan best{224, stages2w_for(224), 2, 0, true, 2 * kBM, 112, 2, 224, true};
+    GemmPlan best{224, stages2w_for(224), 2, 0, true, 2 * kBM, 112, 2, 224, true, 1};
     double best_cost = -1.0;
     for (int bn : kWideWidths) {
         if (g_bn.load() && bn != g_bn.load()) continue;
@@ -209,7 +239,7 @@ GemmPlan plan_gemm_gated(int64_t M, int64_t N, int num_sms)
         if (best_cost < 0 || cost < best_cost) {
             best_cost = cost;
             best = GemmPlan{bn, stages2w_for(bn), static_cast<int>(2 * clusters), 0, true,
-                            2 * kBM, bn / 2, 2, bn, true};
+                            2 * kBM, bn / 2, 2, bn, true, 1};
         }
     }
     best.smem = gemm2_smem_bytes(best.bn, 2);

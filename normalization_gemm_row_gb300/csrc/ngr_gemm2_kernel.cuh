@@ -88,9 +88,9 @@ struct Gemm2Smem {
 // stage (only read), normalizes them in FP32, packs them to 16-bit pairs
 // and stores them with tcgen05.st.
 template <int NORM, bool BF16, int STAGES, int KA, int SLOTS, int HALVES, typename M0Fn,
-          typename ArriveFn>
+          typename KbFn, typename ArriveFn>
 __device__ __forceinline__ void transform_role_tmem(
-    int t, int tile0, int tile_step, int num_tiles, int k_blocks, int M, const float2 *stats,
+    int t, int tile0, int tile_step, int num_tiles, KbFn kb_count, int M, const float2 *stats,
     const uint8_t *sA, const float *sG, uint64_t *full, uint64_t *a_free, uint32_t tmem_base,
     uint32_t a_col0, const WaitCtx &wc, M0Fn m0_of, ArriveFn arrive)
 {
@@ -114,6 +114,7 @@ __device__ __forceinline__ void transform_role_tmem(
         float2 st = make_float2(0.f, 0.f);
         if (row < M) st = stats[row];
         const float2 so = make_float2(st.y, -st.x * st.y);
+        const int k_blocks = kb_count(tile);
         for (int kb = 0; kb < k_blocks; ++kb, ++it) {
             if (HALVES > 1 || it % kTransformGroups == g) {
                 if (!mbar_wait_warp(&full[stage], phase, wc)) return;
@@ -261,6 +262,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int m_tiles = args.m_tiles;   // 256-row pair tiles
     const int k_blocks = args.k_blocks;
     const int num_tiles = args.num_tiles;
+    // Work units: (tile, K range) pairs; without a split a unit is a tile.
+    const int n_splits = GATED ? 1 : max(1, args.k_splits);
+    const int num_units = num_tiles * n_splits;
+    const int kb_per_split = n_splits > 1 ? args.kb_per_split : k_blocks;
+    auto unit_tile = [&](int u) { return u / n_splits; };
+    auto unit_kb0 = [&](int u) { return (u % n_splits) * kb_per_split; };
+    auto unit_kb1 = [&](int u) { return min(k_blocks, unit_kb0(u) + kb_per_split); };
     const int cluster = blockIdx.x >> 1;
     const int n_clusters = gridDim.x >> 1;
     // Leader-side addresses of ready[] and acc_empty[] (shared::cluster).
@@ -278,7 +286,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint32_t phase = 0;
             long long fills = 0;
             bool ok = true;
-            for (int tile = cluster; ok && tile < num_tiles; tile += n_clusters) {
+            for (int u = cluster; ok && u < num_units; u += n_clusters) {
+                const int tile = unit_tile(u);
                 const int m0 = (tile % m_tiles) * 2 * kBM + static_cast<int>(rank) * kBM;
                 const int nt0 = (tile / m_tiles) * kOutW;
                 const int n0 = nt0 + static_cast<int>(rank) * (BN / 2);
@@ -289,7 +298,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 auto wmap = [&](int j) { return (GATED && j == 1) ? &args.map_b2 : &args.map_b; };
                 auto wrow = [&](int j) { return GATED ? n0 : n0 + j * BN; };
                 const uint32_t tx = stage_tx(n_sub);
-                for (int kb = 0; kb < k_blocks; ++kb) {
+                for (int kb = unit_kb0(u), kb_end = unit_kb1(u); kb < kb_end; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, wc)) { ok = false; break; }
                     const int kc = kb * kBK;
                     uint8_t *sb = sB + stage * L::kB;
@@ -336,12 +345,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint32_t acc_phase = 0;
             int it = 0;
             bool ok = true;
-            for (int tile = cluster; ok && tile < num_tiles; tile += n_clusters) {
+            for (int u = cluster; ok && u < num_units; u += n_clusters) {
+                const int tile = unit_tile(u);
+                const int kb0 = unit_kb0(u);
                 if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, wc)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kTW);
                 const int n_sub = GATED ? 2 : min(NSUB, (args.N - (tile / m_tiles) * kTW + BN - 1) / BN);
-                for (int kb = 0; kb < k_blocks; ++kb) {
+                for (int kb = kb0, kb_end = unit_kb1(u); kb < kb_end; ++kb) {
                     if (!mbar_wait(kNorm ? &ready[stage] : &full[stage], phase, wc)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t b_addr = smem_u32(sB + stage * L::kB);
@@ -360,7 +371,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                         umma_f16_ts_pair(d_tmem + static_cast<uint32_t>(j * BN),
                                                          a_tmem + static_cast<uint32_t>(k * (kUmmaK / 2)),
                                                          sdesc_kmajor_sw128(b_addr + j * L::kBSub + kk * 32),
-                                                         kIdesc, (kb | kk) != 0 ? 1u : 0u);
+                                                         kIdesc, (kb != kb0 || kk != 0) ? 1u : 0u);
                                 }
                             }
                             umma_commit_pair(&a_free[slot], 0x3);
@@ -375,7 +386,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                 if (j < n_sub)
                                     umma_f16_ss_pair(d_tmem + static_cast<uint32_t>(j * BN), a_desc,
                                                      sdesc_kmajor_sw128(b_addr + j * L::kBSub + k * 32),
-                                                     kIdesc, (kb | k) != 0 ? 1u : 0u);
+                                                     kIdesc, (kb != kb0 || k != 0) ? 1u : 0u);
                             }
                         }
                     }
@@ -397,15 +408,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if constexpr (kATmem) {
                 // ------------------------------------------ transform (A -> TMEM)
                 transform_role_tmem<NORM, BF16, STAGES, L::kA, kASlots, kHalvesA>(
-                    t, cluster, n_clusters, num_tiles, k_blocks, args.M, args.stats, sA, sG, full,
-                    a_free, tmem_base, kACol0, wc,
-                    [&](int tile) { return (tile % m_tiles) * 2 * kBM + static_cast<int>(rank) * kBM; },
+                    t, cluster, n_clusters, num_units, [&](int u) { return unit_kb1(u) - unit_kb0(u); },
+                    args.M, args.stats, sA, sG, full, a_free, tmem_base, kACol0, wc,
+                    [&](int u) { return (unit_tile(u) % m_tiles) * 2 * kBM + static_cast<int>(rank) * kBM; },
                     [&](int st) { mbar_arrive_cluster(ready_leader + 8u * static_cast<uint32_t>(st)); });
             } else if constexpr (kNorm) {
                 // ----------------------------------------- transform (A in place)
                 transform_role<NORM, BF16, STAGES, L::kA>(
-                    t, cluster, n_clusters, num_tiles, k_blocks, args.M, args.stats, sA, sG, full, wc,
-                    [&](int tile) { return (tile % m_tiles) * 2 * kBM + static_cast<int>(rank) * kBM; },
+                    t, cluster, n_clusters, num_units, [&](int u) { return unit_kb1(u) - unit_kb0(u); },
+                    args.M, args.stats, sA, sG, full, wc,
+                    [&](int u) { return (unit_tile(u) % m_tiles) * 2 * kBM + static_cast<int>(rank) * kBM; },
                     [&](int st) { mbar_arrive_cluster(ready_leader + 8u * static_cast<uint32_t>(st)); });
             }
         }
@@ -417,11 +429,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint32_t acc_phase = 0;
             const int N = args.N;
             if constexpr (is_fold(NORM)) pdl_wait();  // row statistics from the previous grid
-            for (int tile = cluster; tile < num_tiles; tile += n_clusters) {
+            for (int u = cluster; u < num_units; u += n_clusters) {
+                const int tile = unit_tile(u);
+                const int split = u % n_splits;
                 const int cur = acc;
                 const uint32_t cur_phase = acc_phase;
                 if (++acc == kAccBufs) { acc = 0; acc_phase ^= 1u; }
-                const bool helped = kHelpAlways || (kHelpLast && tile + n_clusters >= num_tiles);
+                const bool helped = kHelpAlways || (kHelpLast && u + n_clusters >= num_units);
                 if (!epi_warp && !helped) continue;
                 const int step = (helped ? 3 : 1) * 32;
                 const int nt0 = (tile / m_tiles) * kOutW;
@@ -456,6 +470,64 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         for (int j = 0; j < 32; ++j)
                             v[j] = silu_f(__uint_as_float(rg[j])) * __uint_as_float(ru[j]);
                         store_row32<BF16>(v, row, nt0 + c, args.y, args.M, N);
+                    }
+                } else if (n_splits > 1) {
+                    // K split: (1) this unit's FP32 partials of the warp's
+                    // 32 x 32 chunks; (2) one fence, then one counter per
+                    // chunk (lane i takes the i-th chunk); (3) the chunks
+                    // this unit arrived last at are summed over the K
+                    // ranges in range order and finished.
+                    const size_t blk0 = ((static_cast<size_t>(tile) * 2 + rank) * 4 + q) *
+                                        static_cast<size_t>(kTW / 32);
+                    const size_t part_stride = static_cast<size_t>(n_splits) * 1024;
+                    int nch = 0;
+#pragma unroll 1
+                    for (int c = e * 32; c < ncols; c += step, ++nch) {
+                        uint32_t r[32];
+                        tmem_ld32(t_base + static_cast<uint32_t>(c), r);
+                        tmem_ld_wait();
+                        // column-major within the chunk: each store of the
+                        // warp writes one contiguous 128-byte line
+                        float *mine = args.partials + (blk0 + (c >> 5)) * part_stride + split * 1024 + lane;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) __stcg(mine + j * 32, __uint_as_float(r[j]));
+                    }
+                    __threadfence();
+                    __syncwarp();
+                    int last = 0;
+                    if (lane < nch)
+                        last = atomicAdd(&args.split_counters[blk0 + ((e * 32 + lane * step) >> 5)], 1) ==
+                               n_splits - 1;
+                    const unsigned last_mask = __ballot_sync(0xffffffffu, last);
+                    if (last_mask != 0u) {
+                        __threadfence();
+#pragma unroll 1
+                        for (int i = 0; i < nch; ++i) {
+                            if (((last_mask >> i) & 1u) == 0u) continue;
+                            const int c = e * 32 + i * step;
+                            uint32_t r[32];
+                            tmem_ld32(t_base + static_cast<uint32_t>(c), r);
+                            tmem_ld_wait();
+                            const float *part = args.partials + (blk0 + (c >> 5)) * part_stride + lane;
+                            float v[32];
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+                            for (int sp = 0; sp < n_splits; ++sp) {
+                                if (sp == split) {
+#pragma unroll
+                                    for (int j = 0; j < 32; ++j) v[j] += __uint_as_float(r[j]);
+                                } else {
+                                    const float *o = part + sp * 1024;
+#pragma unroll
+                                    for (int j = 0; j < 32; ++j) v[j] += __ldcg(o + j * 32);
+                                }
+                            }
+                            epilogue_store32<NORM, BF16>(v, row, nt0 + c, args, so);
+                        }
+                        __syncwarp();
+                        // ready for the next call (every unit of these chunks has arrived)
+                        if (lane < nch && ((last_mask >> lane) & 1u))
+                            args.split_counters[blk0 + ((e * 32 + lane * step) >> 5)] = 0;
                     }
                 } else {
                     // The load of the next chunk is in flight while this one

@@ -97,26 +97,40 @@ __device__ __forceinline__ void apply_act32(int act, float (&v)[32])
     }
 }
 
+// A 32-byte store (one full L2 sector) of 8 words.
+__device__ __forceinline__ void st_global_v8(void *p, const uint32_t (&w)[8])
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]),
+                 "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
 // Round 32 values of one output row to the 16-bit type and store the
-// columns [n0, n0 + 32) that lie inside [0, N) (N % 8 == 0) with 16-byte
-// stores; rows at or past M are skipped.
+// columns [n0, n0 + 32) that lie inside [0, N) (N % 8 == 0); rows at or past
+// M are skipped.  Each lane writes its own row, so whole 32-byte sectors
+// are stored where y and its row pitch allow it (half-sector writes from
+// every SM at once are what makes a tile's output slow to drain), else
+// 16-byte pieces.
 template <bool BF16>
 __device__ __forceinline__ void store_row32(const float (&v)[32], int row, int n0, void *y, int M,
                                             int N)
 {
     if (row >= M) return;
     uint16_t *yrow = static_cast<uint16_t *>(y) + static_cast<int64_t>(row) * N;
+    uint32_t o[16];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        if (n0 + 8 * j < N) {
-            uint4 o;
-            o.x = from_float2<BF16>(v[8 * j + 0], v[8 * j + 1]);
-            o.y = from_float2<BF16>(v[8 * j + 2], v[8 * j + 3]);
-            o.z = from_float2<BF16>(v[8 * j + 4], v[8 * j + 5]);
-            o.w = from_float2<BF16>(v[8 * j + 6], v[8 * j + 7]);
-            *reinterpret_cast<uint4 *>(yrow + n0 + 8 * j) = o;
-        }
+    for (int j = 0; j < 16; ++j) o[j] = from_float2<BF16>(v[2 * j], v[2 * j + 1]);
+    const bool sectors = ((reinterpret_cast<uintptr_t>(y) | static_cast<uintptr_t>(N) * 2u) & 31u) == 0;
+    if (sectors && n0 + 32 <= N) {
+        st_global_v8(yrow + n0, *reinterpret_cast<const uint32_t(*)[8]>(&o[0]));
+        st_global_v8(yrow + n0 + 16, *reinterpret_cast<const uint32_t(*)[8]>(&o[8]));
+        return;
     }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        if (n0 + 8 * j < N)
+            *reinterpret_cast<uint4 *>(yrow + n0 + 8 * j) =
+                make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
 }
 
 // Normalize + affine 8 consecutive elements held as 4 packed 16-bit pairs.
@@ -272,10 +286,11 @@ __device__ __forceinline__ float2 fold_row_scale(const GemmArgs &args, int row)
 // (conflict free under the swizzle) and gamma/beta of the chunk are read
 // once per stage.  After its stores each thread fences them for the async
 // proxy, and one lane per warp calls arrive(stage).
-// m0_of(tile) gives the tile's first x row in this CTA.
-template <int NORM, bool BF16, int STAGES, int KA, typename M0Fn, typename ArriveFn>
+// m0_of(unit) gives the unit's first x row in this CTA and kb_count(unit)
+// the number of k blocks the unit covers (all of them unless K is split).
+template <int NORM, bool BF16, int STAGES, int KA, typename M0Fn, typename KbFn, typename ArriveFn>
 __device__ __forceinline__ void transform_role(int t, int tile0, int tile_step, int num_tiles,
-                                               int k_blocks, int M, const float2 *stats,
+                                               KbFn kb_count, int M, const float2 *stats,
                                                uint8_t *sA, const float *sG, uint64_t *full,
                                                const WaitCtx &wc, M0Fn m0_of, ArriveFn arrive)
 {
@@ -306,6 +321,7 @@ __device__ __forceinline__ void transform_role(int t, int tile0, int tile_step, 
             if (row < M) st = stats[row];
             so[i] = make_float2(st.y, -st.x * st.y);
         }
+        const int k_blocks = kb_count(tile);
         for (int kb = 0; kb < k_blocks; ++kb, ++it) {
             if (it % kTransformGroups == g) {
                 if (!mbar_wait_warp(&full[stage], phase, wc)) return;
@@ -518,8 +534,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if constexpr (kNorm) {
             // ---------------------------------------------------- transform
             transform_role<NORM, BF16, STAGES, L::kA>(
-                threadIdx.x - kTransformWarp0 * 32, blockIdx.x, gridDim.x, num_tiles, k_blocks,
-                args.M, args.stats, sA, sG, full, wc,
+                threadIdx.x - kTransformWarp0 * 32, blockIdx.x, gridDim.x, num_tiles,
+                [&](int) { return k_blocks; }, args.M, args.stats, sA, sG, full, wc,
                 [&](int tile) { return (tile % m_tiles) * kBM; },
                 [&](int st) { mbar_arrive(&ready[st]); });
         }

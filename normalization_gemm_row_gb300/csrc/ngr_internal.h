@@ -61,6 +61,13 @@ struct alignas(128) GemmArgs {
     int act;                // kAct*: activation after the bias (not used when gated)
     int M, N, K;
     int m_tiles, n_tiles, k_blocks, num_tiles;
+    // CTA-pair kernel: K split into k_splits ranges of kb_per_split k blocks
+    // (1 = no split).  Each (tile, range) unit writes FP32 partials of its
+    // 32 x 32 accumulator chunks; the last of a chunk's units (its counter)
+    // sums them in range order and finishes the chunk.
+    int k_splits, kb_per_split;
+    float *partials;        // [tiles][2][4][chunks][k_splits][32 cols][32 rows]
+    int *split_counters;    // [tiles][2][4][chunks], zero at kernel start
     unsigned long long timeout_ns;
 };
 
@@ -100,7 +107,12 @@ struct GemmPlan {
     int nsub;        // N sub-tiles of BN columns per output tile (CTA pair: 1 or 2)
     int tw;          // output tile width in N: bn * nsub, or bn when gated
     bool gated;      // SwiGLU: sub-tile 0 multiplies the gate weight, 1 the up weight
+    int splits;      // K ranges per output tile (CTA pair only; 1 = none)
 };
+
+// Bytes of FP32 partials and of counters a split plan needs.
+size_t split_partial_bytes(int64_t num_tiles, int tw, int splits);
+size_t split_counter_bytes(int64_t num_tiles, int tw);
 
 // Record why a CUDA call failed (thread-local; read back through
 // ngr_last_error).  Returns -7 (NGR_ERR_CUDA) for use in return statements.
@@ -124,7 +136,9 @@ int launch_unpad_rows(const void *src, int64_t rows, int64_t cols, int64_t src_p
 
 int launch_gemm(int norm, bool bf16, const GemmPlan &plan, const GemmArgs &args, bool pdl,
                 cudaStream_t stream);
-GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, bool norm);
+// max_split_bytes: room for split-K partials and counters (0 = never split).
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, bool norm,
+                   size_t max_split_bytes = 0);
 // The SwiGLU variant: CTA-pair tiles of 256 x BN outputs, two BN-column
 // accumulators (gate, up) per tile.
 GemmPlan plan_gemm_gated(int64_t M, int64_t N, int num_sms);

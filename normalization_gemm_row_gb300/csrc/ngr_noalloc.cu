@@ -170,6 +170,8 @@ extern "C" int ngr_fused_layernorm_linear_noalloc(const void *x, const void *gam
     a.num_tiles = a.m_tiles * a.n_tiles;
     a.timeout_ns = 2000ull * 1000000ull;
     a.act = kActNone;
+    a.k_splits = 1;   // no K split: the scratch holds no partials
+    a.kb_per_split = a.k_blocks;
     rc = launch_gemm(kNormLayer, bf16, plan, a, true, stream);
     if (rc != NGR_OK) return rc;
     return cudaGetLastError() == cudaSuccess ? NGR_OK : NGR_ERR_CUDA;

@@ -90,6 +90,34 @@ def test_other_entry_points_still_need_alignment(lib):
                                           A16 * 16, big, None) == -3
 
 
+def test_split_k_reserve(lib):
+    """Room for a two-way K split only where the output has few 256 x 448
+    tiles: the 1024 x 8192 output (76 tiles) gets none, 512 x 8192 (38)
+    does; it is the largest two-way plan over the pair tile widths."""
+    wb = B.ngr_workspace_bytes
+    a256 = lambda v: (v + 255) // 256 * 256
+    assert wb(B.OP_LINEAR_SILU, 1024, 8192, 8192) == 256
+    got = wb(B.OP_LINEAR_SILU, 512, 8192, 8192)
+    mt = 2
+    cnt = max(mt * -(-8192 // tw) * 2 * 4 * (tw // 32) * 4 for tw in (128, 192, 224, 256, 384, 448, 512))
+    part = max(mt * -(-8192 // tw) * 2 * 128 * tw * 2 * 4 for tw in (128, 192, 224, 256, 384, 448, 512))
+    assert got == 256 + a256(cnt) + a256(part)
+    # none at decode sizes or at M <= 128 (no CTA-pair kernel there)
+    assert wb(B.OP_LINEAR_SILU, 16, 8192, 8192) == wb(B.OP_LINEAR_SILU, 16, 8192, 8192, 0)
+    assert wb(B.OP_LINEAR_SILU, 128, 8192, 8192) == 256
+    # the chains reserve for their second product (K output columns)
+    assert wb(B.OP_FFN, 512, 4096, 11008) > 256 and wb(B.OP_FFN, 512, 14336, 11008) == 256
+
+
+def test_tile_plan_rejects(lib):
+    plan = (ctypes.c_int * 6)()
+    p = ctypes.cast(plan, ctypes.c_void_p)
+    assert B.ngr_tile_plan(9, 512, 64, 64, p) == -9
+    assert B.ngr_tile_plan(B.OP_SWIGLU, 512, 64, 64, p) == -9
+    assert B.ngr_tile_plan(B.OP_LINEAR_SILU, 16, 64, 64, p) == -9     # decode kernel
+    assert B.ngr_tile_plan(B.OP_LINEAR_SILU, 512, 64, 64, None) == -1
+
+
 def test_post_norm_workspace_and_rejections(lib):
     wb = B.ngr_workspace_bytes
     w0 = wb(B.OP_LINEAR_RESIDUAL_NORM, 1024, 8192, 8192, 0)
@@ -125,7 +153,8 @@ def test_workspace_bytes_new_ops(lib):
     assert wb(B.OP_SWIGLU, 4, 4096, 11008, 1) == wb(B.OP_SWIGLU, 4, 4096, 11008)
     # ... but its MLP form keeps the down projection's split-K regions at decode sizes
     assert wb(B.OP_MLP_SWIGLU, 4, 4096, 11008) > wb(B.OP_SWIGLU, 4, 4096, 11008)
-    assert wb(B.OP_MLP_SWIGLU, 512, 4096, 11008) == wb(B.OP_SWIGLU, 512, 4096, 11008)
+    # (its down product, 512 x 4096, has few output tiles: room for a K split)
+    assert wb(B.OP_MLP_SWIGLU, 512, 4096, 11008) > wb(B.OP_SWIGLU, 512, 4096, 11008)
     assert (wb(B.OP_MLP_SWIGLU, 512, 4096, 11008, 1) - wb(B.OP_MLP_SWIGLU, 512, 4096, 11008)
             == 512 * 11008 * 2)
 

@@ -108,3 +108,82 @@ def test_ffn_f16(tile_config):
     y = ngr.ffn_linear_silu_linear(g["x"], g["W1"], g["W2"])
     torch.cuda.synchronize()
     check(y, oracle.ffn(d["x"], d["W1"], d["W2"]), f"FFN {tile_config}")
+
+
+# --------------------------------------------------------------- K splits
+SPLIT_CONFIGS = [(1, 224, 1), (1, 256, 1), (1, 224, 2), (1, 192, 2), (1, 256, 2)]
+
+
+@pytest.fixture(params=SPLIT_CONFIGS, ids=[f"pair-bn{bn}x{ns}" for _, bn, ns in SPLIT_CONFIGS])
+def split_config(request):
+    pair, bn, nsub = request.param
+    B.set_tile_config(pair, bn, nsub)
+    yield request.param
+    B.set_tile_config(-1, 0, 0)
+
+
+SM, SK, SN = 300, 4096, 1000   # few output tiles, 64 k blocks: the planner splits K in two
+
+
+def test_split_k_is_planned(split_config):
+    plan = B.tile_plan(B.OP_LAYERNORM_LINEAR, SM, SK, SN)
+    assert plan["pair"] == 1 and plan["splits"] == 2, plan
+    assert plan["bn"] == split_config[1] and plan["nsub"] == split_config[2], plan
+
+
+def test_split_k_layernorm_and_silu(split_config):
+    d = inputs.case("layernorm_linear", SM, SK, SN, torch.bfloat16, True, 1e-5, seed=21,
+                    x_mean=2.0)
+    g = to_dev(d)
+    y = ngr.fused_layernorm_linear(g["x"], g["gamma"], g["beta"], g["W"], g["bias"], 1e-5)
+    torch.cuda.synchronize()
+    check(y, oracle.layernorm_linear(d["x"], d["gamma"], d["beta"], d["W"], d["bias"], 1e-5),
+          f"split LN {split_config}")
+    d = inputs.case("linear_silu", SM, SK, SN, torch.float16, True, 0.0, seed=22)
+    g = to_dev(d)
+    y = ngr.fused_linear_silu(g["x"], g["W"], g["bias"])
+    torch.cuda.synchronize()
+    check(y, oracle.linear_silu(d["x"], d["W"], d["bias"]), f"split SiLU {split_config}")
+
+
+def test_split_k_folded_and_post_norm(split_config):
+    d = inputs.case("rmsnorm_linear", SM, SK, SN, torch.float16, True, 1e-5, seed=23)
+    g = to_dev(d)
+    Wf, cb = B.fold_prepare(oracle.NORM_RMS, g["gamma"], None, g["W"], g["bias"])
+    y = B.fused_norm_linear_folded(oracle.NORM_RMS, g["x"], Wf, cb, 1e-5)
+    torch.cuda.synchronize()
+    check(y, oracle.rmsnorm_linear(d["x"], d["gamma"], d["W"], d["bias"], 1e-5),
+          f"split folded RMS {split_config}")
+    gen = torch.Generator().manual_seed(24)
+    res = torch.randn((SM, SN), generator=gen).to(torch.float16)
+    gam = (1.0 + 0.1 * torch.randn((SN,), generator=gen)).to(torch.float16)
+    h, y = ngr.fused_linear_residual_norm(g["x"], g["W"], gam.cuda(), norm=B.NORM_RMS,
+                                          bias=g["bias"], residual=res.cuda(), eps=1e-5)
+    torch.cuda.synchronize()
+    href, yref = oracle.linear_residual_norm(oracle.NORM_RMS, d["x"], d["W"], d["bias"], res, gam,
+                                             None, 1e-5)
+    check(h, href, f"split post-norm h {split_config}")
+    check(y, yref, f"split post-norm y {split_config}")
+
+
+def test_split_k_is_deterministic():
+    d = inputs.case("layernorm_linear", SM, SK, SN, torch.bfloat16, True, 1e-5, seed=25)
+    g = to_dev(d)
+    ys = [ngr.fused_layernorm_linear(g["x"], g["gamma"], g["beta"], g["W"], g["bias"], 1e-5)
+          for _ in range(3)]
+    torch.cuda.synchronize()
+    assert torch.equal(ys[0], ys[1]) and torch.equal(ys[0], ys[2])
+
+
+def test_split_k_default_plan_llama_output_projection():
+    """512 x 8192 x 8192 (38 wide tiles for 76 pairs): the default plan
+    splits K; sampled rows against the oracle."""
+    plan = B.tile_plan(B.OP_LINEAR_SILU, 512, 8192, 8192)
+    assert plan["splits"] == 2, plan
+    d = inputs.case("linear_silu", 512, 8192, 8192, torch.bfloat16, True, 0.0, seed=26)
+    g = to_dev(d)
+    y = ngr.fused_linear_silu(g["x"], g["W"], g["bias"])
+    torch.cuda.synchronize()
+    rows = inputs.sample_rows(512, 12, seed=3, always=(0, 255, 256, 511)).tolist()
+    got = y[torch.as_tensor(rows, device="cuda")]
+    check(got, oracle.linear_silu(d["x"], d["W"], d["bias"], rows), "split default 512x8192")
