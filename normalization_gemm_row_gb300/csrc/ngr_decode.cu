@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             for (long long u = u_begin; u < u_end; ++u) {
                 const int tile = static_cast<int>(u / KB);
                 const int kc = static_cast<int>(u % KB) * kBK;
-                if (!mbar_wait(&empty[stage], phase ^ 1u, wc)) break;
+                if (!mbar_wait_spin(&empty[stage], phase ^ 1u, wc)) break;
                 mbar_arrive_expect_tx(&full[stage], kTx);
                 tma_load_2d(sW + stage * L::kW, &args.map_w, &full[stage], kc, tile * 128, pol_w);
                 tma_load_2d(sX + stage * L::kX, &args.map_x, &full[stage], kc, 0, pol_x);
@@ -153,12 +153,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             while (ok && u < u_end) {
                 const long long tile = u / KB;
                 const long long seg_end = (tile + 1) * KB < u_end ? (tile + 1) * KB : u_end;
-                if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, wc)) break;
+                if (!mbar_wait_spin(&acc_empty[acc], acc_phase ^ 1u, wc)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * MN);
                 bool first = true;
                 for (; u < seg_end; ++u) {
-                    if (!mbar_wait(&full[stage], phase, wc)) { ok = false; break; }
+                    if (!mbar_wait_spin(&full[stage], phase, wc)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(sW + stage * L::kW);
                     const uint32_t b_addr = smem_u32(sX + stage * L::kX);

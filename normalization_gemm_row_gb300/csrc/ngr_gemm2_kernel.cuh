@@ -57,6 +57,13 @@ namespace ngr {
 #define NGR_PAIR_A_TMEM_WIDE 0
 #endif
 constexpr int kMaxASlots = 8;
+// Column parts per stage of the in-place transform (1, 2 or 4): the MMAs of
+// a part's K steps are issued once that part of both CTAs' stages is
+// normalized.
+#ifndef NGR_TRANSFORM_PARTS
+#define NGR_TRANSFORM_PARTS 2
+#endif
+constexpr int kMaxParts = 4;
 
 template <int BN, int STAGES, int NSUB>
 struct Gemm2Smem {
@@ -68,7 +75,7 @@ struct Gemm2Smem {
     static constexpr int off_b = off_a + STAGES * kA;
     static constexpr int off_g = off_b + STAGES * kB;
     static constexpr int off_bar = off_g + STAGES * kGB;
-    static constexpr int n_bars = 3 * STAGES + 5 + kMaxASlots;
+    static constexpr int n_bars = (2 + kMaxParts) * STAGES + 5 + kMaxASlots;
     static constexpr int off_tmem = off_bar + n_bars * 8;
     static constexpr int bytes = off_tmem + 16;
     static constexpr int alloc = bytes + 1024;
@@ -197,6 +204,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ready[s] arrivals: one per warp of each transform group that works on
     // the stage, in each CTA (used with a norm only).
     constexpr uint32_t kReadyCount = 2 * kGroupWarps * (kATmem ? kHalvesA : 1);
+    constexpr int kParts = (kNorm && !kATmem) ? NGR_TRANSFORM_PARTS : 1;
+    static_assert(kParts >= 1 && kParts <= kMaxParts && (kBK / kUmmaK) % kParts == 0,
+                  "whole K steps per transform part");
     static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "UMMA N for M = 256");
     static_assert((BN / 2) % 8 == 0, "B half tile rows (1024-byte swizzle atoms)");
     static_assert(NSUB >= 1 && kAccBufs * kTW <= 512, "accumulators fit in tensor memory");
@@ -214,11 +224,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::off_bar);
     uint64_t *full = bars;
     uint64_t *empty = bars + STAGES;
-    uint64_t *ready = bars + 2 * STAGES;
-    uint64_t *acc_full = bars + 3 * STAGES;
-    uint64_t *acc_empty = bars + 3 * STAGES + 2;
-    uint64_t *drain = bars + 3 * STAGES + 4;
-    uint64_t *a_free = bars + 3 * STAGES + 5;   // [kMaxASlots] A slot read by the MMAs (commit, multicast)
+    uint64_t *ready = bars + 2 * STAGES;        // [STAGES * kParts] part of both stages normalized
+    uint64_t *acc_full = bars + (2 + kMaxParts) * STAGES;
+    uint64_t *acc_empty = acc_full + 2;
+    uint64_t *drain = acc_full + 4;
+    uint64_t *a_free = acc_full + 5;            // [kMaxASlots] A slot read by the MMAs (commit, multicast)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::off_tmem);
 
     const int warp = threadIdx.x >> 5;
@@ -238,7 +248,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
-            mbar_init(&ready[s], kReadyCount);
+            for (int p = 0; p < kParts; ++p) mbar_init(&ready[s * kParts + p], kReadyCount);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&acc_full[a], 1);
@@ -299,7 +309,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 auto wrow = [&](int j) { return GATED ? n0 : n0 + j * BN; };
                 const uint32_t tx = stage_tx(n_sub);
                 for (int kb = unit_kb0(u), kb_end = unit_kb1(u); kb < kb_end; ++kb) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, wc)) { ok = false; break; }
+                    if (!mbar_wait_spin(&empty[stage], phase ^ 1u, wc)) { ok = false; break; }
                     const int kc = kb * kBK;
                     uint8_t *sb = sB + stage * L::kB;
                     if constexpr (kNorm) {
@@ -348,12 +358,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (int u = cluster; ok && u < num_units; u += n_clusters) {
                 const int tile = unit_tile(u);
                 const int kb0 = unit_kb0(u);
-                if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, wc)) break;
+                if (!mbar_wait_spin(&acc_empty[acc], acc_phase ^ 1u, wc)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kTW);
                 const int n_sub = GATED ? 2 : min(NSUB, (args.N - (tile / m_tiles) * kTW + BN - 1) / BN);
                 for (int kb = kb0, kb_end = unit_kb1(u); kb < kb_end; ++kb) {
-                    if (!mbar_wait(kNorm ? &ready[stage] : &full[stage], phase, wc)) { ok = false; break; }
+                    if (!mbar_wait_spin(kNorm ? &ready[stage * kParts] : &full[stage], phase, wc)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t b_addr = smem_u32(sB + stage * L::kB);
                     if constexpr (kATmem) {
@@ -378,8 +388,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         }
                     } else {
                         const uint32_t a_addr = smem_u32(sA + stage * L::kA);
+                        constexpr int kStepsPerPart = (kBK / kUmmaK) / kParts;
 #pragma unroll
                         for (int k = 0; k < kBK / kUmmaK; ++k) {
+                            if (kParts > 1 && k > 0 && k % kStepsPerPart == 0) {
+                                // The next column part of both CTAs' stages.
+                                if (!mbar_wait_spin(&ready[stage * kParts + k / kStepsPerPart], phase, wc)) {
+                                    ok = false;
+                                    break;
+                                }
+                                tc_fence_after();
+                            }
                             const uint64_t a_desc = sdesc_kmajor_sw128(a_addr + k * 32);
 #pragma unroll
                             for (int j = 0; j < NSUB; ++j) {
@@ -390,6 +409,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             }
                         }
                     }
+                    if (!ok) break;
                     umma_commit_pair(&empty[stage], 0x3);
                     ++it;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -414,7 +434,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     [&](int st) { mbar_arrive_cluster(ready_leader + 8u * static_cast<uint32_t>(st)); });
             } else if constexpr (kNorm) {
                 // ----------------------------------------- transform (A in place)
-                transform_role<NORM, BF16, STAGES, L::kA>(
+                transform_role<NORM, BF16, STAGES, L::kA, kParts>(
                     t, cluster, n_clusters, num_units, [&](int u) { return unit_kb1(u) - unit_kb0(u); },
                     args.M, args.stats, sA, sG, full, wc,
                     [&](int u) { return (unit_tile(u) % m_tiles) * 2 * kBM + static_cast<int>(rank) * kBM; },

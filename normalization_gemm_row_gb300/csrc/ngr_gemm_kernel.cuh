@@ -281,31 +281,42 @@ __device__ __forceinline__ float2 fold_row_scale(const GemmArgs &args, int row)
 // The transform role, shared by the tile kernels.  Transform thread t
 // (0 <= t < kTransformThreads) belongs to group t / kGroupThreads; group g
 // normalizes the stages of the k blocks with running index % groups == g.
-// Within a group, thread u owns 16-byte chunk u % 8 (8 columns) of rows
-// u / 8 + (kGroupThreads / 8) i: a quarter-warp covers one 128-byte row
-// (conflict free under the swizzle) and gamma/beta of the chunk are read
-// once per stage.  After its stores each thread fences them for the async
-// proxy, and one lane per warp calls arrive(stage).
+// A stage is normalized in PARTS column parts of 64 / PARTS columns each,
+// and after each part one lane per warp calls arrive(stage * PARTS + part),
+// so that the tensor core can start on the first columns of a stage while
+// the rest are still being normalized.  Within a part, thread u owns 16-byte
+// chunk u % CP (CP = 8 / PARTS chunks, 8 columns each) of the part, for the
+// rows r0 + 16 PARTS i, where the PARTS threads of a quarter-warp that share
+// a chunk take rows whose index differs by 8 / PARTS: the quarter-warp then
+// covers 8 distinct 16-byte positions of the 128-byte swizzle pattern
+// (conflict free), and gamma/beta of the chunk are read once per part.
+// After its stores each thread fences them for the async proxy.
 // m0_of(unit) gives the unit's first x row in this CTA and kb_count(unit)
 // the number of k blocks the unit covers (all of them unless K is split).
-template <int NORM, bool BF16, int STAGES, int KA, typename M0Fn, typename KbFn, typename ArriveFn>
+template <int NORM, bool BF16, int STAGES, int KA, int PARTS = 1, typename M0Fn, typename KbFn,
+          typename ArriveFn>
 __device__ __forceinline__ void transform_role(int t, int tile0, int tile_step, int num_tiles,
                                                KbFn kb_count, int M, const float2 *stats,
                                                uint8_t *sA, const float *sG, uint64_t *full,
                                                const WaitCtx &wc, M0Fn m0_of, ArriveFn arrive)
 {
-    constexpr int kRows = kBM * 8 / kGroupThreads;   // rows per thread
-    constexpr int kRowStep = kGroupThreads / 8;
+    static_assert(PARTS == 1 || PARTS == 2 || PARTS == 4, "a part is a whole number of 16-byte chunks");
+    static_assert(kGroupThreads == 128, "a group covers 128 rows x 8 chunks per pass");
+    constexpr int kCP = 8 / PARTS;                    // chunks of a row per part
+    constexpr int kRowStride = 16 * PARTS;            // rows between a thread's rows
+    constexpr int kRows = kBM / kRowStride;           // rows per thread
     constexpr int kBatch = kRows < 8 ? kRows : 8;
+    constexpr int kS = 8 / PARTS;                     // row offset of a quarter-warp's row sets
     // A group waits on a stage barrier kTransformGroups fills after its
     // previous one; with more groups than stages it could be two phases
     // ahead, which a parity wait cannot tell from a completed phase.
     static_assert(kTransformGroups <= STAGES, "more transform groups than pipeline stages");
     const int g = t / kGroupThreads;
     const int u = t % kGroupThreads;
-    const int c = u & 7;
-    const int r0 = u >> 3;
-    const int pc = (c ^ (r0 & 7)) << 4;  // swizzled chunk offset (row % 8 == r0 % 8)
+    const int cl = u % kCP;                           // chunk within the part
+    const int j = (u / kCP) % PARTS;                  // row set within the quarter-warp
+    const int qw = u >> 3;                            // quarter-warp of the group
+    const int r0 = (qw % kS) + 8 * (qw / kS) + kS * j;
     const int lane = threadIdx.x & 31;
     pdl_wait();                          // statistics come from the previous grid
     int stage = 0;
@@ -316,7 +327,7 @@ __device__ __forceinline__ void transform_role(int t, int tile0, int tile_step, 
         float2 so[kRows];
 #pragma unroll
         for (int i = 0; i < kRows; ++i) {
-            const int row = m0 + r0 + kRowStep * i;
+            const int row = m0 + r0 + kRowStride * i;
             float2 st = make_float2(0.f, 0.f);
             if (row < M) st = stats[row];
             so[i] = make_float2(st.y, -st.x * st.y);
@@ -324,44 +335,49 @@ __device__ __forceinline__ void transform_role(int t, int tile0, int tile_step, 
         const int k_blocks = kb_count(tile);
         for (int kb = 0; kb < k_blocks; ++kb, ++it) {
             if (it % kTransformGroups == g) {
-                if (!mbar_wait_warp(&full[stage], phase, wc)) return;
-                // gamma/beta of columns 8c..8c+7; the two halves are read
-                // in separate instructions so that a quarter-warp touches
-                // 8 distinct 16-byte slots of one 128-byte line each time.
-                const float *gp = sG + stage * 2 * kBK + 8 * c;
-                float4 q[4];
-                q[0] = *reinterpret_cast<const float4 *>(gp);
-                q[1] = *reinterpret_cast<const float4 *>(gp + 4);
-                if constexpr (NORM == kNormLayer) {
-                    q[2] = *reinterpret_cast<const float4 *>(gp + kBK);
-                    q[3] = *reinterpret_cast<const float4 *>(gp + kBK + 4);
-                }
-                const float2 gg[4] = {make_float2(q[0].x, q[0].y), make_float2(q[0].z, q[0].w),
-                                      make_float2(q[1].x, q[1].y), make_float2(q[1].z, q[1].w)};
-                float2 bb[4];
-                if constexpr (NORM == kNormLayer) {
-                    bb[0] = make_float2(q[2].x, q[2].y);
-                    bb[1] = make_float2(q[2].z, q[2].w);
-                    bb[2] = make_float2(q[3].x, q[3].y);
-                    bb[3] = make_float2(q[3].z, q[3].w);
-                }
-                uint8_t *base = sA + stage * KA + r0 * 128 + pc;
-                // Rows in batches of up to 8: all loads of a batch are in
-                // flight before its first store.
+                if (!mbar_wait_warp_spin(&full[stage], phase, wc)) return;
 #pragma unroll
-                for (int b0 = 0; b0 < kRows; b0 += kBatch) {
-                    uint4 v[kBatch];
+                for (int part = 0; part < PARTS; ++part) {
+                    const int c = cl + kCP * part;    // logical chunk: columns 8c .. 8c+7
+                    // gamma/beta of the chunk; the two halves are read in
+                    // separate instructions so that a quarter-warp touches
+                    // 8 distinct 16-byte slots of one 128-byte line each time.
+                    const float *gp = sG + stage * 2 * kBK + 8 * c;
+                    float4 q[4];
+                    q[0] = *reinterpret_cast<const float4 *>(gp);
+                    q[1] = *reinterpret_cast<const float4 *>(gp + 4);
+                    if constexpr (NORM == kNormLayer) {
+                        q[2] = *reinterpret_cast<const float4 *>(gp + kBK);
+                        q[3] = *reinterpret_cast<const float4 *>(gp + kBK + 4);
+                    }
+                    const float2 gg[4] = {make_float2(q[0].x, q[0].y), make_float2(q[0].z, q[0].w),
+                                          make_float2(q[1].x, q[1].y), make_float2(q[1].z, q[1].w)};
+                    float2 bb[4];
+                    if constexpr (NORM == kNormLayer) {
+                        bb[0] = make_float2(q[2].x, q[2].y);
+                        bb[1] = make_float2(q[2].z, q[2].w);
+                        bb[2] = make_float2(q[3].x, q[3].y);
+                        bb[3] = make_float2(q[3].z, q[3].w);
+                    }
+                    const int pc = (c ^ (r0 & 7)) << 4;   // swizzled chunk offset (same for all rows)
+                    uint8_t *base = sA + stage * KA + r0 * 128 + pc;
+                    // Rows in batches of up to 8: all loads of a batch are in
+                    // flight before its first store.
 #pragma unroll
-                    for (int i = 0; i < kBatch; ++i)
-                        v[i] = *reinterpret_cast<const uint4 *>(base + (b0 + i) * kRowStep * 128);
+                    for (int b0 = 0; b0 < kRows; b0 += kBatch) {
+                        uint4 v[kBatch];
 #pragma unroll
-                    for (int i = 0; i < kBatch; ++i)
-                        *reinterpret_cast<uint4 *>(base + (b0 + i) * kRowStep * 128) =
-                            transform8_pk<NORM, BF16>(v[i], so[b0 + i], gg, bb);
+                        for (int i = 0; i < kBatch; ++i)
+                            v[i] = *reinterpret_cast<const uint4 *>(base + (b0 + i) * kRowStride * 128);
+#pragma unroll
+                        for (int i = 0; i < kBatch; ++i)
+                            *reinterpret_cast<uint4 *>(base + (b0 + i) * kRowStride * 128) =
+                                transform8_pk<NORM, BF16>(v[i], so[b0 + i], gg, bb);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) arrive(stage * PARTS + part);
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) arrive(stage);
             }
             if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -472,7 +488,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const int m0 = (tile % m_tiles) * kBM;
                 const int n0 = (tile / m_tiles) * BN;
                 for (int kb = 0; kb < k_blocks; ++kb) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, wc)) { ok = false; break; }
+                    if (!mbar_wait_spin(&empty[stage], phase ^ 1u, wc)) { ok = false; break; }
                     mbar_arrive_expect_tx(&full[stage], kTx);
                     const int kc = kb * kBK;
                     tma_load_2d(sA + stage * L::kA, &args.map_a, &full[stage], kc, m0, pol_x);
@@ -502,13 +518,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint32_t acc_phase = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, wc)) break;
+                if (!mbar_wait_spin(&acc_empty[acc], acc_phase ^ 1u, wc)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
                 for (int kb = 0; kb < k_blocks; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, wc)) { ok = false; break; }
+                    if (!mbar_wait_spin(&full[stage], phase, wc)) { ok = false; break; }
                     if constexpr (kNorm) {
-                        if (!mbar_wait(&ready[stage], phase, wc)) { ok = false; break; }
+                        if (!mbar_wait_spin(&ready[stage], phase, wc)) { ok = false; break; }
                     }
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(sA + stage * L::kA);

@@ -97,6 +97,60 @@ static __device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, co
     }
 }
 
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// The same bounded wait for the pipeline roles whose wake-up latency sits
+// on every stage's round trip (TMA producer, MMA issuer, transform): it
+// polls with the non-blocking test instead of the potentially suspending
+// try, so that the thread resumes as soon as the phase completes (a
+// suspended thread was measured to resume late enough to slow the tile
+// kernels by several per cent).  NGR_SPIN_WAIT=0 selects the suspending
+// form.
+#ifndef NGR_SPIN_WAIT
+#define NGR_SPIN_WAIT 1
+#endif
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t parity, const WaitCtx &w)
+{
+#if NGR_SPIN_WAIT == 0
+    return mbar_wait(bar, parity, w);
+#else
+    if (mbar_test_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_test_wait(bar, parity)) return true;
+        if ((it & 1023u) == 0) {
+            if (*reinterpret_cast<volatile int *>(w.abort) != 0) return false;
+            if (global_timer_ns() - t0 > w.timeout_ns) {
+                *reinterpret_cast<volatile int *>(w.abort) = 1;
+                atomicExch(w.err, kDevErrTimeout);
+                return false;
+            }
+        }
+    }
+#endif
+}
+
+// Warp-uniform form of mbar_wait_spin (lane 0 polls).
+__device__ __forceinline__ bool mbar_wait_warp_spin(uint64_t *bar, uint32_t parity, const WaitCtx &w)
+{
+    int ok = 0;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait_spin(bar, parity, w) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) (void)mbar_try_wait(bar, parity);
+    return ok != 0;
+}
+
 // Warp-uniform form for roles whose next step is warp-collective: lane 0
 // waits, the verdict is broadcast, and every lane then acquires the
 // completed phase itself.  All 32 lanes must call it.
