@@ -105,7 +105,7 @@ __device__ __forceinline__ void chan_merge(float &n, float &mean, float &m2, flo
     const float nt = n + nb;
     if (nt > 0.f) {
         const float d = mb - mean;
-        const float wb = nb / nt;
+        const float wb = __fdividef(nb, nt);   // 0 <= nb <= nt: well inside its range
         mean = fmaf(d, wb, mean);
         m2 = m2 + m2b + d * d * (n * wb);
         n = nt;
@@ -196,8 +196,9 @@ __global__ void __launch_bounds__(kStatsThreads, XHAT ? 1 : kStatsCtasPerSm) row
                     n += static_cast<float>(nv);
                 }
             }
-            float mean = n > 0.f ? s + s1 / n : 0.f;
-            float m2 = n > 0.f ? fmaxf(s2 - s1 * (s1 / n), 0.f) : 0.f;
+            const float s1n = n > 0.f ? __fdividef(s1, n) : 0.f;
+            float mean = s + s1n;
+            float m2 = fmaxf(s2 - s1 * s1n, 0.f);
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) {
                 const float nb = __shfl_xor_sync(0xffffffffu, n, off);
