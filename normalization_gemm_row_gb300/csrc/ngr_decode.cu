@@ -117,21 +117,42 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
-            pdl_wait();  // the tokens may come from the previous grid
+            // The tokens may come from the previous grid (the statistics
+            // kernel's normalized rows, or the first product of a chain);
+            // the weights never do.  The first STAGES fills therefore start
+            // their weight boxes at once and add the token boxes after the
+            // dependency wait, so the weight stream overlaps the previous
+            // grid's tail.
             const uint64_t pol_x = policy_evict_last();
             const uint64_t pol_w = policy_evict_first();  // each weight byte is read once
+            bool waited = false;
+            int deferred_kc[STAGES];
             int stage = 0;
             uint32_t phase = 0;
             long long fills = 0;
             for (long long u = u_begin; u < u_end; ++u) {
                 const int tile = static_cast<int>(u / KB);
                 const int kc = static_cast<int>(u % KB) * kBK;
+                if (!waited && fills == STAGES) {
+                    pdl_wait();
+                    waited = true;
+                    for (int s2 = 0; s2 < STAGES; ++s2)
+                        tma_load_2d(sX + s2 * L::kX, &args.map_x, &full[s2], deferred_kc[s2], 0, pol_x);
+                }
                 if (!mbar_wait_spin(&empty[stage], phase ^ 1u, wc)) break;
                 mbar_arrive_expect_tx(&full[stage], kTx);
                 tma_load_2d(sW + stage * L::kW, &args.map_w, &full[stage], kc, tile * 128, pol_w);
-                tma_load_2d(sX + stage * L::kX, &args.map_x, &full[stage], kc, 0, pol_x);
+                if (waited)
+                    tma_load_2d(sX + stage * L::kX, &args.map_x, &full[stage], kc, 0, pol_x);
+                else
+                    deferred_kc[stage] = kc;
                 ++fills;
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+            if (!waited) {   // fewer fills than stages (or a failed wait)
+                pdl_wait();
+                for (int s2 = 0; s2 < static_cast<int>(fills < STAGES ? fills : STAGES); ++s2)
+                    tma_load_2d(sX + s2 * L::kX, &args.map_x, &full[s2], deferred_kc[s2], 0, pol_x);
             }
             const int outstanding = fills < STAGES ? static_cast<int>(fills) : STAGES;
             for (int j = 1; j <= outstanding; ++j) {
