@@ -364,15 +364,15 @@ int finish(int rc, void *ws, cudaStream_t stream)
 }
 
 // One linear layer y = act(norm(x) W^T + bias) on its own, given the
-// workspace regions.  `pdl` says whether a preceding grid on the stream
-// produced what this one reads (then it is launched as a programmatic
-// dependent); `ab_ready` that x and W are not among what it produced.
+// workspace regions.  `stats_ready` says whether a preceding grid on the
+// stream produced what this one reads (then it is launched as a
+// programmatic dependent).
 int launch_layer(int norm, int act, bool bf16, const void *x, const void *W,
                  const void *bias, int64_t M, int64_t K, int64_t N, void *y,
                  char *ws, const WsLayout &L, size_t counters_off, bool pdl,
                  const DevInfo &di, cudaStream_t stream, const float *fold_c = nullptr,
                  const float *fold_b = nullptr, int64_t w_rows = -1,
-                 const void *residual = nullptr, bool may_split = false, bool ab_ready = false)
+                 const void *residual = nullptr, bool may_split = false)
 {
     // W has w_rows rows (N unless the output is padded past W's rows; the
     // tensor maps zero-fill the rest).
@@ -446,7 +446,6 @@ int launch_layer(int norm, int act, bool bf16, const void *x, const void *W,
     a.num_tiles = a.m_tiles * a.n_tiles;
     a.timeout_ns = wait_timeout_ns();
     a.act = act;
-    a.ab_ready = ab_ready ? 1 : 0;
     a.k_splits = plan.splits > 1 ? plan.splits : 1;
     a.kb_per_split = static_cast<int>(ceil_div(a.k_blocks, a.k_splits));
     if (a.k_splits > 1) {
@@ -460,7 +459,7 @@ int launch_layer(int norm, int act, bool bf16, const void *x, const void *W,
 // CTA-pair kernel, at any M.
 int launch_gated(int norm, bool bf16, const void *x, const void *Wg, const void *Wu, int64_t M,
                  int64_t K, int64_t F, void *h, char *ws, const WsLayout &L, bool pdl,
-                 const DevInfo &di, cudaStream_t stream, bool ab_ready = false)
+                 const DevInfo &di, cudaStream_t stream)
 {
     GemmArgs a;
     std::memset(&a, 0, sizeof(a));
@@ -481,7 +480,6 @@ int launch_gated(int norm, bool bf16, const void *x, const void *Wg, const void 
     a.y = h;
     a.err = reinterpret_cast<int *>(ws);
     a.zero_err = pdl ? 0 : 1;
-    a.ab_ready = ab_ready ? 1 : 0;
     a.act = kActNone;
     a.M = static_cast<int>(M);
     a.N = static_cast<int>(F);
@@ -575,7 +573,7 @@ int norm_linear(int op, int norm, int act, const void *x, const void *gamma, con
                           L.counters, true, di, stream, nullptr, nullptr, N, nullptr, true);
     else
         rc = launch_layer(norm, act, bf16, xa, Wa, biasa, M, K8, N8, ya, w, L, L.counters,
-                          need_stats, di, stream, nullptr, nullptr, N, nullptr, true, true);
+                          need_stats, di, stream, nullptr, nullptr, N, nullptr, true);
     event_after(stream);
     if (rc == NGR_OK && ya != y) rc = launch_unpad_rows(ya, M, N, N8, y, di.sms, stream);
     events_call_done();
@@ -620,7 +618,7 @@ int folded_linear(int norm, const void *x, const void *Wf, const float *cb, floa
     event_before(stream);
     rc = launch_layer(norm == kNormLayer ? kNormFoldLayer : kNormFoldRms, kActNone, bf16, x, Wf,
                       nullptr, M, K, N, y, w, L, L.counters, true, di, stream, cb, cb + N, -1,
-                      nullptr, true, true);
+                      nullptr, true);
     event_after(stream);
     events_call_done();
     return finish(rc, ws, stream);
@@ -684,7 +682,7 @@ int mlp_chain(int op, int norm, int act, const void *x, const void *gamma, const
                           true, di, stream);
     else
         rc = launch_layer(norm, act, bf16, x, W1, b1, M, K, F, H, w, L, L.counters, need_stats, di,
-                          stream, nullptr, nullptr, -1, nullptr, false, true);
+                          stream);
     event_after(stream);
     if (rc != NGR_OK) return rc;
     event_before(stream);
@@ -744,7 +742,7 @@ int swiglu_chain(int op, int norm, const void *x, const void *gamma, const void 
         if (rc != NGR_OK) return rc;
     }
     event_before(stream);
-    rc = launch_gated(norm, bf16, x, Wg, Wu, M, K, F, H, w, L, need_stats, di, stream, true);
+    rc = launch_gated(norm, bf16, x, Wg, Wu, M, K, F, H, w, L, need_stats, di, stream);
     event_after(stream);
     if (rc != NGR_OK) return rc;
     if (down) {
@@ -802,7 +800,7 @@ int linear_residual_norm(int norm, const void *x, const void *W, const void *bia
     }
     event_before(stream);
     rc = launch_layer(kNormNone, kActNone, bf16, x, W, bias, M, K, N, H, w, L, L.counters, decode,
-                      di, stream, nullptr, nullptr, -1, residual, true, true);
+                      di, stream, nullptr, nullptr, -1, residual, true);
     event_after(stream);
     if (rc != NGR_OK) return rc;
     // The norm over each h row (a plain launch: it reads the product's output).

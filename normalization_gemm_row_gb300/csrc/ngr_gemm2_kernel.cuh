@@ -289,13 +289,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
-            // When no preceding grid of the call wrote x and W, the first
-            // STAGES fills load them before the dependency wait (overlapping
-            // the statistics kernel); the FP32 gamma/beta of those stages,
-            // which that kernel writes, are loaded once the wait is over.
-            bool waited = args.ab_ready == 0;
-            if (waited) pdl_wait();
-            int deferred_kc[STAGES];
+            pdl_wait();
             const uint64_t pol_x = policy_evict_last();
             const uint64_t pol_w = policy_evict_first();
             int stage = 0;
@@ -315,14 +309,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 auto wrow = [&](int j) { return GATED ? n0 : n0 + j * BN; };
                 const uint32_t tx = stage_tx(n_sub);
                 for (int kb = unit_kb0(u), kb_end = unit_kb1(u); kb < kb_end; ++kb) {
-                    if (!waited && fills == STAGES) {
-                        pdl_wait();
-                        waited = true;
-                        if constexpr (kNorm)
-                            for (int s2 = 0; s2 < STAGES; ++s2)
-                                tma_load_2d(sG + s2 * 2 * kBK, &args.map_gb, &full[s2],
-                                            deferred_kc[s2], 0, pol_x);
-                    }
                     if (!mbar_wait_spin(&empty[stage], phase ^ 1u, wc)) { ok = false; break; }
                     const int kc = kb * kBK;
                     uint8_t *sb = sB + stage * L::kB;
@@ -332,10 +318,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         tma_load_2d(sA + stage * L::kA, &args.map_a, &full[stage], kc, m0, pol_x);
                         for (int j = 0; j < n_sub; ++j)
                             tma_load_2d(sb + j * L::kBSub, wmap(j), &full[stage], kc, wrow(j), pol_w);
-                        if (waited)
-                            tma_load_2d(sG + stage * 2 * kBK, &args.map_gb, &full[stage], kc, 0, pol_x);
-                        else
-                            deferred_kc[stage] = kc;
+                        tma_load_2d(sG + stage * 2 * kBK, &args.map_gb, &full[stage], kc, 0, pol_x);
                     } else {
                         // Both CTAs' copies complete on the leader's barrier,
                         // which expects the bytes of both.
@@ -348,13 +331,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     ++fills;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
-            }
-            if (!waited) {   // fewer fills than stages (or a failed wait)
-                pdl_wait();
-                if constexpr (kNorm)
-                    for (int s2 = 0; s2 < static_cast<int>(fills < STAGES ? fills : STAGES); ++s2)
-                        tma_load_2d(sG + s2 * 2 * kBK, &args.map_gb, &full[s2], deferred_kc[s2], 0,
-                                    pol_x);
             }
             // Copies signalled on this CTA's own barriers: wait for the last
             // fills.  (Without a norm the peer's copies complete on the

@@ -58,8 +58,6 @@ struct alignas(128) GemmArgs {
     void *y;                // [M, N]
     int *err;               // device error word
     int zero_err;           // nonzero: this kernel is the call's first and clears *err
-    int ab_ready;           // nonzero: x and W come from no preceding grid of the call, so
-                            // the CTA-pair producer loads them before the dependency wait
     int act;                // kAct*: activation after the bias (not used when gated)
     int M, N, K;
     int m_tiles, n_tiles, k_blocks, num_tiles;
