@@ -581,14 +581,20 @@ def our_arm(args, rank, world, local):
         for i in range(args.warmup):
             tstep(i)
         torch.cuda.synchronize(dev)
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        t0.record(stream)
-        for i in range(args.steps):
-            tstep(i)
-        t1.record(stream)
-        torch.cuda.synchronize(dev)
-        tms = t0.elapsed_time(t1) / args.steps
+
+        def twindow():
+            t0 = torch.cuda.Event(enable_timing=True)
+            t1 = torch.cuda.Event(enable_timing=True)
+            t0.record(stream)
+            for i in range(args.steps):
+                tstep(i)
+            t1.record(stream)
+            torch.cuda.synchronize(dev)
+            return t0.elapsed_time(t1) / args.steps
+
+        # The median of three windows of K steps: a comparison, kept robust
+        # against a single disturbed window.
+        tms = statistics.median(twindow() for _ in range(3))
         alternatives["torch_unfused_same_gpu"] = {
             "what": "the same computation as separate torch ops (layer_norm/rms_norm, linear on "
                     "cuBLAS, activations, the SwiGLU product), intermediates written to HBM",
