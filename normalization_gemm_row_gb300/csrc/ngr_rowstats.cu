@@ -3,13 +3,18 @@
 // "LayerNorm 融合算子如何让大模型推理再快 15%？深度拆解 ATB 的实现", §1.1: the
 // statistics are a reduction over each row (a sum and a sum of squares);
 // §2.3: they are computed in FP32.  One CTA reduces one row with 16-byte
-// loads.  LayerNorm uses a shifted, mergeable form so that a large row mean
-// (inputs centred far from zero) does not cancel the variance: each thread
-// keeps (n, mean, M2) of its own elements, built from sums of (x - s) with s
-// the thread's first element, and threads are merged pairwise with the
-// parallel-variance update of Chan, Golub and LeVeque (1979):
-//   n = na + nb,  d = mb - ma,  mean = ma + d nb / n,
-//   M2 = M2a + M2b + d^2 na nb / n.
+// loads.  LayerNorm uses shifted sums so that a large row mean (inputs
+// centred far from zero) does not cancel the variance:
+//  - each thread forms (n, mean, M2) of its own elements from sums of
+//    (x - s), s its first element;
+//  - a warp re-centres its threads' triples on lane 0's mean m0
+//    (sum n (mean - m0) and sum M2 + n (mean - m0)^2 add exactly like plain
+//    sums), which costs no more than a factor 32 in cancellation because m0
+//    is the mean of 32 of the warp's own elements;
+//  - the 8 warps are merged with the parallel-variance update of Chan,
+//    Golub and LeVeque (1979):
+//      n = na + nb,  d = mb - ma,  mean = ma + d nb / n,
+//      M2 = M2a + M2b + d^2 na nb / n.
 // var = M2 / K (biased), rstd = 1 / sqrt(var + eps).  RMSNorm: rstd =
 // 1 / sqrt(sum x^2 / K + eps) and mu = 0.
 //
@@ -98,6 +103,16 @@ __device__ __forceinline__ uint4 normalize8(const uint4 &v, const uint4 &g, cons
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// A 16-bit value's bits as FP32.
+template <bool BF16>
+__device__ __forceinline__ float half_bits_to_float(uint32_t h)
+{
+    if constexpr (BF16)
+        return __uint_as_float(h << 16);
+    else
+        return __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
+}
+
 // Merge (nb, mb, m2b) into (n, mean, m2): the parallel-variance update.
 __device__ __forceinline__ void chan_merge(float &n, float &mean, float &m2, float nb, float mb,
                                            float m2b)
@@ -162,50 +177,65 @@ __global__ void __launch_bounds__(kStatsThreads, XHAT ? 1 : kStatsCtasPerSm) row
     for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
         const uint4 *xr = x + row * vec_per_row;
         if constexpr (NORM == kNormLayer) {
-            // This thread's elements as shifted sums, shift = its first element.
-            float s = 0.f, s1 = 0.f, s2 = 0.f, n = 0.f;
-            bool have_shift = false;
-            for (int64_t v0 = tid; v0 < vec_per_row; v0 += 4 * kStatsThreads) {
+            // This thread's elements as shifted sums in packed FP32x2, shift
+            // = its first element.  Slots past the row read as the shift
+            // itself (they add exactly zero); a padded row's zero padding,
+            // in its last vector only, is taken out afterwards by the thread
+            // that read it.
+            const int nvec = static_cast<int>(vec_per_row);
+            const uint32_t h = tid < nvec ? static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short *>(xr + tid))) : 0u;
+            const float s = half_bits_to_float<BF16>(h);
+            const uint32_t hh = h | (h << 16);
+            const float2 ns = make_float2(-s, -s);
+            float2 s1p = make_float2(0.f, 0.f), s2p = make_float2(0.f, 0.f);
+#pragma unroll 1
+            for (int v0 = tid; v0 < nvec; v0 += 4 * kStatsThreads) {
                 uint4 q[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    const int64_t v = v0 + static_cast<int64_t>(u) * kStatsThreads;
-                    if (v < vec_per_row) q[u] = __ldg(xr + v);
+                    const int v = v0 + u * kStatsThreads;
+                    q[u] = v < nvec ? __ldg(xr + v) : make_uint4(hh, hh, hh, hh);
                 }
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    const int64_t v = v0 + static_cast<int64_t>(u) * kStatsThreads;
-                    if (v >= vec_per_row) break;
-                    float f[8];
-                    unpack8<BF16>(q[u], f);
-                    // real columns of this vector (all 8 except in a padded tail)
-                    const int64_t rem = k_valid - 8 * v;
-                    const int nv = rem >= 8 ? 8 : (rem > 0 ? static_cast<int>(rem) : 0);
-                    if (!have_shift && nv > 0) {
-                        s = f[0];
-                        have_shift = true;
-                    }
+                    const uint32_t w[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        if (i < nv) {
-                            const float d = f[i] - s;
-                            s1 += d;
-                            s2 = fmaf(d, d, s2);
-                        }
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 d = __fadd2_rn(unpack_pair<BF16>(w[i]), ns);
+                        s1p = __fadd2_rn(s1p, d);
+                        s2p = __ffma2_rn(d, d, s2p);
                     }
-                    n += static_cast<float>(nv);
                 }
             }
+            float s1 = s1p.x + s1p.y, s2 = s2p.x + s2p.y;
+            float n = tid < nvec ? 8.f * static_cast<float>((nvec - 1 - tid) / kStatsThreads + 1) : 0.f;
+            const int pad = nvec * 8 - static_cast<int>(k_valid);
+            if (pad > 0 && (nvec - 1) % kStatsThreads == tid) {
+                // Each padding zero added (0 - s) to s1 and s^2 to s2.
+                const float p = static_cast<float>(pad);
+                n -= p;
+                s1 = fmaf(p, s, s1);
+                s2 = fmaf(-p * s, s, s2);
+            }
+            // (n, mean, M2) of this thread, then re-centred on lane 0's mean
+            // (a mean of the warp's own elements) so that the warp's sums
+            // need plain additions only.
             const float s1n = n > 0.f ? __fdividef(s1, n) : 0.f;
-            float mean = s + s1n;
-            float m2 = fmaxf(s2 - s1 * s1n, 0.f);
+            const float mean_t = s + s1n;
+            const float m2_t = fmaxf(s2 - s1 * s1n, 0.f);
+            const float sw = __shfl_sync(0xffffffffu, mean_t, 0);
+            const float dt = mean_t - sw;
+            float a1 = n * dt;
+            float a2 = fmaf(a1, dt, m2_t);
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) {
-                const float nb = __shfl_xor_sync(0xffffffffu, n, off);
-                const float mb = __shfl_xor_sync(0xffffffffu, mean, off);
-                const float m2b = __shfl_xor_sync(0xffffffffu, m2, off);
-                chan_merge(n, mean, m2, nb, mb, m2b);
+                n += __shfl_xor_sync(0xffffffffu, n, off);
+                a1 += __shfl_xor_sync(0xffffffffu, a1, off);
+                a2 += __shfl_xor_sync(0xffffffffu, a2, off);
             }
+            const float a1n = n > 0.f ? __fdividef(a1, n) : 0.f;
+            const float mean = sw + a1n;
+            const float m2 = fmaxf(a2 - a1 * a1n, 0.f);
             if (lane == 0) {
                 red[0][wid] = n;
                 red[1][wid] = mean;
