@@ -541,6 +541,24 @@ def our_arm(args, rank, world, local):
             "frac": (fval / (peaks["hbm_gbs"] if decode else peaks["bf16_tflops"])),
         }
         del folded
+    # ------------- the same steps on one input set (whatever of it L2 holds)
+    if not args.no_alternatives:
+        for i in range(args.warmup):
+            step(sets[0])
+        torch.cuda.synchronize(dev)
+        w0 = torch.cuda.Event(enable_timing=True)
+        w1 = torch.cuda.Event(enable_timing=True)
+        w0.record(stream)
+        for i in range(args.steps):
+            step(sets[0])
+        w1.record(stream)
+        torch.cuda.synchronize(dev)
+        wms = w0.elapsed_time(w1) / args.steps
+        alternatives["same_inputs_every_step"] = {
+            "what": "every step on input set 0, so x and W stay in L2 as far as it holds them "
+                    "(the headline value rotates sets larger than L2)",
+            "value": (algo_bytes / (wms / 1e3) / 1e9) if decode else (flops / (wms / 1e3) / 1e12),
+            "unit": unit, "ms_per_step": wms}
     # ---------------- unfused torch pipeline on the same GPU (cuBLAS GEMM)
     if not args.no_alternatives:
         import torch.nn.functional as F
