@@ -45,18 +45,6 @@
 
 namespace ngr {
 
-// Where the normalized A operand lives in the CTA-pair kernel with a norm:
-// 1 = tensor memory (written with tcgen05.st by row-owning threads; the
-// MMAs read it from there), 0 = shared memory (normalized in place, like
-// the single-CTA kernel).  One switch for one-sub-tile tiles, one for
-// two-sub-tile tiles.
-#ifndef NGR_PAIR_A_TMEM
-#define NGR_PAIR_A_TMEM 0
-#endif
-#ifndef NGR_PAIR_A_TMEM_WIDE
-#define NGR_PAIR_A_TMEM_WIDE 0
-#endif
-constexpr int kMaxASlots = 8;
 // Column parts per stage of the in-place transform (1, 2 or 4): the MMAs of
 // a part's K steps are issued once that part of both CTAs' stages is
 // normalized.
@@ -75,99 +63,12 @@ struct Gemm2Smem {
     static constexpr int off_b = off_a + STAGES * kA;
     static constexpr int off_g = off_b + STAGES * kB;
     static constexpr int off_bar = off_g + STAGES * kGB;
-    static constexpr int n_bars = (2 + kMaxParts) * STAGES + 5 + kMaxASlots;
+    static constexpr int n_bars = (2 + kMaxParts) * STAGES + 5;
     static constexpr int off_tmem = off_bar + n_bars * 8;
     static constexpr int bytes = off_tmem + 16;
     static constexpr int alloc = bytes + 1024;
 };
 
-
-// The transform role of the CTA-pair kernel with A in tensor memory.
-// A slot holds SLOT_K of a k block's 64 columns (SLOT_K / 2 tensor-memory
-// columns of packed 16-bit pairs); a k block fills HALVES = 64 / SLOT_K
-// slots, the j-th of the running sequence going to slot j % SLOTS, which is
-// free once the MMAs that read its previous contents have completed
-// (a_free, committed by the MMA issuer to both CTAs).  With one slot per k
-// block, transform group g takes the k blocks with running index
-// it % groups == g; with two, group h fills slot half h of every k block.
-// Each warp covers the tensor-memory lane quarter warp % 4, and each lane
-// one row: it reads its row's raw x chunks from the swizzled shared-memory
-// stage (only read), normalizes them in FP32, packs them to 16-bit pairs
-// and stores them with tcgen05.st.
-template <int NORM, bool BF16, int STAGES, int KA, int SLOTS, int HALVES, typename M0Fn,
-          typename KbFn, typename ArriveFn>
-__device__ __forceinline__ void transform_role_tmem(
-    int t, int tile0, int tile_step, int num_tiles, KbFn kb_count, int M, const float2 *stats,
-    const uint8_t *sA, const float *sG, uint64_t *full, uint64_t *a_free, uint32_t tmem_base,
-    uint32_t a_col0, const WaitCtx &wc, M0Fn m0_of, ArriveFn arrive)
-{
-    constexpr int kChunks = 8 / HALVES;   // 16-byte chunks of a row per slot
-    constexpr int kCols = kChunks * 4;    // tensor-memory columns per slot
-    static_assert(KA > 0 && kGroupThreads == 128, "a group must cover the four lane quarters");
-    static_assert(HALVES == 1 || (HALVES == 2 && kTransformGroups == 2), "one group per slot half");
-    const int g = t / kGroupThreads;
-    const int lane = threadIdx.x & 31;
-    const int q = (threadIdx.x >> 5) & 3;   // lane quarter this warp may access
-    const int r = q * 32 + lane;            // row of the 128-row tile
-    const int sw = r & 7;
-    const int h = HALVES > 1 ? g : 0;       // slot half this thread fills
-    const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + a_col0;
-    pdl_wait();
-    int stage = 0;
-    uint32_t phase = 0;
-    int it = 0;
-    for (int tile = tile0; tile < num_tiles; tile += tile_step) {
-        const int row = m0_of(tile) + r;
-        float2 st = make_float2(0.f, 0.f);
-        if (row < M) st = stats[row];
-        const float2 so = make_float2(st.y, -st.x * st.y);
-        const int k_blocks = kb_count(tile);
-        for (int kb = 0; kb < k_blocks; ++kb, ++it) {
-            if (HALVES > 1 || it % kTransformGroups == g) {
-                if (!mbar_wait_warp(&full[stage], phase, wc)) return;
-                const int sidx = it * HALVES + h;
-                const int slot = sidx % SLOTS;
-                const int use = sidx / SLOTS;
-                if (use > 0 && !mbar_wait_warp(&a_free[slot], (use - 1) & 1, wc)) return;
-                tc_fence_after();
-                const uint8_t *xrow = sA + stage * KA + r * 128;
-                const float *gs = sG + stage * 2 * kBK;
-                uint32_t packed[kCols];
-#pragma unroll
-                for (int c0 = 0; c0 < kChunks; ++c0) {
-                    const int c = h * kChunks + c0;
-                    const uint4 v = *reinterpret_cast<const uint4 *>(xrow + ((c ^ sw) << 4));
-                    const float4 g0 = *reinterpret_cast<const float4 *>(gs + 8 * c);
-                    const float4 g1 = *reinterpret_cast<const float4 *>(gs + 8 * c + 4);
-                    const float2 gg[4] = {make_float2(g0.x, g0.y), make_float2(g0.z, g0.w),
-                                          make_float2(g1.x, g1.y), make_float2(g1.z, g1.w)};
-                    float2 bb[4];
-                    if constexpr (NORM == kNormLayer) {
-                        const float4 b0 = *reinterpret_cast<const float4 *>(gs + kBK + 8 * c);
-                        const float4 b1 = *reinterpret_cast<const float4 *>(gs + kBK + 8 * c + 4);
-                        bb[0] = make_float2(b0.x, b0.y);
-                        bb[1] = make_float2(b0.z, b0.w);
-                        bb[2] = make_float2(b1.x, b1.y);
-                        bb[3] = make_float2(b1.z, b1.w);
-                    }
-                    const uint4 o = transform8_pk<NORM, BF16>(v, so, gg, bb);
-                    packed[4 * c0 + 0] = o.x;
-                    packed[4 * c0 + 1] = o.y;
-                    packed[4 * c0 + 2] = o.z;
-                    packed[4 * c0 + 3] = o.w;
-                }
-                const uint32_t taddr = tbase + static_cast<uint32_t>(slot * kCols);
-                if constexpr (kCols == 32) tmem_st32(taddr, packed);
-                else tmem_st16(taddr, packed);
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) arrive(stage);
-            }
-            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-        }
-    }
-}
 
 template <int NORM, bool BF16, int BN, int STAGES, int NSUB, bool GATED>
 __global__ void __launch_bounds__(kGemmThreads, 1)
@@ -182,29 +83,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     auto stage_tx = [](int n_sub) -> uint32_t {
         return static_cast<uint32_t>(L::kA + n_sub * L::kBSub + (kNorm ? L::kGB : 0));
     };
-    // Accumulators (two of kTW columns when they fit and A is not in tensor
-    // memory, else one), then the A slots: a whole k block per slot with one
-    // sub-tile, half a k block with two (only 64 columns are left beside a
-    // 448-column accumulator).
+    // Accumulators: two of kTW columns with one sub-tile (the epilogue of a
+    // tile overlaps the next tile's MMAs), one with two.
     constexpr uint32_t kTmemCols = 512;
-    constexpr int kSlotK = NSUB > 1 ? 32 : kBK;        // K columns of x per A slot
-    constexpr int kHalvesA = kBK / kSlotK;             // A slots per k block
-    constexpr int kSlotCols = kSlotK / 2;              // tensor-memory columns per slot
-    // (A in tensor memory needs at least two k blocks' slots beside one
-    // accumulator: not with a 512-column tile.)
-    constexpr bool kATmem = kNorm && !GATED && (NSUB > 1 ? NGR_PAIR_A_TMEM_WIDE : NGR_PAIR_A_TMEM) &&
-                            static_cast<int>(kTmemCols) - kTW >= 2 * kHalvesA * kSlotCols;
-    constexpr int kAccBufs = (kATmem || NSUB > 1) ? 1 : 2;
-    constexpr uint32_t kACol0 = kAccBufs * kTW;
-    constexpr int kSlotsFit = static_cast<int>((kTmemCols - kACol0) / kSlotCols);
-    constexpr int kASlots = kSlotsFit < kMaxASlots ? kSlotsFit : kMaxASlots;
-    static_assert(!kATmem || (kASlots >= 2 * kHalvesA && kASlots % (kHalvesA * kTransformGroups) == 0),
-                  "tensor memory: accumulator + A slots");
+    constexpr int kAccBufs = NSUB > 1 ? 1 : 2;
     constexpr uint32_t kIdesc = idesc_f16(BF16, 2 * kBM, BN);
-    // ready[s] arrivals: one per warp of each transform group that works on
-    // the stage, in each CTA (used with a norm only).
-    constexpr uint32_t kReadyCount = 2 * kGroupWarps * (kATmem ? kHalvesA : 1);
-    constexpr int kParts = (kNorm && !kATmem) ? NGR_TRANSFORM_PARTS : 1;
+    // ready[s * kParts + p] arrivals: one per warp of the transform group
+    // that works on the stage, in each CTA (used with a norm only).
+    constexpr uint32_t kReadyCount = 2 * kGroupWarps;
+    constexpr int kParts = kNorm ? NGR_TRANSFORM_PARTS : 1;
     static_assert(kParts >= 1 && kParts <= kMaxParts && (kBK / kUmmaK) % kParts == 0,
                   "whole K steps per transform part");
     static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "UMMA N for M = 256");
@@ -228,7 +115,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t *acc_full = bars + (2 + kMaxParts) * STAGES;
     uint64_t *acc_empty = acc_full + 2;
     uint64_t *drain = acc_full + 4;
-    uint64_t *a_free = acc_full + 5;            // [kMaxASlots] A slot read by the MMAs (commit, multicast)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::off_tmem);
 
     const int warp = threadIdx.x >> 5;
@@ -255,7 +141,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(&acc_empty[a], 2 * kDrainWarps);
         }
         mbar_init(drain, 1);
-        for (int j = 0; j < kMaxASlots; ++j) mbar_init(&a_free[j], 1);
         fence_mbarrier_init();
     }
     if (warp == 2) {
@@ -353,7 +238,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
-            int it = 0;
             bool ok = true;
             for (int u = cluster; ok && u < num_units; u += n_clusters) {
                 const int tile = unit_tile(u);
@@ -366,52 +250,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     if (!mbar_wait_spin(kNorm ? &ready[stage * kParts] : &full[stage], phase, wc)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t b_addr = smem_u32(sB + stage * L::kB);
-                    if constexpr (kATmem) {
+                    const uint32_t a_addr = smem_u32(sA + stage * L::kA);
+                    constexpr int kStepsPerPart = (kBK / kUmmaK) / kParts;
 #pragma unroll
-                        for (int hh = 0; hh < kHalvesA; ++hh) {
-                            const int slot = (it * kHalvesA + hh) % kASlots;
-                            const uint32_t a_tmem = tmem_base + kACol0 +
-                                                    static_cast<uint32_t>(slot * kSlotCols);
-#pragma unroll
-                            for (int k = 0; k < kSlotK / kUmmaK; ++k) {
-                                const int kk = hh * (kSlotK / kUmmaK) + k;   // K step in the block
-#pragma unroll
-                                for (int j = 0; j < NSUB; ++j) {
-                                    if (j < n_sub)
-                                        umma_f16_ts_pair(d_tmem + static_cast<uint32_t>(j * BN),
-                                                         a_tmem + static_cast<uint32_t>(k * (kUmmaK / 2)),
-                                                         sdesc_kmajor_sw128(b_addr + j * L::kBSub + kk * 32),
-                                                         kIdesc, (kb != kb0 || kk != 0) ? 1u : 0u);
-                                }
+                    for (int k = 0; k < kBK / kUmmaK; ++k) {
+                        if (kParts > 1 && k > 0 && k % kStepsPerPart == 0) {
+                            // The next column part of both CTAs' stages.
+                            if (!mbar_wait_spin(&ready[stage * kParts + k / kStepsPerPart], phase, wc)) {
+                                ok = false;
+                                break;
                             }
-                            umma_commit_pair(&a_free[slot], 0x3);
+                            tc_fence_after();
                         }
-                    } else {
-                        const uint32_t a_addr = smem_u32(sA + stage * L::kA);
-                        constexpr int kStepsPerPart = (kBK / kUmmaK) / kParts;
+                        const uint64_t a_desc = sdesc_kmajor_sw128(a_addr + k * 32);
 #pragma unroll
-                        for (int k = 0; k < kBK / kUmmaK; ++k) {
-                            if (kParts > 1 && k > 0 && k % kStepsPerPart == 0) {
-                                // The next column part of both CTAs' stages.
-                                if (!mbar_wait_spin(&ready[stage * kParts + k / kStepsPerPart], phase, wc)) {
-                                    ok = false;
-                                    break;
-                                }
-                                tc_fence_after();
-                            }
-                            const uint64_t a_desc = sdesc_kmajor_sw128(a_addr + k * 32);
-#pragma unroll
-                            for (int j = 0; j < NSUB; ++j) {
-                                if (j < n_sub)
-                                    umma_f16_ss_pair(d_tmem + static_cast<uint32_t>(j * BN), a_desc,
-                                                     sdesc_kmajor_sw128(b_addr + j * L::kBSub + k * 32),
-                                                     kIdesc, (kb != kb0 || k != 0) ? 1u : 0u);
-                            }
+                        for (int j = 0; j < NSUB; ++j) {
+                            if (j < n_sub)
+                                umma_f16_ss_pair(d_tmem + static_cast<uint32_t>(j * BN), a_desc,
+                                                 sdesc_kmajor_sw128(b_addr + j * L::kBSub + k * 32),
+                                                 kIdesc, (kb != kb0 || k != 0) ? 1u : 0u);
                         }
                     }
                     if (!ok) break;
                     umma_commit_pair(&empty[stage], 0x3);
-                    ++it;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
@@ -425,14 +286,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const bool epi_warp = warp >= kEpilogueWarp0;
         if (!epi_warp) {
             const int t = threadIdx.x - kTransformWarp0 * 32;
-            if constexpr (kATmem) {
-                // ------------------------------------------ transform (A -> TMEM)
-                transform_role_tmem<NORM, BF16, STAGES, L::kA, kASlots, kHalvesA>(
-                    t, cluster, n_clusters, num_units, [&](int u) { return unit_kb1(u) - unit_kb0(u); },
-                    args.M, args.stats, sA, sG, full, a_free, tmem_base, kACol0, wc,
-                    [&](int u) { return (unit_tile(u) % m_tiles) * 2 * kBM + static_cast<int>(rank) * kBM; },
-                    [&](int st) { mbar_arrive_cluster(ready_leader + 8u * static_cast<uint32_t>(st)); });
-            } else if constexpr (kNorm) {
+            if constexpr (kNorm) {
                 // ----------------------------------------- transform (A in place)
                 transform_role<NORM, BF16, STAGES, L::kA, kParts>(
                     t, cluster, n_clusters, num_units, [&](int u) { return unit_kb1(u) - unit_kb0(u); },
