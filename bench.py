@@ -610,14 +610,30 @@ def our_arm(args, rank, world, local):
             torch.cuda.synchronize(dev)
             return t0.elapsed_time(t1) / args.steps
 
-        # The median of three windows of K steps: a comparison, kept robust
-        # against a single disturbed window.
-        tms = statistics.median(twindow() for _ in range(3))
+        def owindow():
+            o0 = torch.cuda.Event(enable_timing=True)
+            o1 = torch.cuda.Event(enable_timing=True)
+            o0.record(stream)
+            for i in range(args.steps):
+                step(sets[i % n_sets])
+            o1.record(stream)
+            torch.cuda.synchronize(dev)
+            return o0.elapsed_time(o1) / args.steps
+
+        # Three windows of K steps of each, alternating, so that both sides
+        # see the same clocks; medians.
+        tw, ow = [], []
+        for _ in range(3):
+            tw.append(twindow())
+            ow.append(owindow())
+        tms = statistics.median(tw)
+        oms = statistics.median(ow)
         alternatives["torch_unfused_same_gpu"] = {
             "what": "the same computation as separate torch ops (layer_norm/rms_norm, linear on "
                     "cuBLAS, activations, the SwiGLU product), intermediates written to HBM",
             "value": (algo_bytes / (tms / 1e3) / 1e9) if decode else (flops / (tms / 1e3) / 1e12),
-            "unit": unit, "ms_per_step": tms}
+            "unit": unit, "ms_per_step": tms,
+            "ours_in_alternating_windows_ms_per_step": oms}
 
     out = {
         "metric": metric, "value": value, "unit": unit, "n_gpus": world,
