@@ -27,8 +27,9 @@
 //   full[s]        with a norm: this CTA's copies landed (its producer's
 //                  expect_tx); without: the leader's, on which both CTAs'
 //                  copies complete (cta_group::2 TMA) -- the MMA waits on it;
-//   ready[s]       leader, with a norm: each transform warp of both CTAs
-//                  arrives once its CTA's stage is normalized;
+//   ready[s, p]    leader, with a norm: each transform warp of both CTAs
+//                  arrives once column part p of its CTA's stage is
+//                  normalized (the MMAs of that part's K steps wait on it);
 //   empty[s]       the leader's tcgen05.commit, multicast to both CTAs;
 //   acc_full[a]    the leader's commit at the end of a tile, multicast;
 //   acc_empty[a]   leader: each draining warp of both CTAs arrives after
