@@ -111,6 +111,32 @@ def test_ops_dtypes_bias(op, dtype, M, K, N):
                       f"{op} {dtype} {M}x{K}x{N} bias={bias}")
 
 
+@pytest.mark.parametrize("M", [31, 32, 33, 127, 128, 129, 255, 256, 257, 513])
+def test_path_boundaries(M):
+    """Batch sizes on both sides of each kernel switch (decode up to 32 rows,
+    single-CTA tiles up to 128, 256-row CTA-pair tiles above), with K = 576
+    (nine 64-column stages) and N = 904 (a last output tile of 8 columns)."""
+    K, N = 576, 904
+    for op in ("layernorm_linear", "linear_silu"):
+        d = inputs.case(op, M, K, N, torch.float16, True, 1e-5, seed=M + 7,
+                        x_mean=2.0 if op == "layernorm_linear" else 0.0)
+        y = run_op(op, to_dev(d), 1e-5)
+        torch.cuda.synchronize()
+        assert_parity(y.double().cpu().numpy(), ref_op(op, d, 1e-5), f"{op} M={M}")
+
+
+def test_many_tiles_per_pair():
+    """4096 x 256 -> 2048: more output tiles than resident CTA pairs, so
+    each pair runs several tiles through its accumulators; every element."""
+    M, K, N = 4096, 256, 2048
+    d = inputs.case("rmsnorm_linear", M, K, N, torch.bfloat16, True, 1e-5, seed=4096)
+    y = run_op("rmsnorm_linear", to_dev(d), 1e-5)
+    torch.cuda.synchronize()
+    plan = B.tile_plan(B.OP_RMSNORM_LINEAR, M, K, N)
+    assert plan["pair"] == 1, plan
+    assert_parity(y.double().cpu().numpy(), ref_op("rmsnorm_linear", d, 1e-5), "4096x256x2048")
+
+
 @pytest.mark.parametrize("M", [1, 5, 40, 130])
 def test_ffn_small(M):
     K, F = 256, 520
