@@ -803,10 +803,12 @@ int linear_residual_norm(int norm, const void *x, const void *W, const void *bia
                       di, stream, nullptr, nullptr, -1, residual, true);
     event_after(stream);
     if (rc != NGR_OK) return rc;
-    // The norm over each h row (a plain launch: it reads the product's output).
+    // The norm over each h row, launched as a programmatic dependent of the
+    // product: its CTAs take the SMs the product leaves and wait for the
+    // product's grid before reading h.
     event_before(stream);
     rc = launch_rowstats(norm, bf16, H, M, N, eps, reinterpret_cast<float2 *>(w + L.stats), gamma,
-                         beta, nullptr, nullptr, nullptr, 0, nullptr, di.sms, stream, y);
+                         beta, nullptr, nullptr, nullptr, 0, nullptr, di.sms, stream, y, -1, true);
     event_after(stream);
     events_call_done();
     return finish(rc, ws, stream);

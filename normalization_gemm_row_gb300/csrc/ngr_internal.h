@@ -124,7 +124,7 @@ int launch_rowstats(int norm, bool bf16, const void *x, int64_t M, int64_t K,
                     const void *beta, float *gamma_f, float *beta_f,
                     int *counters, int n_counters, int *err_to_clear,
                     int num_sms, cudaStream_t stream, void *xhat = nullptr,
-                    int64_t k_valid = -1);
+                    int64_t k_valid = -1, bool pdl = false);
 
 // Copies for shapes whose K or N is not a multiple of 8 (ngr_pad.cu):
 // rows of `cols` 16-bit values (pitch `src_pitch`) into rows of `dst_cols`

@@ -147,6 +147,9 @@ __global__ void __launch_bounds__(kStatsThreads, XHAT ? 1 : kStatsCtasPerSm) row
     // The dependent GEMM may start its prologue while this grid runs; it
     // waits for this grid's completion before reading the statistics.
     pdl_launch_dependents();
+    // Launched as a dependent of the product that wrote x (the norm after a
+    // GEMM), wait for that grid; otherwise this returns at once.
+    pdl_wait();
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -302,7 +305,7 @@ int launch_rowstats(int norm, bool bf16, const void *x, int64_t M, int64_t K,
                     float eps, float2 *stats, const void *gamma,
                     const void *beta, float *gamma_f, float *beta_f,
                     int *counters, int n_counters, int *err_to_clear,
-                    int num_sms, cudaStream_t stream, void *xhat, int64_t k_valid)
+                    int num_sms, cudaStream_t stream, void *xhat, int64_t k_valid, bool pdl)
 {
     if (k_valid < 0) k_valid = K;
     const int threads = kStatsThreads;
@@ -315,15 +318,26 @@ int launch_rowstats(int norm, bool bf16, const void *x, int64_t M, int64_t K,
     const uint4 *xv = static_cast<const uint4 *>(x);
     dim3 grid(static_cast<unsigned>(blocks)), block(threads);
     uint4 *xh = static_cast<uint4 *>(xhat);
+    // As a programmatic dependent (pdl) the grid may be scheduled while the
+    // previous one finishes; the kernel waits for it before reading x.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
 #define NGR_STATS(N_, B_)                                                                     \
     if (xh)                                                                                   \
-        rowstats_kernel<N_, B_, true><<<grid, block, 0, stream>>>(                            \
-            xv, M, K, eps, stats, gamma, beta, gamma_f, beta_f, counters, n_counters,          \
-            err_to_clear, xh, k_valid);                                                                \
+        cudaLaunchKernelEx(&cfg, rowstats_kernel<N_, B_, true>, xv, M, K, eps, stats, gamma,  \
+                           beta, gamma_f, beta_f, counters, n_counters, err_to_clear, xh,     \
+                           k_valid);                                                          \
     else                                                                                      \
-        rowstats_kernel<N_, B_, false><<<grid, block, 0, stream>>>(                           \
-            xv, M, K, eps, stats, gamma, beta, gamma_f, beta_f, counters, n_counters,          \
-            err_to_clear, nullptr, k_valid);
+        cudaLaunchKernelEx(&cfg, rowstats_kernel<N_, B_, false>, xv, M, K, eps, stats, gamma, \
+                           beta, gamma_f, beta_f, counters, n_counters, err_to_clear,         \
+                           static_cast<uint4 *>(nullptr), k_valid);
     if (norm == kNormLayer) {
         if (bf16) { NGR_STATS(kNormLayer, true) } else { NGR_STATS(kNormLayer, false) }
     } else {
