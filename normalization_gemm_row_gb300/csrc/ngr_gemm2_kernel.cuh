@@ -53,6 +53,9 @@ namespace ngr {
 #define NGR_TRANSFORM_PARTS 2
 #endif
 constexpr int kMaxParts = 4;
+#ifndef NGR_RMS_RSTD_OUT
+#define NGR_RMS_RSTD_OUT 1
+#endif
 
 template <int BN, int STAGES, int NSUB>
 struct Gemm2Smem {
@@ -93,6 +96,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // that works on the stage, in each CTA (used with a norm only).
     constexpr uint32_t kReadyCount = 2 * kGroupWarps;
     constexpr int kParts = kNorm ? NGR_TRANSFORM_PARTS : 1;
+    // RMSNorm in bf16: the transform applies gamma only and the epilogue
+    // multiplies each row by its rstd (one multiply per element instead of
+    // two on the stage round trip).  bf16's range makes x * gamma safe; in
+    // fp16 it could overflow where x * rstd * gamma would not.
+    constexpr bool kRstdOut = NORM == kNormRms && BF16 && NGR_RMS_RSTD_OUT;
     static_assert(kParts >= 1 && kParts <= kMaxParts && (kBK / kUmmaK) % kParts == 0,
                   "whole K steps per transform part");
     static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "UMMA N for M = 256");
@@ -289,7 +297,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int t = threadIdx.x - kTransformWarp0 * 32;
             if constexpr (kNorm) {
                 // ----------------------------------------- transform (A in place)
-                transform_role<NORM, BF16, STAGES, L::kA, kParts>(
+                transform_role<NORM, BF16, STAGES, L::kA, kParts, !kRstdOut>(
                     t, cluster, n_clusters, num_units, [&](int u) { return unit_kb1(u) - unit_kb0(u); },
                     args.M, args.stats, sA, sG, full, wc,
                     [&](int u) { return (unit_tile(u) % m_tiles) * 2 * kBM + static_cast<int>(rank) * kBM; },
@@ -303,7 +311,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             int acc = 0;
             uint32_t acc_phase = 0;
             const int N = args.N;
-            if constexpr (is_fold(NORM)) pdl_wait();  // row statistics from the previous grid
+            if constexpr (is_fold(NORM) || kRstdOut) pdl_wait();  // row statistics from the previous grid
             for (int u = cluster; u < num_units; u += n_clusters) {
                 const int tile = unit_tile(u);
                 const int split = u % n_splits;
@@ -328,7 +336,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 if (!mbar_wait_warp(&acc_full[cur], cur_phase, wc)) break;
                 tc_fence_after();
                 const int row = (tile % m_tiles) * 2 * kBM + static_cast<int>(rank) * kBM + q * 32 + lane;
-                const float2 so = fold_row_scale<NORM>(args, row);
+                float2 so = fold_row_scale<NORM>(args, row);
+                if constexpr (kRstdOut) so = make_float2(row < args.M ? args.stats[row].y : 0.f, 0.f);
                 const uint32_t t_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                         static_cast<uint32_t>(cur * kTW);
                 if constexpr (GATED) {
@@ -342,8 +351,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         tmem_ld_wait();
                         float v[32];
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            v[j] = silu_f(__uint_as_float(rg[j])) * __uint_as_float(ru[j]);
+                        for (int j = 0; j < 32; ++j) {
+                            float gj = __uint_as_float(rg[j]), uj = __uint_as_float(ru[j]);
+                            if constexpr (kRstdOut) {
+                                gj *= so.x;
+                                uj *= so.x;
+                            }
+                            v[j] = silu_f(gj) * uj;
+                        }
                         store_row32<BF16>(v, row, nt0 + c, args.y, args.M, N);
                     }
                 } else if (n_splits > 1) {
@@ -397,7 +412,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                     for (int j = 0; j < 32; ++j) v[j] += __ldcg(o + j * 32);
                                 }
                             }
-                            epilogue_store32<NORM, BF16>(v, row, nt0 + c, args, so);
+                            epilogue_store32<NORM, BF16, kRstdOut>(v, row, nt0 + c, args, so);
                         }
                         __syncwarp();
                         // ready for the next call (every unit of these chunks has arrived)
@@ -418,7 +433,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
                         const int cn = c + step;
                         if (cn < ncols) tmem_ld32(t_base + static_cast<uint32_t>(cn), r);
-                        epilogue_store32<NORM, BF16>(v, row, nt0 + c, args, so);
+                        epilogue_store32<NORM, BF16, kRstdOut>(v, row, nt0 + c, args, so);
                         c = cn;
                     }
                 }

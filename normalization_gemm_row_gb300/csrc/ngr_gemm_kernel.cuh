@@ -180,11 +180,15 @@ __device__ __forceinline__ float2 unpack2(uint32_t w)
 // LayerNorm a = (x * rstd + (-mu * rstd)) * gamma + beta, RMSNorm
 // a = (x * rstd) * gamma; one rounding to the 16-bit type at the end.
 // so = (rstd, -mu * rstd) of the row; g[4], b[4] = gamma/beta pairs of the
-// 8 columns.
-template <int NORM, bool BF16>
+// 8 columns.  With ROW_SCALE false (RMSNorm only) the row's rstd is left to
+// the epilogue and a = x * gamma: rstd is a factor of the whole row, so
+// rstd * sum_k (x gamma)_k W_nk is the same product, and the rounding is one
+// rounding of a value of the same relative precision.
+template <int NORM, bool BF16, bool ROW_SCALE = true>
 __device__ __forceinline__ uint4 transform8_pk(uint4 v, float2 so, const float2 (&g)[4],
                                                const float2 (&b)[4])
 {
+    static_assert(ROW_SCALE || NORM == kNormRms, "only RMSNorm's scale factors out of the row");
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t o[4];
     const float2 sc = make_float2(so.x, so.x);
@@ -195,8 +199,10 @@ __device__ __forceinline__ uint4 transform8_pk(uint4 v, float2 so, const float2 
         float2 a;
         if constexpr (NORM == kNormLayer)
             a = __ffma2_rn(__ffma2_rn(f, sc, of), g[i], b[i]);
-        else
+        else if constexpr (ROW_SCALE)
             a = __fmul2_rn(__fmul2_rn(f, sc), g[i]);
+        else
+            a = __fmul2_rn(f, g[i]);
         o[i] = from_float2<BF16>(a.x, a.y);
     }
     return make_uint4(o[0], o[1], o[2], o[3]);
@@ -205,12 +211,17 @@ __device__ __forceinline__ uint4 transform8_pk(uint4 v, float2 so, const float2 
 // The epilogue of 32 accumulator columns [n0, n0 + 32) of one row: + bias,
 // or with a folded norm y = rstd acc + (-mu rstd) c[n] + b'[n] (so =
 // (rstd, -mu rstd) of the row), then the activation, + residual, rounding,
-// 16-byte stores.
-template <int NORM, bool BF16>
+// 16-byte stores.  With ROW_SCALE_OUT the accumulator is first multiplied
+// by so.x (the row's rstd, left out of an RMSNorm transform).
+template <int NORM, bool BF16, bool ROW_SCALE_OUT = false>
 __device__ __forceinline__ void epilogue_store32(float (&v)[32], int row, int n0,
                                                  const GemmArgs &args, float2 so)
 {
     const int M = args.M, N = args.N;
+    if constexpr (ROW_SCALE_OUT) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] *= so.x;
+    }
     if constexpr (is_fold(NORM)) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -293,8 +304,8 @@ __device__ __forceinline__ float2 fold_row_scale(const GemmArgs &args, int row)
 // After its stores each thread fences them for the async proxy.
 // m0_of(unit) gives the unit's first x row in this CTA and kb_count(unit)
 // the number of k blocks the unit covers (all of them unless K is split).
-template <int NORM, bool BF16, int STAGES, int KA, int PARTS = 1, typename M0Fn, typename KbFn,
-          typename ArriveFn>
+template <int NORM, bool BF16, int STAGES, int KA, int PARTS = 1, bool ROW_SCALE = true,
+          typename M0Fn, typename KbFn, typename ArriveFn>
 __device__ __forceinline__ void transform_role(int t, int tile0, int tile_step, int num_tiles,
                                                KbFn kb_count, int M, const float2 *stats,
                                                uint8_t *sA, const float *sG, uint64_t *full,
@@ -372,7 +383,7 @@ __device__ __forceinline__ void transform_role(int t, int tile0, int tile_step, 
 #pragma unroll
                         for (int i = 0; i < kBatch; ++i)
                             *reinterpret_cast<uint4 *>(base + (b0 + i) * kRowStride * 128) =
-                                transform8_pk<NORM, BF16>(v[i], so[b0 + i], gg, bb);
+                                transform8_pk<NORM, BF16, ROW_SCALE>(v[i], so[b0 + i], gg, bb);
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
