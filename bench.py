@@ -1,11 +1,17 @@
 """Benchmark of the fused pre-norm linear layer on GB300.
 
-One step = one fused LayerNorm + linear + bias call over one batch:
-x [1024, 8192] fp16 (the [8, 128, 8192] activations) against W [8192, 8192]
-with FP32 statistics and accumulation.  Prints ONE JSON line on rank 0.
+One step = one fused RMSNorm + linear call over one batch: x [512, 14336]
+fp16 with 1 % outlier rows against W [49152, 14336], FP32 statistics and
+accumulation (the largest norm + GEMM workload that fits one GPU).  The same
+JSON line carries, under "other_configs", the LayerNorm + linear + bias
+workload x [8, 128, 8192] against W [8192, 8192] in TFLOP/s and the
+decode-sized LayerNorm + linear + bias bf16 workload (K = 8192, N = 28672)
+at M = 1, 4 and 16 in HBM GB/s, each timed the same way with its own
+roofline and CPU-oracle baseline.  Prints ONE JSON line on rank 0.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME] [--no-cpu-baseline]
+                  [--workload NAME] [--m M] [--no-cpu-baseline]
+                  [--no-other-configs] [--no-alternatives]
 
 --impl reference times the fp64 CPU oracle (the reference arm of this
 build) on the host cores, each step a bounded sample of rows of the same
@@ -22,6 +28,7 @@ step finds its weights in L2.
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import math
@@ -41,7 +48,14 @@ import torch  # noqa: E402
 import torch.distributed as dist  # noqa: E402
 
 L2_BYTES = 129 * 2 ** 20
-DEFAULT_WORKLOAD = "ln_linear_bias_f16_m1024_k8192_n8192"
+DEFAULT_WORKLOAD = "rms_linear_f16_m512_k14336_n49152_outliers"
+# Measured in the same run as the default workload, reported under
+# "other_configs": (workload, M override).
+OTHER_CONFIGS = (("ln_linear_bias_f16_m1024_k8192_n8192", None),
+                 ("decode_ln_linear_bias_bf16_k8192_n28672", 1),
+                 ("decode_ln_linear_bias_bf16_k8192_n28672", 4),
+                 ("decode_ln_linear_bias_bf16_k8192_n28672", 16))
+METRIC = "fused LN/RMSNorm+GEMM TFLOP/s (% dense FP16 peak); HBM GB/s at M\u226416"
 PROFILES = os.path.join(ROOT, "profiles")
 
 
@@ -165,6 +179,19 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------
+LEAD_IN_MS = 3.0
+
+
+def lead_in(stream):
+    """Keep the GPU busy for a few milliseconds before a timed region starts,
+    so that the host has queued the first steps by the time the start event
+    is reached (otherwise the first step's launch latency on the host is
+    timed as GPU time).  The sleep precedes the start event: it is not
+    timed."""
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(LEAD_IN_MS * 1e-3 * 2.1e9))
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -278,7 +305,7 @@ def oracle_run(w, host, rows, lib):
                              host["Wu"], host["Wd"], w.eps, rows, lib)
 
 
-def our_arm(args, rank, world, local):
+def our_arm(args, rank, world, local, workload, m_override):
     import normalization_gemm_row_gb300 as ngr
     from normalization_gemm_row_gb300 import binding as B
     from normalization_gemm_row_gb300 import inputs
@@ -286,9 +313,9 @@ def our_arm(args, rank, world, local):
     ngr.build()
     dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
     torch.cuda.set_device(dev)
-    w = inputs.BY_NAME[args.workload]
-    if args.m is not None:
-        w = w.with_m(args.m)
+    w = inputs.BY_NAME[workload]
+    if m_override is not None:
+        w = w.with_m(m_override)
     M, K, N = w.M, w.K, w.N
     decode = M <= 32
     two_gemm = w.op in _TWO_GEMM
@@ -367,6 +394,7 @@ def our_arm(args, rank, world, local):
     barrier()
     torch.cuda.synchronize(dev)
     clocks.mark_start()
+    lead_in(stream)
     ev0.record(stream)
     for i in range(args.steps):
         step(sets[i % n_sets])
@@ -385,11 +413,12 @@ def our_arm(args, rank, world, local):
         algo_bytes += 2 * M * N * 2  # h written once and read once
     ms_step = ms_total_max / args.steps
     if decode:
-        metric, unit = "fused LN+GEMM HBM GB/s at M<=16 (decode)", "GB/s"
+        unit = "GB/s"
         value = job_value(algo_bytes * args.steps / 1e9, world, ms_total_max / 1e3)
     else:
-        metric, unit = "fused LN/RMSNorm+GEMM TFLOP/s (% dense FP16 peak)", "TFLOP/s"
+        unit = "TFLOP/s"
         value = job_value(flops * args.steps / 1e12, world, ms_total_max / 1e3)
+    metric = METRIC
 
     # ------------------------- dominant-kernel time (CUDA events per kernel)
     torch.cuda.synchronize(dev)
@@ -410,7 +439,7 @@ def our_arm(args, rank, world, local):
         roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = stored_traffic(w.name if args.m is None else f"{w.name}_m{M}")
+    roof["traffic"] = stored_traffic(w.name if m_override is None else f"{w.name}_m{M}")
     roof["peak_source"] = peaks["source"] + " (burst)"
     roof["kernel_ms"] = per_kernel[dom]
     roof["kernel_ms_all"] = per_kernel
@@ -430,6 +459,7 @@ def our_arm(args, rank, world, local):
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    lead_in(stream)
     e0.record(stream)
     for i in range(args.steps):
         s = sets[i % n_sets]
@@ -478,6 +508,7 @@ def our_arm(args, rank, world, local):
     barrier()
     p0 = torch.cuda.Event(enable_timing=True)
     p1 = torch.cuda.Event(enable_timing=True)
+    lead_in(s_in)
     p0.record(s_in)
     pipelined(args.steps)
     s_in.wait_stream(s_out)
@@ -521,6 +552,7 @@ def our_arm(args, rank, world, local):
         torch.cuda.synchronize(dev)
         f0 = torch.cuda.Event(enable_timing=True)
         f1 = torch.cuda.Event(enable_timing=True)
+        lead_in(stream)
         f0.record(stream)
         for i in range(args.steps):
             fstep(i)
@@ -548,6 +580,7 @@ def our_arm(args, rank, world, local):
         torch.cuda.synchronize(dev)
         w0 = torch.cuda.Event(enable_timing=True)
         w1 = torch.cuda.Event(enable_timing=True)
+        lead_in(stream)
         w0.record(stream)
         for i in range(args.steps):
             step(sets[0])
@@ -603,6 +636,7 @@ def our_arm(args, rank, world, local):
         def twindow():
             t0 = torch.cuda.Event(enable_timing=True)
             t1 = torch.cuda.Event(enable_timing=True)
+            lead_in(stream)
             t0.record(stream)
             for i in range(args.steps):
                 tstep(i)
@@ -613,6 +647,7 @@ def our_arm(args, rank, world, local):
         def owindow():
             o0 = torch.cuda.Event(enable_timing=True)
             o1 = torch.cuda.Event(enable_timing=True)
+            lead_in(stream)
             o0.record(stream)
             for i in range(args.steps):
                 step(sets[i % n_sets])
@@ -711,6 +746,7 @@ def reference_arm(args, rank):
         w = w.with_m(args.m)
     host = inputs.make(w)
     threads = oracle.num_threads(lib)
+    decode = w.M <= 32
     rows_per_step = max(1, min(w.M, args.ref_rows or threads))
 
     def step(i):
@@ -724,12 +760,16 @@ def reference_arm(args, rank):
     for i in range(args.steps):
         step(args.warmup + i)
     dt = time.perf_counter() - t
-    flops = w.flops / w.M * rows_per_step * args.steps
-    value = flops / dt / 1e12
-    unit = "TFLOP/s"
+    if decode:
+        # rows_per_step rows of the batch stream all of W once per step
+        nbytes = (w.N * w.K + w.M * w.K + w.M * w.N) * 2 * rows_per_step / w.M
+        value, unit = nbytes * args.steps / dt / 1e9, "GB/s"
+    else:
+        flops = w.flops / w.M * rows_per_step * args.steps
+        value, unit = flops / dt / 1e12, "TFLOP/s"
     return {
         "impl": "reference",
-        "metric": "fused LN/RMSNorm+GEMM TFLOP/s (% dense FP16 peak)", "value": value,
+        "metric": METRIC, "value": value,
         "unit": unit, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
@@ -752,6 +792,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-alternatives", action="store_true",
                     help="skip the inference-fold and unfused-torch comparison runs")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="measure only --workload (default: the default workload plus "
+                         "the LayerNorm and decode workloads under other_configs)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-rows", type=int, default=0)
     args = ap.parse_args(argv)
@@ -765,12 +808,26 @@ def main(argv=None):
             print(json.dumps(out), flush=True)
         return 0
 
-    out, w, host = our_arm(args, rank, world, local)
+    out, w, host = our_arm(args, rank, world, local, args.workload, args.m)
     if rank == 0:
-        if args.no_cpu_baseline:
-            out["cpu_baseline"] = None
-        else:
-            out["cpu_baseline"] = cpu_baseline(w, host, args.cpu_seconds)
+        out["cpu_baseline"] = None if args.no_cpu_baseline else cpu_baseline(w, host, args.cpu_seconds)
+    del host
+    if args.workload == DEFAULT_WORKLOAD and args.m is None and not args.no_other_configs:
+        others = {}
+        for name, m in OTHER_CONFIGS:
+            gc.collect()
+            torch.cuda.empty_cache()
+            o, w2, h2 = our_arm(args, rank, world, local, name, m)
+            if rank == 0:
+                o["cpu_baseline"] = (None if args.no_cpu_baseline
+                                     else cpu_baseline(w2, h2, args.cpu_seconds / 3))
+            del h2
+            for k in ("metric", "n_gpus", "steps", "warmup", "higher_is_better", "scaling",
+                      "vs_baseline", "data"):
+                o.pop(k, None)
+            others[name if m is None else f"{name}_m{m}"] = o
+        out["other_configs"] = others
+    if rank == 0:
         print(json.dumps(out), flush=True)
     if dist.is_available() and dist.is_initialized():
         dist.destroy_process_group()

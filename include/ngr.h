@@ -258,19 +258,30 @@ int ngr_fused_norm_linear_folded(int norm, const void *x, const void *Wf,
  * device memory and so cannot supply a workspace -- for example code running
  * where every device allocation is planned or owned by someone else, or an
  * embedding that can only pass input and output tensors.  It computes the
- * same y = LayerNorm(x) . W^T (+ bias) with the same arguments minus the
- * workspace.  The paper has no counterpart; this is a deployment variant.
+ * same y = LayerNorm(x) . W^T (+ bias; bias may be NULL) as
+ * ngr_fused_layernorm_linear, with the same arguments minus the workspace.
+ * The paper has no counterpart; this is a deployment variant.
+ *
+ * Unlike ngr_fused_layernorm_linear it makes no zero-padded copies (they
+ * would need scratch of the operands' size): K and N must be multiples of 8
+ * and x, gamma, beta, W, bias and y 16-byte aligned, else NGR_ERR_ALIGN.  It
+ * always runs the tile kernel without a K split, and never the decode
+ * kernel, so for small M or few output tiles it can be slower than the
+ * workspace entry point.
  *
  * Its scratch (per-row statistics, FP32 gamma/beta, the error word) is one
  * fixed array of about 256 KiB in the library's device memory, present on
  * every GPU that loads the library until the process exits.  The call
  * allocates nothing.  Limits: M <= NGR_NOALLOC_MAX_M and
- * K <= NGR_NOALLOC_MAX_K, else NGR_ERR_SHAPE.  The first call on each device
- * looks up the array's device address (cudaGetSymbolAddress), so make that
- * first call before any stream capture.  All calls share the one array, which
- * keeps the last call's contents; each call rewrites what it reads, but calls
- * that overlap on the GPU race on it and must not be issued.  Other
- * conventions as above. */
+ * K <= NGR_NOALLOC_MAX_K, else NGR_ERR_SHAPE.  The first call in each CUDA
+ * context looks up the array's device address (cudaGetSymbolAddress), so
+ * make that first call before any stream capture.  All calls share the one
+ * array, which keeps the last call's contents; each call rewrites what it
+ * reads, but calls that overlap on the GPU race on it and must not be
+ * issued.  Errors: argument checks and launch failures as for the other
+ * entry points; a kernel whose bounded wait ran out leaves its mark in the
+ * array's error word, which ngr_noalloc_error reads (with NGR_DEBUG=1 every
+ * call does that before returning). */
 #define NGR_NOALLOC_MAX_M 16384
 #define NGR_NOALLOC_MAX_K 16384
 int ngr_fused_layernorm_linear_noalloc(const void *x, const void *gamma,
@@ -278,6 +289,14 @@ int ngr_fused_layernorm_linear_noalloc(const void *x, const void *gamma,
                                        const void *bias, float eps, int64_t M,
                                        int64_t K, int64_t N, int dtype, void *y,
                                        ngr_stream_t stream);
+
+/* The error word of ngr_fused_layernorm_linear_noalloc, for callers without
+ * a workspace: synchronize `stream`, then return and clear the word kept in
+ * the library's fixed array (NGR_OK, or NGR_ERR_TIMEOUT when a kernel of
+ * the last call gave up on a bounded wait).  NGR_ERR_CUDA if the
+ * synchronization or the read fails.  Allocates nothing.  The paper has no
+ * counterpart. */
+int ngr_noalloc_error(ngr_stream_t stream);
 
 /* Step a1 alone: per-row FP32 statistics into stats[2*M] as (mu, rstd)
  * pairs.  norm: 1 = LayerNorm, 2 = RMSNorm (mu = 0).  [LNF] §1.1, §2.3.

@@ -52,6 +52,7 @@ SIGNATURES = {
     "ngr_fold_prepare": (_I, [_I, _P, _P, _P, _P, _I64, _I64, _I, _P, _P, _P]),
     "ngr_fused_norm_linear_folded": (_I, [_I, _P, _P, _P, _F, _I64, _I64, _I64, _I, _P, _P, _SZ, _P]),
     "ngr_workspace_error": (_I, [_P, _P]),
+    "ngr_noalloc_error": (_I, [_P]),
     "ngr_debug_bounded_wait": (_I, [_P, _U32, _P]),
     "ngr_status_string": (ctypes.c_char_p, [_I]),
     "ngr_version": (_I, []),
@@ -178,6 +179,10 @@ def ngr_row_stats(norm, x, eps, M, K, dtype, stats, stream) -> int:
 
 def ngr_workspace_error(ws, stream) -> int:
     return lib().ngr_workspace_error(ws, stream)
+
+
+def ngr_noalloc_error(stream) -> int:
+    return lib().ngr_noalloc_error(stream)
 
 
 def ngr_debug_bounded_wait(ws, timeout_us, stream) -> int:

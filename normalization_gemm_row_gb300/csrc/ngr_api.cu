@@ -229,6 +229,8 @@ int current_device_info(DevInfo *out)
     return d.arch_ok ? NGR_OK : NGR_ERR_ARCH;
 }
 
+}  // namespace
+
 // ------------------------------------------------------------ environment
 bool debug_mode()
 {
@@ -329,6 +331,8 @@ bool map_gb(CUtensorMap *m, const float *gamma_f, int64_t K, size_t row_stride)
     }
     return true;
 }
+
+namespace {
 
 // ------------------------------------------------------------- validation
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

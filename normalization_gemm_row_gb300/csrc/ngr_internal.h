@@ -118,6 +118,20 @@ size_t split_counter_bytes(int64_t num_tiles, int tw);
 // ngr_last_error).  Returns -7 (NGR_ERR_CUDA) for use in return statements.
 int record_cuda_error(const char *what, int code, const char *detail);
 
+// NGR_DEBUG set (and not "0"): every entry point synchronizes its stream
+// after launching and reports the device error word.
+bool debug_mode();
+// Bound on every in-kernel barrier wait: NGR_WAIT_TIMEOUT_MS, default 2 s.
+unsigned long long wait_timeout_ns();
+// Tensor maps (record the reason in ngr_last_error on failure):
+// row-major [rows, cols] 16-bit matrix, box {64 columns, box_rows rows},
+// 128-byte swizzle;
+bool map_2d(CUtensorMap *m, const void *ptr, bool bf16, int64_t rows, int64_t cols,
+            uint32_t box_rows);
+// FP32 gamma and beta as the two rows of a [2, K] matrix whose rows are
+// `row_stride` bytes apart, box {64 columns, 2 rows}, no swizzle.
+bool map_gb(CUtensorMap *m, const float *gamma_f, int64_t K, size_t row_stride);
+
 // Launchers (return 0 or a negative ngr_status).
 int launch_rowstats(int norm, bool bf16, const void *x, int64_t M, int64_t K,
                     float eps, float2 *stats, const void *gamma,

@@ -41,60 +41,73 @@ constexpr size_t kNaBytes = kNaHeader + kNaStats + 2 * kNaGB;
 // the device address comes from cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNaBytes];
 
-constexpr int kNaMaxDevices = 64;
-std::mutex g_na_mu;
-void *g_na_ptr[kNaMaxDevices] = {};
+// Device address of the scratch in the CUDA context current on this
+// thread, looked up once per context (the first call in a context does it,
+// with that context's device current) and kept for later calls.  The cache
+// is keyed on the context's process-unique ID, so a context created after a
+// cudaDeviceReset, or a caller's own non-primary context on the same device,
+// gets its own lookup instead of an address from a module instance that is
+// gone or different.
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
 
-// Device address of the scratch on the current device, looked up once per
-// device with that device current (the first call on a device does it).
+template <typename Fn>
+Fn driver_fn(const char *name, int version)
+{
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &p, version, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<Fn>(p);
+}
+
+struct CtxEntry {
+    unsigned long long id;
+    void *ptr;
+};
+constexpr int kNaMaxContexts = 64;
+std::mutex g_na_mu;
+CtxEntry g_na_cache[kNaMaxContexts] = {};
+int g_na_next = 0;
+
 int scratch_address(void **out)
 {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNaMaxDevices)
-        return NGR_ERR_CUDA;
+    static const CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent", 12000);
+    static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId", 12000);
+    if (!get_current || !get_id)
+        return record_cuda_error("cudaGetDriverEntryPointByVersion(cuCtxGetCurrent/cuCtxGetId)", 0, "");
     std::lock_guard<std::mutex> lock(g_na_mu);
-    if (!g_na_ptr[dev]) {
-        void *p = nullptr;
+    CUcontext ctx = nullptr;
+    CUresult r = get_current(&ctx);
+    if (r != CUDA_SUCCESS) return record_cuda_error("cuCtxGetCurrent", static_cast<int>(r), "");
+    void *p = nullptr;
+    if (!ctx) {
+        // No context yet on this thread: the symbol lookup brings up the
+        // current device's primary context.
         const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess || !p) return NGR_ERR_CUDA;
-        g_na_ptr[dev] = p;
+        if (e != cudaSuccess || !p)
+            return record_cuda_error("cudaGetSymbolAddress (no-alloc scratch)", e, cudaGetErrorString(e));
+        r = get_current(&ctx);
+        if (r != CUDA_SUCCESS || !ctx) return record_cuda_error("cuCtxGetCurrent", static_cast<int>(r), "");
     }
-    *out = g_na_ptr[dev];
+    unsigned long long id = 0;
+    r = get_id(ctx, &id);
+    if (r != CUDA_SUCCESS) return record_cuda_error("cuCtxGetId", static_cast<int>(r), "");
+    for (const CtxEntry &c : g_na_cache)
+        if (c.ptr && c.id == id) {
+            *out = c.ptr;
+            return NGR_OK;
+        }
+    if (!p) {
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p)
+            return record_cuda_error("cudaGetSymbolAddress (no-alloc scratch)", e, cudaGetErrorString(e));
+    }
+    g_na_cache[g_na_next] = CtxEntry{id, p};
+    g_na_next = (g_na_next + 1) % kNaMaxContexts;
+    *out = p;
     return NGR_OK;
-}
-
-using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                              const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                              const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeFn na_encode()
-{
-    static EncodeFn fn = [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                             cudaEnableDefault, &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            p = nullptr;
-        return reinterpret_cast<EncodeFn>(p);
-    }();
-    return fn;
-}
-
-bool na_map(CUtensorMap *m, CUtensorMapDataType t, void *ptr, uint64_t cols, uint64_t rows,
-            uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw)
-{
-    EncodeFn enc = na_encode();
-    if (!enc) return false;
-    cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {row_bytes};
-    cuuint32_t box[2] = {box_cols, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    return enc(m, t, 2, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-               sw == CU_TENSOR_MAP_SWIZZLE_NONE ? CU_TENSOR_MAP_L2_PROMOTION_NONE
-                                                : CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool al16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -147,14 +160,9 @@ extern "C" int ngr_fused_layernorm_linear_noalloc(const void *x, const void *gam
     GemmArgs a;
     std::memset(&a, 0, sizeof(a));
     const GemmPlan plan = plan_gemm(M, N, K, sms, true);
-    const CUtensorMapDataType t16 =
-        bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    if (!na_map(&a.map_a, t16, const_cast<void *>(x), K, M, K * 2, kBK, kBM,
-                CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !na_map(&a.map_b, t16, const_cast<void *>(W), K, N, K * 2, kBK,
-                static_cast<uint32_t>(plan.b_rows), CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !na_map(&a.map_gb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, gamma_f, K, 2, kNaGB, kBK, 2,
-                CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (!map_2d(&a.map_a, x, bf16, M, K, kBM) ||
+        !map_2d(&a.map_b, W, bf16, N, K, static_cast<uint32_t>(plan.b_rows)) ||
+        !map_gb(&a.map_gb, gamma_f, K, kNaGB))
         return NGR_ERR_CUDA;
     a.stats = stats;
     a.bias = bias;
@@ -168,11 +176,32 @@ extern "C" int ngr_fused_layernorm_linear_noalloc(const void *x, const void *gam
     a.n_tiles = static_cast<int>((N + plan.tw - 1) / plan.tw);
     a.k_blocks = static_cast<int>((K + kBK - 1) / kBK);
     a.num_tiles = a.m_tiles * a.n_tiles;
-    a.timeout_ns = 2000ull * 1000000ull;
+    a.timeout_ns = wait_timeout_ns();
     a.act = kActNone;
     a.k_splits = 1;   // no K split: the scratch holds no partials
     a.kb_per_split = a.k_blocks;
     rc = launch_gemm(kNormLayer, bf16, plan, a, true, stream);
     if (rc != NGR_OK) return rc;
-    return cudaGetLastError() == cudaSuccess ? NGR_OK : NGR_ERR_CUDA;
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return record_cuda_error("kernel launch (no-alloc)", e, cudaGetErrorString(e));
+    if (debug_mode()) return ngr_noalloc_error(stream_);
+    return NGR_OK;
+}
+
+extern "C" int ngr_noalloc_error(ngr_stream_t stream_)
+{
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    void *base = nullptr;
+    int rc = scratch_address(&base);
+    if (rc != NGR_OK) return rc;
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return record_cuda_error("cudaStreamSynchronize", e, cudaGetErrorString(e));
+    int v = 0;
+    e = cudaMemcpy(&v, base, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return record_cuda_error("cudaMemcpy (no-alloc error word)", e, cudaGetErrorString(e));
+    if (v != 0) {
+        e = cudaMemset(base, 0, sizeof(int));
+        if (e != cudaSuccess) return record_cuda_error("cudaMemset (no-alloc error word)", e, cudaGetErrorString(e));
+    }
+    return v == 0 ? NGR_OK : NGR_ERR_TIMEOUT;
 }
