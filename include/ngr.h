@@ -4,12 +4,12 @@
  *
  * The library computes a LayerNorm or RMSNorm row reduction whose normalized
  * rows feed a dense matrix product directly, with a bias and/or SiLU
- * epilogue.  For M > 32 the normalized activations exist only in on-chip
- * memory and are never written to device memory.  For decode-sized batches
- * (M <= 32) the statistics kernel writes them once into the workspace (at
- * most 32 x K values, which stay in L2) and the weight-streaming kernel
- * reads them there, instead of re-normalizing the same rows for every
- * weight tile.
+ * epilogue.  The normalized activations exist only in on-chip memory and
+ * are never written to device memory: for M > 32 each tile of x is
+ * normalized in shared memory on its way to the tensor core; for
+ * decode-sized batches (M <= 32) each CTA of the weight-streaming kernel
+ * normalizes its slice of the tokens in shared memory once and streams its
+ * weight tiles against it.
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -20,17 +20,20 @@
  *    beta are [K]; bias is [N]; y is [M, N].  Every tensor has the element
  *    type `dtype` (NGR_F16 or NGR_BF16).  Statistics, the normalization and
  *    the accumulation are FP32; y is rounded to nearest-even once.
- *  - Alignment: K % 8 == 0 and N % 8 == 0 (16-byte row pitch), every pointer
- *    16-byte aligned, the workspace 256-byte aligned.  M is arbitrary
- *    (M == 0 is a no-op that returns NGR_OK).  The single-layer entry
- *    points (ngr_fused_layernorm_linear, ngr_fused_rmsnorm_linear,
- *    ngr_fused_linear_silu, ngr_fused_norm_linear_act) also take any K and
- *    N: when either is not a multiple of 8 they copy x, W, gamma, beta and
- *    bias into the workspace with rows padded by zeros to a multiple of 8,
- *    run the aligned kernels and copy the real columns of y out
- *    ([MMF] §五 optimization 1: a 513 x 14337 activation).  ngr_workspace_bytes
- *    includes those copies; W is copied on every such call.  Pointers then
- *    need only 2-byte alignment (y 16-byte when N % 8 == 0).
+ *  - Alignment: the kernels read rows of a 16-byte pitch, so when K and N
+ *    (F for the chains) are multiples of 8 every pointer must be 16-byte
+ *    aligned.  Every entry point also takes any K and N (F): when one is not
+ *    a multiple of 8 it copies its operands into the workspace with rows
+ *    padded by zeros to a multiple of 8 (weights also get zero rows up to a
+ *    multiple of 8), runs the aligned kernels with statistics over the real
+ *    columns only, and copies the real columns of its outputs back
+ *    ([MMF] §五 optimization 1: a 513 x 14337 activation).  Pointers then
+ *    need only 2-byte alignment (for the single-layer entry points y needs
+ *    16 bytes when N % 8 == 0), ngr_workspace_bytes includes the copies and
+ *    the weights are copied on every such call.  The folded layer is the
+ *    exception: its weight is prepared once in the padded layout (see
+ *    ngr_fold_prepare).  The workspace is 256-byte aligned.  M is arbitrary
+ *    (M == 0 is a no-op that returns NGR_OK).
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *    stream) and is asynchronous: the call returns once the kernels are
  *    launched.  Argument errors are detected before anything is launched and
@@ -153,7 +156,7 @@ int ngr_fused_linear_silu(const void *x, const void *W, const void *bias,
 /* FFN chain: H = SiLU(x . W1^T) [M, F], y = H . W2^T [M, K].
  * W1 is [F, K], W2 is [K, F].  H is written to device memory exactly once
  * and read once: into `h` ([M, F], dtype) when non-NULL, else into the
- * workspace (size it with ffn_h_in_workspace = 1).  F % 8 == 0.
+ * workspace (size it with ffn_h_in_workspace = 1).
  * [MMF] §二 strategy 2 (fused_matmul_silu_matmul(x, w1.T, w2.T)). */
 int ngr_ffn_linear_silu_linear(const void *x, const void *W1, const void *W2,
                                int64_t M, int64_t K, int64_t F, int dtype,
@@ -230,12 +233,17 @@ int ngr_fused_linear_residual_norm(int norm, const void *x, const void *W,
 
 /* Inference-mode weight fold, step 1 of 2 ([LNF] §6.2: with gamma and beta
  * fixed, gamma is folded into the matmul weight once, ahead of the calls).
- * norm: 1 = LayerNorm, 2 = RMSNorm (beta ignored, may be NULL).  Writes
- *   Wf[n,k] = gamma[k] W[n,k] rounded to `dtype`           ([N, K], dtype),
- *   cb[n]     = c[n]  = sum_k Wf[n,k] (from the rounded Wf)   (FP32),
- *   cb[N + n] = b'[n] = sum_k beta[k] W[n,k] + bias[n]      (FP32),
- * so cb is FP32 [2, N].  bias may be NULL.  All pointers are device memory,
- * 16-byte aligned; K % 8 == 0, N % 8 == 0.  Reads W once, writes Wf once. */
+ * norm: 1 = LayerNorm, 2 = RMSNorm (beta ignored, may be NULL).  With K8,
+ * N8 = K, N rounded up to multiples of 8 (K8 = K, N8 = N when aligned), it
+ * writes
+ *   Wf[n,k]    = gamma[k] W[n,k] rounded to `dtype`   ([N, K8] rows, dtype;
+ *                columns K..K8 zero),
+ *   cb[n]      = c[n]  = sum_k Wf[n,k] (from the rounded Wf)   (FP32),
+ *   cb[N8 + n] = b'[n] = sum_k beta[k] W[n,k] + bias[n]      (FP32),
+ * so cb is FP32 [2, N8] (zero past N).  bias may be NULL.  Wf and cb must be
+ * 16-byte aligned, the other pointers 2-byte aligned (16-byte aligned and
+ * K, N multiples of 8 select the vectorized kernel).  Reads W once, writes
+ * Wf once. */
 int ngr_fold_prepare(int norm, const void *gamma, const void *beta,
                      const void *W, const void *bias, int64_t K, int64_t N,
                      int dtype, void *Wf, float *cb, ngr_stream_t stream);
@@ -245,8 +253,9 @@ int ngr_fold_prepare(int norm, const void *gamma, const void *beta,
  * (norm = 2), from the folded weight:
  *   y[i,n] = rstd_i (x[i,:] . Wf[n,:]) - rstd_i mu_i c[n] + b'[n]
  * (RMSNorm: mu = 0), mu and rstd the FP32 row statistics of x.  The matrix
- * product runs on raw x; no normalized operand exists at all.  Workspace as
- * for the unfolded op (ngr_workspace_bytes of NGR_OP_LAYERNORM_LINEAR or
+ * product runs on raw x; no normalized operand exists at all.  Wf and cb
+ * are in ngr_fold_prepare's layout ([N, K8], [2, N8]).  Workspace as for the
+ * unfolded op (ngr_workspace_bytes of NGR_OP_LAYERNORM_LINEAR or
  * NGR_OP_RMSNORM_LINEAR).  [LNF] §6.2. */
 int ngr_fused_norm_linear_folded(int norm, const void *x, const void *Wf,
                                  const float *cb, float eps, int64_t M,

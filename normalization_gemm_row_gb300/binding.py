@@ -475,11 +475,13 @@ def fused_linear_residual_norm(x, W, gamma, norm: int = NORM_RMS, beta=None, bia
 
 def fold_prepare(norm: int, gamma, beta, W, bias=None, stream=None):
     """Inference-mode fold of gamma (and beta, bias) into the weight:
-    returns (Wf [N, K] in W's dtype, cb float32 [2, N] = (c, b'))."""
+    returns (Wf [N, K8] in W's dtype, cb float32 [2, N8] = (c, b')), with
+    K8, N8 = K, N rounded up to multiples of 8 (zero padding)."""
     N, K = W.shape
     _check(gamma, beta, W, bias, dtype=W.dtype)
-    Wf = torch.empty_like(W)
-    cb = torch.empty((2, N), dtype=torch.float32, device=W.device)
+    K8, N8 = (K + 7) // 8 * 8, (N + 7) // 8 * 8
+    Wf = torch.empty((N, K8), dtype=W.dtype, device=W.device)
+    cb = torch.empty((2, N8), dtype=torch.float32, device=W.device)
     rc = ngr_fold_prepare(norm, _ptr(gamma), _ptr(beta), _ptr(W), _ptr(bias), K, N,
                           _dtype_code(W), _ptr(Wf), _ptr(cb), _stream(stream))
     _raise(rc, "fold_prepare")
@@ -494,8 +496,10 @@ def fused_norm_linear_folded(norm: int, x, Wf, cb, eps, out=None, workspace=None
     x2 = x.reshape(-1, K)
     M = x2.shape[0]
     _check(x2, Wf, out, dtype=x.dtype)
+    if Wf.shape[1] != (K + 7) // 8 * 8:
+        raise ValueError("Wf must be [N, K8] as fold_prepare returns it")
     if cb.dtype != torch.float32 or not cb.is_cuda or not cb.is_contiguous():
-        raise TypeError("cb must be a contiguous float32 CUDA tensor [2, N]")
+        raise TypeError("cb must be a contiguous float32 CUDA tensor [2, N8]")
     y = out if out is not None else torch.empty((M, N), dtype=x.dtype, device=x.device)
     op = OP_LAYERNORM_LINEAR if norm == 1 else OP_RMSNORM_LINEAR
     ws = _workspace(ngr_workspace_bytes(op, M, K, N), x.device, workspace)

@@ -9,6 +9,7 @@
 #include <cstdlib>
 #include <cstdio>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 #include <vector>
 
@@ -66,7 +67,7 @@ constexpr int kMaxDevices = 64;
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
 struct WsLayout {
-    size_t stats = 0, gamma_f = 0, beta_f = 0, xhat = 0;
+    size_t stats = 0, gamma_f = 0, beta_f = 0;
     // padded copies (single-layer ops with K or N not a multiple of 8)
     size_t xp = 0, wp = 0, gp = 0, bp = 0, biasp = 0, yp = 0;
     bool padded = false;
@@ -136,10 +137,6 @@ WsLayout ws_layout(int op, int64_t M, int64_t K_, int64_t N_, bool h_in_ws)
         off += align256(static_cast<size_t>(K) * 4);
         L.beta_f = off;
         off += align256(static_cast<size_t>(K) * 4);
-        if (decode && !gated) {
-            L.xhat = off;
-            off += align256(static_cast<size_t>(M) * static_cast<size_t>(K) * 2);
-        }
     }
     if (decode) {
         const int64_t mn = M <= 16 ? 16 : 32;
@@ -147,7 +144,7 @@ WsLayout ws_layout(int op, int64_t M, int64_t K_, int64_t N_, bool h_in_ws)
         const int64_t tiles2 = chain ? ceil_div(K, 128) : 0;
         const int64_t tmax = tiles1 > tiles2 ? tiles1 : tiles2;
         L.partials = off;
-        off += align256(static_cast<size_t>(tmax) * kDecodeMaxContrib * mn * 128 * 4);
+        off += align256(static_cast<size_t>(tmax) * kDecodeMaxGroups * mn * 128 * 4);
         L.counters = off;
         off += align256(static_cast<size_t>(tiles1) * 4 * 4);
         L.counters2 = off;
@@ -394,8 +391,9 @@ int launch_layer(int norm, int act, bool bf16, const void *x, const void *W,
         const int mn = M <= 16 ? 16 : 32;
         if (!map_2d(&d.map_w, W, bf16, w_rows, K, 128) || !map_2d(&d.map_x, x, bf16, M, K, mn))
             return NGR_ERR_CUDA;
-        if (has_norm && !map_gb(&d.map_gb, gf, K, L.beta_f - L.gamma_f)) return NGR_ERR_CUDA;
         d.stats = stats;
+        d.gamma_f = gf;
+        d.beta_f = norm == kNormLayer ? reinterpret_cast<float *>(ws + L.beta_f) : nullptr;
         d.bias = bias;
         d.fold_c = fold_c;
         d.fold_b = fold_b;
@@ -410,12 +408,14 @@ int launch_layer(int norm, int act, bool bf16, const void *x, const void *W,
         d.K = static_cast<int>(K);
         d.n_tiles = static_cast<int>(ceil_div(N, 128));
         d.k_blocks = static_cast<int>(ceil_div(K, kBK));
-        d.units = static_cast<long long>(d.n_tiles) * d.k_blocks;
-        d.grid = plan_decode_grid(d.n_tiles, d.k_blocks, di.sms);
+        const DecodePlan dp = plan_decode(d.n_tiles, d.k_blocks, mn, di.sms);
+        d.k_groups = dp.k_groups;
+        d.kb_per_group = dp.kb_per_group;
+        d.n_groups = dp.n_groups;
         if (trace_mode())
-            std::fprintf(stderr, "ngr: decode kernel M=%lld N=%lld K=%lld MN=%d grid=%d units=%lld\n",
+            std::fprintf(stderr, "ngr: decode kernel M=%lld N=%lld K=%lld norm=%d MN=%d grid=%d x %d (k blocks per group %d)\n",
                          static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(K),
-                         mn, d.grid, d.units);
+                         norm, mn, dp.k_groups, dp.n_groups, dp.kb_per_group);
         d.timeout_ns = wait_timeout_ns();
         d.act = act;
         return launch_decode(norm, bf16, mn, d, pdl, stream);
@@ -565,19 +565,13 @@ int norm_linear(int op, int norm, int act, const void *x, const void *gamma, con
                                                 : (norm == kNormRms ? reinterpret_cast<float *>(w + L.beta_f) : nullptr),
                              decode ? reinterpret_cast<int *>(w + L.counters) : nullptr,
                              decode ? static_cast<int>(ceil_div(N8, 128) * 4) : 0,
-                             reinterpret_cast<int *>(w), di.sms, stream,
-                             decode && norm != kNormNone ? w + L.xhat : nullptr, K);
+                             reinterpret_cast<int *>(w), di.sms, stream, nullptr, K);
         event_after(stream);
         if (rc != NGR_OK) return rc;
     }
     event_before(stream);
-    // Decode sizes multiply the normalized rows the statistics kernel wrote.
-    if (decode && norm != kNormNone)
-        rc = launch_layer(kNormNone, act, bf16, w + L.xhat, Wa, biasa, M, K8, N8, ya, w, L,
-                          L.counters, true, di, stream, nullptr, nullptr, N, nullptr, true);
-    else
-        rc = launch_layer(norm, act, bf16, xa, Wa, biasa, M, K8, N8, ya, w, L, L.counters,
-                          need_stats, di, stream, nullptr, nullptr, N, nullptr, true);
+    rc = launch_layer(norm, act, bf16, xa, Wa, biasa, M, K8, N8, ya, w, L, L.counters, need_stats,
+                      di, stream, nullptr, nullptr, N, nullptr, true);
     event_after(stream);
     if (rc == NGR_OK && ya != y) rc = launch_unpad_rows(ya, M, N, N8, y, di.sms, stream);
     events_call_done();
@@ -591,39 +585,57 @@ int folded_linear(int norm, const void *x, const void *Wf, const float *cb, floa
                   size_t ws_bytes, cudaStream_t stream)
 {
     if (norm != kNormLayer && norm != kNormRms) return NGR_ERR_ARG;
-    int rc = check_sizes(M, K, N, dtype);
-    if (rc != NGR_OK) return rc;
+    if (dtype != NGR_F16 && dtype != NGR_BF16) return NGR_ERR_DTYPE;
+    if (M < 0 || K <= 0 || N <= 0 || M >= kMaxDim || K >= kMaxDim || N >= kMaxDim)
+        return NGR_ERR_SHAPE;
     if (M == 0) return NGR_OK;
     if (!x || !Wf || !cb || !y) return NGR_ERR_NULL;
     if (!ws) return NGR_ERR_WORKSPACE;
-    if (!aligned16(x) || !aligned16(Wf) || !aligned16(cb) || !aligned16(y)) return NGR_ERR_ALIGN;
+    // Wf and cb come from ngr_fold_prepare: [N, K8] rows and [2, N8].  x and y
+    // go through zero-padded copies when K or N is not a multiple of 8.
+    const bool pad = K % 8 != 0 || N % 8 != 0;
+    if (!aligned16(Wf) || !aligned16(cb)) return NGR_ERR_ALIGN;
+    if (pad ? (!aligned2(x) || !aligned2(y)) : (!aligned16(x) || !aligned16(y)))
+        return NGR_ERR_ALIGN;
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return NGR_ERR_ALIGN;
     const WsLayout L = ws_layout(norm == kNormLayer ? NGR_OP_LAYERNORM_LINEAR : NGR_OP_RMSNORM_LINEAR,
                                  M, K, N, false);
     if (ws_bytes < L.total) return NGR_ERR_WORKSPACE;
     DevInfo di;
-    rc = current_device_info(&di);
+    int rc = current_device_info(&di);
     if (rc != NGR_OK) return rc;
     const bool bf16 = dtype == NGR_BF16;
     char *w = static_cast<char *>(ws);
     if (debug_mode() && cudaMemsetAsync(w, 0, 4, stream) != cudaSuccess) return NGR_ERR_CUDA;
+    const int64_t K8 = round8(K), N8 = round8(N);
+    const void *xa = x;
+    void *ya = y;
+    if (pad) {
+        if (K8 != K || !aligned16(x)) {
+            rc = launch_pad_rows(x, M, K, K, w + L.xp, K8, di.sms, stream);
+            if (rc != 0) return rc;
+            xa = w + L.xp;
+        }
+        if (N8 != N || !aligned16(y)) ya = w + L.yp;
+    }
     const bool decode = M <= kDecodeMaxM;
     rc = zero_split_counters(L, w, stream);
     if (rc != NGR_OK) return rc;
     events_reset();
     event_before(stream);
-    rc = launch_rowstats(norm, bf16, x, M, K, eps, reinterpret_cast<float2 *>(w + L.stats), nullptr,
+    rc = launch_rowstats(norm, bf16, xa, M, K8, eps, reinterpret_cast<float2 *>(w + L.stats), nullptr,
                          nullptr, nullptr, nullptr,
                          decode ? reinterpret_cast<int *>(w + L.counters) : nullptr,
-                         decode ? static_cast<int>(ceil_div(N, 128) * 4) : 0,
-                         reinterpret_cast<int *>(w), di.sms, stream);
+                         decode ? static_cast<int>(ceil_div(N8, 128) * 4) : 0,
+                         reinterpret_cast<int *>(w), di.sms, stream, nullptr, K);
     event_after(stream);
     if (rc != NGR_OK) return rc;
     event_before(stream);
-    rc = launch_layer(norm == kNormLayer ? kNormFoldLayer : kNormFoldRms, kActNone, bf16, x, Wf,
-                      nullptr, M, K, N, y, w, L, L.counters, true, di, stream, cb, cb + N, -1,
+    rc = launch_layer(norm == kNormLayer ? kNormFoldLayer : kNormFoldRms, kActNone, bf16, xa, Wf,
+                      nullptr, M, K8, N8, ya, w, L, L.counters, true, di, stream, cb, cb + N8, N,
                       nullptr, true);
     event_after(stream);
+    if (rc == NGR_OK && ya != y) rc = launch_unpad_rows(ya, M, N, N8, y, di.sms, stream);
     events_call_done();
     return finish(rc, ws, stream);
 }
@@ -635,7 +647,7 @@ int folded_linear(int norm, const void *x, const void *Wf, const float *cb, floa
 int mlp_chain(int op, int norm, int act, const void *x, const void *gamma, const void *beta,
               const void *W1, const void *b1, const void *W2, const void *b2, float eps,
               int64_t M, int64_t K, int64_t F, int dtype, void *h, void *y, void *ws,
-              size_t ws_bytes, cudaStream_t stream)
+              size_t ws_bytes, cudaStream_t stream, int64_t k_valid = -1)
 {
     int rc = check_sizes(M, K, F, dtype);
     if (rc != NGR_OK) return rc;
@@ -675,18 +687,13 @@ int mlp_chain(int op, int norm, int act, const void *x, const void *gamma, const
                              norm == kNormNone ? nullptr : reinterpret_cast<float *>(w + L.gamma_f),
                              norm == kNormNone ? nullptr : reinterpret_cast<float *>(w + L.beta_f),
                              decode ? reinterpret_cast<int *>(w + L.counters) : nullptr, n_counters,
-                             reinterpret_cast<int *>(w), di.sms, stream,
-                             decode && norm != kNormNone ? w + L.xhat : nullptr);
+                             reinterpret_cast<int *>(w), di.sms, stream, nullptr, k_valid);
         event_after(stream);
         if (rc != NGR_OK) return rc;
     }
     event_before(stream);
-    if (decode && norm != kNormNone)
-        rc = launch_layer(kNormNone, act, bf16, w + L.xhat, W1, b1, M, K, F, H, w, L, L.counters,
-                          true, di, stream);
-    else
-        rc = launch_layer(norm, act, bf16, x, W1, b1, M, K, F, H, w, L, L.counters, need_stats, di,
-                          stream);
+    rc = launch_layer(norm, act, bf16, x, W1, b1, M, K, F, H, w, L, L.counters, need_stats, di,
+                      stream);
     event_after(stream);
     if (rc != NGR_OK) return rc;
     event_before(stream);
@@ -702,7 +709,7 @@ int mlp_chain(int op, int norm, int act, const void *x, const void *gamma, const
 int swiglu_chain(int op, int norm, const void *x, const void *gamma, const void *beta,
                  const void *Wg, const void *Wu, const void *Wd, float eps, int64_t M, int64_t K,
                  int64_t F, int dtype, void *h, void *y, void *ws, size_t ws_bytes,
-                 cudaStream_t stream)
+                 cudaStream_t stream, int64_t k_valid = -1)
 {
     const bool down = op == NGR_OP_MLP_SWIGLU;
     int rc = check_sizes(M, K, F, dtype);
@@ -741,7 +748,7 @@ int swiglu_chain(int op, int norm, const void *x, const void *gamma, const void 
                              norm == kNormNone ? nullptr : reinterpret_cast<float *>(w + L.beta_f),
                              down && decode ? reinterpret_cast<int *>(w + L.counters2) : nullptr,
                              down && decode ? static_cast<int>(ceil_div(K, 128) * 4) : 0,
-                             reinterpret_cast<int *>(w), di.sms, stream);
+                             reinterpret_cast<int *>(w), di.sms, stream, nullptr, k_valid);
         event_after(stream);
         if (rc != NGR_OK) return rc;
     }
@@ -766,7 +773,7 @@ int swiglu_chain(int op, int norm, const void *x, const void *gamma, const void 
 int linear_residual_norm(int norm, const void *x, const void *W, const void *bias,
                          const void *residual, const void *gamma, const void *beta, float eps,
                          int64_t M, int64_t K, int64_t N, int dtype, void *h, void *y, void *ws,
-                         size_t ws_bytes, cudaStream_t stream)
+                         size_t ws_bytes, cudaStream_t stream, int64_t n_valid = -1)
 {
     if (norm != kNormLayer && norm != kNormRms) return NGR_ERR_ARG;
     int rc = check_sizes(M, K, N, dtype);
@@ -812,10 +819,229 @@ int linear_residual_norm(int norm, const void *x, const void *W, const void *bia
     // product's grid before reading h.
     event_before(stream);
     rc = launch_rowstats(norm, bf16, H, M, N, eps, reinterpret_cast<float2 *>(w + L.stats), gamma,
-                         beta, nullptr, nullptr, nullptr, 0, nullptr, di.sms, stream, y, -1, true);
+                         beta, nullptr, nullptr, nullptr, 0, nullptr, di.sms, stream, y, n_valid, true);
     event_after(stream);
     events_call_done();
     return finish(rc, ws, stream);
+}
+
+// ---------------------------------------------- any K and N for the chains
+// The chains, SwiGLU and the post-GEMM norm take any K and N (F) the same
+// way the single layer does ("昇腾CANN的MatMul融合玩法，让大模型推理快3倍",
+// §五 optimization 1): every operand is copied into rows padded with zeros
+// to a multiple of 8 elements (weights also get zero rows up to a multiple
+// of 8), the aligned implementation runs on the padded problem with its
+// statistics counting only the real columns, and the real columns of the
+// outputs are copied back.  Zero weight rows and zero biases make the padded
+// hidden units act(0) = 0 (SiLU, ReLU, GELU and SiLU-gating all map 0 to
+// 0), and their zero weight columns in the next product add nothing.  The
+// copies follow the aligned implementation's own workspace regions.
+
+bool chain_op(int op)
+{
+    return op == NGR_OP_FFN || op == NGR_OP_MLP || op == NGR_OP_SWIGLU ||
+           op == NGR_OP_MLP_SWIGLU || op == NGR_OP_LINEAR_RESIDUAL_NORM;
+}
+
+bool needs_pad(int op, int64_t K, int64_t N)
+{
+    return chain_op(op) && (K % 8 != 0 || N % 8 != 0);
+}
+
+// The padded copies of a chain op, in workspace order (each 256-byte
+// aligned), after ws_layout(op, M, K8, N8, h_in_ws).
+struct PadRegions {
+    size_t x = 0, g = 0, b = 0, w1 = 0, b1 = 0, w2 = 0, b2 = 0, w3 = 0, res = 0, h = 0, y = 0;
+    size_t total = 0;
+};
+
+PadRegions pad_regions(int op, int64_t M, int64_t K, int64_t N, bool h_in_ws, size_t base)
+{
+    PadRegions R;
+    const size_t K8 = static_cast<size_t>(round8(K)), N8 = static_cast<size_t>(round8(N));
+    const size_t m = static_cast<size_t>(M);
+    size_t off = base;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off += align256(bytes);
+        return at;
+    };
+    const bool post = op == NGR_OP_LINEAR_RESIDUAL_NORM;
+    R.x = take(m * K8 * 2);
+    if (post) {
+        R.w1 = take(N8 * K8 * 2);   // W
+        R.b1 = take(N8 * 2);        // bias
+        R.res = take(m * N8 * 2);   // residual
+        R.g = take(N8 * 2);
+        R.b = take(N8 * 2);
+        R.y = take(m * N8 * 2);
+        if (!h_in_ws) R.h = take(m * N8 * 2);
+    } else {
+        R.g = take(K8 * 2);
+        R.b = take(K8 * 2);
+        R.w1 = take(N8 * K8 * 2);   // W1 or W_gate
+        if (op == NGR_OP_SWIGLU || op == NGR_OP_MLP_SWIGLU) {
+            R.w3 = take(N8 * K8 * 2);   // W_up
+        } else {
+            R.b1 = take(N8 * 2);
+            R.b2 = take(K8 * 2);
+        }
+        if (op != NGR_OP_SWIGLU) {
+            R.w2 = take(K8 * N8 * 2);   // W2 or W_down
+            R.y = take(m * K8 * 2);
+        }
+        if (op == NGR_OP_SWIGLU || !h_in_ws) R.h = take(m * N8 * 2);
+    }
+    R.total = off;
+    return R;
+}
+
+// Workspace bytes of any op at any K and N.
+size_t ws_total(int op, int64_t M, int64_t K, int64_t N, bool h_in_ws)
+{
+    if (!needs_pad(op, K, N)) return ws_layout(op, M, K, N, h_in_ws).total;
+    const size_t inner = ws_layout(op, M, round8(K), round8(N), h_in_ws).total;
+    return pad_regions(op, M, K, N, h_in_ws, inner).total;
+}
+
+// Checks shared by the padded wrappers: sizes, dtype, 2-byte pointers,
+// the workspace; fills *inner and *R.
+int pad_prologue(int op, int64_t M, int64_t K, int64_t N, int dtype, bool h_in_ws, void *ws,
+                 size_t ws_bytes, std::initializer_list<const void *> ptrs, size_t *inner,
+                 PadRegions *R, DevInfo *di)
+{
+    if (dtype != NGR_F16 && dtype != NGR_BF16) return NGR_ERR_DTYPE;
+    if (M < 0 || K <= 0 || N <= 0 || M >= kMaxDim || K >= kMaxDim || N >= kMaxDim)
+        return NGR_ERR_SHAPE;
+    if (!ws) return NGR_ERR_WORKSPACE;
+    for (const void *p : ptrs)
+        if (p && !aligned2(p)) return NGR_ERR_ALIGN;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return NGR_ERR_ALIGN;
+    *inner = ws_layout(op, M, round8(K), round8(N), h_in_ws).total;
+    *R = pad_regions(op, M, K, N, h_in_ws, *inner);
+    if (ws_bytes < R->total) return NGR_ERR_WORKSPACE;
+    return current_device_info(di);
+}
+
+// Copy a [rows, cols] operand (nullptr stays nullptr) into the workspace at
+// `off` as [rows8, round8(cols)] with zero padding.
+int pad_in(const void *src, int64_t rows, int64_t cols, int64_t rows8, char *ws, size_t off,
+           const void **out, const DevInfo &di, cudaStream_t stream)
+{
+    if (!src) {
+        *out = nullptr;
+        return NGR_OK;
+    }
+    *out = ws + off;
+    return launch_pad_rows(src, rows, cols, cols, ws + off, round8(cols), di.sms, stream, rows8);
+}
+
+int mlp_chain_any(int op, int norm, int act, const void *x, const void *gamma, const void *beta,
+                  const void *W1, const void *b1, const void *W2, const void *b2, float eps,
+                  int64_t M, int64_t K, int64_t F, int dtype, void *h, void *y, void *ws,
+                  size_t ws_bytes, cudaStream_t stream)
+{
+    if (!needs_pad(op, K, F))
+        return mlp_chain(op, norm, act, x, gamma, beta, W1, b1, W2, b2, eps, M, K, F, dtype, h, y,
+                         ws, ws_bytes, stream);
+    if (!x || !W1 || !W2 || !y) return NGR_ERR_NULL;
+    if (norm != kNormNone && !gamma) return NGR_ERR_NULL;
+    if (norm == kNormLayer && !beta) return NGR_ERR_NULL;
+    size_t inner = 0;
+    PadRegions R;
+    DevInfo di;
+    int rc = pad_prologue(op, M, K, F, dtype, h == nullptr, ws, ws_bytes,
+                          {x, gamma, beta, W1, b1, W2, b2, h, y}, &inner, &R, &di);
+    if (rc != NGR_OK || M == 0) return rc;
+    char *w = static_cast<char *>(ws);
+    const int64_t K8 = round8(K), F8 = round8(F);
+    const void *xp, *gp, *bp, *W1p, *b1p, *W2p, *b2p;
+    rc = pad_in(x, M, K, M, w, R.x, &xp, di, stream);
+    if (rc == NGR_OK) rc = pad_in(gamma, 1, K, 1, w, R.g, &gp, di, stream);
+    if (rc == NGR_OK) rc = pad_in(beta, 1, K, 1, w, R.b, &bp, di, stream);
+    if (rc == NGR_OK) rc = pad_in(W1, F, K, F8, w, R.w1, &W1p, di, stream);
+    if (rc == NGR_OK) rc = pad_in(b1, 1, F, 1, w, R.b1, &b1p, di, stream);
+    if (rc == NGR_OK) rc = pad_in(W2, K, F, K8, w, R.w2, &W2p, di, stream);
+    if (rc == NGR_OK) rc = pad_in(b2, 1, K, 1, w, R.b2, &b2p, di, stream);
+    if (rc != NGR_OK) return rc;
+    void *Hp = h ? static_cast<void *>(w + R.h) : nullptr;
+    rc = mlp_chain(op, norm, act, xp, gp, bp, W1p, b1p, W2p, b2p, eps, M, K8, F8, dtype, Hp,
+                   w + R.y, ws, inner, stream, K);
+    if (rc == NGR_OK) rc = launch_unpad_rows(w + R.y, M, K, K8, y, di.sms, stream);
+    if (rc == NGR_OK && h) rc = launch_unpad_rows(Hp, M, F, F8, h, di.sms, stream);
+    return rc;
+}
+
+int swiglu_chain_any(int op, int norm, const void *x, const void *gamma, const void *beta,
+                     const void *Wg, const void *Wu, const void *Wd, float eps, int64_t M,
+                     int64_t K, int64_t F, int dtype, void *h, void *y, void *ws,
+                     size_t ws_bytes, cudaStream_t stream)
+{
+    const bool down = op == NGR_OP_MLP_SWIGLU;
+    if (!needs_pad(op, K, F))
+        return swiglu_chain(op, norm, x, gamma, beta, Wg, Wu, Wd, eps, M, K, F, dtype, h, y, ws,
+                            ws_bytes, stream);
+    if (!x || !Wg || !Wu || (down ? (!Wd || !y) : !h)) return NGR_ERR_NULL;
+    if (norm != kNormNone && !gamma) return NGR_ERR_NULL;
+    if (norm == kNormLayer && !beta) return NGR_ERR_NULL;
+    const bool h_in_ws = down && h == nullptr;
+    size_t inner = 0;
+    PadRegions R;
+    DevInfo di;
+    int rc = pad_prologue(op, M, K, F, dtype, h_in_ws, ws, ws_bytes,
+                          {x, gamma, beta, Wg, Wu, Wd, h, y}, &inner, &R, &di);
+    if (rc != NGR_OK || M == 0) return rc;
+    char *w = static_cast<char *>(ws);
+    const int64_t K8 = round8(K), F8 = round8(F);
+    const void *xp, *gp, *bp, *Wgp, *Wup, *Wdp = nullptr;
+    rc = pad_in(x, M, K, M, w, R.x, &xp, di, stream);
+    if (rc == NGR_OK) rc = pad_in(gamma, 1, K, 1, w, R.g, &gp, di, stream);
+    if (rc == NGR_OK) rc = pad_in(beta, 1, K, 1, w, R.b, &bp, di, stream);
+    if (rc == NGR_OK) rc = pad_in(Wg, F, K, F8, w, R.w1, &Wgp, di, stream);
+    if (rc == NGR_OK) rc = pad_in(Wu, F, K, F8, w, R.w3, &Wup, di, stream);
+    if (rc == NGR_OK && down) rc = pad_in(Wd, K, F, K8, w, R.w2, &Wdp, di, stream);
+    if (rc != NGR_OK) return rc;
+    void *Hp = h ? static_cast<void *>(w + R.h) : nullptr;
+    rc = swiglu_chain(op, norm, xp, gp, bp, Wgp, Wup, Wdp, eps, M, K8, F8, dtype, Hp,
+                      down ? w + R.y : nullptr, ws, inner, stream, K);
+    if (rc == NGR_OK && down) rc = launch_unpad_rows(w + R.y, M, K, K8, y, di.sms, stream);
+    if (rc == NGR_OK && h) rc = launch_unpad_rows(Hp, M, F, F8, h, di.sms, stream);
+    return rc;
+}
+
+int linear_residual_norm_any(int norm, const void *x, const void *W, const void *bias,
+                             const void *residual, const void *gamma, const void *beta, float eps,
+                             int64_t M, int64_t K, int64_t N, int dtype, void *h, void *y,
+                             void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    const int op = NGR_OP_LINEAR_RESIDUAL_NORM;
+    if (!needs_pad(op, K, N))
+        return linear_residual_norm(norm, x, W, bias, residual, gamma, beta, eps, M, K, N, dtype,
+                                    h, y, ws, ws_bytes, stream);
+    if (norm != kNormLayer && norm != kNormRms) return NGR_ERR_ARG;
+    if (!x || !W || !gamma || !y || (norm == kNormLayer && !beta)) return NGR_ERR_NULL;
+    size_t inner = 0;
+    PadRegions R;
+    DevInfo di;
+    int rc = pad_prologue(op, M, K, N, dtype, h == nullptr, ws, ws_bytes,
+                          {x, W, bias, residual, gamma, beta, h, y}, &inner, &R, &di);
+    if (rc != NGR_OK || M == 0) return rc;
+    char *w = static_cast<char *>(ws);
+    const int64_t N8 = round8(N);
+    const void *xp, *Wp, *biasp, *resp, *gp, *bp;
+    rc = pad_in(x, M, K, M, w, R.x, &xp, di, stream);
+    if (rc == NGR_OK) rc = pad_in(W, N, K, N8, w, R.w1, &Wp, di, stream);
+    if (rc == NGR_OK) rc = pad_in(bias, 1, N, 1, w, R.b1, &biasp, di, stream);
+    if (rc == NGR_OK) rc = pad_in(residual, M, N, M, w, R.res, &resp, di, stream);
+    if (rc == NGR_OK) rc = pad_in(gamma, 1, N, 1, w, R.g, &gp, di, stream);
+    if (rc == NGR_OK) rc = pad_in(beta, 1, N, 1, w, R.b, &bp, di, stream);
+    if (rc != NGR_OK) return rc;
+    void *Hp = h ? static_cast<void *>(w + R.h) : nullptr;
+    rc = linear_residual_norm(norm, xp, Wp, biasp, resp, gp, bp, eps, M, round8(K), N8, dtype, Hp,
+                              w + R.y, ws, inner, stream, N);
+    if (rc == NGR_OK) rc = launch_unpad_rows(w + R.y, M, N, N8, y, di.sms, stream);
+    if (rc == NGR_OK && h) rc = launch_unpad_rows(Hp, M, N, N8, h, di.sms, stream);
+    return rc;
 }
 
 __global__ void bounded_wait_probe_kernel(int *err, unsigned long long timeout_ns)
@@ -852,7 +1078,7 @@ size_t ngr_workspace_bytes(int op, int64_t M, int64_t K, int64_t N, int ffn_h_in
 {
     if (op < NGR_OP_LAYERNORM_LINEAR || op > NGR_OP_LINEAR_RESIDUAL_NORM) return 0;
     if (M < 0 || K <= 0 || N <= 0 || M >= kMaxDim || K >= kMaxDim || N >= kMaxDim) return 0;
-    return ws_layout(op, M, K, N, ffn_h_in_workspace != 0).total;
+    return ws_total(op, M, K, N, ffn_h_in_workspace != 0);
 }
 
 int ngr_fused_layernorm_linear(const void *x, const void *gamma, const void *beta, const void *W,
@@ -887,9 +1113,9 @@ int ngr_ffn_linear_silu_linear(const void *x, const void *W1, const void *W2, in
                                int64_t K, int64_t F, int dtype, void *h, void *y, void *workspace,
                                size_t workspace_bytes, ngr_stream_t stream)
 {
-    return mlp_chain(NGR_OP_FFN, kNormNone, kActSilu, x, nullptr, nullptr, W1, nullptr, W2, nullptr,
-                     0.f, M, K, F, dtype, h, y, workspace, workspace_bytes,
-                     reinterpret_cast<cudaStream_t>(stream));
+    return mlp_chain_any(NGR_OP_FFN, kNormNone, kActSilu, x, nullptr, nullptr, W1, nullptr, W2,
+                         nullptr, 0.f, M, K, F, dtype, h, y, workspace, workspace_bytes,
+                         reinterpret_cast<cudaStream_t>(stream));
 }
 
 int ngr_fused_norm_linear_act(int norm, int act, const void *x, const void *gamma,
@@ -911,9 +1137,9 @@ int ngr_fused_mlp(int norm, int act, const void *x, const void *gamma, const voi
 {
     if (norm < kNormNone || norm > kNormRms || act < kActNone || act > kActGelu)
         return NGR_ERR_ARG;
-    return mlp_chain(NGR_OP_MLP, norm, act, x, gamma, norm == kNormLayer ? beta : nullptr, W1, b1,
-                     W2, b2, eps, M, K, F, dtype, h, y, workspace, workspace_bytes,
-                     reinterpret_cast<cudaStream_t>(stream));
+    return mlp_chain_any(NGR_OP_MLP, norm, act, x, gamma, norm == kNormLayer ? beta : nullptr, W1,
+                         b1, W2, b2, eps, M, K, F, dtype, h, y, workspace, workspace_bytes,
+                         reinterpret_cast<cudaStream_t>(stream));
 }
 
 int ngr_fused_norm_swiglu(int norm, const void *x, const void *gamma, const void *beta,
@@ -922,9 +1148,9 @@ int ngr_fused_norm_swiglu(int norm, const void *x, const void *gamma, const void
                           ngr_stream_t stream)
 {
     if (norm < kNormNone || norm > kNormRms) return NGR_ERR_ARG;
-    return swiglu_chain(NGR_OP_SWIGLU, norm, x, gamma, norm == kNormLayer ? beta : nullptr, Wg, Wu,
-                        nullptr, eps, M, K, F, dtype, h, nullptr, workspace, workspace_bytes,
-                        reinterpret_cast<cudaStream_t>(stream));
+    return swiglu_chain_any(NGR_OP_SWIGLU, norm, x, gamma, norm == kNormLayer ? beta : nullptr, Wg,
+                            Wu, nullptr, eps, M, K, F, dtype, h, nullptr, workspace,
+                            workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int ngr_fused_mlp_swiglu(int norm, const void *x, const void *gamma, const void *beta,
@@ -933,9 +1159,9 @@ int ngr_fused_mlp_swiglu(int norm, const void *x, const void *gamma, const void 
                          size_t workspace_bytes, ngr_stream_t stream)
 {
     if (norm < kNormNone || norm > kNormRms) return NGR_ERR_ARG;
-    return swiglu_chain(NGR_OP_MLP_SWIGLU, norm, x, gamma, norm == kNormLayer ? beta : nullptr, Wg,
-                        Wu, Wd, eps, M, K, F, dtype, h, y, workspace, workspace_bytes,
-                        reinterpret_cast<cudaStream_t>(stream));
+    return swiglu_chain_any(NGR_OP_MLP_SWIGLU, norm, x, gamma, norm == kNormLayer ? beta : nullptr,
+                            Wg, Wu, Wd, eps, M, K, F, dtype, h, y, workspace, workspace_bytes,
+                            reinterpret_cast<cudaStream_t>(stream));
 }
 
 int ngr_fused_linear_residual_norm(int norm, const void *x, const void *W, const void *bias,
@@ -944,9 +1170,10 @@ int ngr_fused_linear_residual_norm(int norm, const void *x, const void *W, const
                                    void *h, void *y, void *workspace, size_t workspace_bytes,
                                    ngr_stream_t stream)
 {
-    return linear_residual_norm(norm, x, W, bias, residual, gamma, norm == kNormLayer ? beta : nullptr,
-                                eps, M, K, N, dtype, h, y, workspace, workspace_bytes,
-                                reinterpret_cast<cudaStream_t>(stream));
+    return linear_residual_norm_any(norm, x, W, bias, residual, gamma,
+                                    norm == kNormLayer ? beta : nullptr, eps, M, K, N, dtype, h, y,
+                                    workspace, workspace_bytes,
+                                    reinterpret_cast<cudaStream_t>(stream));
 }
 
 int ngr_fold_prepare(int norm, const void *gamma, const void *beta, const void *W,
@@ -954,17 +1181,22 @@ int ngr_fold_prepare(int norm, const void *gamma, const void *beta, const void *
                      ngr_stream_t stream)
 {
     if (norm != kNormLayer && norm != kNormRms) return NGR_ERR_ARG;
-    int rc = check_sizes(0, K, N, dtype);
-    if (rc != NGR_OK) return rc;
+    if (dtype != NGR_F16 && dtype != NGR_BF16) return NGR_ERR_DTYPE;
+    if (K <= 0 || N <= 0 || K >= kMaxDim || N >= kMaxDim) return NGR_ERR_SHAPE;
+    int rc = NGR_OK;
     if (!gamma || !W || !Wf || !cb || (norm == kNormLayer && !beta)) return NGR_ERR_NULL;
-    if (!aligned16(gamma) || !aligned16(W) || !aligned16(Wf) || !aligned16(cb) ||
-        (beta && !aligned16(beta)) || (bias && !aligned16(bias)))
+    if (norm == kNormRms) beta = nullptr;
+    const bool aligned = K % 8 == 0 && N % 8 == 0 && aligned16(gamma) && aligned16(W) &&
+                         (!beta || aligned16(beta)) && (!bias || aligned16(bias));
+    if (!aligned16(Wf) || !aligned16(cb) || !aligned2(gamma) || !aligned2(W) ||
+        (beta && !aligned2(beta)) || (bias && !aligned2(bias)))
         return NGR_ERR_ALIGN;
     DevInfo di;
     rc = current_device_info(&di);
     if (rc != NGR_OK) return rc;
-    rc = launch_fold_prepare(norm, dtype == NGR_BF16, gamma, norm == kNormLayer ? beta : nullptr, W,
-                             bias, K, N, Wf, cb, di.sms, reinterpret_cast<cudaStream_t>(stream));
+    auto launch = aligned ? launch_fold_prepare : launch_fold_prepare_any;
+    rc = launch(norm, dtype == NGR_BF16, gamma, beta, W, bias, K, N, Wf, cb, di.sms,
+                reinterpret_cast<cudaStream_t>(stream));
     return rc == 0 ? NGR_OK : rc;
 }
 

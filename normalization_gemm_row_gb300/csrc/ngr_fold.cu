@@ -86,6 +86,85 @@ __global__ void __launch_bounds__(kFoldThreads) fold_prepare_kernel(
     }
 }
 
+// The same fold for any K and N and 2-byte-aligned operands, one element at
+// a time: W' is written as [N, K8] rows (K8 = K rounded up to a multiple of
+// 8, zero columns past K) and cb as [2, N8] (c, then b'; zero past N), the
+// layouts the folded layer reads.  Every W' element is still rounded once
+// and c still sums the rounded values.
+template <bool BF16, bool HAS_BETA>
+__global__ void __launch_bounds__(kFoldThreads) fold_prepare_any_kernel(
+    const uint16_t *__restrict__ gamma, const uint16_t *__restrict__ beta,
+    const uint16_t *__restrict__ W, const void *__restrict__ bias, int64_t K, int64_t N,
+    int64_t K8, int64_t N8, uint16_t *__restrict__ Wf, float *__restrict__ cb)
+{
+    __shared__ float red[2][kFoldThreads / 32];
+    const int tid = threadIdx.x;
+    for (int64_t n = blockIdx.x; n < N; n += gridDim.x) {
+        float c = 0.f, b = 0.f;
+        for (int64_t k = tid; k < K8; k += kFoldThreads) {
+            uint16_t o = 0;
+            if (k < K) {
+                const float w = to_float1<BF16>(W + n * K, static_cast<int>(k));
+                const float g = to_float1<BF16>(gamma, static_cast<int>(k));
+                const uint32_t r = from_float2<BF16>(g * w, 0.f);
+                o = static_cast<uint16_t>(r & 0xffffu);
+                c += to_float1<BF16>(&o, 0);
+                if constexpr (HAS_BETA) b = fmaf(to_float1<BF16>(beta, static_cast<int>(k)), w, b);
+            }
+            Wf[n * K8 + k] = o;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            c += __shfl_xor_sync(0xffffffffu, c, off);
+            b += __shfl_xor_sync(0xffffffffu, b, off);
+        }
+        if ((tid & 31) == 0) {
+            red[0][tid >> 5] = c;
+            red[1][tid >> 5] = b;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            float tc = 0.f, tb = 0.f;
+            for (int w = 0; w < kFoldThreads / 32; ++w) {
+                tc += red[0][w];
+                tb += red[1][w];
+            }
+            if (bias) tb += to_float1<BF16>(bias, static_cast<int>(n));
+            cb[n] = tc;
+            cb[N8 + n] = tb;
+        }
+        __syncthreads();
+    }
+    if (blockIdx.x == 0)
+        for (int64_t n = N + tid; n < N8; n += kFoldThreads) cb[n] = cb[N8 + n] = 0.f;
+}
+
+int launch_fold_prepare_any(int norm, bool bf16, const void *gamma, const void *beta,
+                            const void *W, const void *bias, int64_t K, int64_t N, void *Wf,
+                            float *cb, int num_sms, cudaStream_t stream)
+{
+    int64_t blocks = N;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    if (blocks > cap) blocks = cap;
+    const dim3 grid(static_cast<unsigned>(blocks)), block(kFoldThreads);
+    const int64_t K8 = (K + 7) & ~static_cast<int64_t>(7), N8 = (N + 7) & ~static_cast<int64_t>(7);
+    const uint16_t *g = static_cast<const uint16_t *>(gamma);
+    const uint16_t *bt = static_cast<const uint16_t *>(beta);
+    const uint16_t *w = static_cast<const uint16_t *>(W);
+    uint16_t *f = static_cast<uint16_t *>(Wf);
+    const bool has_beta = norm == kNormLayer;
+#define NGR_FOLD_ANY(B_, H_) \
+    fold_prepare_any_kernel<B_, H_><<<grid, block, 0, stream>>>(g, bt, w, bias, K, N, K8, N8, f, cb)
+    if (bf16) {
+        if (has_beta) NGR_FOLD_ANY(true, true); else NGR_FOLD_ANY(true, false);
+    } else {
+        if (has_beta) NGR_FOLD_ANY(false, true); else NGR_FOLD_ANY(false, false);
+    }
+#undef NGR_FOLD_ANY
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? 0 : record_cuda_error("fold preparation launch", e, cudaGetErrorString(e));
+}
+
 int launch_fold_prepare(int norm, bool bf16, const void *gamma, const void *beta, const void *W,
                         const void *bias, int64_t K, int64_t N, void *Wf, float *cb, int num_sms,
                         cudaStream_t stream)

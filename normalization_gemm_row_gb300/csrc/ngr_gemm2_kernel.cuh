@@ -57,6 +57,7 @@ constexpr int kMaxParts = 4;
 #define NGR_RMS_RSTD_OUT 1
 #endif
 
+
 template <int BN, int STAGES, int NSUB>
 struct Gemm2Smem {
     static constexpr int kA = kBM * kBK * 2;          // 16 KB: this CTA's 128 x rows
@@ -96,11 +97,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // that works on the stage, in each CTA (used with a norm only).
     constexpr uint32_t kReadyCount = 2 * kGroupWarps;
     constexpr int kParts = kNorm ? NGR_TRANSFORM_PARTS : 1;
-    // RMSNorm in bf16: the transform applies gamma only and the epilogue
-    // multiplies each row by its rstd (one multiply per element instead of
-    // two on the stage round trip).  bf16's range makes x * gamma safe; in
-    // fp16 it could overflow where x * rstd * gamma would not.
-    constexpr bool kRstdOut = NORM == kNormRms && BF16 && NGR_RMS_RSTD_OUT;
+    // RMSNorm: the transform computes x s gamma in packed 16-bit arithmetic
+    // (s a power of two near the row's rstd; transform8_rms16) and the
+    // epilogue multiplies each row by rstd / s.
+    constexpr bool kRstdOut = NORM == kNormRms && NGR_RMS_RSTD_OUT;
     static_assert(kParts >= 1 && kParts <= kMaxParts && (kBK / kUmmaK) % kParts == 0,
                   "whole K steps per transform part");
     static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "UMMA N for M = 256");
@@ -337,7 +337,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 tc_fence_after();
                 const int row = (tile % m_tiles) * 2 * kBM + static_cast<int>(rank) * kBM + q * 32 + lane;
                 float2 so = fold_row_scale<NORM>(args, row);
-                if constexpr (kRstdOut) so = make_float2(row < args.M ? args.stats[row].y : 0.f, 0.f);
+                if constexpr (kRstdOut)
+                    so = make_float2(row < args.M ? rms_out_scale<BF16>(args.stats[row].y) : 0.f, 0.f);
                 const uint32_t t_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                         static_cast<uint32_t>(cur * kTW);
                 if constexpr (GATED) {

@@ -180,15 +180,11 @@ __device__ __forceinline__ float2 unpack2(uint32_t w)
 // LayerNorm a = (x * rstd + (-mu * rstd)) * gamma + beta, RMSNorm
 // a = (x * rstd) * gamma; one rounding to the 16-bit type at the end.
 // so = (rstd, -mu * rstd) of the row; g[4], b[4] = gamma/beta pairs of the
-// 8 columns.  With ROW_SCALE false (RMSNorm only) the row's rstd is left to
-// the epilogue and a = x * gamma: rstd is a factor of the whole row, so
-// rstd * sum_k (x gamma)_k W_nk is the same product, and the rounding is one
-// rounding of a value of the same relative precision.
-template <int NORM, bool BF16, bool ROW_SCALE = true>
+// 8 columns.  (RMSNorm with the row scale in the epilogue: transform8_rms16.)
+template <int NORM, bool BF16>
 __device__ __forceinline__ uint4 transform8_pk(uint4 v, float2 so, const float2 (&g)[4],
                                                const float2 (&b)[4])
 {
-    static_assert(ROW_SCALE || NORM == kNormRms, "only RMSNorm's scale factors out of the row");
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t o[4];
     const float2 sc = make_float2(so.x, so.x);
@@ -199,12 +195,71 @@ __device__ __forceinline__ uint4 transform8_pk(uint4 v, float2 so, const float2 
         float2 a;
         if constexpr (NORM == kNormLayer)
             a = __ffma2_rn(__ffma2_rn(f, sc, of), g[i], b[i]);
-        else if constexpr (ROW_SCALE)
-            a = __fmul2_rn(__fmul2_rn(f, sc), g[i]);
         else
-            a = __fmul2_rn(f, g[i]);
+            a = __fmul2_rn(__fmul2_rn(f, sc), g[i]);
         o[i] = from_float2<BF16>(a.x, a.y);
     }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// RMSNorm with the row's scale left to the epilogue: the transform computes
+// a' = x s gamma, s = 2^e a power of two close to the row's rstd, in packed
+// 16-bit arithmetic, and the epilogue multiplies the accumulator by
+// rstd / s.  The product of two 16-bit values is exact in FP32, so
+// round16(x s gamma) is the single rounding the FP32 form would make, and
+// it is made here by one packed multiply per two elements, with no
+// conversions.  Multiplying by s is exact (it moves the exponent) and keeps
+// a' at the scale of the normalized row, so fp16 does not overflow where
+// x rstd gamma would not; bf16's range needs no scale (s = 1).
+__device__ __forceinline__ int rms_scale_exp(float rstd)
+{
+    const int e = ((__float_as_int(rstd) >> 23) & 0xff) - 127;   // floor(log2 rstd)
+    return min(max(e, -14), 15);                                  // a normal fp16 power of two
+}
+
+// s, twice, as a packed 16-bit pair.
+template <bool BF16>
+__device__ __forceinline__ uint32_t rms_in_scale2(float rstd)
+{
+    if constexpr (BF16) {
+        return 0x3f803f80u;                                       // (1.0, 1.0)
+    } else {
+        const uint32_t h = static_cast<uint32_t>(rms_scale_exp(rstd) + 15) << 10;
+        return h | (h << 16);
+    }
+}
+
+// rstd / s, exact in FP32.
+template <bool BF16>
+__device__ __forceinline__ float rms_out_scale(float rstd)
+{
+    if constexpr (BF16)
+        return rstd;
+    else
+        return rstd * __int_as_float((127 - rms_scale_exp(rstd)) << 23);
+}
+
+// a * b on two packed 16-bit values, rounded to nearest even, subnormals kept.
+template <bool BF16>
+__device__ __forceinline__ uint32_t mul2_16(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    if constexpr (BF16)
+        asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    else
+        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// a' = x s gamma for 8 elements (RMSNorm, row scale in the epilogue):
+// s2 = (s, s), g2[4] = the gamma pairs of the 8 columns, all packed 16-bit.
+template <bool BF16>
+__device__ __forceinline__ uint4 transform8_rms16(uint4 v, uint32_t s2, const uint32_t (&g2)[4])
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[i] = mul2_16<BF16>(BF16 ? w[i] : mul2_16<BF16>(w[i], s2), g2[i]);
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
@@ -312,9 +367,9 @@ __device__ __forceinline__ void transform_role(int t, int tile0, int tile_step, 
                                                const WaitCtx &wc, M0Fn m0_of, ArriveFn arrive)
 {
     static_assert(PARTS == 1 || PARTS == 2 || PARTS == 4, "a part is a whole number of 16-byte chunks");
-    static_assert(kGroupThreads == 128, "a group covers 128 rows x 8 chunks per pass");
+    static_assert(kGroupThreads == 128 || kGroupThreads == 256, "a group is 4 or 8 warps");
     constexpr int kCP = 8 / PARTS;                    // chunks of a row per part
-    constexpr int kRowStride = 16 * PARTS;            // rows between a thread's rows
+    constexpr int kRowStride = 16 * PARTS * (kGroupThreads / 128);  // rows between a thread's rows
     constexpr int kRows = kBM / kRowStride;           // rows per thread
     constexpr int kBatch = kRows < 8 ? kRows : 8;
     constexpr int kS = 8 / PARTS;                     // row offset of a quarter-warp's row sets
@@ -336,12 +391,14 @@ __device__ __forceinline__ void transform_role(int t, int tile0, int tile_step, 
     for (int tile = tile0; tile < num_tiles; tile += tile_step) {
         const int m0 = m0_of(tile);
         float2 so[kRows];
+        uint32_t s2[kRows];                  // RMSNorm, row scale in the epilogue: (s, s)
 #pragma unroll
         for (int i = 0; i < kRows; ++i) {
             const int row = m0 + r0 + kRowStride * i;
             float2 st = make_float2(0.f, 0.f);
             if (row < M) st = stats[row];
             so[i] = make_float2(st.y, -st.x * st.y);
+            s2[i] = rms_in_scale2<BF16>(st.y);
         }
         const int k_blocks = kb_count(tile);
         for (int kb = 0; kb < k_blocks; ++kb, ++it) {
@@ -370,6 +427,11 @@ __device__ __forceinline__ void transform_role(int t, int tile0, int tile_step, 
                         bb[2] = make_float2(q[3].x, q[3].y);
                         bb[3] = make_float2(q[3].z, q[3].w);
                     }
+                    // gamma pairs as packed 16-bit values (exact: gamma is a 16-bit input)
+                    uint32_t g2[4];
+                    if constexpr (!ROW_SCALE)
+#pragma unroll
+                        for (int q2 = 0; q2 < 4; ++q2) g2[q2] = from_float2<BF16>(gg[q2].x, gg[q2].y);
                     const int pc = (c ^ (r0 & 7)) << 4;   // swizzled chunk offset (same for all rows)
                     uint8_t *base = sA + stage * KA + r0 * 128 + pc;
                     // Rows in batches of up to 8: all loads of a batch are in
@@ -381,9 +443,14 @@ __device__ __forceinline__ void transform_role(int t, int tile0, int tile_step, 
                         for (int i = 0; i < kBatch; ++i)
                             v[i] = *reinterpret_cast<const uint4 *>(base + (b0 + i) * kRowStride * 128);
 #pragma unroll
-                        for (int i = 0; i < kBatch; ++i)
-                            *reinterpret_cast<uint4 *>(base + (b0 + i) * kRowStride * 128) =
-                                transform8_pk<NORM, BF16, ROW_SCALE>(v[i], so[b0 + i], gg, bb);
+                        for (int i = 0; i < kBatch; ++i) {
+                            uint4 o;
+                            if constexpr (ROW_SCALE)
+                                o = transform8_pk<NORM, BF16>(v[i], so[b0 + i], gg, bb);
+                            else
+                                o = transform8_rms16<BF16>(v[i], s2[b0 + i], g2);
+                            *reinterpret_cast<uint4 *>(base + (b0 + i) * kRowStride * 128) = o;
+                        }
                     }
                     fence_proxy_async_smem();
                     __syncwarp();

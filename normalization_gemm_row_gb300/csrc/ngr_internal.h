@@ -30,10 +30,12 @@ constexpr int kGemmThreads = 512;
 constexpr int kTransformWarp0 = 4;
 constexpr int kTransformThreads = 256;
 constexpr int kEpilogueWarp0 = 12;
-// The transform warps form groups that take turns on consecutive stages,
-// so that several stages are normalized at once.
+// The transform warps form groups that take turns on consecutive stages
+// (2 groups of 4 warps), or all 8 normalize every stage (1 group): the
+// single group halves each stage's normalization latency and measured
+// 0.5-2 % faster with RMSNorm, the same with LayerNorm.
 #ifndef NGR_TRANSFORM_GROUPS
-#define NGR_TRANSFORM_GROUPS 2
+#define NGR_TRANSFORM_GROUPS 1
 #endif
 constexpr int kTransformGroups = NGR_TRANSFORM_GROUPS;
 constexpr int kGroupThreads = kTransformThreads / kTransformGroups;
@@ -41,8 +43,11 @@ constexpr int kGroupWarps = kGroupThreads / 32;
 
 // Decode (swap-AB) path: weight rows on the UMMA M side, tokens on N.
 constexpr int kDecodeMaxM = 32;      // M up to this uses the decode path
-constexpr int kDecodeMaxContrib = 4; // CTAs sharing one 128-row weight tile (split-K)
+constexpr int kDecodeMaxGroups = 8;  // k groups (CTAs sharing one 128-row weight tile)
 constexpr int kDecodeThreads = 384;
+// k blocks of tokens one decode CTA holds in shared memory (its slice of x):
+// 64 KB of [MN x 64] 16-bit boxes beside the weight ring.
+__host__ __device__ constexpr int decode_max_kb(int mn) { return (64 * 1024) / (mn * kBK * 2); }
 
 // Arguments of the persistent GEMM kernel (normal orientation: x rows on M).
 struct alignas(128) GemmArgs {
@@ -71,28 +76,34 @@ struct alignas(128) GemmArgs {
     unsigned long long timeout_ns;
 };
 
-// Arguments of the decode kernel (swap-AB, split-K over a stream of
-// (weight tile, k block) units).
+// Arguments of the decode kernel (swap-AB; CTA (kg, ng) of a k_groups x
+// n_groups grid takes k blocks [kg kb_per_group, +kb_per_group) of the
+// 128-row weight tiles of n group ng).
 struct alignas(128) DecodeArgs {
     CUtensorMap map_w;      // weights [N, K], box {64, 128}, 128-byte swizzle
     CUtensorMap map_x;      // activations [M, K], box {64, MN}, 128-byte swizzle
-    CUtensorMap map_gb;
-    const float2 *stats;
+    const float2 *stats;    // [M] (mu, rstd): a norm or a folded weight
+    const float *gamma_f;   // [K] FP32 (a norm)
+    const float *beta_f;    // [K] FP32 (LayerNorm)
     const void *bias;
     const float *fold_c;
     const float *fold_b;
     const void *residual;   // [M, N] added last, or nullptr
     void *y;
-    float *partials;        // [n_tiles][kDecodeMaxContrib][MN][128] fp32
-    int *counters;          // [n_tiles], zero at kernel start
+    float *partials;        // [n_tiles][kDecodeMaxGroups][MN][128] fp32
+    int *counters;          // [n_tiles][4], zero at kernel start
     int *err;
     int zero_err;
     int act;                // kAct*
     int M, N, K;
     int n_tiles, k_blocks;
-    long long units;        // n_tiles * k_blocks
-    int grid;               // CTAs the units are divided among
+    int k_groups, kb_per_group, n_groups;
     unsigned long long timeout_ns;
+};
+
+// The decode grid: k groups of kb_per_group k blocks x n groups of tiles.
+struct DecodePlan {
+    int k_groups, kb_per_group, n_groups;
 };
 
 // GEMM tile variant selected by the host planner.
@@ -142,9 +153,10 @@ int launch_rowstats(int norm, bool bf16, const void *x, int64_t M, int64_t K,
 
 // Copies for shapes whose K or N is not a multiple of 8 (ngr_pad.cu):
 // rows of `cols` 16-bit values (pitch `src_pitch`) into rows of `dst_cols`
-// (a multiple of 8) with a zero tail, and back.
+// (a multiple of 8) with a zero tail, followed by zero rows up to
+// `dst_rows` (default: none), and back.
 int launch_pad_rows(const void *src, int64_t rows, int64_t cols, int64_t src_pitch, void *dst,
-                    int64_t dst_cols, int num_sms, cudaStream_t stream);
+                    int64_t dst_cols, int num_sms, cudaStream_t stream, int64_t dst_rows = 0);
 int launch_unpad_rows(const void *src, int64_t rows, int64_t cols, int64_t src_pitch, void *dst,
                       int num_sms, cudaStream_t stream);
 
@@ -161,12 +173,17 @@ size_t gemm_smem_bytes(int bn, int stages, bool norm);
 
 int launch_decode(int norm, bool bf16, int mn, const DecodeArgs &args, bool pdl,
                   cudaStream_t stream);
-int plan_decode_grid(int64_t n_tiles, int64_t k_blocks, int num_sms);
+DecodePlan plan_decode(int64_t n_tiles, int64_t k_blocks, int mn, int num_sms);
 size_t decode_smem_bytes(int mn);
 
 int launch_fold_prepare(int norm, bool bf16, const void *gamma, const void *beta,
                         const void *W, const void *bias, int64_t K, int64_t N, void *Wf,
                         float *cb, int num_sms, cudaStream_t stream);
+// The fold for any K, N and 2-byte-aligned operands: Wf as [N, K8] rows, cb
+// as [2, N8] (K8, N8: K, N rounded up to multiples of 8; zero padding).
+int launch_fold_prepare_any(int norm, bool bf16, const void *gamma, const void *beta,
+                            const void *W, const void *bias, int64_t K, int64_t N, void *Wf,
+                            float *cb, int num_sms, cudaStream_t stream);
 
 int launch_bounded_wait_probe(int *err, unsigned long long timeout_ns,
                               cudaStream_t stream);

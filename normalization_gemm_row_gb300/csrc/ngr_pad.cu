@@ -19,26 +19,29 @@ namespace ngr {
 
 constexpr int kPadThreads = 256;
 
-// dst[r, c] = c < cols ? src[r * src_pitch + c] : 0 for c < dst_cols
-// (dst_cols % 8 == 0, dst 16-byte aligned); one 16-byte vector per thread.
+// dst[r, c] = r < rows && c < cols ? src[r * src_pitch + c] : 0 for
+// r < dst_rows, c < dst_cols (dst_cols % 8 == 0, dst 16-byte aligned); one
+// 16-byte vector per thread.
 __global__ void __launch_bounds__(kPadThreads) pad_rows_kernel(
     const uint16_t *__restrict__ src, int64_t rows, int64_t cols, int64_t src_pitch,
-    uint4 *__restrict__ dst, int64_t dst_cols)
+    uint4 *__restrict__ dst, int64_t dst_cols, int64_t dst_rows)
 {
     const int64_t vecs = dst_cols >> 3;
-    const int64_t total = rows * vecs;
+    const int64_t total = dst_rows * vecs;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t r = i / vecs;
         const int64_t c0 = (i - r * vecs) << 3;
-        const uint16_t *s = src + r * src_pitch;
-        uint32_t w[4];
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+        if (r < rows) {
+            const uint16_t *s = src + r * src_pitch;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int64_t c = c0 + 2 * j;
-            const uint32_t lo = c < cols ? __ldg(s + c) : 0u;
-            const uint32_t hi = c + 1 < cols ? __ldg(s + c + 1) : 0u;
-            w[j] = lo | (hi << 16);
+            for (int j = 0; j < 4; ++j) {
+                const int64_t c = c0 + 2 * j;
+                const uint32_t lo = c < cols ? __ldg(s + c) : 0u;
+                const uint32_t hi = c + 1 < cols ? __ldg(s + c + 1) : 0u;
+                w[j] = lo | (hi << 16);
+            }
         }
         dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
     }
@@ -67,12 +70,13 @@ static unsigned grid_for(int64_t work, int num_sms)
 }
 
 int launch_pad_rows(const void *src, int64_t rows, int64_t cols, int64_t src_pitch, void *dst,
-                    int64_t dst_cols, int num_sms, cudaStream_t stream)
+                    int64_t dst_cols, int num_sms, cudaStream_t stream, int64_t dst_rows)
 {
-    if (rows <= 0) return 0;
-    pad_rows_kernel<<<grid_for(rows * (dst_cols >> 3), num_sms), kPadThreads, 0, stream>>>(
+    if (dst_rows < rows) dst_rows = rows;
+    if (dst_rows <= 0) return 0;
+    pad_rows_kernel<<<grid_for(dst_rows * (dst_cols >> 3), num_sms), kPadThreads, 0, stream>>>(
         static_cast<const uint16_t *>(src), rows, cols, src_pitch, static_cast<uint4 *>(dst),
-        dst_cols);
+        dst_cols, dst_rows);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? 0 : record_cuda_error("padding copy launch", e, cudaGetErrorString(e));
 }

@@ -188,3 +188,39 @@ def sample_rows(M: int, count: int, seed: int, always=()) -> torch.Tensor:
     pick = torch.randperm(M, generator=g)[:min(count, M)]
     rows = torch.cat([pick, torch.as_tensor(list(always), dtype=torch.long)])
     return torch.unique(rows).sort().values
+
+
+# Edge rows: the degenerate inputs of the normalization (a constant row has
+# zero variance; an all-zero row has zero mean square; rows far from zero
+# mean stress cancellation in the variance; rows near the top of the fp16
+# range stress overflow).  Each kind maps to how the row is drawn.
+EDGE_KINDS = ("constant", "zero", "mean1e3", "near_fp16_max")
+
+
+def with_edge_rows(d: dict, kinds, rows, seed: int = 99, constant: float = 2.5) -> dict:
+    """Return a copy of the inputs ``d`` whose x rows ``rows[i]`` are
+    replaced by an edge row of kind ``kinds[i]``:
+      constant       every element ``constant``;
+      zero           every element 0;
+      mean1e3        1000 + N(0, 1) (rounded to x's 16-bit type);
+      near_fp16_max  2e4 N(0, 1), clipped to +-6e4 (the fp16 maximum is 65504).
+    Values are drawn in fp32 from a seeded generator and cast once."""
+    g = torch.Generator("cpu")
+    g.manual_seed(seed)
+    x = d["x"].clone()
+    K = x.shape[1]
+    for kind, r in zip(kinds, rows):
+        if kind == "constant":
+            v = torch.full((K,), float(constant))
+        elif kind == "zero":
+            v = torch.zeros(K)
+        elif kind == "mean1e3":
+            v = _normal(g, (K,), 1.0, 1000.0)
+        elif kind == "near_fp16_max":
+            v = (2e4 * _normal(g, (K,))).clamp(-6e4, 6e4)
+        else:
+            raise ValueError(kind)
+        x[r] = v.to(x.dtype)
+    out = dict(d)
+    out["x"] = x
+    return out

@@ -76,18 +76,36 @@ def test_workspace_bytes_padded_shapes(lib):
     assert wb(B.OP_LINEAR_SILU, M, K, N) == base + pads
     # N not a multiple of 8: the output is padded too
     assert wb(B.OP_LAYERNORM_LINEAR, 64, 256, 517) > wb(B.OP_LAYERNORM_LINEAR, 64, 256, 520)
-    # ops without the padded path do not grow
-    assert wb(B.OP_FFN, 64, 256, 517) == wb(B.OP_FFN, 64, 256, 517)
+    # the chains pad too: the aligned problem's workspace, then the copies
+    # (x, gamma, beta, W1 [F8, K8], b1, W2 [K8, F8], b2, y, and H when the
+    # caller keeps it)
+    M, K, F = 64, 256, 517
+    F8 = 520
+    inner = wb(B.OP_FFN, M, K, F8, 0)
+    copies = (a256(M * K * 2) + 2 * a256(K * 2) + a256(F8 * K * 2) + a256(F8 * 2)
+              + a256(K * F8 * 2) + a256(K * 2) + a256(M * K * 2) + a256(M * F8 * 2))
+    assert wb(B.OP_FFN, M, K, F, 0) == inner + copies
+    # H in the workspace: the aligned problem holds it, the copies do not
+    assert wb(B.OP_FFN, M, K, F, 1) == wb(B.OP_FFN, M, K, F8, 1) + copies - a256(M * F8 * 2)
+    for op in (B.OP_MLP, B.OP_SWIGLU, B.OP_MLP_SWIGLU, B.OP_LINEAR_RESIDUAL_NORM):
+        assert wb(op, M, 250, 520) > wb(op, M, 256, 520)
 
 
-def test_other_entry_points_still_need_alignment(lib):
+def test_unaligned_shapes_need_two_byte_pointers(lib):
+    """Any K and N are accepted, but an odd address cannot hold a 16-bit
+    element: rejected before anything runs."""
     big = 1 << 24
-    assert B.ngr_fused_norm_swiglu(0, A16, None, None, A16, A16, 0.0, 4, 60, 64, 0, A16,
+    odd = A16 + 1
+    assert B.ngr_fused_norm_swiglu(0, odd, None, None, A16, A16, 0.0, 4, 60, 64, 0, A16,
                                    A16 * 16, big, None) == -3
-    assert B.ngr_fused_mlp(0, 1, A16, None, None, A16, None, A16, None, 0.0, 4, 60, 64, 0,
+    assert B.ngr_fused_mlp(0, 1, A16, None, None, odd, None, A16, None, 0.0, 4, 60, 64, 0,
                            None, A16, A16 * 16, big, None) == -3
-    assert B.ngr_fused_norm_linear_folded(1, A16, A16, A16, 1e-5, 4, 60, 64, 0, A16,
+    assert B.ngr_fused_norm_linear_folded(1, odd, A16, A16, 1e-5, 4, 60, 64, 0, A16,
                                           A16 * 16, big, None) == -3
+    # the prepared fold operands are read with 16-byte accesses
+    assert B.ngr_fused_norm_linear_folded(1, A16, A16 + 2, A16, 1e-5, 4, 60, 64, 0, A16,
+                                          A16 * 16, big, None) == -3
+    assert B.ngr_fold_prepare(1, A16, A16, A16, None, 60, 64, 0, A16 + 2, A16, None) == -3
 
 
 def test_split_k_reserve(lib):
@@ -131,8 +149,8 @@ def test_post_norm_workspace_and_rejections(lib):
     assert f(1, A16, A16, None, None, A16, 0, 1e-5, 4, 64, 64, 0, None, A16, ws, big, None) == -1
     assert f(2, A16, A16, None, A16 + 8, A16, None, 1e-5, 4, 64, 64, 0, None, A16, ws, big,
              None) == -3                                               # misaligned residual
-    assert f(2, A16, A16, None, None, A16, None, 1e-5, 4, 64, 60, 0, None, A16, ws, big,
-             None) == -3                                               # N % 8
+    assert f(2, A16, A16, None, A16 + 1, A16, None, 1e-5, 4, 64, 60, 0, None, A16, ws, big,
+             None) == -3                               # N % 8 is padded; an odd pointer is not
     assert f(2, A16, A16, None, None, A16, None, 1e-5, 4, 64, 64, 0, None, A16, ws, 300,
              None) == -5
     assert f(2, A16, A16, None, None, A16, None, 1e-5, 0, 64, 64, 0, None, A16, ws, big,
@@ -178,8 +196,8 @@ def test_new_entry_points_reject(lib):
                            None, A16, ws, big, None) == -3           # misaligned b1
     assert B.ngr_fused_norm_swiglu(2, A16, A16, None, A16, 0, 1e-5, 4, 64, 64, 0, A16, ws,
                                    big, None) == -1                  # no up weight
-    assert B.ngr_fused_norm_swiglu(0, A16, None, None, A16, A16, 0.0, 4, 64, 60, 0, A16, ws,
-                                   big, None) == -3                  # F % 8
+    assert B.ngr_fused_norm_swiglu(0, A16, None, None, A16 + 1, A16, 0.0, 4, 64, 60, 0, A16,
+                                   ws, big, None) == -3              # F % 8 padded, odd pointer
     assert B.ngr_fused_norm_swiglu(0, A16, None, None, A16, A16, 0.0, 4, 64, 64, 0, A16, ws,
                                    100, None) == -5                  # workspace too small
     assert B.ngr_fused_mlp_swiglu(2, A16, A16, None, A16, A16, 0, 1e-5, 4, 64, 64, 0, None,

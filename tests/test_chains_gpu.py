@@ -127,6 +127,20 @@ def swiglu_atol(norm_id, d, eps):
     return ATOL * (1.0 + 1.1 * np.abs(u) + np.abs(g / (1.0 + np.exp(-g))))
 
 
+def report_plain_bar(h, ref, what):
+    """How h fares against the single-product bar 1e-2 + 1e-2 |h| that the
+    product-rule bar widens: the number of elements above it and the largest
+    ratio of error to that bar.  Printed (pytest -s shows it) and bounded:
+    the widening may not hide an error of more than twice the plain bar."""
+    err = np.abs(h.double().cpu().numpy() - ref)
+    ratio = err / (ATOL + RTOL * np.abs(ref))
+    over = int((ratio > 1.0).sum())
+    print(f"{what}: {over} of {ratio.size} elements above the plain bar "
+          f"({100.0 * over / ratio.size:.4f} %), largest error / plain bar {ratio.max():.2f}")
+    assert ratio.max() <= 2.0, (what, float(ratio.max()))
+    return over, float(ratio.max())
+
+
 @pytest.mark.parametrize("bn", GATED_BN)
 @pytest.mark.parametrize("norm", list(NORMS))
 def test_swiglu_tile_widths(norm, bn):
@@ -146,6 +160,7 @@ def test_swiglu_tile_widths(norm, bn):
                                 1e-5)
             check(h, ref, f"swiglu {norm} bn={bn} {dtype}",
                   atol=swiglu_atol(NORMS[norm][0], d, 1e-5))
+            report_plain_bar(h, ref, f"swiglu {norm} bn={bn} {dtype}")
     finally:
         B.set_tile_config(-1, 0, 0)
 
@@ -158,6 +173,7 @@ def test_swiglu_small_batches(M):
     torch.cuda.synchronize()
     ref = oracle.swiglu(oracle.NORM_RMS, d["x"], d["gamma"], None, d["Wg"], d["Wu"], 1e-5)
     check(h, ref, f"swiglu M={M}", atol=swiglu_atol(oracle.NORM_RMS, d, 1e-5))
+    report_plain_bar(h, ref, f"swiglu M={M}")
 
 
 @pytest.mark.parametrize("M", [4, 300], ids=["decode", "tile"])
@@ -192,7 +208,7 @@ def test_rmsnorm_qkv_concatenated():
 
 
 # ------------------------------------------------------- full-size workloads
-def _full(idx_name, count=24):
+def _full(idx_name, count=64):
     w = inputs.BY_NAME[idx_name]
     d = inputs.make(w)
     rows = inputs.sample_rows(w.M, count, seed=7).tolist()
@@ -212,7 +228,7 @@ def test_chain_full_size_sampled_rows():
 
 
 def test_mlp_swiglu_full_size_sampled_rows():
-    w, d, rows = _full("mlp_swiglu_rms_bf16_m512_k8192_f28672", count=12)
+    w, d, rows = _full("mlp_swiglu_rms_bf16_m512_k8192_f28672")
     y = ngr.fused_mlp_swiglu(dev(d["x"]), dev(d["Wg"]), dev(d["Wu"]), dev(d["Wd"]),
                              norm=B.NORM_RMS, gamma=dev(d["gamma"]), eps=w.eps)
     torch.cuda.synchronize()
@@ -256,7 +272,7 @@ def test_linear_residual_norm_llama_output_projection():
     h, y = ngr.fused_linear_residual_norm(dev(d["x"]), dev(d["W"]), dev(gamma), norm=B.NORM_RMS,
                                           residual=dev(res), eps=1e-5)
     torch.cuda.synchronize()
-    rows = inputs.sample_rows(M, 16, seed=2).tolist()
+    rows = inputs.sample_rows(M, 64, seed=2).tolist()
     idx = torch.as_tensor(rows, device="cuda")
     href, yref = oracle.linear_residual_norm(oracle.NORM_RMS, d["x"], d["W"], None, res, gamma,
                                              None, 1e-5, rows)

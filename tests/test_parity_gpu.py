@@ -247,9 +247,10 @@ def test_full_size_workload_sampled_rows(idx):
 
 
 def test_full_size_ffn_sampled_rows():
+    """The largest workload: all N columns of a seeded sample of 64 rows."""
     w = inputs.WORKLOADS[3]
     d = inputs.make(w)
-    rows = inputs.sample_rows(w.M, 16, seed=w.seed + 1).numpy()
+    rows = inputs.sample_rows(w.M, SAMPLE_ROWS, seed=w.seed + 1).numpy()
     g = to_dev(d)
     y = run_op("ffn", g, 0.0)
     torch.cuda.synchronize()

@@ -115,3 +115,113 @@ def test_pages_example_shape_sampled_rows():
     got = y[torch.as_tensor(rows, device="cuda")]
     ref = oracle.linear_silu(d["x"], d["W"], None, rows)
     check(got, ref, "513 x 14337 -> 49152")
+
+
+# ----------------------------------------- the chains, SwiGLU, fold, post-norm
+# Each of these pads its operands (and the hidden width F) the same way; the
+# padded hidden units must contribute nothing, the statistics must count the
+# real columns only, and h and y must hold exactly their real columns.
+CHAIN_SHAPES = [(5, 250, 517), (300, 1001, 264), (129, 64, 131), (17, 13, 9), (600, 200, 1003)]
+
+
+@pytest.mark.parametrize("M,K,F", CHAIN_SHAPES)
+@pytest.mark.parametrize("norm,act,bias", [("layer", "relu", True), ("rms", "silu", False),
+                                           ("none", "gelu", True)])
+def test_unaligned_mlp_chain(norm, act, bias, M, K, F):
+    ids = {"none": (B.NORM_NONE, oracle.NORM_NONE), "layer": (B.NORM_LAYER, oracle.NORM_LAYER),
+           "rms": (B.NORM_RMS, oracle.NORM_RMS)}
+    acts = {"relu": (B.ACT_RELU, oracle.ACT_RELU), "silu": (B.ACT_SILU, oracle.ACT_SILU),
+            "gelu": (B.ACT_GELU, oracle.ACT_GELU)}
+    for dtype in (torch.float16, torch.bfloat16):
+        d = inputs.case("mlp", M, K, F, dtype, bias, 1e-5, seed=M + K + F + len(act),
+                        x_mean=2.0 if norm == "layer" else 0.0, norm=norm, act=act)
+        h = torch.empty((M, F), dtype=dtype, device="cuda")
+        y = ngr.fused_mlp(dev(d["x"]), dev(d["W1"]), dev(d["W2"]), norm=ids[norm][0],
+                          act=acts[act][0], gamma=dev(d["gamma"]), beta=dev(d["beta"]),
+                          b1=dev(d["b1"]), b2=dev(d["b2"]), eps=1e-5, h=h)
+        y2 = ngr.fused_mlp(dev(d["x"]), dev(d["W1"]), dev(d["W2"]), norm=ids[norm][0],
+                           act=acts[act][0], gamma=dev(d["gamma"]), beta=dev(d["beta"]),
+                           b1=dev(d["b1"]), b2=dev(d["b2"]), eps=1e-5)   # H in the workspace
+        torch.cuda.synchronize()
+        ref = oracle.mlp(ids[norm][1], acts[act][1], d["x"], d["gamma"], d["beta"], d["W1"],
+                         d["b1"], d["W2"], d["b2"], 1e-5)
+        href = oracle.norm_linear(ids[norm][1], acts[act][1], d["x"], d["gamma"], d["beta"],
+                                  d["W1"], d["b1"], 1e-5)
+        what = f"mlp {norm} {act} {M}x{K}x{F} {dtype}"
+        check(y, ref, what)
+        check(h, href, what + " h")
+        assert torch.equal(y, y2), what + ": h in the workspace differs"
+
+
+@pytest.mark.parametrize("M,K,F", [(3, 1001, 517), (260, 250, 1003)])
+def test_unaligned_ffn(M, K, F):
+    d = inputs.case("ffn", M, K, F, torch.float16, False, 0.0, seed=M + F)
+    y = ngr.ffn_linear_silu_linear(dev(d["x"]), dev(d["W1"]), dev(d["W2"]))
+    torch.cuda.synchronize()
+    check(y, oracle.ffn(d["x"], d["W1"], d["W2"]), f"ffn {M}x{K}x{F}")
+
+
+def _swiglu_atol(nid, d, eps):
+    g = oracle.norm_linear(nid, oracle.ACT_NONE, d["x"], d["gamma"], d["beta"], d["Wg"], None, eps)
+    u = oracle.norm_linear(nid, oracle.ACT_NONE, d["x"], d["gamma"], d["beta"], d["Wu"], None, eps)
+    return ATOL * (1.0 + 1.1 * np.abs(u) + np.abs(g / (1.0 + np.exp(-g))))
+
+
+@pytest.mark.parametrize("M,K,F", [(7, 250, 517), (300, 1001, 131), (600, 13, 264)])
+@pytest.mark.parametrize("norm", ["rms", "layer"])
+def test_unaligned_swiglu_and_mlp(norm, M, K, F):
+    bn, on = (B.NORM_RMS, oracle.NORM_RMS) if norm == "rms" else (B.NORM_LAYER, oracle.NORM_LAYER)
+    d = inputs.case("mlp_swiglu", M, K, F, torch.bfloat16, False, 1e-5, seed=M * 3 + K,
+                    x_mean=1.0, norm=norm)
+    g = {k: dev(v) for k, v in d.items() if k != "outlier_rows"}
+    h = ngr.fused_norm_swiglu(g["x"], g["Wg"], g["Wu"], norm=bn, gamma=g["gamma"],
+                              beta=g["beta"], eps=1e-5)
+    h2 = torch.empty_like(h)
+    y = ngr.fused_mlp_swiglu(g["x"], g["Wg"], g["Wu"], g["Wd"], norm=bn, gamma=g["gamma"],
+                             beta=g["beta"], eps=1e-5, h=h2)
+    torch.cuda.synchronize()
+    href = oracle.swiglu(on, d["x"], d["gamma"], d["beta"], d["Wg"], d["Wu"], 1e-5)
+    got = h.double().cpu().numpy()
+    err = np.abs(got - href)
+    assert (err <= _swiglu_atol(on, d, 1e-5) + RTOL * np.abs(href)).all(), f"swiglu {norm}"
+    assert torch.equal(h, h2)
+    yref = oracle.mlp_swiglu(on, d["x"], d["gamma"], d["beta"], d["Wg"], d["Wu"], d["Wd"], 1e-5)
+    check(y, yref, f"mlp_swiglu {norm} {M}x{K}x{F}")
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 1001, 517), (40, 250, 131), (300, 13, 1003)])
+@pytest.mark.parametrize("norm", [oracle.NORM_LAYER, oracle.NORM_RMS], ids=["ln", "rms"])
+def test_unaligned_fold(norm, M, K, N):
+    op = "layernorm_linear" if norm == oracle.NORM_LAYER else "rmsnorm_linear"
+    for dtype in (torch.float16, torch.bfloat16):
+        d = inputs.case(op, M, K, N, dtype, True, 1e-5, seed=M + K + N + norm)
+        g = {k: dev(v) for k, v in d.items() if k != "outlier_rows"}
+        Wf, cb = B.fold_prepare(norm, g["gamma"], g["beta"], g["W"], g["bias"])
+        assert Wf.shape == (N, (K + 7) // 8 * 8) and cb.shape == (2, (N + 7) // 8 * 8)
+        y = B.fused_norm_linear_folded(norm, g["x"], Wf, cb, 1e-5)
+        torch.cuda.synchronize()
+        assert not Wf[:, K:].any() and not cb[:, N:].any(), "padding of the folded weight"
+        ref = oracle.layernorm_linear(d["x"], d["gamma"], d["beta"], d["W"], d["bias"], 1e-5) \
+            if norm == oracle.NORM_LAYER else \
+            oracle.rmsnorm_linear(d["x"], d["gamma"], d["W"], d["bias"], 1e-5)
+        check(y, ref, f"folded {op} {M}x{K}x{N} {dtype}")
+
+
+@pytest.mark.parametrize("M,K,N", [(3, 250, 517), (300, 1001, 131), (129, 13, 1003)])
+@pytest.mark.parametrize("norm", ["rms", "layer"])
+def test_unaligned_post_norm(norm, M, K, N):
+    bn, on = (B.NORM_RMS, oracle.NORM_RMS) if norm == "rms" else (B.NORM_LAYER, oracle.NORM_LAYER)
+    for dtype in (torch.float16, torch.bfloat16):
+        d = inputs.case("norm_linear", M, K, N, dtype, True, 1e-5, seed=M + N, norm="none")
+        gen = torch.Generator().manual_seed(M + K)
+        res = (torch.randn((M, N), generator=gen) + 1.0).to(dtype)
+        gamma = (1.0 + 0.1 * torch.randn((N,), generator=gen)).to(dtype)
+        beta = (0.1 * torch.randn((N,), generator=gen)).to(dtype) if norm == "layer" else None
+        h, y = ngr.fused_linear_residual_norm(dev(d["x"]), dev(d["W"]), dev(gamma), norm=bn,
+                                              beta=dev(beta), bias=dev(d["bias"]),
+                                              residual=dev(res), eps=1e-5)
+        torch.cuda.synchronize()
+        href, yref = oracle.linear_residual_norm(on, d["x"], d["W"], d["bias"], res, gamma, beta,
+                                                 1e-5)
+        check(h, href, f"post-norm h {norm} {M}x{K}x{N} {dtype}")
+        check(y, yref, f"post-norm y {norm} {M}x{K}x{N} {dtype}")
