@@ -432,8 +432,12 @@ int launch_layer(int norm, int act, bool bf16, const void *x, const void *W,
     if (!map_2d(&a.map_a, x, bf16, M, K, kBM) ||
         !map_2d(&a.map_b, W, bf16, w_rows, K, static_cast<uint32_t>(plan.b_rows)))
         return NGR_ERR_CUDA;
+    // The multicast kernel's second weight map: 64-row parts of the 240-row sub-tile.
+    if (plan.mc && !map_2d(&a.map_b2, W, bf16, w_rows, K, 64)) return NGR_ERR_CUDA;
     if (has_norm && !map_gb(&a.map_gb, gf, K, L.beta_f - L.gamma_f)) return NGR_ERR_CUDA;
     a.stats = stats;
+    a.gamma_f = gf;
+    a.beta_f = has_norm ? reinterpret_cast<float *>(ws + L.beta_f) : nullptr;
     a.bias = bias;
     a.fold_c = fold_c;
     a.fold_b = fold_b;
@@ -1267,7 +1271,7 @@ int ngr_tile_plan(int op, int64_t M, int64_t K, int64_t N, int *plan)
     const int64_t n_out = chain ? K : (L.padded ? round8(N) : N);
     const int64_t k_in = chain ? N : (L.padded ? round8(K) : K);
     const GemmPlan p = plan_gemm(M, n_out, k_in, di.sms, true, L.split_cnt_bytes + L.split_part_bytes);
-    plan[0] = p.pair ? 1 : 0;
+    plan[0] = p.mc ? 2 : (p.pair ? 1 : 0);
     plan[1] = p.bn;
     plan[2] = p.nsub;
     plan[3] = p.splits > 1 ? p.splits : 1;

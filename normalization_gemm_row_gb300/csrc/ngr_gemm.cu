@@ -134,7 +134,7 @@ static int env_int(const char *name, int dflt)
     const char *e = std::getenv(name);
     return (e && e[0]) ? std::atoi(e) : dflt;
 }
-static std::atomic<int> g_pair{env_int("NGR_PAIR", -1) < 0 ? -1 : (env_int("NGR_PAIR", -1) ? 1 : 0)};
+static std::atomic<int> g_pair{env_int("NGR_PAIR", -1) < 0 ? -1 : (env_int("NGR_PAIR", -1) > 2 ? 1 : env_int("NGR_PAIR", -1))};
 static std::atomic<int> g_bn{env_int("NGR_BN", 0)};
 static std::atomic<int> g_nsub{env_int("NGR_NSUB", 0)};
 // NGR_MAX_SPLITS caps the K split (1 = never split).
@@ -142,7 +142,7 @@ static const int g_max_splits = env_int("NGR_MAX_SPLITS", 2);
 
 int set_tile_config(int pair, int bn, int nsub)
 {
-    if (pair < -1 || pair > 1) return -9;
+    if (pair < -1 || pair > 2) return -9;
     if (bn != 0 && bn != 128 && bn != 192 && bn != 224 && bn != 256) return -9;
     if (nsub < 0 || nsub > 2) return -9;
     if (nsub == 2 && (pair == 0 || (bn != 0 && bn != 192 && bn != 224 && bn != 256))) return -9;
@@ -209,10 +209,36 @@ static GemmPlan plan_with(int64_t M, int64_t N, int64_t K, int num_sms, int want
     return best;
 }
 
+// Clusters of four of the multicast kernel resident at once (cached per
+// device).
+static int max_clusters4()
+{
+    static std::mutex mu;
+    static int cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev] == 0) {
+        const int n = gemm4_clusters();
+        cache[dev] = n > 0 ? n : -1;
+    }
+    return cache[dev] > 0 ? cache[dev] : 0;
+}
+
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, bool norm,
                    size_t max_split_bytes)
 {
-    (void)norm;
+    if (g_pair.load() == 2 && norm && M > 2 * kBM) {
+        const int clusters = max_clusters4();
+        if (clusters > 0) {
+            const int64_t tiles = ((M + kMcRows - 1) / kMcRows) * ((N + kMcCols - 1) / kMcCols);
+            GemmPlan p{224, 5, static_cast<int>(4 * (tiles < clusters ? tiles : clusters)), 0, true,
+                       kMcRows, 56, 2, kMcCols, false, 1};
+            p.mc = true;
+            p.smem = gemm4_smem_bytes();
+            return p;
+        }
+    }
     double cost = -1.0;
     GemmPlan best = plan_with(M, N, K, num_sms, g_pair.load(), g_bn.load(), g_nsub.load(),
                               max_split_bytes, &cost);
@@ -249,6 +275,7 @@ GemmPlan plan_gemm_gated(int64_t M, int64_t N, int num_sms)
 int launch_gemm(int norm, bool bf16, const GemmPlan &plan, const GemmArgs &args, bool pdl,
                 cudaStream_t stream)
 {
+    if (plan.mc) return launch_gemm4(norm, bf16, args, plan.grid, pdl, stream);
     if (plan.gated) {
         switch (plan.bn) {
         case 192: return launch_gemm2g_bn192(norm, bf16, args, plan.grid, pdl, stream);

@@ -113,22 +113,23 @@ __device__ __forceinline__ void st_global_v8(void *p, const uint32_t (&w)[8])
 // 16-byte pieces.
 template <bool BF16>
 __device__ __forceinline__ void store_row32(const float (&v)[32], int row, int n0, void *y, int M,
-                                            int N)
+                                            int N, int n_lim = -1)
 {
     if (row >= M) return;
+    if (n_lim < 0) n_lim = N;     // columns stored: [n0, min(n0 + 32, n_lim)); row pitch N
     uint16_t *yrow = static_cast<uint16_t *>(y) + static_cast<int64_t>(row) * N;
     uint32_t o[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) o[j] = from_float2<BF16>(v[2 * j], v[2 * j + 1]);
     const bool sectors = ((reinterpret_cast<uintptr_t>(y) | static_cast<uintptr_t>(N) * 2u) & 31u) == 0;
-    if (sectors && n0 + 32 <= N) {
+    if (sectors && n0 + 32 <= n_lim) {
         st_global_v8(yrow + n0, *reinterpret_cast<const uint32_t(*)[8]>(&o[0]));
         st_global_v8(yrow + n0 + 16, *reinterpret_cast<const uint32_t(*)[8]>(&o[8]));
         return;
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-        if (n0 + 8 * j < N)
+        if (n0 + 8 * j < n_lim)
             *reinterpret_cast<uint4 *>(yrow + n0 + 8 * j) =
                 make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
 }
@@ -270,9 +271,10 @@ __device__ __forceinline__ uint4 transform8_rms16(uint4 v, uint32_t s2, const ui
 // by so.x (the row's rstd, left out of an RMSNorm transform).
 template <int NORM, bool BF16, bool ROW_SCALE_OUT = false>
 __device__ __forceinline__ void epilogue_store32(float (&v)[32], int row, int n0,
-                                                 const GemmArgs &args, float2 so)
+                                                 const GemmArgs &args, float2 so, int n_lim = -1)
 {
-    const int M = args.M, N = args.N;
+    // Columns at or past n_lim (default N) are neither read nor stored.
+    const int M = args.M, N = n_lim < 0 ? args.N : n_lim;
     if constexpr (ROW_SCALE_OUT) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] *= so.x;
@@ -313,7 +315,7 @@ __device__ __forceinline__ void epilogue_store32(float (&v)[32], int row, int n0
     }
     apply_act32(args.act, v);
     if (args.residual != nullptr && row < M) {
-        const uint16_t *rrow = static_cast<const uint16_t *>(args.residual) + static_cast<int64_t>(row) * N;
+        const uint16_t *rrow = static_cast<const uint16_t *>(args.residual) + static_cast<int64_t>(row) * args.N;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             if (n0 + 8 * j < N) {
@@ -328,7 +330,7 @@ __device__ __forceinline__ void epilogue_store32(float (&v)[32], int row, int n0
             }
         }
     }
-    store_row32<BF16>(v, row, n0, args.y, M, N);
+    store_row32<BF16>(v, row, n0, args.y, M, args.N, N);
 }
 
 // (rstd, -mu rstd) of `row` for the folded epilogue.
@@ -359,12 +361,18 @@ __device__ __forceinline__ float2 fold_row_scale(const GemmArgs &args, int row)
 // After its stores each thread fences them for the async proxy.
 // m0_of(unit) gives the unit's first x row in this CTA and kb_count(unit)
 // the number of k blocks the unit covers (all of them unless K is split).
+// gamma/beta come from each stage's FP32 box in shared memory (sG), or,
+// with GB_GLOBAL, from the FP32 rows g_glob / b_glob in global memory: a
+// thread then issues the loads of its chunks before waiting for the stage
+// (they do not depend on it) and treats columns at or past K as zero.
 template <int NORM, bool BF16, int STAGES, int KA, int PARTS = 1, bool ROW_SCALE = true,
-          typename M0Fn, typename KbFn, typename ArriveFn>
+          bool GB_GLOBAL = false, typename M0Fn, typename KbFn, typename ArriveFn>
 __device__ __forceinline__ void transform_role(int t, int tile0, int tile_step, int num_tiles,
                                                KbFn kb_count, int M, const float2 *stats,
                                                uint8_t *sA, const float *sG, uint64_t *full,
-                                               const WaitCtx &wc, M0Fn m0_of, ArriveFn arrive)
+                                               const WaitCtx &wc, M0Fn m0_of, ArriveFn arrive,
+                                               const float *g_glob = nullptr,
+                                               const float *b_glob = nullptr, int K = 0)
 {
     static_assert(PARTS == 1 || PARTS == 2 || PARTS == 4, "a part is a whole number of 16-byte chunks");
     static_assert(kGroupThreads == 128 || kGroupThreads == 256, "a group is 4 or 8 warps");
@@ -403,20 +411,44 @@ __device__ __forceinline__ void transform_role(int t, int tile0, int tile_step, 
         const int k_blocks = kb_count(tile);
         for (int kb = 0; kb < k_blocks; ++kb, ++it) {
             if (it % kTransformGroups == g) {
+                float4 qg[GB_GLOBAL ? PARTS : 1][4];
+                if constexpr (GB_GLOBAL) {
+#pragma unroll
+                    for (int part = 0; part < PARTS; ++part) {
+                        const int col = kb * kBK + 8 * (cl + kCP * part);
+                        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+                        const bool in = col < K;
+                        qg[part][0] = in ? __ldg(reinterpret_cast<const float4 *>(g_glob + col)) : z;
+                        qg[part][1] = in ? __ldg(reinterpret_cast<const float4 *>(g_glob + col + 4)) : z;
+                        if constexpr (NORM == kNormLayer) {
+                            qg[part][2] = in ? __ldg(reinterpret_cast<const float4 *>(b_glob + col)) : z;
+                            qg[part][3] = in ? __ldg(reinterpret_cast<const float4 *>(b_glob + col + 4)) : z;
+                        }
+                    }
+                }
                 if (!mbar_wait_warp_spin(&full[stage], phase, wc)) return;
 #pragma unroll
                 for (int part = 0; part < PARTS; ++part) {
                     const int c = cl + kCP * part;    // logical chunk: columns 8c .. 8c+7
-                    // gamma/beta of the chunk; the two halves are read in
-                    // separate instructions so that a quarter-warp touches
-                    // 8 distinct 16-byte slots of one 128-byte line each time.
-                    const float *gp = sG + stage * 2 * kBK + 8 * c;
                     float4 q[4];
-                    q[0] = *reinterpret_cast<const float4 *>(gp);
-                    q[1] = *reinterpret_cast<const float4 *>(gp + 4);
-                    if constexpr (NORM == kNormLayer) {
-                        q[2] = *reinterpret_cast<const float4 *>(gp + kBK);
-                        q[3] = *reinterpret_cast<const float4 *>(gp + kBK + 4);
+                    if constexpr (GB_GLOBAL) {
+                        q[0] = qg[part][0];
+                        q[1] = qg[part][1];
+                        if constexpr (NORM == kNormLayer) {
+                            q[2] = qg[part][2];
+                            q[3] = qg[part][3];
+                        }
+                    } else {
+                        // gamma/beta of the chunk; the two halves are read in
+                        // separate instructions so that a quarter-warp touches
+                        // 8 distinct 16-byte slots of one 128-byte line each time.
+                        const float *gp = sG + stage * 2 * kBK + 8 * c;
+                        q[0] = *reinterpret_cast<const float4 *>(gp);
+                        q[1] = *reinterpret_cast<const float4 *>(gp + 4);
+                        if constexpr (NORM == kNormLayer) {
+                            q[2] = *reinterpret_cast<const float4 *>(gp + kBK);
+                            q[3] = *reinterpret_cast<const float4 *>(gp + kBK + 4);
+                        }
                     }
                     const float2 gg[4] = {make_float2(q[0].x, q[0].y), make_float2(q[0].z, q[0].w),
                                           make_float2(q[1].x, q[1].y), make_float2(q[1].z, q[1].w)};

@@ -56,6 +56,8 @@ struct alignas(128) GemmArgs {
     CUtensorMap map_gb;     // FP32 [2, K] = rows gamma, beta; box {64, 2}
     CUtensorMap map_b2;     // gated (SwiGLU) kernel: the up projection [N, K], like map_b
     const float2 *stats;    // [M] (mu, rstd); unused without a norm
+    const float *gamma_f;   // [K] FP32 gamma (kernels that read it from global memory)
+    const float *beta_f;    // [K] FP32 beta
     const void *bias;       // [N] or nullptr
     const float *fold_c;    // folded forms: c[n] = sum_k W'[n,k] (FP32)
     const float *fold_b;    // folded forms: b'[n] = beta . W[n,:] + bias[n] (FP32)
@@ -119,7 +121,13 @@ struct GemmPlan {
     int tw;          // output tile width in N: bn * nsub, or bn when gated
     bool gated;      // SwiGLU: sub-tile 0 multiplies the gate weight, 1 the up weight
     int splits;      // K ranges per output tile (CTA pair only; 1 = none)
+    bool mc = false; // clusters of two CTA pairs sharing the weight boxes (multicast):
+                     // 512 x 464 super-tiles, sub-tiles 224 + 240, a norm only
 };
+
+// The multicast cluster kernel's super-tile and weight-box geometry.
+constexpr int kMcRows = 512;
+constexpr int kMcCols = 464;
 
 // Bytes of FP32 partials and of counters a split plan needs.
 size_t split_partial_bytes(int64_t num_tiles, int tw, int splits);
@@ -162,6 +170,9 @@ int launch_unpad_rows(const void *src, int64_t rows, int64_t cols, int64_t src_p
 
 int launch_gemm(int norm, bool bf16, const GemmPlan &plan, const GemmArgs &args, bool pdl,
                 cudaStream_t stream);
+int launch_gemm4(int norm, bool bf16, const GemmArgs &args, int grid, bool pdl, cudaStream_t stream);
+int gemm4_clusters();           // resident clusters of four of the multicast kernel
+size_t gemm4_smem_bytes();
 // max_split_bytes: room for split-K partials and counters (0 = never split).
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, bool norm,
                    size_t max_split_bytes = 0);

@@ -162,9 +162,12 @@ extern "C" int ngr_fused_layernorm_linear_noalloc(const void *x, const void *gam
     const GemmPlan plan = plan_gemm(M, N, K, sms, true);
     if (!map_2d(&a.map_a, x, bf16, M, K, kBM) ||
         !map_2d(&a.map_b, W, bf16, N, K, static_cast<uint32_t>(plan.b_rows)) ||
+        (plan.mc && !map_2d(&a.map_b2, W, bf16, N, K, 64)) ||
         !map_gb(&a.map_gb, gamma_f, K, kNaGB))
         return NGR_ERR_CUDA;
     a.stats = stats;
+    a.gamma_f = gamma_f;
+    a.beta_f = beta_f;
     a.bias = bias;
     a.y = y;
     a.err = err;

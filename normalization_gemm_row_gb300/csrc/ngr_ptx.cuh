@@ -196,6 +196,21 @@ __device__ __forceinline__ void tma_load_1d(void *dst, const CUtensorMap *m,
         : "memory");
 }
 
+// The same load delivered to every CTA of the cluster whose bit is set in
+// `cta_mask`, at the same shared-memory offset in each, with completion
+// signalled on the mbarrier at the same offset in each destination CTA.
+__device__ __forceinline__ void tma_load_2d_mc(void *dst, const CUtensorMap *m, uint64_t *bar,
+                                               int c0, int c1, uint16_t cta_mask,
+                                               uint64_t cache_hint)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(cta_mask),
+        "l"(cache_hint)
+        : "memory");
+}
+
 // L2 eviction-priority policies for the cache_hint operand.
 __device__ __forceinline__ uint64_t policy_evict_first()
 {

@@ -1,0 +1,85 @@
+"""GPU parity of the multicast cluster kernel (clusters of two CTA pairs that
+share each weight box; 512 x 464 super-tiles of sub-tiles 224 + 240),
+forced through ngr_set_tile_config(2, 0, 0), against the fp64 oracle.
+
+Shapes cover: a second pair wholly or partly past M (M = 300, 600), several
+super-tiles in M (M = 1112), a last super-tile whose second sub-tile is
+wholly past N (N = 1000: 72 columns), one whose second sub-tile is partly
+past N (N = 700: 236 columns), exactly whole super-tiles (N = 928), a
+ragged last k block (K = 1000) and several k blocks per stage ring turn.
+Bar: |y - y_ref| <= 1e-2 + 1e-2 |y_ref|, every element.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import normalization_gemm_row_gb300 as ngr
+from normalization_gemm_row_gb300 import binding as B
+from normalization_gemm_row_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL = 1e-2, 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ngr.build()
+    oracle.build()
+    torch.cuda.init()
+    yield
+    B.set_tile_config(-1, 0, 0)
+
+
+@pytest.fixture
+def multicast():
+    B.set_tile_config(2, 0, 0)
+    yield
+    B.set_tile_config(-1, 0, 0)
+
+
+def check(got, ref, what):
+    got = got.double().cpu().numpy()
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    err = np.abs(got - ref)
+    bad = err > ATOL + RTOL * np.abs(ref)
+    assert not bad.any(), (f"{what}: {bad.sum()} / {bad.size} out of tolerance, max err "
+                           f"{err.max():.4e} at {np.unravel_index(err.argmax(), err.shape)}")
+
+
+SHAPES = [(600, 1000, 1000), (300, 512, 928), (1112, 4096, 700), (600, 2048, 1856)]
+
+
+@pytest.mark.parametrize("M,K,N", SHAPES)
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
+@pytest.mark.parametrize("op", ["layernorm_linear", "rmsnorm_linear"])
+def test_multicast_against_oracle(multicast, op, dtype, M, K, N):
+    code = B.OP_LAYERNORM_LINEAR if op == "layernorm_linear" else B.OP_RMSNORM_LINEAR
+    assert B.tile_plan(code, M, K, N)["pair"] == 2
+    d = inputs.case(op, M, K, N, dtype, op == "layernorm_linear", 1e-5, seed=M + K + N,
+                    x_mean=2.0 if op == "layernorm_linear" else 0.0,
+                    outlier_frac=0.02 if op == "rmsnorm_linear" else 0.0, outlier_scale=50.0)
+    g = {k: (v.cuda() if isinstance(v, torch.Tensor) and k != "outlier_rows" else v)
+         for k, v in d.items()}
+    ws = torch.empty(B.ngr_workspace_bytes(code, M, K, N), dtype=torch.uint8, device="cuda")
+    if op == "layernorm_linear":
+        y = ngr.fused_layernorm_linear(g["x"], g["gamma"], g["beta"], g["W"], g["bias"], 1e-5,
+                                       workspace=ws)
+        ref = oracle.layernorm_linear(d["x"], d["gamma"], d["beta"], d["W"], d["bias"], 1e-5)
+    else:
+        y = ngr.fused_rmsnorm_linear(g["x"], g["gamma"], g["W"], g["bias"], 1e-5, workspace=ws)
+        ref = oracle.rmsnorm_linear(d["x"], d["gamma"], d["W"], d["bias"], 1e-5)
+    s = torch.cuda.current_stream().cuda_stream
+    assert B.ngr_workspace_error(ws.data_ptr(), s) == 0, "a bounded wait ran out"
+    check(y, ref, f"multicast {op} {dtype} {M}x{K}x{N}")
+
+
+def test_multicast_repeat_is_deterministic(multicast):
+    d = inputs.case("layernorm_linear", 1024, 2048, 1856, torch.float16, True, 1e-5, seed=5)
+    g = {k: (v.cuda() if isinstance(v, torch.Tensor) and k != "outlier_rows" else v)
+         for k, v in d.items()}
+    y1 = ngr.fused_layernorm_linear(g["x"], g["gamma"], g["beta"], g["W"], g["bias"], 1e-5)
+    y2 = ngr.fused_layernorm_linear(g["x"], g["gamma"], g["beta"], g["W"], g["bias"], 1e-5)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
