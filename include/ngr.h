@@ -328,7 +328,9 @@ int ngr_debug_bounded_wait(void *workspace, uint32_t timeout_us,
 /* Tuning aid: restrict the choice of the tile kernel (M > 32) for every
  * later call in this process, on every thread.  `pair`: -1 let the planner
  * decide, 0 the single-CTA kernel (128-row tiles), 1 the CTA-pair kernel
- * (256-row tiles; only taken when M > 128).  `bn`: 0 any, else the N tile
+ * (256-row tiles; only taken when M > 128), 2 the multicast cluster kernel
+ * (clusters of two CTA pairs sharing each weight box, 512 x 464 tiles; only
+ * taken with a LayerNorm or RMSNorm and M > 256; bn and nsub are ignored).  `bn`: 0 any, else the N tile
  * (or sub-tile) width, one of 128, 192, 224, 256.  `nsub`: 0 any, else the
  * N sub-tiles per CTA-pair tile, 1 or 2 (2 only with bn 192, 224 or 256).  The
  * planner picks the cheapest variant that satisfies all three; if none does
@@ -340,7 +342,8 @@ int ngr_set_tile_config(int pair, int bn, int nsub);
 /* Inspection aid: the tile-kernel variant a call of `op` with these sizes
  * would launch on the current device, with a workspace of
  * ngr_workspace_bytes(op, M, K, N, 0) bytes, for its main product (the
- * chains' second product).  Writes plan[0..5] = pair (0/1), N (sub-)tile
+ * chains' second product).  Writes plan[0..5] = pair (0 single CTA, 1 CTA
+ * pair, 2 multicast cluster of two pairs), N (sub-)tile
  * width, sub-tiles per tile, K splits, CTAs, pipeline stages.  Returns
  * NGR_OK, NGR_ERR_ARG (bad op, or a shape that takes the decode or gated
  * kernel), NGR_ERR_NULL, or NGR_ERR_ARCH / NGR_ERR_CUDA. */

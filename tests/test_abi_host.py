@@ -265,8 +265,8 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
 
 
 def test_set_tile_config_arguments(lib):
-    ok = [(-1, 0, 0), (0, 128, 0), (1, 224, 2), (1, 0, 2), (-1, 256, 1)]
-    bad = [(2, 0, 0), (-2, 0, 0), (1, 100, 0), (1, 128, 2), (0, 0, 2), (-1, 0, 3),
+    ok = [(-1, 0, 0), (0, 128, 0), (1, 224, 2), (1, 0, 2), (-1, 256, 1), (2, 0, 0)]
+    bad = [(3, 0, 0), (-2, 0, 0), (1, 100, 0), (1, 128, 2), (0, 0, 2), (-1, 0, 3),
            (-1, 0, -1)]
     try:
         for a in ok:
