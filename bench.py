@@ -210,8 +210,8 @@ def kernel_source_hash() -> str:
     traffic figure still describes the kernel that runs."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "normalization_gemm_row_gb300", "csrc")
-    for name in ("ngr_gemm_kernel.cuh", "ngr_gemm2_kernel.cuh", "ngr_gemm.cu", "ngr_ptx.cuh",
-                 "ngr_internal.h", "ngr_decode.cu"):
+    for name in ("ngr_gemm_kernel.cuh", "ngr_gemm2_kernel.cuh", "ngr_gemm4_kernel.cuh", "ngr_gemm.cu",
+                 "ngr_ptx.cuh", "ngr_internal.h", "ngr_decode.cu", "ngr_rowstats.cu"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]

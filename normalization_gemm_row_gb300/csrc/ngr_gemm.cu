@@ -225,26 +225,58 @@ static int max_clusters4()
     return cache[dev] > 0 ? cache[dev] : 0;
 }
 
+// The multicast cluster kernel (a norm only, M > 256): clusters of two CTA
+// pairs sharing each weight box, 512 x 464 super-tiles.  Measured on GB300
+// against the CTA-pair kernel on the same shapes, it is faster only where
+// every cluster runs at least three super-tiles over a long K (the
+// 512 x 14336 -> 49152 RMSNorm and LayerNorm workloads: 0.966x and 0.976x),
+// and 0.5-2.4 % slower with one or two super-tiles per cluster (1024 and
+// 2048 x 8192 -> 8192, 512 x 8192 -> 28672), where its fill and drain and
+// its 3.6 % wider tiles on 144 of 152 SMs are not repaid.  So the planner
+// takes it when each cluster gets at least three super-tiles and its
+// columns per SM stay within 4 % of the pair plan's.
+static bool prefer_multicast(int64_t M, int64_t N, const GemmPlan &pair_plan, int num_sms)
+{
+    const int clusters = max_clusters4();
+    if (clusters <= 0 || M <= 2 * kBM) return false;
+    const int64_t super = ((M + kMcRows - 1) / kMcRows) * ((N + kMcCols - 1) / kMcCols);
+    const int64_t per_cluster = (super + clusters - 1) / clusters;
+    if (per_cluster < 3) return false;
+    if (!pair_plan.pair) return false;
+    const int64_t tiles = ((M + pair_plan.bm - 1) / pair_plan.bm) * ((N + pair_plan.tw - 1) / pair_plan.tw) *
+                          pair_plan.splits;
+    const int64_t pairs = pair_plan.grid / 2;
+    const int64_t per_pair = (tiles + pairs - 1) / pairs;
+    (void)num_sms;
+    return static_cast<double>(per_cluster * kMcCols) <=
+           1.04 * static_cast<double>(per_pair * pair_plan.tw) / pair_plan.splits;
+}
+
+static GemmPlan multicast_plan(int64_t M, int64_t N)
+{
+    const int clusters = max_clusters4();
+    const int64_t super = ((M + kMcRows - 1) / kMcRows) * ((N + kMcCols - 1) / kMcCols);
+    GemmPlan p{224, 5, static_cast<int>(4 * (super < clusters ? super : clusters)), 0, true,
+               kMcRows, 56, 2, kMcCols, false, 1};
+    p.mc = true;
+    p.smem = gemm4_smem_bytes();
+    return p;
+}
+
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, bool norm,
                    size_t max_split_bytes)
 {
-    if (g_pair.load() == 2 && norm && M > 2 * kBM) {
-        const int clusters = max_clusters4();
-        if (clusters > 0) {
-            const int64_t tiles = ((M + kMcRows - 1) / kMcRows) * ((N + kMcCols - 1) / kMcCols);
-            GemmPlan p{224, 5, static_cast<int>(4 * (tiles < clusters ? tiles : clusters)), 0, true,
-                       kMcRows, 56, 2, kMcCols, false, 1};
-            p.mc = true;
-            p.smem = gemm4_smem_bytes();
-            return p;
-        }
-    }
+    const int want = g_pair.load();
+    if (want == 2 && norm && M > 2 * kBM && max_clusters4() > 0) return multicast_plan(M, N);
     double cost = -1.0;
-    GemmPlan best = plan_with(M, N, K, num_sms, g_pair.load(), g_bn.load(), g_nsub.load(),
+    GemmPlan best = plan_with(M, N, K, num_sms, want == 2 ? -1 : want, g_bn.load(), g_nsub.load(),
                               max_split_bytes, &cost);
     if (cost < 0) best = plan_with(M, N, K, num_sms, -1, 0, 0, max_split_bytes, &cost);
     best.smem = best.pair ? gemm2_smem_bytes(best.bn, best.nsub)
                           : gemm_smem_bytes(best.bn, best.stages, true);
+    if (want == -1 && norm && g_bn.load() == 0 && g_nsub.load() == 0 &&
+        prefer_multicast(M, N, best, num_sms))
+        return multicast_plan(M, N);
     return best;
 }
 
