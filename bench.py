@@ -655,12 +655,14 @@ def our_arm(args, rank, world, local, workload, m_override):
             torch.cuda.synchronize(dev)
             return o0.elapsed_time(o1) / args.steps
 
-        # Three windows of K steps of each, alternating, so that both sides
-        # see the same clocks; medians.
+        # Three windows of K steps of each, alternating (the side that goes
+        # first alternates too), each after a short idle gap, so that both
+        # sides see the same clocks and power state; medians.
         tw, ow = [], []
-        for _ in range(3):
-            tw.append(twindow())
-            ow.append(owindow())
+        for i in range(3):
+            for side in ((twindow, tw), (owindow, ow))[::1 if i % 2 == 0 else -1]:
+                time.sleep(0.2)
+                side[1].append(side[0]())
         tms = statistics.median(tw)
         oms = statistics.median(ow)
         alternatives["torch_unfused_same_gpu"] = {

@@ -110,7 +110,13 @@ constexpr double kPairCostFactor = 1.0;
 constexpr double kWideCostFactor = 0.8;
 constexpr int kWideTileOverhead = 32;
 constexpr int kSplitOverhead = 24;
-constexpr int kMinKbPerSplit = 16;
+// A K split pays only when each half keeps a long K: its fill, drain and
+// partial reduction are fixed costs.  Measured on GB300 (alternating runs):
+// at 512 x 8192 -> 8192 (64 k blocks per half) the split 448-column plan
+// takes 55.3 us against 52.0 for unsplit 256 x 224 pair tiles, while at
+// 512 x 28672 -> 8192 (224 k blocks per half) it is the fastest (147.0
+// against 150-153).
+constexpr int kMinKbPerSplit = 128;
 
 size_t split_partial_bytes(int64_t num_tiles, int tw, int splits)
 {

@@ -18,10 +18,11 @@
 // var = M2 / K (biased), rstd = 1 / sqrt(var + eps).  RMSNorm: rstd =
 // 1 / sqrt(sum x^2 / K + eps) and mu = 0.
 //
-// For decode-sized batches the kernel also writes the normalized rows
+// On request the kernel also writes the normalized rows
 // xhat = (x - mu) rstd gamma + beta (RMSNorm: x rstd gamma), with the FP32
-// arithmetic and the single rounding of the tile kernel's transform, so that
-// the weight-streaming kernel multiplies them without re-normalizing.
+// arithmetic and the single rounding of the tile kernel's transform: the
+// norm that follows a product writes its output this way (the fused
+// pre-norm paths never write normalized rows).
 //
 // When the rows are padded (K is the padded pitch, a multiple of 8), only the
 // first k_valid columns count: the padding is excluded from the LayerNorm

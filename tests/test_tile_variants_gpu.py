@@ -122,7 +122,7 @@ def split_config(request):
     B.set_tile_config(-1, 0, 0)
 
 
-SM, SK, SN = 300, 4096, 1000   # few output tiles, 64 k blocks: the planner splits K in two
+SM, SK, SN = 300, 16384, 1000  # few output tiles, 256 k blocks: the planner splits K in two
 
 
 def test_split_k_is_planned(split_config):
@@ -175,15 +175,18 @@ def test_split_k_is_deterministic():
     assert torch.equal(ys[0], ys[1]) and torch.equal(ys[0], ys[2])
 
 
-def test_split_k_default_plan_llama_output_projection():
-    """512 x 8192 x 8192 (38 wide tiles for 76 pairs): the default plan
-    splits K; sampled rows against the oracle."""
-    plan = B.tile_plan(B.OP_LINEAR_SILU, 512, 8192, 8192)
+def test_split_k_default_plan_llama_down_projection():
+    """512 x 28672 -> 8192 (38 wide tiles for 76 pairs, 448 k blocks): the
+    default plan splits K; 512 x 8192 -> 8192 (128 k blocks) does not, its
+    halves would be too short to repay the split.  Sampled rows against the
+    oracle."""
+    assert B.tile_plan(B.OP_LINEAR_SILU, 512, 8192, 8192)["splits"] == 1
+    plan = B.tile_plan(B.OP_LINEAR_SILU, 512, 28672, 8192)
     assert plan["splits"] == 2, plan
-    d = inputs.case("linear_silu", 512, 8192, 8192, torch.bfloat16, True, 0.0, seed=26)
+    d = inputs.case("linear_silu", 512, 28672, 8192, torch.bfloat16, True, 0.0, seed=26)
     g = to_dev(d)
     y = ngr.fused_linear_silu(g["x"], g["W"], g["bias"])
     torch.cuda.synchronize()
     rows = inputs.sample_rows(512, 12, seed=3, always=(0, 255, 256, 511)).tolist()
     got = y[torch.as_tensor(rows, device="cuda")]
-    check(got, oracle.linear_silu(d["x"], d["W"], d["bias"], rows), "split default 512x8192")
+    check(got, oracle.linear_silu(d["x"], d["W"], d["bias"], rows), "split default 512x28672")
