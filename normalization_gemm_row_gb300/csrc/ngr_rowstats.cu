@@ -134,11 +134,14 @@ constexpr int kStatsThreads = 256;
 // 16-byte loads of the row at once, so a row costs one memory round trip.
 // At most 32 registers, so that 8 CTAs (2048 threads) fit on an SM and the
 // rows of a batch of up to 8 x SMs run in a single wave.  The variant that
-// also writes the normalized rows serves at most 32 rows and is not capped.
+// also writes the normalized rows (the norm after a product) holds a row of
+// up to 8192 elements in registers between its two passes and runs at most
+// 64 registers, 4 CTAs per SM.
 constexpr int kStatsCtasPerSm = 8;
+constexpr int kXhatCtasPerSm = 4;
 
 template <int NORM, bool BF16, bool XHAT>
-__global__ void __launch_bounds__(kStatsThreads, XHAT ? 1 : kStatsCtasPerSm) rowstats_kernel(
+__global__ void __launch_bounds__(kStatsThreads, XHAT ? kXhatCtasPerSm : kStatsCtasPerSm) rowstats_kernel(
     const uint4 *__restrict__ x, int64_t M, int64_t K, float eps,
     float2 *__restrict__ stats, const void *__restrict__ gamma,
     const void *__restrict__ beta, float *__restrict__ gamma_f,
@@ -178,6 +181,9 @@ __global__ void __launch_bounds__(kStatsThreads, XHAT ? 1 : kStatsCtasPerSm) row
     __shared__ float red[3][kStatsThreads / 32];
     __shared__ float2 row_stats;
     const int64_t vec_per_row = K >> 3;  // 8 elements per 16-byte vector
+    // With XHAT and rows of at most 4 vectors per thread (K <= 8192) the
+    // statistics pass keeps the row in registers for the output pass.
+    uint4 keep[4];
     for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
         const uint4 *xr = x + row * vec_per_row;
         if constexpr (NORM == kNormLayer) {
@@ -199,6 +205,10 @@ __global__ void __launch_bounds__(kStatsThreads, XHAT ? 1 : kStatsCtasPerSm) row
                 for (int u = 0; u < 4; ++u) {
                     const int v = v0 + u * kStatsThreads;
                     q[u] = v < nvec ? __ldg(xr + v) : make_uint4(hh, hh, hh, hh);
+                }
+                if constexpr (XHAT) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) keep[u] = q[u];
                 }
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
@@ -263,6 +273,10 @@ __global__ void __launch_bounds__(kStatsThreads, XHAT ? 1 : kStatsCtasPerSm) row
                     const int64_t v = v0 + static_cast<int64_t>(u) * kStatsThreads;
                     if (v < vec_per_row) q[u] = __ldg(xr + v);
                 }
+                if constexpr (XHAT) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) keep[u] = q[u];
+                }
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int64_t v = v0 + static_cast<int64_t>(u) * kStatsThreads;
@@ -292,11 +306,30 @@ __global__ void __launch_bounds__(kStatsThreads, XHAT ? 1 : kStatsCtasPerSm) row
             const uint4 *gv = static_cast<const uint4 *>(gamma);
             const uint4 *bv = static_cast<const uint4 *>(beta);
             uint4 *out = xhat + row * vec_per_row;
+            if (vec_per_row <= 4 * kStatsThreads) {
+                // The row is in registers (keep[u] = vector tid + u threads):
+                // all gamma/beta loads in flight at once, then the stores.
+                uint4 gq[4], bq[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int64_t v = tid + static_cast<int64_t>(u) * kStatsThreads;
+                    if (v < vec_per_row) {
+                        gq[u] = __ldg(gv + v);
+                        bq[u] = NORM == kNormLayer ? __ldg(bv + v) : make_uint4(0, 0, 0, 0);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int64_t v = tid + static_cast<int64_t>(u) * kStatsThreads;
+                    if (v < vec_per_row) out[v] = normalize8<NORM, BF16>(keep[u], gq[u], bq[u], sc, of);
+                }
+            } else {
 #pragma unroll 1
-            for (int64_t v = tid; v < vec_per_row; v += kStatsThreads)
-                out[v] = normalize8<NORM, BF16>(__ldg(xr + v), __ldg(gv + v),
-                                                NORM == kNormLayer ? __ldg(bv + v) : make_uint4(0, 0, 0, 0),
-                                                sc, of);
+                for (int64_t v = tid; v < vec_per_row; v += kStatsThreads)
+                    out[v] = normalize8<NORM, BF16>(__ldg(xr + v), __ldg(gv + v),
+                                                    NORM == kNormLayer ? __ldg(bv + v) : make_uint4(0, 0, 0, 0),
+                                                    sc, of);
+            }
             __syncthreads();   // row_stats is rewritten by the next row
         }
     }
@@ -311,7 +344,7 @@ int launch_rowstats(int norm, bool bf16, const void *x, int64_t M, int64_t K,
     if (k_valid < 0) k_valid = K;
     const int threads = kStatsThreads;
     int64_t blocks = M;
-    const int64_t cap = static_cast<int64_t>(num_sms) * kStatsCtasPerSm;   // one wave
+    const int64_t cap = static_cast<int64_t>(num_sms) * (xhat ? kXhatCtasPerSm : kStatsCtasPerSm);   // one wave
     if (blocks > cap) blocks = cap;
     const int64_t kblocks = (K + threads - 1) / threads;
     if (gamma_f && blocks < kblocks) blocks = kblocks < cap ? kblocks : cap;
