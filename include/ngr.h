@@ -342,7 +342,8 @@ int ngr_set_tile_config(int pair, int bn, int nsub);
 /* Inspection aid: the tile-kernel variant a call of `op` with these sizes
  * would launch on the current device, with a workspace of
  * ngr_workspace_bytes(op, M, K, N, 0) bytes, for its main product (the
- * chains' second product).  Writes plan[0..5] = pair (0 single CTA, 1 CTA
+ * chains' second product; NGR_OP_NORM_LINEAR is planned as if it had a
+ * norm).  Writes plan[0..5] = pair (0 single CTA, 1 CTA
  * pair, 2 multicast cluster of two pairs), N (sub-)tile
  * width, sub-tiles per tile, K splits, CTAs, pipeline stages.  Returns
  * NGR_OK, NGR_ERR_ARG (bad op, or a shape that takes the decode or gated

@@ -1270,7 +1270,12 @@ int ngr_tile_plan(int op, int64_t M, int64_t K, int64_t N, int *plan)
     const WsLayout L = ws_layout(op, M, K, N, false);
     const int64_t n_out = chain ? K : (L.padded ? round8(N) : N);
     const int64_t k_in = chain ? N : (L.padded ? round8(K) : K);
-    const GemmPlan p = plan_gemm(M, n_out, k_in, di.sms, true, L.split_cnt_bytes + L.split_part_bytes);
+    // the products with a norm on their input: the single layers' (the
+    // general layer's taken as normalized); the chains' second product and
+    // the post-norm op's product have none
+    const bool in_norm = op == NGR_OP_LAYERNORM_LINEAR || op == NGR_OP_RMSNORM_LINEAR ||
+                         op == NGR_OP_NORM_LINEAR;
+    const GemmPlan p = plan_gemm(M, n_out, k_in, di.sms, in_norm, L.split_cnt_bytes + L.split_part_bytes);
     plan[0] = p.mc ? 2 : (p.pair ? 1 : 0);
     plan[1] = p.bn;
     plan[2] = p.nsub;

@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                 if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
             }
             umma_commit(drain);
-            mbar_wait(drain, 0, wc);
+            mbar_wait_long(drain, 0, wc);
         }
     } else if (warp >= 4 && warp < 8) {
         // -------------------------------- token slice: normalize in place
@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = t0; t < t1; ++t) {
-            if (!mbar_wait_warp(&acc_full[acc], acc_phase, wc)) break;
+            if (!mbar_wait_warp_long(&acc_full[acc], acc_phase, wc)) break;
             tc_fence_after();
             float v[MN];
             {

@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 if (++acc == kAccBufs) { acc = 0; acc_phase ^= 1u; }
             }
             umma_commit_pair(drain, 0x1);
-            mbar_wait(drain, 0, wc);
+            mbar_wait_long(drain, 0, wc);
         }
     } else if (warp >= kTransformWarp0) {
         const bool epi_warp = warp >= kEpilogueWarp0;
@@ -336,7 +336,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             prefetch_l1(static_cast<const uint16_t *>(args.bias) + nt0 + c);
                     }
                 }
-                if (!mbar_wait_warp(&acc_full[cur], cur_phase, wc)) break;
+                if (!mbar_wait_warp_long(&acc_full[cur], cur_phase, wc)) break;
                 tc_fence_after();
                 const int row = (tile % m_tiles) * 2 * kBM + static_cast<int>(rank) * kBM + q * 32 + lane;
                 float2 so = fold_row_scale<NORM>(args, row);

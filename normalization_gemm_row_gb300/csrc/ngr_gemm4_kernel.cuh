@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 acc_phase ^= 1u;
             }
             umma_commit_pair(drain, static_cast<uint16_t>(1u << crank));
-            mbar_wait(drain, 0, wc);
+            mbar_wait_long(drain, 0, wc);
         }
     } else if (warp >= kTransformWarp0) {
         const bool epi_warp = warp >= kEpilogueWarp0;
@@ -260,7 +260,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const int step = (helped ? 3 : 1);
                 const int nt0 = (su / m_tiles) * kMcTW;
                 const int ncols = min(kMcTW, N - nt0);
-                if (!mbar_wait_warp(&acc_full[0], cur_phase, wc)) break;
+                if (!mbar_wait_warp_long(&acc_full[0], cur_phase, wc)) break;
                 tc_fence_after();
                 const int row = m0_of(su) + q * 32 + lane;
                 float2 so = make_float2(1.f, 0.f);

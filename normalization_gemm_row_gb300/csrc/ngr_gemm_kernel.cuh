@@ -654,7 +654,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             // All MMAs issued by this thread complete before TMEM is freed.
             umma_commit(drain);
-            mbar_wait(drain, 0, wc);
+            mbar_wait_long(drain, 0, wc);
         }
     } else if (warp >= kTransformWarp0 && warp < kEpilogueWarp0) {
         if constexpr (kNorm) {
@@ -673,7 +673,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int N = args.N;
         if constexpr (is_fold(NORM)) pdl_wait();  // row statistics from the previous grid
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-            if (!mbar_wait_warp(&acc_full[acc], acc_phase, wc)) break;
+            if (!mbar_wait_warp_long(&acc_full[acc], acc_phase, wc)) break;
             tc_fence_after();
             const int row = (tile % m_tiles) * kBM + q * 32 + lane;
             const float2 so = fold_row_scale<NORM>(args, row);

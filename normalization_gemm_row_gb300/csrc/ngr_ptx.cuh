@@ -151,6 +151,51 @@ __device__ __forceinline__ bool mbar_wait_warp_spin(uint64_t *bar, uint32_t pari
     return ok != 0;
 }
 
+// The bounded wait for phases that take long to come (a tile's accumulator
+// for the epilogue, the last commit before a kernel exits): a test, then a
+// short sleep, repeated.  A waiting warp costs few issue slots, and it
+// resumes within about NGR_NAP_NS of the phase completing, whereas a
+// try_wait may suspend the thread for microseconds past it (measured:
+// four such waits in a row added about 20 us to a kernel's tail).
+// NGR_LONG_WAIT_NAP=0 selects the suspending form.
+#ifndef NGR_NAP_NS
+#define NGR_NAP_NS 128
+#endif
+#ifndef NGR_LONG_WAIT_NAP
+#define NGR_LONG_WAIT_NAP 1
+#endif
+__device__ __forceinline__ bool mbar_wait_long(uint64_t *bar, uint32_t parity, const WaitCtx &w)
+{
+#if NGR_LONG_WAIT_NAP == 0
+    return mbar_wait(bar, parity, w);
+#else
+    if (mbar_test_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        __nanosleep(NGR_NAP_NS);
+        if (mbar_test_wait(bar, parity)) return true;
+        if ((it & 15u) == 0) {
+            if (*reinterpret_cast<volatile int *>(w.abort) != 0) return false;
+            if (global_timer_ns() - t0 > w.timeout_ns) {
+                *reinterpret_cast<volatile int *>(w.abort) = 1;
+                atomicExch(w.err, kDevErrTimeout);
+                return false;
+            }
+        }
+    }
+#endif
+}
+
+// Warp-uniform form of mbar_wait_long (lane 0 waits).
+__device__ __forceinline__ bool mbar_wait_warp_long(uint64_t *bar, uint32_t parity, const WaitCtx &w)
+{
+    int ok = 0;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait_long(bar, parity, w) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) (void)mbar_try_wait(bar, parity);
+    return ok != 0;
+}
+
 // Warp-uniform form for roles whose next step is warp-collective: lane 0
 // waits, the verdict is broadcast, and every lane then acquires the
 // completed phase itself.  All 32 lanes must call it.

@@ -278,3 +278,32 @@ def test_linear_residual_norm_llama_output_projection():
                                              None, 1e-5, rows)
     check(h[idx], href, "llama o-proj h")
     check(y[idx], yref, "llama o-proj y")
+
+
+@pytest.mark.parametrize("M,N", [(512, 4096), (2048, 8192)], ids=["one-wave", "multi-wave"])
+@pytest.mark.parametrize("norm", ["rms", "layer"])
+def test_linear_residual_norm_row_mean(norm, M, N):
+    """The norm after the product with rows whose mean is well above their
+    spread (the residual is centred at 8), on a grid of one wave of tiles and
+    on one of several, against the oracle; fp16, whose spacing there (2^-7)
+    keeps the rounding of the stored h -- which the norm reads, as the
+    unfused norm would -- far inside the bar.  Two calls agree bit for bit."""
+    K = 256
+    dt = torch.float16
+    d = inputs.case("norm_linear", M, K, N, dt, True, 1e-5, seed=M + N, norm="none")
+    g = torch.Generator().manual_seed(N)
+    res = (torch.randn((M, N), generator=g) + 8.0).to(dt)
+    gamma = (1.0 + 0.1 * torch.randn((N,), generator=g)).to(dt)
+    beta = (0.1 * torch.randn((N,), generator=g)).to(dt) if norm == "layer" else None
+    args = (dev(d["x"]), dev(d["W"]), dev(gamma))
+    kw = dict(norm=NORMS[norm][1], beta=dev(beta), bias=dev(d["bias"]), residual=dev(res), eps=1e-5)
+    h, y = ngr.fused_linear_residual_norm(*args, **kw)
+    h2, y2 = ngr.fused_linear_residual_norm(*args, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y2) and torch.equal(h, h2)
+    rows = inputs.sample_rows(M, 64, seed=3).tolist()
+    idx = torch.as_tensor(rows, device="cuda")
+    href, yref = oracle.linear_residual_norm(NORMS[norm][0], d["x"], d["W"], d["bias"], res,
+                                             gamma, beta, 1e-5, rows)
+    check(h[idx], href, f"post-norm h {norm} {M}x{K}x{N}")
+    check(y[idx], yref, f"post-norm y {norm} {M}x{K}x{N}")
