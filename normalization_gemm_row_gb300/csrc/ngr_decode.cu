@@ -170,9 +170,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                 int s = stage - j;
                 uint32_t p = phase;
                 if (s < 0) { s += STAGES; p ^= 1u; }
-                mbar_wait(&full[s], p, wc);
+                mbar_wait_long(&full[s], p, wc);
             }
-            for (int q = 0; ok && q < kDecodeSliceParts; ++q) mbar_wait(&x_full[q], 0, wc);
+            for (int q = 0; ok && q < kDecodeSliceParts; ++q) mbar_wait_long(&x_full[q], 0, wc);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             named_bar_sync(1, 128);
         }
         for (int q = 0; q < kDecodeSliceParts; ++q) {
-            if (!mbar_wait_warp(&x_full[q], 0, wc)) break;
+            if (!mbar_wait_warp_long(&x_full[q], 0, wc)) break;
             if constexpr (kNorm) {
                 constexpr int kRowBatch = 8;
                 const int cc_end = (q * pkb + part_blocks(q)) * 8;
