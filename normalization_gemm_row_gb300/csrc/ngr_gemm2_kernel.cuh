@@ -23,14 +23,21 @@
 // Llama2 inference, model structure and fusion opportunities: the FFN's
 // SiLU-gated linear transform fused with its matmuls).
 //
+// The gated tiles with a norm keep x and W in separate rings: a deeper x
+// ring that warp 0 fills and the transform normalizes ahead of the MMAs,
+// and a W ring that warp 3 fills (split_rings).
+//
 // Synchronization (barriers are per CTA unless marked "leader"):
-//   full[s]        with a norm: this CTA's copies landed (its producer's
-//                  expect_tx); without: the leader's, on which both CTAs'
-//                  copies complete (cta_group::2 TMA) -- the MMA waits on it;
+//   full[s]        with a norm: this CTA's copies of (x) stage s landed (its
+//                  producer's expect_tx); without: the leader's, on which
+//                  both CTAs' copies complete (cta_group::2 TMA) -- the MMA
+//                  waits on it;
 //   ready[s, p]    leader, with a norm: each transform warp of both CTAs
-//                  arrives once column part p of its CTA's stage is
+//                  arrives once column part p of its CTA's (x) stage is
 //                  normalized (the MMAs of that part's K steps wait on it);
 //   empty[s]       the leader's tcgen05.commit, multicast to both CTAs;
+//   wfull[s], wempty[s]  split rings: W stage s, the leader's barrier on
+//                  which both CTAs' W copies complete, and its release;
 //   acc_full[a]    the leader's commit at the end of a tile, multicast;
 //   acc_empty[a]   leader: each draining warp of both CTAs arrives after
 //                  reading its share of accumulator a.
@@ -61,28 +68,63 @@ constexpr int kMaxParts = 4;
 #endif
 
 
-template <int BN, int STAGES, int NSUB>
+// With a norm, x and W stages can live in separate rings (SPLIT): the W
+// ring is one stage shorter than the unified ring of the same tile, and the
+// x ring (x box + FP32 gamma/beta box per stage) takes the shared memory
+// left, so the transform normalizes x stages ahead of the MMAs that consume
+// them.  Measured on GB300: the gated (SwiGLU) tiles run 6 % faster split
+// (512 x 8192 -> 2 x 28672, RMSNorm, bf16), the plain two-sub-tile tiles
+// 1-5 % slower (their W ring's lost stage costs more than the transform's
+// latency); so the gated variants split.  NGR_SPLIT_RINGS: 0 never,
+// 1 gated tiles (default), 2 every tile with a norm and two sub-tiles.
+#ifndef NGR_SPLIT_RINGS
+#define NGR_SPLIT_RINGS 1
+#endif
+constexpr int kSmemLimit = 232448;   // dynamic shared memory per CTA (227 KB)
+
+template <int BN, int STAGES, int NSUB, bool SPLIT = false>
 struct Gemm2Smem {
     static constexpr int kA = kBM * kBK * 2;          // 16 KB: this CTA's 128 x rows
     static constexpr int kBSub = (BN / 2) * kBK * 2;  // this CTA's BN/2 W rows of one sub-tile
     static constexpr int kB = NSUB * kBSub;
     static constexpr int kGB = 2 * kBK * 4;           // FP32 gamma[64], beta[64]
+    // Ring depths: W stages, and x stages (equal without SPLIT).
+    static constexpr int kBStages = SPLIT ? STAGES - 1 : STAGES;
+    static constexpr int kMaxAStages = 12;
+    static constexpr int kBarReserve = 8 * ((2 + kMaxParts) * kMaxAStages + 2 * STAGES + 5) + 16;
+    static constexpr int kAFit = (kSmemLimit - 1024 - kBarReserve - kBStages * kB) / (kA + kGB);
+    static constexpr int kAStages = SPLIT ? (kAFit < kMaxAStages ? kAFit : kMaxAStages) : STAGES;
     static constexpr int off_a = 0;
-    static constexpr int off_b = off_a + STAGES * kA;
-    static constexpr int off_g = off_b + STAGES * kB;
-    static constexpr int off_bar = off_g + STAGES * kGB;
-    static constexpr int n_bars = (2 + kMaxParts) * STAGES + 5;
+    static constexpr int off_b = off_a + kAStages * kA;
+    static constexpr int off_g = off_b + kBStages * kB;
+    static constexpr int off_bar = off_g + kAStages * kGB;
+    // full/empty/ready[parts] per x stage (per unified stage without
+    // SPLIT), full/empty per W stage (SPLIT), acc_full[2], acc_empty[2], drain
+    static constexpr int n_bars = (2 + kMaxParts) * kAStages + (SPLIT ? 2 * kBStages : 0) + 5;
     static constexpr int off_tmem = off_bar + n_bars * 8;
     static constexpr int bytes = off_tmem + 16;
     static constexpr int alloc = bytes + 1024;
+    static_assert(!SPLIT || kAStages > kBStages, "the x ring is the deeper one");
+    static_assert(alloc <= kSmemLimit, "shared memory");
 };
+
+// Whether a variant runs separate x and W rings.
+template <int NORM, int NSUB, bool GATED>
+constexpr bool split_rings()
+{
+    return (NORM == kNormLayer || NORM == kNormRms) && NSUB == 2 &&
+           (NGR_SPLIT_RINGS == 2 || (NGR_SPLIT_RINGS == 1 && GATED));
+}
 
 
 template <int NORM, bool BF16, int BN, int STAGES, int NSUB, bool GATED>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm2_kernel(const __grid_constant__ GemmArgs args)
 {
-    using L = Gemm2Smem<BN, STAGES, NSUB>;
+    constexpr bool kSplit = split_rings<NORM, NSUB, GATED>();
+    using L = Gemm2Smem<BN, STAGES, NSUB, kSplit>;
+    constexpr int SA = L::kAStages;    // x ring (the unified ring without kSplit)
+    constexpr int SB = L::kBStages;    // W ring
     constexpr bool kNorm = NORM == kNormLayer || NORM == kNormRms;  // transform stage
     constexpr int kTW = NSUB * BN;                 // accumulator columns of a tile
     constexpr int kOutW = GATED ? BN : kTW;        // output columns of a tile
@@ -121,12 +163,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint8_t *sB = smem + L::off_b;
     float *sG = reinterpret_cast<float *>(smem + L::off_g);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::off_bar);
-    uint64_t *full = bars;
-    uint64_t *empty = bars + STAGES;
-    uint64_t *ready = bars + 2 * STAGES;        // [STAGES * kParts] part of both stages normalized
-    uint64_t *acc_full = bars + (2 + kMaxParts) * STAGES;
+    uint64_t *full = bars;                      // [SA] (x) stage landed
+    uint64_t *empty = bars + SA;                // [SA] (x) stage released by the MMAs
+    uint64_t *ready = bars + 2 * SA;            // [SA * kParts] part of both stages normalized
+    uint64_t *acc_full = bars + (2 + kMaxParts) * SA;
     uint64_t *acc_empty = acc_full + 2;
     uint64_t *drain = acc_full + 4;
+    // kSplit: the W ring's barriers, the leader's full on which both CTAs'
+    // W copies complete, and empty (the MMAs' commit, multicast).
+    uint64_t *wfull = kSplit ? drain + 1 : full;
+    uint64_t *wempty = kSplit ? drain + 1 + SB : empty;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::off_tmem);
 
     const int warp = threadIdx.x >> 5;
@@ -143,10 +189,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         prefetch_tmap(&args.map_b);
         if constexpr (GATED) prefetch_tmap(&args.map_b2);
         if constexpr (kNorm) prefetch_tmap(&args.map_gb);
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < SA; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
             for (int p = 0; p < kParts; ++p) mbar_init(&ready[s * kParts + p], kReadyCount);
+        }
+        if constexpr (kSplit) {
+            for (int s = 0; s < SB; ++s) {
+                mbar_init(&wfull[s], 1);
+                mbar_init(&wempty[s], 1);
+            }
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&acc_full[a], 1);
@@ -181,11 +233,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // Leader-side addresses of ready[] and acc_empty[] (shared::cluster).
     const uint32_t ready_leader = mapa_shared(smem_u32(ready), 0);
     const uint32_t full_leader = mapa_shared(smem_u32(full), 0);
+    const uint32_t wfull_leader = mapa_shared(smem_u32(wfull), 0);
     const uint32_t acc_empty_leader = mapa_shared(smem_u32(acc_empty), 0);
 
-    if (warp == 0) {
+    if (warp == 0 || (kSplit && warp == 3)) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
+            // One ring: warp 0 loads each stage's x and W boxes (and the
+            // FP32 gamma/beta box with a norm).  Split rings: warp 0 loads
+            // the x ring (x and gamma/beta boxes, on this CTA's barriers),
+            // warp 3 the W ring (both CTAs' copies complete on the leader's
+            // barrier, which expects the bytes of both).
+            const bool x_side = warp == 0;
+            const int depth = x_side ? SA : SB;
+            uint64_t *rempty = x_side ? empty : wempty;
             pdl_wait();
             const uint64_t pol_x = policy_evict_last();
             const uint64_t pol_w = policy_evict_first();
@@ -206,11 +267,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 auto wrow = [&](int j) { return GATED ? n0 : n0 + j * BN; };
                 const uint32_t tx = stage_tx(n_sub);
                 for (int kb = unit_kb0(u), kb_end = unit_kb1(u); kb < kb_end; ++kb) {
-                    if (!mbar_wait_spin(&empty[stage], phase ^ 1u, wc)) { ok = false; break; }
+                    if (!mbar_wait_spin(&rempty[stage], phase ^ 1u, wc)) { ok = false; break; }
                     const int kc = kb * kBK;
-                    uint8_t *sb = sB + stage * L::kB;
-                    if constexpr (kNorm) {
+                    if constexpr (kSplit) {
+                        if (x_side) {
+                            mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(L::kA + L::kGB));
+                            tma_load_2d(sA + stage * L::kA, &args.map_a, &full[stage], kc, m0, pol_x);
+                            tma_load_2d(sG + stage * 2 * kBK, &args.map_gb, &full[stage], kc, 0, pol_x);
+                        } else {
+                            uint8_t *sb = sB + stage * L::kB;
+                            const uint32_t fb = wfull_leader + 8u * static_cast<uint32_t>(stage);
+                            if (leader)
+                                mbar_arrive_expect_tx(&wfull[stage], static_cast<uint32_t>(2 * n_sub * L::kBSub));
+                            for (int j = 0; j < n_sub; ++j)
+                                tma_load_2d_pair(sb + j * L::kBSub, wmap(j), fb, kc, wrow(j), pol_w);
+                        }
+                    } else if constexpr (kNorm) {
                         // Each CTA normalizes its own stage: local barrier.
+                        uint8_t *sb = sB + stage * L::kB;
                         mbar_arrive_expect_tx(&full[stage], tx);
                         tma_load_2d(sA + stage * L::kA, &args.map_a, &full[stage], kc, m0, pol_x);
                         for (int j = 0; j < n_sub; ++j)
@@ -219,6 +293,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     } else {
                         // Both CTAs' copies complete on the leader's barrier,
                         // which expects the bytes of both.
+                        uint8_t *sb = sB + stage * L::kB;
                         const uint32_t fb = full_leader + 8u * static_cast<uint32_t>(stage);
                         if (leader) mbar_arrive_expect_tx(&full[stage], 2 * tx);
                         tma_load_2d_pair(sA + stage * L::kA, &args.map_a, fb, kc, m0, pol_x);
@@ -226,28 +301,33 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             tma_load_2d_pair(sb + j * L::kBSub, wmap(j), fb, kc, wrow(j), pol_w);
                     }
                     ++fills;
-                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                    if (++stage == depth) { stage = 0; phase ^= 1u; }
                 }
             }
             // Copies signalled on this CTA's own barriers: wait for the last
-            // fills.  (Without a norm the peer's copies complete on the
-            // leader's barriers; the leader's MMAs, and so the final cluster
-            // barrier, come after them.)
-            if (kNorm || leader) {
-                const int outstanding = fills < STAGES ? static_cast<int>(fills) : STAGES;
+            // fills.  (Copies that complete on the leader's barriers -- all
+            // of them without a norm, the W ring's with split rings -- are
+            // waited for by the leader alone; the leader's MMAs, and so the
+            // final cluster barrier, come after them.)
+            const bool own = kSplit ? x_side : kNorm;
+            if (own || leader) {
+                uint64_t *rfull = (kSplit && !x_side) ? wfull : full;
+                const int outstanding = fills < depth ? static_cast<int>(fills) : depth;
                 for (int j = 1; j <= outstanding; ++j) {
                     int s = stage - j;
                     uint32_t p = phase;
-                    if (s < 0) { s += STAGES; p ^= 1u; }
-                    mbar_wait(&full[s], p, wc);
+                    if (s < 0) { s += depth; p ^= 1u; }
+                    mbar_wait(&rfull[s], p, wc);
                 }
             }
         }
     } else if (warp == 1) {
         if (leader && lane == 0) {
             // ------------------------------------- MMA issuer (even CTA)
-            int stage = 0;
+            int stage = 0;          // x stage (the unified stage without split rings)
             uint32_t phase = 0;
+            int wstage = 0;         // W stage (split rings)
+            uint32_t wphase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
@@ -259,9 +339,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kTW);
                 const int n_sub = GATED ? 2 : min(NSUB, (args.N - (tile / m_tiles) * kTW + BN - 1) / BN);
                 for (int kb = kb0, kb_end = unit_kb1(u); kb < kb_end; ++kb) {
+                    if (kSplit && !mbar_wait_spin(&wfull[wstage], wphase, wc)) { ok = false; break; }
                     if (!mbar_wait_spin(kNorm ? &ready[stage * kParts] : &full[stage], phase, wc)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t b_addr = smem_u32(sB + stage * L::kB);
+                    const uint32_t b_addr = smem_u32(sB + (kSplit ? wstage : stage) * L::kB);
                     const uint32_t a_addr = smem_u32(sA + stage * L::kA);
                     constexpr int kStepsPerPart = (kBK / kUmmaK) / kParts;
 #pragma unroll
@@ -285,7 +366,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                     if (!ok) break;
                     umma_commit_pair(&empty[stage], 0x3);
-                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                    if (++stage == SA) { stage = 0; phase ^= 1u; }
+                    if constexpr (kSplit) {
+                        umma_commit_pair(&wempty[wstage], 0x3);
+                        if (++wstage == SB) { wstage = 0; wphase ^= 1u; }
+                    }
                 }
                 if (!ok) break;
                 umma_commit_pair(&acc_full[acc], 0x3);
@@ -300,7 +385,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int t = threadIdx.x - kTransformWarp0 * 32;
             if constexpr (kNorm) {
                 // ----------------------------------------- transform (A in place)
-                transform_role<NORM, BF16, STAGES, L::kA, kParts, !kRstdOut>(
+                transform_role<NORM, BF16, SA, L::kA, kParts, !kRstdOut>(
                     t, cluster, n_clusters, num_units, [&](int u) { return unit_kb1(u) - unit_kb0(u); },
                     args.M, args.stats, sA, sG, full, wc,
                     [&](int u) { return (unit_tile(u) % m_tiles) * 2 * kBM + static_cast<int>(rank) * kBM; },
@@ -464,7 +549,7 @@ template <int NORM, bool BF16, int BN, int STAGES, int NSUB, bool GATED>
 int launch_gemm2_variant(const GemmArgs &args, int grid, bool pdl, cudaStream_t stream)
 {
     auto kern = gemm2_kernel<NORM, BF16, BN, STAGES, NSUB, GATED>;
-    constexpr int smem = Gemm2Smem<BN, STAGES, NSUB>::alloc;
+    constexpr int smem = Gemm2Smem<BN, STAGES, NSUB, split_rings<NORM, NSUB, GATED>()>::alloc;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess)
         return record_cuda_error("cudaFuncSetAttribute(max dynamic smem)", e, cudaGetErrorString(e));
