@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 auto wrow = [&](int j) { return GATED ? n0 : n0 + j * BN; };
                 const uint32_t tx = stage_tx(n_sub);
                 for (int kb = unit_kb0(u), kb_end = unit_kb1(u); kb < kb_end; ++kb) {
-                    if (!mbar_wait_spin(&rempty[stage], phase ^ 1u, wc)) { ok = false; break; }
+                    if (!mbar_wait_ahead(&rempty[stage], phase ^ 1u, wc)) { ok = false; break; }
                     const int kc = kb * kBK;
                     if constexpr (kSplit) {
                         if (x_side) {

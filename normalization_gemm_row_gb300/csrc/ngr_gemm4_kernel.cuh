@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const int w1 = nt0 + kMcBN0 + r * (kMcBN1 / 2) + mc_part_row(1, p);
                 const CUtensorMap *map1 = p == 0 ? &args.map_b2 : &args.map_b;   // 64 or 56 rows
                 for (int kb = 0; kb < k_blocks; ++kb) {
-                    if (!mbar_wait_spin(&empty[stage], phase ^ 1u, wc)) { ok = false; break; }
+                    if (!mbar_wait_ahead(&empty[stage], phase ^ 1u, wc)) { ok = false; break; }
                     const int kc = kb * kBK;
                     uint8_t *sb = sB + stage * L::kB;
                     mbar_arrive_expect_tx(&full[stage], tx);

@@ -426,7 +426,7 @@ __device__ __forceinline__ void transform_role(int t, int tile0, int tile_step, 
                         }
                     }
                 }
-                if (!mbar_wait_warp_spin(&full[stage], phase, wc)) return;
+                if (!mbar_wait_warp_ahead(&full[stage], phase, wc)) return;
 #pragma unroll
                 for (int part = 0; part < PARTS; ++part) {
                     const int c = cl + kCP * part;    // logical chunk: columns 8c .. 8c+7
@@ -598,7 +598,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const int m0 = (tile % m_tiles) * kBM;
                 const int n0 = (tile / m_tiles) * BN;
                 for (int kb = 0; kb < k_blocks; ++kb) {
-                    if (!mbar_wait_spin(&empty[stage], phase ^ 1u, wc)) { ok = false; break; }
+                    if (!mbar_wait_ahead(&empty[stage], phase ^ 1u, wc)) { ok = false; break; }
                     mbar_arrive_expect_tx(&full[stage], kTx);
                     const int kc = kb * kBK;
                     tma_load_2d(sA + stage * L::kA, &args.map_a, &full[stage], kc, m0, pol_x);
