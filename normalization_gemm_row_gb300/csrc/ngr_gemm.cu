@@ -233,21 +233,25 @@ static int max_clusters4()
 
 // The multicast cluster kernel (a norm only, M > 256): clusters of two CTA
 // pairs sharing each weight box, 512 x 464 super-tiles.  Measured on GB300
-// against the CTA-pair kernel on the same shapes, it is faster only where
-// every cluster runs at least three super-tiles over a long K (the
-// 512 x 14336 -> 49152 RMSNorm and LayerNorm workloads: 0.966x and 0.976x),
-// and 0.5-2.4 % slower with one or two super-tiles per cluster (1024 and
-// 2048 x 8192 -> 8192, 512 x 8192 -> 28672), where its fill and drain and
-// its 3.6 % wider tiles on 144 of 152 SMs are not repaid.  So the planner
-// takes it when each cluster gets at least three super-tiles and its
-// columns per SM stay within 4 % of the pair plan's.
+// against the CTA-pair kernel on the same shapes (with the transform in two
+// alternating groups and its waits sleeping with a time hint): 0.960 /
+// 0.967 / 0.996 at LayerNorm / RMSNorm fp16 / LayerNorm bf16
+// 1024 x 8192 -> 8192 (one super-tile per cluster), 0.964 / 0.970 at
+// 2048 x 8192 -> 8192 (two), 1.009 at RMSNorm bf16 512 x 8192 -> 28672,
+// where it has 3.5 % more columns per SM; at 512 x 14336 -> 49152 it is
+// the faster by 4.4 %.  So the planner takes it when its columns per SM
+// stay within 4 % of the pair plan's, for any number of super-tiles per
+// cluster (NGR_MC_MIN_RUN raises that minimum).
+#ifndef NGR_MC_MIN_RUN
+#define NGR_MC_MIN_RUN 1
+#endif
 static bool prefer_multicast(int64_t M, int64_t N, const GemmPlan &pair_plan, int num_sms)
 {
     const int clusters = max_clusters4();
     if (clusters <= 0 || M <= 2 * kBM) return false;
     const int64_t super = ((M + kMcRows - 1) / kMcRows) * ((N + kMcCols - 1) / kMcCols);
     const int64_t per_cluster = (super + clusters - 1) / clusters;
-    if (per_cluster < 3) return false;
+    if (per_cluster < NGR_MC_MIN_RUN) return false;
     if (!pair_plan.pair) return false;
     const int64_t tiles = ((M + pair_plan.bm - 1) / pair_plan.bm) * ((N + pair_plan.tw - 1) / pair_plan.tw) *
                           pair_plan.splits;

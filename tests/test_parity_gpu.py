@@ -125,15 +125,21 @@ def test_path_boundaries(M):
         assert_parity(y.double().cpu().numpy(), ref_op(op, d, 1e-5), f"{op} M={M}")
 
 
-def test_many_tiles_per_pair():
-    """4096 x 256 -> 2048: more output tiles than resident CTA pairs, so
-    each pair runs several tiles through its accumulators; every element."""
+@pytest.mark.parametrize("pair", [1, 2], ids=["cta-pair", "multicast"])
+def test_many_tiles_per_pair(pair):
+    """4096 x 256 -> 2048: more output tiles than resident CTA pairs (or
+    clusters), so each runs several tiles through its accumulators; every
+    element, on the CTA-pair kernel and on the multicast cluster kernel."""
     M, K, N = 4096, 256, 2048
     d = inputs.case("rmsnorm_linear", M, K, N, torch.bfloat16, True, 1e-5, seed=4096)
-    y = run_op("rmsnorm_linear", to_dev(d), 1e-5)
-    torch.cuda.synchronize()
-    plan = B.tile_plan(B.OP_RMSNORM_LINEAR, M, K, N)
-    assert plan["pair"] == 1, plan
+    B.set_tile_config(pair, 0, 0)
+    try:
+        plan = B.tile_plan(B.OP_RMSNORM_LINEAR, M, K, N)
+        assert plan["pair"] == pair, plan
+        y = run_op("rmsnorm_linear", to_dev(d), 1e-5)
+        torch.cuda.synchronize()
+    finally:
+        B.set_tile_config(-1, 0, 0)
     assert_parity(y.double().cpu().numpy(), ref_op("rmsnorm_linear", d, 1e-5), "4096x256x2048")
 
 
