@@ -423,7 +423,8 @@ int launch_layer(int norm, int act, bool bf16, const void *x, const void *W,
     GemmArgs a;
     std::memset(&a, 0, sizeof(a));
     const GemmPlan plan = plan_gemm(M, N, K, di.sms, has_norm,
-                                    may_split ? L.split_cnt_bytes + L.split_part_bytes : 0);
+                                    may_split ? L.split_cnt_bytes + L.split_part_bytes : 0,
+                                    norm == kNormNone);
     if (trace_mode())
         std::fprintf(stderr, "ngr: tile kernel M=%lld N=%lld K=%lld norm=%d %s BN=%d x %d splits=%d stages=%d grid=%d smem=%zu\n",
                      static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(K), norm,
@@ -1275,7 +1276,8 @@ int ngr_tile_plan(int op, int64_t M, int64_t K, int64_t N, int *plan)
     // the post-norm op's product have none
     const bool in_norm = op == NGR_OP_LAYERNORM_LINEAR || op == NGR_OP_RMSNORM_LINEAR ||
                          op == NGR_OP_NORM_LINEAR;
-    const GemmPlan p = plan_gemm(M, n_out, k_in, di.sms, in_norm, L.split_cnt_bytes + L.split_part_bytes);
+    const GemmPlan p = plan_gemm(M, n_out, k_in, di.sms, in_norm, L.split_cnt_bytes + L.split_part_bytes,
+                                 !in_norm);
     plan[0] = p.mc ? 2 : (p.pair ? 1 : 0);
     plan[1] = p.bn;
     plan[2] = p.nsub;

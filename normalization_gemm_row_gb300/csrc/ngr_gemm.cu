@@ -274,17 +274,18 @@ static GemmPlan multicast_plan(int64_t M, int64_t N)
 }
 
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, bool norm,
-                   size_t max_split_bytes)
+                   size_t max_split_bytes, bool plain)
 {
     const int want = g_pair.load();
-    if (want == 2 && norm && M > 2 * kBM && max_clusters4() > 0) return multicast_plan(M, N);
+    const bool mc_ok = norm || plain;
+    if (want == 2 && mc_ok && M > 2 * kBM && max_clusters4() > 0) return multicast_plan(M, N);
     double cost = -1.0;
     GemmPlan best = plan_with(M, N, K, num_sms, want == 2 ? -1 : want, g_bn.load(), g_nsub.load(),
                               max_split_bytes, &cost);
     if (cost < 0) best = plan_with(M, N, K, num_sms, -1, 0, 0, max_split_bytes, &cost);
     best.smem = best.pair ? gemm2_smem_bytes(best.bn, best.nsub)
                           : gemm_smem_bytes(best.bn, best.stages, true);
-    if (want == -1 && norm && g_bn.load() == 0 && g_nsub.load() == 0 &&
+    if (want == -1 && mc_ok && g_bn.load() == 0 && g_nsub.load() == 0 &&
         prefer_multicast(M, N, best, num_sms))
         return multicast_plan(M, N);
     return best;

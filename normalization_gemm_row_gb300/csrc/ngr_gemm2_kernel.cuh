@@ -181,6 +181,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const bool leader = rank == 0;
     __shared__ int abort_flag;
     const WaitCtx wc{&abort_flag, args.err, args.timeout_ns};
+    // The last unit's accumulator, once (the transform warps that help to
+    // drain it wait here: a one-shot barrier cannot be confused with an
+    // earlier unit's phase, however early or late the helpers arrive).
+    __shared__ uint64_t acc_last;
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
@@ -205,6 +209,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(&acc_empty[a], 2 * kDrainWarps);
         }
         mbar_init(drain, 1);
+        mbar_init(&acc_last, 1);
         fence_mbarrier_init();
     }
     if (warp == 2) {
@@ -374,6 +379,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
                 if (!ok) break;
                 umma_commit_pair(&acc_full[acc], 0x3);
+                if (kHelpLast && u + n_clusters >= num_units) umma_commit_pair(&acc_last, 0x3);
                 if (++acc == kAccBufs) { acc = 0; acc_phase ^= 1u; }
             }
             umma_commit_pair(drain, 0x1);
@@ -421,7 +427,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             prefetch_l1(static_cast<const uint16_t *>(args.bias) + nt0 + c);
                     }
                 }
-                if (!mbar_wait_warp_long(&acc_full[cur], cur_phase, wc)) break;
+                // (helpers: the last unit's one-shot barrier)
+                if (!(epi_warp || kHelpAlways ? mbar_wait_warp_long(&acc_full[cur], cur_phase, wc)
+                                              : mbar_wait_warp_long(&acc_last, 0, wc)))
+                    break;
                 tc_fence_after();
                 const int row = (tile % m_tiles) * 2 * kBM + static_cast<int>(rank) * kBM + q * 32 + lane;
                 float2 so = fold_row_scale<NORM>(args, row);

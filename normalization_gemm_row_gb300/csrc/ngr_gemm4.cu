@@ -1,5 +1,5 @@
 // ngr_gemm4.cu -- instantiations and launch of the multicast cluster
-// kernel (ngr_gemm4_kernel.cuh): LayerNorm or RMSNorm, fp16 or bf16.
+// kernel (ngr_gemm4_kernel.cuh): LayerNorm, RMSNorm or no norm, fp16 or bf16.
 #include "ngr_gemm4_kernel.cuh"
 
 namespace ngr {
@@ -12,6 +12,9 @@ int launch_gemm4(int norm, bool bf16, const GemmArgs &args, int grid, bool pdl, 
     if (norm == kNormRms)
         return bf16 ? launch_gemm4_variant<kNormRms, true>(args, grid, pdl, stream)
                     : launch_gemm4_variant<kNormRms, false>(args, grid, pdl, stream);
+    if (norm == kNormNone)
+        return bf16 ? launch_gemm4_variant<kNormNone, true>(args, grid, pdl, stream)
+                    : launch_gemm4_variant<kNormNone, false>(args, grid, pdl, stream);
     return -9;
 }
 

@@ -65,7 +65,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 {
     using L = Gemm4Smem;
     constexpr int STAGES = kMcStages;
-    static_assert(NORM == kNormLayer || NORM == kNormRms, "the multicast kernel normalizes x");
+    static_assert(NORM == kNormLayer || NORM == kNormRms || NORM == kNormNone,
+                  "the multicast kernel normalizes x or takes it as it is");
     constexpr int kParts = NGR_TRANSFORM_PARTS;
     constexpr uint32_t kReadyCount = 2 * kGroupWarps;
     constexpr bool kRstdOut = NORM == kNormRms && NGR_RMS_RSTD_OUT;
@@ -98,6 +99,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t pair_leader = crank & ~1u;
     __shared__ int abort_flag;
     const WaitCtx wc{&abort_flag, args.err, args.timeout_ns};
+    // The cluster's last super-tile accumulator, once (the transform warps
+    // that help to drain it wait here: a one-shot barrier cannot be confused
+    // with an earlier super-tile's phase, however early or late they come).
+    __shared__ uint64_t acc_last;
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
@@ -113,6 +118,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         mbar_init(&acc_full[0], 1);
         mbar_init(&acc_empty[0], 2 * 4);
         mbar_init(drain, 1);
+        mbar_init(&acc_last, 1);
         fence_mbarrier_init();
     }
     if (warp == 2) {
@@ -227,6 +233,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
                 if (!ok) break;
                 umma_commit_pair(&acc_full[0], own);
+                if (su + n_clusters >= num_tiles) umma_commit_pair(&acc_last, own);
                 acc_phase ^= 1u;
             }
             umma_commit_pair(drain, static_cast<uint16_t>(1u << crank));
@@ -260,7 +267,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const int step = (helped ? 3 : 1);
                 const int nt0 = (su / m_tiles) * kMcTW;
                 const int ncols = min(kMcTW, N - nt0);
-                if (!mbar_wait_warp_long(&acc_full[0], cur_phase, wc)) break;
+                // (helpers: the last super-tile's one-shot barrier)
+                if (!(epi_warp ? mbar_wait_warp_long(&acc_full[0], cur_phase, wc)
+                               : mbar_wait_warp_long(&acc_last, 0, wc)))
+                    break;
                 tc_fence_after();
                 const int row = m0_of(su) + q * 32 + lane;
                 float2 so = make_float2(1.f, 0.f);

@@ -392,6 +392,9 @@ __device__ __forceinline__ void transform_role(int t, int tile0, int tile_step, 
     const int qw = u >> 3;                            // quarter-warp of the group
     const int r0 = (qw % kS) + 8 * (qw / kS) + kS * j;
     const int lane = threadIdx.x & 31;
+    // Without a norm (the multicast kernel's plain product) the role only
+    // relays each landed stage to the MMA issuer.
+    constexpr bool kMath = NORM == kNormLayer || NORM == kNormRms;
     pdl_wait();                          // statistics come from the previous grid
     int stage = 0;
     uint32_t phase = 0;
@@ -404,13 +407,23 @@ __device__ __forceinline__ void transform_role(int t, int tile0, int tile_step, 
         for (int i = 0; i < kRows; ++i) {
             const int row = m0 + r0 + kRowStride * i;
             float2 st = make_float2(0.f, 0.f);
-            if (row < M) st = stats[row];
+            if (kMath && row < M) st = stats[row];
             so[i] = make_float2(st.y, -st.x * st.y);
             s2[i] = rms_in_scale2<BF16>(st.y);
         }
         const int k_blocks = kb_count(tile);
         for (int kb = 0; kb < k_blocks; ++kb, ++it) {
             if (it % kTransformGroups == g) {
+                if constexpr (!kMath) {
+                    // No norm: only relay each landed stage to the MMA issuer.
+                    if (!mbar_wait_warp_ahead(&full[stage], phase, wc)) return;
+                    __syncwarp();
+#pragma unroll
+                    for (int part = 0; part < PARTS; ++part)
+                        if (lane == 0) arrive(stage * PARTS + part);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                    continue;
+                }
                 float4 qg[GB_GLOBAL ? PARTS : 1][4];
                 if constexpr (GB_GLOBAL) {
 #pragma unroll

@@ -177,8 +177,10 @@ int launch_gemm4(int norm, bool bf16, const GemmArgs &args, int grid, bool pdl, 
 int gemm4_clusters();           // resident clusters of four of the multicast kernel
 size_t gemm4_smem_bytes();
 // max_split_bytes: room for split-K partials and counters (0 = never split).
+// norm: a LayerNorm or RMSNorm on x; plain: no norm and no folded weight
+// (the multicast kernel takes either, not a folded product).
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, bool norm,
-                   size_t max_split_bytes = 0);
+                   size_t max_split_bytes = 0, bool plain = false);
 // The SwiGLU variant: CTA-pair tiles of 256 x BN outputs, two BN-column
 // accumulators (gate, up) per tile.
 GemmPlan plan_gemm_gated(int64_t M, int64_t N, int num_sms);

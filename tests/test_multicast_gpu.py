@@ -83,3 +83,77 @@ def test_multicast_repeat_is_deterministic(multicast):
     y2 = ngr.fused_layernorm_linear(g["x"], g["gamma"], g["beta"], g["W"], g["bias"], 1e-5)
     torch.cuda.synchronize()
     assert torch.equal(y1, y2)
+
+
+# ------------------------------------------------------ products with no norm
+# The multicast kernel without a norm: the transform warps only relay each
+# landed stage to the MMA issuer; epilogues with bias, activations and a
+# residual, and a chain whose second product takes the first one's output.
+PLAIN_SHAPES = [(600, 1000, 1000), (300, 512, 928), (1112, 4096, 700)]
+
+
+@pytest.mark.parametrize("M,K,N", PLAIN_SHAPES)
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
+def test_multicast_plain_products(multicast, dtype, M, K, N):
+    assert B.tile_plan(B.OP_LINEAR_SILU, M, K, N)["pair"] == 2
+    d = inputs.case("linear_silu", M, K, N, dtype, True, 0.0, seed=M + K + N + 3)
+    g = {k: (v.cuda() if isinstance(v, torch.Tensor) and k != "outlier_rows" else v)
+         for k, v in d.items()}
+    y = ngr.fused_linear_silu(g["x"], g["W"], g["bias"])
+    check(y, oracle.linear_silu(d["x"], d["W"], d["bias"]), f"multicast linear+SiLU {dtype} {M}x{K}x{N}")
+    for act, bact in ((oracle.ACT_GELU, B.ACT_GELU), (oracle.ACT_NONE, B.ACT_NONE)):
+        y = ngr.fused_norm_linear_act(g["x"], g["W"], norm=B.NORM_NONE, act=bact, bias=g["bias"])
+        ref = oracle.norm_linear(oracle.NORM_NONE, act, d["x"], None, None, d["W"], d["bias"], 0.0)
+        check(y, ref, f"multicast plain act={act} {dtype} {M}x{K}x{N}")
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
+def test_multicast_plain_residual_and_chain(multicast, dtype):
+    M, K, N = 600, 1000, 1000
+    d = inputs.case("norm_linear", M, K, N, dtype, True, 1e-5, seed=77, norm="none")
+    gen = torch.Generator().manual_seed(78)
+    res = (torch.randn((M, N), generator=gen) + 1.0).to(dtype)
+    gamma = (1.0 + 0.1 * torch.randn((N,), generator=gen)).to(dtype)
+    g = {k: (v.cuda() if isinstance(v, torch.Tensor) and k != "outlier_rows" else v)
+         for k, v in d.items()}
+    h, y = ngr.fused_linear_residual_norm(g["x"], g["W"], gamma.cuda(), norm=B.NORM_RMS,
+                                          bias=g["bias"], residual=res.cuda(), eps=1e-5)
+    href, yref = oracle.linear_residual_norm(oracle.NORM_RMS, d["x"], d["W"], d["bias"], res,
+                                             gamma, None, 1e-5)
+    check(h, href, f"multicast post-norm h {dtype}")
+    check(y, yref, f"multicast post-norm y {dtype}")
+    f = inputs.case("ffn", M, K, N, dtype, False, 0.0, seed=79)
+    gf = {k: (v.cuda() if isinstance(v, torch.Tensor) and k != "outlier_rows" else v)
+          for k, v in f.items()}
+    yf = ngr.ffn_linear_silu_linear(gf["x"], gf["W1"], gf["W2"])
+    check(yf, oracle.ffn(f["x"], f["W1"], f["W2"]), f"multicast FFN {dtype}")
+
+
+# Several tiles per cluster (or pair) over a short K: the transform warps
+# finish their stages long before the first tile's products, then help drain
+# the last tile; they must wait for each tile's accumulator in turn.  Every
+# element against the oracle, and two calls agree bit for bit.
+@pytest.mark.parametrize("config", [(2, 0, 0), (1, 224, 2), (1, 224, 1)],
+                         ids=["multicast", "pair-2sub", "pair-1sub"])
+@pytest.mark.parametrize("norm", ["layer", "none"])
+def test_helpers_wait_every_tile(config, norm):
+    M, K, N = 2048, 128, 8192
+    B.set_tile_config(*config)
+    try:
+        if norm == "layer":
+            d = inputs.case("layernorm_linear", M, K, N, torch.float16, True, 1e-5, seed=11)
+        else:
+            d = inputs.case("linear_silu", M, K, N, torch.float16, True, 0.0, seed=12)
+        g = {k: (v.cuda() if isinstance(v, torch.Tensor) and k != "outlier_rows" else v)
+             for k, v in d.items()}
+        run = (lambda: ngr.fused_layernorm_linear(g["x"], g["gamma"], g["beta"], g["W"], g["bias"], 1e-5)) \
+            if norm == "layer" else (lambda: ngr.fused_linear_silu(g["x"], g["W"], g["bias"]))
+        y1 = run()
+        y2 = run()
+        torch.cuda.synchronize()
+    finally:
+        B.set_tile_config(-1, 0, 0)
+    assert torch.equal(y1, y2)
+    ref = oracle.layernorm_linear(d["x"], d["gamma"], d["beta"], d["W"], d["bias"], 1e-5) \
+        if norm == "layer" else oracle.linear_silu(d["x"], d["W"], d["bias"])
+    check(y1, ref, f"helpers {config} {norm}")
