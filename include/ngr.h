@@ -330,7 +330,7 @@ int ngr_debug_bounded_wait(void *workspace, uint32_t timeout_us,
  * decide, 0 the single-CTA kernel (128-row tiles), 1 the CTA-pair kernel
  * (256-row tiles; only taken when M > 128), 2 the multicast cluster kernel
  * (clusters of two CTA pairs sharing each weight box, 512 x 464 tiles; only
- * taken with a LayerNorm or RMSNorm and M > 256; bn and nsub are ignored).  `bn`: 0 any, else the N tile
+ * taken when M > 256; bn and nsub are ignored).  `bn`: 0 any, else the N tile
  * (or sub-tile) width, one of 128, 192, 224, 256.  `nsub`: 0 any, else the
  * N sub-tiles per CTA-pair tile, 1 or 2 (2 only with bn 192, 224 or 256).  The
  * planner picks the cheapest variant that satisfies all three; if none does

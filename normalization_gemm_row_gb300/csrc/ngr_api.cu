@@ -424,7 +424,7 @@ int launch_layer(int norm, int act, bool bf16, const void *x, const void *W,
     std::memset(&a, 0, sizeof(a));
     const GemmPlan plan = plan_gemm(M, N, K, di.sms, has_norm,
                                     may_split ? L.split_cnt_bytes + L.split_part_bytes : 0,
-                                    norm == kNormNone);
+                                    norm == kNormNone || is_fold(norm));
     if (trace_mode())
         std::fprintf(stderr, "ngr: tile kernel M=%lld N=%lld K=%lld norm=%d %s BN=%d x %d splits=%d stages=%d grid=%d smem=%zu\n",
                      static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(K), norm,

@@ -231,8 +231,9 @@ static int max_clusters4()
     return cache[dev] > 0 ? cache[dev] : 0;
 }
 
-// The multicast cluster kernel (a norm only, M > 256): clusters of two CTA
-// pairs sharing each weight box, 512 x 464 super-tiles.  Measured on GB300
+// The multicast cluster kernel (M > 256; a norm, a folded weight or a plain
+// product): clusters of two CTA pairs sharing each weight box, 512 x 464
+// super-tiles.  Measured on GB300
 // against the CTA-pair kernel on the same shapes (with the transform in two
 // alternating groups and its waits sleeping with a time hint): 0.960 /
 // 0.967 / 0.996 at LayerNorm / RMSNorm fp16 / LayerNorm bf16

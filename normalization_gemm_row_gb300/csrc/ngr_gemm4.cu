@@ -1,5 +1,6 @@
 // ngr_gemm4.cu -- instantiations and launch of the multicast cluster
-// kernel (ngr_gemm4_kernel.cuh): LayerNorm, RMSNorm or no norm, fp16 or bf16.
+// kernel (ngr_gemm4_kernel.cuh): LayerNorm, RMSNorm, no norm or a folded
+// weight (LayerNorm or RMSNorm), fp16 or bf16.
 #include "ngr_gemm4_kernel.cuh"
 
 namespace ngr {
@@ -15,6 +16,12 @@ int launch_gemm4(int norm, bool bf16, const GemmArgs &args, int grid, bool pdl, 
     if (norm == kNormNone)
         return bf16 ? launch_gemm4_variant<kNormNone, true>(args, grid, pdl, stream)
                     : launch_gemm4_variant<kNormNone, false>(args, grid, pdl, stream);
+    if (norm == kNormFoldLayer)
+        return bf16 ? launch_gemm4_variant<kNormFoldLayer, true>(args, grid, pdl, stream)
+                    : launch_gemm4_variant<kNormFoldLayer, false>(args, grid, pdl, stream);
+    if (norm == kNormFoldRms)
+        return bf16 ? launch_gemm4_variant<kNormFoldRms, true>(args, grid, pdl, stream)
+                    : launch_gemm4_variant<kNormFoldRms, false>(args, grid, pdl, stream);
     return -9;
 }
 

@@ -65,7 +65,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 {
     using L = Gemm4Smem;
     constexpr int STAGES = kMcStages;
-    static_assert(NORM == kNormLayer || NORM == kNormRms || NORM == kNormNone,
+    static_assert(NORM == kNormLayer || NORM == kNormRms || NORM == kNormNone || is_fold(NORM),
                   "the multicast kernel normalizes x or takes it as it is");
     constexpr int kParts = NGR_TRANSFORM_PARTS;
     constexpr uint32_t kReadyCount = 2 * kGroupWarps;
@@ -258,7 +258,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int e = epi_warp ? 0 : 1 + (warp - kTransformWarp0) / 4;
             uint32_t acc_phase = 0;
             const int N = args.N;
-            if constexpr (kRstdOut) pdl_wait();
+            if constexpr (kRstdOut || is_fold(NORM)) pdl_wait();   // row statistics from the previous grid
             for (int su = cluster; su < num_tiles; su += n_clusters) {
                 const uint32_t cur_phase = acc_phase;
                 acc_phase ^= 1u;
@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     break;
                 tc_fence_after();
                 const int row = m0_of(su) + q * 32 + lane;
-                float2 so = make_float2(1.f, 0.f);
+                float2 so = fold_row_scale<NORM>(args, row);
                 if constexpr (kRstdOut)
                     so = make_float2(row < args.M ? rms_out_scale<BF16>(args.stats[row].y) : 0.f, 0.f);
                 const uint32_t t_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);

@@ -125,7 +125,7 @@ struct GemmPlan {
     bool gated;      // SwiGLU: sub-tile 0 multiplies the gate weight, 1 the up weight
     int splits;      // K ranges per output tile (CTA pair only; 1 = none)
     bool mc = false; // clusters of two CTA pairs sharing the weight boxes (multicast):
-                     // 512 x 464 super-tiles, sub-tiles 224 + 240, a norm only
+                     // 512 x 464 super-tiles, sub-tiles 224 + 240
 };
 
 // The multicast cluster kernel's super-tile and weight-box geometry.
@@ -177,8 +177,9 @@ int launch_gemm4(int norm, bool bf16, const GemmArgs &args, int grid, bool pdl, 
 int gemm4_clusters();           // resident clusters of four of the multicast kernel
 size_t gemm4_smem_bytes();
 // max_split_bytes: room for split-K partials and counters (0 = never split).
-// norm: a LayerNorm or RMSNorm on x; plain: no norm and no folded weight
-// (the multicast kernel takes either, not a folded product).
+// norm: a LayerNorm or RMSNorm on x; plain: no transform of x (no norm, or
+// a folded weight with the statistics applied in the epilogue).  The
+// multicast kernel takes either.
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, bool norm,
                    size_t max_split_bytes = 0, bool plain = false);
 // The SwiGLU variant: CTA-pair tiles of 256 x BN outputs, two BN-column

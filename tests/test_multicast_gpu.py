@@ -157,3 +157,32 @@ def test_helpers_wait_every_tile(config, norm):
     ref = oracle.layernorm_linear(d["x"], d["gamma"], d["beta"], d["W"], d["bias"], 1e-5) \
         if norm == "layer" else oracle.linear_silu(d["x"], d["W"], d["bias"])
     check(y1, ref, f"helpers {config} {norm}")
+
+
+# ------------------------------------------------- folded weights (inference)
+# The folded form (gamma folded into W once; statistics and the folded bias
+# in the epilogue) on the multicast kernel: its transform warps only relay
+# each landed stage, and the epilogue applies y = rstd acc - rstd mu c + b'.
+# Held to the direct layer's oracle (LayerNorm rows at mean 3, where the
+# fold's two epilogue terms cancel most).
+@pytest.mark.parametrize("M,K,N", SHAPES)
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
+@pytest.mark.parametrize("norm", [oracle.NORM_LAYER, oracle.NORM_RMS], ids=["ln", "rms"])
+def test_multicast_folded_against_oracle(multicast, norm, dtype, M, K, N):
+    op = "layernorm_linear" if norm == oracle.NORM_LAYER else "rmsnorm_linear"
+    d = inputs.case(op, M, K, N, dtype, True, 1e-5, seed=M * 3 + N,
+                    x_mean=3.0 if norm == oracle.NORM_LAYER else 0.0,
+                    outlier_frac=0.02 if norm == oracle.NORM_RMS else 0.0, outlier_scale=50.0)
+    g = {k: (v.cuda() if isinstance(v, torch.Tensor) and k != "outlier_rows" else v)
+         for k, v in d.items()}
+    Wf, cb = B.fold_prepare(norm, g["gamma"], g["beta"] if norm == oracle.NORM_LAYER else None,
+                            g["W"], g["bias"])
+    y1 = B.fused_norm_linear_folded(norm, g["x"], Wf, cb, 1e-5)
+    y2 = B.fused_norm_linear_folded(norm, g["x"], Wf, cb, 1e-5)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+    if norm == oracle.NORM_LAYER:
+        ref = oracle.layernorm_linear(d["x"], d["gamma"], d["beta"], d["W"], d["bias"], 1e-5)
+    else:
+        ref = oracle.rmsnorm_linear(d["x"], d["gamma"], d["W"], d["bias"], 1e-5)
+    check(y1, ref, f"multicast folded {op} {dtype} {M}x{K}x{N}")

@@ -340,12 +340,13 @@ def test_folded_layer_against_direct_oracle(norm, dtype, M, K, N):
     assert_parity(y.double().cpu().numpy(), ref_op(op, d, 1e-5), f"folded {op} {M}x{K}x{N}")
 
 
-@pytest.mark.parametrize("idx,M", [(1, None), (4, 16), (4, 1)])
+@pytest.mark.parametrize("idx,M", [(1, None), (2, None), (4, 16), (4, 1)])
 def test_folded_full_size(idx, M):
     w, d, rows = full_case(inputs.WORKLOADS[idx], M)
     g = to_dev(d)
-    norm = oracle.NORM_LAYER
-    Wf, cb = B.fold_prepare(norm, g["gamma"], g["beta"], g["W"], g["bias"])
+    norm = oracle.NORM_RMS if w.op == "rmsnorm_linear" else oracle.NORM_LAYER
+    Wf, cb = B.fold_prepare(norm, g["gamma"], g["beta"] if norm == oracle.NORM_LAYER else None,
+                            g["W"], g["bias"])
     y = B.fused_norm_linear_folded(norm, g["x"], Wf, cb, w.eps)
     torch.cuda.synchronize()
     got = y[torch.as_tensor(rows, device="cuda")].double().cpu().numpy()
