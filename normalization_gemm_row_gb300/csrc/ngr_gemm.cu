@@ -246,7 +246,7 @@ static int max_clusters4()
 #ifndef NGR_MC_MIN_RUN
 #define NGR_MC_MIN_RUN 1
 #endif
-static bool prefer_multicast(int64_t M, int64_t N, const GemmPlan &pair_plan, int num_sms)
+static bool prefer_multicast(int64_t M, int64_t N, int64_t K, const GemmPlan &pair_plan, int num_sms)
 {
     const int clusters = max_clusters4();
     if (clusters <= 0 || M <= 2 * kBM) return false;
@@ -254,13 +254,21 @@ static bool prefer_multicast(int64_t M, int64_t N, const GemmPlan &pair_plan, in
     const int64_t per_cluster = (super + clusters - 1) / clusters;
     if (per_cluster < NGR_MC_MIN_RUN) return false;
     if (!pair_plan.pair) return false;
-    const int64_t tiles = ((M + pair_plan.bm - 1) / pair_plan.bm) * ((N + pair_plan.tw - 1) / pair_plan.tw) *
-                          pair_plan.splits;
+    const int64_t m_tiles = (M + pair_plan.bm - 1) / pair_plan.bm;
+    const int64_t tiles = m_tiles * ((N + pair_plan.tw - 1) / pair_plan.tw) * pair_plan.splits;
     const int64_t pairs = pair_plan.grid / 2;
     const int64_t per_pair = (tiles + pairs - 1) / pairs;
     (void)num_sms;
+    // With several 256-row tiles per weight column and a long K, the pairs
+    // that share a weight column drift apart along K and read it from DRAM
+    // again: measured at 512 x 49152 -> 14336 (768 k blocks), the pair plan
+    // read 1.98-2.02 GB per launch for 1.41 GB of weights, and the multicast
+    // kernel, which reads each weight byte once per cluster, took the same
+    // time (440-445 against 443 us).  There it may cost up to 25 % more
+    // columns per SM.
+    const double margin = (m_tiles >= 2 && K >= 512 * kBK) ? 1.25 : 1.04;
     return static_cast<double>(per_cluster * kMcCols) <=
-           1.04 * static_cast<double>(per_pair * pair_plan.tw) / pair_plan.splits;
+           margin * static_cast<double>(per_pair * pair_plan.tw) / pair_plan.splits;
 }
 
 static GemmPlan multicast_plan(int64_t M, int64_t N)
@@ -287,7 +295,7 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, bool norm,
     best.smem = best.pair ? gemm2_smem_bytes(best.bn, best.nsub)
                           : gemm_smem_bytes(best.bn, best.stages, true);
     if (want == -1 && mc_ok && g_bn.load() == 0 && g_nsub.load() == 0 &&
-        prefer_multicast(M, N, best, num_sms))
+        prefer_multicast(M, N, K, best, num_sms))
         return multicast_plan(M, N);
     return best;
 }
