@@ -80,14 +80,25 @@ struct WsLayout {
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int64_t round8(int64_t v) { return (v + 7) & ~static_cast<int64_t>(7); }
 
-// Room for a two-way K split of an M x Nout product on the CTA-pair kernel,
-// reserved only when the output has few 256 x 448 tiles (a GPU's pairs
-// would otherwise idle): the largest counters and partials over the pair
-// tile widths, so any two-way plan fits.  Independent of the device.
-void split_reserve(int64_t M, int64_t Nout, size_t *cnt_bytes, size_t *part_bytes)
+// Room for a K split of an M x Nout product (K_in input columns), reserved
+// only where the tiles are few for a GPU's SMs: on the CTA-pair kernel
+// (M > 128) a two-way split when the output has few 256 x 448 tiles; on the
+// single-CTA kernel (M <= 128) up to kMaxSplitsSingle ways when the output
+// has fewer than 256 tiles of 128 columns and K_in is long enough to split.
+// The largest counters and partials over the tile widths, so that any plan
+// fits.  Independent of the device.
+void split_reserve(int64_t M, int64_t Nout, int64_t K_in, size_t *cnt_bytes, size_t *part_bytes)
 {
     *cnt_bytes = *part_bytes = 0;
-    if (M <= kBM) return;
+    if (M <= kBM) {
+        if ((Nout + 127) / 128 >= 256 || (K_in + kBK - 1) / kBK < 2 * kMinKbPerSplitSingle) return;
+        for (int tw : {128, 192, 224, 256}) {
+            const int64_t tiles = (Nout + tw - 1) / tw;
+            *cnt_bytes = std::max(*cnt_bytes, split_counter_bytes(tiles, tw, 1));
+            *part_bytes = std::max(*part_bytes, split_partial_bytes(tiles, tw, kMaxSplitsSingle, 1));
+        }
+        return;
+    }
     const int64_t mt = (M + 2 * kBM - 1) / (2 * kBM);
     if (mt * ((Nout + 447) / 448) > 48) return;
     for (int tw : {128, 192, 224, 256, 384, 448, 512}) {
@@ -168,8 +179,9 @@ WsLayout ws_layout(int op, int64_t M, int64_t K_, int64_t N_, bool h_in_ws)
         // second (K output columns)
         const bool single = single_layer_op(op) || post_norm;
         const int64_t nout = single ? N : K;
+        const int64_t kin = single ? K : N;
         if ((single || chain) && !decode) {
-            split_reserve(M, nout, &L.split_cnt_bytes, &L.split_part_bytes);
+            split_reserve(M, nout, kin, &L.split_cnt_bytes, &L.split_part_bytes);
             L.split_cnt = off;
             off += align256(L.split_cnt_bytes);
             L.split_part = off;
@@ -530,8 +542,15 @@ int norm_linear(int op, int norm, int act, const void *x, const void *gamma, con
     const bool bf16 = dtype == NGR_BF16;
     char *w = static_cast<char *>(ws);
     if (debug_mode() && cudaMemsetAsync(w, 0, 4, stream) != cudaSuccess) return NGR_ERR_CUDA;
-    rc = zero_split_counters(L, w, stream);
-    if (rc != NGR_OK) return rc;
+    const bool decode = M <= kDecodeMaxM;
+    const bool need_stats = norm != kNormNone || decode;
+    // With the statistics kernel first on the stream, it zeroes the K-split
+    // counters itself (no separate memset before it).
+    const bool stats_zero = need_stats && !decode && L.split_cnt_bytes != 0;
+    if (!stats_zero) {
+        rc = zero_split_counters(L, w, stream);
+        if (rc != NGR_OK) return rc;
+    }
     // Padded operands: rows of K8 (N8) elements with zero tails.
     const int64_t K8 = round8(K), N8 = round8(N);
     const void *xa = x, *Wa = W, *ga = gamma, *ba = beta, *biasa = bias;
@@ -557,8 +576,6 @@ int norm_linear(int op, int norm, int act, const void *x, const void *gamma, con
         }
         if (N8 != N) ya = w + L.yp;
     }
-    const bool decode = M <= kDecodeMaxM;
-    const bool need_stats = norm != kNormNone || decode;
     events_reset();
     if (need_stats) {
         event_before(stream);
@@ -568,8 +585,10 @@ int norm_linear(int op, int norm, int act, const void *x, const void *gamma, con
                              norm == kNormNone ? nullptr : reinterpret_cast<float *>(w + L.gamma_f),
                              norm == kNormLayer ? reinterpret_cast<float *>(w + L.beta_f)
                                                 : (norm == kNormRms ? reinterpret_cast<float *>(w + L.beta_f) : nullptr),
-                             decode ? reinterpret_cast<int *>(w + L.counters) : nullptr,
-                             decode ? static_cast<int>(ceil_div(N8, 128) * 4) : 0,
+                             decode ? reinterpret_cast<int *>(w + L.counters)
+                                    : (stats_zero ? reinterpret_cast<int *>(w + L.split_cnt) : nullptr),
+                             decode ? static_cast<int>(ceil_div(N8, 128) * 4)
+                                    : (stats_zero ? static_cast<int>(L.split_cnt_bytes / 4) : 0),
                              reinterpret_cast<int *>(w), di.sms, stream, nullptr, K);
         event_after(stream);
         if (rc != NGR_OK) return rc;
@@ -624,14 +643,14 @@ int folded_linear(int norm, const void *x, const void *Wf, const float *cb, floa
         if (N8 != N || !aligned16(y)) ya = w + L.yp;
     }
     const bool decode = M <= kDecodeMaxM;
-    rc = zero_split_counters(L, w, stream);
-    if (rc != NGR_OK) return rc;
+    // The statistics kernel, first on the stream, zeroes the K-split counters.
     events_reset();
     event_before(stream);
     rc = launch_rowstats(norm, bf16, xa, M, K8, eps, reinterpret_cast<float2 *>(w + L.stats), nullptr,
                          nullptr, nullptr, nullptr,
-                         decode ? reinterpret_cast<int *>(w + L.counters) : nullptr,
-                         decode ? static_cast<int>(ceil_div(N8, 128) * 4) : 0,
+                         decode ? reinterpret_cast<int *>(w + L.counters)
+                                : (L.split_cnt_bytes != 0 ? reinterpret_cast<int *>(w + L.split_cnt) : nullptr),
+                         decode ? static_cast<int>(ceil_div(N8, 128) * 4) : static_cast<int>(L.split_cnt_bytes / 4),
                          reinterpret_cast<int *>(w), di.sms, stream, nullptr, K);
     event_after(stream);
     if (rc != NGR_OK) return rc;

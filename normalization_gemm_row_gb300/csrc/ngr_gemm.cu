@@ -118,15 +118,16 @@ constexpr int kSplitOverhead = 24;
 // against 150-153).
 constexpr int kMinKbPerSplit = 128;
 
-size_t split_partial_bytes(int64_t num_tiles, int tw, int splits)
+size_t split_partial_bytes(int64_t num_tiles, int tw, int splits, int ctas)
 {
-    return static_cast<size_t>(num_tiles) * 2 * 128 * static_cast<size_t>(tw) *
+    return static_cast<size_t>(num_tiles) * static_cast<size_t>(ctas) * 128 * static_cast<size_t>(tw) *
            static_cast<size_t>(splits) * 4;
 }
 
-size_t split_counter_bytes(int64_t num_tiles, int tw)
+size_t split_counter_bytes(int64_t num_tiles, int tw, int ctas)
 {
-    return static_cast<size_t>(num_tiles) * 2 * 4 * static_cast<size_t>((tw + 31) / 32) * 4;
+    return static_cast<size_t>(num_tiles) * static_cast<size_t>(ctas) * 4 *
+           static_cast<size_t>((tw + 31) / 32) * 4;
 }
 
 // Stages of the two-sub-tile CTA-pair kernel for a sub-tile width.
@@ -174,13 +175,29 @@ static GemmPlan plan_with(int64_t M, int64_t N, int64_t K, int num_sms, int want
         }
     };
     if (want_pair != 1 && want_nsub != 2) {
+        // With fewer tiles than SMs (at most 128 rows against a narrow W,
+        // where streaming W is the work) a K split of up to
+        // kMaxSplitsSingle ranges puts more SMs on it.  Measured on GB300 at
+        // LayerNorm 128 x 8192 -> 8192: unsplit, 64 CTAs of 128 x 128 tiles
+        // ran the product in 67 us at 2.0 TB/s of W.
+        const int max_splits = g_max_splits > 1 ? kMaxSplitsSingle : 1;
         for (int bn : kTileWidths) {
             if (want_bn && bn != want_bn) continue;
             const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + bn - 1) / bn);
-            const int64_t grid = tiles < num_sms ? tiles : num_sms;
-            const int64_t per_cta = (tiles + grid - 1) / grid;
-            take(kSingleCostFactor * static_cast<double>(per_cta) * (bn + 16),
-                 GemmPlan{bn, stages_for(bn), static_cast<int>(grid), 0, false, kBM, bn, 1, bn, false, 1});
+            for (int splits = 1; splits <= max_splits; ++splits) {
+                if (splits > 1 && (tiles >= num_sms || k_blocks / splits < kMinKbPerSplitSingle ||
+                                   split_partial_bytes(tiles, bn, splits, 1) +
+                                           split_counter_bytes(tiles, bn, 1) >
+                                       max_split_bytes))
+                    continue;
+                const int64_t units = tiles * splits;
+                const int64_t grid = units < num_sms ? units : num_sms;
+                const int64_t per_cta = (units + grid - 1) / grid;
+                const double cols = static_cast<double>(bn) / splits + 16 + (splits > 1 ? kSplitOverhead : 0);
+                take(kSingleCostFactor * static_cast<double>(per_cta) * cols,
+                     GemmPlan{bn, stages_for(bn), static_cast<int>(grid), 0, false, kBM, bn, 1, bn, false,
+                              splits});
+            }
         }
     }
     if (M > kBM && want_pair != 0) {

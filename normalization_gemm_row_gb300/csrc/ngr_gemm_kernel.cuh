@@ -595,6 +595,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int m_tiles = args.m_tiles;
     const int k_blocks = args.k_blocks;
     const int num_tiles = args.num_tiles;
+    // Work units: (tile, K range) pairs; without a split a unit is a tile.
+    // (With fewer tiles than SMs -- up to 128 rows against a narrow W -- a
+    // K split streams W on more SMs.)
+    const int n_splits = max(1, args.k_splits);
+    const int num_units = num_tiles * n_splits;
+    const int kb_per_split = n_splits > 1 ? args.kb_per_split : k_blocks;
+    auto unit_tile = [&](int u) { return u / n_splits; };
+    auto unit_kb0 = [&](int u) { return (u % n_splits) * kb_per_split; };
+    auto unit_kb1 = [&](int u) { return min(k_blocks, unit_kb0(u) + kb_per_split); };
 
     if (warp == 0) {
         if (lane == 0) {
@@ -607,10 +616,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint32_t phase = 0;
             long long fills = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
+                const int tile = unit_tile(u);
                 const int m0 = (tile % m_tiles) * kBM;
                 const int n0 = (tile / m_tiles) * BN;
-                for (int kb = 0; kb < k_blocks; ++kb) {
+                for (int kb = unit_kb0(u), kb_end = unit_kb1(u); kb < kb_end; ++kb) {
                     if (!mbar_wait_ahead(&empty[stage], phase ^ 1u, wc)) { ok = false; break; }
                     mbar_arrive_expect_tx(&full[stage], kTx);
                     const int kc = kb * kBK;
@@ -640,11 +650,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
                 if (!mbar_wait_spin(&acc_empty[acc], acc_phase ^ 1u, wc)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kb = 0; kb < k_blocks; ++kb) {
+                const int kb0 = unit_kb0(u);
+                for (int kb = kb0, kb_end = unit_kb1(u); kb < kb_end; ++kb) {
                     if (!mbar_wait_spin(&full[stage], phase, wc)) { ok = false; break; }
                     if constexpr (kNorm) {
                         if (!mbar_wait_spin(&ready[stage], phase, wc)) { ok = false; break; }
@@ -656,7 +667,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     for (int k = 0; k < kBK / kUmmaK; ++k) {
                         umma_f16_ss(d_tmem, sdesc_kmajor_sw128(a_addr + k * 32),
                                     sdesc_kmajor_sw128(b_addr + k * 32), kIdesc,
-                                    (kb | k) != 0 ? 1u : 0u);
+                                    (kb != kb0 || k != 0) ? 1u : 0u);
                     }
                     umma_commit(&empty[stage]);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -673,9 +684,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if constexpr (kNorm) {
             // ---------------------------------------------------- transform
             transform_role<NORM, BF16, STAGES, L::kA>(
-                threadIdx.x - kTransformWarp0 * 32, blockIdx.x, gridDim.x, num_tiles,
-                [&](int) { return k_blocks; }, args.M, args.stats, sA, sG, full, wc,
-                [&](int tile) { return (tile % m_tiles) * kBM; },
+                threadIdx.x - kTransformWarp0 * 32, blockIdx.x, gridDim.x, num_units,
+                [&](int u) { return unit_kb1(u) - unit_kb0(u); }, args.M, args.stats, sA, sG, full, wc,
+                [&](int u) { return (unit_tile(u) % m_tiles) * kBM; },
                 [&](int st) { mbar_arrive(&ready[st]); });
         }
     } else if (warp >= kEpilogueWarp0) {
@@ -685,7 +696,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         uint32_t acc_phase = 0;
         const int N = args.N;
         if constexpr (is_fold(NORM)) pdl_wait();  // row statistics from the previous grid
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+            const int tile = unit_tile(u);
             if (!mbar_wait_warp_long(&acc_full[acc], acc_phase, wc)) break;
             tc_fence_after();
             const int row = (tile % m_tiles) * kBM + q * 32 + lane;
@@ -693,17 +705,70 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int nt0 = (tile / m_tiles) * BN;
             const uint32_t t_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                     static_cast<uint32_t>(acc * BN);
+            const int nch = (min(BN, N - nt0) + 31) / 32;   // 32-column chunks inside N
+            if (n_splits > 1) {
+                // K split: (1) this unit's FP32 partials of the warp's
+                // 32 x 32 chunks (column-major within a chunk, so that each
+                // store of the warp writes one 128-byte line); (2) one fence,
+                // then one counter per chunk (lane i takes chunk i); (3) the
+                // chunks this unit arrived last at are summed over the K
+                // ranges in range order and finished, and their counters
+                // reset for the next call.
+                const int split = u % n_splits;
+                const size_t blk0 = (static_cast<size_t>(tile) * 4 + q) * (BN / 32);
+                const size_t part_stride = static_cast<size_t>(n_splits) * 1024;
 #pragma unroll 1
-            for (int c = 0; c < BN; c += 32) {
-                const int n0 = nt0 + c;
-                if (n0 >= N) break;  // uniform across the warp
-                uint32_t r[32];
-                tmem_ld32(t_base + static_cast<uint32_t>(c), r);
-                tmem_ld_wait();
-                float v[32];
+                for (int i = 0; i < nch; ++i) {
+                    uint32_t r[32];
+                    tmem_ld32(t_base + static_cast<uint32_t>(32 * i), r);
+                    tmem_ld_wait();
+                    float *mine = args.partials + (blk0 + i) * part_stride + split * 1024 + lane;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                epilogue_store32<NORM, BF16>(v, row, n0, args, so);
+                    for (int j = 0; j < 32; ++j) __stcg(mine + j * 32, __uint_as_float(r[j]));
+                }
+                __threadfence();
+                __syncwarp();
+                int last = 0;
+                if (lane < nch) last = atomicAdd(&args.split_counters[blk0 + lane], 1) == n_splits - 1;
+                const unsigned last_mask = __ballot_sync(0xffffffffu, last);
+                if (last_mask != 0u) {
+                    __threadfence();
+#pragma unroll 1
+                    for (int i = 0; i < nch; ++i) {
+                        if (((last_mask >> i) & 1u) == 0u) continue;
+                        uint32_t r[32];
+                        tmem_ld32(t_base + static_cast<uint32_t>(32 * i), r);
+                        tmem_ld_wait();
+                        const float *part = args.partials + (blk0 + i) * part_stride + lane;
+                        float v[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+                        for (int sp = 0; sp < n_splits; ++sp) {
+                            if (sp == split) {
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) v[j] += __uint_as_float(r[j]);
+                            } else {
+                                const float *o = part + sp * 1024;
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) v[j] += __ldcg(o + j * 32);
+                            }
+                        }
+                        epilogue_store32<NORM, BF16>(v, row, nt0 + 32 * i, args, so);
+                    }
+                    __syncwarp();
+                    if (lane < nch && ((last_mask >> lane) & 1u)) args.split_counters[blk0 + lane] = 0;
+                }
+            } else {
+#pragma unroll 1
+                for (int i = 0; i < nch; ++i) {
+                    uint32_t r[32];
+                    tmem_ld32(t_base + static_cast<uint32_t>(32 * i), r);
+                    tmem_ld_wait();
+                    float v[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                    epilogue_store32<NORM, BF16>(v, row, nt0 + 32 * i, args, so);
+                }
             }
             tc_fence_before();
             mbar_arrive(&acc_empty[acc]);

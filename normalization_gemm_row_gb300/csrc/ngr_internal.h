@@ -71,13 +71,13 @@ struct alignas(128) GemmArgs {
     int act;                // kAct*: activation after the bias (not used when gated)
     int M, N, K;
     int m_tiles, n_tiles, k_blocks, num_tiles;
-    // CTA-pair kernel: K split into k_splits ranges of kb_per_split k blocks
-    // (1 = no split).  Each (tile, range) unit writes FP32 partials of its
-    // 32 x 32 accumulator chunks; the last of a chunk's units (its counter)
-    // sums them in range order and finishes the chunk.
+    // Tile kernels (single CTA or CTA pair): K split into k_splits ranges of
+    // kb_per_split k blocks (1 = no split).  Each (tile, range) unit writes
+    // FP32 partials of its 32 x 32 accumulator chunks; the last of a chunk's
+    // units (its counter) sums them in range order and finishes the chunk.
     int k_splits, kb_per_split;
-    float *partials;        // [tiles][2][4][chunks][k_splits][32 cols][32 rows]
-    int *split_counters;    // [tiles][2][4][chunks], zero at kernel start
+    float *partials;        // [tiles][CTAs per tile][4][chunks][k_splits][32 cols][32 rows]
+    int *split_counters;    // [tiles][CTAs per tile][4][chunks], zero at kernel start
     unsigned long long timeout_ns;
 };
 
@@ -123,7 +123,7 @@ struct GemmPlan {
     int nsub;        // N sub-tiles of BN columns per output tile (CTA pair: 1 or 2)
     int tw;          // output tile width in N: bn * nsub, or bn when gated
     bool gated;      // SwiGLU: sub-tile 0 multiplies the gate weight, 1 the up weight
-    int splits;      // K ranges per output tile (CTA pair only; 1 = none)
+    int splits;      // K ranges per output tile (1 = none)
     bool mc = false; // clusters of two CTA pairs sharing the weight boxes (multicast):
                      // 512 x 464 super-tiles, sub-tiles 224 + 240
 };
@@ -132,9 +132,14 @@ struct GemmPlan {
 constexpr int kMcRows = 512;
 constexpr int kMcCols = 464;
 
-// Bytes of FP32 partials and of counters a split plan needs.
-size_t split_partial_bytes(int64_t num_tiles, int tw, int splits);
-size_t split_counter_bytes(int64_t num_tiles, int tw);
+// Bytes of FP32 partials and of counters a split plan needs (ctas: CTAs
+// per output tile, 2 for the CTA pair, 1 for the single-CTA kernel).
+size_t split_partial_bytes(int64_t num_tiles, int tw, int splits, int ctas = 2);
+size_t split_counter_bytes(int64_t num_tiles, int tw, int ctas = 2);
+// The single-CTA kernel splits K at most this many ways, into ranges of at
+// least kMinKbPerSplitSingle k blocks.
+constexpr int kMaxSplitsSingle = 4;
+constexpr int kMinKbPerSplitSingle = 16;
 
 // Record why a CUDA call failed (thread-local; read back through
 // ngr_last_error).  Returns -7 (NGR_ERR_CUDA) for use in return statements.

@@ -29,9 +29,10 @@
 // sums and every mean divides by k_valid.
 //
 // The same launch converts gamma and beta to FP32 once per call (the GEMM's
-// producer streams them with the tiles) and zeroes the split-K tile counters
-// of the decode path when asked to, so that they start from zero every call;
-// as the first kernel of a call it also clears the call's error word.
+// producer streams them with the tiles) and zeroes the split-K counters of
+// the kernel that follows (the decode kernel's, or a tile kernel's when its
+// plan splits K) when asked to, so that they start from zero every call; as
+// the first kernel of a call it also clears the call's error word.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>

@@ -120,9 +120,17 @@ def test_split_k_reserve(lib):
     cnt = max(mt * -(-8192 // tw) * 2 * 4 * (tw // 32) * 4 for tw in (128, 192, 224, 256, 384, 448, 512))
     part = max(mt * -(-8192 // tw) * 2 * 128 * tw * 2 * 4 for tw in (128, 192, 224, 256, 384, 448, 512))
     assert got == 256 + a256(cnt) + a256(part)
-    # none at decode sizes or at M <= 128 (no CTA-pair kernel there)
+    # none at decode sizes
     assert wb(B.OP_LINEAR_SILU, 16, 8192, 8192) == wb(B.OP_LINEAR_SILU, 16, 8192, 8192, 0)
-    assert wb(B.OP_LINEAR_SILU, 128, 8192, 8192) == 256
+    # at M <= 128 the single-CTA kernel may split K up to 4 ways: partials of
+    # 128-row tiles over the tile widths, when the output has fewer than 256
+    # tiles of 128 columns and K has at least 32 k blocks
+    cnt1 = max(-(-8192 // tw) * 4 * (tw // 32) * 4 for tw in (128, 192, 224, 256))
+    part1 = max(-(-8192 // tw) * 128 * tw * 4 * 4 for tw in (128, 192, 224, 256))
+    assert wb(B.OP_LINEAR_SILU, 128, 8192, 8192) == 256 + a256(cnt1) + a256(part1)
+    assert wb(B.OP_LINEAR_SILU, 64, 8192, 8192) == 256 + a256(cnt1) + a256(part1)
+    assert wb(B.OP_LINEAR_SILU, 128, 1024, 8192) == 256          # K too short to split
+    assert wb(B.OP_LINEAR_SILU, 128, 8192, 32768) == 256         # enough tiles
     # the chains reserve for their second product (K output columns)
     assert wb(B.OP_FFN, 512, 4096, 11008) > 256 and wb(B.OP_FFN, 512, 14336, 11008) == 256
 

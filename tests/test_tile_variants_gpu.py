@@ -190,3 +190,73 @@ def test_split_k_default_plan_llama_down_projection():
     rows = inputs.sample_rows(512, 12, seed=3, always=(0, 255, 256, 511)).tolist()
     got = y[torch.as_tensor(rows, device="cuda")]
     check(got, oracle.linear_silu(d["x"], d["W"], d["bias"], rows), "split default 512x28672")
+
+
+# ------------------------------------------- K split on the single-CTA kernel
+# Batches of 33-128 rows against a W with few 128-row tiles: the default plan
+# splits K on the single-CTA kernel (up to 4 ranges of at least 16 k
+# blocks), each range writing FP32 partials and the last of a chunk's ranges
+# summing them in range order.  Shapes: 128 and 64 rows at 8192 -> 8192 (a
+# 4-way split of 224-column tiles), 96 rows at 4096 -> 4096, a ragged N (a
+# last tile of 104 columns) with a 2-way split, a ragged last k block, and
+# 33 rows (just above the decode kernel).  Every element against the oracle,
+# and two calls agree bit for bit.
+SPLIT1_CASES = [("layernorm_linear", 128, 8192, 8192, torch.float16),
+                ("rmsnorm_linear", 64, 8192, 8192, torch.bfloat16),
+                ("linear_silu", 96, 4096, 4096, torch.float16),
+                ("layernorm_linear", 100, 2048, 1000, torch.bfloat16),
+                ("rmsnorm_linear", 128, 4000, 520, torch.float16),
+                ("linear_silu", 33, 4096, 520, torch.bfloat16)]
+
+
+@pytest.mark.parametrize("op,M,K,N,dtype", SPLIT1_CASES,
+                         ids=[f"{c[0]}-{c[1]}x{c[2]}x{c[3]}-{'bf16' if c[4] == torch.bfloat16 else 'f16'}"
+                              for c in SPLIT1_CASES])
+def test_single_cta_k_split_against_oracle(op, M, K, N, dtype):
+    code = {"layernorm_linear": B.OP_LAYERNORM_LINEAR, "rmsnorm_linear": B.OP_RMSNORM_LINEAR,
+            "linear_silu": B.OP_LINEAR_SILU}[op]
+    plan = B.tile_plan(code, M, K, N)
+    assert plan["pair"] == 0 and plan["splits"] > 1, plan
+    d = inputs.case(op, M, K, N, dtype, True, 1e-5 if op != "linear_silu" else 0.0, seed=M + K + N + 41,
+                    x_mean=2.0 if op == "layernorm_linear" else 0.0)
+    g = to_dev(d)
+    ws = torch.empty(B.ngr_workspace_bytes(code, M, K, N), dtype=torch.uint8, device="cuda")
+    if op == "layernorm_linear":
+        run = lambda: ngr.fused_layernorm_linear(g["x"], g["gamma"], g["beta"], g["W"], g["bias"], 1e-5,
+                                                 workspace=ws)
+        ref = oracle.layernorm_linear(d["x"], d["gamma"], d["beta"], d["W"], d["bias"], 1e-5)
+    elif op == "rmsnorm_linear":
+        run = lambda: ngr.fused_rmsnorm_linear(g["x"], g["gamma"], g["W"], g["bias"], 1e-5, workspace=ws)
+        ref = oracle.rmsnorm_linear(d["x"], d["gamma"], d["W"], d["bias"], 1e-5)
+    else:
+        run = lambda: ngr.fused_linear_silu(g["x"], g["W"], g["bias"], workspace=ws)
+        ref = oracle.linear_silu(d["x"], d["W"], d["bias"])
+    y1 = run()
+    y2 = run()
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream().cuda_stream
+    assert B.ngr_workspace_error(ws.data_ptr(), s) == 0, "a bounded wait ran out"
+    assert torch.equal(y1, y2)
+    check(y1, ref, f"single-CTA split {op} {M}x{K}x{N}")
+
+
+@pytest.mark.parametrize("norm", [oracle.NORM_LAYER, oracle.NORM_RMS], ids=["ln", "rms"])
+def test_single_cta_k_split_folded_and_chain(norm):
+    M, K, N = 100, 4096, 1000
+    op = "layernorm_linear" if norm == oracle.NORM_LAYER else "rmsnorm_linear"
+    d = inputs.case(op, M, K, N, torch.float16, True, 1e-5, seed=43 + norm,
+                    x_mean=3.0 if norm == oracle.NORM_LAYER else 0.0)
+    g = to_dev(d)
+    Wf, cb = B.fold_prepare(norm, g["gamma"], g["beta"] if norm == oracle.NORM_LAYER else None,
+                            g["W"], g["bias"])
+    y = B.fused_norm_linear_folded(norm, g["x"], Wf, cb, 1e-5)
+    ref = oracle.layernorm_linear(d["x"], d["gamma"], d["beta"], d["W"], d["bias"], 1e-5) \
+        if norm == oracle.NORM_LAYER else oracle.rmsnorm_linear(d["x"], d["gamma"], d["W"], d["bias"], 1e-5)
+    check(y, ref, f"single-CTA split folded {op}")
+    # the FFN's second product (1000 -> 4096 columns of K = 1000... here
+    # F = 4096 input columns): its K splits too
+    f = inputs.case("ffn", M, 1000, 4096, torch.float16, False, 0.0, seed=44 + norm)
+    assert B.tile_plan(B.OP_FFN, M, 1000, 4096)["splits"] > 1
+    gf = to_dev(f)
+    yf = ngr.ffn_linear_silu_linear(gf["x"], gf["W1"], gf["W2"])
+    check(yf, oracle.ffn(f["x"], f["W1"], f["W2"]), "single-CTA split FFN")
