@@ -476,6 +476,16 @@ int launch_layer(int norm, int act, bool bf16, const void *x, const void *W,
     return launch_gemm(norm, bf16, plan, a, pdl, stream);
 }
 
+// Whether the product launch_layer runs for these sizes (with the split
+// regions of L) splits K, and so needs its split counters at zero.
+bool product_splits(int norm, int64_t M, int64_t K, int64_t N, const WsLayout &L, const DevInfo &di)
+{
+    if (M <= kDecodeMaxM || L.split_cnt_bytes == 0) return false;
+    const bool has_norm = norm == kNormLayer || norm == kNormRms;
+    return plan_gemm(M, N, K, di.sms, has_norm, L.split_cnt_bytes + L.split_part_bytes,
+                     norm == kNormNone || is_fold(norm)).splits > 1;
+}
+
 // The gated (SwiGLU) layer h = SiLU(norm(x) Wg^T) * (norm(x) Wu^T) on the
 // CTA-pair kernel, at any M.
 int launch_gated(int norm, bool bf16, const void *x, const void *Wg, const void *Wu, int64_t M,
@@ -547,7 +557,7 @@ int norm_linear(int op, int norm, int act, const void *x, const void *gamma, con
     // With the statistics kernel first on the stream, it zeroes the K-split
     // counters itself (no separate memset before it).
     const bool stats_zero = need_stats && !decode && L.split_cnt_bytes != 0;
-    if (!stats_zero) {
+    if (!stats_zero && product_splits(norm, M, round8(K), round8(N), L, di)) {
         rc = zero_split_counters(L, w, stream);
         if (rc != NGR_OK) return rc;
     }
@@ -696,8 +706,10 @@ int mlp_chain(int op, int norm, int act, const void *x, const void *gamma, const
     if (debug_mode() && cudaMemsetAsync(w, 0, 4, stream) != cudaSuccess) return NGR_ERR_CUDA;
     const bool decode = M <= kDecodeMaxM;
     const bool need_stats = norm != kNormNone || decode;
-    rc = zero_split_counters(L, w, stream);
-    if (rc != NGR_OK) return rc;
+    if (product_splits(kNormNone, M, F, K, L, di)) {   // the second product
+        rc = zero_split_counters(L, w, stream);
+        if (rc != NGR_OK) return rc;
+    }
     events_reset();
     if (need_stats) {
         event_before(stream);
@@ -759,8 +771,10 @@ int swiglu_chain(int op, int norm, const void *x, const void *gamma, const void 
     if (debug_mode() && cudaMemsetAsync(w, 0, 4, stream) != cudaSuccess) return NGR_ERR_CUDA;
     const bool decode = M <= kDecodeMaxM;
     const bool need_stats = norm != kNormNone || (down && decode);
-    rc = zero_split_counters(L, w, stream);
-    if (rc != NGR_OK) return rc;
+    if (down && product_splits(kNormNone, M, F, K, L, di)) {   // the down projection
+        rc = zero_split_counters(L, w, stream);
+        if (rc != NGR_OK) return rc;
+    }
     events_reset();
     if (need_stats) {
         event_before(stream);
@@ -820,8 +834,10 @@ int linear_residual_norm(int norm, const void *x, const void *W, const void *bia
     void *H = h ? h : static_cast<void *>(w + L.h);
     if (debug_mode() && cudaMemsetAsync(w, 0, 4, stream) != cudaSuccess) return NGR_ERR_CUDA;
     const bool decode = M <= kDecodeMaxM;
-    rc = zero_split_counters(L, w, stream);
-    if (rc != NGR_OK) return rc;
+    if (product_splits(kNormNone, M, K, N, L, di)) {
+        rc = zero_split_counters(L, w, stream);
+        if (rc != NGR_OK) return rc;
+    }
     events_reset();
     if (decode) {
         // the decode product's split-K counters start from zero
