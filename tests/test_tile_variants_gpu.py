@@ -260,3 +260,60 @@ def test_single_cta_k_split_folded_and_chain(norm):
     gf = to_dev(f)
     yf = ngr.ffn_linear_silu_linear(gf["x"], gf["W1"], gf["W2"])
     check(yf, oracle.ffn(f["x"], f["W1"], f["W2"]), "single-CTA split FFN")
+
+
+# The K split at 100 rows through the other entry points whose product may
+# split: the MLP chain's and the SwiGLU MLP's second products, the post-GEMM
+# norm's product and a plain product (their split counters cleared by a
+# memset where the planned product splits, not by the statistics kernel).
+@pytest.mark.parametrize("which", ["mlp", "mlp_swiglu", "post_norm", "plain"])
+def test_single_cta_k_split_other_entry_points(which):
+    M = 100
+    if which == "mlp":
+        K, F = 512, 4096
+        assert B.tile_plan(B.OP_MLP, M, K, F)["splits"] > 1
+        d = inputs.case("mlp", M, K, F, torch.float16, True, 1e-5, seed=51, x_mean=0.5,
+                        norm="layer", act="relu")
+        g = to_dev(d)
+        y = ngr.fused_mlp(g["x"], g["W1"], g["W2"], norm=B.NORM_LAYER, act=B.ACT_RELU,
+                          gamma=g["gamma"], beta=g["beta"], b1=g["b1"], b2=g["b2"], eps=1e-5)
+        ref = oracle.mlp(oracle.NORM_LAYER, oracle.ACT_RELU, d["x"], d["gamma"], d["beta"], d["W1"],
+                         d["b1"], d["W2"], d["b2"], 1e-5)
+        check(y, ref, "split MLP chain")
+    elif which == "mlp_swiglu":
+        K, F = 512, 4096
+        assert B.tile_plan(B.OP_MLP_SWIGLU, M, K, F)["splits"] > 1
+        d = inputs.case("mlp_swiglu", M, K, F, torch.bfloat16, False, 1e-5, seed=52, norm="rms")
+        g = to_dev(d)
+        y = ngr.fused_mlp_swiglu(g["x"], g["Wg"], g["Wu"], g["Wd"], norm=B.NORM_RMS,
+                                 gamma=g["gamma"], beta=None, eps=1e-5)
+        ref = oracle.mlp_swiglu(oracle.NORM_RMS, d["x"], d["gamma"], None, d["Wg"], d["Wu"],
+                                d["Wd"], 1e-5)
+        check(y, ref, "split SwiGLU MLP")
+    elif which == "post_norm":
+        K, N = 4096, 520
+        assert B.tile_plan(B.OP_LINEAR_RESIDUAL_NORM, M, K, N)["splits"] > 1
+        d = inputs.case("norm_linear", M, K, N, torch.float16, True, 1e-5, seed=53, norm="none")
+        gen = torch.Generator().manual_seed(54)
+        res = (torch.randn((M, N), generator=gen) + 1.0).half()
+        gamma = (1.0 + 0.1 * torch.randn((N,), generator=gen)).half()
+        g = to_dev(d)
+        h, y = ngr.fused_linear_residual_norm(g["x"], g["W"], gamma.cuda(), norm=B.NORM_RMS,
+                                              bias=g["bias"], residual=res.cuda(), eps=1e-5)
+        href, yref = oracle.linear_residual_norm(oracle.NORM_RMS, d["x"], d["W"], d["bias"], res,
+                                                 gamma, None, 1e-5)
+        check(h, href, "split post-norm h")
+        check(y, yref, "split post-norm y")
+    else:
+        K, N = 4096, 520
+        assert B.tile_plan(B.OP_NORM_LINEAR, M, K, N)["splits"] > 1
+        d = inputs.case("norm_linear", M, K, N, torch.bfloat16, True, 1e-5, seed=55, norm="none",
+                        act="gelu")
+        g = to_dev(d)
+        y1 = ngr.fused_norm_linear_act(g["x"], g["W"], norm=B.NORM_NONE, act=B.ACT_GELU, bias=g["bias"])
+        y2 = ngr.fused_norm_linear_act(g["x"], g["W"], norm=B.NORM_NONE, act=B.ACT_GELU, bias=g["bias"])
+        torch.cuda.synchronize()
+        assert torch.equal(y1, y2)
+        ref = oracle.norm_linear(oracle.NORM_NONE, oracle.ACT_GELU, d["x"], None, None, d["W"],
+                                 d["bias"], 0.0)
+        check(y1, ref, "split plain product")
