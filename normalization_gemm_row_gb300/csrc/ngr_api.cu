@@ -81,8 +81,9 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int64_t round8(int64_t v) { return (v + 7) & ~static_cast<int64_t>(7); }
 
 // Room for a K split of an M x Nout product (K_in input columns), reserved
-// only where the tiles are few for a GPU's SMs: on the CTA-pair kernel
-// (M > 128) a two-way split when the output has few 256 x 448 tiles; on the
+// only where the tiles are few for a GPU's SMs: on the CTA-pair and
+// multicast kernels (M > 128) a two-way split when the output has few
+// 256 x 448 tiles; on the
 // single-CTA kernel (M <= 128) up to kMaxSplitsSingle ways when the output
 // has fewer than 256 tiles of 128 columns and K_in is long enough to split.
 // The largest counters and partials over the tile widths, so that any plan
@@ -105,6 +106,11 @@ void split_reserve(int64_t M, int64_t Nout, int64_t K_in, size_t *cnt_bytes, siz
         const int64_t tiles = mt * ((Nout + tw - 1) / tw);
         *cnt_bytes = std::max(*cnt_bytes, split_counter_bytes(tiles, tw));
         *part_bytes = std::max(*part_bytes, split_partial_bytes(tiles, tw, 2));
+    }
+    if (M > 2 * kBM) {   // the multicast kernel's 512 x 464 super-tiles, split in two
+        const int64_t super = ((M + kMcRows - 1) / kMcRows) * ((Nout + kMcCols - 1) / kMcCols);
+        *cnt_bytes = std::max(*cnt_bytes, mc_split_counter_bytes(super));
+        *part_bytes = std::max(*part_bytes, mc_split_partial_bytes(super, 2));
     }
 }
 

@@ -130,6 +130,16 @@ size_t split_counter_bytes(int64_t num_tiles, int tw, int ctas)
            static_cast<size_t>((tw + 31) / 32) * 4;
 }
 
+size_t mc_split_partial_bytes(int64_t super, int splits)
+{
+    return static_cast<size_t>(super) * 4 * 4 * kMcChunks * 1024 * static_cast<size_t>(splits) * 4;
+}
+
+size_t mc_split_counter_bytes(int64_t super)
+{
+    return static_cast<size_t>(super) * 4 * 4 * kMcChunks * 4;
+}
+
 // Stages of the two-sub-tile CTA-pair kernel for a sub-tile width.
 static int stages2w_for(int bn) { return bn == 256 ? 4 : 5; }
 static const int kWideWidths[] = {256, 224, 192};
@@ -288,12 +298,28 @@ static bool prefer_multicast(int64_t M, int64_t N, int64_t K, const GemmPlan &pa
            margin * static_cast<double>(per_pair * pair_plan.tw) / pair_plan.splits;
 }
 
-static GemmPlan multicast_plan(int64_t M, int64_t N)
+// A two-way K split on the multicast kernel: when the super-tiles fill at
+// most half the clusters, each K half is a unit (FP32 partials, the last of
+// a chunk's two units finishes it), if the halves keep kMinKbPerSplitMc k
+// blocks and the workspace holds the partials.
+constexpr int kMinKbPerSplitMc = 32;
+static int mc_splits(int64_t M, int64_t N, int64_t K, size_t max_split_bytes)
 {
     const int clusters = max_clusters4();
     const int64_t super = ((M + kMcRows - 1) / kMcRows) * ((N + kMcCols - 1) / kMcCols);
-    GemmPlan p{224, 5, static_cast<int>(4 * (super < clusters ? super : clusters)), 0, true,
-               kMcRows, 56, 2, kMcCols, false, 1};
+    const int64_t k_blocks = (K + kBK - 1) / kBK;
+    if (2 * super <= clusters && k_blocks / 2 >= kMinKbPerSplitMc &&
+        mc_split_partial_bytes(super, 2) + mc_split_counter_bytes(super) <= max_split_bytes)
+        return 2;
+    return 1;
+}
+
+static GemmPlan multicast_plan(int64_t M, int64_t N, int splits)
+{
+    const int clusters = max_clusters4();
+    const int64_t units = ((M + kMcRows - 1) / kMcRows) * ((N + kMcCols - 1) / kMcCols) * splits;
+    GemmPlan p{224, 5, static_cast<int>(4 * (units < clusters ? units : clusters)), 0, true,
+               kMcRows, 56, 2, kMcCols, false, splits};
     p.mc = true;
     p.smem = gemm4_smem_bytes();
     return p;
@@ -304,16 +330,25 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, bool norm,
 {
     const int want = g_pair.load();
     const bool mc_ok = norm || plain;
-    if (want == 2 && mc_ok && M > 2 * kBM && max_clusters4() > 0) return multicast_plan(M, N);
+    if (want == 2 && mc_ok && M > 2 * kBM && max_clusters4() > 0)
+        return multicast_plan(M, N, mc_splits(M, N, K, max_split_bytes));
     double cost = -1.0;
     GemmPlan best = plan_with(M, N, K, num_sms, want == 2 ? -1 : want, g_bn.load(), g_nsub.load(),
                               max_split_bytes, &cost);
     if (cost < 0) best = plan_with(M, N, K, num_sms, -1, 0, 0, max_split_bytes, &cost);
     best.smem = best.pair ? gemm2_smem_bytes(best.bn, best.nsub)
                           : gemm_smem_bytes(best.bn, best.stages, true);
-    if (want == -1 && mc_ok && g_bn.load() == 0 && g_nsub.load() == 0 &&
-        prefer_multicast(M, N, K, best, num_sms))
-        return multicast_plan(M, N);
+    if (want == -1 && mc_ok && g_bn.load() == 0 && g_nsub.load() == 0) {
+        // Few super-tiles: the multicast kernel with K split in two, for a
+        // normalized product or a long K.  Measured on GB300 against the
+        // CTA-pair plans (alternating bursts): 0.942 at RMSNorm fp16 and
+        // 0.908 at LayerNorm bf16 512 x 8192 -> 8192, 0.986 at 512 x 28672 ->
+        // 8192 without a norm; at 512 x 8192 -> 8192 without a norm (64 k
+        // blocks per half) the pair plan stays ahead (1.118).
+        const int ms = mc_splits(M, N, K, max_split_bytes);
+        if (ms > 1 && (norm || (K + kBK - 1) / kBK >= 256)) return multicast_plan(M, N, ms);
+        if (prefer_multicast(M, N, K, best, num_sms)) return multicast_plan(M, N, 1);
+    }
     return best;
 }
 

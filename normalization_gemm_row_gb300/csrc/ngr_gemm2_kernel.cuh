@@ -392,7 +392,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if constexpr (kNorm) {
                 // ----------------------------------------- transform (A in place)
                 transform_role<NORM, BF16, SA, L::kA, kParts, !kRstdOut>(
-                    t, cluster, n_clusters, num_units, [&](int u) { return unit_kb1(u) - unit_kb0(u); },
+                    t, cluster, n_clusters, num_units, [&](int u) { return make_int2(unit_kb0(u), unit_kb1(u)); },
                     args.M, args.stats, sA, sG, full, wc,
                     [&](int u) { return (unit_tile(u) % m_tiles) * 2 * kBM + static_cast<int>(rank) * kBM; },
                     [&](int st) { mbar_arrive_cluster(ready_leader + 8u * static_cast<uint32_t>(st)); });

@@ -144,6 +144,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     auto m0_of = [&](int su) { return (su % m_tiles) * 4 * kBM + p * 2 * kBM + r * kBM; };
     // Sub-tile 1 wholly past N is neither loaded nor multiplied.
     auto n_sub_of = [&](int su) { return (su / m_tiles) * kMcTW + kMcBN0 < args.N ? 2 : 1; };
+    // Work units: (super-tile, K range) pairs; without a split a unit is a
+    // super-tile.  (With few super-tiles for the clusters, a K split fills
+    // them: each unit writes FP32 partials, and the last of a chunk's units
+    // sums them in range order.)
+    const int n_splits = max(1, args.k_splits);
+    const int num_units = num_tiles * n_splits;
+    const int kb_per_split = n_splits > 1 ? args.kb_per_split : k_blocks;
+    auto unit_su = [&](int u) { return u / n_splits; };
+    auto unit_kb = [&](int u) {
+        const int kb0 = (u % n_splits) * kb_per_split;
+        return make_int2(kb0, min(k_blocks, kb0 + kb_per_split));
+    };
 
     if (warp == 0) {
         if (lane == 0) {
@@ -156,7 +168,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint32_t phase = 0;
             long long fills = 0;
             bool ok = true;
-            for (int su = cluster; ok && su < num_tiles; su += n_clusters) {
+            for (int u = cluster; ok && u < num_units; u += n_clusters) {
+                const int su = unit_su(u);
+                const int2 kr = unit_kb(u);
                 const int m0 = m0_of(su);
                 const int nt0 = (su / m_tiles) * kMcTW;
                 const int n_sub = n_sub_of(su);
@@ -166,7 +180,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const int w0 = nt0 + r * (kMcBN0 / 2) + mc_part_row(0, p);
                 const int w1 = nt0 + kMcBN0 + r * (kMcBN1 / 2) + mc_part_row(1, p);
                 const CUtensorMap *map1 = p == 0 ? &args.map_b2 : &args.map_b;   // 64 or 56 rows
-                for (int kb = 0; kb < k_blocks; ++kb) {
+                for (int kb = kr.x; kb < kr.y; ++kb) {
                     if (!mbar_wait_ahead(&empty[stage], phase ^ 1u, wc)) { ok = false; break; }
                     const int kc = kb * kBK;
                     uint8_t *sb = sB + stage * L::kB;
@@ -199,11 +213,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             bool ok = true;
             const uint16_t all = 0xF;
             const uint16_t own = static_cast<uint16_t>(0x3u << (2 * p));
-            for (int su = cluster; ok && su < num_tiles; su += n_clusters) {
+            for (int u = cluster; ok && u < num_units; u += n_clusters) {
                 if (!mbar_wait_spin(&acc_empty[0], acc_phase ^ 1u, wc)) break;
                 tc_fence_after();
-                const int n_sub = n_sub_of(su);
-                for (int kb = 0; kb < k_blocks; ++kb) {
+                const int n_sub = n_sub_of(unit_su(u));
+                const int2 kr = unit_kb(u);
+                for (int kb = kr.x; kb < kr.y; ++kb) {
                     if (!mbar_wait_spin(&ready[stage * kParts], phase, wc)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t b_addr = smem_u32(sB + stage * L::kB);
@@ -219,7 +234,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             tc_fence_after();
                         }
                         const uint64_t a_desc = sdesc_kmajor_sw128(a_addr + k * 32);
-                        const uint32_t acc = (kb != 0 || k != 0) ? 1u : 0u;
+                        const uint32_t acc = (kb != kr.x || k != 0) ? 1u : 0u;
                         umma_f16_ss_pair(tmem_base, a_desc, sdesc_kmajor_sw128(b_addr + k * 32), kIdesc0, acc);
                         if (n_sub == 2)
                             umma_f16_ss_pair(tmem_base + static_cast<uint32_t>(kMcBN0), a_desc,
@@ -233,7 +248,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
                 if (!ok) break;
                 umma_commit_pair(&acc_full[0], own);
-                if (su + n_clusters >= num_tiles) umma_commit_pair(&acc_last, own);
+                if (u + n_clusters >= num_units) umma_commit_pair(&acc_last, own);
                 acc_phase ^= 1u;
             }
             umma_commit_pair(drain, static_cast<uint16_t>(1u << crank));
@@ -245,8 +260,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             // ----------------------------------------- transform (A in place)
             const int t = threadIdx.x - kTransformWarp0 * 32;
             transform_role<NORM, BF16, STAGES, L::kA, kParts, !kRstdOut, true>(
-                t, cluster, n_clusters, num_tiles, [&](int) { return k_blocks; }, args.M, args.stats,
-                sA, nullptr, full, wc, m0_of,
+                t, cluster, n_clusters, num_units, unit_kb, args.M, args.stats, sA, nullptr, full, wc,
+                [&](int u) { return m0_of(unit_su(u)); },
                 [&](int st) { mbar_arrive_cluster(ready_leader + 8u * static_cast<uint32_t>(st)); },
                 args.gamma_f, args.beta_f, args.K);
         }
@@ -259,10 +274,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint32_t acc_phase = 0;
             const int N = args.N;
             if constexpr (kRstdOut || is_fold(NORM)) pdl_wait();   // row statistics from the previous grid
-            for (int su = cluster; su < num_tiles; su += n_clusters) {
+            for (int u = cluster; u < num_units; u += n_clusters) {
+                const int su = unit_su(u);
                 const uint32_t cur_phase = acc_phase;
                 acc_phase ^= 1u;
-                const bool helped = su + n_clusters >= num_tiles;
+                const bool helped = u + n_clusters >= num_units;
                 if (!epi_warp && !helped) continue;
                 const int step = (helped ? 3 : 1);
                 const int nt0 = (su / m_tiles) * kMcTW;
@@ -279,12 +295,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const uint32_t t_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
                 // Chunks: 7 of 32 over sub-tile 0 ([0, 224)), then 7 of 32 and
                 // one of 16 over sub-tile 1 ([224, 464)).
-                constexpr int kChunks = 15;
-#pragma unroll 1
-                for (int ci = e; ci < kChunks; ci += step) {
+                constexpr int kChunks = kMcChunks;
+                // This warp's chunk i is ci = e + i * step, for i < nch.
+                int nch = 0;
+                for (int ci = e; ci < kChunks && (ci < 14 ? 32 * ci : 448) < ncols; ci += step) ++nch;
+                auto load_chunk = [&](int ci, float (&v)[32]) {
                     const int c = ci < 14 ? 32 * ci : 448;
-                    if (c >= ncols) break;
-                    float v[32];
                     if (ci < 14) {
                         uint32_t rr[32];
                         tmem_ld32(t_base + static_cast<uint32_t>(c), rr);
@@ -300,8 +316,75 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
                         for (int j = 16; j < 32; ++j) v[j] = 0.f;
                     }
+                };
+                auto finish_chunk = [&](int ci, float (&v)[32]) {
+                    const int c = ci < 14 ? 32 * ci : 448;
                     epilogue_store32<NORM, BF16, kRstdOut>(v, row, nt0 + c, args, so,
                                                            ci < 14 ? N : min(N, nt0 + kMcTW));
+                };
+                if (n_splits > 1) {
+                    // K split: (1) this unit's FP32 partials of the warp's
+                    // chunks (column-major within a chunk, so that each store
+                    // of the warp writes one 128-byte line); (2) one fence,
+                    // then one counter per chunk (lane i takes the warp's
+                    // chunk i); (3) the chunks this unit arrived last at are
+                    // summed over the K ranges in range order and finished,
+                    // and their counters reset for the next call.
+                    const int split = u % n_splits;
+                    const size_t blk0 = (static_cast<size_t>(su) * 4 + crank) * 4 * kChunks +
+                                        static_cast<size_t>(q) * kChunks;
+                    const size_t part_stride = static_cast<size_t>(n_splits) * 1024;
+#pragma unroll 1
+                    for (int i = 0; i < nch; ++i) {
+                        const int ci = e + i * step;
+                        float v[32];
+                        load_chunk(ci, v);
+                        float *mine = args.partials + (blk0 + ci) * part_stride + split * 1024 + lane;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) __stcg(mine + j * 32, v[j]);
+                    }
+                    __threadfence();
+                    __syncwarp();
+                    int last = 0;
+                    if (lane < nch)
+                        last = atomicAdd(&args.split_counters[blk0 + e + lane * step], 1) == n_splits - 1;
+                    const unsigned last_mask = __ballot_sync(0xffffffffu, last);
+                    if (last_mask != 0u) {
+                        __threadfence();
+#pragma unroll 1
+                        for (int i = 0; i < nch; ++i) {
+                            if (((last_mask >> i) & 1u) == 0u) continue;
+                            const int ci = e + i * step;
+                            float own[32];
+                            load_chunk(ci, own);
+                            const float *part = args.partials + (blk0 + ci) * part_stride + lane;
+                            float v[32];
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+                            for (int sp = 0; sp < n_splits; ++sp) {
+                                if (sp == split) {
+#pragma unroll
+                                    for (int j = 0; j < 32; ++j) v[j] += own[j];
+                                } else {
+                                    const float *o = part + sp * 1024;
+#pragma unroll
+                                    for (int j = 0; j < 32; ++j) v[j] += __ldcg(o + j * 32);
+                                }
+                            }
+                            finish_chunk(ci, v);
+                        }
+                        __syncwarp();
+                        if (lane < nch && ((last_mask >> lane) & 1u))
+                            args.split_counters[blk0 + e + lane * step] = 0;
+                    }
+                } else {
+#pragma unroll 1
+                    for (int i = 0; i < nch; ++i) {
+                        const int ci = e + i * step;
+                        float v[32];
+                        load_chunk(ci, v);
+                        finish_chunk(ci, v);
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();

@@ -359,8 +359,8 @@ __device__ __forceinline__ float2 fold_row_scale(const GemmArgs &args, int row)
 // covers 8 distinct 16-byte positions of the 128-byte swizzle pattern
 // (conflict free), and gamma/beta of the chunk are read once per part.
 // After its stores each thread fences them for the async proxy.
-// m0_of(unit) gives the unit's first x row in this CTA and kb_count(unit)
-// the number of k blocks the unit covers (all of them unless K is split).
+// m0_of(unit) gives the unit's first x row in this CTA and kb_range(unit)
+// the k blocks [x, y) it covers (all of them unless K is split).
 // gamma/beta come from each stage's FP32 box in shared memory (sG), or,
 // with GB_GLOBAL, from the FP32 rows g_glob / b_glob in global memory: a
 // thread then issues the loads of its chunks before waiting for the stage
@@ -368,7 +368,7 @@ __device__ __forceinline__ float2 fold_row_scale(const GemmArgs &args, int row)
 template <int NORM, bool BF16, int STAGES, int KA, int PARTS = 1, bool ROW_SCALE = true,
           bool GB_GLOBAL = false, typename M0Fn, typename KbFn, typename ArriveFn>
 __device__ __forceinline__ void transform_role(int t, int tile0, int tile_step, int num_tiles,
-                                               KbFn kb_count, int M, const float2 *stats,
+                                               KbFn kb_range, int M, const float2 *stats,
                                                uint8_t *sA, const float *sG, uint64_t *full,
                                                const WaitCtx &wc, M0Fn m0_of, ArriveFn arrive,
                                                const float *g_glob = nullptr,
@@ -411,8 +411,8 @@ __device__ __forceinline__ void transform_role(int t, int tile0, int tile_step, 
             so[i] = make_float2(st.y, -st.x * st.y);
             s2[i] = rms_in_scale2<BF16>(st.y);
         }
-        const int k_blocks = kb_count(tile);
-        for (int kb = 0; kb < k_blocks; ++kb, ++it) {
+        const int2 kr = kb_range(tile);
+        for (int kb = kr.x; kb < kr.y; ++kb, ++it) {
             if (it % kTransformGroups == g) {
                 if constexpr (!kMath) {
                     // No norm: only relay each landed stage to the MMA issuer.
@@ -685,7 +685,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             // ---------------------------------------------------- transform
             transform_role<NORM, BF16, STAGES, L::kA>(
                 threadIdx.x - kTransformWarp0 * 32, blockIdx.x, gridDim.x, num_units,
-                [&](int u) { return unit_kb1(u) - unit_kb0(u); }, args.M, args.stats, sA, sG, full, wc,
+                [&](int u) { return make_int2(unit_kb0(u), unit_kb1(u)); }, args.M, args.stats, sA, sG, full, wc,
                 [&](int u) { return (unit_tile(u) % m_tiles) * kBM; },
                 [&](int st) { mbar_arrive(&ready[st]); });
         }

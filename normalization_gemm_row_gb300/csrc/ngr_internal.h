@@ -128,14 +128,20 @@ struct GemmPlan {
                      // 512 x 464 super-tiles, sub-tiles 224 + 240
 };
 
-// The multicast cluster kernel's super-tile and weight-box geometry.
+// The multicast cluster kernel's super-tile and weight-box geometry, and
+// the epilogue chunks of a CTA's 464 accumulator columns (14 of 32, one of
+// 16), which are also the units of its K-split partials and counters.
 constexpr int kMcRows = 512;
 constexpr int kMcCols = 464;
+constexpr int kMcChunks = 15;
 
 // Bytes of FP32 partials and of counters a split plan needs (ctas: CTAs
 // per output tile, 2 for the CTA pair, 1 for the single-CTA kernel).
 size_t split_partial_bytes(int64_t num_tiles, int tw, int splits, int ctas = 2);
 size_t split_counter_bytes(int64_t num_tiles, int tw, int ctas = 2);
+// The multicast kernel's split partials and counters for `super` super-tiles.
+size_t mc_split_partial_bytes(int64_t super, int splits);
+size_t mc_split_counter_bytes(int64_t super);
 // The single-CTA kernel splits K at most this many ways, into ranges of at
 // least kMinKbPerSplitSingle k blocks.
 constexpr int kMaxSplitsSingle = 4;

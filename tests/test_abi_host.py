@@ -119,6 +119,11 @@ def test_split_k_reserve(lib):
     mt = 2
     cnt = max(mt * -(-8192 // tw) * 2 * 4 * (tw // 32) * 4 for tw in (128, 192, 224, 256, 384, 448, 512))
     part = max(mt * -(-8192 // tw) * 2 * 128 * tw * 2 * 4 for tw in (128, 192, 224, 256, 384, 448, 512))
+    # ... and the multicast kernel's two-way split of 512 x 464 super-tiles:
+    # [super-tiles][4 CTAs][4][15 chunks] counters, 32 x 32 partials each
+    sup = 1 * -(-8192 // 464)
+    cnt = max(cnt, sup * 4 * 4 * 15 * 4)
+    part = max(part, sup * 4 * 4 * 15 * 1024 * 2 * 4)
     assert got == 256 + a256(cnt) + a256(part)
     # none at decode sizes
     assert wb(B.OP_LINEAR_SILU, 16, 8192, 8192) == wb(B.OP_LINEAR_SILU, 16, 8192, 8192, 0)

@@ -186,3 +186,72 @@ def test_multicast_folded_against_oracle(multicast, norm, dtype, M, K, N):
     else:
         ref = oracle.rmsnorm_linear(d["x"], d["gamma"], d["W"], d["bias"], 1e-5)
     check(y1, ref, f"multicast folded {op} {dtype} {M}x{K}x{N}")
+
+
+# ------------------------------------------------- K split on the multicast kernel
+# When the super-tiles fill at most half of the clusters, the multicast
+# kernel splits K in two: each half writes FP32 partials of its 32 x 32
+# chunks, and the last of a chunk's two units sums them in range order and
+# finishes it.  Shapes: a second pair partly past M (300 rows), a last
+# super-tile partly past N (1000 and 928 columns), several m super-tiles
+# (1112 rows), and a full 8192-column output (18 super-tiles).  Every element
+# against the oracle, and two calls agree bit for bit.
+MC_SPLIT_SHAPES = [(600, 4096, 1000), (300, 8192, 928), (1112, 4096, 700), (512, 4096, 8192)]
+
+
+@pytest.mark.parametrize("M,K,N", MC_SPLIT_SHAPES)
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
+@pytest.mark.parametrize("op", ["layernorm_linear", "rmsnorm_linear", "linear_silu"])
+def test_multicast_k_split_against_oracle(multicast, op, dtype, M, K, N):
+    code = {"layernorm_linear": B.OP_LAYERNORM_LINEAR, "rmsnorm_linear": B.OP_RMSNORM_LINEAR,
+            "linear_silu": B.OP_LINEAR_SILU}[op]
+    plan = B.tile_plan(code, M, K, N)
+    assert plan["pair"] == 2 and plan["splits"] == 2, plan
+    d = inputs.case(op, M, K, N, dtype, op != "rmsnorm_linear", 1e-5 if op != "linear_silu" else 0.0,
+                    seed=M + K + N + 61, x_mean=2.0 if op == "layernorm_linear" else 0.0,
+                    outlier_frac=0.02 if op == "rmsnorm_linear" else 0.0, outlier_scale=50.0)
+    g = {k: (v.cuda() if isinstance(v, torch.Tensor) and k != "outlier_rows" else v)
+         for k, v in d.items()}
+    ws = torch.empty(B.ngr_workspace_bytes(code, M, K, N), dtype=torch.uint8, device="cuda")
+    if op == "layernorm_linear":
+        run = lambda: ngr.fused_layernorm_linear(g["x"], g["gamma"], g["beta"], g["W"], g["bias"], 1e-5,
+                                                 workspace=ws)
+        ref = oracle.layernorm_linear(d["x"], d["gamma"], d["beta"], d["W"], d["bias"], 1e-5)
+    elif op == "rmsnorm_linear":
+        run = lambda: ngr.fused_rmsnorm_linear(g["x"], g["gamma"], g["W"], g["bias"], 1e-5, workspace=ws)
+        ref = oracle.rmsnorm_linear(d["x"], d["gamma"], d["W"], d["bias"], 1e-5)
+    else:
+        run = lambda: ngr.fused_linear_silu(g["x"], g["W"], g["bias"], workspace=ws)
+        ref = oracle.linear_silu(d["x"], d["W"], d["bias"])
+    y1 = run()
+    y2 = run()
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream().cuda_stream
+    assert B.ngr_workspace_error(ws.data_ptr(), s) == 0, "a bounded wait ran out"
+    assert torch.equal(y1, y2)
+    check(y1, ref, f"multicast K split {op} {dtype} {M}x{K}x{N}")
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
+def test_multicast_k_split_residual_and_fold(multicast, dtype):
+    M, K, N = 300, 4096, 1000
+    assert B.tile_plan(B.OP_LINEAR_RESIDUAL_NORM, M, K, N)["splits"] == 2
+    d = inputs.case("norm_linear", M, K, N, dtype, True, 1e-5, seed=71, norm="none")
+    gen = torch.Generator().manual_seed(72)
+    res = (torch.randn((M, N), generator=gen) + 1.0).to(dtype)
+    gamma = (1.0 + 0.1 * torch.randn((N,), generator=gen)).to(dtype)
+    g = {k: (v.cuda() if isinstance(v, torch.Tensor) and k != "outlier_rows" else v)
+         for k, v in d.items()}
+    h, y = ngr.fused_linear_residual_norm(g["x"], g["W"], gamma.cuda(), norm=B.NORM_RMS,
+                                          bias=g["bias"], residual=res.cuda(), eps=1e-5)
+    href, yref = oracle.linear_residual_norm(oracle.NORM_RMS, d["x"], d["W"], d["bias"], res,
+                                             gamma, None, 1e-5)
+    check(h, href, f"multicast K split post-norm h {dtype}")
+    check(y, yref, f"multicast K split post-norm y {dtype}")
+    e = inputs.case("layernorm_linear", M, K, N, dtype, True, 1e-5, seed=73, x_mean=3.0)
+    ge = {k: (v.cuda() if isinstance(v, torch.Tensor) and k != "outlier_rows" else v)
+          for k, v in e.items()}
+    Wf, cb = B.fold_prepare(oracle.NORM_LAYER, ge["gamma"], ge["beta"], ge["W"], ge["bias"])
+    yf = B.fused_norm_linear_folded(oracle.NORM_LAYER, ge["x"], Wf, cb, 1e-5)
+    check(yf, oracle.layernorm_linear(e["x"], e["gamma"], e["beta"], e["W"], e["bias"], 1e-5),
+          f"multicast K split folded {dtype}")
