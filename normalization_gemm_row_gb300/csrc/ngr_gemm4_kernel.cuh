@@ -21,7 +21,9 @@
 // multicast parts are 56 + 56 and 64 + 56 rows, each a whole number of
 // 8-row swizzle atoms.  gamma/beta are read by the transform from global
 // memory (L1) instead of shared memory, which keeps five 45-KB stages
-// within the 227 KB of shared memory.
+// within the 227 KB of shared memory.  When the super-tiles fill at most
+// half the clusters, K is split in two (units of a super-tile and a K half,
+// FP32 partials summed in range order by the last of a chunk's units).
 //
 // Synchronization (as in gemm2_kernel, plus):
 //   full[s]   per CTA: its own x box and both weight parts landed (the
@@ -283,7 +285,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const int step = (helped ? 3 : 1);
                 const int nt0 = (su / m_tiles) * kMcTW;
                 const int ncols = min(kMcTW, N - nt0);
-                // (helpers: the last super-tile's one-shot barrier)
+                // (helpers: the cluster's last unit's one-shot barrier)
                 if (!(epi_warp ? mbar_wait_warp_long(&acc_full[0], cur_phase, wc)
                                : mbar_wait_warp_long(&acc_last, 0, wc)))
                     break;

@@ -12,7 +12,9 @@
 // weights); "昇腾CANN的MatMul融合玩法，让大模型推理快3倍", §二 strategies 1-3.
 //
 // GB300 design.  One CTA per SM loops over output tiles (m fastest, so the
-// CTAs resident at one time share weight tiles through L2).  Warp roles:
+// CTAs resident at one time share weight tiles through L2), or, with fewer
+// tiles than SMs, over (tile, K range) units whose FP32 partials the last
+// unit of each chunk sums in range order.  Warp roles:
 //   warp 0      TMA producer: x tile [128 x 64] and W tile [BN x 64] (both
 //               in the 128-byte swizzled K-major layout the tensor core
 //               reads), plus FP32 gamma/beta [64] (converted once per call
