@@ -176,10 +176,12 @@ def test_split_k_is_deterministic():
 
 
 def test_split_k_default_plan_llama_down_projection():
-    """512 x 28672 -> 8192 (38 wide tiles for 76 pairs, 448 k blocks): the
-    default plan splits K; 512 x 8192 -> 8192 (128 k blocks) does not, its
-    halves would be too short to repay the split.  Sampled rows against the
-    oracle."""
+    """512 x 28672 -> 8192 (448 k blocks, few output tiles): the default plan
+    splits K in two, on the multicast kernel (18 super-tiles for 36 clusters)
+    or on the CTA-pair kernel (38 wide tiles for 76 pairs) where fewer
+    clusters are resident; 512 x 8192 -> 8192 without a norm (128 k blocks)
+    does not, its halves would be too short to repay the split.  Sampled
+    rows against the oracle."""
     assert B.tile_plan(B.OP_LINEAR_SILU, 512, 8192, 8192)["splits"] == 1
     plan = B.tile_plan(B.OP_LINEAR_SILU, 512, 28672, 8192)
     assert plan["splits"] == 2, plan
